@@ -1,0 +1,31 @@
+"""Plain, slow, fp64 CPU oracle for decode attention over a paged KV cache.
+
+TEST INFRASTRUCTURE. Only the tests, the package smoke check and the
+benchmark's CPU-baseline / reference leg import this package. The CUDA
+product path never imports, calls or links it, and it shares no code with
+the CUDA library: no kernels, headers, helpers or constant tables.
+
+Every function works on numpy arrays. Cache contents are passed as raw
+storage (bf16 as uint16 bit patterns, fp8-e4m3 as uint8 codes) and decoded
+here, exactly, to float64 before any arithmetic.
+
+Pinned by tests/test_oracle_pins.py (closed forms, page figures, brute force,
+library special cases). Parity status per function is listed in the module
+docstrings of ``attention`` and ``numerics``.
+"""
+from .numerics import (bf16_bits_to_f64, e4m3_value_table, e4m3_codes_to_f64,
+                       e4m3_encode_f32)
+from .attention import (attend, attend_scores, decode_rows, gather_positions, gather_rows, kv_append,
+                        gqa_decode, mla_decode, indexer_scores, topk_select,
+                        indexer_topk, sparse_decode, lse_merge, split_decode,
+                        bytes_per_token, cache_bytes, paged_waste_slots,
+                        sparse_schedule)
+
+__all__ = [
+    "bf16_bits_to_f64", "e4m3_value_table", "e4m3_codes_to_f64",
+    "e4m3_encode_f32",
+    "attend", "attend_scores", "decode_rows", "gather_positions", "gather_rows", "kv_append", "gqa_decode",
+    "mla_decode", "indexer_scores", "topk_select", "indexer_topk",
+    "sparse_decode", "lse_merge", "split_decode", "bytes_per_token",
+    "cache_bytes", "paged_waste_slots", "sparse_schedule",
+]

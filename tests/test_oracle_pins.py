@@ -1,0 +1,590 @@
+"""Pins of the fp64 oracle against things other than itself: the pages'
+figures (tests/golden/page_figures.json), hand-worked examples, closed forms,
+brute force in plain Python, library conversions, and invariants of the
+mathematics. A plausible mistake in the oracle (a dropped scale, a transposed
+operand, a wrong head-to-group map, a tie broken the wrong way, an off-by-one
+length) fails at least one test here; test_oracle_mutants.py plants such
+mistakes to check that.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def _bf16_bits(x):
+    """float64 array -> bf16 bit patterns (library rounding, torch CPU)."""
+    t = torch.tensor(np.asarray(x, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _bf16_round(x):
+    return O.bf16_bits_to_f64(_bf16_bits(x))
+
+
+# ---------------------------------------------------------------------------
+# element formats
+# ---------------------------------------------------------------------------
+def test_bf16_closed_form():
+    bits = np.array([0x3F80, 0xC000, 0x0001, 0x7F80, 0x8000, 0x4049],
+                    dtype=np.uint16)
+    v = O.bf16_bits_to_f64(bits)
+    assert v[0] == 1.0 and v[1] == -2.0
+    assert v[2] == 2.0 ** -133                     # smallest subnormal
+    assert np.isinf(v[3]) and v[3] > 0
+    assert v[4] == 0.0 and np.signbit(v[4])
+    assert v[5] == 3.140625
+
+
+def test_bf16_matches_torch():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=20000).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]          # drop inf / NaN
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double()
+    assert np.array_equal(O.bf16_bits_to_f64(bits), ref.numpy())
+
+
+def test_e4m3_closed_form(golden_dir):
+    g = _load(golden_dir, "page_figures.json")["e4m3_max"]
+    t = O.e4m3_value_table()
+    assert t[0x7E] == g["value"] == 448.0
+    assert t[0x7E] * 6 == g["fp4_bound"]
+    assert t[0xFE] == -448.0
+    assert t[0x01] == 2.0 ** -9                     # smallest subnormal
+    assert t[0x07] == 7 * 2.0 ** -9
+    assert t[0x08] == 2.0 ** -6                     # smallest normal
+    assert t[0x38] == 1.0
+    assert t[0x00] == 0.0 and t[0x80] == 0.0 and np.signbit(t[0x80])
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.isfinite(t).sum() == 254
+    pos = t[:127]
+    assert np.all(np.diff(pos) > 0)                 # codes ordered by value
+
+
+def test_e4m3_decode_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    mine = O.e4m3_codes_to_f64(codes)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    assert np.array_equal(ref[fin], mine[fin])
+
+
+def test_e4m3_encode_round_trip_all_codes():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F],
+                     dtype=np.uint8)
+    vals = O.e4m3_codes_to_f64(codes).astype(np.float32)
+    assert np.array_equal(O.e4m3_encode_f32(vals), codes)
+
+
+def test_e4m3_encode_midpoints_ties_to_even():
+    t = O.e4m3_value_table()[:127]
+    for c in range(126):
+        mid = np.float32((t[c] + t[c + 1]) / 2)     # exact in fp32
+        assert float(mid) == (t[c] + t[c + 1]) / 2
+        want = c if c % 2 == 0 else c + 1
+        assert O.e4m3_encode_f32(np.array([mid]))[0] == want, c
+        assert O.e4m3_encode_f32(np.array([-mid]))[0] == (want | 0x80), c
+        up = np.nextafter(mid, np.float32(np.inf), dtype=np.float32)
+        dn = np.nextafter(mid, np.float32(0), dtype=np.float32)
+        assert O.e4m3_encode_f32(np.array([up]))[0] == c + 1
+        assert O.e4m3_encode_f32(np.array([dn]))[0] == c
+
+
+def test_e4m3_encode_saturates_and_edges():
+    x = np.array([448.0, 449.0, 464.0, 500.0, 1e30, np.inf, -np.inf, -1e9,
+                  2.0 ** -10, 2.0 ** -10 * 1.0001, 3 * 2.0 ** -10, -1e-30,
+                  0.0, np.nan], dtype=np.float32)
+    got = O.e4m3_encode_f32(x)
+    want = [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE,
+            0x00, 0x01, 0x02, 0x80, 0x00, 0x7F]
+    assert got.tolist() == want
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(2)
+    x = np.concatenate([rng.standard_normal(50000) * 30,
+                        rng.standard_normal(20000) * 0.01,
+                        rng.uniform(-448, 448, 20000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(O.e4m3_encode_f32(x), ref.numpy())
+
+
+# ---------------------------------------------------------------------------
+# attention at one position
+# ---------------------------------------------------------------------------
+def test_worked_examples(golden_dir):
+    for case in _load(golden_dir, "worked_attention.json")["cases"]:
+        out, lse = O.attend(np.array(case["q"]), np.array(case["K"]),
+                            np.array(case["V"]), case["scale"])
+        np.testing.assert_allclose(out, case["out"], rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+        np.testing.assert_allclose(lse, case["lse"], rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+
+
+def _brute_attend(q, K, V, scale):
+    """Plain-Python loops: one head, one position."""
+    T = len(K)
+    s = [scale * sum(q[i] * K[t][i] for i in range(len(q))) for t in range(T)]
+    m = max(s)
+    e = [math.exp(x - m) for x in s]
+    z = sum(e)
+    out = [sum(e[t] * V[t][j] for t in range(T)) / z for j in range(len(V[0]))]
+    return out, m + math.log(z)
+
+
+def test_attend_brute_force():
+    rng = np.random.default_rng(3)
+    for T in (1, 2, 5, 9):
+        for d in (1, 3, 4):
+            q = rng.standard_normal((2, d))
+            K = rng.standard_normal((T, d))
+            V = rng.standard_normal((T, d + 1))
+            out, lse = O.attend(q, K, V, 0.37)
+            for h in range(2):
+                bo, bl = _brute_attend(q[h].tolist(), K.tolist(), V.tolist(),
+                                       0.37)
+                np.testing.assert_allclose(out[h], bo, atol=1e-12)
+                assert abs(lse[h] - bl) < 1e-12
+
+
+def test_weights_sum_to_one_and_identity_values():
+    rng = np.random.default_rng(4)
+    T = 37
+    S = rng.standard_normal((3, T)) * 4
+    w, _ = O.attend_scores(S, np.eye(T))            # out = the weights
+    assert np.all(w >= 0)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, atol=1e-14)
+    # weights are proportional to exp(score)
+    np.testing.assert_allclose(w[:, 1:] / w[:, :1], np.exp(S[:, 1:] - S[:, :1]),
+                               rtol=1e-12)
+
+
+def test_empty_prefix():
+    out, lse = O.attend(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 3)), 1)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def _causal_full(Q, K, V):
+    """Causal self-attention for every position at once, with an explicit
+    -inf mask over future positions (no cache), written independently of
+    the oracle. Q [T][n_h][d], K, V [T][n_kv][d]."""
+    T, n_h, d = Q.shape
+    g = n_h // K.shape[1]
+    mask = np.triu(np.full((T, T), -np.inf), k=1)
+    out = np.zeros((T, n_h, d))
+    for h in range(n_h):
+        kv = h // g
+        S = Q[:, h, :] @ K[:, kv, :].T / math.sqrt(d) + mask
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, h, :] = P @ V[:, kv, :]
+    return out
+
+
+@pytest.mark.parametrize("n_h,n_kv", [(4, 4), (8, 2), (6, 1)])
+def test_cached_decode_equals_full_recompute(n_h, n_kv):
+    """KV cache, 'A cache you keep ...': k_i, v_i depend on h_i alone and
+    causality fixes h_i, so attending over cached k, v at the last position
+    equals recomputing causal attention over the whole sequence. The
+    projections k = W_K h, v = W_V h are stored in bf16, and the recompute
+    uses those stored values too."""
+    rng = np.random.default_rng(5)
+    T, d_model, d, bs = 23, 16, 8, 4
+    H = rng.standard_normal((T, d_model))
+    Wq = rng.standard_normal((d_model, n_h * d)) / 4
+    Wk = rng.standard_normal((d_model, n_kv * d)) / 4
+    Wv = rng.standard_normal((d_model, n_kv * d)) / 4
+    Q = (H @ Wq).reshape(T, n_h, d)
+    K = _bf16_round((H @ Wk).reshape(T, n_kv, d))
+    V = _bf16_round((H @ Wv).reshape(T, n_kv, d))
+    full = _causal_full(Q, K, V)
+    nb = (T + bs - 1) // bs
+    perm = rng.permutation(nb + 3)[:nb]
+    k_raw = np.zeros((nb + 3, n_kv, bs, d), dtype=np.uint16)
+    v_raw = np.zeros_like(k_raw)
+    for t in range(T):
+        k_raw[perm[t // bs], :, t % bs, :] = _bf16_bits(K[t])
+        v_raw[perm[t // bs], :, t % bs, :] = _bf16_bits(V[t])
+    for t_last in (0, 5, T - 1):
+        out, _ = O.gqa_decode(Q[t_last][None], k_raw, v_raw, perm[None],
+                              [t_last + 1], bs)
+        np.testing.assert_allclose(out[0], full[t_last], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# paging and grouped heads
+# ---------------------------------------------------------------------------
+def _random_paged(rng, B, n_kv, d, bs, lens, spare=2, dtype=np.uint16):
+    nbs = [(L + bs - 1) // bs for L in lens]
+    nb = sum(nbs) + spare
+    perm = rng.permutation(nb)
+    mb = max(max(nbs), 1)
+    bt = np.full((B, mb), -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        bt[b, :nbs[b]] = perm[k:k + nbs[b]]
+        k += nbs[b]
+    if dtype == np.uint16:
+        kr = _bf16_bits(rng.standard_normal((nb, n_kv, bs, d)))
+        vr = _bf16_bits(rng.standard_normal((nb, n_kv, bs, d)))
+    else:
+        kr = rng.integers(0, 256, (nb, n_kv, bs, d)).astype(np.uint8)
+        kr[(kr & 0x7F) == 0x7F] = 0x11
+        vr = rng.integers(0, 256, (nb, n_kv, bs, d)).astype(np.uint8)
+        vr[(vr & 0x7F) == 0x7F] = 0x22
+    return kr, vr, bt
+
+
+def _contiguous_copy(raw, bt, lens, bs):
+    """Same sequences, one contiguous block per sequence."""
+    B = len(lens)
+    cap = max(max(lens), 1)
+    out = np.zeros((B, raw.shape[1], cap, raw.shape[3]), dtype=raw.dtype)
+    for b in range(B):
+        for t in range(lens[b]):
+            out[b, :, t, :] = raw[bt[b, t // bs], :, t % bs, :]
+    return out
+
+
+def test_paging_is_transparent():
+    rng = np.random.default_rng(6)
+    lens = [1, 15, 16, 17, 40]
+    B, n_kv, d, bs, n_h = len(lens), 2, 8, 16, 4
+    kr, vr, bt = _random_paged(rng, B, n_kv, d, bs, lens)
+    q = rng.standard_normal((B, n_h, d))
+    o1, l1 = O.gqa_decode(q, kr, vr, bt, lens, bs)
+    cap = max(lens)
+    kc = _contiguous_copy(kr, bt, lens, bs)
+    vc = _contiguous_copy(vr, bt, lens, bs)
+    o2, l2 = O.gqa_decode(q, kc, vc, np.arange(B)[:, None], lens, cap)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    """KV cache, 'Fewer KV heads ...': GQA partitions the query heads into
+    groups sharing one KV head; it is exactly MHA over the KV heads repeated
+    per group (query head h reads KV head h // g)."""
+    rng = np.random.default_rng(7)
+    lens = [5, 33, 64]
+    B, n_kv, g, d, bs = 3, 2, 4, 16, 16
+    kr, vr, bt = _random_paged(rng, B, n_kv, d, bs, lens)
+    q = rng.standard_normal((B, n_kv * g, d))
+    o1, l1 = O.gqa_decode(q, kr, vr, bt, lens, bs)
+    o2, l2 = O.gqa_decode(q, np.repeat(kr, g, axis=1), np.repeat(vr, g, axis=1),
+                          bt, lens, bs)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_mha_brute_force_per_head():
+    rng = np.random.default_rng(8)
+    lens = [3, 7]
+    B, n_kv, d, bs = 2, 3, 4, 4
+    kr, vr, bt = _random_paged(rng, B, n_kv, d, bs, lens)
+    q = rng.standard_normal((B, n_kv, d))
+    out, lse = O.gqa_decode(q, kr, vr, bt, lens, bs, scale=0.5)
+    for b in range(B):
+        for h in range(n_kv):
+            K = [O.bf16_bits_to_f64(kr[bt[b, t // bs], h, t % bs]).tolist()
+                 for t in range(lens[b])]
+            V = [O.bf16_bits_to_f64(vr[bt[b, t // bs], h, t % bs]).tolist()
+                 for t in range(lens[b])]
+            bo, bl = _brute_attend(q[b, h].tolist(), K, V, 0.5)
+            np.testing.assert_allclose(out[b, h], bo, atol=1e-12)
+            assert abs(lse[b, h] - bl) < 1e-12
+
+
+def test_default_scale_is_inverse_sqrt_head_dim():
+    rng = np.random.default_rng(9)
+    kr, vr, bt = _random_paged(rng, 1, 1, 16, 8, [11])
+    q = rng.standard_normal((1, 2, 16))
+    a = O.gqa_decode(q, kr, vr, bt, [11], 8)
+    b = O.gqa_decode(q, kr, vr, bt, [11], 8, scale=0.25)
+    np.testing.assert_allclose(a[0], b[0], atol=0)
+
+
+def test_fp8_cache_is_scaled_codes():
+    rng = np.random.default_rng(10)
+    lens = [9, 20]
+    kr, vr, bt = _random_paged(rng, 2, 2, 8, 8, lens, dtype=np.uint8)
+    ks = np.array([0.5, 0.125], dtype=np.float32)
+    vs = np.array([2.0, 0.25], dtype=np.float32)
+    q = rng.standard_normal((2, 4, 8))
+    o1, l1 = O.gqa_decode(q, kr, vr, bt, lens, 8, dtype="fp8", k_scale=ks,
+                          v_scale=vs)
+    # the same values stored as exact bf16 (each code * power-of-two scale
+    # has <= 4 significant bits, so bf16 holds it exactly)
+    kv = O.e4m3_codes_to_f64(kr) * ks[None, :, None, None].astype(np.float64)
+    vv = O.e4m3_codes_to_f64(vr) * vs[None, :, None, None].astype(np.float64)
+    o2, l2 = O.gqa_decode(q, _bf16_bits(kv), _bf16_bits(vv), bt, lens, 8)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# append
+# ---------------------------------------------------------------------------
+def test_append_bf16_writes_one_slot():
+    rng = np.random.default_rng(11)
+    lens = [3, 16, 30]
+    kr, _, bt = _random_paged(rng, 3, 2, 8, 16, [L + 1 for L in lens])
+    new = _bf16_bits(rng.standard_normal((3, 2, 8)))
+    out = O.kv_append(kr, bt, lens, new, 16)
+    changed = np.argwhere(np.any(out != kr, axis=3))
+    for b, L in enumerate(lens):
+        assert np.array_equal(out[bt[b, L // 16], :, L % 16, :], new[b])
+    assert len(changed) <= 3 * 2                    # nothing else moved
+    mask = np.ones(kr.shape[:3], dtype=bool)
+    for b, L in enumerate(lens):
+        mask[bt[b, L // 16], :, L % 16] = False
+    assert np.array_equal(out[mask], kr[mask])
+
+
+def test_append_fp8_codes():
+    rng = np.random.default_rng(12)
+    kr, _, bt = _random_paged(rng, 2, 2, 8, 8, [5, 9], dtype=np.uint8)
+    new_f = rng.standard_normal((2, 2, 8)) * 3
+    new = _bf16_bits(new_f)
+    inv = np.array([8.0, 1 / 0.07], dtype=np.float32)
+    out = O.kv_append(kr, bt, [4, 8], new, 8, dtype="fp8", inv_scale=inv)
+    for b, p in enumerate([4, 8]):
+        x = O.bf16_bits_to_f64(new[b]).astype(np.float32)
+        y = x * inv[:, None]                         # float32 products
+        ref = torch.from_numpy(np.ascontiguousarray(y)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(out[bt[b, p // 8], :, p % 8, :], ref)
+
+
+# ---------------------------------------------------------------------------
+# latent cache
+# ---------------------------------------------------------------------------
+def test_mla_absorbed_equals_explicit():
+    """KV cache, 'Caching a compressed latent ...': folding W_UK into the
+    query gives the same scores as decompressing per-head keys, and the
+    value up-projection can be applied after the weighted sum."""
+    rng = np.random.default_rng(13)
+    n_h, d_c, d_r, d_nope, d_v, bs = 3, 16, 4, 6, 5, 8
+    T = 19
+    c = _bf16_round(rng.standard_normal((T, d_c)))
+    kr = _bf16_round(rng.standard_normal((T, d_r)))
+    W_uk = rng.standard_normal((n_h, d_c, d_nope)) / 3
+    W_uv = rng.standard_normal((n_h, d_c, d_v)) / 3
+    q_nope = rng.standard_normal((n_h, d_nope))
+    q_rope = rng.standard_normal((n_h, d_r))
+    scale = 1 / math.sqrt(d_c + d_r)
+    # explicit: per-head keys [W_uk^T c | k_rope], values W_uv^T c
+    explicit = np.zeros((n_h, d_v))
+    for h in range(n_h):
+        Kh = np.concatenate([c @ W_uk[h], kr], axis=1)
+        Vh = c @ W_uv[h]
+        qh = np.concatenate([q_nope[h], q_rope[h]])
+        explicit[h] = O.attend(qh[None], Kh, Vh, scale)[0][0]
+    # absorbed: q_lat = W_uk q_nope, attend over [c | k_rope], out in latent
+    q_lat = np.einsum("hcn,hn->hc", W_uk, q_nope)
+    nb = (T + bs - 1) // bs
+    lat = np.zeros((nb, 1, bs, d_c + d_r), dtype=np.uint16)
+    rows = _bf16_bits(np.concatenate([c, kr], axis=1))
+    for t in range(T):
+        lat[t // bs, 0, t % bs] = rows[t]
+    q = np.concatenate([q_lat, q_rope], axis=1)[None]
+    out_lat, _ = O.mla_decode(q, lat, np.arange(nb)[None], [T], bs, d_c=d_c,
+                              scale=scale)
+    absorbed = np.einsum("hcv,hc->hv", W_uv, out_lat[0])
+    np.testing.assert_allclose(absorbed, explicit, atol=1e-12)
+
+
+def test_mla_is_mqa_with_shared_row():
+    rng = np.random.default_rng(14)
+    d_c, d_r, bs, n_h = 8, 4, 4, 5
+    lens = [6, 13]
+    kr, _, bt = _random_paged(rng, 2, 1, d_c + d_r, bs, lens)
+    q = rng.standard_normal((2, n_h, d_c + d_r))
+    o1, l1 = O.mla_decode(q, kr, bt, lens, bs, d_c=d_c)
+    vr = kr.copy()
+    vr[..., d_c:] = 0                                 # values: c only
+    o2, l2 = O.gqa_decode(q, kr, vr, bt, lens, bs)
+    np.testing.assert_allclose(o1, o2[..., :d_c], atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# indexer and top-k
+# ---------------------------------------------------------------------------
+def test_indexer_brute_force():
+    rng = np.random.default_rng(15)
+    lens = [1, 9, 25]
+    kr, _, bt = _random_paged(rng, 3, 1, 6, 8, lens)
+    qI = rng.standard_normal((3, 4, 6))
+    w = rng.uniform(0, 1, (3, 4))
+    sc = O.indexer_scores(qI, w, kr, bt, lens, 8)
+    for b, L in enumerate(lens):
+        assert sc[b].shape == (L,)
+        for t in range(L):
+            k = O.bf16_bits_to_f64(kr[bt[b, t // 8], 0, t % 8]).tolist()
+            want = 0.0
+            for j in range(4):
+                dot = sum(qI[b, j, i] * k[i] for i in range(6))
+                want += w[b, j] * (dot if dot > 0 else 0.0)
+            assert abs(sc[b][t] - want) < 1e-12
+
+
+def test_indexer_exact_arithmetic_values():
+    """q, k in {a/8}, w in {1..4}: every score is a multiple of 2^-6 and the
+    fp64 sum is exact; checked against integer arithmetic."""
+    rng = np.random.default_rng(16)
+    T, d, bs = 40, 64, 16
+    ka = rng.integers(-7, 9, (T, d))
+    qa = rng.integers(-7, 9, (1, 4, d))
+    w = rng.integers(1, 5, (1, 4)).astype(np.float64)
+    nb = (T + bs - 1) // bs
+    raw = np.zeros((nb, 1, bs, d), dtype=np.uint16)
+    bits = _bf16_bits(ka / 8.0)
+    for t in range(T):
+        raw[t // bs, 0, t % bs] = bits[t]
+    sc = O.indexer_scores(qa / 8.0, w, raw, np.arange(nb)[None], [T], bs)[0]
+    dots = ka @ qa[0].T                                # integers * 64
+    want = (np.maximum(dots, 0) * w[0]).sum(axis=1) / 64.0
+    assert np.array_equal(sc, want)
+
+
+def test_topk_golden(golden_dir):
+    for case in _load(golden_dir, "topk_ties.json")["cases"]:
+        got = O.topk_select(np.array(case["scores"], dtype=np.float64),
+                            case["k"])
+        assert got.tolist() == case["indices"], case["why"]
+
+
+def test_topk_brute_force():
+    rng = np.random.default_rng(17)
+    for T in (1, 7, 100, 513):
+        s = np.round(rng.standard_normal(T) * 3) / 2     # many ties
+        for k in (1, 5, 64, 600):
+            want = sorted(sorted(range(T), key=lambda t: (-s[t], t))[:k])
+            want += [-1] * (k - len(want))
+            assert O.topk_select(s, k).tolist() == want
+
+
+def test_topk_all_equal_takes_lowest():
+    assert O.topk_select(np.zeros(10), 3).tolist() == [0, 1, 2]
+
+
+def test_sparse_all_positions_equals_dense():
+    rng = np.random.default_rng(18)
+    lens = [10, 40]
+    kr, vr, bt = _random_paged(rng, 2, 1, 16, 8, lens)
+    q = rng.standard_normal((2, 4, 16))
+    idx = np.full((2, 48), -1, dtype=np.int32)
+    for b, L in enumerate(lens):
+        idx[b, :L] = np.arange(L)
+    o1, l1 = O.sparse_decode(q, kr, vr, bt, lens, 8, idx)
+    o2, l2 = O.gqa_decode(q, kr, vr, bt, lens, 8)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_sparse_subset_equals_dense_over_subset():
+    rng = np.random.default_rng(19)
+    L, bs, d = 50, 8, 8
+    kr, vr, bt = _random_paged(rng, 1, 1, d, bs, [L])
+    q = rng.standard_normal((1, 3, d))
+    sel = np.sort(rng.choice(L, 12, replace=False))
+    idx = np.concatenate([sel, [-1, -1, L + 5]]).astype(np.int32)[None]
+    o1, l1 = O.sparse_decode(q, kr, vr, bt, [L], bs, idx, scale=0.3)
+    K = np.stack([O.bf16_bits_to_f64(kr[bt[0, t // bs], 0, t % bs])
+                  for t in sel])
+    V = np.stack([O.bf16_bits_to_f64(vr[bt[0, t // bs], 0, t % bs])
+                  for t in sel])
+    o2, l2 = O.attend(q[0], K, V, 0.3)
+    np.testing.assert_allclose(o1[0], o2, atol=1e-13)
+    np.testing.assert_allclose(l1[0], l2, atol=1e-13)
+
+
+def test_schedule_reuse_and_reindex():
+    rng = np.random.default_rng(20)
+    lens = [30, 70]
+    bs, k = 8, 16
+    kr, vr, bt = _random_paged(rng, 2, 1, 16, bs, lens)
+    ir, _, _ = _random_paged(np.random.default_rng(21), 2, 1, 8, bs, lens)
+    ir = ir[:kr.shape[0]] if ir.shape[0] >= kr.shape[0] else None
+    assert ir is not None
+    modes = ["full", "reuse", "reindex", "reuse"]
+    q = [rng.standard_normal((2, 4, 16)) for _ in modes]
+    qI = [rng.standard_normal((2, 4, 8)) for _ in modes]
+    w = [rng.uniform(0, 1, (2, 4)) for _ in modes]
+    outs, _, sel = O.sparse_schedule(modes, q, qI, w, kr, vr, ir, bt, lens, bs,
+                                     k)
+    i0, _ = O.indexer_topk(qI[0], w[0], ir, bt, lens, bs, k)
+    i2, _ = O.indexer_topk(qI[2], w[2], ir, bt, lens, bs, k)
+    assert np.array_equal(sel[0], i0) and np.array_equal(sel[1], i0)
+    assert np.array_equal(sel[2], i2) and np.array_equal(sel[3], i2)
+    o1, _ = O.sparse_decode(q[1], kr, vr, bt, lens, bs, i0)
+    np.testing.assert_allclose(outs[1], o1, atol=0)
+    with pytest.raises(ValueError):
+        O.sparse_schedule(["reuse"], q, qI, w, kr, vr, ir, bt, lens, bs, k)
+
+
+# ---------------------------------------------------------------------------
+# split-K merge
+# ---------------------------------------------------------------------------
+def test_split_merge_equals_unsplit():
+    rng = np.random.default_rng(22)
+    T, d = 200, 16
+    q = rng.standard_normal((4, d)) * 2
+    K = rng.standard_normal((T, d))
+    V = rng.standard_normal((T, d))
+    ref = O.attend(q, K, V, 0.25)
+    for bounds in ([0, T], [0, 1, T], [0, 64, 128, 192, T],
+                   [0, 0, 50, 50, 199, T], [0, 7, 13, 150, T]):
+        out, lse = O.split_decode(q, K, V, 0.25, bounds)
+        np.testing.assert_allclose(out, ref[0], atol=1e-12)
+        np.testing.assert_allclose(lse, ref[1], atol=1e-12)
+
+
+def test_merge_of_only_empty_parts():
+    out, lse = O.lse_merge([(np.zeros((2, 3)), np.full(2, -np.inf))] * 3)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+# ---------------------------------------------------------------------------
+# size accounting (page figures)
+# ---------------------------------------------------------------------------
+def test_bytes_per_token_llama31_70b(golden_dir):
+    g = _load(golden_dir, "page_figures.json")["llama31_70b_bytes_per_token"]
+    f = g["factors"]
+    assert O.bytes_per_token(f["n_l"], f["n_kv"], f["d_h"], f["b"]) == g["value"]
+    assert g["value"] == 320 * 1024
+
+
+def test_llama2_7b_cache_about_2gb(golden_dir):
+    g = _load(golden_dir, "page_figures.json")["llama2_7b_4096_cache"]
+    f = g["factors"]
+    n = O.cache_bytes(f["n_l"], f["n_kv"], f["d_h"], f["b"], f["B"], f["L"])
+    assert n == 2147483648
+    assert abs(n - g["approx_bytes"]) / g["approx_bytes"] < g["rel_tol"]
+
+
+def test_paged_waste_bound(golden_dir):
+    g = _load(golden_dir, "page_figures.json")["paged_waste"]
+    bs, Lbar = g["block_size"], g["mean_len"]
+    rng = np.random.default_rng(23)
+    for _ in range(20):
+        lens = rng.integers(1, 2 * Lbar, 64)
+        waste = O.paged_waste_slots(lens, bs)
+        assert np.all((waste >= 0) & (waste <= bs - 1))
+        assert waste.sum() <= len(lens) * (bs - 1)
+    assert (bs - 1) / Lbar < g["bound_fraction_below"]
+    assert O.paged_waste_slots([16, 17, 1], 16).tolist() == [0, 15, 15]
