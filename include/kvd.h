@@ -1,0 +1,282 @@
+/*
+ * kvd.h -- C ABI of libkvd.so: one decode step of attention over a paged KV
+ * cache on one GB300 (sm_103a) GPU.
+ *
+ * What is computed (pages cited by title and section):
+ *   "KV cache" (this.guide), "A cache you keep because attention looks
+ *   backwards": at decode step t the new token's query attends over the keys
+ *   and values of every position up to and including t,
+ *       o_t = softmax(q_t K^T * scale) V,   scale = 1/sqrt(d_h) by default,
+ *   and the keys and values of earlier positions are read from a cache
+ *   instead of being recomputed. "Two tensors per layer": per sequence and
+ *   layer the cache is K and V, each [n_kv, L, d_h].
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument that names tensor data is DEVICE memory owned by
+ *     the caller. The library allocates nothing, frees nothing and never
+ *     synchronises the device (kvd_device_error is the one exception).
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream). Outputs are valid once the stream reaches
+ *     that point.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     call that returns anything but KVD_OK launched nothing (except
+ *     KVD_ERR_CUDA, which reports a failed launch). kvd_last_error() then
+ *     describes the problem in words (per host thread).
+ *   - Device-resident values (block table entries, positions, lengths,
+ *     top-k indices) cannot be checked on the host. Kernels check them and,
+ *     instead of touching memory out of bounds, skip the access and set a
+ *     bit in the library's device error word (KVD_DEVERR_*), which
+ *     kvd_device_error() reads.
+ *   - No exception crosses this boundary.
+ *
+ * Workspace: the decode calls split each sequence into runs of positions
+ * processed by separate CTAs and merge the partial results (log-sum-exp
+ * merge). The caller passes the scratch for the partials: at least
+ * kvd_workspace_size() bytes, 256-byte aligned, zero-filled once before its
+ * first use. It also holds arrival counters that every call leaves at zero,
+ * so a workspace can be reused by later calls on the same stream without
+ * clearing; two calls that may run at the same time need two workspaces.
+ *
+ * Paged layout ("KV cache", "The allocator, not the algorithm"; the paging
+ * of the My Weird Prompts 640482 transcript): a cache is a pool of fixed-size
+ * blocks, each holding `block_size` consecutive positions of one sequence,
+ *     element (block, kv_head, slot, i) at
+ *     ((block * n_kv + kv_head) * block_size + slot) * head_dim + i,
+ * and a per-sequence block table maps logical block j (positions
+ * [j*block_size, (j+1)*block_size)) to a physical block. Block tables may
+ * alias physical blocks (shared prefixes are read-only here).
+ */
+#ifndef KVD_H
+#define KVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVD_VERSION 1
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *kvd_stream;
+
+typedef enum kvd_status {
+  KVD_OK = 0,
+  KVD_ERR_NULL = 1,        /* a required pointer is NULL                     */
+  KVD_ERR_SHAPE = 2,       /* inconsistent sizes, or a pointer misaligned    */
+  KVD_ERR_UNSUPPORTED = 3, /* head size / group size / dtype not compiled in */
+  KVD_ERR_CAPACITY = 4,    /* a host-visible length exceeds the block table  */
+  KVD_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required        */
+  KVD_ERR_CUDA = 6         /* a CUDA runtime call or launch failed           */
+} kvd_status;
+
+/* Bits of the device error word. */
+#define KVD_DEVERR_BLOCK 1   /* a block table entry outside [0, num_blocks)   */
+#define KVD_DEVERR_POS 2     /* an append position outside the block table    */
+#define KVD_DEVERR_TIMEOUT 4 /* a bounded wait on a copy gave up               */
+#define KVD_DEVERR_INDEX 8   /* a top-k index >= that sequence's length        */
+#define KVD_DEVERR_LEN 16    /* a sequence length above the block table, or
+                                above the max_seq_len the call was given      */
+
+typedef enum kvd_dtype {
+  KVD_BF16 = 0,    /* 2-byte bfloat16 elements                               */
+  KVD_FP8_E4M3 = 1 /* 1-byte OCP E4M3 codes; value = code * per-head scale   */
+} kvd_dtype;
+
+/*
+ * One layer's cache. Layout [num_blocks][n_kv][block_size][head_dim] for K
+ * and for V. `v` is NULL for a K-only cache (the MLA latent cache and the
+ * indexer key cache). Both base pointers must be 16-byte aligned.
+ *
+ * fp8 ("KV cache", "Fewer bits per number": halving the element size
+ * halves the cache and doubles arithmetic intensity): one fp32 scale per
+ * (layer, kv head) for K and one for V. A stored code c means c * scale;
+ * kvd_kv_append stores E4M3(x * inv_scale) rounded to nearest even and
+ * saturated to +-448. Scale arrays are device memory, [n_kv] each; unused
+ * (may be NULL) for bf16 caches.
+ */
+typedef struct kvd_cache {
+  void *k;
+  void *v;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t n_kv;
+  int32_t head_dim;
+  int32_t dtype; /* kvd_dtype */
+  int32_t reserved;
+  const float *k_scale;
+  const float *v_scale;
+  const float *k_inv_scale;
+  const float *v_inv_scale;
+} kvd_cache;
+
+/*
+ * The batch of sequences being decoded.
+ *   block_table   device [batch][max_blocks_per_seq] int32 physical block ids
+ *   seq_lens      device [batch] int32: positions visible to this step's
+ *                 query, i.e. the cached length AFTER this step's append
+ *   max_seq_len   host: an upper bound on every seq_lens[b]; sizes the split
+ *                 plan and the workspace. Must be <= max_blocks_per_seq *
+ *                 block_size (else KVD_ERR_CAPACITY). A device length above
+ *                 it is clamped to it and flagged KVD_DEVERR_LEN.
+ */
+typedef struct kvd_seqs {
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  int32_t batch;
+  int32_t max_blocks_per_seq;
+  int32_t max_seq_len;
+  int32_t reserved;
+} kvd_seqs;
+
+typedef enum kvd_op {
+  KVD_OP_GQA_DECODE = 0,
+  KVD_OP_MLA_DECODE = 1,
+  KVD_OP_INDEXER_TOPK = 2,
+  KVD_OP_SPARSE_DECODE = 3
+} kvd_op;
+
+/*
+ * kvd_kv_append -- write this step's new key (and value) of every sequence
+ * into the cache. The My Weird Prompts 640482 transcript, on decode: each
+ * new token computes its own query, key and value, and its key and value
+ * are appended, so the cache grows by one entry per layer per token.
+ *
+ *   cache          the layer's cache (K-only when cache->v is NULL)
+ *   block_table    device [batch][max_blocks_per_seq]
+ *   pos            device [batch]: the slot (logical position) to write,
+ *                  normally the cached length before this step
+ *   k_new, v_new   device bf16 [batch][n_kv][head_dim]; v_new is ignored
+ *                  (may be NULL) for a K-only cache and required otherwise
+ * bf16 caches receive the bytes unchanged; fp8 caches receive
+ * E4M3_rne_satfinite(float(x) * inv_scale[kv_head]).
+ * Errors: KVD_ERR_NULL, KVD_ERR_SHAPE (batch < 0, head_dim not a multiple of
+ * 8, misaligned pointer), KVD_ERR_UNSUPPORTED (dtype). A position or block id
+ * out of range on the device skips that row and sets KVD_DEVERR_POS /
+ * KVD_DEVERR_BLOCK.
+ */
+kvd_status kvd_kv_append(const kvd_cache *cache, const int32_t *block_table,
+                         int32_t max_blocks_per_seq, const int32_t *pos,
+                         int32_t batch, const void *k_new, const void *v_new,
+                         kvd_stream stream);
+
+/*
+ * kvd_gqa_decode -- grouped-query attention for one decode step ("KV cache",
+ * "Fewer KV heads, held at the same quality": n_h query heads in n_kv groups,
+ * one KV head per group; MHA is n_kv == n_h and MQA is n_kv == 1). Query
+ * head h reads KV head h / (n_h / n_kv).
+ *
+ *   q         device bf16 [batch][n_h][head_dim]
+ *   scale     softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   out       device bf16 [batch][n_h][head_dim]
+ *   lse       device fp32 [batch][n_h], natural-log log-sum-exp of the
+ *             scaled scores (-inf for an empty sequence); may be NULL
+ *   workspace device scratch of at least kvd_workspace_size(KVD_OP_GQA_DECODE)
+ *             bytes, 256-byte aligned, zero-filled before its first use (see
+ *             "Workspace" above)
+ * Supported: bf16 or fp8 cache, head_dim 64 or 128, n_h / n_kv in
+ * {1, 2, 4, 8, 16}. An empty sequence gives out = 0 and lse = -inf.
+ */
+kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                          const void *q, int32_t n_h, float scale, void *out,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          kvd_stream stream);
+
+/*
+ * kvd_mla_decode -- decode against a latent cache ("KV cache", "Caching a
+ * compressed latent instead of the keys", and the MLA footnote of "Where the
+ * memory actually goes": one latent c of d_c dims plus one shared positional
+ * key of head_dim - d_c dims per token and layer). The key up-projection is
+ * folded into the query ahead of time, so scores run directly against the
+ * cached rows, and the output stays in latent space:
+ *     s_t = scale * (q_lat . c_t + q_rope . k_rope_t),  out = softmax(s) . c
+ *
+ *   latent    K-only bf16 cache with n_kv = 1, head_dim = d_c + d_rope
+ *   q         device bf16 [batch][n_h][head_dim] = [q_lat | q_rope]
+ *   out       device bf16 [batch][n_h][d_c]
+ *   lse       device fp32 [batch][n_h] or NULL
+ * Supported: d_c = 512, head_dim = 576, n_h a multiple of 64.
+ */
+kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
+                          const kvd_seqs *seqs, const void *q, int32_t n_h,
+                          float scale, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, kvd_stream stream);
+
+/*
+ * kvd_indexer_topk -- score every visible cached position with the indexer
+ * and select the top k (the My Weird Prompts 640482 transcript on DeepSeek
+ * Sparse Attention: a lightning indexer scores the prefix and a top-k subset,
+ * k = 2048, is read; "890 bytes a token", section 3: Full and Reindex layers
+ * score with their own indexer query over a shared indexer key cache):
+ *     s_t = sum_j w[j] * max(0, q_idx[j] . k_t),   t < seq_lens[b]
+ *
+ *   index_cache  K-only bf16 cache, n_kv = 1, head_dim = d_idx (64)
+ *   q_idx        device bf16 [batch][n_idx_heads][d_idx]
+ *   w            device fp32 [batch][n_idx_heads]
+ *   indices      device int32 [batch][k]: the k positions with the largest
+ *                scores (computed in fp32), equal scores going to the lower
+ *                position, in ascending position order; -1 pads when fewer
+ *                than k positions are visible
+ *   scores       device fp32 [batch][max_seq_len] or NULL: if given, the
+ *                scores the selection used (entries >= seq_lens[b] are
+ *                unspecified)
+ * Supported: d_idx = 64, n_idx_heads <= 8, 1 <= k <= 16384.
+ */
+kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
+                            const void *q_idx, int32_t n_idx_heads,
+                            const float *w, int32_t k, int32_t *indices,
+                            float *scores, void *workspace,
+                            size_t workspace_bytes, kvd_stream stream);
+
+/*
+ * kvd_sparse_decode -- GQA decode restricted to given positions ("890 bytes
+ * a token", section 3: a Reuse layer attends to the selection an earlier
+ * layer computed; the transcript: sparse attention changes which stored
+ * positions are read).
+ *
+ *   indices  device int32 [batch][k] positions; entries < 0 are skipped, and
+ *            so are entries >= seq_lens[b] (flagged KVD_DEVERR_INDEX)
+ *   q, out, lse, scale as for kvd_gqa_decode
+ * Supported: bf16 cache with n_kv = 1, head_dim = 512, n_h a multiple of 64.
+ */
+kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                             const int32_t *indices, int32_t k, const void *q,
+                             int32_t n_h, float scale, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes,
+                             kvd_stream stream);
+
+/*
+ * kvd_workspace_size -- bytes of workspace the call `op` needs for these
+ * shapes on the current device (the split plan depends on its SM count).
+ * `n_h` is the query head count (indexer heads for KVD_OP_INDEXER_TOPK) and
+ * `k` the top-k size (0 where unused). Queries the device; KVD_ERR_CUDA if
+ * there is none.
+ */
+kvd_status kvd_workspace_size(kvd_op op, const kvd_cache *cache,
+                              const kvd_seqs *seqs, int32_t n_h, int32_t k,
+                              size_t *bytes);
+
+/*
+ * kvd_bytes_per_token -- cache bytes per token ("KV cache", "The size
+ * formula"): 2 tensors x n_l layers x n_kv heads x d_h x elem_bytes.
+ */
+uint64_t kvd_bytes_per_token(int32_t n_l, int32_t n_kv, int32_t d_h,
+                             int32_t elem_bytes);
+
+/* Text for a status code, and the last error of this host thread. */
+const char *kvd_status_string(kvd_status status);
+const char *kvd_last_error(void);
+
+/*
+ * kvd_device_error -- synchronise the current device, then read and clear
+ * the device error word (KVD_DEVERR_* bits; 0 means no error).
+ */
+kvd_status kvd_device_error(int32_t *code);
+
+int32_t kvd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVD_H */

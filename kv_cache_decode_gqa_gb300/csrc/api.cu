@@ -1,0 +1,640 @@
+// The C ABI of libkvd.so (declared in include/kvd.h): host-side argument
+// validation, split planning and kernel dispatch. Nothing here allocates
+// device memory or synchronises, except kvd_device_error().
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kvd.h"
+#include "kvd_internal.h"
+
+namespace {
+
+// The library's device error word (one per device that loads the module).
+__device__ int g_kvd_device_error;
+
+thread_local char g_msg[512] = "";
+
+kvd_status fail(kvd_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kvd_status ok() {
+  g_msg[0] = 0;
+  return KVD_OK;
+}
+
+kvd_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(KVD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+// Per-device facts, looked up once per device with that device current.
+kvd_status device_info(const DeviceInfo **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(KVD_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  DeviceInfo &d = g_devices[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err),
+                             g_kvd_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.ready = true;
+  }
+  *out = &d;
+  return KVD_OK;
+}
+
+bool aligned(const void *p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+int env_int(const char *name, int dflt) {
+  const char *s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  return std::atoi(s);
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+kvd_status check_cache(const kvd_cache *c, bool need_v, const char *what) {
+  if (!c) return fail(KVD_ERR_NULL, "%s: cache is NULL", what);
+  if (!c->k) return fail(KVD_ERR_NULL, "%s: cache->k is NULL", what);
+  if (need_v && !c->v)
+    return fail(KVD_ERR_NULL, "%s: cache->v is NULL (K and V required)", what);
+  if (c->num_blocks < 1 || c->block_size < 1 || c->n_kv < 1 ||
+      c->head_dim < 1)
+    return fail(KVD_ERR_SHAPE,
+                "%s: num_blocks, block_size, n_kv and head_dim must be >= 1",
+                what);
+  if (c->dtype != KVD_BF16 && c->dtype != KVD_FP8_E4M3)
+    return fail(KVD_ERR_UNSUPPORTED, "%s: unknown dtype %d", what, c->dtype);
+  if (!aligned(c->k, 16) || (c->v && !aligned(c->v, 16)))
+    return fail(KVD_ERR_SHAPE, "%s: cache base pointers must be 16-byte aligned",
+                what);
+  const long row_bytes =
+      (long)c->head_dim * (c->dtype == KVD_BF16 ? 2 : 1);
+  if (row_bytes % 16 != 0)
+    return fail(KVD_ERR_SHAPE, "%s: a cache row (%ld bytes) must be a multiple "
+                "of 16 bytes", what, row_bytes);
+  return KVD_OK;
+}
+
+kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
+  if (!s) return fail(KVD_ERR_NULL, "%s: seqs is NULL", what);
+  if (s->batch < 0 || s->max_blocks_per_seq < 1 || s->max_seq_len < 0)
+    return fail(KVD_ERR_SHAPE,
+                "%s: batch >= 0, max_blocks_per_seq >= 1, max_seq_len >= 0 "
+                "required", what);
+  if (s->batch > 65535)
+    return fail(KVD_ERR_SHAPE, "%s: batch %d above 65535", what, s->batch);
+  if (s->batch > 0 && (!s->block_table || !s->seq_lens))
+    return fail(KVD_ERR_NULL, "%s: block_table and seq_lens are required", what);
+  if ((long)s->max_seq_len > (long)s->max_blocks_per_seq * c->block_size)
+    return fail(KVD_ERR_CAPACITY,
+                "%s: max_seq_len %d exceeds the block table's capacity %ld",
+                what, s->max_seq_len,
+                (long)s->max_blocks_per_seq * c->block_size);
+  return KVD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// split plans
+// ---------------------------------------------------------------------------
+struct Plan {
+  int split_len = kvd::kStageRows;
+  int n_splits = 1;
+  int n_groups = 1;        // counters per sequence
+  size_t ws_o_bytes = 0;   // partial outputs
+  size_t ws_lse_bytes = 0; // partial log-sum-exps
+  size_t ws_bytes = 0;     // + arrival counters
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of a split launch: partial outputs, partial lse, then one
+// arrival counter per (sequence, head group), each region 256-byte aligned.
+void finish_plan(Plan &pl, int batch, int n_h, int dv, int n_groups) {
+  pl.n_groups = n_groups;
+  if (pl.n_splits > 1) {
+    pl.ws_o_bytes = round_up((size_t)batch * n_h * pl.n_splits * dv * 4, 256);
+    pl.ws_lse_bytes = round_up((size_t)batch * n_h * pl.n_splits * 4, 256);
+    pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
+                  round_up((size_t)batch * n_groups * 4, 256);
+  }
+}
+
+// Dense decode over positions [0, T): `units` independent (sequence, head
+// group) pairs, each cut into splits of whole 64-token stages so that the
+// launch has enough CTAs for every SM.
+Plan plan_dense(int sms, int units, int max_seq_len, int batch, int n_h,
+                int dv, int n_groups, int ctas_per_sm, int min_chunks) {
+  Plan pl;
+  const int chunks = (max_seq_len + kvd::kStageRows - 1) / kvd::kStageRows;
+  if (chunks <= 1 || units <= 0) {
+    finish_plan(pl, batch, n_h, dv, n_groups);
+    return pl;
+  }
+  const long target = (long)sms * ctas_per_sm;
+  int splits = (int)std::min<long>(chunks, (target + units - 1) / units);
+  splits = std::max(splits, 1);
+  int cps = (chunks + splits - 1) / splits;
+  const int forced = env_int("KVD_SPLIT_CHUNKS", 0);
+  if (forced > 0) cps = forced;
+  cps = std::max(cps, std::min(min_chunks, chunks));
+  pl.n_splits = (chunks + cps - 1) / cps;
+  pl.split_len = cps * kvd::kStageRows;
+  finish_plan(pl, batch, n_h, dv, n_groups);
+  return pl;
+}
+
+enum class DenseKernel { Simt, Mma };
+
+kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
+  if (n_h < 1 || n_h % c->n_kv != 0)
+    return fail(KVD_ERR_SHAPE, "gqa_decode: n_h (%d) must be a positive "
+                "multiple of n_kv (%d)", n_h, c->n_kv);
+  const int g = n_h / c->n_kv;
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(KVD_ERR_UNSUPPORTED, "gqa_decode: head_dim %d (64 or 128)",
+                c->head_dim);
+  if (g == 1 || g == 2 || g == 4) {
+    *kind = DenseKernel::Simt;
+  } else if ((g == 8 || g == 16) && c->head_dim == 128) {
+    *kind = DenseKernel::Mma;
+  } else {
+    return fail(KVD_ERR_UNSUPPORTED,
+                "gqa_decode: group size %d with head_dim %d", g, c->head_dim);
+  }
+  return KVD_OK;
+}
+
+Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
+              DenseKernel kind) {
+  const int units = s->batch * c->n_kv;
+  if (kind == DenseKernel::Simt)
+    return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, c->head_dim,
+                      c->n_kv, 4, 2);
+  return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, c->head_dim,
+                    c->n_kv, 4, 2);
+}
+
+Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms) {
+  // one CTA per (sequence, 64-head tile, split)
+  const int units = s->batch * (n_h / 64);
+  return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, dv, n_h / 64,
+                    1, 2);
+}
+
+Plan sparse_plan(const kvd_seqs *s, int n_h, int k, int dv, int sms) {
+  Plan pl;
+  const int units = s->batch * (n_h / 64);
+  const int rows = 32;  // gathered positions per pipeline stage
+  const int chunks = (k + rows - 1) / rows;
+  int splits = units > 0 ? std::max(1, std::min(chunks, sms / std::max(units, 1)))
+                         : 1;
+  int cps = (chunks + splits - 1) / splits;
+  pl.n_splits = std::max(1, (chunks + cps - 1) / cps);
+  pl.split_len = cps * rows;
+  finish_plan(pl, s->batch, n_h, dv, n_h / 64);
+  return pl;
+}
+
+size_t topk_ws_bytes(const kvd_seqs *s) {
+  return round_up((size_t)s->batch * std::max(s->max_seq_len, 1) * 4, 256);
+}
+
+kvd_status check_ws(const Plan &pl, void *ws, size_t bytes, const char *what) {
+  if (pl.ws_bytes == 0) return KVD_OK;
+  if (!ws)
+    return fail(KVD_ERR_WORKSPACE, "%s: workspace of %zu bytes required", what,
+                pl.ws_bytes);
+  if (!aligned(ws, 256))
+    return fail(KVD_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned",
+                what);
+  if (bytes < pl.ws_bytes)
+    return fail(KVD_ERR_WORKSPACE, "%s: workspace %zu < required %zu bytes",
+                what, bytes, pl.ws_bytes);
+  return KVD_OK;
+}
+
+float log2_scale(float scale, int dk) {
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt((float)dk);
+  return s * 1.4426950408889634f;
+}
+
+kvd_status launched(cudaError_t e, const char *what) {
+  if (e == cudaErrorNotSupported)
+    return fail(KVD_ERR_UNSUPPORTED, "%s: kernel not available", what);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return ok();
+}
+
+kvd_status run_merge(const Plan &pl, const kvd_seqs *s, int n_h, int dv,
+                     float *ws_o, float *ws_lse, void *out, float *lse,
+                     bool dense, cudaStream_t st) {
+  kvd::MergeParams m{};
+  m.ws_o = ws_o;
+  m.ws_lse = ws_lse;
+  m.seq_lens = dense ? s->seq_lens : nullptr;
+  m.out = static_cast<uint16_t *>(out);
+  m.lse = lse;
+  m.batch = s->batch;
+  m.n_h = n_h;
+  m.dv = dv;
+  m.n_splits = pl.n_splits;
+  m.split_len = pl.split_len;
+  m.max_seq_len = s->max_seq_len;
+  return launched(kvd::launch_merge(m, st), "merge");
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+int32_t kvd_version(void) { return KVD_VERSION; }
+
+const char *kvd_last_error(void) { return g_msg; }
+
+const char *kvd_status_string(kvd_status st) {
+  switch (st) {
+    case KVD_OK: return "KVD_OK";
+    case KVD_ERR_NULL: return "KVD_ERR_NULL";
+    case KVD_ERR_SHAPE: return "KVD_ERR_SHAPE";
+    case KVD_ERR_UNSUPPORTED: return "KVD_ERR_UNSUPPORTED";
+    case KVD_ERR_CAPACITY: return "KVD_ERR_CAPACITY";
+    case KVD_ERR_WORKSPACE: return "KVD_ERR_WORKSPACE";
+    case KVD_ERR_CUDA: return "KVD_ERR_CUDA";
+  }
+  return "KVD_ERR_UNKNOWN";
+}
+
+uint64_t kvd_bytes_per_token(int32_t n_l, int32_t n_kv, int32_t d_h,
+                             int32_t elem_bytes) {
+  if (n_l < 0 || n_kv < 0 || d_h < 0 || elem_bytes < 0) return 0;
+  return 2ull * (uint64_t)n_l * (uint64_t)n_kv * (uint64_t)d_h *
+         (uint64_t)elem_bytes;
+}
+
+kvd_status kvd_device_error(int32_t *code) {
+  if (!code) return fail(KVD_ERR_NULL, "device_error: code is NULL");
+  const DeviceInfo *d = nullptr;
+  kvd_status st = device_info(&d);
+  if (st != KVD_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, d->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  const int zero = 0;
+  e = cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  *code = v;
+  return ok();
+}
+
+kvd_status kvd_kv_append(const kvd_cache *cache, const int32_t *block_table,
+                         int32_t max_blocks_per_seq, const int32_t *pos,
+                         int32_t batch, const void *k_new, const void *v_new,
+                         kvd_stream stream) {
+  kvd_status st = check_cache(cache, false, "kv_append");
+  if (st != KVD_OK) return st;
+  if (batch < 0 || batch > 65535 || max_blocks_per_seq < 1)
+    return fail(KVD_ERR_SHAPE, "kv_append: 0 <= batch <= 65535 and "
+                "max_blocks_per_seq >= 1 required");
+  if (cache->head_dim % 8 != 0)
+    return fail(KVD_ERR_SHAPE, "kv_append: head_dim must be a multiple of 8");
+  if (batch == 0) return ok();
+  if (!block_table || !pos || !k_new)
+    return fail(KVD_ERR_NULL, "kv_append: block_table, pos and k_new required");
+  if (cache->v && !v_new)
+    return fail(KVD_ERR_NULL, "kv_append: v_new required for a K/V cache");
+  if (!aligned(k_new, 16) || (cache->v && !aligned(v_new, 16)))
+    return fail(KVD_ERR_SHAPE, "kv_append: k_new / v_new must be 16-byte "
+                "aligned");
+  if (cache->dtype == KVD_FP8_E4M3 &&
+      (!cache->k_inv_scale || (cache->v && !cache->v_inv_scale)))
+    return fail(KVD_ERR_NULL, "kv_append: fp8 cache needs inverse scales");
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  kvd::AppendParams p{};
+  p.k_cache = static_cast<uint8_t *>(cache->k);
+  p.v_cache = static_cast<uint8_t *>(cache->v);
+  p.k_inv_scale = cache->k_inv_scale;
+  p.v_inv_scale = cache->v_inv_scale;
+  p.block_table = block_table;
+  p.pos = pos;
+  p.k_new = static_cast<const uint16_t *>(k_new);
+  p.v_new = static_cast<const uint16_t *>(v_new);
+  p.num_blocks = cache->num_blocks;
+  p.block_size = cache->block_size;
+  p.n_kv = cache->n_kv;
+  p.head_dim = cache->head_dim;
+  p.dtype = cache->dtype;
+  p.max_blocks = max_blocks_per_seq;
+  p.batch = batch;
+  p.err = d->err;
+  return launched(kvd::launch_append(p, reinterpret_cast<cudaStream_t>(stream)),
+                  "kv_append");
+}
+
+kvd_status kvd_workspace_size(kvd_op op, const kvd_cache *cache,
+                              const kvd_seqs *seqs, int32_t n_h, int32_t k,
+                              size_t *bytes) {
+  if (!bytes) return fail(KVD_ERR_NULL, "workspace_size: bytes is NULL");
+  kvd_status st = check_cache(cache, false, "workspace_size");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, cache, "workspace_size");
+  if (st != KVD_OK) return st;
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  switch (op) {
+    case KVD_OP_GQA_DECODE: {
+      DenseKernel kind;
+      st = gqa_shape(cache, n_h, &kind);
+      if (st != KVD_OK) return st;
+      *bytes = gqa_plan(cache, seqs, n_h, d->sms, kind).ws_bytes;
+      return ok();
+    }
+    case KVD_OP_MLA_DECODE:
+      if (n_h < 64 || n_h % 64 != 0)
+        return fail(KVD_ERR_UNSUPPORTED, "mla: n_h must be a multiple of 64");
+      *bytes = mla_plan(seqs, n_h, 512, d->sms).ws_bytes;
+      return ok();
+    case KVD_OP_SPARSE_DECODE:
+      if (n_h < 64 || n_h % 64 != 0 || k < 1)
+        return fail(KVD_ERR_UNSUPPORTED,
+                    "sparse: n_h must be a multiple of 64 and k >= 1");
+      *bytes = sparse_plan(seqs, n_h, k, cache->head_dim, d->sms).ws_bytes;
+      return ok();
+    case KVD_OP_INDEXER_TOPK:
+      *bytes = topk_ws_bytes(seqs);
+      return ok();
+  }
+  return fail(KVD_ERR_UNSUPPORTED, "workspace_size: unknown op %d", (int)op);
+}
+
+kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                          const void *q, int32_t n_h, float scale, void *out,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          kvd_stream stream) {
+  kvd_status st = check_cache(cache, true, "gqa_decode");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, cache, "gqa_decode");
+  if (st != KVD_OK) return st;
+  DenseKernel kind;
+  st = gqa_shape(cache, n_h, &kind);
+  if (st != KVD_OK) return st;
+  if (cache->dtype == KVD_FP8_E4M3 && (!cache->k_scale || !cache->v_scale))
+    return fail(KVD_ERR_NULL, "gqa_decode: fp8 cache needs k_scale, v_scale");
+  if (seqs->batch == 0) return ok();
+  if (!q || !out) return fail(KVD_ERR_NULL, "gqa_decode: q and out required");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(KVD_ERR_SHAPE, "gqa_decode: q and out must be 16-byte aligned");
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  const Plan pl = gqa_plan(cache, seqs, n_h, d->sms, kind);
+  st = check_ws(pl, workspace, workspace_bytes, "gqa_decode");
+  if (st != KVD_OK) return st;
+
+  kvd::DecodeParams p{};
+  p.k = static_cast<const uint8_t *>(cache->k);
+  p.v = static_cast<const uint8_t *>(cache->v);
+  p.k_scale = cache->k_scale;
+  p.v_scale = cache->v_scale;
+  p.block_table = seqs->block_table;
+  p.seq_lens = seqs->seq_lens;
+  p.q = static_cast<const uint16_t *>(q);
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  p.ws_o = static_cast<float *>(workspace);
+  p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes);
+  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes + pl.ws_lse_bytes);
+  p.n_groups = pl.n_groups;
+  p.batch = seqs->batch;
+  p.n_h = n_h;
+  p.n_kv = cache->n_kv;
+  p.dk = p.dv = cache->head_dim;
+  p.dtype = cache->dtype;
+  p.block_size = cache->block_size;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = seqs->max_blocks_per_seq;
+  p.max_seq_len = seqs->max_seq_len;
+  p.split_len = pl.split_len;
+  p.n_splits = pl.n_splits;
+  p.scale_log2 = log2_scale(scale, cache->head_dim);
+  p.err = d->err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = kind == DenseKernel::Simt
+                      ? kvd::launch_decode_simt(p, s)
+                      : kvd::launch_decode_mma(p, cache->dtype, s);
+  return launched(e, "gqa_decode");
+}
+
+kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
+                          const kvd_seqs *seqs, const void *q, int32_t n_h,
+                          float scale, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, kvd_stream stream) {
+  kvd_status st = check_cache(latent, false, "mla_decode");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, latent, "mla_decode");
+  if (st != KVD_OK) return st;
+  if (latent->dtype != KVD_BF16 || latent->n_kv != 1 || d_c != 512 ||
+      latent->head_dim != 576)
+    return fail(KVD_ERR_UNSUPPORTED, "mla_decode: bf16 latent cache with "
+                "n_kv = 1, d_c = 512, head_dim = 576 required");
+  if (n_h < 64 || n_h % 64 != 0)
+    return fail(KVD_ERR_UNSUPPORTED, "mla_decode: n_h must be a multiple of 64");
+  if (seqs->batch == 0) return ok();
+  if (!q || !out) return fail(KVD_ERR_NULL, "mla_decode: q and out required");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(KVD_ERR_SHAPE, "mla_decode: q and out must be 16-byte aligned");
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  const Plan pl = mla_plan(seqs, n_h, d_c, d->sms);
+  st = check_ws(pl, workspace, workspace_bytes, "mla_decode");
+  if (st != KVD_OK) return st;
+  kvd::DecodeParams p{};
+  p.k = p.v = static_cast<const uint8_t *>(latent->k);
+  p.block_table = seqs->block_table;
+  p.seq_lens = seqs->seq_lens;
+  p.q = static_cast<const uint16_t *>(q);
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  p.ws_o = static_cast<float *>(workspace);
+  p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes);
+  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes + pl.ws_lse_bytes);
+  p.n_groups = pl.n_groups;
+  p.batch = seqs->batch;
+  p.n_h = n_h;
+  p.n_kv = 1;
+  p.dk = latent->head_dim;
+  p.dv = d_c;
+  p.block_size = latent->block_size;
+  p.num_blocks = latent->num_blocks;
+  p.max_blocks = seqs->max_blocks_per_seq;
+  p.max_seq_len = seqs->max_seq_len;
+  p.split_len = pl.split_len;
+  p.n_splits = pl.n_splits;
+  p.scale_log2 = log2_scale(scale, latent->head_dim);
+  p.err = d->err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = launched(kvd::launch_decode_mla(p, s), "mla_decode");
+  if (st != KVD_OK || pl.n_splits == 1) return st;
+  return run_merge(pl, seqs, n_h, d_c, p.ws_o, p.ws_lse, out, lse, true, s);
+}
+
+kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                             const int32_t *indices, int32_t k, const void *q,
+                             int32_t n_h, float scale, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes,
+                             kvd_stream stream) {
+  kvd_status st = check_cache(cache, true, "sparse_decode");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, cache, "sparse_decode");
+  if (st != KVD_OK) return st;
+  if (cache->dtype != KVD_BF16 || cache->n_kv != 1 || cache->head_dim != 512)
+    return fail(KVD_ERR_UNSUPPORTED, "sparse_decode: bf16 cache with n_kv = 1 "
+                "and head_dim = 512 required");
+  if (n_h < 64 || n_h % 64 != 0)
+    return fail(KVD_ERR_UNSUPPORTED,
+                "sparse_decode: n_h must be a multiple of 64");
+  if (k < 1) return fail(KVD_ERR_SHAPE, "sparse_decode: k must be >= 1");
+  if (seqs->batch == 0) return ok();
+  if (!indices || !q || !out)
+    return fail(KVD_ERR_NULL, "sparse_decode: indices, q and out required");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(KVD_ERR_SHAPE, "sparse_decode: q and out must be 16-byte "
+                "aligned");
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  const Plan pl = sparse_plan(seqs, n_h, k, cache->head_dim, d->sms);
+  st = check_ws(pl, workspace, workspace_bytes, "sparse_decode");
+  if (st != KVD_OK) return st;
+  kvd::DecodeParams p{};
+  p.k = static_cast<const uint8_t *>(cache->k);
+  p.v = static_cast<const uint8_t *>(cache->v);
+  p.block_table = seqs->block_table;
+  p.seq_lens = seqs->seq_lens;
+  p.indices = indices;
+  p.q = static_cast<const uint16_t *>(q);
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  p.ws_o = static_cast<float *>(workspace);
+  p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes);
+  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                       pl.ws_o_bytes + pl.ws_lse_bytes);
+  p.n_groups = pl.n_groups;
+  p.batch = seqs->batch;
+  p.n_h = n_h;
+  p.n_kv = 1;
+  p.dk = p.dv = cache->head_dim;
+  p.block_size = cache->block_size;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = seqs->max_blocks_per_seq;
+  p.max_seq_len = seqs->max_seq_len;
+  p.n_idx = k;
+  p.split_len = pl.split_len;
+  p.n_splits = pl.n_splits;
+  p.scale_log2 = log2_scale(scale, cache->head_dim);
+  p.err = d->err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = launched(kvd::launch_decode_sparse(p, s), "sparse_decode");
+  if (st != KVD_OK) return st;
+  return run_merge(pl, seqs, n_h, p.dv, p.ws_o, p.ws_lse, out, lse, false, s);
+}
+
+kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
+                            const void *q_idx, int32_t n_idx_heads,
+                            const float *w, int32_t k, int32_t *indices,
+                            float *scores, void *workspace,
+                            size_t workspace_bytes, kvd_stream stream) {
+  kvd_status st = check_cache(index_cache, false, "indexer_topk");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, index_cache, "indexer_topk");
+  if (st != KVD_OK) return st;
+  if (index_cache->dtype != KVD_BF16 || index_cache->n_kv != 1 ||
+      index_cache->head_dim != 64)
+    return fail(KVD_ERR_UNSUPPORTED, "indexer_topk: bf16 K-only cache with "
+                "n_kv = 1 and head_dim = 64 required");
+  if (n_idx_heads < 1 || n_idx_heads > 8)
+    return fail(KVD_ERR_UNSUPPORTED, "indexer_topk: 1..8 indexer heads");
+  if (k < 1 || k > 16384)
+    return fail(KVD_ERR_UNSUPPORTED, "indexer_topk: k must be in [1, 16384]");
+  if (seqs->batch == 0) return ok();
+  if (!q_idx || !w || !indices)
+    return fail(KVD_ERR_NULL, "indexer_topk: q_idx, w and indices required");
+  if (!aligned(q_idx, 16))
+    return fail(KVD_ERR_SHAPE, "indexer_topk: q_idx must be 16-byte aligned");
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  float *sc = scores;
+  if (!sc) {
+    const size_t need = topk_ws_bytes(seqs);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+      return fail(KVD_ERR_WORKSPACE, "indexer_topk: workspace of %zu bytes "
+                  "(256-byte aligned) required when scores is NULL", need);
+    sc = static_cast<float *>(workspace);
+  }
+  kvd::IndexerParams p{};
+  p.cache = static_cast<const uint8_t *>(index_cache->k);
+  p.block_table = seqs->block_table;
+  p.seq_lens = seqs->seq_lens;
+  p.q = static_cast<const uint16_t *>(q_idx);
+  p.w = w;
+  p.scores = sc;
+  p.indices = indices;
+  p.batch = seqs->batch;
+  p.n_heads = n_idx_heads;
+  p.block_size = index_cache->block_size;
+  p.num_blocks = index_cache->num_blocks;
+  p.max_blocks = seqs->max_blocks_per_seq;
+  p.max_seq_len = seqs->max_seq_len;
+  p.score_stride = std::max(seqs->max_seq_len, 1);
+  p.topk = k;
+  p.err = d->err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = launched(kvd::launch_indexer_scores(p, s), "indexer_topk (scores)");
+  if (st != KVD_OK) return st;
+  return launched(kvd::launch_topk(p, s), "indexer_topk (select)");
+}
+
+}  // extern "C"

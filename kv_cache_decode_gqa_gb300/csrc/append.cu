@@ -1,0 +1,81 @@
+// kv_append: write the new token's key and value rows into the paged cache.
+//
+// One thread moves 8 elements (16 bytes of bf16 input). bf16 caches get the
+// bytes unchanged; fp8 caches get E4M3(x * inv_scale[kv_head]) with the
+// product rounded once to fp32 and the conversion done by the hardware's
+// round-to-nearest-even, saturating cvt.
+#include <cuda_fp16.h>
+
+#include "kvd_common.cuh"
+
+namespace kvd {
+
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float first, float second) {
+  uint16_t r;
+  // cvt puts its first source operand in the upper byte.
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(r)
+      : "f"(second), "f"(first));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  const int chunks = p.head_dim / 8;
+  const long per_tensor = (long)p.batch * p.n_kv * chunks;
+  const long total = p.v_cache ? 2 * per_tensor : per_tensor;
+  const long gid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= total) return;
+  const bool is_v = gid >= per_tensor;
+  long r = is_v ? gid - per_tensor : gid;
+  const int c = (int)(r % chunks);
+  r /= chunks;
+  const int h = (int)(r % p.n_kv);
+  const int b = (int)(r / p.n_kv);
+
+  const int pos = p.pos[b];
+  if (pos < 0 || pos >= p.max_blocks * p.block_size) {
+    if (c == 0 && h == 0 && !is_v) report(p.err, DEVERR_POS);
+    return;
+  }
+  const int blk = p.block_table[(long)b * p.max_blocks + pos / p.block_size];
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (c == 0 && h == 0 && !is_v) report(p.err, DEVERR_BLOCK);
+    return;
+  }
+  const long row = ((long)blk * p.n_kv + h) * p.block_size + pos % p.block_size;
+  const uint16_t *src = (is_v ? p.v_new : p.k_new) +
+                        ((long)b * p.n_kv + h) * p.head_dim + c * 8;
+  const uint4 x = *reinterpret_cast<const uint4 *>(src);
+  uint8_t *cache = is_v ? p.v_cache : p.k_cache;
+
+  if (p.dtype == DT_BF16) {
+    *reinterpret_cast<uint4 *>(cache + (row * p.head_dim + c * 8) * 2) = x;
+  } else {
+    const float inv = (is_v ? p.v_inv_scale : p.k_inv_scale)[h];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t packed[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint16_t a = e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j]), inv),
+                                         __fmul_rn(bf16hi(w[2 * j]), inv));
+      const uint16_t bb =
+          e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j + 1]), inv),
+                          __fmul_rn(bf16hi(w[2 * j + 1]), inv));
+      packed[j] = (uint32_t)a | ((uint32_t)bb << 16);
+    }
+    *reinterpret_cast<uint2 *>(cache + row * p.head_dim + c * 8) =
+        make_uint2(packed[0], packed[1]);
+  }
+}
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {
+  const long per_tensor = (long)p.batch * p.n_kv * (p.head_dim / 8);
+  const long total = p.v_cache ? 2 * per_tensor : per_tensor;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const long blocks = (total + threads - 1) / threads;
+  append_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvd

@@ -1,0 +1,234 @@
+// Device helpers shared by the libkvd kernels: inline PTX for mbarriers,
+// bulk asynchronous copies (the TMA engine's untiled form), warp MMA, and
+// exact bf16 / fp8 unpacking. Only documented PTX instructions are used.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvd_internal.h"
+
+namespace kvd {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void report(int *err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`. Each try_wait may suspend the
+// thread for a short hardware-defined time; 2^22 tries bound the wait to well
+// under a few seconds. Returns false (and the caller reports
+// KVD_DEVERR_TIMEOUT) if the phase never completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0),
+// completion counted in bytes on `bar`.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
+                                         uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (used for data read exactly once).
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
+                                              uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes."
+      "L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// numbers
+// ---------------------------------------------------------------------------
+// 2^x with the hardware approximation (relative error ~2^-22).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// bf16 pair (low element in the low half) -> two exact floats.
+__device__ __forceinline__ float bf16lo(uint32_t u) {
+  return __uint_as_float(u << 16);
+}
+__device__ __forceinline__ float bf16hi(uint32_t u) {
+  return __uint_as_float(u & 0xffff0000u);
+}
+
+// float -> bf16 bits, round to nearest even (hardware conversion).
+__device__ __forceinline__ uint16_t f2bf(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+
+// two floats -> packed bf16x2 (a in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two floats -> packed f16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two E4M3 codes (low byte = first element) -> packed f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+// f16 halves of a packed pair -> float, exact.
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+__device__ __forceinline__ float f16lo(uint32_t u) {
+  return f16_to_f32(static_cast<uint16_t>(u & 0xffffu));
+}
+__device__ __forceinline__ float f16hi(uint32_t u) {
+  return f16_to_f32(static_cast<uint16_t>(u >> 16));
+}
+
+// ---------------------------------------------------------------------------
+// split-K merge by the last CTA to finish a (sequence, kv head) group
+// ---------------------------------------------------------------------------
+// Called by every CTA of a split launch after it wrote its partial output
+// ws_o[bh][split][dv] and natural-log lse ws_lse[bh][split] for the heads
+// h0 .. h0 + n_heads - 1 of group `grp` of sequence b. The CTA that arrives
+// last on the group's counter (n_valid arrivals) merges the partials:
+//   out = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M),  M = max_s lse_s,
+//   lse = M + ln sum_s e^(lse_s - M),
+// then resets the counter to zero for the next call. Nothing waits: the
+// other CTAs simply exit.
+__device__ __forceinline__ void merge_if_last(const DecodeParams &p, int b,
+                                              int grp, int n_heads, int dv,
+                                              int n_valid) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int *ctr = p.counters + (long)b * p.n_groups + grp;
+    const int prev = atomicAdd(ctr, 1);
+    s_last = prev == n_valid - 1;
+    if (s_last) atomicExch(ctr, 0);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int h0 = grp * n_heads;
+  for (int idx = threadIdx.x; idx < n_heads * dv; idx += blockDim.x) {
+    const int h = idx / dv, d = idx % dv;
+    const long bh = (long)b * p.n_h + h0 + h;
+    const float *lse_s = p.ws_lse + bh * p.n_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < n_valid; ++s) M = fmaxf(M, __ldcg(lse_s + s));
+    float W = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < n_valid; ++s) {
+        const float ls = __ldcg(lse_s + s);
+        const float w = ls == -INFINITY ? 0.f : expf(ls - M);
+        W += w;
+        acc = fmaf(w, __ldcg(p.ws_o + (bh * p.n_splits + s) * dv + d), acc);
+      }
+    }
+    p.out[bh * dv + d] = f2bf(W > 0.f ? acc / W : 0.f);
+    if (d == 0 && p.lse) p.lse[bh] = W > 0.f ? M + logf(W) : -INFINITY;
+  }
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory, once per device (the
+// attribute call stays out of stream capture after the first launch). Each
+// kernel passes its own `done` table (one flag per device ordinal).
+template <typename K>
+inline cudaError_t set_smem_once(K kern, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+}  // namespace kvd

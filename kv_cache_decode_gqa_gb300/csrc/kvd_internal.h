@@ -1,0 +1,102 @@
+// Internal interface between the C ABI layer (api.cu) and the kernel
+// translation units: plain parameter structs and launcher functions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvd {
+
+// Device error bits (mirrors of the KVD_DEVERR_* values in kvd.h).
+enum : int {
+  DEVERR_BLOCK = 1,
+  DEVERR_POS = 2,
+  DEVERR_TIMEOUT = 4,
+  DEVERR_INDEX = 8,
+  DEVERR_LEN = 16
+};
+
+enum : int { DT_BF16 = 0, DT_FP8 = 1 };
+
+struct AppendParams {
+  uint8_t *k_cache;  // [num_blocks][n_kv][block_size][head_dim]
+  uint8_t *v_cache;  // may be null (K-only)
+  const float *k_inv_scale;
+  const float *v_inv_scale;
+  const int32_t *block_table;
+  const int32_t *pos;
+  const uint16_t *k_new;  // bf16 [batch][n_kv][head_dim]
+  const uint16_t *v_new;
+  int32_t num_blocks, block_size, n_kv, head_dim, dtype;
+  int32_t max_blocks, batch;
+  int *err;
+};
+
+// One decode launch over a paged cache (dense, MLA or gathered positions).
+struct DecodeParams {
+  const uint8_t *k;  // cache base pointers
+  const uint8_t *v;  // == k for a latent cache (values are the first dv dims)
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *indices;  // gathered positions (sparse), else null
+  const uint16_t *q;       // bf16 [batch][n_h][dk]
+  uint16_t *out;           // bf16 [batch][n_h][dv]
+  float *lse;              // [batch][n_h] or null
+  float *ws_o;             // partials [batch][n_h][n_splits][dv]
+  float *ws_lse;           // partials [batch][n_h][n_splits]
+  int *counters;           // [batch][n_groups] arrival counters, kept zero
+  int32_t n_groups;        // head groups per sequence sharing a counter
+  int32_t batch, n_h, n_kv, dk, dv, block_size, num_blocks, max_blocks;
+  int32_t dtype;        // DT_BF16 or DT_FP8
+  int32_t max_seq_len;  // clamp for device lengths
+  int32_t n_idx;        // entries per row of `indices`
+  int32_t split_len;    // tokens (or index entries) per split
+  int32_t n_splits;
+  float scale_log2;  // softmax scale * log2(e)
+  int *err;
+};
+
+struct MergeParams {
+  const float *ws_o;
+  const float *ws_lse;
+  const int32_t *seq_lens;  // null: every split is potentially non-empty
+  uint16_t *out;
+  float *lse;
+  int32_t batch, n_h, dv, n_splits, split_len, max_seq_len, n_idx;
+};
+
+struct IndexerParams {
+  const uint8_t *cache;  // indexer key cache [num_blocks][1][block_size][64]
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const uint16_t *q;  // bf16 [batch][n_heads][64]
+  const float *w;     // [batch][n_heads]
+  float *scores;      // [batch][score_stride]
+  int32_t *indices;   // [batch][k]
+  int32_t batch, n_heads, block_size, num_blocks, max_blocks, max_seq_len;
+  int32_t score_stride, topk;
+  int *err;
+};
+
+// Launchers. Each returns the launch error (cudaSuccess if queued).
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+// Dense GQA/MHA, CUDA cores (group size <= 4).
+cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s);
+// Dense GQA on the tensor cores (group size 8 or 16, head_dim 128).
+cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
+                              cudaStream_t s);
+// MLA latent decode (dk 576, dv 512, n_h multiple of 64).
+cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s);
+// Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64).
+cudaError_t launch_decode_sparse(const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
+cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
+cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);
+
+// Split plans (shared by workspace sizing and the calls).
+constexpr int kStageRows = 64;  // tokens per pipeline stage (dense paths)
+
+}  // namespace kvd

@@ -1,0 +1,21 @@
+// Launchers whose kernels are not compiled into this build yet: each reports
+// cudaErrorNotSupported, which the C ABI turns into KVD_ERR_UNSUPPORTED.
+#include "kvd_internal.h"
+
+namespace kvd {
+cudaError_t launch_decode_mma(const DecodeParams &, int, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_decode_mla(const DecodeParams &, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_decode_sparse(const DecodeParams &, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_indexer_scores(const IndexerParams &, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_topk(const IndexerParams &, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+}  // namespace kvd

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every function
+include/kvd.h declares, and rejects bad arguments on the host before any
+CUDA call. Fake, aligned pointers stand in for device buffers; every call
+here fails validation (or has nothing to do) before it could launch, so the
+fakes are never dereferenced, on a GPU machine either."""
+import ctypes
+import os
+
+import pytest
+
+from kv_cache_decode_gqa_gb300 import _native as N
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(N.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return N.lib()
+
+
+def _cache(**kw):
+    c = N.KvdCache(FAKE, FAKE + 0x100000, 10, 64, 8, 128, 0, 0, None, None,
+                   None, None)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _seqs(**kw):
+    s = N.KvdSeqs(FAKE + 0x200000, FAKE + 0x300000, 4, 16, 1000, 0)
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def test_exports_every_declared_function(lib):
+    names = N.header_functions()
+    assert len(names) == 11
+    for name in names:
+        assert hasattr(lib, name), name
+    assert lib.kvd_version() == 1
+
+
+def test_bytes_per_token(lib):
+    assert lib.kvd_bytes_per_token(80, 8, 128, 2) == 327680
+    assert lib.kvd_bytes_per_token(32, 32, 128, 2) * 4096 == 2147483648
+    assert lib.kvd_bytes_per_token(-1, 8, 128, 2) == 0
+
+
+def test_status_strings(lib):
+    assert lib.kvd_status_string(0) == b"KVD_OK"
+    assert lib.kvd_status_string(5) == b"KVD_ERR_WORKSPACE"
+
+
+def _gqa(lib, c, s, n_h=64, q=FAKE, out=FAKE):
+    return lib.kvd_gqa_decode(ctypes.byref(c), ctypes.byref(s), q, n_h, 0.0,
+                              out, None, None, 0, None)
+
+
+def test_gqa_validation(lib):
+    assert _gqa(lib, _cache(k=None), _seqs()) == 1
+    assert b"cache->k" in lib.kvd_last_error()
+    assert _gqa(lib, _cache(v=None), _seqs()) == 1
+    assert _gqa(lib, _cache(), _seqs(), q=None) == 1
+    assert _gqa(lib, _cache(), _seqs(), n_h=60) == 2      # not a multiple
+    assert _gqa(lib, _cache(), _seqs(), n_h=8 * 32) == 3  # group 32
+    assert _gqa(lib, _cache(head_dim=96), _seqs(), n_h=8) == 3
+    assert _gqa(lib, _cache(dtype=7), _seqs()) == 3
+    assert _gqa(lib, _cache(k=FAKE + 8), _seqs()) == 2    # misaligned
+    assert _gqa(lib, _cache(), _seqs(max_seq_len=64 * 16 + 1)) == 4
+    assert b"capacity" in lib.kvd_last_error()
+    assert _gqa(lib, _cache(), _seqs(batch=-1)) == 2
+    assert _gqa(lib, _cache(dtype=1), _seqs()) == 1       # fp8 needs scales
+    assert _gqa(lib, _cache(), _seqs(batch=0)) == 0       # nothing to do
+
+
+def test_append_validation(lib):
+    c = _cache()
+    f = lib.kvd_kv_append
+    assert f(ctypes.byref(c), FAKE, 16, FAKE, 4, FAKE, None, None) == 1
+    assert f(ctypes.byref(c), FAKE, 0, FAKE, 4, FAKE, FAKE, None) == 2
+    assert f(ctypes.byref(_cache(head_dim=4)), FAKE, 16, FAKE, 4, FAKE, FAKE,
+             None) == 2
+    assert f(ctypes.byref(c), FAKE, 16, FAKE, 4, FAKE + 2, FAKE, None) == 2
+    assert f(ctypes.byref(_cache(dtype=1)), FAKE, 16, FAKE, 4, FAKE, FAKE,
+             None) == 1
+    assert f(ctypes.byref(c), FAKE, 16, FAKE, 0, None, None, None) == 0
+
+
+def test_mla_sparse_indexer_validation(lib):
+    lat = _cache(v=None, n_kv=1, head_dim=576)
+    s = _seqs()
+    m = lib.kvd_mla_decode
+    assert m(ctypes.byref(lat), 256, ctypes.byref(s), FAKE, 128, 0.0, FAKE,
+             None, None, 0, None) == 3
+    assert m(ctypes.byref(lat), 512, ctypes.byref(s), FAKE, 100, 0.0, FAKE,
+             None, None, 0, None) == 3
+    sp = _cache(n_kv=1, head_dim=512)
+    f = lib.kvd_sparse_decode
+    assert f(ctypes.byref(sp), ctypes.byref(s), None, 2048, FAKE, 64, 0.0,
+             FAKE, None, None, 0, None) == 1
+    assert f(ctypes.byref(sp), ctypes.byref(s), FAKE, 0, FAKE, 64, 0.0,
+             FAKE, None, None, 0, None) == 2
+    assert f(ctypes.byref(_cache(n_kv=2, head_dim=512)), ctypes.byref(s),
+             FAKE, 2048, FAKE, 64, 0.0, FAKE, None, None, 0, None) == 3
+    ix = _cache(v=None, n_kv=1, head_dim=64)
+    g = lib.kvd_indexer_topk
+    assert g(ctypes.byref(ix), ctypes.byref(s), FAKE, 4, FAKE, 0, FAKE, None,
+             None, 0, None) == 3
+    assert g(ctypes.byref(ix), ctypes.byref(s), FAKE, 9, FAKE, 16, FAKE, None,
+             None, 0, None) == 3
+    assert g(ctypes.byref(ix), ctypes.byref(s), None, 4, FAKE, 16, FAKE, None,
+             None, 0, None) == 1
+
+
+def test_no_gpu_means_cuda_error_not_crash(lib):
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    size = ctypes.c_size_t(0)
+    st = lib.kvd_workspace_size(0, ctypes.byref(_cache()),
+                                ctypes.byref(_seqs()), 64, 0,
+                                ctypes.byref(size))
+    assert st == 6

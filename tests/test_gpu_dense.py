@@ -1,0 +1,218 @@
+"""GPU parity of kv_append and gqa_decode against the fp64 oracle, through
+the C ABI. Small shapes compare every output element; the full-size
+workloads compare sampled sequences in the launch configuration the bench
+times."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import kv_cache_decode_gqa_gb300 as K  # noqa: E402
+from kv_cache_decode_gqa_gb300 import workloads as W  # noqa: E402
+from tests import gpu_helpers as H  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    K.device_error()            # clear the error word
+    yield
+    assert K.device_error() == 0
+
+
+def _cache_bytes(t):
+    return t.contiguous().view(torch.uint8).cpu().numpy()
+
+
+def _host_bytes(a):
+    return np.ascontiguousarray(a).view(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# append: whole-cache byte equality, canary blocks included
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("bs,lengths", [(16, [0, 15, 16, 47]),
+                                        (64, [63, 64, 200])])
+def test_append_bitexact(dtype, bs, lengths):
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, dtype=dtype, n_h=16, n_kv=2)
+    wl = W.DeviceWorkload(s, layers=[0])
+    c = wl.caches[0]
+    K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
+    torch.cuda.synchronize()
+    kr = W.host_cache_full(s, wl.paging, 0, W.T_K)
+    vr = W.host_cache_full(s, wl.paging, 0, W.T_V)
+    kn = H.host_bits(s, 0, W.T_KNEW, (s.batch, s.n_kv, s.head_dim))
+    vn = H.host_bits(s, 0, W.T_VNEW, (s.batch, s.n_kv, s.head_dim))
+    bt = wl.paging.table
+    if dtype == "fp8":
+        _, kinv, _, vinv = H.host_scales(s, 0)
+        kr = oracle.kv_append(kr, bt, s.lengths, kn, bs, "fp8", kinv)
+        vr = oracle.kv_append(vr, bt, s.lengths, vn, bs, "fp8", vinv)
+    else:
+        kr = oracle.kv_append(kr, bt, s.lengths, kn, bs)
+        vr = oracle.kv_append(vr, bt, s.lengths, vn, bs)
+    assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr))
+    assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr))
+
+
+def test_append_fp8_rounding_edges():
+    """Midpoints between adjacent E4M3 values (ties to even), values past
+    448 (saturate), subnormals and signed zeros, with inv_scale = 1 and a
+    non-power-of-two inv_scale."""
+    t = oracle.e4m3_value_table()[:127]
+    mids = (t[:-1] + t[1:]) / 2
+    vals = np.concatenate([mids, -mids, t, -t,
+                           [448.0, 464.0, 480.0, 12288.0, -12288.0, 2.0 ** -10,
+                            3 * 2.0 ** -10, -2.0 ** -11, 0.0, -0.0]])
+    n_kv, d = 1, 64
+    rows = (len(vals) + d - 1) // d
+    vals = np.concatenate([vals, np.zeros(rows * d - len(vals))])
+    bits = torch.tensor(vals).to(torch.bfloat16)
+    assert np.array_equal(bits.double().numpy(), vals)   # all exact in bf16
+    for inv in (1.0, 1.0 / 0.07):
+        inv32 = np.float32(inv)
+        cache = torch.zeros((rows + 1, n_kv, 1, d), dtype=torch.uint8,
+                            device="cuda")
+        c = K.PagedCache(cache, None, 1, n_kv, d, "fp8",
+                         k_scale=torch.ones(1, device="cuda"),
+                         k_inv_scale=torch.full((1,), float(inv32),
+                                                device="cuda"))
+        bt = torch.arange(rows, dtype=torch.int32,
+                          device="cuda").reshape(rows, 1) + 1
+        pos = torch.zeros(rows, dtype=torch.int32, device="cuda")
+        k_new = bits.reshape(rows, 1, d).cuda()
+        K.kv_append(c, bt, pos, k_new)
+        torch.cuda.synchronize()
+        got = cache.cpu().numpy()[1:, 0, 0, :].reshape(-1)
+        x = vals.astype(np.float32) * inv32
+        want = oracle.e4m3_encode_f32(x.astype(np.float32))
+        assert np.array_equal(got, want), np.nonzero(got != want)
+        assert np.all(cache.cpu().numpy()[0] == 0)        # untouched block
+
+
+# ---------------------------------------------------------------------------
+# dense decode, every element
+# ---------------------------------------------------------------------------
+DENSE_CASES = [
+    # name, n_h, n_kv, d, block_size, cached lengths
+    ("mha_d128", 4, 4, 128, 64, [0, 1, 63, 64, 200, 1000]),
+    ("gqa2_d128", 8, 4, 128, 16, [5, 130, 511]),
+    ("gqa4_d64", 8, 2, 64, 64, [100, 256, 777]),
+    ("gqa4_d128_bs32", 16, 4, 128, 32, [31, 32, 33, 1500]),
+    ("mha_d64_bs320", 2, 2, 64, 320, [1, 319, 600]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("case", DENSE_CASES, ids=[c[0] for c in DENSE_CASES])
+def test_gqa_decode_small(case, dtype):
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=d)
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/{dtype}")
+
+
+def test_tiny_config_full():
+    s = W.config("tiny_gqa")
+    wl = W.DeviceWorkload(s)
+    out, lse = H.device_step(wl, 0)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    H.assert_close(H.to_np_bf16(out), ref, "tiny_gqa")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, "tiny_gqa")
+
+
+def test_empty_and_peaked_sequences():
+    """seq_len 0 gives out = 0, lse = -inf; a query 64x larger makes the
+    softmax nearly one-hot (checks the running-max rescaling)."""
+    s = W.config("llama2_7b_mha", batch=3, lengths=[70, 300, 5], n_layers=1,
+                 n_h=4, n_kv=4)
+    wl = W.DeviceWorkload(s, layers=[0])
+    c = wl.caches[0]
+    K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
+    q = (wl.q[0].float() * 64).to(torch.bfloat16)
+    lens = torch.tensor([0, 301, 6], dtype=torch.int32, device="cuda")
+    out, lse = K.gqa_decode(c, wl.block_table, lens, s.max_seq_len, q)
+    torch.cuda.synchronize()
+    _, _, (kr, vr) = H.oracle_dense_step(s, wl.paging, 0)
+    qh = oracle.bf16_bits_to_f64(
+        q.view(torch.int16).cpu().numpy().view(np.uint16))
+    ref, ref_lse = oracle.gqa_decode(qh, kr, vr, wl.paging.table, [0, 301, 6],
+                                     s.block_size)
+    H.assert_close(H.to_np_bf16(out), ref, "peaked")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, "peaked")
+    assert np.all(H.to_np_bf16(out)[0] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[0]))
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    s = W.config("llama2_7b_mha", batch=1, lengths=[100], n_layers=1, n_h=2,
+                 n_kv=2)
+    wl = W.DeviceWorkload(s, layers=[0])
+    bt = wl.block_table.clone()
+    bt[0, 1] = 1 << 30
+    K.gqa_decode(wl.caches[0], bt, wl.seq_lens, s.max_seq_len, wl.q[0])
+    assert K.device_error() & 1            # KVD_DEVERR_BLOCK
+    bt[0, 1] = -5
+    pos = torch.tensor([64], dtype=torch.int32, device="cuda")
+    K.kv_append(wl.caches[0], bt, pos, wl.k_new[0], wl.v_new[0])
+    assert K.device_error() & 1
+    assert K.device_error() == 0           # cleared by the read
+
+
+def test_workspace_errors():
+    s = W.config("llama2_7b_mha", batch=1, lengths=[4000], n_layers=1, n_h=2,
+                 n_kv=2)
+    wl = W.DeviceWorkload(s, layers=[0])
+    need = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                            wl.seq_lens, s.max_seq_len, 2)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(K.KvdError) as e:
+        K.gqa_decode(wl.caches[0], wl.block_table, wl.seq_lens, s.max_seq_len,
+                     wl.q[0], workspace=small)
+    assert e.value.status == 5
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled sequences, the bench's launch configuration
+# ---------------------------------------------------------------------------
+def test_llama2_7b_full_size_sampled_layers():
+    s = W.config("llama2_7b_mha")
+    wl = W.DeviceWorkload(s, layers=[0, 31])
+    for layer in (0, 31):
+        out, lse = H.device_step(wl, layer)
+        torch.cuda.synchronize()
+        ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, layer, seqs=[0])
+        H.assert_close(H.to_np_bf16(out), ref, f"llama2 layer {layer}")
+        H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"layer {layer}")
+
+
+@pytest.mark.parametrize("name", ["llama31_70b_gqa", "llama31_70b_gqa_fp8"])
+def test_llama31_70b_full_size_sampled(name):
+    s = W.config(name)
+    wl = W.DeviceWorkload(s, layers=[0])
+    try:
+        out, lse = H.device_step(wl, 0)
+    except K.KvdError as e:
+        if e.status == 3:
+            pytest.skip(f"{name}: kernel not built yet")
+        raise
+    torch.cuda.synchronize()
+    seqs = [0, int(np.argmax(s.lengths)), int(np.argmin(s.lengths)), 31]
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0, seqs=seqs)
+    H.assert_close(H.to_np_bf16(out)[seqs], ref, name)
+    H.assert_lse_close(lse.cpu().numpy()[seqs], ref_lse, name)
