@@ -184,6 +184,38 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                           kvd_stream stream);
 
 /*
+ * kvd_gqa_decode_noalloc -- kvd_gqa_decode for callers that cannot allocate
+ * device memory. (The pages have no counterpart of this call; it exists for
+ * how the library is embedded, not for what it computes.)
+ *
+ * kvd_gqa_decode needs scratch memory for its split-K partial results, which
+ * its caller normally allocates and passes as `workspace`. Some callers
+ * cannot do that: a plug-in loaded into a host program that owns every
+ * device allocation and gives it no allocator, or a latency-critical path
+ * that must not call cudaMalloc (an allocation can synchronise the device).
+ * This variant takes only inputs and outputs and uses a scratch array
+ * compiled into the library: KVD_NOALLOC_SCRATCH_BYTES (16 MiB) of device
+ * memory that every GPU which loads the library holds until the process
+ * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments, results and supported shapes are those of kvd_gqa_decode.
+ *   Shapes whose workspace (kvd_workspace_size) exceeds the array return
+ *   KVD_ERR_WORKSPACE and launch nothing.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   Every call uses the same array, and it keeps the last call's contents
+ *   (the call clears the part that must start at zero, in stream order).
+ *   Calls whose work can overlap on the GPU -- on different streams or from
+ *   different host threads -- race on the array and give wrong results;
+ *   serialise them, or use kvd_gqa_decode with separate workspaces.
+ */
+#define KVD_NOALLOC_SCRATCH_BYTES (16u << 20)
+kvd_status kvd_gqa_decode_noalloc(const kvd_cache *cache,
+                                  const kvd_seqs *seqs, const void *q,
+                                  int32_t n_h, float scale, void *out,
+                                  float *lse, kvd_stream stream);
+
+/*
  * kvd_mla_decode -- decode against a latent cache ("KV cache", "Caching a
  * compressed latent instead of the keys", and the MLA footnote of "Where the
  * memory actually goes": one latent c of d_c dims plus one shared positional

@@ -54,6 +54,9 @@ _SIGS = {
     "kvd_gqa_decode": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32, c_float,
                                  c_void_p, c_void_p, c_void_p, c_size_t,
                                  c_void_p]),
+    "kvd_gqa_decode_noalloc": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
+                                         c_float, c_void_p, c_void_p,
+                                         c_void_p]),
     "kvd_mla_decode": (c_int32, [_PCACHE, c_int32, _PSEQS, c_void_p, c_int32,
                                  c_float, c_void_p, c_void_p, c_void_p,
                                  c_size_t, c_void_p]),

@@ -274,6 +274,37 @@ kvd_status run_merge(const Plan &pl, const kvd_seqs *s, int n_h, int dv,
 
 }  // namespace
 
+namespace kvd {
+// Workspace layout of a gqa_decode call with these arguments on the current
+// device: total bytes, and the byte range of the arrival counters (the only
+// part that must be zero when a call starts). Used by the no-allocation
+// entry point.
+kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
+                                int32_t n_h, size_t *total,
+                                size_t *counters_offset,
+                                size_t *counters_bytes) {
+  kvd_status st = check_cache(cache, true, "gqa_decode");
+  if (st != KVD_OK) return st;
+  st = check_seqs(seqs, cache, "gqa_decode");
+  if (st != KVD_OK) return st;
+  DenseKernel kind;
+  st = gqa_shape(cache, n_h, &kind);
+  if (st != KVD_OK) return st;
+  const DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != KVD_OK) return st;
+  const Plan pl = gqa_plan(cache, seqs, n_h, d->sms, kind);
+  *total = pl.ws_bytes;
+  *counters_offset = pl.ws_o_bytes + pl.ws_lse_bytes;
+  *counters_bytes = pl.ws_bytes - *counters_offset;
+  return KVD_OK;
+}
+
+kvd_status set_error(kvd_status st, const char *msg) {
+  return fail(st, "%s", msg);
+}
+}  // namespace kvd
+
 // ===========================================================================
 // C ABI
 // ===========================================================================

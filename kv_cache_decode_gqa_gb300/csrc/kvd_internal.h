@@ -96,6 +96,19 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);
 
+}  // namespace kvd
+
+#include "kvd.h"
+
+namespace kvd {
+// Workspace layout of a gqa_decode call (api.cu).
+kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
+                                int32_t n_h, size_t *total,
+                                size_t *counters_offset,
+                                size_t *counters_bytes);
+// Record `msg` as this host thread's last error and return `st` (api.cu).
+kvd_status set_error(kvd_status st, const char *msg);
+
 // Split plans (shared by workspace sizing and the calls).
 constexpr int kStageRows = 64;  // tokens per pipeline stage (dense paths)
 
