@@ -581,6 +581,30 @@ def run_ours(args, ws, rank, local):
     return line
 
 
+def profile_run(args, local):
+    """The workload's step, eagerly, warmup + steps times: a short program
+    for profilers (no graph, no clock sampling, no oracle)."""
+    import torch
+    import kv_cache_decode_gqa_gb300 as K
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s = W.config(args.config)
+    wl = W.DeviceWorkload(s, device=dev)
+    outs = {l: torch.empty((s.batch, s.n_h, s.dv), dtype=torch.bfloat16,
+                           device=dev) for l in wl.layers}
+    wss = {l: None for l in wl.layers}
+    if s.kind == "sparse":
+        wss["idx"] = {l: torch.empty((s.batch, s.topk), dtype=torch.int32,
+                                     device=dev) for l in wl.layers}
+        wss["topk"] = None
+    step = build_step(K, wl, outs, wss)
+    for _ in range(args.warmup + args.steps):
+        step()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": s.name, "steps": args.warmup + args.steps,
+                      "device_error": K.device_error()}))
+
+
 def launches(s):
     """Kernels the library launches per step (append + decode per layer;
     sparse: appends, indexer score + select per Full/Reindex layer, gather
@@ -686,10 +710,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for profiler runs)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only run warmup + steps eager steps (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
+    if args.profile_run:
+        profile_run(args, local)
+        return
     if args.impl == "reference":
         line = run_reference(args, ws, rank)
         if line is not None:

@@ -193,14 +193,32 @@ kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
   return KVD_OK;
 }
 
+// Persistent stream-K plan of the dense GQA kernels: `ctas_per_sm` CTAs per
+// SM (never more CTAs than 64-token chunks), each leaving at most two
+// partials of G heads x head_dim; one arrival counter per (sequence, kv head).
+Plan plan_stream_k(int sms, int ctas_per_sm, int batch, int n_kv, int g,
+                   int d, int max_seq_len) {
+  Plan pl;
+  const long chunks = (long)batch * n_kv *
+                      ((max_seq_len + kvd::kStageRows - 1) / kvd::kStageRows);
+  long ctas = (long)sms * ctas_per_sm;
+  const int forced = env_int("KVD_DECODE_CTAS", 0);
+  if (forced > 0) ctas = forced;
+  ctas = std::max(1L, std::min(ctas, std::max(chunks, 1L)));
+  pl.n_splits = (int)ctas;
+  pl.n_groups = n_kv;
+  pl.ws_o_bytes = round_up((size_t)ctas * 2 * g * d * 4, 256);
+  pl.ws_lse_bytes = round_up((size_t)ctas * 2 * g * 4, 256);
+  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
+                round_up((size_t)batch * n_kv * 4, 256);
+  return pl;
+}
+
 Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
               DenseKernel kind) {
-  const int units = s->batch * c->n_kv;
-  if (kind == DenseKernel::Simt)
-    return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, c->head_dim,
-                      c->n_kv, 4, 2);
-  return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, c->head_dim,
-                    c->n_kv, 4, 2);
+  (void)kind;
+  return plan_stream_k(sms, 1, s->batch, c->n_kv, n_h / c->n_kv, c->head_dim,
+                       s->max_seq_len);
 }
 
 Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms) {
@@ -445,6 +463,9 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   DenseKernel kind;
   st = gqa_shape(cache, n_h, &kind);
   if (st != KVD_OK) return st;
+  if (seqs->batch > 1024)
+    return fail(KVD_ERR_UNSUPPORTED, "gqa_decode: at most 1024 sequences "
+                "per call (got %d)", seqs->batch);
   if (cache->dtype == KVD_FP8_E4M3 && (!cache->k_scale || !cache->v_scale))
     return fail(KVD_ERR_NULL, "gqa_decode: fp8 cache needs k_scale, v_scale");
   if (seqs->batch == 0) return ok();

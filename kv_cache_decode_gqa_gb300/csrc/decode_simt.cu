@@ -1,33 +1,70 @@
-// Split-K decode attention on the CUDA cores, for small query groups
-// (n_h / n_kv = G in {1, 2, 4}: MHA and narrow GQA). At these group sizes a
-// decode step does 2G FLOPs per cached element ("KV cache", "Why decoding
-// wastes almost all of your FLOPs": intensity 2 n_h / (n_kv b)), so the
-// kernel is bound by HBM bandwidth and the work is to keep the copy engine
-// streaming.
+// Decode attention on the CUDA cores for small query groups (n_h / n_kv =
+// G in {1, 2, 4}: MHA and narrow GQA). At these group sizes a decode step
+// does 2G FLOPs per cached element ("KV cache", "Why decoding wastes almost
+// all of your FLOPs": intensity 2 n_h / (n_kv b)), so the kernel is bound by
+// HBM bandwidth and its job is to keep every SM's copy engine streaming.
 //
-// One CTA handles (split, kv head, sequence): a run of whole 64-token stages.
-// Thread 0 streams each stage's K and V rows (contiguous within a paged
-// block) into a 4-deep shared-memory ring with bulk asynchronous copies
-// completing on an mbarrier. Four warps consume a stage: lane group
-// g = lane / 8 of warp w owns rows 16w + 4i + g (i = 0..3); its 8 lanes each
-// hold D/8 elements of the row, so a row is read from shared memory as one
-// conflict-free 128-byte (or 256-byte) sweep, and the dot product finishes
-// with three xor-shuffles. Every lane group keeps its own online-softmax
-// state (max, sum, output slice) per head; the 16 streams are merged in
-// shared memory at the end. Scores are kept in log2 units (the query is
-// pre-multiplied by scale * log2 e) so each exponential is one ex2.
+// Persistent stream-K launch (stream_k.cuh): one CTA per SM, each taking an
+// equal contiguous share of all (sequence, kv head, 64-token chunk) work.
+// A producer warp resolves 32 chunks at a time (cursor and block ids, one
+// chunk per lane, loaded in parallel), then streams each chunk's K and V
+// rows (contiguous within a paged block) into an NS-deep shared-memory ring
+// with bulk asynchronous copies completing on "full" mbarriers; it refills
+// a stage once the consumers release it on its "empty" mbarrier, so it runs
+// up to NS chunks ahead across unit boundaries.
+//
+// The producer also copies the chunk's query rows into the stage, so a
+// consumer starting a new unit reads its query from shared memory.
+//
+// Eight consumer warps process a chunk: lane group g = lane / 8 of warp w
+// owns rows 8w + 4i + g (i = 0, 1); its 8 lanes each hold D/8 elements of
+// the row, so a row is read from shared memory as one conflict-free sweep,
+// and the dot product finishes with three xor-shuffles. Each lane group
+// keeps its own online-softmax state (running max, sum, output slice) per
+// head, in log2 units (the query is pre-multiplied by scale * log2 e). Each
+// consumer warp walks the same deterministic chunk sequence as the
+// producer, so all warps agree on unit changes. At a unit change a warp
+// merges its four lane-group states and drops the result into one of two
+// shared-memory flush slots, then goes on with the next unit at once. A
+// finisher warp combines the eight warp states of each flushed unit and
+// writes the final output (a unit lying wholly in this CTA's range) or a
+// partial plus a release-ordered arrival on the unit's counter; after the
+// range is done, for every unit on which it arrived last, it merges the
+// partials of all covering CTAs (log-sum-exp merge) and resets the counter.
 #include <cuda_fp16.h>
 
 #include <cmath>
 
 #include "kvd_common.cuh"
+#include "stream_k.cuh"
 
 namespace kvd {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kStages = 4;
-constexpr int kStreams = 16;  // 4 warps x 4 lane groups
+constexpr int kConsumers = 256;            // 8 consumer warps
+constexpr int kWarps = kConsumers / 32;
+constexpr int kProducer = kWarps;          // warp index of the producer
+constexpr int kFinisher = kWarps + 1;      // warp index of the finisher
+constexpr int kThreads = kConsumers + 64;
+constexpr int kEndBar = 1;                 // consumers + finisher, at the end
+
+template <int D, int G, int DT>
+struct Cfg {
+  static constexpr int ES = DT == DT_BF16 ? 2 : 1;
+  static constexpr int ROW = D * ES;                 // bytes per cached row
+  static constexpr int STAGE = kStageRows * ROW;     // K (or V) bytes / chunk
+  static constexpr int NS_RAW = (160 * 1024) / (2 * STAGE);
+  static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW; // ring depth
+  static constexpr int E = D / 8;                    // elements per lane
+  static constexpr int QB = G * D * 2;               // query rows / stage
+  static constexpr int RING = 2 * NS * STAGE + NS * QB;
+  static constexpr int SLOT = kWarps * G * (D + 2);   // floats per slot
+  static constexpr int MERGE = 2 * SLOT * 4;
+  static constexpr int WP_OFF = RING + MERGE;
+  static constexpr int BAR_OFF =
+      (WP_OFF + (int)sizeof(WorkPartition) + 15) / 16 * 16;
+  static constexpr int SMEM = BAR_OFF + (2 * NS + 4) * 8;
+};
 
 // Element index (within a row of D) of the e-th value a lane holds.
 template <int D, int DT>
@@ -39,7 +76,7 @@ __device__ __forceinline__ int elem_index(int sub, int e) {
   }
 }
 
-// Load the lane's D/8 elements of a shared-memory row as floats.
+// The lane's D/8 elements of a shared-memory row, as floats.
 template <int D, int DT>
 __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
                                          float (&x)[D / 8]) {
@@ -55,23 +92,18 @@ __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
         x[j * 8 + 2 * t + 1] = bf16hi(w[t]);
       }
     }
-  } else if constexpr (D == 128) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(row + sub * 16);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t a = e4m3x2_to_f16x2((uint16_t)(w[t] & 0xffff));
-      const uint32_t b = e4m3x2_to_f16x2((uint16_t)(w[t] >> 16));
-      x[4 * t] = f16lo(a);
-      x[4 * t + 1] = f16hi(a);
-      x[4 * t + 2] = f16lo(b);
-      x[4 * t + 3] = f16hi(b);
-    }
   } else {
-    const uint2 u = *reinterpret_cast<const uint2 *>(row + sub * 8);
-    const uint32_t w[2] = {u.x, u.y};
+    constexpr int WORDS = D / 32;  // 32-bit words of fp8 codes per lane
+    uint32_t w[WORDS];
+    if constexpr (WORDS == 4) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(row + sub * 16);
+      w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+    } else {
+      const uint2 u = *reinterpret_cast<const uint2 *>(row + sub * 8);
+      w[0] = u.x, w[1] = u.y;
+    }
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < WORDS; ++t) {
       const uint32_t a = e4m3x2_to_f16x2((uint16_t)(w[t] & 0xffff));
       const uint32_t b = e4m3x2_to_f16x2((uint16_t)(w[t] >> 16));
       x[4 * t] = f16lo(a);
@@ -82,260 +114,476 @@ __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
   }
 }
 
+// 2^(x - M) for a state with running max x, 0 for an empty state.
+__device__ __forceinline__ float weight(float x, float M) {
+  return x == -INFINITY ? 0.f : ex2(x - M);
+}
+
+// Merge the partials of every unit in `merge` (unit start chunks, -1 for
+// none): out = sum_s w_s o_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
+// lse = M + ln sum e^(lse_s - M). Thread `t` of `nt` cooperating threads;
+// `scratch` holds the weights (one float per part). Every load of a pass is
+// independent, so a pass costs about one L2 round trip.
+template <int D, int G>
+__device__ __forceinline__ void merge_owed(const DecodeParams &p,
+                                           const WorkPartition &wp,
+                                           const int *merge, float *scratch,
+                                           int cap, int total, int P, int t,
+                                           int nt) {
+  for (int j = 0; j < 2; ++j) {
+    const int ustart = merge[j];
+    if (ustart < 0) continue;
+    const int b = find_seq(wp, p.batch, ustart);
+    const int h = (ustart - wp.pre[b]) / wp.nch[b];
+    const int uend = ustart + wp.nch[b];
+    const int c_first = cta_of(ustart, total, P);
+    const int parts = cta_of(uend - 1, total, P) - c_first + 1;
+    __threadfence();
+    // pass 1: lse of every part (part i of CTA c_first + i; the first CTA's
+    // partial for this unit is its side-1 slot, the others' their side 0),
+    // kept in shared memory when they fit
+    const bool staged = parts * G <= cap;
+    for (int i = t; staged && i < parts * G; i += nt) {
+      const int part = i / G, g = i % G;
+      const int ws = (c_first + part) * 2 + (part == 0 ? 1 : 0);
+      scratch[i] = __ldcg(p.ws_lse + (long)ws * G + g);
+    }
+    named_sync(kEndBar, nt);
+    for (int idx = t; idx < G * D; idx += nt) {
+      const int g = idx / D, d = idx % D;
+      auto lse_of = [&](int i) {
+        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
+        return staged ? scratch[i * G + g] : __ldcg(p.ws_lse + (long)ws * G + g);
+      };
+      float M = -INFINITY;
+      for (int i = 0; i < parts; ++i) M = fmaxf(M, lse_of(i));
+      float W = 0.f, acc = 0.f;
+      // pass 2: the partial outputs
+      for (int i = 0; i < parts; ++i) {
+        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
+        const float w = expf(lse_of(i) - M);
+        W += w;
+        acc = fmaf(w, __ldcg(p.ws_o + ((long)ws * G + g) * D + d), acc);
+      }
+      const long bh = (long)b * p.n_h + h * G + g;
+      p.out[bh * D + d] = f2bf(acc / W);
+      if (d == 0 && p.lse) p.lse[bh] = M + logf(W);
+    }
+    named_sync(kEndBar, nt);
+  }
+}
+
 template <int D, int G, int DT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_simt_kernel(const DecodeParams p) {
-  constexpr int ES = DT == DT_BF16 ? 2 : 1;
-  constexpr int ROW = D * ES;  // bytes per cached row
-  constexpr int ROWS = kStageRows;
-  constexpr int STAGE = ROWS * ROW;
-  constexpr int E = D / 8;
+  using C = Cfg<D, G, DT>;
+  constexpr int E = C::E;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sk = smem;
-  uint8_t *sv = smem + kStages * STAGE;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * kStages * STAGE);
+  uint8_t *sv = smem + C::NS * C::STAGE;
+  uint8_t *sq = smem + 2 * C::NS * C::STAGE;
+  float *slots = reinterpret_cast<float *>(smem + C::RING);
+  WorkPartition &wp = *reinterpret_cast<WorkPartition *>(smem + C::WP_OFF);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *empty = full + C::NS;
+  uint64_t *sfull = empty + C::NS;  // flush slot written (8 warp arrivals)
+  uint64_t *sempty = sfull + 2;     // flush slot consumed (finisher)
+  __shared__ int s_len_err;
+  __shared__ int s_merge[2];  // unit starts this CTA must merge, or -1
+  __shared__ volatile int s_abort, s_issued, s_producer_done;
 
-  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  const int h0 = hkv * G;
 
-  int T = p.seq_lens[b];
-  if (T > p.max_seq_len) {
-    if (tid == 0 && split == 0 && hkv == 0) report(p.err, DEVERR_LEN);
-    T = p.max_seq_len;
+  if (tid == 0) {
+    s_len_err = 0;
+    s_abort = 0;
+    s_issued = 0;
+    s_producer_done = 0;
+    s_merge[0] = s_merge[1] = -1;
   }
-  T = max(T, 0);
-  const int t0 = split * p.split_len;
-  const int t1 = min(T, t0 + p.split_len);
-  if (t0 >= t1) {
-    // an empty sequence (T == 0) has no split to merge: split 0 writes
-    // out = 0, lse = -inf
-    if (split == 0) {
-      for (int i = tid; i < G * D; i += kThreads)
-        p.out[((long)b * p.n_h + h0 + i / D) * D + i % D] = 0;
-      if (p.lse && tid < G) p.lse[(long)b * p.n_h + h0 + tid] = -INFINITY;
+  __syncthreads();
+  build_partition(wp, p, &s_len_err);
+  if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
+  const int total = wp.total;
+  const int P = min((int)gridDim.x, max(total, 1));
+  const int c = blockIdx.x;
+
+  // sequences with nothing visible: out = 0, lse = -inf
+  if (c == 0) {
+    for (int b = 0; b < p.batch; ++b) {
+      if (wp.nch[b] != 0) continue;
+      for (int i = tid; i < p.n_h * D; i += kThreads)
+        p.out[(long)b * p.n_h * D + i] = 0;
+      if (p.lse)
+        for (int i = tid; i < p.n_h; i += kThreads)
+          p.lse[(long)b * p.n_h + i] = -INFINITY;
     }
-    return;
   }
-  const int nchunks = (t1 - t0 + ROWS - 1) / ROWS;
-  const int32_t *bt = p.block_table + (long)b * p.max_blocks;
+  if (c >= P || total == 0) return;
+  const int lo = range_lo(c, total, P);
+  const int hi = range_lo(c + 1, total, P);
+  const int n = hi - lo;
 
   if (tid == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sfull[s], kWarps);
+      mbar_init(&sempty[s], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Producer (thread 0): copy the rows of chunk c into stage c % kStages.
-  auto issue = [&](int c) {
-    const int s = c % kStages;
-    const int tok = t0 + c * ROWS;
-    const int n = min(ROWS, t1 - tok);
-    mbar_arrive_expect_tx(&bars[s], 2u * n * ROW);
-    int done = 0;
-    while (done < n) {
-      const int t = tok + done;
-      const int slot = t % p.block_size;
-      const int piece = min(n - done, p.block_size - slot);
-      int blk = bt[t / p.block_size];
-      if (blk < 0 || blk >= p.num_blocks) {
-        report(p.err, DEVERR_BLOCK);
-        blk = 0;  // read a valid block; the result is flagged as wrong
+  // ======================= producer warp ==================================
+  if (warp == kProducer) {
+    const uint64_t policy = policy_evict_first();
+    constexpr int kPre = 4;  // block ids prefetched per chunk
+    for (int base = 0; base < n; base += 32) {
+      const int mine = base + lane;
+      int mb = 0, mh = 0, mk = 0, mrows = 0, mblk[kPre] = {0, 0, 0, 0};
+      if (mine < n) {
+        const ChunkCursor cur = cursor_at(wp, p.batch, lo + mine);
+        mb = cur.b, mh = cur.h, mk = cur.k;
+        const int tok = mk * kStageRows;
+        mrows = min(kStageRows, wp.len[mb] - tok);
+        const int lb0 = tok / p.block_size;
+        const int lb1 = (tok + mrows - 1) / p.block_size;
+        const int32_t *bt = p.block_table + (long)mb * p.max_blocks;
+#pragma unroll
+        for (int j = 0; j < kPre; ++j)
+          if (lb0 + j <= lb1) mblk[j] = bt[lb0 + j];
       }
-      const size_t off =
-          (((size_t)blk * p.n_kv + hkv) * p.block_size + slot) * ROW;
-      bulk_g2s(sk + s * STAGE + done * ROW, p.k + off, piece * ROW, &bars[s]);
-      bulk_g2s(sv + s * STAGE + done * ROW, p.v + off, piece * ROW, &bars[s]);
-      done += piece;
-    }
-  };
-  if (tid == 0) {
-    for (int c = 0; c < min(kStages, nchunks); ++c) issue(c);
-  }
-
-  // Query slice of this lane, in log2 units (fp8: times the K scale).
-  float qf[G][E];
-  {
-    const float qs =
-        p.scale_log2 * (DT == DT_FP8 ? p.k_scale[hkv] : 1.0f);
+      const int cnt = min(32, n - base);
+      bool stop = false;
+      for (int j = 0; j < cnt && !stop; ++j) {
+        const int b = __shfl_sync(0xffffffffu, mb, j);
+        const int h = __shfl_sync(0xffffffffu, mh, j);
+        const int k = __shfl_sync(0xffffffffu, mk, j);
+        const int rows = __shfl_sync(0xffffffffu, mrows, j);
+        int blk[kPre];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint16_t *qrow = p.q + ((long)b * p.n_h + h0 + h) * D;
-#pragma unroll
-      for (int e = 0; e < E; e += 8) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(
-            qrow + elem_index<D, DT>(sub, e));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          qf[h][e + 2 * t] = bf16lo(w[t]) * qs;
-          qf[h][e + 2 * t + 1] = bf16hi(w[t]) * qs;
-        }
-      }
-    }
-  }
-
-  float m[G], l[G], o[G][E];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[h][e] = 0.f;
-  }
-
-  int fail_chunk = -1;
-  for (int c = 0; c < nchunks; ++c) {
-    const int s = c % kStages;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[s], (c / kStages) & 1));
-    if (ok) {
-      const int nvalid = min(ROWS, t1 - (t0 + c * ROWS));
-      const uint8_t *kst = sk + s * STAGE;
-      const uint8_t *vst = sv + s * STAGE;
-
-      float sc[4][G];
-  #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = warp * 16 + i * 4 + grp;
-        float kx[E];
-        load_row<D, DT>(kst + r * ROW, sub, kx);
-  #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float a0 = 0.f, a1 = 0.f;
-  #pragma unroll
-          for (int e = 0; e < E; e += 2) {
-            a0 = fmaf(qf[h][e], kx[e], a0);
-            a1 = fmaf(qf[h][e + 1], kx[e + 1], a1);
+        for (int t = 0; t < kPre; ++t)
+          blk[t] = __shfl_sync(0xffffffffu, mblk[t], j);
+        int go = 1;
+        if (lane == 0) {
+          const int i = base + j;
+          const int s = i % C::NS;
+          if (i >= C::NS && !mbar_wait(&empty[s], (i / C::NS - 1) & 1)) {
+            report(p.err, DEVERR_TIMEOUT);
+            go = 0;
           }
-          sc[i][h] = a0 + a1;
-        }
-      }
-  #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-  #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float v = sc[i][h];
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          const int r = warp * 16 + i * 4 + grp;
-          sc[i][h] = r < nvalid ? v : -INFINITY;
-        }
-      }
-      float pr[4][G];
-  #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float mx = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-        const float m_new = fmaxf(m[h], mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float corr = ex2(m[h] - m_use);
-        float psum = 0.f;
-  #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          pr[i][h] = ex2(sc[i][h] - m_use);
-          psum += pr[i][h];
-        }
-        l[h] = l[h] * corr + psum;
-        m[h] = m_new;
-  #pragma unroll
-        for (int e = 0; e < E; ++e) o[h][e] *= corr;
-      }
-  #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = warp * 16 + i * 4 + grp;
-        if (r < nvalid) {
-          float vx[E];
-          load_row<D, DT>(vst + r * ROW, sub, vx);
-  #pragma unroll
-          for (int h = 0; h < G; ++h) {
-  #pragma unroll
-            for (int e = 0; e < E; ++e) o[h][e] = fmaf(pr[i][h], vx[e], o[h][e]);
+          if (s_abort) go = 0;
+          if (go) {
+            const int tok = k * kStageRows;
+            mbar_arrive_expect_tx(&full[s], 2u * rows * C::ROW + C::QB);
+            bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * G) * D,
+                     C::QB, &full[s]);
+            const int32_t *bt = p.block_table + (long)b * p.max_blocks;
+            const int lb0 = tok / p.block_size;
+            int done = 0;
+            while (done < rows) {
+              const int t = tok + done;
+              const int slot = t % p.block_size;
+              const int piece = min(rows - done, p.block_size - slot);
+              const int lb = t / p.block_size - lb0;
+              int pb = lb == 0   ? blk[0]
+                       : lb == 1 ? blk[1]
+                       : lb == 2 ? blk[2]
+                       : lb == 3 ? blk[3]
+                                 : bt[lb0 + lb];
+              if (pb < 0 || pb >= p.num_blocks) {
+                report(p.err, DEVERR_BLOCK);
+                pb = 0;  // read a valid block; the result is flagged as wrong
+              }
+              const size_t off =
+                  (((size_t)pb * p.n_kv + h) * p.block_size + slot) * C::ROW;
+              bulk_g2s_hint(sk + s * C::STAGE + done * C::ROW, p.k + off,
+                            piece * C::ROW, &full[s], policy);
+              bulk_g2s_hint(sv + s * C::STAGE + done * C::ROW, p.v + off,
+                            piece * C::ROW, &full[s], policy);
+              done += piece;
+            }
+            s_issued = i + 1;
           }
         }
+        stop = __shfl_sync(0xffffffffu, go, 0) == 0;
       }
+      if (stop) break;
     }
-    if (__syncthreads_or(!ok)) {
-      fail_chunk = c;
-      break;
-    }
-    if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
-  }
-  if (fail_chunk >= 0) {
-    if (tid == 0) report(p.err, DEVERR_TIMEOUT);
-    // let every copy already issued land before the CTA exits
-    const int issued = min(fail_chunk + kStages, nchunks);
-    for (int st = 0; st < kStages; ++st) {
-      int last = -1;
-      for (int c2 = st; c2 < issued; c2 += kStages) last = c2;
-      if (last >= 0) mbar_wait(&bars[st], (last / kStages) & 1);
-    }
+    if (lane == 0) s_producer_done = 1;
     return;
   }
 
-  // Merge the 16 streams (stages are all consumed; reuse their memory).
-  float *sm_m = reinterpret_cast<float *>(smem);
-  float *sm_l = sm_m + kStreams * G;
-  float *sm_o = sm_l + kStreams * G;  // [stream][G][D]
-  const int stream = warp * 4 + grp;
-  if (sub == 0) {
+  // ======================= finisher warp ==================================
+  if (warp == kFinisher) {
+    int pend_prev[2] = {-1, -1}, pend_start[2] = {0, 0}, n_pend = 0;
+    ChunkCursor fc = cursor_at(wp, p.batch, lo);
+    int x = lo;
+    for (int e = 0; x < hi; ++e) {
+      const int b = fc.b, h = fc.h;
+      const int ustart = wp.pre[b] + h * wp.nch[b];
+      const int uend = ustart + wp.nch[b];
+      const int xend = min(uend, hi);
+      const int sl = e & 1;
+      if (!mbar_wait(&sfull[sl], (e >> 1) & 1)) {
+        if (lane == 0) report(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const float *wm = slots + sl * C::SLOT;
+      const float *wl = wm + kWarps * G;
+      const float *wo = wl + kWarps * G;  // [warp][G][D]
+      const bool whole = ustart >= lo && uend <= hi;
+      const float vs = DT == DT_FP8 ? p.v_scale[h] : 1.0f;
+      const int wslot = c * 2 + partial_side(ustart, lo);
+      for (int idx = lane; idx < G * D; idx += 32) {
+        const int g = idx / D, d = idx % D;
+        float M = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      sm_m[stream * G + h] = m[h];
-      sm_l[stream * G + h] = l[h];
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + g]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float a = weight(wm[w * G + g], M);
+          L = fmaf(wl[w * G + g], a, L);
+          acc = fmaf(wo[(w * G + g) * D + d], a, acc);
+        }
+        const float res = acc / L * vs;
+        const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
+        const long bh = (long)b * p.n_h + h * G + g;
+        if (whole) {
+          p.out[bh * D + d] = f2bf(res);
+          if (d == 0 && p.lse) p.lse[bh] = lse_nat;
+        } else {
+          p.ws_o[((long)wslot * G + g) * D + d] = res;
+          if (d == 0) p.ws_lse[(long)wslot * G + g] = lse_nat;
+        }
+      }
+      if (!whole) __threadfence();  // each lane's partial writes first
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sempty[sl]);  // the slot may be reused
+        if (!whole) {
+          pend_prev[n_pend] = arrive_release(p.counters + (long)b * p.n_kv + h);
+          pend_start[n_pend] = ustart;
+          ++n_pend;
+        }
+      }
+      x = xend;
+      if (x < hi) fc = cursor_at(wp, p.batch, x);
     }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      sm_o[(stream * G + h) * D + elem_index<D, DT>(sub, e)] = o[h][e];
-  }
-  __syncthreads();
-  const float vs = DT == DT_FP8 ? p.v_scale[hkv] : 1.0f;
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int h = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < kStreams; ++s2) M = fmaxf(M, sm_m[s2 * G + h]);
-    float L = 0.f, acc = 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < kStreams; ++s2) {
-      const float ms = sm_m[s2 * G + h];
-      const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
-      L = fmaf(sm_l[s2 * G + h], wgt, L);
-      acc = fmaf(sm_o[(s2 * G + h) * D + d], wgt, acc);
+    // units on which this CTA arrived last: it merges them (below, with the
+    // consumer warps), after resetting their counters for the next call
+    if (lane == 0) {
+      for (int j = 0; j < n_pend; ++j) {
+        const int ustart = pend_start[j];
+        const int bb = find_seq(wp, p.batch, ustart);
+        const int hh = (ustart - wp.pre[bb]) / wp.nch[bb];
+        const int uend = ustart + wp.nch[bb];
+        const int parts =
+            cta_of(uend - 1, total, P) - cta_of(ustart, total, P) + 1;
+        if (pend_prev[j] == parts - 1) {
+          s_merge[j] = ustart;
+          atomicExch(p.counters + (long)bb * p.n_kv + hh, 0);
+        }
+      }
     }
-    const float res = acc / L * vs;
-    const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-    const long bh = (long)b * p.n_h + h0 + h;
-    if (p.n_splits == 1) {
-      p.out[bh * D + d] = f2bf(res);
-      if (d == 0 && p.lse) p.lse[bh] = lse_nat;
-    } else {
-      p.ws_o[(bh * p.n_splits + split) * D + d] = res;
-      if (d == 0) p.ws_lse[bh * p.n_splits + split] = lse_nat;
-    }
+    __threadfence();
+    named_sync(kEndBar, kConsumers + 32);
+    merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, lane,
+                     32 + kConsumers);
+    return;
   }
-  if (p.n_splits > 1) {
-    const int n_valid = (T + p.split_len - 1) / p.split_len;
-    merge_if_last(p, b, hkv, G, D, n_valid);
+
+  // ======================= consumer warps =================================
+  int cur_b = -1, cur_h = -1, n_flush = 0;
+  float qf[G][E], m[G], l[G], o[G][E];
+
+  auto start_unit = [&](int s, int h) {
+    const float qs = p.scale_log2 * (DT == DT_FP8 ? p.k_scale[h] : 1.0f);
+    const uint16_t *qrows = reinterpret_cast<const uint16_t *>(sq + s * C::QB);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int e = 0; e < E; e += 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(
+            qrows + g * D + elem_index<D, DT>(sub, e));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          qf[g][e + 2 * t] = bf16lo(w[t]) * qs;
+          qf[g][e + 2 * t + 1] = bf16hi(w[t]) * qs;
+        }
+      }
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[g][e] = 0.f;
+    }
+  };
+
+  // Merge this warp's four lane-group states and hand them to the finisher.
+  auto flush = [&]() {
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m[g], off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l[g], off);
+        const float M = fmaxf(m[g], m2);
+        const float a = weight(m[g], M);
+        const float a2 = weight(m2, M);
+        l[g] = l[g] * a + l2 * a2;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float o2 = __shfl_xor_sync(0xffffffffu, o[g][e], off);
+          o[g][e] = o[g][e] * a + o2 * a2;
+        }
+        m[g] = M;
+      }
+    }
+    const int sl = n_flush & 1;
+    if (n_flush >= 2) {
+      bool ok = !s_abort && mbar_wait(&sempty[sl], ((n_flush >> 1) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok) && lane == 0) {
+        if (!s_abort) report(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+      }
+    }
+    float *wm = slots + sl * C::SLOT;
+    float *wl = wm + kWarps * G;
+    float *wo = wl + kWarps * G;
+    if (lane < 8) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (sub == 0) {
+          wm[warp * G + g] = m[g];
+          wl[warp * G + g] = l[g];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          wo[(warp * G + g) * D + elem_index<D, DT>(sub, e)] = o[g][e];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sfull[sl]);
+    ++n_flush;
+  };
+
+  ChunkCursor cc = cursor_at(wp, p.batch, lo);
+  for (int i = 0; i < n; ++i) {
+    const int s = i % C::NS;
+    // a copy that never completes (bounded wait) sets the abort flag; the
+    // remaining chunks are then skipped and the results flagged wrong
+    bool ok = !s_abort && mbar_wait(&full[s], (i / C::NS) & 1);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) {
+      if (!s_abort) report(p.err, DEVERR_TIMEOUT);
+      s_abort = 1;
+    }
+    if (cc.b != cur_b || cc.h != cur_h) {
+      if (cur_b >= 0) flush();
+      cur_b = cc.b;
+      cur_h = cc.h;
+      start_unit(s, cur_h);
+    }
+    const int nvalid = min(kStageRows, wp.len[cc.b] - cc.k * kStageRows);
+    if (ok) {
+      const uint8_t *kst = sk + s * C::STAGE;
+      const uint8_t *vst = sv + s * C::STAGE;
+      float sc[2][G];
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int r = warp * 8 + i2 * 4 + grp;
+        float kx[E];
+        load_row<D, DT>(kst + r * C::ROW, sub, kx);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            a0 = fmaf(qf[g][e], kx[e], a0);
+            a1 = fmaf(qf[g][e + 1], kx[e + 1], a1);
+          }
+          sc[i2][g] = a0 + a1;
+        }
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int r = warp * 8 + i2 * 4 + grp;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float v = sc[i2][g];
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          sc[i2][g] = r < nvalid ? v : -INFINITY;
+        }
+      }
+      float pr[2][G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float m_new = fmaxf(m[g], fmaxf(sc[0][g], sc[1][g]));
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float corr = ex2(m[g] - m_use);
+        pr[0][g] = ex2(sc[0][g] - m_use);
+        pr[1][g] = ex2(sc[1][g] - m_use);
+        l[g] = l[g] * corr + pr[0][g] + pr[1][g];
+        m[g] = m_new;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[g][e] *= corr;
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int r = warp * 8 + i2 * 4 + grp;
+        if (r < nvalid) {
+          float vx[E];
+          load_row<D, DT>(vst + r * C::ROW, sub, vx);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+              o[g][e] = fmaf(pr[i2][g], vx[e], o[g][e]);
+          }
+        }
+      }
+    }
+    // release the stage to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    cursor_next(wp, p.batch, p.n_kv, cc);
+  }
+  if (cur_b >= 0) flush();
+  named_sync(kEndBar, kConsumers + 32);
+  merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, 32 + tid,
+                   32 + kConsumers);
+
+  if (s_abort && tid == 0) {
+    // let every copy the producer issued land before the CTA exits
+    for (int t = 0; t < (1 << 20) && !s_producer_done; ++t) __nanosleep(1000);
+    const int issued = s_issued;
+    for (int st = 0; st < C::NS; ++st) {
+      int last = -1;
+      for (int c2 = st; c2 < issued; c2 += C::NS) last = c2;
+      if (last >= 0) mbar_wait(&full[st], (last / C::NS) & 1);
+    }
   }
 }
 
 template <int D, int G, int DT>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
-  constexpr int ROW = D * (DT == DT_BF16 ? 2 : 1);
-  constexpr int SMEM = 2 * kStages * kStageRows * ROW + kStages * 8;
-  static_assert(kStreams * G * (D + 2) * 4 <= 2 * kStages * kStageRows * ROW,
-                "stream merge must fit in the stage buffers");
+  using C = Cfg<D, G, DT>;
+  static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
   auto kern = decode_simt_kernel<D, G, DT>;
   static bool done[64] = {};  // one table per instantiation
-  cudaError_t e = set_smem_once(kern, SMEM, done);
+  cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_splits, p.n_kv, p.batch);
-  kern<<<grid, kThreads, SMEM, s>>>(p);
+  kern<<<p.n_splits, kThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -353,6 +601,7 @@ cudaError_t launch_g(const DecodeParams &p, cudaStream_t s) {
 
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s) {
   const bool fp8 = p.dtype == DT_FP8;
+  if (p.batch > kMaxDecodeBatch) return cudaErrorNotSupported;
   if (p.dk == 128) return fp8 ? launch_g<128, DT_FP8>(p, s)
                               : launch_g<128, DT_BF16>(p, s);
   if (p.dk == 64) return fp8 ? launch_g<64, DT_FP8>(p, s)

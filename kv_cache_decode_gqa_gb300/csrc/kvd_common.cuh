@@ -101,6 +101,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 }
 
 // ---------------------------------------------------------------------------
+// named barriers (a subset of the CTA's warps)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dep_wait() {

@@ -83,10 +83,10 @@ def test_noalloc_matches_workspace_entry_point(case):
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(monkeypatch):
-    """With one 64-token stage per split, 8 sequences of 65,536 positions and
-    32 heads need ~135 MB of partials: more than the static array. The call
-    must return KVD_ERR_WORKSPACE without launching anything."""
-    monkeypatch.setenv("KVD_SPLIT_CHUNKS", "1")
+    """A launch of 200,000 CTAs (the tuning override KVD_DECODE_CTAS) over 32
+    heads of 128 needs ~200 MB of partials: more than the static array. The
+    call must return KVD_ERR_WORKSPACE without launching anything."""
+    monkeypatch.setenv("KVD_DECODE_CTAS", "200000")
     B, n_h, d, bs, T = 8, 32, 128, 64, 65536
     dev = "cuda"
     cache = K.PagedCache(torch.zeros((2, n_h, bs, d), dtype=torch.bfloat16,
