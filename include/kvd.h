@@ -176,7 +176,8 @@ kvd_status kvd_kv_append(const kvd_cache *cache, const int32_t *block_table,
  *             bytes, 256-byte aligned, zero-filled before its first use (see
  *             "Workspace" above)
  * Supported: bf16 or fp8 cache, head_dim 64 or 128, n_h / n_kv in
- * {1, 2, 4, 8, 16}, at most 1024 sequences per call. An empty sequence
+ * {1, 2, 4, 8, 16} (8 and 16 need head_dim 128 and a block_size that is a
+ * multiple of 64 or one of 16, 32), at most 1024 sequences per call. An empty sequence
  * gives out = 0 and lse = -inf.
  */
 kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 LIB_SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "merge.cu",
-               "pending.cu", "noalloc.cu"]
+               "pending.cu", "noalloc.cu", "decode_mma.cu"]
 INPUTS_SOURCES = ["inputs_fill.cu"]
 LIB = os.path.join(PKG, "libkvd.so")
 INPUTS_LIB = os.path.join(PKG, "libkvd_inputs.so")

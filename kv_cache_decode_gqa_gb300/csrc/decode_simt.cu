@@ -119,60 +119,6 @@ __device__ __forceinline__ float weight(float x, float M) {
   return x == -INFINITY ? 0.f : ex2(x - M);
 }
 
-// Merge the partials of every unit in `merge` (unit start chunks, -1 for
-// none): out = sum_s w_s o_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
-// lse = M + ln sum e^(lse_s - M). Thread `t` of `nt` cooperating threads;
-// `scratch` holds the weights (one float per part). Every load of a pass is
-// independent, so a pass costs about one L2 round trip.
-template <int D, int G>
-__device__ __forceinline__ void merge_owed(const DecodeParams &p,
-                                           const WorkPartition &wp,
-                                           const int *merge, float *scratch,
-                                           int cap, int total, int P, int t,
-                                           int nt) {
-  for (int j = 0; j < 2; ++j) {
-    const int ustart = merge[j];
-    if (ustart < 0) continue;
-    const int b = find_seq(wp, p.batch, ustart);
-    const int h = (ustart - wp.pre[b]) / wp.nch[b];
-    const int uend = ustart + wp.nch[b];
-    const int c_first = cta_of(ustart, total, P);
-    const int parts = cta_of(uend - 1, total, P) - c_first + 1;
-    __threadfence();
-    // pass 1: lse of every part (part i of CTA c_first + i; the first CTA's
-    // partial for this unit is its side-1 slot, the others' their side 0),
-    // kept in shared memory when they fit
-    const bool staged = parts * G <= cap;
-    for (int i = t; staged && i < parts * G; i += nt) {
-      const int part = i / G, g = i % G;
-      const int ws = (c_first + part) * 2 + (part == 0 ? 1 : 0);
-      scratch[i] = __ldcg(p.ws_lse + (long)ws * G + g);
-    }
-    named_sync(kEndBar, nt);
-    for (int idx = t; idx < G * D; idx += nt) {
-      const int g = idx / D, d = idx % D;
-      auto lse_of = [&](int i) {
-        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
-        return staged ? scratch[i * G + g] : __ldcg(p.ws_lse + (long)ws * G + g);
-      };
-      float M = -INFINITY;
-      for (int i = 0; i < parts; ++i) M = fmaxf(M, lse_of(i));
-      float W = 0.f, acc = 0.f;
-      // pass 2: the partial outputs
-      for (int i = 0; i < parts; ++i) {
-        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
-        const float w = expf(lse_of(i) - M);
-        W += w;
-        acc = fmaf(w, __ldcg(p.ws_o + ((long)ws * G + g) * D + d), acc);
-      }
-      const long bh = (long)b * p.n_h + h * G + g;
-      p.out[bh * D + d] = f2bf(acc / W);
-      if (d == 0 && p.lse) p.lse[bh] = M + logf(W);
-    }
-    named_sync(kEndBar, nt);
-  }
-}
-
 template <int D, int G, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_simt_kernel(const DecodeParams p) {
@@ -396,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     named_sync(kEndBar, kConsumers + 32);
     merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, lane,
-                     32 + kConsumers);
+                     32 + kConsumers, kEndBar);
     return;
   }
 
@@ -561,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cur_b >= 0) flush();
   named_sync(kEndBar, kConsumers + 32);
   merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, 32 + tid,
-                   32 + kConsumers);
+                   32 + kConsumers, kEndBar);
 
   if (s_abort && tid == 0) {
     // let every copy the producer issued land before the CTA exits

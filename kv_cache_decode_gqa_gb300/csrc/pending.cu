@@ -3,9 +3,6 @@
 #include "kvd_internal.h"
 
 namespace kvd {
-cudaError_t launch_decode_mma(const DecodeParams &, int, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 cudaError_t launch_decode_mla(const DecodeParams &, cudaStream_t) {
   return cudaErrorNotSupported;
 }

@@ -152,4 +152,58 @@ __device__ __forceinline__ int arrive_release(int *ctr) {
   return prev;
 }
 
+// Merge the partials of every unit in `merge` (unit start chunks, -1 for
+// none): out = sum_s w_s o_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
+// lse = M + ln sum e^(lse_s - M). Thread `t` of `nt` cooperating threads (named barrier `bar`);
+// `scratch` holds the weights (one float per part). Every load of a pass is
+// independent, so a pass costs about one L2 round trip.
+template <int D, int G>
+__device__ __forceinline__ void merge_owed(const DecodeParams &p,
+                                           const WorkPartition &wp,
+                                           const int *merge, float *scratch,
+                                           int cap, int total, int P, int t,
+                                           int nt, int bar) {
+  for (int j = 0; j < 2; ++j) {
+    const int ustart = merge[j];
+    if (ustart < 0) continue;
+    const int b = find_seq(wp, p.batch, ustart);
+    const int h = (ustart - wp.pre[b]) / wp.nch[b];
+    const int uend = ustart + wp.nch[b];
+    const int c_first = cta_of(ustart, total, P);
+    const int parts = cta_of(uend - 1, total, P) - c_first + 1;
+    __threadfence();
+    // pass 1: lse of every part (part i of CTA c_first + i; the first CTA's
+    // partial for this unit is its side-1 slot, the others' their side 0),
+    // kept in shared memory when they fit
+    const bool staged = parts * G <= cap;
+    for (int i = t; staged && i < parts * G; i += nt) {
+      const int part = i / G, g = i % G;
+      const int ws = (c_first + part) * 2 + (part == 0 ? 1 : 0);
+      scratch[i] = __ldcg(p.ws_lse + (long)ws * G + g);
+    }
+    named_sync(bar, nt);
+    for (int idx = t; idx < G * D; idx += nt) {
+      const int g = idx / D, d = idx % D;
+      auto lse_of = [&](int i) {
+        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
+        return staged ? scratch[i * G + g] : __ldcg(p.ws_lse + (long)ws * G + g);
+      };
+      float M = -INFINITY;
+      for (int i = 0; i < parts; ++i) M = fmaxf(M, lse_of(i));
+      float W = 0.f, acc = 0.f;
+      // pass 2: the partial outputs
+      for (int i = 0; i < parts; ++i) {
+        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
+        const float w = expf(lse_of(i) - M);
+        W += w;
+        acc = fmaf(w, __ldcg(p.ws_o + ((long)ws * G + g) * D + d), acc);
+      }
+      const long bh = (long)b * p.n_h + h * G + g;
+      p.out[bh * D + d] = f2bf(acc / W);
+      if (d == 0 && p.lse) p.lse[bh] = M + logf(W);
+    }
+    named_sync(bar, nt);
+  }
+}
+
 }  // namespace kvd

@@ -107,6 +107,11 @@ DENSE_CASES = [
     ("gqa4_d64", 8, 2, 64, 64, [100, 256, 777]),
     ("gqa4_d128_bs32", 16, 4, 128, 32, [31, 32, 33, 1500]),
     ("mha_d64_bs320", 2, 2, 64, 320, [1, 319, 600]),
+    # tensor-core path: query groups of 8 and 16
+    ("gqa8_bs64", 16, 2, 128, 64, [0, 1, 63, 64, 65, 500]),
+    ("gqa16_bs16", 32, 2, 128, 16, [3, 100, 257]),
+    ("gqa8_bs128", 8, 1, 128, 128, [129, 1000]),
+    ("gqa8_bs32", 64, 8, 128, 32, [31, 700]),
 ]
 
 
