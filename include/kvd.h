@@ -230,7 +230,8 @@ kvd_status kvd_gqa_decode_noalloc(const kvd_cache *cache,
  *   q         device bf16 [batch][n_h][head_dim] = [q_lat | q_rope]
  *   out       device bf16 [batch][n_h][d_c]
  *   lse       device fp32 [batch][n_h] or NULL
- * Supported: d_c = 512, head_dim = 576, n_h a multiple of 64.
+ * Supported: d_c = 512, head_dim = 576, n_h a multiple of 64, at most 256
+ * sequences per call.
  */
 kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
                           const kvd_seqs *seqs, const void *q, int32_t n_h,
@@ -272,7 +273,8 @@ kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
  *   indices  device int32 [batch][k] positions; entries < 0 are skipped, and
  *            so are entries >= seq_lens[b] (flagged KVD_DEVERR_INDEX)
  *   q, out, lse, scale as for kvd_gqa_decode
- * Supported: bf16 cache with n_kv = 1, head_dim = 512, n_h a multiple of 64.
+ * Supported: bf16 cache with n_kv = 1, head_dim = 512, n_h a multiple of 64,
+ * at most 256 sequences per call.
  */
 kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                              const int32_t *indices, int32_t k, const void *q,

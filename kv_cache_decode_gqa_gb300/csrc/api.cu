@@ -148,30 +148,6 @@ void finish_plan(Plan &pl, int batch, int n_h, int dv, int n_groups) {
   }
 }
 
-// Dense decode over positions [0, T): `units` independent (sequence, head
-// group) pairs, each cut into splits of whole 64-token stages so that the
-// launch has enough CTAs for every SM.
-Plan plan_dense(int sms, int units, int max_seq_len, int batch, int n_h,
-                int dv, int n_groups, int ctas_per_sm, int min_chunks) {
-  Plan pl;
-  const int chunks = (max_seq_len + kvd::kStageRows - 1) / kvd::kStageRows;
-  if (chunks <= 1 || units <= 0) {
-    finish_plan(pl, batch, n_h, dv, n_groups);
-    return pl;
-  }
-  const long target = (long)sms * ctas_per_sm;
-  int splits = (int)std::min<long>(chunks, (target + units - 1) / units);
-  splits = std::max(splits, 1);
-  int cps = (chunks + splits - 1) / splits;
-  const int forced = env_int("KVD_SPLIT_CHUNKS", 0);
-  if (forced > 0) cps = forced;
-  cps = std::max(cps, std::min(min_chunks, chunks));
-  pl.n_splits = (chunks + cps - 1) / cps;
-  pl.split_len = cps * kvd::kStageRows;
-  finish_plan(pl, batch, n_h, dv, n_groups);
-  return pl;
-}
-
 enum class DenseKernel { Simt, Mma };
 
 kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
@@ -221,25 +197,33 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
                        s->max_seq_len);
 }
 
+// Persistent stream-K plan of the 64-head-tile kernels (latent and sparse
+// decode): 32-position chunks of `rows` positions (or index entries) per
+// sequence and head tile; partials of 64 heads x dv per CTA side; one
+// arrival counter per (sequence, head tile).
+Plan plan_wide(int sms, int batch, int n_h, int rows, int dv) {
+  Plan pl;
+  const int tiles = n_h / 64;
+  const long chunks = (long)batch * tiles * ((rows + 31) / 32);
+  long ctas = sms;
+  const int forced = env_int("KVD_DECODE_CTAS", 0);
+  if (forced > 0) ctas = forced;
+  ctas = std::max(1L, std::min(ctas, std::max(chunks, 1L)));
+  pl.n_splits = (int)ctas;
+  pl.n_groups = tiles;
+  pl.ws_o_bytes = round_up((size_t)ctas * 2 * 64 * dv * 4, 256);
+  pl.ws_lse_bytes = round_up((size_t)ctas * 2 * 64 * 4, 256);
+  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
+                round_up((size_t)batch * tiles * 4, 256);
+  return pl;
+}
+
 Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms) {
-  // one CTA per (sequence, 64-head tile, split)
-  const int units = s->batch * (n_h / 64);
-  return plan_dense(sms, units, s->max_seq_len, s->batch, n_h, dv, n_h / 64,
-                    1, 2);
+  return plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
 }
 
 Plan sparse_plan(const kvd_seqs *s, int n_h, int k, int dv, int sms) {
-  Plan pl;
-  const int units = s->batch * (n_h / 64);
-  const int rows = 32;  // gathered positions per pipeline stage
-  const int chunks = (k + rows - 1) / rows;
-  int splits = units > 0 ? std::max(1, std::min(chunks, sms / std::max(units, 1)))
-                         : 1;
-  int cps = (chunks + splits - 1) / splits;
-  pl.n_splits = std::max(1, (chunks + cps - 1) / cps);
-  pl.split_len = cps * rows;
-  finish_plan(pl, s->batch, n_h, dv, n_h / 64);
-  return pl;
+  return plan_wide(sms, s->batch, n_h, k, dv);
 }
 
 size_t topk_ws_bytes(const kvd_seqs *s) {
@@ -270,24 +254,6 @@ kvd_status launched(cudaError_t e, const char *what) {
     return fail(KVD_ERR_UNSUPPORTED, "%s: kernel not available", what);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return ok();
-}
-
-kvd_status run_merge(const Plan &pl, const kvd_seqs *s, int n_h, int dv,
-                     float *ws_o, float *ws_lse, void *out, float *lse,
-                     bool dense, cudaStream_t st) {
-  kvd::MergeParams m{};
-  m.ws_o = ws_o;
-  m.ws_lse = ws_lse;
-  m.seq_lens = dense ? s->seq_lens : nullptr;
-  m.out = static_cast<uint16_t *>(out);
-  m.lse = lse;
-  m.batch = s->batch;
-  m.n_h = n_h;
-  m.dv = dv;
-  m.n_splits = pl.n_splits;
-  m.split_len = pl.split_len;
-  m.max_seq_len = s->max_seq_len;
-  return launched(kvd::launch_merge(m, st), "merge");
 }
 
 }  // namespace
@@ -529,6 +495,8 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
                 "n_kv = 1, d_c = 512, head_dim = 576 required");
   if (n_h < 64 || n_h % 64 != 0)
     return fail(KVD_ERR_UNSUPPORTED, "mla_decode: n_h must be a multiple of 64");
+  if (seqs->batch > 256)
+    return fail(KVD_ERR_UNSUPPORTED, "mla_decode: at most 256 sequences");
   if (seqs->batch == 0) return ok();
   if (!q || !out) return fail(KVD_ERR_NULL, "mla_decode: q and out required");
   if (!aligned(q, 16) || !aligned(out, 16))
@@ -566,9 +534,7 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
   p.scale_log2 = log2_scale(scale, latent->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = launched(kvd::launch_decode_mla(p, s), "mla_decode");
-  if (st != KVD_OK || pl.n_splits == 1) return st;
-  return run_merge(pl, seqs, n_h, d_c, p.ws_o, p.ws_lse, out, lse, true, s);
+  return launched(kvd::launch_decode_mla(p, s), "mla_decode");
 }
 
 kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
@@ -587,6 +553,8 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
     return fail(KVD_ERR_UNSUPPORTED,
                 "sparse_decode: n_h must be a multiple of 64");
   if (k < 1) return fail(KVD_ERR_SHAPE, "sparse_decode: k must be >= 1");
+  if (seqs->batch > 256)
+    return fail(KVD_ERR_UNSUPPORTED, "sparse_decode: at most 256 sequences");
   if (seqs->batch == 0) return ok();
   if (!indices || !q || !out)
     return fail(KVD_ERR_NULL, "sparse_decode: indices, q and out required");
@@ -628,9 +596,7 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.scale_log2 = log2_scale(scale, cache->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = launched(kvd::launch_decode_sparse(p, s), "sparse_decode");
-  if (st != KVD_OK) return st;
-  return run_merge(pl, seqs, n_h, p.dv, p.ws_o, p.ws_lse, out, lse, false, s);
+  return launched(kvd::launch_decode_sparse(p, s), "sparse_decode");
 }
 
 kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,

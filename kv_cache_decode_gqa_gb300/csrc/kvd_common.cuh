@@ -244,53 +244,6 @@ __device__ __forceinline__ float f16hi(uint32_t u) {
   return f16_to_f32(static_cast<uint16_t>(u >> 16));
 }
 
-// ---------------------------------------------------------------------------
-// split-K merge by the last CTA to finish a (sequence, kv head) group
-// ---------------------------------------------------------------------------
-// Called by every CTA of a split launch after it wrote its partial output
-// ws_o[bh][split][dv] and natural-log lse ws_lse[bh][split] for the heads
-// h0 .. h0 + n_heads - 1 of group `grp` of sequence b. The CTA that arrives
-// last on the group's counter (n_valid arrivals) merges the partials:
-//   out = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M),  M = max_s lse_s,
-//   lse = M + ln sum_s e^(lse_s - M),
-// then resets the counter to zero for the next call. Nothing waits: the
-// other CTAs simply exit.
-__device__ __forceinline__ void merge_if_last(const DecodeParams &p, int b,
-                                              int grp, int n_heads, int dv,
-                                              int n_valid) {
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int *ctr = p.counters + (long)b * p.n_groups + grp;
-    const int prev = atomicAdd(ctr, 1);
-    s_last = prev == n_valid - 1;
-    if (s_last) atomicExch(ctr, 0);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int h0 = grp * n_heads;
-  for (int idx = threadIdx.x; idx < n_heads * dv; idx += blockDim.x) {
-    const int h = idx / dv, d = idx % dv;
-    const long bh = (long)b * p.n_h + h0 + h;
-    const float *lse_s = p.ws_lse + bh * p.n_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < n_valid; ++s) M = fmaxf(M, __ldcg(lse_s + s));
-    float W = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < n_valid; ++s) {
-        const float ls = __ldcg(lse_s + s);
-        const float w = ls == -INFINITY ? 0.f : expf(ls - M);
-        W += w;
-        acc = fmaf(w, __ldcg(p.ws_o + (bh * p.n_splits + s) * dv + d), acc);
-      }
-    }
-    p.out[bh * dv + d] = f2bf(W > 0.f ? acc / W : 0.f);
-    if (d == 0 && p.lse) p.lse[bh] = W > 0.f ? M + logf(W) : -INFINITY;
-  }
-}
-
 // Opt a kernel into `bytes` of dynamic shared memory, once per device (the
 // attribute call stays out of stream capture after the first launch). Each
 // kernel passes its own `done` table (one flag per device ordinal).

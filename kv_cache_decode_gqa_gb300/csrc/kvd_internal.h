@@ -59,15 +59,6 @@ struct DecodeParams {
   int *err;
 };
 
-struct MergeParams {
-  const float *ws_o;
-  const float *ws_lse;
-  const int32_t *seq_lens;  // null: every split is potentially non-empty
-  uint16_t *out;
-  float *lse;
-  int32_t batch, n_h, dv, n_splits, split_len, max_seq_len, n_idx;
-};
-
 struct IndexerParams {
   const uint8_t *cache;  // indexer key cache [num_blocks][1][block_size][64]
   const int32_t *block_table;
@@ -92,7 +83,6 @@ cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
 cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s);
 // Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64).
 cudaError_t launch_decode_sparse(const DecodeParams &p, cudaStream_t s);
-cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);
 

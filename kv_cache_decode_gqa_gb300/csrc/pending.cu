@@ -3,12 +3,6 @@
 #include "kvd_internal.h"
 
 namespace kvd {
-cudaError_t launch_decode_mla(const DecodeParams &, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-cudaError_t launch_decode_sparse(const DecodeParams &, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 cudaError_t launch_indexer_scores(const IndexerParams &, cudaStream_t) {
   return cudaErrorNotSupported;
 }

@@ -17,21 +17,33 @@ namespace kvd {
 
 constexpr int kMaxDecodeBatch = 1024;
 
-struct WorkPartition {
-  int total;                     // chunks in the launch
-  int pre[kMaxDecodeBatch + 1];  // first chunk of sequence b's first unit
-  int nch[kMaxDecodeBatch];      // chunks per unit of sequence b
-  int len[kMaxDecodeBatch];      // visible length of sequence b (clamped)
+// Chunk list of one launch: `units` units per sequence (kv heads, or query
+// head tiles) of nch[b] chunks each.
+template <int NB>
+struct WorkPartitionT {
+  int total;        // chunks in the launch
+  int units;        // units per sequence
+  int pre[NB + 1];  // first chunk of sequence b's first unit
+  int nch[NB];      // chunks per unit of sequence b
+  int len[NB];      // visible length of sequence b (clamped)
 };
+using WorkPartition = WorkPartitionT<kMaxDecodeBatch>;
 
-// Fill `wp` (shared memory) from the device sequence lengths. Every thread
-// of the block calls it (blockDim.x a multiple of 32); it ends with a
-// barrier.
-__device__ __forceinline__ void build_partition(WorkPartition &wp,
+// Fill `wp` (shared memory) from the device sequence lengths. Sequence b
+// has `units` units of ceil(rows_b / chunk) chunks, rows_b = its visible
+// length, or `fixed_rows` (a position list's length) when that is > 0 and
+// the sequence is not empty. Every thread of the block calls it (blockDim.x
+// a multiple of 32); it ends with a barrier.
+template <int NB>
+__device__ __forceinline__ void build_partition(WorkPartitionT<NB> &wp,
                                                 const DecodeParams &p,
-                                                int *len_error) {
+                                                int *len_error,
+                                                int chunk = kStageRows,
+                                                int units = -1,
+                                                int fixed_rows = 0) {
   const int nthreads = blockDim.x;
   const int tid = threadIdx.x;
+  if (units < 0) units = p.n_kv;
   for (int b = tid; b < p.batch; b += nthreads) {
     int T = p.seq_lens[b];
     if (T > p.max_seq_len) {
@@ -40,8 +52,10 @@ __device__ __forceinline__ void build_partition(WorkPartition &wp,
     }
     T = max(T, 0);
     wp.len[b] = T;
-    wp.nch[b] = (T + kStageRows - 1) / kStageRows;
+    const int rows = (fixed_rows > 0 && T > 0) ? fixed_rows : T;
+    wp.nch[b] = (rows + chunk - 1) / chunk;
   }
+  if (tid == 0) wp.units = units;
   __syncthreads();
   // exclusive scan over b of the chunks of sequence b's n_kv units: each
   // thread sums a run of consecutive sequences, then warp and block scans
@@ -51,7 +65,7 @@ __device__ __forceinline__ void build_partition(WorkPartition &wp,
   const int b0 = tid * per;
   int local = 0;
   for (int j = 0; j < per; ++j)
-    if (b0 + j < p.batch) local += wp.nch[b0 + j] * p.n_kv;
+    if (b0 + j < p.batch) local += wp.nch[b0 + j] * units;
   int x = local;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -74,7 +88,7 @@ __device__ __forceinline__ void build_partition(WorkPartition &wp,
   for (int j = 0; j < per; ++j) {
     if (b0 + j < p.batch) {
       wp.pre[b0 + j] = excl;
-      excl += wp.nch[b0 + j] * p.n_kv;
+      excl += wp.nch[b0 + j] * units;
     }
   }
   if (tid == 0) {
@@ -86,8 +100,9 @@ __device__ __forceinline__ void build_partition(WorkPartition &wp,
 
 // Sequence owning global chunk x (0 <= x < total): the largest b with
 // pre[b] <= x (sequences without chunks share the next one's prefix).
-__device__ __forceinline__ int find_seq(const WorkPartition &wp, int batch,
-                                        int x) {
+template <int NB>
+__device__ __forceinline__ int find_seq(const WorkPartitionT<NB> &wp,
+                                        int batch, int x) {
   int lo = 0, hi = batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -112,7 +127,8 @@ struct ChunkCursor {
   int b, h, k;  // sequence, kv head, chunk within the unit
 };
 
-__device__ __forceinline__ ChunkCursor cursor_at(const WorkPartition &wp,
+template <int NB>
+__device__ __forceinline__ ChunkCursor cursor_at(const WorkPartitionT<NB> &wp,
                                                  int batch, int x) {
   ChunkCursor cur;
   cur.b = find_seq(wp, batch, x);
@@ -122,7 +138,8 @@ __device__ __forceinline__ ChunkCursor cursor_at(const WorkPartition &wp,
   return cur;
 }
 
-__device__ __forceinline__ void cursor_next(const WorkPartition &wp,
+template <int NB>
+__device__ __forceinline__ void cursor_next(const WorkPartitionT<NB> &wp,
                                             int batch, int n_kv,
                                             ChunkCursor &cur) {
   if (++cur.k < wp.nch[cur.b]) return;
@@ -157,9 +174,9 @@ __device__ __forceinline__ int arrive_release(int *ctr) {
 // lse = M + ln sum e^(lse_s - M). Thread `t` of `nt` cooperating threads (named barrier `bar`);
 // `scratch` holds the weights (one float per part). Every load of a pass is
 // independent, so a pass costs about one L2 round trip.
-template <int D, int G>
+template <int D, int G, int NB>
 __device__ __forceinline__ void merge_owed(const DecodeParams &p,
-                                           const WorkPartition &wp,
+                                           const WorkPartitionT<NB> &wp,
                                            const int *merge, float *scratch,
                                            int cap, int total, int P, int t,
                                            int nt, int bar) {
@@ -171,6 +188,7 @@ __device__ __forceinline__ void merge_owed(const DecodeParams &p,
     const int uend = ustart + wp.nch[b];
     const int c_first = cta_of(ustart, total, P);
     const int parts = cta_of(uend - 1, total, P) - c_first + 1;
+    const long bh0 = (long)b * p.n_h + (long)h * G;  // first head of the unit
     __threadfence();
     // pass 1: lse of every part (part i of CTA c_first + i; the first CTA's
     // partial for this unit is its side-1 slot, the others' their side 0),
@@ -198,7 +216,7 @@ __device__ __forceinline__ void merge_owed(const DecodeParams &p,
         W += w;
         acc = fmaf(w, __ldcg(p.ws_o + ((long)ws * G + g) * D + d), acc);
       }
-      const long bh = (long)b * p.n_h + h * G + g;
+      const long bh = bh0 + g;
       p.out[bh * D + d] = f2bf(acc / W);
       if (d == 0 && p.lse) p.lse[bh] = M + logf(W);
     }
