@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-LIB_SOURCES = ["api.cu", "append.cu", "decode_simt.cu",
-               "pending.cu", "noalloc.cu", "decode_mma.cu", "decode_wide.cu"]
+LIB_SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "noalloc.cu",
+               "decode_mma.cu", "decode_wide.cu", "indexer.cu"]
 INPUTS_SOURCES = ["inputs_fill.cu"]
 LIB = os.path.join(PKG, "libkvd.so")
 INPUTS_LIB = os.path.join(PKG, "libkvd_inputs.so")

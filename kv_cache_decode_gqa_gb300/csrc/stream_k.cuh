@@ -170,16 +170,21 @@ __device__ __forceinline__ int arrive_release(int *ctr) {
 }
 
 // Merge the partials of every unit in `merge` (unit start chunks, -1 for
-// none): out = sum_s w_s o_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
-// lse = M + ln sum e^(lse_s - M). Thread `t` of `nt` cooperating threads (named barrier `bar`);
-// `scratch` holds the weights (one float per part). Every load of a pass is
-// independent, so a pass costs about one L2 round trip.
+// none): out = sum_s w_s o_s with w_s = e^(lse_s - M) / sum_s e^(lse_s - M),
+// M = max_s lse_s, and lse = M + ln sum_s e^(lse_s - M). Thread `t` of `nt`
+// cooperating threads (named barrier `bar`). `scratch` (cap floats) first
+// holds the parts' lse values, then their weights e^(lse_s - M); the partial
+// outputs are then summed part by part with batches of independent 16-byte
+// loads, so a part costs about one L2 round trip. Part i is the partial of
+// CTA c_first + i: side 1 of the first covering CTA, side 0 of the others.
 template <int D, int G, int NB>
 __device__ __forceinline__ void merge_owed(const DecodeParams &p,
                                            const WorkPartitionT<NB> &wp,
                                            const int *merge, float *scratch,
                                            int cap, int total, int P, int t,
                                            int nt, int bar) {
+  static_assert(D % 4 == 0, "vector loads");
+  float *mg = scratch + cap - 2 * G;  // per-head M and 1 / W
   for (int j = 0; j < 2; ++j) {
     const int ustart = merge[j];
     if (ustart < 0) continue;
@@ -189,36 +194,77 @@ __device__ __forceinline__ void merge_owed(const DecodeParams &p,
     const int c_first = cta_of(ustart, total, P);
     const int parts = cta_of(uend - 1, total, P) - c_first + 1;
     const long bh0 = (long)b * p.n_h + (long)h * G;  // first head of the unit
+    const bool staged = parts * G <= cap - 2 * G;
+    auto slot = [&](int i) { return (c_first + i) * 2 + (i == 0 ? 1 : 0); };
     __threadfence();
-    // pass 1: lse of every part (part i of CTA c_first + i; the first CTA's
-    // partial for this unit is its side-1 slot, the others' their side 0),
-    // kept in shared memory when they fit
-    const bool staged = parts * G <= cap;
-    for (int i = t; staged && i < parts * G; i += nt) {
-      const int part = i / G, g = i % G;
-      const int ws = (c_first + part) * 2 + (part == 0 ? 1 : 0);
-      scratch[i] = __ldcg(p.ws_lse + (long)ws * G + g);
+    if (staged)
+      for (int i = t; i < parts * G; i += nt)
+        scratch[i] = __ldcg(p.ws_lse + (long)slot(i / G) * G + i % G);
+    named_sync(bar, nt);
+    for (int g = t; g < G; g += nt) {
+      float M = -INFINITY;
+      for (int i = 0; i < parts; ++i)
+        M = fmaxf(M, staged ? scratch[i * G + g]
+                            : __ldcg(p.ws_lse + (long)slot(i) * G + g));
+      float W = 0.f;
+      for (int i = 0; i < parts; ++i) {
+        const float l = staged ? scratch[i * G + g]
+                               : __ldcg(p.ws_lse + (long)slot(i) * G + g);
+        const float w = M == -INFINITY ? 0.f : expf(l - M);
+        if (staged) scratch[i * G + g] = w;
+        W += w;
+      }
+      mg[g] = M;
+      mg[G + g] = W > 0.f ? 1.f / W : 0.f;
+      if (p.lse) p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
     }
     named_sync(bar, nt);
-    for (int idx = t; idx < G * D; idx += nt) {
-      const int g = idx / D, d = idx % D;
-      auto lse_of = [&](int i) {
-        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
-        return staged ? scratch[i * G + g] : __ldcg(p.ws_lse + (long)ws * G + g);
-      };
-      float M = -INFINITY;
-      for (int i = 0; i < parts; ++i) M = fmaxf(M, lse_of(i));
-      float W = 0.f, acc = 0.f;
-      // pass 2: the partial outputs
+    constexpr int kBatch = 8;  // float4 loads in flight per thread
+    const int n4 = G * D / 4;
+    for (int e0 = t; e0 < n4; e0 += nt * kBatch) {
+      float4 acc[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = 0; i < parts; ++i) {
-        const int ws = (c_first + i) * 2 + (i == 0 ? 1 : 0);
-        const float w = expf(lse_of(i) - M);
-        W += w;
-        acc = fmaf(w, __ldcg(p.ws_o + ((long)ws * G + g) * D + d), acc);
+        const float4 *src =
+            reinterpret_cast<const float4 *>(p.ws_o + (long)slot(i) * G * D);
+        float4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + u * nt;
+          v[u] = e < n4 ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + u * nt;
+          if (e >= n4) continue;
+          const int g = (4 * e) / D;
+          float w;
+          if (staged) {
+            w = scratch[i * G + g];
+          } else {
+            const float M = mg[g];
+            w = M == -INFINITY
+                    ? 0.f
+                    : expf(__ldcg(p.ws_lse + (long)slot(i) * G + g) - M);
+          }
+          acc[u].x = fmaf(w, v[u].x, acc[u].x);
+          acc[u].y = fmaf(w, v[u].y, acc[u].y);
+          acc[u].z = fmaf(w, v[u].z, acc[u].z);
+          acc[u].w = fmaf(w, v[u].w, acc[u].w);
+        }
       }
-      const long bh = bh0 + g;
-      p.out[bh * D + d] = f2bf(acc / W);
-      if (d == 0 && p.lse) p.lse[bh] = M + logf(W);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * nt;
+        if (e >= n4) continue;
+        const int g = (4 * e) / D;
+        const float iw = mg[G + g];
+        uint2 packed;
+        packed.x = pack_bf16x2(acc[u].x * iw, acc[u].y * iw);
+        packed.y = pack_bf16x2(acc[u].z * iw, acc[u].w * iw);
+        *reinterpret_cast<uint2 *>(p.out + bh0 * D + 4 * e) = packed;
+      }
     }
     named_sync(bar, nt);
   }

@@ -1,0 +1,187 @@
+"""GPU parity of the indexer scores, the top-k selection and the static
+Full / Reuse / Reindex schedule, through the C ABI.
+
+Top-k indices are checked bit-exactly in two ways: (i) the oracle's
+selection rule applied to the scores the GPU computed must give exactly
+the GPU's indices (every shape, full size included); (ii) on an
+exact-arithmetic input set (indexer queries and keys in {a/8}, weights in
+{1,2,3,4}) every fp32 score is exact, so the GPU's indices must equal the
+fp64 oracle's, heavy ties included."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import kv_cache_decode_gqa_gb300 as K  # noqa: E402
+from kv_cache_decode_gqa_gb300 import inputs as I  # noqa: E402
+from kv_cache_decode_gqa_gb300 import schedule as S  # noqa: E402
+from kv_cache_decode_gqa_gb300 import workloads as W  # noqa: E402
+from tests import gpu_helpers as H  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    K.device_error()
+    yield
+    assert K.device_error() == 0
+
+
+def _shape(lengths, k, bs=64, heads=4, modes=("full",)):
+    return W.config("sparse", batch=len(lengths), lengths=list(lengths),
+                    topk=k, block_size=bs, idx_heads=heads,
+                    n_layers=len(modes), modes=list(modes))
+
+
+def _exact_inputs(wl, s, layer_keys):
+    """Replace the indexer cache, queries and weights by the exact set."""
+    tab = I.eighths_bf16_table()
+    I.device_fill(wl.idx_cache.k, tab, W._key(s, 0, W.T_IDXK))
+    for layer in layer_keys:
+        q = I.host_tensor(tab, W._key(s, layer, W.T_QIDX),
+                          (s.batch, s.idx_heads, s.idx_dim))
+        wl.q_idx[layer] = torch.from_numpy(q.view(np.int16)).view(
+            torch.bfloat16).cuda()
+        wi = I.uniform_int(W._key(s, layer, W.T_W), s.batch * s.idx_heads, 1, 4)
+        wl.w[layer] = torch.from_numpy(
+            wi.reshape(s.batch, s.idx_heads).astype(np.float32)).cuda()
+    return tab
+
+
+def _host_idx_cache(s, pg, table):
+    return W.host_cache_full(s, pg, 0, W.T_IDXK, width=s.idx_dim, n_kv=1,
+                             table=table)
+
+
+def _run_indexer(wl, layer, scores=True):
+    s = wl.shape
+    sc = torch.empty((s.batch, max(wl.max_seq_len, 1)), dtype=torch.float32,
+                     device="cuda") if scores else None
+    idx, sc = K.indexer_topk(wl.idx_cache, wl.block_table, wl.seq_lens,
+                             wl.max_seq_len, wl.q_idx[layer], wl.w[layer],
+                             s.topk, scores=sc)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), None if sc is None else sc.cpu().numpy()
+
+
+CASES = [
+    # cached lengths, k, block size, indexer heads
+    ([5, 63, 64, 200], 64, 64, 4),       # T < k, T == k, T > k
+    ([1000, 4000], 256, 16, 4),
+    ([3000], 2048, 64, 8),
+    ([700, 1500], 100, 32, 1),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=["small", "bs16", "k2048",
+                                             "one_head"])
+def test_scores_and_selection(case):
+    lengths, k, bs, heads = case
+    s = _shape(lengths, k, bs, heads)
+    wl = W.DeviceWorkload(s)
+    idx, sc = _run_indexer(wl, 0)
+    # scores vs the fp64 oracle
+    tab = I.normal_bf16_table()
+    ir = _host_idx_cache(s, wl.paging, tab)
+    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, 0, W.T_QIDX,
+                                             (s.batch, heads, s.idx_dim)))
+    w = W.host_weights(s, 0).astype(np.float64)
+    ref = oracle.indexer_scores(qI, w, ir, wl.paging.table, s.seq_lens, bs)
+    for b, T in enumerate(s.seq_lens):
+        np.testing.assert_allclose(sc[b, :T], ref[b], rtol=1e-5, atol=1e-4)
+        # (i) the selection the GPU's own scores define, exactly
+        want = oracle.topk_select(sc[b, :T].astype(np.float64), k)
+        assert np.array_equal(idx[b], want), f"row {b}"
+
+
+def test_exact_arithmetic_set_matches_fp64_oracle():
+    s = _shape([5000, 2000, 64], 512, 64, 4)
+    wl = W.DeviceWorkload(s)
+    tab = _exact_inputs(wl, s, [0])
+    idx, sc = _run_indexer(wl, 0)
+    ir = _host_idx_cache(s, wl.paging, tab)
+    qI = oracle.bf16_bits_to_f64(I.host_tensor(tab, W._key(s, 0, W.T_QIDX),
+                                               (s.batch, 4, 64)))
+    w = wl.w[0].cpu().numpy().astype(np.float64)
+    ref_idx, ref_sc = oracle.indexer_topk(qI, w, ir, wl.paging.table,
+                                          s.seq_lens, 64, 512)
+    for b, T in enumerate(s.seq_lens):
+        assert np.array_equal(sc[b, :T].astype(np.float64), ref_sc[b])
+    assert np.array_equal(idx, ref_idx)
+    # the set really has ties at the selection boundary
+    b0 = ref_sc[0]
+    kth = np.sort(b0)[-512]
+    assert (b0 == kth).sum() > 1
+
+
+def test_full_size_indexer():
+    s = W.config("sparse")
+    wl = W.DeviceWorkload(s, layers=[0])
+    idx, sc = _run_indexer(wl, 0)
+    T = s.seq_lens[0]
+    for b in range(s.batch):
+        want = oracle.topk_select(sc[b, :T].astype(np.float64), s.topk)
+        assert np.array_equal(idx[b], want), f"row {b}"
+    # sampled sequence: scores against the fp64 oracle
+    b = 3
+    ir, bt = W.host_cache_compact(s, wl.paging, 0, W.T_IDXK, [b],
+                                  width=s.idx_dim, n_kv=1,
+                                  table=I.normal_bf16_table())
+    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, 0, W.T_QIDX,
+                                             (s.batch, 4, 64)))[[b]]
+    w = W.host_weights(s, 0)[[b]].astype(np.float64)
+    ref = oracle.indexer_scores(qI, w, ir, bt, [T], s.block_size)[0]
+    np.testing.assert_allclose(sc[b, :T], ref, rtol=1e-5, atol=1e-4)
+
+
+def test_schedule_matches_oracle():
+    """Full, Reuse x3, Reindex x4 over one main cache and one indexer
+    cache (exact indexer inputs, so the selections are identical)."""
+    modes = W.SPARSE_MODES
+    s = _shape([3000, 900], 128, 64, 4, modes)
+    wl = W.DeviceWorkload(s)
+    tab = _exact_inputs(wl, s, [l for l, m in enumerate(modes)
+                                if m != "reuse"])
+    outs = [torch.empty((s.batch, s.n_h, 512), dtype=torch.bfloat16,
+                        device="cuda") for _ in modes]
+    lses = [torch.empty((s.batch, s.n_h), dtype=torch.float32, device="cuda")
+            for _ in modes]
+    idxs = [torch.empty((s.batch, s.topk), dtype=torch.int32, device="cuda")
+            for _ in modes]
+    used = S.sparse_schedule_step(
+        modes, wl.caches[0], wl.idx_cache, wl.block_table, wl.pos,
+        wl.seq_lens, wl.max_seq_len, [wl.q[l] for l in range(len(modes))],
+        wl.q_idx, wl.w, s.topk, outs, idxs, k_new=wl.k_new[0],
+        v_new=wl.v_new[0], idx_k_new=wl.idx_k_new, lses=lses)
+    torch.cuda.synchronize()
+    # oracle: append the new token to the three caches, then the schedule
+    pg = wl.paging
+    kr = W.host_cache_full(s, pg, 0, W.T_K, n_kv=1)
+    vr = W.host_cache_full(s, pg, 0, W.T_V, n_kv=1)
+    ir = _host_idx_cache(s, pg, tab)
+    kn = W.host_bf16(s, 0, W.T_KNEW, (s.batch, 1, 512))
+    vn = W.host_bf16(s, 0, W.T_VNEW, (s.batch, 1, 512))
+    xn = W.host_bf16(s, 0, W.T_IDXKNEW, (s.batch, 1, 64))
+    kr = oracle.kv_append(kr, pg.table, s.lengths, kn, s.block_size)
+    vr = oracle.kv_append(vr, pg.table, s.lengths, vn, s.block_size)
+    ir = oracle.kv_append(ir, pg.table, s.lengths, xn, s.block_size)
+    qs = [oracle.bf16_bits_to_f64(W.host_bf16(s, l, W.T_Q,
+                                              (s.batch, s.n_h, 512)))
+          for l in range(len(modes))]
+    qIs = [None if m == "reuse" else oracle.bf16_bits_to_f64(
+        I.host_tensor(tab, W._key(s, l, W.T_QIDX), (s.batch, 4, 64)))
+        for l, m in enumerate(modes)]
+    ws = [None if m == "reuse" else wl.w[l].cpu().numpy().astype(np.float64)
+          for l, m in enumerate(modes)]
+    r_out, r_lse, r_idx = oracle.sparse_schedule(
+        modes, qs, qIs, ws, kr, vr, ir, pg.table, s.seq_lens, s.block_size,
+        s.topk)
+    for l in range(len(modes)):
+        assert np.array_equal(used[l].cpu().numpy(), r_idx[l]), f"layer {l}"
+        H.assert_close(H.to_np_bf16(outs[l]), r_out[l], f"layer {l}")
+        H.assert_lse_close(lses[l].cpu().numpy(), r_lse[l], f"layer {l}")
