@@ -588,7 +588,8 @@ def profile_run(args, local):
     import kv_cache_decode_gqa_gb300 as K
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    s = W.config(args.config)
+    s = W.config(args.config, **({"n_layers": args.layers}
+                                 if args.layers else {}))
     wl = W.DeviceWorkload(s, device=dev)
     outs = {l: torch.empty((s.batch, s.n_h, s.dv), dtype=torch.bfloat16,
                            device=dev) for l in wl.layers}
@@ -607,11 +608,11 @@ def profile_run(args, local):
 
 def launches(s):
     """Kernels the library launches per step (append + decode per layer;
-    sparse: appends, indexer score + select per Full/Reindex layer, gather
-    decode + merge per layer)."""
+    sparse: two appends, indexer score + select per Full/Reindex layer, one
+    gather decode per layer; split merges run inside the decode kernels)."""
     if s.kind == "sparse":
         sel = sum(1 for m in s.modes if m != "reuse")
-        return 2 + 2 * sel + 2 * s.n_layers
+        return 2 + 2 * sel + s.n_layers
     return 2 * s.n_layers
 
 
@@ -712,6 +713,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile-run", action="store_true",
                     help="only run warmup + steps eager steps (for ncu)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="with --profile-run: keep only this many layers of "
+                         "the workload (same per-layer shape), so a profiler "
+                         "capture holds a few GB")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
