@@ -24,6 +24,7 @@ across GPUs here), one process per GPU under torchrun, no collective on the
 data path; the step time is the max over ranks.
 """
 import argparse
+import hashlib
 import json
 import math
 import multiprocessing as mp
@@ -88,18 +89,35 @@ def measured_peaks():
 
 
 def profile_traffic(kernel_tag):
-    """dram bytes per launch recorded from an ncu capture of the current
-    kernel, if profiles/ holds one (a line 'traffic_bytes_per_launch: N')."""
+    """DRAM bytes per launch from an ncu capture of this kernel, if profiles/
+    holds one ('traffic_bytes_per_launch: N') and the kernel's sources are
+    unchanged since the capture (the file's 'kernel_sources_sha256:' matches
+    a hash of the listed sources); otherwise None."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
+    fields = {}
     try:
         with open(path) as f:
             for line in f:
-                if line.startswith("traffic_bytes_per_launch:"):
-                    v = line.split(":", 1)[1].strip()
-                    return None if v in ("", "null") else float(v)
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
     except OSError:
-        pass
-    return None
+        return None
+    v = fields.get("traffic_bytes_per_launch", "null")
+    srcs = fields.get("kernel_sources", "").split()
+    if v in ("", "null") or not srcs:
+        return None
+    h = hashlib.sha256()
+    try:
+        for name in srcs:
+            with open(os.path.join(ROOT, "kv_cache_decode_gqa_gb300", "csrc",
+                                   name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    if h.hexdigest()[:16] != fields.get("kernel_sources_sha256"):
+        return None  # the kernel changed after the counters were taken
+    return float(v)
 
 
 # ---------------------------------------------------------------------------
