@@ -132,21 +132,10 @@ struct Plan {
   size_t ws_o_bytes = 0;   // partial outputs
   size_t ws_lse_bytes = 0; // partial log-sum-exps
   size_t ws_bytes = 0;     // + arrival counters
+  int hp = 1;              // kv heads per work unit (CUDA-core GQA kernel)
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Workspace of a split launch: partial outputs, partial lse, then one
-// arrival counter per (sequence, head group), each region 256-byte aligned.
-void finish_plan(Plan &pl, int batch, int n_h, int dv, int n_groups) {
-  pl.n_groups = n_groups;
-  if (pl.n_splits > 1) {
-    pl.ws_o_bytes = round_up((size_t)batch * n_h * pl.n_splits * dv * 4, 256);
-    pl.ws_lse_bytes = round_up((size_t)batch * n_h * pl.n_splits * 4, 256);
-    pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
-                  round_up((size_t)batch * n_groups * 4, 256);
-  }
-}
 
 enum class DenseKernel { Simt, Mma };
 
@@ -192,9 +181,15 @@ Plan plan_stream_k(int sms, int ctas_per_sm, int batch, int n_kv, int g,
 
 Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
               DenseKernel kind) {
-  (void)kind;
-  return plan_stream_k(sms, 1, s->batch, c->n_kv, n_h / c->n_kv, c->head_dim,
-                       s->max_seq_len);
+  const int g = n_h / c->n_kv;
+  const int hp = kind == DenseKernel::Simt
+                     ? kvd::simt_heads_per_stage(c->n_kv, g, c->head_dim,
+                                                 c->dtype, c->block_size)
+                     : 1;
+  Plan pl = plan_stream_k(sms, 1, s->batch, c->n_kv / hp, g * hp,
+                          c->head_dim, s->max_seq_len);
+  pl.hp = hp;
+  return pl;
 }
 
 // Persistent stream-K plan of the 64-head-tile kernels (latent and sparse
@@ -204,11 +199,13 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
 Plan plan_wide(int sms, int batch, int n_h, int rows, int dv) {
   Plan pl;
   const int tiles = n_h / 64;
-  const long chunks = (long)batch * tiles * ((rows + 31) / 32);
+  // lanes of `tiles` CTAs each (one per head tile) share a chunk range
+  const long chunks = (long)batch * ((rows + 31) / 32);
   long ctas = sms;
   const int forced = env_int("KVD_DECODE_CTAS", 0);
   if (forced > 0) ctas = forced;
-  ctas = std::max(1L, std::min(ctas, std::max(chunks, 1L)));
+  const long lanes = std::max(1L, std::min(ctas / tiles, std::max(chunks, 1L)));
+  ctas = lanes * tiles;
   pl.n_splits = (int)ctas;
   pl.n_groups = tiles;
   pl.ws_o_bytes = round_up((size_t)ctas * 2 * 64 * dv * 4, 256);
@@ -472,6 +469,7 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.max_seq_len = seqs->max_seq_len;
   p.split_len = pl.split_len;
   p.n_splits = pl.n_splits;
+  p.hp = pl.hp;
   p.scale_log2 = log2_scale(scale, cache->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -20,6 +20,8 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f32(float first, float second) {
 }
 
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int chunks = p.head_dim / 8;
   const long per_tensor = (long)p.batch * p.n_kv * chunks;
   const long total = p.v_cache ? 2 * per_tensor : per_tensor;
@@ -74,8 +76,8 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const long blocks = (total + threads - 1) / threads;
-  append_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(threads), 0, s,
+                    1, p);
 }
 
 }  // namespace kvd

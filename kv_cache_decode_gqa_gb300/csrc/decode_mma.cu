@@ -43,7 +43,6 @@ constexpr int kConsumers = kWarps * 32;
 constexpr int kProducer = kWarps;
 constexpr int kFinisher = kWarps + 1;
 constexpr int kThreads = kConsumers + 64;
-constexpr int kEndBar = 1;
 
 struct MmaParams {
   DecodeParams p;
@@ -106,11 +105,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sfull = empty + C::NS;
   uint64_t *sempty = sfull + 2;
   __shared__ int s_len_err;
-  __shared__ int s_merge[2];
   __shared__ volatile int s_abort, s_issued, s_producer_done;
 
   const int G = p.n_h / p.n_kv;  // 8 or 16 (checked by the launcher)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
   const int qr = lane >> 2, qc = lane & 3;  // MMA fragment row / column quad
 
   if (tid == 0) {
@@ -118,7 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     s_issued = 0;
     s_producer_done = 0;
-    s_merge[0] = s_merge[1] = -1;
   }
   __syncthreads();
   build_partition(wp, p, &s_len_err);
@@ -235,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ======================= finisher warp ==================================
   if (warp == kFinisher) {
-    int pend_prev[2] = {-1, -1}, pend_start[2] = {0, 0}, n_pend = 0;
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {
@@ -279,41 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (d == 0) p.ws_lse[(long)wslot * G + g] = lse_nat;
         }
       }
-      if (!whole) __threadfence();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sempty[sl]);
-        if (!whole) {
-          pend_prev[n_pend] = arrive_release(p.counters + (long)b * p.n_kv + h);
-          pend_start[n_pend] = ustart;
-          ++n_pend;
-        }
-      }
+      if (lane == 0) mbar_arrive(&sempty[sl]);
       x = xend;
       if (x < hi) fc = cursor_at(wp, p.batch, x);
     }
-    if (lane == 0) {
-      for (int j = 0; j < n_pend; ++j) {
-        const int ustart = pend_start[j];
-        const int bb = find_seq(wp, p.batch, ustart);
-        const int hh = (ustart - wp.pre[bb]) / wp.nch[bb];
-        const int uend = ustart + wp.nch[bb];
-        const int parts =
-            cta_of(uend - 1, total, P) - cta_of(ustart, total, P) + 1;
-        if (pend_prev[j] == parts - 1) {
-          s_merge[j] = ustart;
-          atomicExch(p.counters + (long)bb * p.n_kv + hh, 0);
-        }
-      }
-    }
-    __threadfence();
-    named_sync(kEndBar, kConsumers + 32);
-    if (G == 16)
-      merge_owed<kD, 16>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, lane,
-                         32 + kConsumers, kEndBar);
-    else
-      merge_owed<kD, 8>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, lane,
-                        32 + kConsumers, kEndBar);
     return;
   }
 
@@ -549,13 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     cursor_next(wp, p.batch, p.n_kv, cc);
   }
   if (cur_b >= 0) flush();
-  named_sync(kEndBar, kConsumers + 32);
-  if (G == 16)
-    merge_owed<kD, 16>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, 32 + tid,
-                       32 + kConsumers, kEndBar);
-  else
-    merge_owed<kD, 8>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, 32 + tid,
-                      32 + kConsumers, kEndBar);
 
   if (s_abort && tid == 0) {
     for (int t = 0; t < (1 << 20) && !s_producer_done; ++t) __nanosleep(1000);
@@ -611,8 +572,11 @@ cudaError_t launch_t(const MmaParams &mp, cudaStream_t s) {
   static bool done[64] = {};
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
-  kern<<<mp.p.n_splits, kThreads, C::SMEM, s>>>(mp);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(mp.p.n_splits), dim3(kThreads), C::SMEM, s, 1, mp);
+  if (e != cudaSuccess) return e;
+  const int g = mp.p.n_h / mp.p.n_kv;
+  return g == 16 ? launch_merge_dense<kD, 16>(mp.p, mp.p.n_kv, s)
+                 : launch_merge_dense<kD, 8>(mp.p, mp.p.n_kv, s);
 }
 
 }  // namespace

@@ -5,10 +5,14 @@
 // HBM bandwidth and its job is to keep every SM's copy engine streaming.
 //
 // Persistent stream-K launch (stream_k.cuh): one CTA per SM, each taking an
-// equal contiguous share of all (sequence, kv head, 64-token chunk) work.
-// A producer warp resolves 32 chunks at a time (cursor and block ids, one
-// chunk per lane, loaded in parallel), then streams each chunk's K and V
-// rows (contiguous within a paged block) into an NS-deep shared-memory ring
+// equal contiguous share of all (sequence, head group, 64-token chunk)
+// work. A head group is HP consecutive kv heads: with 64-token blocks the
+// HP heads' rows of one block are adjacent in the cache layout, so a whole
+// chunk of a group moves as one bulk copy of HP x 64 rows for K and one for
+// V. HP is chosen so that a copy is about 32 KB: the copy engine streams
+// large copies much faster than small ones. A producer warp resolves 32
+// chunks at a time (cursor and block ids, one chunk per lane, loaded in
+// parallel), then streams each chunk into an NS-deep shared-memory ring
 // with bulk asynchronous copies completing on "full" mbarriers; it refills
 // a stage once the consumers release it on its "empty" mbarrier, so it runs
 // up to NS chunks ahead across unit boundaries.
@@ -16,8 +20,9 @@
 // The producer also copies the chunk's query rows into the stage, so a
 // consumer starting a new unit reads its query from shared memory.
 //
-// Eight consumer warps process a chunk: lane group g = lane / 8 of warp w
-// owns rows 8w + 4i + g (i = 0, 1); its 8 lanes each hold D/8 elements of
+// Eight consumer warps process a chunk, 8 / HP warps per head of the group:
+// lane group g = lane / 8 of local warp w owns the head's rows
+// 8 HP w + 4 i + g (i < 2 HP); its 8 lanes each hold D/8 elements of
 // the row, so a row is read from shared memory as one conflict-free sweep,
 // and the dot product finishes with three xor-shuffles. Each lane group
 // keeps its own online-softmax state (running max, sum, output slice) per
@@ -26,11 +31,10 @@
 // producer, so all warps agree on unit changes. At a unit change a warp
 // merges its four lane-group states and drops the result into one of two
 // shared-memory flush slots, then goes on with the next unit at once. A
-// finisher warp combines the eight warp states of each flushed unit and
+// finisher warp combines the warp states of each head of a flushed unit and
 // writes the final output (a unit lying wholly in this CTA's range) or a
-// partial plus a release-ordered arrival on the unit's counter; after the
-// range is done, for every unit on which it arrived last, it merges the
-// partials of all covering CTAs (log-sum-exp merge) and resets the counter.
+// partial, which the merge launch queued after this one combines with the
+// other covering CTAs' partials (log-sum-exp merge).
 #include <cuda_fp16.h>
 
 #include <cmath>
@@ -46,17 +50,20 @@ constexpr int kWarps = kConsumers / 32;
 constexpr int kProducer = kWarps;          // warp index of the producer
 constexpr int kFinisher = kWarps + 1;      // warp index of the finisher
 constexpr int kThreads = kConsumers + 64;
-constexpr int kEndBar = 1;                 // consumers + finisher, at the end
 
-template <int D, int G, int DT>
+template <int D, int G, int DT, int HP>
 struct Cfg {
   static constexpr int ES = DT == DT_BF16 ? 2 : 1;
   static constexpr int ROW = D * ES;                 // bytes per cached row
-  static constexpr int STAGE = kStageRows * ROW;     // K (or V) bytes / chunk
-  static constexpr int NS_RAW = (160 * 1024) / (2 * STAGE);
+  static constexpr int HSTAGE = kStageRows * ROW;    // one head's K (or V)
+  static constexpr int STAGE = HP * HSTAGE;          // K (or V) bytes / chunk
+  static constexpr int RING_BUDGET = HP == 1 ? 160 * 1024 : 192 * 1024;
+  static constexpr int NS_RAW = RING_BUDGET / (2 * STAGE);
   static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW; // ring depth
   static constexpr int E = D / 8;                    // elements per lane
-  static constexpr int QB = G * D * 2;               // query rows / stage
+  static constexpr int WPH = kWarps / HP;            // warps per head
+  static constexpr int ITER = 2 * HP;                // 4-row steps per warp
+  static constexpr int QB = HP * G * D * 2;          // query rows / stage
   static constexpr int RING = 2 * NS * STAGE + NS * QB;
   static constexpr int SLOT = kWarps * G * (D + 2);   // floats per slot
   static constexpr int MERGE = 2 * SLOT * 4;
@@ -119,10 +126,11 @@ __device__ __forceinline__ float weight(float x, float M) {
   return x == -INFINITY ? 0.f : ex2(x - M);
 }
 
-template <int D, int G, int DT>
+template <int D, int G, int DT, int HP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_simt_kernel(const DecodeParams p) {
-  using C = Cfg<D, G, DT>;
+  using C = Cfg<D, G, DT, HP>;
+  constexpr int GU = HP * G;  // query heads per unit
   constexpr int E = C::E;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sk = smem;
@@ -135,21 +143,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sfull = empty + C::NS;  // flush slot written (8 warp arrivals)
   uint64_t *sempty = sfull + 2;     // flush slot consumed (finisher)
   __shared__ int s_len_err;
-  __shared__ int s_merge[2];  // unit starts this CTA must merge, or -1
   __shared__ volatile int s_abort, s_issued, s_producer_done;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
+  pdl_trigger();
+  pdl_wait();
 
   if (tid == 0) {
     s_len_err = 0;
     s_abort = 0;
     s_issued = 0;
     s_producer_done = 0;
-    s_merge[0] = s_merge[1] = -1;
   }
   __syncthreads();
-  build_partition(wp, p, &s_len_err);
+  const int n_units = p.n_kv / HP;  // head groups per sequence
+  build_partition(wp, p, &s_len_err, kStageRows, n_units);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
   const int P = min((int)gridDim.x, max(total, 1));
@@ -226,12 +235,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (s_abort) go = 0;
           if (go) {
             const int tok = k * kStageRows;
-            mbar_arrive_expect_tx(&full[s], 2u * rows * C::ROW + C::QB);
-            bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * G) * D,
+            mbar_arrive_expect_tx(&full[s],
+                                  2u * HP * rows * C::ROW + C::QB);
+            bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * D,
                      C::QB, &full[s]);
             const int32_t *bt = p.block_table + (long)b * p.max_blocks;
             const int lb0 = tok / p.block_size;
-            int done = 0;
+            if constexpr (HP > 1) {
+              // 64-token blocks: the chunk is one block; its HP heads' rows
+              // are adjacent, so a full chunk is one copy per tensor
+              int pb = blk[0];
+              if (pb < 0 || pb >= p.num_blocks) {
+                report(p.err, DEVERR_BLOCK);
+                pb = 0;  // read a valid block; the result is flagged as wrong
+              }
+              const size_t off =
+                  ((size_t)pb * p.n_kv + (size_t)h * HP) * kStageRows * C::ROW;
+              if (rows == kStageRows) {
+                bulk_g2s_hint(sk + s * C::STAGE, p.k + off, C::STAGE,
+                              &full[s], policy);
+                bulk_g2s_hint(sv + s * C::STAGE, p.v + off, C::STAGE,
+                              &full[s], policy);
+              } else {
+#pragma unroll
+                for (int j = 0; j < HP; ++j) {
+                  const size_t oj = off + (size_t)j * C::HSTAGE;
+                  bulk_g2s_hint(sk + s * C::STAGE + j * C::HSTAGE, p.k + oj,
+                                rows * C::ROW, &full[s], policy);
+                  bulk_g2s_hint(sv + s * C::STAGE + j * C::HSTAGE, p.v + oj,
+                                rows * C::ROW, &full[s], policy);
+                }
+              }
+            }
+            int done = HP > 1 ? rows : 0;
             while (done < rows) {
               const int t = tok + done;
               const int slot = t % p.block_size;
@@ -267,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ======================= finisher warp ==================================
   if (warp == kFinisher) {
-    int pend_prev[2] = {-1, -1}, pend_start[2] = {0, 0}, n_pend = 0;
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {
@@ -285,74 +320,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *wl = wm + kWarps * G;
       const float *wo = wl + kWarps * G;  // [warp][G][D]
       const bool whole = ustart >= lo && uend <= hi;
-      const float vs = DT == DT_FP8 ? p.v_scale[h] : 1.0f;
       const int wslot = c * 2 + partial_side(ustart, lo);
-      for (int idx = lane; idx < G * D; idx += 32) {
-        const int g = idx / D, d = idx % D;
+      for (int idx = lane; idx < GU * D; idx += 32) {
+        const int jg = idx / D, d = idx % D;  // head (j, g) of the unit
+        const int j = jg / G, g = jg % G;
+        const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
+        const int w0 = j * C::WPH;  // the head's warps
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + g]);
+        for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, wm[(w0 + w) * G + g]);
         float L = 0.f, acc = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float a = weight(wm[w * G + g], M);
-          L = fmaf(wl[w * G + g], a, L);
-          acc = fmaf(wo[(w * G + g) * D + d], a, acc);
+        for (int w = 0; w < C::WPH; ++w) {
+          const float a = weight(wm[(w0 + w) * G + g], M);
+          L = fmaf(wl[(w0 + w) * G + g], a, L);
+          acc = fmaf(wo[((w0 + w) * G + g) * D + d], a, acc);
         }
         const float res = acc / L * vs;
         const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-        const long bh = (long)b * p.n_h + h * G + g;
+        const long bh = (long)b * p.n_h + h * GU + jg;
         if (whole) {
           p.out[bh * D + d] = f2bf(res);
           if (d == 0 && p.lse) p.lse[bh] = lse_nat;
         } else {
-          p.ws_o[((long)wslot * G + g) * D + d] = res;
-          if (d == 0) p.ws_lse[(long)wslot * G + g] = lse_nat;
+          p.ws_o[((long)wslot * GU + jg) * D + d] = res;
+          if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
         }
       }
-      if (!whole) __threadfence();  // each lane's partial writes first
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sempty[sl]);  // the slot may be reused
-        if (!whole) {
-          pend_prev[n_pend] = arrive_release(p.counters + (long)b * p.n_kv + h);
-          pend_start[n_pend] = ustart;
-          ++n_pend;
-        }
-      }
+      if (lane == 0) mbar_arrive(&sempty[sl]);  // the slot may be reused
       x = xend;
       if (x < hi) fc = cursor_at(wp, p.batch, x);
     }
-    // units on which this CTA arrived last: it merges them (below, with the
-    // consumer warps), after resetting their counters for the next call
-    if (lane == 0) {
-      for (int j = 0; j < n_pend; ++j) {
-        const int ustart = pend_start[j];
-        const int bb = find_seq(wp, p.batch, ustart);
-        const int hh = (ustart - wp.pre[bb]) / wp.nch[bb];
-        const int uend = ustart + wp.nch[bb];
-        const int parts =
-            cta_of(uend - 1, total, P) - cta_of(ustart, total, P) + 1;
-        if (pend_prev[j] == parts - 1) {
-          s_merge[j] = ustart;
-          atomicExch(p.counters + (long)bb * p.n_kv + hh, 0);
-        }
-      }
-    }
-    __threadfence();
-    named_sync(kEndBar, kConsumers + 32);
-    merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, lane,
-                     32 + kConsumers, kEndBar);
     return;
   }
 
   // ======================= consumer warps =================================
   int cur_b = -1, cur_h = -1, n_flush = 0;
   float qf[G][E], m[G], l[G], o[G][E];
+  const int hj = warp / C::WPH;  // this warp's head within the group
+  const int lw = warp % C::WPH;  // and its rank among that head's warps
 
   auto start_unit = [&](int s, int h) {
-    const float qs = p.scale_log2 * (DT == DT_FP8 ? p.k_scale[h] : 1.0f);
-    const uint16_t *qrows = reinterpret_cast<const uint16_t *>(sq + s * C::QB);
+    const float qs =
+        p.scale_log2 * (DT == DT_FP8 ? p.k_scale[h * HP + hj] : 1.0f);
+    const uint16_t *qrows =
+        reinterpret_cast<const uint16_t *>(sq + s * C::QB) + hj * G * D;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
 #pragma unroll
@@ -440,12 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int nvalid = min(kStageRows, wp.len[cc.b] - cc.k * kStageRows);
     if (ok) {
-      const uint8_t *kst = sk + s * C::STAGE;
-      const uint8_t *vst = sv + s * C::STAGE;
-      float sc[2][G];
+      const uint8_t *kst = sk + s * C::STAGE + hj * C::HSTAGE;
+      const uint8_t *vst = sv + s * C::STAGE + hj * C::HSTAGE;
+      float sc[C::ITER][G];
 #pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int r = warp * 8 + i2 * 4 + grp;
+      for (int i2 = 0; i2 < C::ITER; ++i2) {
+        const int r = lw * 4 * C::ITER + i2 * 4 + grp;
         float kx[E];
         load_row<D, DT>(kst + r * C::ROW, sub, kx);
 #pragma unroll
@@ -460,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int r = warp * 8 + i2 * 4 + grp;
+      for (int i2 = 0; i2 < C::ITER; ++i2) {
+        const int r = lw * 4 * C::ITER + i2 * 4 + grp;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float v = sc[i2][g];
@@ -471,22 +484,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc[i2][g] = r < nvalid ? v : -INFINITY;
         }
       }
-      float pr[2][G];
+      float pr[C::ITER][G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float m_new = fmaxf(m[g], fmaxf(sc[0][g], sc[1][g]));
+        float mx = sc[0][g];
+#pragma unroll
+        for (int i2 = 1; i2 < C::ITER; ++i2) mx = fmaxf(mx, sc[i2][g]);
+        const float m_new = fmaxf(m[g], mx);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float corr = ex2(m[g] - m_use);
-        pr[0][g] = ex2(sc[0][g] - m_use);
-        pr[1][g] = ex2(sc[1][g] - m_use);
-        l[g] = l[g] * corr + pr[0][g] + pr[1][g];
+        float lsum = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < C::ITER; ++i2) {
+          pr[i2][g] = ex2(sc[i2][g] - m_use);
+          lsum += pr[i2][g];
+        }
+        l[g] = l[g] * corr + lsum;
         m[g] = m_new;
 #pragma unroll
         for (int e = 0; e < E; ++e) o[g][e] *= corr;
       }
 #pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int r = warp * 8 + i2 * 4 + grp;
+      for (int i2 = 0; i2 < C::ITER; ++i2) {
+        const int r = lw * 4 * C::ITER + i2 * 4 + grp;
         if (r < nvalid) {
           float vx[E];
           load_row<D, DT>(vst + r * C::ROW, sub, vx);
@@ -502,12 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // release the stage to the producer
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    cursor_next(wp, p.batch, p.n_kv, cc);
+    cursor_next(wp, p.batch, n_units, cc);
   }
   if (cur_b >= 0) flush();
-  named_sync(kEndBar, kConsumers + 32);
-  merge_owed<D, G>(p, wp, s_merge, slots, 2 * C::SLOT, total, P, 32 + tid,
-                   32 + kConsumers, kEndBar);
 
   if (s_abort && tid == 0) {
     // let every copy the producer issued land before the CTA exits
@@ -521,29 +538,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int G, int DT>
+template <int D, int G, int DT, int HP>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
-  using C = Cfg<D, G, DT>;
+  using C = Cfg<D, G, DT, HP>;
   static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-  auto kern = decode_simt_kernel<D, G, DT>;
+  static_assert(C::NS >= 2, "ring depth");
+  auto kern = decode_simt_kernel<D, G, DT, HP>;
   static bool done[64] = {};  // one table per instantiation
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_splits, kThreads, C::SMEM, s>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s, 1, p);
+  if (e != cudaSuccess) return e;
+  return launch_merge_dense<D, G * HP>(p, p.n_kv / HP, s);
 }
+
+// Head-group sizes built: 1 always; one larger size per row width (a 32 KB
+// copy of 64-token rows), for groups of 1 or 2 query heads.
+template <int D, int DT>
+constexpr int kWideHP = D * (DT == DT_BF16 ? 2 : 1) >= 256 ? 2 : 4;
 
 template <int D, int DT>
 cudaError_t launch_g(const DecodeParams &p, cudaStream_t s) {
-  switch (p.n_h / p.n_kv) {
-    case 1: return launch_t<D, 1, DT>(p, s);
-    case 2: return launch_t<D, 2, DT>(p, s);
-    case 4: return launch_t<D, 4, DT>(p, s);
+  constexpr int W = kWideHP<D, DT>;
+  const int g = p.n_h / p.n_kv;
+  if (p.hp == 1) {
+    switch (g) {
+      case 1: return launch_t<D, 1, DT, 1>(p, s);
+      case 2: return launch_t<D, 2, DT, 1>(p, s);
+      case 4: return launch_t<D, 4, DT, 1>(p, s);
+    }
+  } else if (p.hp == W) {
+    switch (g) {
+      case 1: return launch_t<D, 1, DT, W>(p, s);
+      case 2: return launch_t<D, 2, DT, W>(p, s);
+    }
   }
   return cudaErrorNotSupported;
 }
 
 }  // namespace
+
+int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
+                         int block_size) {
+  if (block_size != kStageRows || g > 2) return 1;
+  const int w = head_dim == 128 ? (dtype == DT_BF16 ? kWideHP<128, DT_BF16>
+                                                    : kWideHP<128, DT_FP8>)
+                                : (dtype == DT_BF16 ? kWideHP<64, DT_BF16>
+                                                    : kWideHP<64, DT_FP8>);
+  return n_kv % w == 0 ? w : 1;
+}
 
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s) {
   const bool fp8 = p.dtype == DT_FP8;

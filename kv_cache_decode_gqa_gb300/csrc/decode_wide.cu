@@ -10,8 +10,11 @@
 //    one kv head, only the positions an index list names are read.
 //
 // A unit is (sequence, 64-head tile); its work is cut into 32-position
-// chunks and spread over a persistent launch by the stream-K partition of
-// stream_k.cuh. A producer warp fetches a chunk with one bulk copy per row
+// chunks. The stream-K partition of stream_k.cuh spreads the chunks of all
+// sequences over gridDim / tiles CTA "lanes", and the `tiles` neighbouring
+// CTAs of a lane take the same chunk range, one head tile each: they stream
+// the same rows at about the same time, so a row read for one tile is
+// still in L2 for the others and HBM delivers it once. A producer warp fetches a chunk with one bulk copy per row
 // and lane (the positions of a chunk need not be contiguous: paged blocks,
 // or index-selected positions) into rows padded by 16 bytes, which keeps
 // every 8-row ldmatrix read free of bank conflicts. Sixteen consumer warps
@@ -21,8 +24,11 @@
 // probabilities P (rounded to bf16) through shared memory, and each warp
 // accumulates O += P V for its quarter of the value columns. So no product
 // is computed twice. At a unit boundary the row sums are combined, and the
-// unit is written out, or as a partial merged by the last covering CTA
-// (log-sum-exp merge).
+// unit is written out, or as a partial. The partials of a unit cut between
+// CTAs (64 heads x 512 values each, so a unit cut 19 ways holds 2.4 MB) are
+// merged by a second, wide launch: one CTA per (unit, 1/32 of the unit's
+// outputs), each running an online log-sum-exp merge over the parts with
+// independent loads in flight, so no single SM reads a whole unit.
 #include <cmath>
 
 #include "kvd_common.cuh"
@@ -80,12 +86,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *empty = full + C::NS;
   uint64_t *qbar = empty + C::NS;
   __shared__ int s_len_err;
-  __shared__ int s_merge[2];
   __shared__ volatile int s_abort, s_issued, s_producer_done;
   __shared__ unsigned s_valid[C::NS];  // rows of each stage that were fetched
 
   const int tiles = p.n_h / kHeads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
   const int qr = lane >> 2, qc = lane & 3;
 
   if (tid == 0) {
@@ -93,16 +100,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     s_issued = 0;
     s_producer_done = 0;
-    s_merge[0] = s_merge[1] = -1;
   }
   __syncthreads();
-  build_partition(wp, p, &s_len_err, kRows, tiles, GATHER ? p.n_idx : 0);
+  build_partition(wp, p, &s_len_err, kRows, 1, GATHER ? p.n_idx : 0);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
-  const int P = min((int)gridDim.x, max(total, 1));
-  const int c = blockIdx.x;
+  const int lanes = (int)gridDim.x / tiles;
+  const int P = min(lanes, max(total, 1));
+  const int c = (int)blockIdx.x / tiles;     // lane: a range of chunks
+  const int tile = (int)blockIdx.x % tiles;  // head tile of this CTA
 
-  if (c == 0) {  // sequences with nothing visible: out = 0, lse = -inf
+  if (blockIdx.x == 0) {  // sequences with nothing visible: out = 0, lse = -inf
     for (int b = 0; b < p.batch; ++b) {
       if (wp.nch[b] != 0) continue;
       for (int i = tid; i < p.n_h * DV; i += kThreads)
@@ -112,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[(long)b * p.n_h + i] = -INFINITY;
     }
   }
-  if (c >= P || total == 0) return;
+  if (c >= P || total == 0) return;  // (also CTAs beyond lanes * tiles)
   const int lo = range_lo(c, total, P);
   const int hi = range_lo(c + 1, total, P);
   const int n = hi - lo;
@@ -133,6 +141,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   // one bulk copy per cached tensor.
   if (warp == kCWarps) {
     ChunkCursor pc = cursor_at(wp, p.batch, lo);
+    // position and block of this lane's row of the chunk at `cc` (-1: none)
+    auto lookup = [&](const ChunkCursor &cc, int &t, int &blk) {
+      const int T = wp.len[cc.b];
+      const int e = cc.k * kRows + lane;  // entry of this lane's row
+      if constexpr (GATHER) {
+        t = e < p.n_idx ? p.indices[(long)cc.b * p.n_idx + e] : -1;
+        if (t >= T) {
+          report(p.err, DEVERR_INDEX);
+          t = -1;
+        }
+      } else {
+        t = e < T ? e : -1;
+      }
+      blk = -1;
+      if (t >= 0) {
+        blk = p.block_table[(long)cc.b * p.max_blocks + t / p.block_size];
+        if (blk < 0 || blk >= p.num_blocks) {
+          report(p.err, DEVERR_BLOCK);
+          blk = 0;  // read a valid block; the result is flagged as wrong
+        }
+      }
+    };
+    int t, blk;
+    lookup(pc, t, blk);
     for (int i = 0; i < n; ++i) {
       const int s = i % C::NS;
       int go = 1;
@@ -141,26 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!go) {
         if (lane == 0) report(p.err, DEVERR_TIMEOUT);
         break;
-      }
-      const int T = wp.len[pc.b];
-      const int e = pc.k * kRows + lane;  // entry of this lane's row
-      int t;
-      if constexpr (GATHER) {
-        t = e < p.n_idx ? p.indices[(long)pc.b * p.n_idx + e] : -1;
-        if (t >= T) {
-          report(p.err, DEVERR_INDEX);
-          t = -1;
-        }
-      } else {
-        t = e < T ? e : -1;
-      }
-      int blk = -1;
-      if (t >= 0) {
-        blk = p.block_table[(long)pc.b * p.max_blocks + t / p.block_size];
-        if (blk < 0 || blk >= p.num_blocks) {
-          report(p.err, DEVERR_BLOCK);
-          blk = 0;  // read a valid block; the result is flagged as wrong
-        }
       }
       const unsigned valid = __ballot_sync(0xffffffffu, t >= 0);
       if (t < 0) {
@@ -189,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    DV * 2, &full[s]);
       }
       if (lane == 0) s_issued = i + 1;
-      cursor_next(wp, p.batch, tiles, pc);
+      // the next chunk's rows are looked up now, while the ring is full
+      cursor_next(wp, p.batch, 1, pc);
+      if (i + 1 < n) lookup(pc, t, blk);
     }
     if (lane == 0) s_producer_done = 1;
     return;
@@ -203,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float o[C::DVQ / 8][4];      // O: 16 rows x DVQ columns
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int cur_b = -1, cur_h = -1, n_units = 0;
-  int pend_prev[2] = {-1, -1}, pend_start[2] = {0, 0}, n_pend = 0;
 
   auto start_unit = [&](int b, int h) {
     // the query tile of (b, head tile h): 64 rows, one bulk copy each
@@ -246,10 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       L0 += lsum[(grp * 4 + w) * 16 + qr];
       L1 += lsum[(grp * 4 + w) * 16 + qr + 8];
     }
-    const int ustart = wp.pre[b] + h * wp.nch[b];
+    const int ustart = wp.pre[b];
     const int uend = ustart + wp.nch[b];
     const bool whole = ustart >= lo && uend <= hi;
-    const int wslot = c * 2 + partial_side(ustart, lo);
+    const int wslot = (c * 2 + partial_side(ustart, lo)) * tiles + h;
     const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
     const int row0 = grp * 16 + qr, row1 = row0 + 8;  // head within the tile
     const float lse0 = L0 > 0.f ? (m0 + log2f(L0)) * 0.69314718055994531f
@@ -284,23 +297,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.ws_lse[(long)wslot * kHeads + row1] = lse1;
       }
     }
-    if (!whole) __threadfence();
-    named_sync(kAllBar, kConsumers);  // partials written; lsum reusable
-    if (!whole && tid == 0) {
-      pend_prev[n_pend] = arrive_release(p.counters + (long)b * tiles + h);
-      pend_start[n_pend] = ustart;
-      ++n_pend;
-    }
+    named_sync(kAllBar, kConsumers);  // lsum reusable
   };
 
   ChunkCursor cc = cursor_at(wp, p.batch, lo);
   const float sl2 = p.scale_log2;
   for (int i = 0; i < n; ++i) {
     const int s = i % C::NS;
-    if (cc.b != cur_b || cc.h != cur_h) {
+    if (cc.b != cur_b) {
       if (cur_b >= 0) flush(cur_b, cur_h);
       cur_b = cc.b;
-      cur_h = cc.h;
+      cur_h = tile;
       start_unit(cur_b, cur_h);
     }
     bool ok = !s_abort && mbar_wait(&full[s], (i / C::NS) & 1);
@@ -406,30 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    cursor_next(wp, p.batch, tiles, cc);
+    cursor_next(wp, p.batch, 1, cc);
   }
   if (cur_b >= 0) flush(cur_b, cur_h);
-
-  // ---- merges this CTA owes (it arrived last on the unit's counter) ----
-  if (tid == 0) {
-    for (int j = 0; j < n_pend; ++j) {
-      const int ustart = pend_start[j];
-      const int bb = find_seq(wp, p.batch, ustart);
-      const int hh = (ustart - wp.pre[bb]) / wp.nch[bb];
-      const int uend = ustart + wp.nch[bb];
-      const int parts = cta_of(uend - 1, total, P) - cta_of(ustart, total, P) + 1;
-      if (pend_prev[j] == parts - 1) {
-        s_merge[j] = ustart;
-        atomicExch(p.counters + (long)bb * tiles + hh, 0);
-      }
-    }
-    __threadfence();
-  }
-  named_sync(kAllBar, kConsumers);
-  merge_owed<DV, kHeads>(p, wp, s_merge,
-                         reinterpret_cast<float *>(smem + C::K_OFF),
-                         (C::NS * C::KST) / 4, total, P, tid, kConsumers,
-                         kAllBar);
 
   if (s_abort && tid == 0) {
     for (int t = 0; t < (1 << 20) && !s_producer_done; ++t) __nanosleep(1000);
@@ -442,6 +428,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+constexpr int kMergeSlices = 32;    // CTAs per split unit
+constexpr int kMergeThreads = 256;
+
+// Log-sum-exp merge of the partials of every unit the decode launch cut
+// between CTAs. Grid (units, kMergeSlices): CTA (u, j) rebuilds the launch's
+// partition, returns if unit u lies inside one CTA's range, and otherwise
+// merges the j-th 1/32 of the unit's outputs: for each float4 of outputs
+// (4 values of one head) an online merge over the parts, 8 parts' loads in
+// flight at a time. Part i is the partial of lane c_first + i: side 1 of
+// the first covering lane, side 0 of the others.
+template <int DV, bool GATHER>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_wide_kernel(const DecodeParams p) {
+  __shared__ WorkPartitionT<kNB> wp;
+  __shared__ int s_len_err;
+  pdl_trigger();
+  pdl_wait();
+  const int tiles = p.n_h / kHeads;
+  const int u = blockIdx.x, b = u / tiles, h = u % tiles;
+  build_partition(wp, p, &s_len_err, kRows, 1, GATHER ? p.n_idx : 0);
+  const int total = wp.total;
+  if (total == 0 || wp.nch[b] == 0) return;
+  const int P = min(p.n_splits / tiles, total);
+  const int ustart = wp.pre[b];
+  const int uend = ustart + wp.nch[b];
+  const int c_first = cta_of(ustart, total, P);
+  const int parts = cta_of(uend - 1, total, P) - c_first + 1;
+  if (parts == 1) return;  // written whole by the decode launch
+  constexpr int N4 = kHeads * DV / 4;
+  constexpr int PER = N4 / kMergeSlices;
+  static_assert(PER % kMergeThreads == 0, "slice of whole float4 rounds");
+  const long bh0 = (long)b * p.n_h + (long)h * kHeads;
+  for (int e = blockIdx.y * PER + threadIdx.x; e < (blockIdx.y + 1) * PER;
+       e += kMergeThreads) {
+    const int g = (4 * e) / DV;  // head within the tile
+    float M = -INFINITY, W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < parts; i0 += 8) {
+      float4 v[8];
+      float l[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j;
+        const int slot = ((c_first + i) * 2 + (i == 0 ? 1 : 0)) * tiles + h;
+        if (i < parts) {
+          l[j] = __ldcg(p.ws_lse + (long)slot * kHeads + g);
+          v[j] = __ldcg(reinterpret_cast<const float4 *>(
+                            p.ws_o + (long)slot * kHeads * DV) + e);
+        } else {
+          l[j] = -INFINITY;
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (l[j] == -INFINITY) continue;  // an empty part adds nothing
+        const float Mn = fmaxf(M, l[j]);
+        const float a = M == -INFINITY ? 0.f : expf(M - Mn);
+        const float w = expf(l[j] - Mn);
+        W = W * a + w;
+        acc.x = acc.x * a + w * v[j].x;
+        acc.y = acc.y * a + w * v[j].y;
+        acc.z = acc.z * a + w * v[j].z;
+        acc.w = acc.w * a + w * v[j].w;
+        M = Mn;
+      }
+    }
+    const float iw = W > 0.f ? 1.f / W : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
+    packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
+    *reinterpret_cast<uint2 *>(p.out + bh0 * DV + 4 * e) = packed;
+    if ((4 * e) % DV == 0 && p.lse)
+      p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
+  }
+}
+
 template <int DK, int DV, bool GATHER>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   using C = WCfg<DK, DV, GATHER>;
@@ -450,8 +513,11 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   static bool done[64] = {};
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_splits, kThreads, C::SMEM, s>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s, 1, p);
+  if (e != cudaSuccess || p.n_splits <= 1) return e;
+  const dim3 grid(p.batch * (p.n_h / kHeads), kMergeSlices);
+  return launch_pdl(merge_wide_kernel<DV, GATHER>, grid, dim3(kMergeThreads),
+                    0, s, 1, p);
 }
 
 }  // namespace

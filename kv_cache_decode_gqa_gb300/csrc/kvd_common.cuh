@@ -19,6 +19,52 @@ __device__ __forceinline__ void report(int *err, int bit) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl): it may be scheduled while the kernel before it
+// on the stream is still running, so its launch overlaps that kernel's last
+// CTAs instead of following their completion. Each kernel first lets its
+// own successor be scheduled (pdl_trigger; the successor still cannot pass
+// its pdl_wait before this grid completes) and then, before it touches
+// global memory, waits until its predecessor has completed and that grid's
+// writes are visible (pdl_wait). Without a programmatic predecessor both
+// are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kern` on `s` with programmatic stream serialisation allowed, plus
+// an optional cluster shape (cluster_x > 1).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s, int cluster_x,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

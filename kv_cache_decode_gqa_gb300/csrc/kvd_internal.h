@@ -55,6 +55,7 @@ struct DecodeParams {
   int32_t n_idx;        // entries per row of `indices`
   int32_t split_len;    // tokens (or index entries) per split
   int32_t n_splits;
+  int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
   float scale_log2;  // softmax scale * log2(e)
   int *err;
 };
@@ -76,6 +77,10 @@ struct IndexerParams {
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 // Dense GQA/MHA, CUDA cores (group size <= 4).
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s);
+// kv heads the CUDA-core kernel takes per work unit for these shapes (its
+// plan and its launch must agree).
+int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
+                         int block_size);
 // Dense GQA on the tensor cores (group size 8 or 16, head_dim 128).
 cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
                               cudaStream_t s);

@@ -8,7 +8,7 @@
 // A unit lying wholly inside one CTA's range is finished by that CTA; a
 // unit cut between CTAs leaves one partial result per covering CTA (at most
 // two per CTA: the unit its range starts in and the unit it ends in), which
-// the last covering CTA to finish merges (log-sum-exp merge).
+// a short second launch merges (log-sum-exp merge).
 #pragma once
 
 #include "kvd_common.cuh"
@@ -157,117 +157,96 @@ __device__ __forceinline__ int partial_side(int ustart, int lo) {
   return ustart < lo ? 0 : 1;
 }
 
-// Arrival counter increment with release semantics: the partial results
-// this CTA wrote (ordered before this call by a barrier) become visible
-// before the increment does. Returns the previous count.
-__device__ __forceinline__ int arrive_release(int *ctr) {
-  int prev;
-  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], 1;"
-               : "=r"(prev)
-               : "l"(ctr)
-               : "memory");
-  return prev;
-}
+// Log-sum-exp merge of the units a dense decode launch cut between CTAs,
+// run as a second launch right after it (programmatic dependent launch, so
+// its CTAs are resident and waiting when the decode grid completes). Each
+// CTA rebuilds the partition from the sequence lengths and takes units
+// u = blockIdx.x, + gridDim.x, ...; for a unit covered by more than one
+// CTA it merges, per float4 of outputs (4 values of one head), the parts'
+// partial results with an online log-sum-exp merge, 8 parts' loads in
+// flight at a time:
+//   out = sum_s w_s o_s,  w_s = e^(lse_s - M) / sum_s e^(lse_s - M),
+//   M = max_s lse_s,  lse = M + ln sum_s e^(lse_s - M).
+// Part i is the partial of CTA c_first + i: side 1 of the first covering
+// CTA, side 0 of the others. Units inside one CTA were written whole.
+constexpr int kMergeThreads = 128;
 
-// Merge the partials of every unit in `merge` (unit start chunks, -1 for
-// none): out = sum_s w_s o_s with w_s = e^(lse_s - M) / sum_s e^(lse_s - M),
-// M = max_s lse_s, and lse = M + ln sum_s e^(lse_s - M). Thread `t` of `nt`
-// cooperating threads (named barrier `bar`). `scratch` (cap floats) first
-// holds the parts' lse values, then their weights e^(lse_s - M); the partial
-// outputs are then summed part by part with batches of independent 16-byte
-// loads, so a part costs about one L2 round trip. Part i is the partial of
-// CTA c_first + i: side 1 of the first covering CTA, side 0 of the others.
-template <int D, int G, int NB>
-__device__ __forceinline__ void merge_owed(const DecodeParams &p,
-                                           const WorkPartitionT<NB> &wp,
-                                           const int *merge, float *scratch,
-                                           int cap, int total, int P, int t,
-                                           int nt, int bar) {
-  static_assert(D % 4 == 0, "vector loads");
-  float *mg = scratch + cap - 2 * G;  // per-head M and 1 / W
-  for (int j = 0; j < 2; ++j) {
-    const int ustart = merge[j];
-    if (ustart < 0) continue;
-    const int b = find_seq(wp, p.batch, ustart);
-    const int h = (ustart - wp.pre[b]) / wp.nch[b];
+template <int D, int GU>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_dense_kernel(const DecodeParams p, int n_units) {
+  __shared__ WorkPartition wp;
+  __shared__ int s_len_err;
+  pdl_trigger();
+  pdl_wait();
+  build_partition(wp, p, &s_len_err, kStageRows, n_units);
+  const int total = wp.total;
+  if (total == 0) return;
+  const int P = min(p.n_splits, total);
+  constexpr int N4 = GU * D / 4;
+  for (int u = blockIdx.x; u < p.batch * n_units; u += gridDim.x) {
+    const int b = u / n_units, h = u % n_units;
+    if (wp.nch[b] == 0) continue;
+    const int ustart = wp.pre[b] + h * wp.nch[b];
     const int uend = ustart + wp.nch[b];
     const int c_first = cta_of(ustart, total, P);
     const int parts = cta_of(uend - 1, total, P) - c_first + 1;
-    const long bh0 = (long)b * p.n_h + (long)h * G;  // first head of the unit
-    const bool staged = parts * G <= cap - 2 * G;
-    auto slot = [&](int i) { return (c_first + i) * 2 + (i == 0 ? 1 : 0); };
-    __threadfence();
-    if (staged)
-      for (int i = t; i < parts * G; i += nt)
-        scratch[i] = __ldcg(p.ws_lse + (long)slot(i / G) * G + i % G);
-    named_sync(bar, nt);
-    for (int g = t; g < G; g += nt) {
-      float M = -INFINITY;
-      for (int i = 0; i < parts; ++i)
-        M = fmaxf(M, staged ? scratch[i * G + g]
-                            : __ldcg(p.ws_lse + (long)slot(i) * G + g));
-      float W = 0.f;
-      for (int i = 0; i < parts; ++i) {
-        const float l = staged ? scratch[i * G + g]
-                               : __ldcg(p.ws_lse + (long)slot(i) * G + g);
-        const float w = M == -INFINITY ? 0.f : expf(l - M);
-        if (staged) scratch[i * G + g] = w;
-        W += w;
-      }
-      mg[g] = M;
-      mg[G + g] = W > 0.f ? 1.f / W : 0.f;
-      if (p.lse) p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
-    }
-    named_sync(bar, nt);
-    constexpr int kBatch = 8;  // float4 loads in flight per thread
-    const int n4 = G * D / 4;
-    for (int e0 = t; e0 < n4; e0 += nt * kBatch) {
-      float4 acc[kBatch];
+    if (parts == 1) continue;
+    const long bh0 = (long)b * p.n_h + (long)h * GU;
+    for (int e = threadIdx.x; e < N4; e += kMergeThreads) {
+      const int g = (4 * e) / D;  // head within the unit
+      float M = -INFINITY, W = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i0 = 0; i0 < parts; i0 += 8) {
+        float4 v[8];
+        float l[8];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i = 0; i < parts; ++i) {
-        const float4 *src =
-            reinterpret_cast<const float4 *>(p.ws_o + (long)slot(i) * G * D);
-        float4 v[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = e0 + u * nt;
-          v[u] = e < n4 ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = e0 + u * nt;
-          if (e >= n4) continue;
-          const int g = (4 * e) / D;
-          float w;
-          if (staged) {
-            w = scratch[i * G + g];
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j;
+          const long slot = (long)(c_first + i) * 2 + (i == 0 ? 1 : 0);
+          if (i < parts) {
+            l[j] = __ldcg(p.ws_lse + slot * GU + g);
+            v[j] = __ldcg(reinterpret_cast<const float4 *>(
+                              p.ws_o + slot * GU * D) + e);
           } else {
-            const float M = mg[g];
-            w = M == -INFINITY
-                    ? 0.f
-                    : expf(__ldcg(p.ws_lse + (long)slot(i) * G + g) - M);
+            l[j] = -INFINITY;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          acc[u].x = fmaf(w, v[u].x, acc[u].x);
-          acc[u].y = fmaf(w, v[u].y, acc[u].y);
-          acc[u].z = fmaf(w, v[u].z, acc[u].z);
-          acc[u].w = fmaf(w, v[u].w, acc[u].w);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (l[j] == -INFINITY) continue;  // an empty part adds nothing
+          const float Mn = fmaxf(M, l[j]);
+          const float a = M == -INFINITY ? 0.f : expf(M - Mn);
+          const float w = expf(l[j] - Mn);
+          W = W * a + w;
+          acc.x = acc.x * a + w * v[j].x;
+          acc.y = acc.y * a + w * v[j].y;
+          acc.z = acc.z * a + w * v[j].z;
+          acc.w = acc.w * a + w * v[j].w;
+          M = Mn;
         }
       }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * nt;
-        if (e >= n4) continue;
-        const int g = (4 * e) / D;
-        const float iw = mg[G + g];
-        uint2 packed;
-        packed.x = pack_bf16x2(acc[u].x * iw, acc[u].y * iw);
-        packed.y = pack_bf16x2(acc[u].z * iw, acc[u].w * iw);
-        *reinterpret_cast<uint2 *>(p.out + bh0 * D + 4 * e) = packed;
-      }
+      const float iw = W > 0.f ? 1.f / W : 0.f;
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
+      packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
+      *reinterpret_cast<uint2 *>(p.out + bh0 * D + 4 * e) = packed;
+      if ((4 * e) % D == 0 && p.lse)
+        p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
     }
-    named_sync(bar, nt);
   }
+}
+
+// Queue the merge launch of a dense decode launch that used more than one
+// CTA (`n_units` work units per sequence of GU query heads each).
+template <int D, int GU>
+inline cudaError_t launch_merge_dense(const DecodeParams &p, int n_units,
+                                      cudaStream_t s) {
+  if (p.n_splits <= 1 || p.batch == 0) return cudaSuccess;
+  const long nu = (long)p.batch * n_units;
+  const int grid = (int)(nu < 1024 ? nu : 1024);
+  return launch_pdl(merge_dense_kernel<D, GU>, dim3(grid),
+                    dim3(kMergeThreads), 0, s, 1, p, n_units);
 }
 
 }  // namespace kvd
