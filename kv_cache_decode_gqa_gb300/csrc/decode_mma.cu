@@ -109,8 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int G = p.n_h / p.n_kv;  // 8 or 16 (checked by the launcher)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: see the merge launch
   const int qr = lane >> 2, qc = lane & 3;  // MMA fragment row / column quad
 
   if (tid == 0) {

@@ -50,6 +50,7 @@ constexpr int kWarps = kConsumers / 32;
 constexpr int kProducer = kWarps;          // warp index of the producer
 constexpr int kFinisher = kWarps + 1;      // warp index of the finisher
 constexpr int kThreads = kConsumers + 64;
+constexpr int kFinalBar = 1;               // the consumer warps, at the end
 
 template <int D, int G, int DT, int HP>
 struct Cfg {
@@ -147,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: see the merge launch
 
   if (tid == 0) {
     s_len_err = 0;
@@ -193,6 +194,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+
+  // Combine the warp states of unit (b, h) held in flush slot sl and write
+  // the unit's outputs (a unit inside this CTA's range) or its partial;
+  // thread t of nt cooperating threads.
+  auto write_unit = [&](int b, int h, int sl, int t, int nt) {
+    const int ustart = wp.pre[b] + h * wp.nch[b];
+    const int uend = ustart + wp.nch[b];
+    const float *wm = slots + sl * C::SLOT;
+    const float *wl = wm + kWarps * G;
+    const float *wo = wl + kWarps * G;  // [warp][G][D]
+    const bool whole = ustart >= lo && uend <= hi;
+    const int wslot = c * 2 + partial_side(ustart, lo);
+    for (int idx = t; idx < GU * D; idx += nt) {
+      const int jg = idx / D, d = idx % D;  // head (j, g) of the unit
+      const int j = jg / G, g = jg % G;
+      const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
+      const int w0 = j * C::WPH;  // the head's warps
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, wm[(w0 + w) * G + g]);
+      float L = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) {
+        const float a = weight(wm[(w0 + w) * G + g], M);
+        L = fmaf(wl[(w0 + w) * G + g], a, L);
+        acc = fmaf(wo[((w0 + w) * G + g) * D + d], a, acc);
+      }
+      const float res = acc / L * vs;
+      const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
+      const long bh = (long)b * p.n_h + h * GU + jg;
+      if (whole) {
+        p.out[bh * D + d] = f2bf(res);
+        if (d == 0 && p.lse) p.lse[bh] = lse_nat;
+      } else {
+        p.ws_o[((long)wslot * GU + jg) * D + d] = res;
+        if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
+      }
+    }
+  };
 
   // ======================= producer warp ==================================
   if (warp == kProducer) {
@@ -302,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= finisher warp ==================================
+  // Every unit of the range but the last: the consumer warps write the last
+  // one themselves, all 256 threads at once, since nothing overlaps it.
   if (warp == kFinisher) {
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
@@ -310,43 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ustart = wp.pre[b] + h * wp.nch[b];
       const int uend = ustart + wp.nch[b];
       const int xend = min(uend, hi);
+      if (xend >= hi) break;  // the last unit
       const int sl = e & 1;
       if (!mbar_wait(&sfull[sl], (e >> 1) & 1)) {
         if (lane == 0) report(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
         break;
       }
-      const float *wm = slots + sl * C::SLOT;
-      const float *wl = wm + kWarps * G;
-      const float *wo = wl + kWarps * G;  // [warp][G][D]
-      const bool whole = ustart >= lo && uend <= hi;
-      const int wslot = c * 2 + partial_side(ustart, lo);
-      for (int idx = lane; idx < GU * D; idx += 32) {
-        const int jg = idx / D, d = idx % D;  // head (j, g) of the unit
-        const int j = jg / G, g = jg % G;
-        const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
-        const int w0 = j * C::WPH;  // the head's warps
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, wm[(w0 + w) * G + g]);
-        float L = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::WPH; ++w) {
-          const float a = weight(wm[(w0 + w) * G + g], M);
-          L = fmaf(wl[(w0 + w) * G + g], a, L);
-          acc = fmaf(wo[((w0 + w) * G + g) * D + d], a, acc);
-        }
-        const float res = acc / L * vs;
-        const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-        const long bh = (long)b * p.n_h + h * GU + jg;
-        if (whole) {
-          p.out[bh * D + d] = f2bf(res);
-          if (d == 0 && p.lse) p.lse[bh] = lse_nat;
-        } else {
-          p.ws_o[((long)wslot * GU + jg) * D + d] = res;
-          if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
-        }
-      }
+      write_unit(b, h, sl, lane, 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sl]);  // the slot may be reused
       x = xend;
@@ -386,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  // Merge this warp's four lane-group states and hand them to the finisher.
-  auto flush = [&]() {
+  // Merge this warp's four lane-group states and hand them to the finisher
+  // (or, for the last unit, leave them in the slot for the consumer warps).
+  auto flush = [&](bool last) {
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
 #pragma unroll
@@ -430,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sfull[sl]);
+    if (lane == 0 && !last) mbar_arrive(&sfull[sl]);
     ++n_flush;
   };
 
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_abort = 1;
     }
     if (cc.b != cur_b || cc.h != cur_h) {
-      if (cur_b >= 0) flush();
+      if (cur_b >= 0) flush(false);
       cur_b = cc.b;
       cur_h = cc.h;
       start_unit(s, cur_h);
@@ -524,7 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&empty[s]);
     cursor_next(wp, p.batch, n_units, cc);
   }
-  if (cur_b >= 0) flush();
+  if (cur_b >= 0) {
+    flush(true);
+    named_sync(kFinalBar, kConsumers);  // every warp's state is in the slot
+    write_unit(cur_b, cur_h, (n_flush - 1) & 1, tid, kConsumers);
+  }
 
   if (s_abort && tid == 0) {
     // let every copy the producer issued land before the CTA exits

@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tiles = p.n_h / kHeads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: see the merge launch
   const int qr = lane >> 2, qc = lane & 3;
 
   if (tid == 0) {
@@ -444,10 +444,14 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ WorkPartitionT<kNB> wp;
   __shared__ int s_len_err;
   pdl_trigger();
-  pdl_wait();
   const int tiles = p.n_h / kHeads;
   const int u = blockIdx.x, b = u / tiles, h = u % tiles;
+  // The lengths may be read before the decode launch completes: that launch
+  // (this launch's only possible predecessor still running, since it lets
+  // its dependants start only after its own predecessor has completed)
+  // does not write them. The partials are read after pdl_wait.
   build_partition(wp, p, &s_len_err, kRows, 1, GATHER ? p.n_idx : 0);
+  pdl_wait();
   const int total = wp.total;
   if (total == 0 || wp.nch[b] == 0) return;
   const int P = min(p.n_splits / tiles, total);

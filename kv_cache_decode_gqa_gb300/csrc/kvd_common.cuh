@@ -24,12 +24,14 @@ __device__ __forceinline__ void report(int *err, int bit) {
 // Every kernel of the library is launched with programmatic stream
 // serialisation (launch_pdl): it may be scheduled while the kernel before it
 // on the stream is still running, so its launch overlaps that kernel's last
-// CTAs instead of following their completion. Each kernel first lets its
-// own successor be scheduled (pdl_trigger; the successor still cannot pass
-// its pdl_wait before this grid completes) and then, before it touches
-// global memory, waits until its predecessor has completed and that grid's
-// writes are visible (pdl_wait). Without a programmatic predecessor both
-// are no-ops.
+// CTAs instead of following their completion. pdl_trigger lets this grid's
+// successor be scheduled (the successor still cannot pass its pdl_wait
+// before this grid completes); pdl_wait blocks until this grid's
+// predecessor has completed and its writes are visible, and every kernel
+// calls it before it touches global memory the predecessor may write.
+// Decode kernels trigger only after their wait, so the merge launch that
+// follows a decode launch never overlaps the decode's predecessor. Without
+// a programmatic predecessor both are no-ops.
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -177,8 +177,12 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ WorkPartition wp;
   __shared__ int s_len_err;
   pdl_trigger();
-  pdl_wait();
+  // The lengths may be read before the decode launch completes: that launch
+  // (this launch's only possible predecessor still running, since it lets
+  // its dependants start only after its own predecessor has completed)
+  // does not write them. The partials are read after pdl_wait.
   build_partition(wp, p, &s_len_err, kStageRows, n_units);
+  pdl_wait();
   const int total = wp.total;
   if (total == 0) return;
   const int P = min(p.n_splits, total);
