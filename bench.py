@@ -370,7 +370,8 @@ def build_step(K, wl, outs, wss):
             else:
                 K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
                              wl.q[layer], out=outs[layer],
-                             workspace=wss[layer], want_lse=False)
+                             workspace=wss[layer], want_lse=False,
+                             seqs_flags=K.SEQS_STABLE)
     return step
 
 
@@ -405,7 +406,7 @@ def decode_only(K, wl, outs, wss, layer):
     elif s.kind == "gqa":
         K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
                      wl.q[layer], out=outs[layer], workspace=wss[layer],
-                     want_lse=False)
+                     want_lse=False, seqs_flags=K.SEQS_STABLE)
 
 
 def pack_inputs(torch, wl):

@@ -120,14 +120,25 @@ typedef struct kvd_cache {
  *                 plan and the workspace. Must be <= max_blocks_per_seq *
  *                 block_size (else KVD_ERR_CAPACITY). A device length above
  *                 it is clamped to it and flagged KVD_DEVERR_LEN.
+ *   flags         0, or KVD_SEQS_STABLE (other bits: KVD_ERR_SHAPE)
+ *
+ * Kernels of this library may start while the kernel before them on the
+ * stream is still running (programmatic dependent launch); they read their
+ * inputs only after that kernel has completed. KVD_SEQS_STABLE declares that
+ * block_table and seq_lens already hold their final values when the kernel
+ * launched just before this call starts, and that no kernel still running
+ * writes them (for example: they are set by host copies at the start of a
+ * decode step and read by every layer). kvd_gqa_decode then reads them, and
+ * plans its work, while that kernel finishes. Other calls ignore the flag.
  */
+#define KVD_SEQS_STABLE 1
 typedef struct kvd_seqs {
   const int32_t *block_table;
   const int32_t *seq_lens;
   int32_t batch;
   int32_t max_blocks_per_seq;
   int32_t max_seq_len;
-  int32_t reserved;
+  int32_t flags;
 } kvd_seqs;
 
 typedef enum kvd_op {

@@ -92,7 +92,10 @@ class PagedCache:
             _ptr(self.v_inv_scale))
 
 
-def _seqs(block_table, seq_lens, max_seq_len):
+SEQS_STABLE = 1  # KVD_SEQS_STABLE
+
+
+def _seqs(block_table, seq_lens, max_seq_len, flags=0):
     import torch
     _need(block_table, "block_table", torch.int32)
     _need(seq_lens, "seq_lens", torch.int32)
@@ -100,7 +103,7 @@ def _seqs(block_table, seq_lens, max_seq_len):
         raise ValueError("block_table must be [batch][max_blocks_per_seq]")
     return _native.KvdSeqs(_ptr(block_table), _ptr(seq_lens),
                            block_table.shape[0], block_table.shape[1],
-                           int(max_seq_len), 0)
+                           int(max_seq_len), int(flags))
 
 
 def workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k=0):
@@ -153,13 +156,14 @@ def _outputs(q, n_h, dv, out, lse, want_lse):
 
 def gqa_decode(cache, block_table, seq_lens, max_seq_len, q, scale=None,
                out=None, lse=None, workspace=None, want_lse=True,
-               stream=None):
-    """GQA/MHA decode: q [batch][n_h][head_dim] bf16 -> (out, lse)."""
+               stream=None, seqs_flags=0):
+    """GQA/MHA decode: q [batch][n_h][head_dim] bf16 -> (out, lse).
+    seqs_flags: 0 or SEQS_STABLE (see KVD_SEQS_STABLE in kvd.h)."""
     import torch
     _need(q, "q", torch.bfloat16)
     n_h = q.shape[1]
     c = cache.struct()
-    s = _seqs(block_table, seq_lens, max_seq_len)
+    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags)
     out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
     ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
                     n_h, 0, workspace)

@@ -112,6 +112,9 @@ kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
                 "required", what);
   if (s->batch > 65535)
     return fail(KVD_ERR_SHAPE, "%s: batch %d above 65535", what, s->batch);
+  if (s->flags & ~KVD_SEQS_STABLE)
+    return fail(KVD_ERR_SHAPE, "%s: unknown seqs flags 0x%x", what,
+                (unsigned)s->flags);
   if (s->batch > 0 && (!s->block_table || !s->seq_lens))
     return fail(KVD_ERR_NULL, "%s: block_table and seq_lens are required", what);
   if ((long)s->max_seq_len > (long)s->max_blocks_per_seq * c->block_size)
@@ -470,6 +473,7 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.split_len = pl.split_len;
   p.n_splits = pl.n_splits;
   p.hp = pl.hp;
+  p.flags = seqs->flags;
   p.scale_log2 = log2_scale(scale, cache->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -109,8 +109,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int G = p.n_h / p.n_kv;  // 8 or 16 (checked by the launcher)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();
-  pdl_trigger();  // after the wait: see the merge launch
+  // With stable lengths and block table, the plan and the producer's first
+  // block-id lookups run before the predecessor grid completes; every other
+  // global access (cache, queries, scales, outputs) waits for it. Dependants
+  // are let in only after this grid's own wait (see the merge launch).
+  const bool early = p.flags & FLAG_SEQS_STABLE;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int qr = lane >> 2, qc = lane & 3;  // MMA fragment row / column quad
 
   if (tid == 0) {
@@ -127,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = blockIdx.x;
 
   if (c == 0) {
+    if (early) pdl_wait();
     for (int b = 0; b < p.batch; ++b) {
       if (wp.nch[b] != 0) continue;
       for (int i = tid; i < p.n_h * kD; i += kThreads)
@@ -178,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int cnt = min(32, n - base);
+      if (early && base == 0) {
+        pdl_wait();
+        pdl_trigger();
+      }
       bool stop = false;
       for (int j = 0; j < cnt && !stop; ++j) {
         const int b = __shfl_sync(0xffffffffu, mb, j);
@@ -234,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ======================= finisher warp ==================================
   if (warp == kFinisher) {
+    if (early) pdl_wait();
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {
@@ -286,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumer warps =================================
+  if (early) pdl_wait();
   // Per thread: rows qr and qr + 8 of the 16-row tiles, columns 2 qc, 2 qc+1
   // of every 8-wide n-tile.
   uint32_t qa[8][4];      // query A fragments, 8 k-steps of 16

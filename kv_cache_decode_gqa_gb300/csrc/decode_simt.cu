@@ -58,16 +58,23 @@ struct Cfg {
   static constexpr int ROW = D * ES;                 // bytes per cached row
   static constexpr int HSTAGE = kStageRows * ROW;    // one head's K (or V)
   static constexpr int STAGE = HP * HSTAGE;          // K (or V) bytes / chunk
-  static constexpr int RING_BUDGET = HP == 1 ? 160 * 1024 : 192 * 1024;
-  static constexpr int NS_RAW = RING_BUDGET / (2 * STAGE);
-  static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW; // ring depth
   static constexpr int E = D / 8;                    // elements per lane
   static constexpr int WPH = kWarps / HP;            // warps per head
   static constexpr int ITER = 2 * HP;                // 4-row steps per warp
   static constexpr int QB = HP * G * D * 2;          // query rows / stage
-  static constexpr int RING = 2 * NS * STAGE + NS * QB;
   static constexpr int SLOT = kWarps * G * (D + 2);   // floats per slot
   static constexpr int MERGE = 2 * SLOT * 4;
+  // ring depth: up to 160 KB (one head) or 192 KB (head groups) of K and V,
+  // within what the flush slots, the partition and the barriers leave of
+  // 227 KB (1 KB kept for the kernel's static shared variables)
+  static constexpr int RING_BUDGET = HP == 1 ? 160 * 1024 : 192 * 1024;
+  static constexpr int FIXED =
+      MERGE + (int)sizeof(WorkPartition) + 16 + 20 * 8 + 1024;
+  static constexpr int NS_FIT = (227 * 1024 - FIXED) / (2 * STAGE + QB);
+  static constexpr int NS_WANT = RING_BUDGET / (2 * STAGE);
+  static constexpr int NS_MIN = NS_FIT < NS_WANT ? NS_FIT : NS_WANT;
+  static constexpr int NS = NS_MIN > 8 ? 8 : NS_MIN;  // ring depth
+  static constexpr int RING = 2 * NS * STAGE + NS * QB;
   static constexpr int WP_OFF = RING + MERGE;
   static constexpr int BAR_OFF =
       (WP_OFF + (int)sizeof(WorkPartition) + 15) / 16 * 16;
@@ -148,8 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  pdl_wait();
-  pdl_trigger();  // after the wait: see the merge launch
+  // With stable lengths and block table, the plan and the producer's first
+  // block-id lookups run before the predecessor grid completes; every other
+  // global access (cache, queries, scales, outputs) waits for it. Dependants
+  // are let in only after this grid's own wait (see the merge launch).
+  const bool early = p.flags & FLAG_SEQS_STABLE;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (tid == 0) {
     s_len_err = 0;
@@ -167,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // sequences with nothing visible: out = 0, lse = -inf
   if (c == 0) {
+    if (early) pdl_wait();
     for (int b = 0; b < p.batch; ++b) {
       if (wp.nch[b] != 0) continue;
       for (int i = tid; i < p.n_h * D; i += kThreads)
@@ -254,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lb0 + j <= lb1) mblk[j] = bt[lb0 + j];
       }
       const int cnt = min(32, n - base);
+      if (early && base == 0) {
+        pdl_wait();
+        pdl_trigger();
+      }
       bool stop = false;
       for (int j = 0; j < cnt && !stop; ++j) {
         const int b = __shfl_sync(0xffffffffu, mb, j);
@@ -345,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every unit of the range but the last: the consumer warps write the last
   // one themselves, all 256 threads at once, since nothing overlaps it.
   if (warp == kFinisher) {
+    if (early) pdl_wait();
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {
@@ -369,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumer warps =================================
+  if (early) pdl_wait();
   int cur_b = -1, cur_h = -1, n_flush = 0;
   float qf[G][E], m[G], l[G], o[G][E];
   const int hj = warp / C::WPH;  // this warp's head within the group
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int G, int DT, int HP>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   using C = Cfg<D, G, DT, HP>;
-  static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(C::SMEM <= 226 * 1024, "shared memory budget");
   static_assert(C::NS >= 2, "ring depth");
   auto kern = decode_simt_kernel<D, G, DT, HP>;
   static bool done[64] = {};  // one table per instantiation

@@ -18,6 +18,8 @@ enum : int {
 };
 
 enum : int { DT_BF16 = 0, DT_FP8 = 1 };
+// kvd_seqs flags (mirror of KVD_SEQS_STABLE in kvd.h).
+enum : int { FLAG_SEQS_STABLE = 1 };
 
 struct AppendParams {
   uint8_t *k_cache;  // [num_blocks][n_kv][block_size][head_dim]
@@ -56,6 +58,7 @@ struct DecodeParams {
   int32_t split_len;    // tokens (or index entries) per split
   int32_t n_splits;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
+  int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE)
   float scale_log2;  // softmax scale * log2(e)
   int *err;
 };

@@ -95,7 +95,7 @@ def oracle_dense_step(shape, paging, layer, seqs=None):
     return out, lse, (kr, vr)
 
 
-def device_step(wl, layer, lse=True):
+def device_step(wl, layer, lse=True, seqs_flags=0):
     """kv_append then the layer's decode through the C ABI."""
     import kv_cache_decode_gqa_gb300 as K
     s = wl.shape
@@ -106,4 +106,4 @@ def device_step(wl, layer, lse=True):
         return K.mla_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
                             wl.q[layer], d_c=s.d_c, want_lse=lse)
     return K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                        wl.q[layer], want_lse=lse)
+                        wl.q[layer], want_lse=lse, seqs_flags=seqs_flags)

@@ -75,6 +75,9 @@ def test_gqa_validation(lib):
     assert _gqa(lib, _cache(), _seqs(batch=-1)) == 2
     assert _gqa(lib, _cache(dtype=1), _seqs()) == 1       # fp8 needs scales
     assert _gqa(lib, _cache(), _seqs(batch=0)) == 0       # nothing to do
+    assert _gqa(lib, _cache(), _seqs(flags=2)) == 2       # unknown flag bit
+    assert b"flags" in lib.kvd_last_error()
+    assert _gqa(lib, _cache(), _seqs(batch=0, flags=1)) == 0  # STABLE is known
 
 
 def test_append_validation(lib):

@@ -107,6 +107,9 @@ DENSE_CASES = [
     ("gqa4_d64", 8, 2, 64, 64, [100, 256, 777]),
     ("gqa4_d128_bs32", 16, 4, 128, 32, [31, 32, 33, 1500]),
     ("mha_d64_bs320", 2, 2, 64, 320, [1, 319, 600]),
+    # head groups per copy: 2 (bf16, d 128) and 4 (fp8, or d 64)
+    ("mha_d64_bs64", 8, 8, 64, 64, [0, 64, 65, 900]),
+    ("gqa2_d128_bs64", 8, 4, 128, 64, [1, 200, 1000]),
     # tensor-core path: query groups of 8 and 16
     ("gqa8_bs64", 16, 2, 128, 64, [0, 1, 63, 64, 65, 500]),
     ("gqa16_bs16", 32, 2, 128, 16, [3, 100, 257]),
@@ -128,6 +131,23 @@ def test_gqa_decode_small(case, dtype):
     ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
     H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}")
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/{dtype}")
+
+
+@pytest.mark.parametrize("case", [c for c in DENSE_CASES if c[0] in
+                                  ("mha_d128", "gqa2_d128_bs64", "gqa8_bs64")],
+                         ids=lambda c: c[0])
+def test_gqa_decode_stable_seqs_flag(case):
+    """KVD_SEQS_STABLE moves the plan before the predecessor's completion;
+    results are those of the default order."""
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, n_h=n_h, n_kv=n_kv, head_dim=d)
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0, seqs_flags=K.SEQS_STABLE)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/stable")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/stable")
 
 
 def test_tiny_config_full():
