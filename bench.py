@@ -361,17 +361,19 @@ def build_step(K, wl, outs, wss):
             return
         for layer in wl.layers:
             c = wl.caches[layer]
-            K.kv_append(c, wl.block_table, wl.pos, wl.k_new[layer],
-                        wl.v_new.get(layer))
             if s.kind == "mla":
+                K.kv_append(c, wl.block_table, wl.pos, wl.k_new[layer])
                 K.mla_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
                              wl.q[layer], d_c=s.d_c, out=outs[layer],
                              workspace=wss[layer], want_lse=False)
             else:
-                K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                             wl.q[layer], out=outs[layer],
-                             workspace=wss[layer], want_lse=False,
-                             seqs_flags=K.SEQS_STABLE)
+                # the append rides in the decode's pass over the cache; the
+                # lengths and block tables are set before the step
+                K.gqa_append_decode(c, wl.block_table, wl.seq_lens,
+                                    wl.max_seq_len, wl.pos, wl.k_new[layer],
+                                    wl.v_new[layer], wl.q[layer],
+                                    out=outs[layer], workspace=wss[layer],
+                                    want_lse=False, seqs_flags=K.SEQS_STABLE)
     return step
 
 
@@ -397,6 +399,8 @@ def run_sparse_schedule(K, wl, outs, wss, events=None):
 
 
 def decode_only(K, wl, outs, wss, layer):
+    """The layer's attention call as the step issues it (GQA: the fused
+    append + decode; latent: the decode after its separate append)."""
     s = wl.shape
     c = wl.caches[layer]
     if s.kind == "mla":
@@ -404,9 +408,11 @@ def decode_only(K, wl, outs, wss, layer):
                      wl.q[layer], d_c=s.d_c, out=outs[layer],
                      workspace=wss[layer], want_lse=False)
     elif s.kind == "gqa":
-        K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                     wl.q[layer], out=outs[layer], workspace=wss[layer],
-                     want_lse=False, seqs_flags=K.SEQS_STABLE)
+        K.gqa_append_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
+                            wl.pos, wl.k_new[layer], wl.v_new[layer],
+                            wl.q[layer], out=outs[layer],
+                            workspace=wss[layer], want_lse=False,
+                            seqs_flags=K.SEQS_STABLE)
 
 
 def pack_inputs(torch, wl):
@@ -626,12 +632,16 @@ def profile_run(args, local):
 
 
 def launches(s):
-    """Kernels the library launches per step (append + decode per layer;
-    sparse: two appends, indexer score + select per Full/Reindex layer, one
-    gather decode per layer; split merges run inside the decode kernels)."""
+    """Kernels the library launches per step. GQA: the fused append + decode
+    and its split merge per layer; latent: append, decode and merge per
+    layer; sparse: two appends, indexer score + select per Full/Reindex
+    layer, gather decode + merge per layer. (Every workload here is split
+    over several CTAs, so every decode has its merge launch.)"""
     if s.kind == "sparse":
         sel = sum(1 for m in s.modes if m != "reuse")
-        return 2 + 2 * sel + s.n_layers
+        return 2 + 2 * sel + 2 * s.n_layers
+    if s.kind == "mla":
+        return 3 * s.n_layers
     return 2 * s.n_layers
 
 
@@ -654,8 +664,8 @@ def time_decode_kernel(torch, K, wl, outs, wss, args):
             else:
                 for l in layers:
                     c = wl.caches[l]
-                    K.kv_append(c, wl.block_table, wl.pos, wl.k_new[l],
-                                wl.v_new.get(l))
+                    if s.kind == "mla":
+                        K.kv_append(c, wl.block_table, wl.pos, wl.k_new[l])
                     evs[l][0].record()
                     decode_only(K, wl, outs, wss, l)
                     evs[l][1].record()

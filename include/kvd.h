@@ -125,11 +125,12 @@ typedef struct kvd_cache {
  * Kernels of this library may start while the kernel before them on the
  * stream is still running (programmatic dependent launch); they read their
  * inputs only after that kernel has completed. KVD_SEQS_STABLE declares that
- * block_table and seq_lens already hold their final values when the kernel
- * launched just before this call starts, and that no kernel still running
- * writes them (for example: they are set by host copies at the start of a
- * decode step and read by every layer). kvd_gqa_decode then reads them, and
- * plans its work, while that kernel finishes. Other calls ignore the flag.
+ * block_table and seq_lens (and, for kvd_gqa_append_decode, pos) already
+ * hold their final values when the kernel launched just before this call
+ * starts, and that no kernel still running writes them (for example: they
+ * are set by host copies at the start of a decode step and read by every
+ * layer). kvd_gqa_decode and kvd_gqa_append_decode then read them, and plan
+ * their work, while that kernel finishes. Other calls ignore the flag.
  */
 #define KVD_SEQS_STABLE 1
 typedef struct kvd_seqs {
@@ -195,6 +196,32 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                           const void *q, int32_t n_h, float scale, void *out,
                           float *lse, void *workspace, size_t workspace_bytes,
                           kvd_stream stream);
+
+/*
+ * kvd_gqa_append_decode -- kvd_kv_append(cache, seqs->block_table,
+ * seqs->max_blocks_per_seq, pos, seqs->batch, k_new, v_new) followed by
+ * kvd_gqa_decode(cache, seqs, q, ...), done in the decode's own pass over
+ * the cache: the CTA that copies the chunk holding pos[b] writes sequence
+ * b's new key and value rows just before it copies that chunk, and rows no
+ * chunk reads (pos[b] at or past the visible length) are written by one
+ * CTA. The My Weird Prompts 640482 transcript: the new token's key and value
+ * join the cache, and its query attends to the cache including them.
+ *
+ *   pos, k_new, v_new   as for kvd_kv_append (v_new required)
+ *   other arguments     as for kvd_gqa_decode; the same workspace size
+ * Cache contents, out and lse equal those of the two separate calls. The
+ * slot written for sequence b must not be visible to another sequence of
+ * the call (no two sequences share the block that receives a new row).
+ * Errors: those of both calls (KVD_ERR_NULL when pos is NULL and batch > 0);
+ * a position or block id out of range on the device is skipped and flagged
+ * as kvd_kv_append does.
+ */
+kvd_status kvd_gqa_append_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                                 const int32_t *pos, const void *k_new,
+                                 const void *v_new, const void *q, int32_t n_h,
+                                 float scale, void *out, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 kvd_stream stream);
 
 /*
  * kvd_gqa_decode_noalloc -- kvd_gqa_decode for callers that cannot allocate

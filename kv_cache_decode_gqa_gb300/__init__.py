@@ -173,6 +173,29 @@ def gqa_decode(cache, block_table, seq_lens, max_seq_len, q, scale=None,
     return out, lse
 
 
+def gqa_append_decode(cache, block_table, seq_lens, max_seq_len, pos, k_new,
+                      v_new, q, scale=None, out=None, lse=None,
+                      workspace=None, want_lse=True, stream=None,
+                      seqs_flags=0):
+    """kv_append then gqa_decode in one pass (kvd_gqa_append_decode)."""
+    import torch
+    _need(q, "q", torch.bfloat16)
+    _need(pos, "pos", torch.int32)
+    _need(k_new, "k_new", torch.bfloat16)
+    _need(v_new, "v_new", torch.bfloat16)
+    n_h = q.shape[1]
+    c = cache.struct()
+    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags)
+    out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
+    ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
+                    n_h, 0, workspace)
+    check(lib().kvd_gqa_append_decode(
+        ctypes.byref(c), ctypes.byref(s), _ptr(pos), _ptr(k_new), _ptr(v_new),
+        _ptr(q), n_h, float(scale or 0.0), _ptr(out), _ptr(lse), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out, lse
+
+
 def mla_decode(cache, block_table, seq_lens, max_seq_len, q, d_c=512,
                scale=None, out=None, lse=None, workspace=None, want_lse=True,
                stream=None):
@@ -240,6 +263,11 @@ def sparse_decode(cache, block_table, seq_lens, max_seq_len, indices, q,
 
 def bytes_per_token(n_l, n_kv, d_h, elem_bytes):
     return int(lib().kvd_bytes_per_token(n_l, n_kv, d_h, elem_bytes))
+
+
+# device error bits (KVD_DEVERR_* in kvd.h)
+DEVERR_BLOCK, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_LEN = (
+    1, 2, 4, 8, 16)
 
 
 def device_error():

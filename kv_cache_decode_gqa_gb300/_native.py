@@ -54,6 +54,10 @@ _SIGS = {
     "kvd_gqa_decode": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32, c_float,
                                  c_void_p, c_void_p, c_void_p, c_size_t,
                                  c_void_p]),
+    "kvd_gqa_append_decode": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_int32, c_float,
+                                        c_void_p, c_void_p, c_void_p,
+                                        c_size_t, c_void_p]),
     "kvd_gqa_decode_noalloc": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
                                          c_float, c_void_p, c_void_p,
                                          c_void_p]),

@@ -418,10 +418,16 @@ kvd_status kvd_workspace_size(kvd_op op, const kvd_cache *cache,
   return fail(KVD_ERR_UNSUPPORTED, "workspace_size: unknown op %d", (int)op);
 }
 
-kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
-                          const void *q, int32_t n_h, float scale, void *out,
-                          float *lse, void *workspace, size_t workspace_bytes,
-                          kvd_stream stream) {
+}  // extern "C"
+
+namespace {
+// kvd_gqa_decode, and kvd_gqa_append_decode when pos != nullptr.
+kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
+                           const int32_t *pos, const void *k_new,
+                           const void *v_new, const void *q, int32_t n_h,
+                           float scale, void *out, float *lse,
+                           void *workspace, size_t workspace_bytes,
+                           kvd_stream stream) {
   kvd_status st = check_cache(cache, true, "gqa_decode");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, cache, "gqa_decode");
@@ -438,6 +444,17 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   if (!q || !out) return fail(KVD_ERR_NULL, "gqa_decode: q and out required");
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(KVD_ERR_SHAPE, "gqa_decode: q and out must be 16-byte aligned");
+  if (pos) {
+    if (!k_new || !v_new)
+      return fail(KVD_ERR_NULL, "gqa_append_decode: k_new and v_new required");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+      return fail(KVD_ERR_SHAPE, "gqa_append_decode: k_new / v_new must be "
+                  "16-byte aligned");
+    if (cache->dtype == KVD_FP8_E4M3 &&
+        (!cache->k_inv_scale || !cache->v_inv_scale))
+      return fail(KVD_ERR_NULL,
+                  "gqa_append_decode: fp8 cache needs inverse scales");
+  }
   const DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != KVD_OK) return st;
@@ -474,6 +491,11 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.n_splits = pl.n_splits;
   p.hp = pl.hp;
   p.flags = seqs->flags;
+  p.pos = pos;
+  p.k_new = static_cast<const uint16_t *>(k_new);
+  p.v_new = static_cast<const uint16_t *>(v_new);
+  p.k_inv_scale = cache->k_inv_scale;
+  p.v_inv_scale = cache->v_inv_scale;
   p.scale_log2 = log2_scale(scale, cache->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -481,6 +503,29 @@ kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                       ? kvd::launch_decode_simt(p, s)
                       : kvd::launch_decode_mma(p, cache->dtype, s);
   return launched(e, "gqa_decode");
+}
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                          const void *q, int32_t n_h, float scale, void *out,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          kvd_stream stream) {
+  return gqa_decode_impl(cache, seqs, nullptr, nullptr, nullptr, q, n_h, scale,
+                         out, lse, workspace, workspace_bytes, stream);
+}
+
+kvd_status kvd_gqa_append_decode(const kvd_cache *cache, const kvd_seqs *seqs,
+                                 const int32_t *pos, const void *k_new,
+                                 const void *v_new, const void *q, int32_t n_h,
+                                 float scale, void *out, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 kvd_stream stream) {
+  if (!pos && seqs && seqs->batch > 0)
+    return fail(KVD_ERR_NULL, "gqa_append_decode: pos required");
+  return gqa_decode_impl(cache, seqs, pos, k_new, v_new, q, n_h, scale, out,
+                         lse, workspace, workspace_bytes, stream);
 }
 
 kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,

@@ -10,15 +10,6 @@
 
 namespace kvd {
 
-__device__ __forceinline__ uint16_t e4m3x2_from_f32(float first, float second) {
-  uint16_t r;
-  // cvt puts its first source operand in the upper byte.
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-      : "=h"(r)
-      : "f"(second), "f"(first));
-  return r;
-}
-
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   pdl_trigger();
   pdl_wait();
@@ -47,27 +38,11 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const long row = ((long)blk * p.n_kv + h) * p.block_size + pos % p.block_size;
   const uint16_t *src = (is_v ? p.v_new : p.k_new) +
                         ((long)b * p.n_kv + h) * p.head_dim + c * 8;
-  const uint4 x = *reinterpret_cast<const uint4 *>(src);
   uint8_t *cache = is_v ? p.v_cache : p.k_cache;
-
-  if (p.dtype == DT_BF16) {
-    *reinterpret_cast<uint4 *>(cache + (row * p.head_dim + c * 8) * 2) = x;
-  } else {
-    const float inv = (is_v ? p.v_inv_scale : p.k_inv_scale)[h];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t packed[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint16_t a = e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j]), inv),
-                                         __fmul_rn(bf16hi(w[2 * j]), inv));
-      const uint16_t bb =
-          e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j + 1]), inv),
-                          __fmul_rn(bf16hi(w[2 * j + 1]), inv));
-      packed[j] = (uint32_t)a | ((uint32_t)bb << 16);
-    }
-    *reinterpret_cast<uint2 *>(cache + row * p.head_dim + c * 8) =
-        make_uint2(packed[0], packed[1]);
-  }
+  const int es = p.dtype == DT_BF16 ? 2 : 1;
+  const float inv =
+      p.dtype == DT_BF16 ? 1.0f : (is_v ? p.v_inv_scale : p.k_inv_scale)[h];
+  store_new8(cache + (row * p.head_dim + c * 8) * es, src, p.dtype, inv);
 }
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {

@@ -37,6 +37,8 @@
 namespace kvd {
 namespace {
 
+constexpr int kAppendBar = 1;  // finisher -> producer: fused-append rows written
+
 constexpr int kD = 128;
 constexpr int kWarps = 4;                 // consumer warps
 constexpr int kConsumers = kWarps * 32;
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (c == 0) {
     if (early) pdl_wait();
+    if (p.pos && warp == 0) append_unread_rows(p, wp, lane);
     for (int b = 0; b < p.batch; ++b) {
       if (wp.nch[b] != 0) continue;
       for (int i = tid; i < p.n_h * kD; i += kThreads)
@@ -170,13 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t policy = policy_evict_first();
     const int br = min(64, p.block_size);  // rows per box (one block piece)
+    bool appended = false;  // fused append: the finisher's rows are written
     const int npiece = 64 / br;            // <= 4 (block_size >= 16)
     for (int base = 0; base < n; base += 32) {
       const int mine = base + lane;
       int mb = 0, mh = 0, mk = 0, mrows = 0, mblk[4] = {0, 0, 0, 0};
+      int mpos = -1;  // fused append: the sequence's new slot
       if (mine < n) {
         const ChunkCursor cur = cursor_at(wp, p.batch, lo + mine);
         mb = cur.b, mh = cur.h, mk = cur.k;
+        if (p.pos) mpos = p.pos[mb];
         const int tok = mk * kStageRows;
         mrows = min(kStageRows, wp.len[mb] - tok);
         const int32_t *bt = p.block_table + (long)mb * p.max_blocks;
@@ -199,6 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int blk[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) blk[t] = __shfl_sync(0xffffffffu, mblk[t], j);
+        if (p.pos && !appended) {
+          // fused append: before the first chunk holding a new row is
+          // copied, wait for the finisher to have written this CTA's rows
+          const int P = __shfl_sync(0xffffffffu, mpos, j);
+          const int tok = k * kStageRows;
+          if (P >= tok && P < tok + rows) {
+            named_sync(kAppendBar, 64);
+            appended = true;
+          }
+        }
         int go = 1;
         if (lane == 0) {
           const int i = base + j;
@@ -240,13 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (stop) break;
     }
+    if (p.pos && !appended) named_sync(kAppendBar, 64);
     if (lane == 0) s_producer_done = 1;
     return;
   }
 
   // ======================= finisher warp ==================================
   if (warp == kFinisher) {
-    if (early) pdl_wait();
+    if (p.pos) {  // fused append: the new rows this CTA's chunks hold
+      append_range_rows(p, wp, 1, lo, hi, lane, early);
+      named_arrive(kAppendBar, 64);
+    } else if (early) {
+      pdl_wait();
+    }
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {

@@ -51,6 +51,7 @@ constexpr int kProducer = kWarps;          // warp index of the producer
 constexpr int kFinisher = kWarps + 1;      // warp index of the finisher
 constexpr int kThreads = kConsumers + 64;
 constexpr int kFinalBar = 1;               // the consumer warps, at the end
+constexpr int kAppendBar = 2;              // finisher -> producer: rows written
 
 template <int D, int G, int DT, int HP>
 struct Cfg {
@@ -179,9 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = min((int)gridDim.x, max(total, 1));
   const int c = blockIdx.x;
 
-  // sequences with nothing visible: out = 0, lse = -inf
+  // sequences with nothing visible: out = 0, lse = -inf; fused-append rows
+  // that no chunk reads
   if (c == 0) {
     if (early) pdl_wait();
+    if (p.pos && warp == 0) append_unread_rows(p, wp, lane);
     for (int b = 0; b < p.batch; ++b) {
       if (wp.nch[b] != 0) continue;
       for (int i = tid; i < p.n_h * D; i += kThreads)
@@ -253,12 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducer) {
     const uint64_t policy = policy_evict_first();
     constexpr int kPre = 4;  // block ids prefetched per chunk
+    bool appended = false;   // fused append: the finisher's rows are written
     for (int base = 0; base < n; base += 32) {
       const int mine = base + lane;
       int mb = 0, mh = 0, mk = 0, mrows = 0, mblk[kPre] = {0, 0, 0, 0};
+      int mpos = -1;  // fused append: the sequence's new slot
       if (mine < n) {
         const ChunkCursor cur = cursor_at(wp, p.batch, lo + mine);
         mb = cur.b, mh = cur.h, mk = cur.k;
+        if (p.pos) mpos = p.pos[mb];
         const int tok = mk * kStageRows;
         mrows = min(kStageRows, wp.len[mb] - tok);
         const int lb0 = tok / p.block_size;
@@ -283,6 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kPre; ++t)
           blk[t] = __shfl_sync(0xffffffffu, mblk[t], j);
+        if (p.pos && !appended) {
+          // fused append: before the first chunk holding a new row is
+          // copied, wait for the finisher to have written this CTA's rows
+          const int P = __shfl_sync(0xffffffffu, mpos, j);
+          const int tok = k * kStageRows;
+          if (P >= tok && P < tok + rows) {
+            named_sync(kAppendBar, 64);
+            appended = true;
+          }
+        }
         int go = 1;
         if (lane == 0) {
           const int i = base + j;
@@ -356,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (stop) break;
     }
+    if (p.pos && !appended) named_sync(kAppendBar, 64);
     if (lane == 0) s_producer_done = 1;
     return;
   }
@@ -364,7 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every unit of the range but the last: the consumer warps write the last
   // one themselves, all 256 threads at once, since nothing overlaps it.
   if (warp == kFinisher) {
-    if (early) pdl_wait();
+    if (p.pos) {  // fused append: the new rows this CTA's chunks hold
+      append_range_rows(p, wp, HP, lo, hi, lane, early);
+      named_arrive(kAppendBar, 64);
+    } else if (early) {
+      pdl_wait();
+    }
     ChunkCursor fc = cursor_at(wp, p.batch, lo);
     int x = lo;
     for (int e = 0; x < hi; ++e) {

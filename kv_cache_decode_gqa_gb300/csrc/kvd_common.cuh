@@ -223,6 +223,11 @@ __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive at named barrier `id` (of `count` threads) without waiting.
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
@@ -290,6 +295,47 @@ __device__ __forceinline__ float f16lo(uint32_t u) {
 }
 __device__ __forceinline__ float f16hi(uint32_t u) {
   return f16_to_f32(static_cast<uint16_t>(u >> 16));
+}
+
+// Two floats -> two E4M3 codes (first in the low byte), round to nearest
+// even, saturating to +-448 (the hardware's satfinite conversion).
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float first, float second) {
+  uint16_t r;
+  // cvt puts its first source operand in the upper byte.
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(r)
+      : "f"(second), "f"(first));
+  return r;
+}
+
+// One 8-element piece of a new key or value row into the cache: the 16
+// bytes of bf16 unchanged, or (fp8) E4M3(x * inv) with the product rounded
+// once to fp32. `src` holds 8 bf16 elements; `dst` is 16 (bf16) or 8 (fp8)
+// bytes of the cached row.
+__device__ __forceinline__ void store_new8(uint8_t *dst, const uint16_t *src,
+                                           int dtype, float inv) {
+  const uint4 x = *reinterpret_cast<const uint4 *>(src);
+  if (dtype == DT_BF16) {
+    *reinterpret_cast<uint4 *>(dst) = x;
+  } else {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t packed[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint16_t a = e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j]), inv),
+                                         __fmul_rn(bf16hi(w[2 * j]), inv));
+      const uint16_t b = e4m3x2_from_f32(__fmul_rn(bf16lo(w[2 * j + 1]), inv),
+                                         __fmul_rn(bf16hi(w[2 * j + 1]), inv));
+      packed[j] = (uint32_t)a | ((uint32_t)b << 16);
+    }
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+  }
+}
+
+// Orders this thread's generic-proxy global-memory writes before later
+// async-proxy (copy engine) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Opt a kernel into `bytes` of dynamic shared memory, once per device (the

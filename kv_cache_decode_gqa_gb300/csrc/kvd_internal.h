@@ -59,6 +59,13 @@ struct DecodeParams {
   int32_t n_splits;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
   int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE)
+  // fused append (kvd_gqa_append_decode), else pos == nullptr: the new key
+  // and value rows, bf16 [batch][n_kv][dk], written at slot pos[b]
+  const int32_t *pos;
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  const float *k_inv_scale;
+  const float *v_inv_scale;
   float scale_log2;  // softmax scale * log2(e)
   int *err;
 };

@@ -157,6 +157,117 @@ __device__ __forceinline__ int partial_side(int ustart, int lo) {
   return ustart < lo ? 0 : 1;
 }
 
+// ---------------------------------------------------------------------------
+// fused append (kvd_gqa_append_decode)
+// ---------------------------------------------------------------------------
+// The calling warp writes the new key and value rows of kv heads
+// [h0, h0 + nh) of sequence b into slot P of physical block pb (checked by
+// the caller), lane-parallel over 8-element pieces, and each lane orders
+// its writes before later copy-engine reads of the same rows.
+__device__ __forceinline__ void append_rows(const DecodeParams &p, int b,
+                                            int h0, int nh, int P, int pb,
+                                            int lane) {
+  const int D = p.dk, pieces = D / 8, es = p.dtype == DT_BF16 ? 2 : 1;
+  for (int e = lane; e < 2 * nh * pieces; e += 32) {
+    const bool is_v = e >= nh * pieces;
+    const int r = is_v ? e - nh * pieces : e;
+    const int h = h0 + r / pieces, c8 = r % pieces;
+    const uint16_t *src =
+        (is_v ? p.v_new : p.k_new) + ((long)b * p.n_kv + h) * D + c8 * 8;
+    const long row =
+        ((long)pb * p.n_kv + h) * p.block_size + P % p.block_size;
+    uint8_t *dst = const_cast<uint8_t *>(is_v ? p.v : p.k) +
+                   (row * D + c8 * 8) * es;
+    const float inv = p.dtype == DT_BF16
+                          ? 1.0f
+                          : (is_v ? p.v_inv_scale : p.k_inv_scale)[h];
+    store_new8(dst, src, p.dtype, inv);
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
+// The fused-append rows that this CTA's chunk range [lo, hi) will read:
+// for every unit (b, h) the range touches whose sequence's new slot pos[b]
+// is visible and lies in one of the range's chunks, the calling warp writes
+// the unit's `nh` kv heads' rows (a block id out of range is left to the
+// copy of that chunk to flag). Units are taken 32 at a time: a walk of the
+// partition gives lane j the j-th unit, the lanes load their slots and
+// block ids together, then the warp writes the rows unit by unit. With
+// `wait_first` (stable metadata) the loads of the first 32 units run before
+// the grid dependency wait and the writes after it. Run by a warp that
+// issues no copies, before the producer copies the first such chunk.
+template <int NB>
+__device__ __forceinline__ void append_range_rows(
+    const DecodeParams &p, const WorkPartitionT<NB> &wp, int nh, int lo,
+    int hi, int lane, bool wait_first) {
+  int x = lo;
+  bool waited = !wait_first;
+  do {
+    int mb = -1, mh = 0, mstart = 0;
+    for (int j = 0; j < 32 && x < hi; ++j) {  // warp-uniform, shared memory
+      const ChunkCursor u = cursor_at(wp, p.batch, x);
+      const int ustart = wp.pre[u.b] + u.h * wp.nch[u.b];
+      if (lane == j) mb = u.b, mh = u.h, mstart = ustart;
+      x = min(ustart + wp.nch[u.b], hi);
+    }
+    int P = -1, pb = -1;
+    if (mb >= 0) {
+      P = p.pos[mb];
+      const int xp = mstart + P / kStageRows;  // the chunk holding P
+      if (P >= 0 && P < wp.len[mb] && xp >= lo && xp < hi)
+        pb = p.block_table[(long)mb * p.max_blocks + P / p.block_size];
+    }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    unsigned todo = __ballot_sync(0xffffffffu, pb >= 0 && pb < p.num_blocks);
+    while (todo) {
+      const int j = __ffs(todo) - 1;
+      todo &= todo - 1;
+      append_rows(p, __shfl_sync(0xffffffffu, mb, j),
+                  __shfl_sync(0xffffffffu, mh, j) * nh, nh,
+                  __shfl_sync(0xffffffffu, P, j),
+                  __shfl_sync(0xffffffffu, pb, j), lane);
+    }
+  } while (x < hi);
+}
+
+// Rows of the fused append that no chunk of this launch reads (a slot at or
+// past the visible length, an empty sequence) or that are out of range: one
+// warp of CTA 0 writes the former and flags the latter, as kv_append does.
+// Visible rows are written by the producer that copies their chunk.
+template <int NB>
+__device__ __forceinline__ void append_unread_rows(
+    const DecodeParams &p, const WorkPartitionT<NB> &wp, int lane) {
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int P = 0, need = 0;
+    if (b < p.batch) {
+      P = p.pos[b];
+      need = !(P >= 0 && P < wp.len[b]);
+    }
+    unsigned todo = __ballot_sync(0xffffffffu, need);
+    while (todo) {
+      const int j = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int bj = b0 + j;
+      const int Pj = __shfl_sync(0xffffffffu, P, j);
+      if (Pj < 0 || Pj >= p.max_blocks * p.block_size) {
+        if (lane == 0) report(p.err, DEVERR_POS);
+        continue;
+      }
+      const int pb = p.block_table[(long)bj * p.max_blocks + Pj / p.block_size];
+      if (pb < 0 || pb >= p.num_blocks) {
+        if (lane == 0) report(p.err, DEVERR_BLOCK);
+        continue;
+      }
+      append_rows(p, bj, 0, p.n_kv, Pj, pb, lane);
+    }
+  }
+}
+
 // Log-sum-exp merge of the units a dense decode launch cut between CTAs,
 // run as a second launch right after it (programmatic dependent launch, so
 // its CTAs are resident and waiting when the decode grid completes). Each

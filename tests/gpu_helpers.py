@@ -95,11 +95,17 @@ def oracle_dense_step(shape, paging, layer, seqs=None):
     return out, lse, (kr, vr)
 
 
-def device_step(wl, layer, lse=True, seqs_flags=0):
-    """kv_append then the layer's decode through the C ABI."""
+def device_step(wl, layer, lse=True, seqs_flags=0, fused=False):
+    """kv_append then the layer's decode through the C ABI (or, fused, the
+    single kvd_gqa_append_decode call)."""
     import kv_cache_decode_gqa_gb300 as K
     s = wl.shape
     c = wl.caches[layer]
+    if fused:
+        return K.gqa_append_decode(c, wl.block_table, wl.seq_lens,
+                                   wl.max_seq_len, wl.pos, wl.k_new[layer],
+                                   wl.v_new[layer], wl.q[layer], want_lse=lse,
+                                   seqs_flags=seqs_flags)
     K.kv_append(c, wl.block_table, wl.pos, wl.k_new[layer],
                 wl.v_new.get(layer))
     if s.kind == "mla":

@@ -38,7 +38,7 @@ def _seqs(**kw):
 
 def test_exports_every_declared_function(lib):
     names = N.header_functions()
-    assert len(names) == 12
+    assert len(names) == 13
     for name in names:
         assert hasattr(lib, name), name
     assert lib.kvd_version() == 1
@@ -78,6 +78,22 @@ def test_gqa_validation(lib):
     assert _gqa(lib, _cache(), _seqs(flags=2)) == 2       # unknown flag bit
     assert b"flags" in lib.kvd_last_error()
     assert _gqa(lib, _cache(), _seqs(batch=0, flags=1)) == 0  # STABLE is known
+
+
+def _append_decode(lib, c, s, pos=FAKE, k_new=FAKE, v_new=FAKE):
+    return lib.kvd_gqa_append_decode(ctypes.byref(c), ctypes.byref(s), pos,
+                                     k_new, v_new, FAKE, 64, 0.0, FAKE, None,
+                                     None, 0, None)
+
+
+def test_append_decode_validation(lib):
+    assert _append_decode(lib, _cache(), _seqs(), pos=None) == 1
+    assert b"pos" in lib.kvd_last_error()
+    assert _append_decode(lib, _cache(), _seqs(), v_new=None) == 1
+    assert _append_decode(lib, _cache(), _seqs(), k_new=FAKE + 4) == 2
+    assert _append_decode(lib, _cache(dtype=1, k_scale=FAKE, v_scale=FAKE),
+                          _seqs()) == 1                   # no inverse scales
+    assert _append_decode(lib, _cache(), _seqs(batch=0), pos=None) == 0
 
 
 def test_append_validation(lib):

@@ -150,6 +150,59 @@ def test_gqa_decode_stable_seqs_flag(case):
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/stable")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("case", DENSE_CASES, ids=[c[0] for c in DENSE_CASES])
+def test_append_decode_fused(case, dtype):
+    """kvd_gqa_append_decode: the cache bytes of kv_append (every block,
+    canaries included) and the outputs of the decode that follows it."""
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=d)
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0, fused=True)
+    torch.cuda.synchronize()
+    ref, ref_lse, (kr, vr) = H.oracle_dense_step(s, wl.paging, 0)
+    c = wl.caches[0]
+    assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr)), name
+    assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr)), name
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}/fused")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/{dtype}/fused")
+
+
+def test_append_decode_unread_rows_and_bad_positions():
+    """Rows no chunk reads (an empty sequence, a slot at the visible length)
+    are written all the same; a position out of range is skipped and
+    flagged, as kv_append does."""
+    s = W.config("llama2_7b_mha", batch=4, lengths=[0, 100, 5, 40],
+                 n_layers=1, n_h=4, n_kv=4)
+    wl = W.DeviceWorkload(s, layers=[0])
+    c = wl.caches[0]
+    lens = torch.tensor([0, 100, 6, 41], dtype=torch.int32, device="cuda")
+    pos = wl.pos.clone()
+    pos[3] = -1                                   # out of range: skipped
+    out, lse = K.gqa_append_decode(c, wl.block_table, lens, s.max_seq_len,
+                                   pos, wl.k_new[0], wl.v_new[0], wl.q[0])
+    torch.cuda.synchronize()
+    assert K.device_error() == K.DEVERR_POS
+    kr = W.host_cache_full(s, wl.paging, 0, W.T_K)
+    vr = W.host_cache_full(s, wl.paging, 0, W.T_V)
+    kn = H.host_bits(s, 0, W.T_KNEW, (s.batch, s.n_kv, s.head_dim))
+    vn = H.host_bits(s, 0, W.T_VNEW, (s.batch, s.n_kv, s.head_dim))
+    bt = wl.paging.table
+    # the oracle appends sequences 0..2 only (sequence 3's slot is invalid)
+    kr = oracle.kv_append(kr, bt[:3], [0, 100, 5], kn[:3], s.block_size)
+    vr = oracle.kv_append(vr, bt[:3], [0, 100, 5], vn[:3], s.block_size)
+    assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr))
+    assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr))
+    q = oracle.bf16_bits_to_f64(H.host_bits(s, 0, W.T_Q,
+                                            (s.batch, s.n_h, s.head_dim)))
+    ref, ref_lse = oracle.gqa_decode(q, kr, vr, bt, [0, 100, 6, 41],
+                                     s.block_size)
+    H.assert_close(H.to_np_bf16(out), ref, "unread rows")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, "unread rows")
+
+
 def test_tiny_config_full():
     s = W.config("tiny_gqa")
     wl = W.DeviceWorkload(s)
@@ -215,23 +268,27 @@ def test_workspace_errors():
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences, the bench's launch configuration
 # ---------------------------------------------------------------------------
-def test_llama2_7b_full_size_sampled_layers():
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_llama2_7b_full_size_sampled_layers(fused):
     s = W.config("llama2_7b_mha")
     wl = W.DeviceWorkload(s, layers=[0, 31])
     for layer in (0, 31):
-        out, lse = H.device_step(wl, layer)
+        out, lse = H.device_step(wl, layer, fused=fused,
+                                 seqs_flags=K.SEQS_STABLE if fused else 0)
         torch.cuda.synchronize()
         ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, layer, seqs=[0])
         H.assert_close(H.to_np_bf16(out), ref, f"llama2 layer {layer}")
         H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"layer {layer}")
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 @pytest.mark.parametrize("name", ["llama31_70b_gqa", "llama31_70b_gqa_fp8"])
-def test_llama31_70b_full_size_sampled(name):
+def test_llama31_70b_full_size_sampled(name, fused):
     s = W.config(name)
     wl = W.DeviceWorkload(s, layers=[0])
     try:
-        out, lse = H.device_step(wl, 0)
+        out, lse = H.device_step(wl, 0, fused=fused,
+                                 seqs_flags=K.SEQS_STABLE if fused else 0)
     except K.KvdError as e:
         if e.status == 3:
             pytest.skip(f"{name}: kernel not built yet")
