@@ -59,15 +59,22 @@ struct MCfg {
   static constexpr int NBOX = ROW / 128;     // 128-byte boxes per row
   static constexpr int BOX = 64 * 128;       // one box of a full chunk
   static constexpr int STAGE = 64 * ROW;     // K (or V) bytes per chunk
-  static constexpr int NS = DT == DT_BF16 ? 3 : 5;
   static constexpr int QB = 16 * kD * 2;     // query rows of a chunk
-  static constexpr int RING = 2 * NS * STAGE + NS * QB;
   static constexpr int SLOT = kWarps * 16 * (kD + 2);  // floats per slot
-  static constexpr int MERGE = 2 * SLOT * 4;
+  // One flush slot (units span tens of chunks here, so the finisher is long
+  // done with a unit before the next one ends); the rest of 226 KB is ring,
+  // as deep as fits: the bytes in flight per SM are what keep HBM busy.
+  static constexpr int NSLOT = 1;
+  static constexpr int MERGE = NSLOT * SLOT * 4;
+  static constexpr int FIXED =
+      MERGE + (int)sizeof(WorkPartition) + 16 + 40 * 8 + 1024;
+  static constexpr int NS_FIT = (226 * 1024 - FIXED) / (2 * STAGE + QB);
+  static constexpr int NS = NS_FIT > 12 ? 12 : NS_FIT;
+  static constexpr int RING = 2 * NS * STAGE + NS * QB;
   static constexpr int WP_OFF = RING + MERGE;
   static constexpr int BAR_OFF =
       (WP_OFF + (int)sizeof(WorkPartition) + 15) / 16 * 16;
-  static constexpr int SMEM = BAR_OFF + (2 * NS + 4) * 8;
+  static constexpr int SMEM = BAR_OFF + (2 * NS + 2 * NSLOT) * 8;
 };
 
 // Shared-memory address of byte `cb` (0..127) of row `r` of a 128-byte
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
   uint64_t *empty = full + C::NS;
   uint64_t *sfull = empty + C::NS;
-  uint64_t *sempty = sfull + 2;
+  uint64_t *sempty = sfull + C::NSLOT;
   __shared__ int s_len_err;
   __shared__ volatile int s_abort, s_issued, s_producer_done;
 
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&sfull[s], kWarps);
       mbar_init(&sempty[s], 1);
     }
@@ -276,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ustart = wp.pre[b] + h * wp.nch[b];
       const int uend = ustart + wp.nch[b];
       const int xend = min(uend, hi);
-      const int sl = e & 1;
-      if (!mbar_wait(&sfull[sl], (e >> 1) & 1)) {
+      const int sl = e % C::NSLOT;
+      if (!mbar_wait(&sfull[sl], (e / C::NSLOT) & 1)) {
         if (lane == 0) report(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
         break;
@@ -368,9 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int sl = n_flush & 1;
-    if (n_flush >= 2) {
-      bool ok = !s_abort && mbar_wait(&sempty[sl], ((n_flush >> 1) - 1) & 1);
+    const int sl = n_flush % C::NSLOT;
+    if (n_flush >= C::NSLOT) {
+      bool ok = !s_abort &&
+                mbar_wait(&sempty[sl], (n_flush / C::NSLOT - 1) & 1);
       if (!__all_sync(0xffffffffu, ok) && lane == 0) {
         if (!s_abort) report(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
@@ -603,7 +611,8 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long rows, bool fp8,
 template <int DT>
 cudaError_t launch_t(const MmaParams &mp, cudaStream_t s) {
   using C = MCfg<DT>;
-  static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(C::SMEM <= 226 * 1024, "shared memory budget");
+  static_assert(C::NS >= 2, "ring depth");
   auto kern = decode_mma_kernel<DT>;
   static bool done[64] = {};
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
