@@ -25,14 +25,11 @@
 // order of its terms); for V the output columns come out permuted and are
 // put back in order when the state is flushed. The V scale multiplies the
 // final output.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cmath>
-#include <mutex>
 
 #include "kvd_common.cuh"
 #include "stream_k.cuh"
+#include "tmap.h"
 
 namespace kvd {
 namespace {
@@ -576,21 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side: tensor maps
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-cudaError_t get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                         cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode ? cudaSuccess : cudaErrorNotSupported;
-}
 
 // The cache as a 2-D tensor [num_blocks * n_kv * block_size][head_dim],
 // copied in boxes of 128-byte rows x `box_rows` rows, 128-byte swizzle.
@@ -600,7 +582,7 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long rows, bool fp8,
   const cuuint64_t strides[1] = {(cuuint64_t)kD * (fp8 ? 1 : 2)};
   const cuuint32_t box[2] = {(cuuint32_t)(fp8 ? 128 : 64), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(
+  const CUresult r = tensor_map_encoder()(
       m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
       2, const_cast<void *>(base), dims, strides, box, estr,
       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -637,8 +619,8 @@ cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
     return cudaErrorNotSupported;
   const long rows = (long)p.num_blocks * p.n_kv * p.block_size;
   if (rows >= (1L << 31)) return cudaErrorNotSupported;
-  cudaError_t e = get_encoder();
-  if (e != cudaSuccess) return e;
+  if (!tensor_map_encoder()) return cudaErrorNotSupported;
+  cudaError_t e;
   MmaParams mp;
   mp.p = p;
   const bool fp8 = dtype == DT_FP8;
