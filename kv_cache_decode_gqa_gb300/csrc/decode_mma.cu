@@ -231,10 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (go) {
             const int tok = k * kStageRows;
             const int pieces = (rows + br - 1) / br;  // only visible blocks
+            // the query rows travel only with a unit's first chunk here (the
+            // consumers read them when the unit starts)
+            const bool qrows = i == 0 || k == 0;
             mbar_arrive_expect_tx(
-                &full[s], 2u * pieces * br * C::ROW + (uint32_t)G * kD * 2);
-            bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * G) * kD,
-                     G * kD * 2, &full[s]);
+                &full[s], 2u * pieces * br * C::ROW +
+                              (qrows ? (uint32_t)G * kD * 2 : 0u));
+            if (qrows)
+              bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * G) * kD,
+                       G * kD * 2, &full[s]);
             for (int pc = 0; pc < pieces; ++pc) {
               const int t = tok + pc * br;
               int pb = blk[pc];

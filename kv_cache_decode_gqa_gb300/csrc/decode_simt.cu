@@ -310,10 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (s_abort) go = 0;
           if (go) {
             const int tok = k * kStageRows;
-            mbar_arrive_expect_tx(&full[s],
-                                  2u * HP * rows * C::ROW + C::QB);
-            bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * D,
-                     C::QB, &full[s]);
+            // the query rows travel only with a unit's first chunk here (the
+            // consumers read them when the unit starts)
+            const bool qrows = i == 0 || k == 0;
+            mbar_arrive_expect_tx(&full[s], 2u * HP * rows * C::ROW +
+                                                (qrows ? C::QB : 0u));
+            if (qrows)
+              bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * D,
+                       C::QB, &full[s]);
             const int32_t *bt = p.block_table + (long)b * p.max_blocks;
             const int lb0 = tok / p.block_size;
             if constexpr (HP > 1) {
