@@ -188,7 +188,8 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
   const int hp = kind == DenseKernel::Simt
                      ? kvd::simt_heads_per_stage(c->n_kv, g, c->head_dim,
                                                  c->dtype, c->block_size)
-                     : 1;
+                     : kvd::mma_heads_per_unit(c->n_kv, c->block_size,
+                                               c->dtype);
   Plan pl = plan_stream_k(sms, 1, s->batch, c->n_kv / hp, g * hp,
                           c->head_dim, s->max_seq_len);
   pl.hp = hp;

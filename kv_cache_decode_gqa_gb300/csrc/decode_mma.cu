@@ -7,12 +7,16 @@
 // (m16n8k16, fp32 accumulators) is enough to keep the kernel bound by HBM.
 //
 // Same persistent stream-K structure as the CUDA-core kernel (stream_k.cuh):
-// one CTA per SM with an equal share of all (sequence, kv head, 64-token
-// chunk) work, a producer warp, a finisher warp, and consumers here made of
-// four warps that each take 16 tokens of every chunk. The producer moves
-// K and V with tiled TMA copies (boxes of 128-byte rows, 128-byte swizzle),
-// so the ldmatrix reads of every 8x8 tile are free of bank conflicts, and
-// copies the G query rows of the chunk's kv head beside them.
+// one CTA per SM with an equal share of all (sequence, head group, 64-token
+// chunk) work, a producer warp, a finisher warp, and four consumer warps.
+// A head group is HP consecutive kv heads (HP = 2 for an fp8 cache with
+// 64-token blocks, whose HP heads' rows are adjacent): the producer moves a
+// chunk's K and V with tiled TMA copies of HP x 64 rows (boxes of 128-byte
+// rows, 128-byte swizzle, so the ldmatrix reads of every 8x8 tile are free
+// of bank conflicts) -- few large copies, which the copy engine streams
+// much faster than many small ones -- and, with a unit's first chunk, the
+// HP x G query rows. 4 / HP consumer warps take each head, 16 HP tokens of
+// it per warp.
 //
 // Per chunk a consumer warp computes S = Q K^T for its 16 tokens (query
 // heads on the MMA's M = 16 rows; G = 8 leaves rows 8..15 at zero), scales
@@ -49,14 +53,17 @@ struct MmaParams {
   CUtensorMap tmv;
 };
 
-template <int DT>
+template <int DT, int HP>
 struct MCfg {
   static constexpr int ES = DT == DT_BF16 ? 2 : 1;
   static constexpr int ROW = kD * ES;        // bytes per cached row
-  static constexpr int NBOX = ROW / 128;     // 128-byte boxes per row
-  static constexpr int BOX = 64 * 128;       // one box of a full chunk
-  static constexpr int STAGE = 64 * ROW;     // K (or V) bytes per chunk
-  static constexpr int QB = 16 * kD * 2;     // query rows of a chunk
+  static constexpr int NBOX = ROW / 128;     // 128-byte column boxes per row
+  static constexpr int BOX = HP * 64 * 128;  // one column box of a chunk
+  static constexpr int STAGE = HP * 64 * ROW;  // K (or V) bytes per chunk
+  static constexpr int QB = HP * 16 * kD * 2;  // query rows of a unit
+  static constexpr int WPH = kWarps / HP;    // consumer warps per head
+  static constexpr int TPW = 64 / WPH;       // tokens per warp and chunk
+  static constexpr int NSUB = TPW / 16;      // 16-token tiles per warp
   static constexpr int SLOT = kWarps * 16 * (kD + 2);  // floats per slot
   // One flush slot (units span tens of chunks here, so the finisher is long
   // done with a unit before the next one ends); the rest of 226 KB is ring,
@@ -95,10 +102,10 @@ __device__ __forceinline__ uint32_t f16pair_from_bf16(uint32_t u) {
   return pack_f16x2(bf16lo(u), bf16hi(u));
 }
 
-template <int DT>
+template <int DT, int HP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mma_kernel(const __grid_constant__ MmaParams mp) {
-  using C = MCfg<DT>;
+  using C = MCfg<DT, HP>;
   const DecodeParams &p = mp.p;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sk = smem;
@@ -114,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int s_abort, s_issued, s_producer_done;
 
   const int G = p.n_h / p.n_kv;  // 8 or 16 (checked by the launcher)
+  const int GU = HP * G;         // query heads per unit
+  const int n_units = p.n_kv / HP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // With stable lengths and block table, the plan and the producer's first
   // block-id lookups run before the predecessor grid completes; every other
@@ -133,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_producer_done = 0;
   }
   __syncthreads();
-  build_partition(wp, p, &s_len_err);
+  build_partition(wp, p, &s_len_err, kStageRows, n_units);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
   const int P = min((int)gridDim.x, max(total, 1));
@@ -176,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&mp.tmv);
     }
     const uint64_t policy = policy_evict_first();
-    const int br = min(64, p.block_size);  // rows per box (one block piece)
+    // rows per box: one block piece (a head group needs 64-token blocks)
+    const int br = HP > 1 ? 64 : min(64, p.block_size);
     bool appended = false;  // fused append: the finisher's rows are written
     const int npiece = 64 / br;            // <= 4 (block_size >= 16)
     for (int base = 0; base < n; base += 32) {
@@ -235,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // consumers read them when the unit starts)
             const bool qrows = i == 0 || k == 0;
             mbar_arrive_expect_tx(
-                &full[s], 2u * pieces * br * C::ROW +
-                              (qrows ? (uint32_t)G * kD * 2 : 0u));
+                &full[s], 2u * HP * pieces * br * C::ROW +
+                              (qrows ? (uint32_t)GU * kD * 2 : 0u));
             if (qrows)
-              bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * G) * kD,
-                       G * kD * 2, &full[s]);
+              bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * kD,
+                       GU * kD * 2, &full[s]);
             for (int pc = 0; pc < pieces; ++pc) {
               const int t = tok + pc * br;
               int pb = blk[pc];
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 report(p.err, DEVERR_BLOCK);
                 pb = 0;  // read a valid block; the result is flagged as wrong
               }
-              const int row = (pb * p.n_kv + h) * p.block_size +
+              const int row = (pb * p.n_kv + h * HP) * p.block_size +
                               t % p.block_size;
 #pragma unroll
               for (int bx = 0; bx < C::NBOX; ++bx) {
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ======================= finisher warp ==================================
   if (warp == kFinisher) {
     if (p.pos) {  // fused append: the new rows this CTA's chunks hold
-      append_range_rows(p, wp, 1, lo, hi, lane, early);
+      append_range_rows(p, wp, HP, lo, hi, lane, early);
       named_arrive(kAppendBar, 64);
     } else if (early) {
       pdl_wait();
@@ -295,30 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *wl = wm + kWarps * 16;           // [warp][16]
       const float *wo = wl + kWarps * 16;           // [warp][16][D]
       const bool whole = ustart >= lo && uend <= hi;
-      const float vs = DT == DT_FP8 ? p.v_scale[h] : 1.0f;
       const int wslot = c * 2 + partial_side(ustart, lo);
-      for (int idx = lane; idx < G * kD; idx += 32) {
-        const int g = idx / kD, d = idx % kD;
+      for (int idx = lane; idx < GU * kD; idx += 32) {
+        const int jg = idx / kD, d = idx % kD;  // query head jg of the unit
+        const int j = jg / G, g = jg % G;       // its kv head, row
+        const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
+        const int w0 = j * C::WPH;              // the kv head's warps
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 16 + g]);
+        for (int w = 0; w < C::WPH; ++w)
+          M = fmaxf(M, wm[(w0 + w) * 16 + g]);
         float L = 0.f, acc = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float mw = wm[w * 16 + g];
+        for (int w = 0; w < C::WPH; ++w) {
+          const float mw = wm[(w0 + w) * 16 + g];
           const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
-          L = fmaf(wl[w * 16 + g], a, L);
-          acc = fmaf(wo[(w * 16 + g) * kD + d], a, acc);
+          L = fmaf(wl[(w0 + w) * 16 + g], a, L);
+          acc = fmaf(wo[((w0 + w) * 16 + g) * kD + d], a, acc);
         }
         const float res = acc / L * vs;
         const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-        const long bh = (long)b * p.n_h + h * G + g;
+        const long bh = (long)b * p.n_h + h * GU + jg;
         if (whole) {
           p.out[bh * kD + d] = f2bf(res);
           if (d == 0 && p.lse) p.lse[bh] = lse_nat;
         } else {
-          p.ws_o[((long)wslot * G + g) * kD + d] = res;
-          if (d == 0) p.ws_lse[(long)wslot * G + g] = lse_nat;
+          p.ws_o[((long)wslot * GU + jg) * kD + d] = res;
+          if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
         }
       }
       __syncwarp();
@@ -332,17 +345,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ======================= consumer warps =================================
   if (early) pdl_wait();
   // Per thread: rows qr and qr + 8 of the 16-row tiles, columns 2 qc, 2 qc+1
-  // of every 8-wide n-tile.
+  // of every 8-wide n-tile. Warp w takes kv head hj = w / WPH of the unit
+  // and tokens wt0 .. wt0 + TPW - 1 of it in every chunk (NSUB tiles of 16);
+  // the head's rows sit at rows 64 hj .. of every column box of a stage.
   uint32_t qa[8][4];      // query A fragments, 8 k-steps of 16
   float o[16][4];         // O accumulators, 16 n-tiles of 8 columns
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int cur_b = -1, cur_h = -1, n_flush = 0;
   float sl2 = 0.f;        // scale of S into log2 units
-  const uint32_t sk0 = smem_u32(sk), sv0 = smem_u32(sv);
-  const int wt0 = warp * 16;  // this warp's first token in a chunk
+  const int hj = warp / C::WPH;
+  const int wt0 = (warp % C::WPH) * C::TPW;  // this warp's first token
+  const uint32_t sk0 = smem_u32(sk) + hj * 64 * 128;
+  const uint32_t sv0 = smem_u32(sv) + hj * 64 * 128;
 
   auto start_unit = [&](int s, int h) {
-    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(sq + s * C::QB);
+    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+        sq + s * C::QB + hj * G * kD * 2);
     const bool r0 = qr < G, r1 = qr + 8 < G;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -362,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         qa[kk][3] = r1 ? f16pair_from_bf16(q32[(qr + 8) * (kD / 2) + w0 + 1]) : 0u;
       }
     }
-    sl2 = p.scale_log2 * (DT == DT_FP8 ? p.k_scale[h] : 1.0f);
+    sl2 = p.scale_log2 * (DT == DT_FP8 ? p.k_scale[h * HP + hj] : 1.0f);
     m0 = m1 = -INFINITY;
     l0 = l1 = 0.f;
 #pragma unroll
@@ -427,60 +445,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       const uint32_t kb = sk0 + s * C::STAGE;
       const uint32_t vb = sv0 + s * C::STAGE;
-      if (nvalid < wt0 + 16) {
+      if (nvalid < wt0 + C::TPW) {
         // rows past the sequence hold stale or unread data: zero this
         // warp's invalid V rows so that 0 * garbage cannot make a NaN
-        for (int r = max(nvalid, wt0) + (lane >> 3); r < wt0 + 16; r += 4)
+        for (int r = max(nvalid, wt0) + (lane >> 3); r < wt0 + C::TPW; r += 4)
           for (int bx = 0; bx < C::NBOX; ++bx)
             *reinterpret_cast<uint4 *>(sv + s * C::STAGE + bx * C::BOX +
-                                       r * 128 + (lane & 7) * 16) =
+                                       (hj * 64 + r) * 128 + (lane & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
         __syncwarp();
       }
-      // ---- S = Q K^T for tokens wt0 .. wt0 + 15 ----
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      // ---- S = Q K^T for tokens wt0 .. wt0 + TPW - 1 ----
+      float sc[C::NSUB][2][4];
+#pragma unroll
+      for (int u = 0; u < C::NSUB; ++u)
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sc[u][t2][j] = 0.f;
+#pragma unroll
+      for (int u = 0; u < C::NSUB; ++u) {
+        const int ws = wt0 + 16 * u;
         const int mtx = lane >> 3, ri = lane & 7;
         if constexpr (DT == DT_BF16) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int tok = wt0 + (mtx >> 1) * 8 + ri;
+            const int tok = ws + (mtx >> 1) * 8 + ri;
             const int d = 16 * kk + (mtx & 1) * 8;
             uint32_t bk[4];
             ldsm_x4(bk, swz(kb + (d >> 6) * C::BOX, tok, (d & 63) * 2));
-            mma_bf16(sc[0], qa[kk], bk[0], bk[1]);
-            mma_bf16(sc[1], qa[kk], bk[2], bk[3]);
+            mma_bf16(sc[u][0], qa[kk], bk[0], bk[1]);
+            mma_bf16(sc[u][1], qa[kk], bk[2], bk[3]);
           }
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; kk += 2) {
-            const int tok = wt0 + (mtx & 1) * 8 + ri;
+            const int tok = ws + (mtx & 1) * 8 + ri;
             const int ks = kk + (mtx >> 1);
             uint32_t bk[4];
             ldsm_x4(bk, swz(kb, tok, ks * 16));
             // bk[m]: 4 codes of token row, dims 16 ks + 4 qc .. + 3
-            mma_f16(sc[0], qa[kk], e4m3x2_to_f16x2(bk[0] & 0xffff),
+            mma_f16(sc[u][0], qa[kk], e4m3x2_to_f16x2(bk[0] & 0xffff),
                     e4m3x2_to_f16x2(bk[0] >> 16));
-            mma_f16(sc[1], qa[kk], e4m3x2_to_f16x2(bk[1] & 0xffff),
+            mma_f16(sc[u][1], qa[kk], e4m3x2_to_f16x2(bk[1] & 0xffff),
                     e4m3x2_to_f16x2(bk[1] >> 16));
-            mma_f16(sc[0], qa[kk + 1], e4m3x2_to_f16x2(bk[2] & 0xffff),
+            mma_f16(sc[u][0], qa[kk + 1], e4m3x2_to_f16x2(bk[2] & 0xffff),
                     e4m3x2_to_f16x2(bk[2] >> 16));
-            mma_f16(sc[1], qa[kk + 1], e4m3x2_to_f16x2(bk[3] & 0xffff),
+            mma_f16(sc[u][1], qa[kk + 1], e4m3x2_to_f16x2(bk[3] & 0xffff),
                     e4m3x2_to_f16x2(bk[3] >> 16));
           }
         }
       }
-      // ---- online softmax over the 16 tokens, rows qr and qr + 8 ----
+      // ---- online softmax over the warp's tokens, rows qr and qr + 8 ----
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+      for (int u = 0; u < C::NSUB; ++u) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int col = wt0 + 8 * t + 2 * qc + (j & 1);
-          sc[t][j] = col < nvalid ? sc[t][j] * sl2 : -INFINITY;
+        for (int t2 = 0; t2 < 2; ++t2) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = wt0 + 16 * u + 8 * t2 + 2 * qc + (j & 1);
+            sc[u][t2][j] = col < nvalid ? sc[u][t2][j] * sl2 : -INFINITY;
+          }
+          mx0 = fmaxf(mx0, fmaxf(sc[u][t2][0], sc[u][t2][1]));
+          mx1 = fmaxf(mx1, fmaxf(sc[u][t2][2], sc[u][t2][3]));
         }
-        mx0 = fmaxf(mx0, fmaxf(sc[t][0], sc[t][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[t][2], sc[t][3]));
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -492,16 +521,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c0 = ex2(m0 - u0), c1 = ex2(m1 - u1);
       m0 = n0;
       m1 = n1;
-      float pp[2][4];
+      uint32_t pa[C::NSUB][4];
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        pp[t][0] = ex2(sc[t][0] - u0);
-        pp[t][1] = ex2(sc[t][1] - u0);
-        pp[t][2] = ex2(sc[t][2] - u1);
-        pp[t][3] = ex2(sc[t][3] - u1);
+      for (int u = 0; u < C::NSUB; ++u) {
+        float pp[2][4];
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+          pp[t2][0] = ex2(sc[u][t2][0] - u0);
+          pp[t2][1] = ex2(sc[u][t2][1] - u0);
+          pp[t2][2] = ex2(sc[u][t2][2] - u1);
+          pp[t2][3] = ex2(sc[u][t2][3] - u1);
+          ls0 += pp[t2][0] + pp[t2][1];
+          ls1 += pp[t2][2] + pp[t2][3];
+        }
+        if constexpr (DT == DT_BF16) {
+          pa[u][0] = pack_bf16x2(pp[0][0], pp[0][1]);
+          pa[u][1] = pack_bf16x2(pp[0][2], pp[0][3]);
+          pa[u][2] = pack_bf16x2(pp[1][0], pp[1][1]);
+          pa[u][3] = pack_bf16x2(pp[1][2], pp[1][3]);
+        } else {
+          pa[u][0] = pack_f16x2(pp[0][0], pp[0][1]);
+          pa[u][1] = pack_f16x2(pp[0][2], pp[0][3]);
+          pa[u][2] = pack_f16x2(pp[1][0], pp[1][1]);
+          pa[u][3] = pack_f16x2(pp[1][2], pp[1][3]);
+        }
       }
-      l0 = l0 * c0 + pp[0][0] + pp[0][1] + pp[1][0] + pp[1][1];
-      l1 = l1 * c1 + pp[0][2] + pp[0][3] + pp[1][2] + pp[1][3];
+      l0 = l0 * c0 + ls0;
+      l1 = l1 * c1 + ls1;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         o[nt][0] *= c0;
@@ -510,29 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[nt][3] *= c1;
       }
       // ---- O += P V ----
-      uint32_t pa[4];
-      if constexpr (DT == DT_BF16) {
-        pa[0] = pack_bf16x2(pp[0][0], pp[0][1]);
-        pa[1] = pack_bf16x2(pp[0][2], pp[0][3]);
-        pa[2] = pack_bf16x2(pp[1][0], pp[1][1]);
-        pa[3] = pack_bf16x2(pp[1][2], pp[1][3]);
-      } else {
-        pa[0] = pack_f16x2(pp[0][0], pp[0][1]);
-        pa[1] = pack_f16x2(pp[0][2], pp[0][3]);
-        pa[2] = pack_f16x2(pp[1][0], pp[1][1]);
-        pa[3] = pack_f16x2(pp[1][2], pp[1][3]);
-      }
-      {
+#pragma unroll
+      for (int u = 0; u < C::NSUB; ++u) {
         const int mtx = lane >> 3, ri = lane & 7;
-        const int tok = wt0 + (mtx & 1) * 8 + ri;
+        const int tok = wt0 + 16 * u + (mtx & 1) * 8 + ri;
         if constexpr (DT == DT_BF16) {
 #pragma unroll
           for (int np = 0; np < 8; ++np) {
             const int d = 8 * (2 * np + (mtx >> 1));
             uint32_t bv[4];
             ldsm_x4_t(bv, swz(vb + (d >> 6) * C::BOX, tok, (d & 63) * 2));
-            mma_bf16(o[2 * np], pa, bv[0], bv[1]);
-            mma_bf16(o[2 * np + 1], pa, bv[2], bv[3]);
+            mma_bf16(o[2 * np], pa[u], bv[0], bv[1]);
+            mma_bf16(o[2 * np + 1], pa[u], bv[2], bv[3]);
           }
         } else {
 #pragma unroll
@@ -546,21 +582,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h2 = 0; h2 < 2; ++h2) {
               const uint32_t lo_t = bv[2 * h2], hi_t = bv[2 * h2 + 1];
               const int gg = 2 * dp + h2;
-              mma_f16(o[2 * gg], pa,
+              mma_f16(o[2 * gg], pa[u],
                       e4m3x2_to_f16x2((uint16_t)prmt(lo_t, 0, 0x0020)),
                       e4m3x2_to_f16x2((uint16_t)prmt(hi_t, 0, 0x0020)));
-              mma_f16(o[2 * gg + 1], pa,
+              mma_f16(o[2 * gg + 1], pa[u],
                       e4m3x2_to_f16x2((uint16_t)prmt(lo_t, 0, 0x0031)),
                       e4m3x2_to_f16x2((uint16_t)prmt(hi_t, 0, 0x0031)));
             }
           }
         }
       }
-      if (nvalid < wt0 + 16) fence_proxy_async_smem();
+      if (nvalid < wt0 + C::TPW) fence_proxy_async_smem();
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    cursor_next(wp, p.batch, p.n_kv, cc);
+    cursor_next(wp, p.batch, n_units, cc);
   }
   if (cur_b >= 0) flush();
 
@@ -595,23 +631,32 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long rows, bool fp8,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int DT>
+template <int DT, int HP>
 cudaError_t launch_t(const MmaParams &mp, cudaStream_t s) {
-  using C = MCfg<DT>;
+  using C = MCfg<DT, HP>;
   static_assert(C::SMEM <= 226 * 1024, "shared memory budget");
   static_assert(C::NS >= 2, "ring depth");
-  auto kern = decode_mma_kernel<DT>;
+  auto kern = decode_mma_kernel<DT, HP>;
   static bool done[64] = {};
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(mp.p.n_splits), dim3(kThreads), C::SMEM, s, 1, mp);
   if (e != cudaSuccess) return e;
-  const int g = mp.p.n_h / mp.p.n_kv;
-  return g == 16 ? launch_merge_dense<kD, 16>(mp.p, mp.p.n_kv, s)
-                 : launch_merge_dense<kD, 8>(mp.p, mp.p.n_kv, s);
+  const int gu = HP * (mp.p.n_h / mp.p.n_kv);  // query heads per unit
+  const int units = mp.p.n_kv / HP;
+  return gu == 32   ? launch_merge_dense<kD, 32>(mp.p, units, s)
+         : gu == 16 ? launch_merge_dense<kD, 16>(mp.p, units, s)
+                    : launch_merge_dense<kD, 8>(mp.p, units, s);
 }
 
 }  // namespace
+
+// Head groups of 2 for the fp8 cache (its 8 KB per head and block is too
+// small a copy); a bf16 head's 16 KB copies stream well, and doubling them
+// would leave room for only two ring stages.
+int mma_heads_per_unit(int n_kv, int block_size, int dtype) {
+  return dtype == DT_FP8 && block_size == 64 && n_kv % 2 == 0 ? 2 : 1;
+}
 
 cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
                               cudaStream_t s) {
@@ -629,12 +674,18 @@ cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
   MmaParams mp;
   mp.p = p;
   const bool fp8 = dtype == DT_FP8;
-  const int box_rows = p.block_size < 64 ? p.block_size : 64;
+  if (p.hp != 1 && p.hp != mma_heads_per_unit(p.n_kv, p.block_size, dtype))
+    return cudaErrorNotSupported;
+  // a box is one block piece of one head, or the hp heads' rows of a block
+  const int box_rows =
+      p.hp > 1 ? p.hp * 64 : (p.block_size < 64 ? p.block_size : 64);
   e = make_map(&mp.tmk, p.k, rows, fp8, box_rows);
   if (e != cudaSuccess) return e;
   e = make_map(&mp.tmv, p.v, rows, fp8, box_rows);
   if (e != cudaSuccess) return e;
-  return fp8 ? launch_t<DT_FP8>(mp, s) : launch_t<DT_BF16>(mp, s);
+  if (p.hp == 2)
+    return fp8 ? launch_t<DT_FP8, 2>(mp, s) : launch_t<DT_BF16, 2>(mp, s);
+  return fp8 ? launch_t<DT_FP8, 1>(mp, s) : launch_t<DT_BF16, 1>(mp, s);
 }
 
 }  // namespace kvd

@@ -94,6 +94,9 @@ int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
 // Dense GQA on the tensor cores (group size 8 or 16, head_dim 128).
 cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
                               cudaStream_t s);
+// kv heads the tensor-core kernel takes per work unit (its plan and its
+// launch must agree).
+int mma_heads_per_unit(int n_kv, int block_size, int dtype);
 // MLA latent decode (dk 576, dv 512, n_h multiple of 64).
 cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s);
 // Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64).
