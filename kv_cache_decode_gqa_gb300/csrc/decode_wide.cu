@@ -43,7 +43,12 @@ constexpr int kGroups = 4;                // 16-head row tiles
 constexpr int kQuarters = 4;              // value-column quarters
 constexpr int kCWarps = kGroups * kQuarters;
 constexpr int kConsumers = kCWarps * 32;  // 512
-constexpr int kThreads = kConsumers + 32; // + producer warp
+// Four producer warps, each fetching 8 rows of every chunk: a warp issues
+// its bulk copies one lane after another (about 50 ns a copy), so one warp
+// copying 32 or 64 short rows per chunk was the kernel's limit.
+constexpr int kPW = 4;                    // producer warps
+constexpr int kPRows = kRows / kPW;       // rows per producer warp
+constexpr int kThreads = kConsumers + 32 * kPW;
 constexpr int kAllBar = 1;                // all consumer warps
 constexpr int kNB = 256;                  // largest batch of these calls
 
@@ -87,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *qbar = empty + C::NS;
   __shared__ int s_len_err;
   __shared__ volatile int s_abort, s_issued, s_producer_done;
-  __shared__ unsigned s_valid[C::NS];  // rows of each stage that were fetched
+  // rows of each stage that were fetched, 8 bits per producer warp
+  __shared__ __align__(4) uint8_t s_vpart[C::NS][kPW];
 
   const int tiles = p.n_h / kHeads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], kPW);  // each producer warp's arrive + bytes
       mbar_init(&empty[s], kCWarps);
     }
     mbar_init(qbar, 1);
@@ -135,20 +141,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ======================= producer warp ==================================
-  // Lane r fetches row r of each chunk: its position (chunk start + r, or
-  // the r-th entry of the chunk's slice of the index list), its block, and
-  // one bulk copy per cached tensor.
-  if (warp == kCWarps) {
+  // ======================= producer warps =================================
+  // Producer warp pw takes rows 8 pw .. 8 pw + 7 of every chunk: lane r < 8
+  // looks up row 8 pw + r (its position: chunk start + r, or that entry of
+  // the chunk's slice of the index list; then its block), lanes 0..7 copy
+  // the rows' K and, for separate values, lanes 8..15 their V -- 8 or 16
+  // bulk copies per warp and chunk, issued by the four warps side by side.
+  if (warp >= kCWarps) {
+    const int pw = warp - kCWarps;
+    const int r8 = lane & 7;            // row of the warp's eight
+    const int row_in_chunk = pw * kPRows + r8;
     ChunkCursor pc = cursor_at(wp, p.batch, lo);
-    // position and block of this lane's row of the chunk at `cc` (-1: none)
+    // position and block of row `row_in_chunk` of the chunk at `cc`
     auto lookup = [&](const ChunkCursor &cc, int &t, int &blk) {
       const int T = wp.len[cc.b];
-      const int e = cc.k * kRows + lane;  // entry of this lane's row
+      const int e = cc.k * kRows + row_in_chunk;  // entry of the row
       if constexpr (GATHER) {
         t = e < p.n_idx ? p.indices[(long)cc.b * p.n_idx + e] : -1;
         if (t >= T) {
-          report(p.err, DEVERR_INDEX);
+          if (lane < 8) report(p.err, DEVERR_INDEX);
           t = -1;
         }
       } else {
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t >= 0) {
         blk = p.block_table[(long)cc.b * p.max_blocks + t / p.block_size];
         if (blk < 0 || blk >= p.num_blocks) {
-          report(p.err, DEVERR_BLOCK);
+          if (lane < 8) report(p.err, DEVERR_BLOCK);
           blk = 0;  // read a valid block; the result is flagged as wrong
         }
       }
@@ -174,19 +185,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) report(p.err, DEVERR_TIMEOUT);
         break;
       }
-      const unsigned valid = __ballot_sync(0xffffffffu, t >= 0);
-      if (t < 0) {
+      const unsigned valid =
+          __ballot_sync(0xffffffffu, lane < 8 && t >= 0) & 0xffu;
+      if (lane < 8 && t < 0) {
         // a row that is not fetched keeps stale data: zero the value part,
         // so that its zero probability cannot meet a NaN in P V
         uint4 *vz = reinterpret_cast<uint4 *>(
-            C::VFROMK ? sk + s * C::KST + lane * C::KROW
-                      : sv + s * C::VST + lane * C::VROW);
+            C::VFROMK ? sk + s * C::KST + row_in_chunk * C::KROW
+                      : sv + s * C::VST + row_in_chunk * C::VROW);
         for (int j = 0; j < DV * 2 / 16; ++j) vz[j] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) {
-        s_valid[s] = valid;
+        s_vpart[s][pw] = (uint8_t)valid;
         mbar_arrive_expect_tx(&full[s], __popc(valid) *
                                             (DK * 2 + (C::VFROMK ? 0 : DV * 2)));
       }
@@ -194,18 +206,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t >= 0) {
         const size_t row =
             ((size_t)blk * p.n_kv) * p.block_size + t % p.block_size;
-        bulk_g2s(sk + s * C::KST + lane * C::KROW, p.k + row * DK * 2, DK * 2,
-                 &full[s]);
-        if constexpr (!C::VFROMK)
-          bulk_g2s(sv + s * C::VST + lane * C::VROW, p.v + row * DV * 2,
-                   DV * 2, &full[s]);
+        if (lane < 8)
+          bulk_g2s(sk + s * C::KST + row_in_chunk * C::KROW,
+                   p.k + row * DK * 2, DK * 2, &full[s]);
       }
-      if (lane == 0) s_issued = i + 1;
+      if constexpr (!C::VFROMK) {
+        // lanes 8..15 copy the values of the rows lanes 0..7 looked up
+        const int tv = __shfl_sync(0xffffffffu, t, r8);
+        const int bv = __shfl_sync(0xffffffffu, blk, r8);
+        if (lane >= 8 && lane < 16 && tv >= 0) {
+          const size_t row =
+              ((size_t)bv * p.n_kv) * p.block_size + tv % p.block_size;
+          bulk_g2s(sv + s * C::VST + row_in_chunk * C::VROW,
+                   p.v + row * DV * 2, DV * 2, &full[s]);
+        }
+      }
+      if (lane == 0 && pw == 0) s_issued = i + 1;
       // the next chunk's rows are looked up now, while the ring is full
       cursor_next(wp, p.batch, 1, pc);
       if (i + 1 < n) lookup(pc, t, blk);
     }
-    if (lane == 0) s_producer_done = 1;
+    if (lane == 0) atomicAdd(const_cast<int *>(&s_producer_done), 1);
     return;
   }
 
@@ -219,15 +240,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   int cur_b = -1, cur_h = -1, n_units = 0;
 
   auto start_unit = [&](int b, int h) {
-    // the query tile of (b, head tile h): 64 rows, one bulk copy each
+    // the query tile of (b, head tile h): 64 rows, one bulk copy each,
+    // issued by lanes 0..3 of every consumer warp (a warp issues its copies
+    // one lane after another)
     named_sync(kAllBar, kConsumers);  // nobody still reads the old tile
-    if (warp == 0) {
-      if (lane == 0) mbar_arrive_expect_tx(qbar, kHeads * DK * 2);
-      __syncwarp();
-      for (int r = lane; r < kHeads; r += 32)
-        bulk_g2s(sq + r * C::QROW,
-                 p.q + ((long)b * p.n_h + (long)h * kHeads + r) * DK,
-                 DK * 2, qbar);
+    if (tid == 0) mbar_arrive_expect_tx(qbar, kHeads * DK * 2);
+    named_sync(kAllBar, kConsumers);  // the bytes are expected before any lands
+    if (lane < kHeads / kCWarps) {
+      const int r = warp * (kHeads / kCWarps) + lane;
+      bulk_g2s(sq + r * C::QROW,
+               p.q + ((long)b * p.n_h + (long)h * kHeads + r) * DK, DK * 2,
+               qbar);
     }
     if (!mbar_wait(qbar, n_units & 1) && lane == 0) {
       report(p.err, DEVERR_TIMEOUT);
@@ -317,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_abort = 1;
     }
     // validity of this warp's S columns: rows qtr * 8 + 2 qc (+1)
-    const unsigned vmask = s_valid[s];
+    const unsigned vmask = *reinterpret_cast<const volatile unsigned *>(
+        &s_vpart[s][0]);
     const bool val0 = (vmask >> (qtr * 8 + 2 * qc)) & 1;
     const bool val1 = (vmask >> (qtr * 8 + 2 * qc + 1)) & 1;
     const uint32_t kst = k0 + s * C::KST;
@@ -418,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cur_b >= 0) flush(cur_b, cur_h);
 
   if (s_abort && tid == 0) {
-    for (int t = 0; t < (1 << 20) && !s_producer_done; ++t) __nanosleep(1000);
+    for (int t = 0; t < (1 << 20) && s_producer_done < kPW; ++t)
+      __nanosleep(1000);
     const int issued = s_issued;
     for (int st = 0; st < C::NS; ++st) {
       int last = -1;
@@ -428,16 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kMergeSlices = 32;    // CTAs per split unit
+constexpr int kMergeSlices = 128;   // CTAs per split unit
 constexpr int kMergeThreads = 256;
 
 // Log-sum-exp merge of the partials of every unit the decode launch cut
 // between CTAs. Grid (units, kMergeSlices): CTA (u, j) rebuilds the launch's
 // partition, returns if unit u lies inside one CTA's range, and otherwise
-// merges the j-th 1/32 of the unit's outputs: for each float4 of outputs
-// (4 values of one head) an online merge over the parts, 8 parts' loads in
-// flight at a time. Part i is the partial of lane c_first + i: side 1 of
-// the first covering lane, side 0 of the others.
+// merges the j-th 1/128 of the unit's outputs: 64 float4s (4 values of one
+// head), each by a quad of lanes (quad_merge: the parts split over the 4
+// lanes, all of a lane's loads in flight at once). Part i is the partial of
+// lane c_first + i: side 1 of the first covering lane, side 0 of the
+// others.
 template <int DV, bool GATHER>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_wide_kernel(const DecodeParams p) {
@@ -462,51 +488,25 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (parts == 1) return;  // written whole by the decode launch
   constexpr int N4 = kHeads * DV / 4;
   constexpr int PER = N4 / kMergeSlices;
-  static_assert(PER % kMergeThreads == 0, "slice of whole float4 rounds");
+  static_assert(4 * PER == kMergeThreads, "one quad of lanes per float4");
   const long bh0 = (long)b * p.n_h + (long)h * kHeads;
-  for (int e = blockIdx.y * PER + threadIdx.x; e < (blockIdx.y + 1) * PER;
-       e += kMergeThreads) {
-    const int g = (4 * e) / DV;  // head within the tile
-    float M = -INFINITY, W = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < parts; i0 += 8) {
-      float4 v[8];
-      float l[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j;
-        const int slot = ((c_first + i) * 2 + (i == 0 ? 1 : 0)) * tiles + h;
-        if (i < parts) {
-          l[j] = __ldcg(p.ws_lse + (long)slot * kHeads + g);
-          v[j] = __ldcg(reinterpret_cast<const float4 *>(
-                            p.ws_o + (long)slot * kHeads * DV) + e);
-        } else {
-          l[j] = -INFINITY;
-          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (l[j] == -INFINITY) continue;  // an empty part adds nothing
-        const float Mn = fmaxf(M, l[j]);
-        const float a = M == -INFINITY ? 0.f : expf(M - Mn);
-        const float w = expf(l[j] - Mn);
-        W = W * a + w;
-        acc.x = acc.x * a + w * v[j].x;
-        acc.y = acc.y * a + w * v[j].y;
-        acc.z = acc.z * a + w * v[j].z;
-        acc.w = acc.w * a + w * v[j].w;
-        M = Mn;
-      }
-    }
-    const float iw = W > 0.f ? 1.f / W : 0.f;
-    uint2 packed;
-    packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
-    packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
-    *reinterpret_cast<uint2 *>(p.out + bh0 * DV + 4 * e) = packed;
-    if ((4 * e) % DV == 0 && p.lse)
-      p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
-  }
+  const int e = blockIdx.y * PER + (threadIdx.x >> 2);
+  const int g = (4 * e) / DV;  // head within the tile
+  float M, W;
+  float4 acc;
+  quad_merge<4>(p.ws_lse, p.ws_o, kHeads, DV, g, e, parts,
+             [&](int i) {
+               return ((long)(c_first + i) * 2 + (i == 0 ? 1 : 0)) * tiles + h;
+             },
+             M, W, acc);
+  if ((threadIdx.x & 3) != 0) return;
+  const float iw = W > 0.f ? 1.f / W : 0.f;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
+  packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
+  *reinterpret_cast<uint2 *>(p.out + bh0 * DV + 4 * e) = packed;
+  if ((4 * e) % DV == 0 && p.lse)
+    p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
 template <int DK, int DV, bool GATHER>

@@ -268,19 +268,87 @@ __device__ __forceinline__ void append_unread_rows(
   }
 }
 
+// Online log-sum-exp merge of the partials of one float4 of outputs, its
+// parts split over an aligned group of LANES (1 or 4) lanes: lane q takes
+// parts q, q + LANES, ... with up to 8 of its loads in flight at once (so
+// 8 LANES parts take one round), then the group's states are combined with
+// xor-shuffles. `slot(i)` is part i's partial slot; `lse` / `o` point at
+// the partials' log-sum-exps and outputs, `g` / `e` index the head and the
+// float4 within a slot of `gu` heads x `d` values. Every lane of the warp
+// calls it (inactive ones with parts = 0). On return the quad's lanes hold
+// M = max lse, W = sum e^(lse - M), acc = sum e^(lse - M) o.
+template <int LANES, class SlotF>
+__device__ __forceinline__ void quad_merge(const float *lse, const float *o,
+                                           int gu, int d, int g, int e,
+                                           int parts, SlotF slot, float &M,
+                                           float &W, float4 &acc) {
+  const int q = threadIdx.x & (LANES - 1);
+  M = -INFINITY;
+  W = 0.f;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = q; i0 < parts; i0 += 8 * LANES) {
+    float4 v[8];
+    float l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + LANES * j;
+      if (i < parts) {
+        const long sl = slot(i);
+        l[j] = __ldcg(lse + sl * gu + g);
+        v[j] = __ldcg(reinterpret_cast<const float4 *>(o + sl * gu * d) + e);
+      } else {
+        l[j] = -INFINITY;
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (l[j] == -INFINITY) continue;  // an empty part adds nothing
+      const float Mn = fmaxf(M, l[j]);
+      const float a = M == -INFINITY ? 0.f : expf(M - Mn);
+      const float w = expf(l[j] - Mn);
+      W = W * a + w;
+      acc.x = acc.x * a + w * v[j].x;
+      acc.y = acc.y * a + w * v[j].y;
+      acc.z = acc.z * a + w * v[j].z;
+      acc.w = acc.w * a + w * v[j].w;
+      M = Mn;
+    }
+  }
+#pragma unroll
+  for (int off = 1; off < LANES; off <<= 1) {
+    const float M2 = __shfl_xor_sync(0xffffffffu, M, off);
+    const float W2 = __shfl_xor_sync(0xffffffffu, W, off);
+    float4 a2;
+    a2.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+    a2.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+    a2.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+    a2.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+    const float Mn = fmaxf(M, M2);
+    const float a = M == -INFINITY ? 0.f : expf(M - Mn);
+    const float b = M2 == -INFINITY ? 0.f : expf(M2 - Mn);
+    W = W * a + W2 * b;
+    acc.x = acc.x * a + a2.x * b;
+    acc.y = acc.y * a + a2.y * b;
+    acc.z = acc.z * a + a2.z * b;
+    acc.w = acc.w * a + a2.w * b;
+    M = Mn;
+  }
+}
+
 // Log-sum-exp merge of the units a dense decode launch cut between CTAs,
 // run as a second launch right after it (programmatic dependent launch, so
 // its CTAs are resident and waiting when the decode grid completes). Each
 // CTA rebuilds the partition from the sequence lengths and takes units
 // u = blockIdx.x, + gridDim.x, ...; for a unit covered by more than one
 // CTA it merges, per float4 of outputs (4 values of one head), the parts'
-// partial results with an online log-sum-exp merge, 8 parts' loads in
-// flight at a time:
+// partial results with an online log-sum-exp merge (quad_merge: 4 lanes
+// per float4, all of a lane's loads in flight at once):
 //   out = sum_s w_s o_s,  w_s = e^(lse_s - M) / sum_s e^(lse_s - M),
 //   M = max_s lse_s,  lse = M + ln sum_s e^(lse_s - M).
 // Part i is the partial of CTA c_first + i: side 1 of the first covering
 // CTA, side 0 of the others. Units inside one CTA were written whole.
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 
 template <int D, int GU>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -307,40 +375,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int parts = cta_of(uend - 1, total, P) - c_first + 1;
     if (parts == 1) continue;
     const long bh0 = (long)b * p.n_h + (long)h * GU;
-    for (int e = threadIdx.x; e < N4; e += kMergeThreads) {
+    auto slot = [&](int i) {
+      return (long)(c_first + i) * 2 + (i == 0 ? 1 : 0);
+    };
+    auto store = [&](int e, float M, float W, const float4 &acc) {
       const int g = (4 * e) / D;  // head within the unit
-      float M = -INFINITY, W = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i0 = 0; i0 < parts; i0 += 8) {
-        float4 v[8];
-        float l[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j;
-          const long slot = (long)(c_first + i) * 2 + (i == 0 ? 1 : 0);
-          if (i < parts) {
-            l[j] = __ldcg(p.ws_lse + slot * GU + g);
-            v[j] = __ldcg(reinterpret_cast<const float4 *>(
-                              p.ws_o + slot * GU * D) + e);
-          } else {
-            l[j] = -INFINITY;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (l[j] == -INFINITY) continue;  // an empty part adds nothing
-          const float Mn = fmaxf(M, l[j]);
-          const float a = M == -INFINITY ? 0.f : expf(M - Mn);
-          const float w = expf(l[j] - Mn);
-          W = W * a + w;
-          acc.x = acc.x * a + w * v[j].x;
-          acc.y = acc.y * a + w * v[j].y;
-          acc.z = acc.z * a + w * v[j].z;
-          acc.w = acc.w * a + w * v[j].w;
-          M = Mn;
-        }
-      }
       const float iw = W > 0.f ? 1.f / W : 0.f;
       uint2 packed;
       packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
@@ -348,6 +387,27 @@ __global__ void __launch_bounds__(kMergeThreads)
       *reinterpret_cast<uint2 *>(p.out + bh0 * D + 4 * e) = packed;
       if ((4 * e) % D == 0 && p.lse)
         p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
+    };
+    float M, W;
+    float4 acc;
+    if (parts <= 8) {
+      // one lane per float4: its loads take one round
+      for (int e = threadIdx.x; e < N4; e += kMergeThreads) {
+        quad_merge<1>(p.ws_lse, p.ws_o, GU, D, (4 * e) / D, e, parts, slot,
+                      M, W, acc);
+        store(e, M, W, acc);
+      }
+    } else {
+      // a quad of lanes per float4; the bound is whole warps, so that every
+      // lane reaches the quad's shuffles
+      for (int e4 = threadIdx.x; e4 < (4 * N4 + 31) / 32 * 32;
+           e4 += kMergeThreads) {
+        const int e = e4 >> 2;
+        const bool active = e < N4;
+        quad_merge<4>(p.ws_lse, p.ws_o, GU, D, active ? (4 * e) / D : 0,
+                      active ? e : 0, active ? parts : 0, slot, M, W, acc);
+        if (active && (e4 & 3) == 0) store(e, M, W, acc);
+      }
     }
   }
 }
