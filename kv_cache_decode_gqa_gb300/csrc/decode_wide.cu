@@ -18,12 +18,13 @@
 // and lane (the positions of a chunk need not be contiguous: paged blocks,
 // or index-selected positions) into rows padded by 16 bytes, which keeps
 // every 8-row ldmatrix read free of bank conflicts. Sixteen consumer warps
-// form 4 groups (16 query heads each) x 4 quarters of the value width: per
-// chunk each warp of a group computes S = Q K^T for 8 of the 32 positions
-// over the full key width, the group exchanges row maxima and the
-// probabilities P (rounded to bf16) through shared memory, and each warp
-// accumulates O += P V for its quarter of the value columns. So no product
-// is computed twice. At a unit boundary the row sums are combined, and the
+// share the products, with tiles as large as the registers allow (the
+// kernel is bound by its ldmatrix traffic): for S = Q K^T a pair of warps
+// takes a 16-head x 16-position tile, each warp half of the key width, the
+// second handing its partial tile to the first; for O += P V a warp takes
+// 32 heads x 64 value columns. Row maxima, P (rounded to bf16) and the
+// per-head rescale factors go through shared memory. So no product is
+// computed twice. At a unit boundary the row sums are combined, and the
 // unit is written out, or as a partial. The partials of a unit cut between
 // CTAs (64 heads x 512 values each, so a unit cut 19 ways holds 2.4 MB) are
 // merged by a second, wide launch: one CTA per (unit, 1/32 of the unit's
@@ -39,9 +40,7 @@ namespace {
 
 constexpr int kHeads = 64;                // query heads per unit
 constexpr int kRows = 32;                 // positions per chunk
-constexpr int kGroups = 4;                // 16-head row tiles
-constexpr int kQuarters = 4;              // value-column quarters
-constexpr int kCWarps = kGroups * kQuarters;
+constexpr int kCWarps = 16;               // consumer warps
 constexpr int kConsumers = kCWarps * 32;  // 512
 // Four producer warps, each fetching 8 rows of every chunk: a warp issues
 // its bulk copies one lane after another (about 50 ns a copy), so one warp
@@ -65,13 +64,16 @@ struct WCfg {
   static constexpr int K_OFF = kHeads * QROW;
   static constexpr int V_OFF = K_OFF + NS * KST;
   static constexpr int PROW = kRows * 2 + 16;  // padded P row (bf16)
-  static constexpr int P_OFF = V_OFF + NS * VST;
-  static constexpr int RED_OFF = P_OFF + kGroups * 16 * PROW;
-  static constexpr int WP_OFF = RED_OFF + 2 * kCWarps * 16 * 4;
+  static constexpr int P_OFF = V_OFF + NS * VST;   // P, two chunk buffers
+  static constexpr int PBUF = kHeads * PROW;
+  static constexpr int SP_OFF = P_OFF + 2 * PBUF;  // K-split partial S tiles
+  static constexpr int RED_OFF = SP_OFF + 8 * 32 * 8 * 4;
+  // row maxima [8 tiles][16]; rescale factors [2][64]; flush: row sums
+  // [2][64] and maxima [64]
+  static constexpr int WP_OFF = RED_OFF + (8 * 16 + 2 * 64 + 3 * 64) * 4;
   static constexpr int BAR_OFF =
       (WP_OFF + (int)sizeof(WorkPartitionT<kNB>) + 15) / 16 * 16;
   static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8;
-  static constexpr int DVQ = DV / kQuarters;  // value columns per warp (128)
 };
 
 template <int DK, int DV, bool GATHER>
@@ -83,8 +85,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sk = smem + C::K_OFF;
   uint8_t *sv = smem + C::V_OFF;
   uint8_t *spv = smem + C::P_OFF;
+  float *spart = reinterpret_cast<float *>(smem + C::SP_OFF);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);  // row maxima
-  float *lsum = red + kCWarps * 16;                            // row sums
+  float *hcor = red + 8 * 16;     // [2][64] per-head rescale of O
+  float *lsum = hcor + 2 * 64;    // [2][64] row sums of the two halves
+  float *mfin = lsum + 2 * 64;    // [64] running maxima at a flush
   WorkPartitionT<kNB> &wp =
       *reinterpret_cast<WorkPartitionT<kNB> *>(smem + C::WP_OFF);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
@@ -231,13 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumer warps =================================
-  const int grp = warp >> 2;   // 16-head row tile
-  const int qtr = warp & 3;    // value quarter / token slice of the group
+  // S roles: tile st = warp / 2 = 16 heads (group hg = st / 2) x 16
+  // positions (half ph = st % 2) of the chunk; the two warps of a tile take
+  // halves of the key width (kh = warp % 2). The kh = 0 warps own the online
+  // softmax state of their tile's head rows (maxima equal across the two
+  // position halves of a group; row sums per half).
+  // PV roles: warp (hh = warp / 8, cb = warp % 8): heads 32 hh .. + 31 (two
+  // m-tiles) x value columns 64 cb .. + 63 (eight n-tiles).
+  const int st = warp >> 1, hg = st >> 1, ph = st & 1, kh = warp & 1;
+  const int hh = warp >> 3, cb = warp & 7;
   const uint32_t q0 = smem_u32(sq), k0 = smem_u32(sk), v0 = smem_u32(sv);
-  const uint32_t p0 = smem_u32(spv) + grp * 16 * C::PROW;
-  float o[C::DVQ / 8][4];      // O: 16 rows x DVQ columns
+  float o[2][8][4];            // O: 32 rows x 64 columns
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int cur_b = -1, cur_h = -1, n_units = 0;
+  const int gbar = 2 + hg;     // the 4 warps of head group hg
 
   auto start_unit = [&](int b, int h) {
     // the query tile of (b, head tile h): 64 rows, one bulk copy each,
@@ -260,73 +272,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     m0 = m1 = -INFINITY;
     l0 = l1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < C::DVQ / 8; ++nt)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[nt][j] = 0.f;
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[mt][nt][j] = 0.f;
   };
 
   auto flush = [&](int b, int h) {
-    // row sums over the group's four token slices
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (qc == 0) {
-      lsum[warp * 16 + qr] = l0;
-      lsum[warp * 16 + qr + 8] = l1;
+    // row sums of each position half (kh = 0 warps), then per head
+    // L = sum of the two halves; the PV warps normalise and write
+    if (kh == 0) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      if (qc == 0) {
+        lsum[ph * 64 + 16 * hg + qr] = l0;
+        lsum[ph * 64 + 16 * hg + qr + 8] = l1;
+        if (ph == 0) {
+          mfin[16 * hg + qr] = m0;
+          mfin[16 * hg + qr + 8] = m1;
+        }
+      }
     }
     named_sync(kAllBar, kConsumers);
-    float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      L0 += lsum[(grp * 4 + w) * 16 + qr];
-      L1 += lsum[(grp * 4 + w) * 16 + qr + 8];
-    }
     const int ustart = wp.pre[b];
     const int uend = ustart + wp.nch[b];
     const bool whole = ustart >= lo && uend <= hi;
     const int wslot = (c * 2 + partial_side(ustart, lo)) * tiles + h;
-    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-    const int row0 = grp * 16 + qr, row1 = row0 + 8;  // head within the tile
-    const float lse0 = L0 > 0.f ? (m0 + log2f(L0)) * 0.69314718055994531f
-                                : -INFINITY;
-    const float lse1 = L1 > 0.f ? (m1 + log2f(L1)) * 0.69314718055994531f
-                                : -INFINITY;
     const long bh0 = (long)b * p.n_h + (long)h * kHeads;
 #pragma unroll
-    for (int nt = 0; nt < C::DVQ / 8; ++nt) {
-      const int col = qtr * C::DVQ + nt * 8 + 2 * qc;
-      if (whole) {
-        *reinterpret_cast<uint32_t *>(p.out + (bh0 + row0) * DV + col) =
-            pack_bf16x2(o[nt][0] * inv0, o[nt][1] * inv0);
-        *reinterpret_cast<uint32_t *>(p.out + (bh0 + row1) * DV + col) =
-            pack_bf16x2(o[nt][2] * inv1, o[nt][3] * inv1);
-      } else {
-        float *dst = p.ws_o + ((long)wslot * kHeads) * DV;
-        *reinterpret_cast<float2 *>(dst + (long)row0 * DV + col) =
-            make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-        *reinterpret_cast<float2 *>(dst + (long)row1 * DV + col) =
-            make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
-      }
-    }
-    if (qtr == 0 && qc == 0) {
-      if (whole) {
-        if (p.lse) {
-          p.lse[bh0 + row0] = lse0;
-          p.lse[bh0 + row1] = lse1;
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int row = 32 * hh + 16 * mt + qr + 8 * half;  // head in tile
+        const float L = lsum[row] + lsum[64 + row];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int col = 64 * cb + 8 * nt + 2 * qc;
+          const float x = o[mt][nt][2 * half] * inv;
+          const float y = o[mt][nt][2 * half + 1] * inv;
+          if (whole) {
+            *reinterpret_cast<uint32_t *>(p.out + (bh0 + row) * DV + col) =
+                pack_bf16x2(x, y);
+          } else {
+            *reinterpret_cast<float2 *>(p.ws_o + ((long)wslot * kHeads + row) *
+                                                     DV + col) =
+                make_float2(x, y);
+          }
         }
-      } else {
-        p.ws_lse[(long)wslot * kHeads + row0] = lse0;
-        p.ws_lse[(long)wslot * kHeads + row1] = lse1;
+        if (cb == 0 && qc == 0) {
+          const float lse = L > 0.f
+                                ? (mfin[row] + log2f(L)) * 0.69314718055994531f
+                                : -INFINITY;
+          if (whole) {
+            if (p.lse) p.lse[bh0 + row] = lse;
+          } else {
+            p.ws_lse[(long)wslot * kHeads + row] = lse;
+          }
+        }
       }
     }
-    named_sync(kAllBar, kConsumers);  // lsum reusable
+    named_sync(kAllBar, kConsumers);  // lsum / mfin reusable
   };
 
   ChunkCursor cc = cursor_at(wp, p.batch, lo);
   const float sl2 = p.scale_log2;
   for (int i = 0; i < n; ++i) {
     const int s = i % C::NS;
+    const int pb = i & 1;  // P / rescale buffer of this chunk
     if (cc.b != cur_b) {
       if (cur_b >= 0) flush(cur_b, cur_h);
       cur_b = cc.b;
@@ -339,99 +355,134 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!s_abort) report(p.err, DEVERR_TIMEOUT);
       s_abort = 1;
     }
-    // validity of this warp's S columns: rows qtr * 8 + 2 qc (+1)
     const unsigned vmask = *reinterpret_cast<const volatile unsigned *>(
         &s_vpart[s][0]);
-    const bool val0 = (vmask >> (qtr * 8 + 2 * qc)) & 1;
-    const bool val1 = (vmask >> (qtr * 8 + 2 * qc + 1)) & 1;
     const uint32_t kst = k0 + s * C::KST;
     const uint32_t vst = (C::VFROMK ? k0 + s * C::KST : v0 + s * C::VST);
-    // ---- S = Q K^T: rows = this group's 16 heads, cols = 8 positions ----
+    const int mtx = lane >> 3, ri = lane & 7;
+    // ---- S tile: heads 16 hg .., positions 16 ph .., key half kh ----
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
-      const int mtx = lane >> 3, ri = lane & 7;
-      // A (query) rows grp*16 + (mtx & 1)*8 + ri, k half (mtx >> 1)
-      const uint32_t qa_base =
-          q0 + (grp * 16 + (mtx & 1) * 8 + ri) * C::QROW + (mtx >> 1) * 16;
-      // B (keys): positions qtr*8 + ri, two k-steps per x4 (k halves)
-      const uint32_t kb_base = kst + (qtr * 8 + ri) * C::KROW + mtx * 16;
-#pragma unroll 4
-      for (int ks = 0; ks < DK / 16; ks += 2) {
-        uint32_t a0[4], a1[4], bk[4];
-        ldsm_x4(a0, qa_base + ks * 32);
-        ldsm_x4(a1, qa_base + (ks + 1) * 32);
+      const uint32_t qa_base = q0 + (16 * hg + (mtx & 1) * 8 + ri) * C::QROW +
+                               (mtx >> 1) * 16;
+      const uint32_t kb_base = kst + (16 * ph + (mtx >> 1) * 8 + ri) * C::KROW +
+                               (mtx & 1) * 16;
+      constexpr int KS = DK / 32;  // k-steps of 16 in half the key width
+#pragma unroll 6
+      for (int ks = kh * KS; ks < (kh + 1) * KS; ++ks) {
+        uint32_t a[4], bk[4];
+        ldsm_x4(a, qa_base + ks * 32);
         ldsm_x4(bk, kb_base + ks * 32);
-        mma_bf16(sa, a0, bk[0], bk[1]);
-        mma_bf16(sb, a1, bk[2], bk[3]);
+        mma_bf16(sa, a, bk[0], bk[1]);  // positions 0..7 of the half
+        mma_bf16(sb, a, bk[2], bk[3]);  // positions 8..15
       }
     }
-    float sc[4];
+    // the kh = 1 warp's partial tile to its partner
+    float *sp = spart + st * 256;
+    if (kh == 1) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sc[j] = (sa[j] + sb[j]) * sl2;
-    if (!val0) sc[0] = sc[2] = -INFINITY;
-    if (!val1) sc[1] = sc[3] = -INFINITY;
-    // ---- row maxima across the group's four slices ----
-    float mx0 = fmaxf(sc[0], sc[1]), mx1 = fmaxf(sc[2], sc[3]);
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    if (qc == 0) {
-      red[warp * 16 + qr] = mx0;
-      red[warp * 16 + qr + 8] = mx1;
+      for (int j = 0; j < 4; ++j) {
+        sp[j * 32 + lane] = sa[j];
+        sp[(4 + j) * 32 + lane] = sb[j];
+      }
     }
-    named_sync(2 + grp, 128);
+    named_sync(gbar, 128);
+    if (kh == 0) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      mx0 = fmaxf(mx0, red[(grp * 4 + w) * 16 + qr]);
-      mx1 = fmaxf(mx1, red[(grp * 4 + w) * 16 + qr + 8]);
+      for (int j = 0; j < 4; ++j) {
+        sa[j] += sp[j * 32 + lane];
+        sb[j] += sp[(4 + j) * 32 + lane];
+      }
+      // scale, mask, row maxima over this half's 16 positions
+      const int c0p = 16 * ph + 2 * qc;  // position of sa[0]
+      float sc[8];
+      sc[0] = ((vmask >> c0p) & 1) ? sa[0] * sl2 : -INFINITY;
+      sc[1] = ((vmask >> (c0p + 1)) & 1) ? sa[1] * sl2 : -INFINITY;
+      sc[2] = ((vmask >> c0p) & 1) ? sa[2] * sl2 : -INFINITY;
+      sc[3] = ((vmask >> (c0p + 1)) & 1) ? sa[3] * sl2 : -INFINITY;
+      sc[4] = ((vmask >> (c0p + 8)) & 1) ? sb[0] * sl2 : -INFINITY;
+      sc[5] = ((vmask >> (c0p + 9)) & 1) ? sb[1] * sl2 : -INFINITY;
+      sc[6] = ((vmask >> (c0p + 8)) & 1) ? sb[2] * sl2 : -INFINITY;
+      sc[7] = ((vmask >> (c0p + 9)) & 1) ? sb[3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[4], sc[5]));
+      float mx1 = fmaxf(fmaxf(sc[2], sc[3]), fmaxf(sc[6], sc[7]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      if (qc == 0) {
+        red[st * 16 + qr] = mx0;
+        red[st * 16 + qr + 8] = mx1;
+      }
+      named_sync(gbar + 4, 64);  // the group's two kh = 0 warps
+      const int other = (2 * hg + (ph ^ 1)) * 16;
+      mx0 = fmaxf(mx0, red[other + qr]);
+      mx1 = fmaxf(mx1, red[other + qr + 8]);
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float u0 = n0 == -INFINITY ? 0.f : n0;
+      const float u1 = n1 == -INFINITY ? 0.f : n1;
+      const float c0 = ex2(m0 - u0), c1 = ex2(m1 - u1);
+      m0 = n0;
+      m1 = n1;
+      float pr[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pr[j] = ex2(sc[j] - ((j & 2) ? u1 : u0));
+      l0 = l0 * c0 + pr[0] + pr[1] + pr[4] + pr[5];
+      l1 = l1 * c1 + pr[2] + pr[3] + pr[6] + pr[7];
+      // P rows 16 hg + qr (+8), positions 16 ph + 2 qc (+1) and + 8
+      uint8_t *prow = spv + pb * C::PBUF + (16 * hg + qr) * C::PROW +
+                      (16 * ph + 2 * qc) * 2;
+      *reinterpret_cast<uint32_t *>(prow) = pack_bf16x2(pr[0], pr[1]);
+      *reinterpret_cast<uint32_t *>(prow + 8 * C::PROW) =
+          pack_bf16x2(pr[2], pr[3]);
+      *reinterpret_cast<uint32_t *>(prow + 16) = pack_bf16x2(pr[4], pr[5]);
+      *reinterpret_cast<uint32_t *>(prow + 8 * C::PROW + 16) =
+          pack_bf16x2(pr[6], pr[7]);
+      if (ph == 0 && qc == 0) {
+        hcor[pb * 64 + 16 * hg + qr] = c0;
+        hcor[pb * 64 + 16 * hg + qr + 8] = c1;
+      }
     }
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float u0 = n0 == -INFINITY ? 0.f : n0;
-    const float u1 = n1 == -INFINITY ? 0.f : n1;
-    const float c0 = ex2(m0 - u0), c1 = ex2(m1 - u1);
-    m0 = n0;
-    m1 = n1;
-    const float p00 = ex2(sc[0] - u0), p01 = ex2(sc[1] - u0);
-    const float p10 = ex2(sc[2] - u1), p11 = ex2(sc[3] - u1);
-    l0 = l0 * c0 + p00 + p01;
-    l1 = l1 * c1 + p10 + p11;
-    // P of this warp's 8 positions into the group's [16][32] tile
+    named_sync(kAllBar, kConsumers);  // P and the rescale factors are in
+    // ---- O += P V: heads 32 hh .., columns 64 cb .. ----
     {
-      uint8_t *prow = spv + grp * 16 * C::PROW;
-      *reinterpret_cast<uint32_t *>(prow + qr * C::PROW + (qtr * 8 + 2 * qc) * 2) =
-          pack_bf16x2(p00, p01);
-      *reinterpret_cast<uint32_t *>(prow + (qr + 8) * C::PROW +
-                                    (qtr * 8 + 2 * qc) * 2) =
-          pack_bf16x2(p10, p11);
-    }
 #pragma unroll
-    for (int nt = 0; nt < C::DVQ / 8; ++nt) {
-      o[nt][0] *= c0;
-      o[nt][1] *= c0;
-      o[nt][2] *= c1;
-      o[nt][3] *= c1;
-    }
-    named_sync(2 + grp, 128);
-    // ---- O += P V for this warp's value quarter ----
-    if (ok) {
-      const int mtx = lane >> 3, ri = lane & 7;
+      for (int mt = 0; mt < 2; ++mt) {
+        const float ca = hcor[pb * 64 + 32 * hh + 16 * mt + qr];
+        const float cbf = hcor[pb * 64 + 32 * hh + 16 * mt + qr + 8];
 #pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {  // 16 positions per k-step
-        uint32_t pa[4];
-        ldsm_x4(pa, p0 + ((mtx & 1) * 8 + ri) * C::PROW + (kt * 16 + (mtx >> 1) * 8) * 2);
-        // positions rows of V: kt*16 + (mtx & 1)*8 + ri; columns pairs
-        const uint32_t vrow =
-            vst + (kt * 16 + (mtx & 1) * 8 + ri) *
-                      (C::VFROMK ? C::KROW : C::VROW) +
-            qtr * C::DVQ * 2;
-        // rows of unfetched positions were zeroed by the producer
+        for (int nt = 0; nt < 8; ++nt) {
+          o[mt][nt][0] *= ca;
+          o[mt][nt][1] *= ca;
+          o[mt][nt][2] *= cbf;
+          o[mt][nt][3] *= cbf;
+        }
+      }
+      if (ok) {
+        const uint32_t pbase = smem_u32(spv) + pb * C::PBUF;
+        const int vrs = C::VFROMK ? C::KROW : C::VROW;
 #pragma unroll
-        for (int np = 0; np < C::DVQ / 16; ++np) {
-          uint32_t bv[4];
-          ldsm_x4_t(bv, vrow + (2 * np + (mtx >> 1)) * 16);
-          mma_bf16(o[2 * np], pa, bv[0], bv[1]);
-          mma_bf16(o[2 * np + 1], pa, bv[2], bv[3]);
+        for (int kt = 0; kt < 2; ++kt) {  // 16 positions per k-step
+          uint32_t pa[2][4];
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+            ldsm_x4(pa[mt], pbase +
+                                (32 * hh + 16 * mt + (mtx & 1) * 8 + ri) *
+                                    C::PROW +
+                                (kt * 16 + (mtx >> 1) * 8) * 2);
+          // rows of unfetched positions were zeroed by the producer
+          const uint32_t vrow = vst + (kt * 16 + (mtx & 1) * 8 + ri) * vrs +
+                                64 * cb * 2;
+#pragma unroll
+          for (int jp = 0; jp < 4; ++jp) {
+            uint32_t bv[4];
+            ldsm_x4_t(bv, vrow + (2 * jp + (mtx >> 1)) * 16);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              mma_bf16(o[mt][2 * jp], pa[mt], bv[0], bv[1]);
+              mma_bf16(o[mt][2 * jp + 1], pa[mt], bv[2], bv[3]);
+            }
+          }
         }
       }
     }
