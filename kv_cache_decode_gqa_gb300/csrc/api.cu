@@ -200,15 +200,20 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
 // decode): 32-position chunks of `rows` positions (or index entries) per
 // sequence and head tile; partials of 64 heads x dv per CTA side; one
 // arrival counter per (sequence, head tile).
-Plan plan_wide(int sms, int batch, int n_h, int rows, int dv) {
+// `per_lane` CTAs of the launch share a lane's chunk range (one per head
+// tile, or per head tile and value quarter for the tensor-core latent
+// kernel); n_splits counts 64-head tiles per lane whatever the kernel.
+Plan plan_wide(int sms, int batch, int n_h, int rows, int dv,
+               int per_lane = 0, int chunk_rows = 32) {
   Plan pl;
   const int tiles = n_h / 64;
-  // lanes of `tiles` CTAs each (one per head tile) share a chunk range
-  const long chunks = (long)batch * ((rows + 31) / 32);
+  if (per_lane <= 0) per_lane = tiles;
+  const long chunks = (long)batch * ((rows + chunk_rows - 1) / chunk_rows);
   long ctas = sms;
   const int forced = env_int("KVD_DECODE_CTAS", 0);
   if (forced > 0) ctas = forced;
-  const long lanes = std::max(1L, std::min(ctas / tiles, std::max(chunks, 1L)));
+  const long lanes =
+      std::max(1L, std::min(ctas / per_lane, std::max(chunks, 1L)));
   ctas = lanes * tiles;
   pl.n_splits = (int)ctas;
   pl.n_groups = tiles;
@@ -219,8 +224,17 @@ Plan plan_wide(int sms, int batch, int n_h, int rows, int dv) {
   return pl;
 }
 
-Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms) {
-  return plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
+// The latent decode runs on the tcgen05 kernel where its shape allows
+// (KVD_MLA_CUDA_CORES=1 selects the CUDA-core kernel everywhere).
+bool mla_on_tensor_memory(const kvd_cache *c, int n_h) {
+  return env_int("KVD_MLA_CUDA_CORES", 0) == 0 &&
+         kvd::latent_tc_supported(n_h, c->block_size, c->num_blocks);
+}
+
+Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms, bool tc) {
+  return tc ? plan_wide(sms, s->batch, n_h, s->max_seq_len, dv, n_h / 32,
+                       kvd::kLatentTcRows)
+            : plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
 }
 
 Plan sparse_plan(const kvd_seqs *s, int n_h, int k, int dv, int sms) {
@@ -404,7 +418,8 @@ kvd_status kvd_workspace_size(kvd_op op, const kvd_cache *cache,
     case KVD_OP_MLA_DECODE:
       if (n_h < 64 || n_h % 64 != 0)
         return fail(KVD_ERR_UNSUPPORTED, "mla: n_h must be a multiple of 64");
-      *bytes = mla_plan(seqs, n_h, 512, d->sms).ws_bytes;
+      *bytes = mla_plan(seqs, n_h, 512, d->sms,
+                        mla_on_tensor_memory(cache, n_h)).ws_bytes;
       return ok();
     case KVD_OP_SPARSE_DECODE:
       if (n_h < 64 || n_h % 64 != 0 || k < 1)
@@ -552,7 +567,8 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
   const DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != KVD_OK) return st;
-  const Plan pl = mla_plan(seqs, n_h, d_c, d->sms);
+  const bool tc = mla_on_tensor_memory(latent, n_h);
+  const Plan pl = mla_plan(seqs, n_h, d_c, d->sms, tc);
   st = check_ws(pl, workspace, workspace_bytes, "mla_decode");
   if (st != KVD_OK) return st;
   kvd::DecodeParams p{};
@@ -582,7 +598,9 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
   p.scale_log2 = log2_scale(scale, latent->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return launched(kvd::launch_decode_mla(p, s), "mla_decode");
+  return launched(tc ? kvd::launch_decode_mla_tc(p, s)
+                     : kvd::launch_decode_mla(p, s),
+                  "mla_decode");
 }
 
 kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,

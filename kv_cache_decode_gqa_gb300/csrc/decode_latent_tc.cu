@@ -1,0 +1,558 @@
+// Latent-cache (MLA) decode on the 5th-generation tensor cores.
+//
+// DeepSeek-V2/V3 multi-head latent attention, absorbed form: every cached
+// token is one 576-wide row (512-dim latent c, then the 64-dim shared rope
+// key); a query head scores a token as q . row (q = absorbed latent query
+// followed by its rope part) and its output is the softmax-weighted sum of
+// the rows' latent parts. With 128 query heads on one row stream, the
+// decode is a dense contraction: 128 x 1088 multiply-adds per 1152 cached
+// bytes. This kernel runs it on tcgen05 MMAs with TMEM accumulators.
+//
+// Work: a persistent stream-K partition like the 64-head-tile latent
+// kernel's, over 64-position chunks, with n_h / 32 CTAs per lane: head tile
+// ht (128 heads = the MMA's M) x value quarter vq (128 of the 512 output
+// columns). Each CTA of a lane computes the full scores S = Q K^T of its
+// head tile (the softmax needs them) and O += P V for its value quarter. The
+// four quarters read the same cache rows at about the same time, so three
+// of the four reads hit L2.
+//
+// Tensor memory (512 columns x 128 lanes, lane = query head):
+//   [0, 288)    Q: the tile's 128 x 576 bf16 query (A operand of S)
+//   [288, 352)  S: 128 x 64 fp32 scores of one chunk
+//   [352, 384)  P: 128 x 64 bf16 probabilities (A operand of O)
+//   [384, 512)  O: 128 x 128 fp32 output accumulator
+// Shared memory holds only the ring of cache chunks (3 x 64 rows x 1152 B,
+// copied by TMA as nine 64-column boxes with 128-byte swizzle), so the
+// tensor core reads just the B operand from shared memory. An MMA of N = 64
+// positions streams its 128 x 16 A operand once per 64 positions; at N = 32
+// that stream, not the multiply-adds, set the MMA's duration.
+//
+// Warp roles (192 threads):
+//   warp 0, one lane: TMA producer (ring stage per chunk; block table
+//     lookup per chunk);
+//   warp 1: TMEM allocation; one lane issues the MMAs: S(j) = 36 k-steps
+//     of M=128 N=64 K=16 (A = Q in TMEM, B = K rows, K-major), and
+//     O += P(j) V(j) as 4 k-steps of M=128 N=128 K=16 (A = P in TMEM,
+//     B = the chunk's latent columns of this value quarter, MN-major);
+//   warps 2..5 (one thread per head): online softmax. Thread r reads row r
+//     of S(j) from TMEM, masks positions past the sequence end, and writes
+//     P(j) = exp2(s * scale * log2 e - m) in bf16 back to TMEM, m the
+//     running maximum of the head's scaled scores. When a chunk raises m the
+//     thread rescales its row of O in TMEM and its running sum l. They also
+//     store each unit's query tile into TMEM and write the results.
+// Order of the MMA lane: S(j+1) as soon as the softmax has read S(j) (so it
+// runs while the softmax of chunk j does), then O(j) once P(j) is written;
+// a chunk that starts a unit gets its S only after the previous unit's
+// last O (its softmax threads first write that unit's results, then the
+// new query tile). The softmax of chunk j+1 writes P and rescales O only
+// after O(j) completed.
+#include <cmath>
+
+#include "kvd_common.cuh"
+#include "stream_k.cuh"
+#include "tcgen05.cuh"
+#include "tmap.h"
+
+namespace kvd {
+namespace {
+
+constexpr int kM = 128;             // query heads per CTA (MMA M)
+constexpr int kDK = 576;            // row width (latent + rope)
+constexpr int kDV = 512;            // latent width = output width
+constexpr int kVQ = 128;            // output columns per CTA
+constexpr int kRows = kLatentTcRows;  // positions per chunk (MMA N of S)
+constexpr int kBoxes = kDK / 64;    // 128-byte column boxes of a row
+constexpr int kBoxBytes = kRows * 128;
+constexpr int kStageBytes = kBoxes * kBoxBytes;  // 73,728
+constexpr int kNS = 3;              // ring stages
+constexpr int kNB = 256;            // largest batch of these calls
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0, kColS = 288, kColP = 352, kColO = 384;
+// The softmax offset m moves when a chunk's maximum exceeds it by more than
+// this (log2 units). Any offset gives the same softmax, but the largest P is
+// then up to 2^slack and its bf16 rounding is no longer exact: 0 keeps the
+// running maximum exact, as the CUDA-core kernels do.
+constexpr float kOffsetSlack = 0.f;
+
+constexpr int K_OFF = 0;
+constexpr int WP_OFF = K_OFF + kNS * kStageBytes;
+constexpr int BAR_OFF =
+    (WP_OFF + (int)sizeof(WorkPartitionT<kNB>) + 15) / 16 * 16;
+// full[3] empty[3] sfull sfree pfull ofull qready done
+constexpr int kBars = 2 * kNS + 6;
+constexpr int FLAG_OFF = BAR_OFF + kBars * 8;
+constexpr int SMEM = FLAG_OFF + 16;
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+static_assert(kColO + kVQ == kTmemCols, "tensor memory budget");
+
+struct LatentTcParams {
+  DecodeParams p;
+  CUtensorMap tmk;  // cache rows: 3-D (64 cols, rows, 9 boxes) or 2-D
+  int maps_3d;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_latent_tc_kernel(const __grid_constant__ LatentTcParams lp) {
+  const DecodeParams &p = lp.p;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t *sk = smem + K_OFF;
+  WorkPartitionT<kNB> &wp =
+      *reinterpret_cast<WorkPartitionT<kNB> *>(smem + WP_OFF);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+  uint64_t *empty = full + kNS;
+  uint64_t *sfull = empty + kNS;
+  uint64_t *sfree = sfull + 1;
+  uint64_t *pfull = sfree + 1;
+  uint64_t *ofull = pfull + 1;
+  uint64_t *qready = ofull + 1;
+  uint64_t *done = qready + 1;
+  int *flags = reinterpret_cast<int *>(smem + FLAG_OFF);
+  int *s_len_err = flags;
+  volatile int *s_abort = flags + 1;
+  volatile int *s_issued = flags + 2;
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(flags + 3);
+
+  const int per_lane = p.n_h / 32;  // CTAs sharing a chunk range
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();  // after the wait: see the merge launch
+
+  if (tid == 0) {
+    *s_len_err = 0;
+    *s_abort = 0;
+    *s_issued = 0;
+  }
+  __syncthreads();
+  build_partition(wp, p, s_len_err, kRows, 1, 0);
+  if (tid == 0 && blockIdx.x == 0 && *s_len_err) report(p.err, DEVERR_LEN);
+  const int total = wp.total;
+  const int lanes = (int)gridDim.x / per_lane;
+  const int P = min(lanes, max(total, 1));
+  const int c = (int)blockIdx.x / per_lane;  // lane: a range of chunks
+  const int ht = ((int)blockIdx.x % per_lane) >> 2;  // head tile
+  const int vq = (int)blockIdx.x & 3;                // value quarter
+
+  if (blockIdx.x == 0) {  // sequences with nothing visible: out = 0, lse = -inf
+    for (int b = 0; b < p.batch; ++b) {
+      if (wp.nch[b] != 0) continue;
+      for (int i = tid; i < p.n_h * kDV; i += kThreads)
+        p.out[(long)b * p.n_h * kDV + i] = 0;
+      if (p.lse)
+        for (int i = tid; i < p.n_h; i += kThreads)
+          p.lse[(long)b * p.n_h + i] = -INFINITY;
+    }
+  }
+  if (c >= P || total == 0) return;  // (also CTAs beyond lanes * per_lane)
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layout needs 1 KB atoms
+    if (tid == 0) report(p.err, DEVERR_TIMEOUT);
+    return;
+  }
+  const int lo = range_lo(c, total, P);
+  const int hi = range_lo(c + 1, total, P);
+  const int n = hi - lo;
+
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sfree, kM);
+    mbar_init(pfull, kM);
+    mbar_init(ofull, 1);
+    mbar_init(qready, kM);
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
+
+  if (warp == 0) {
+    // ======================= TMA producer ==================================
+    if (lane == 0) {
+      prefetch_tmap(&lp.tmk);
+      ChunkCursor pc = cursor_at(wp, p.batch, lo);
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kNS;
+        if (i >= kNS && !mbar_wait(&empty[s], (i / kNS - 1) & 1)) {
+          report(p.err, DEVERR_TIMEOUT);
+          *s_abort = 1;
+        }
+        if (*s_abort) break;
+        const int t0 = pc.k * kRows;  // chunk start (inside one block)
+        int blk = p.block_table[(long)pc.b * p.max_blocks + t0 / p.block_size];
+        if (blk < 0 || blk >= p.num_blocks) {
+          report(p.err, DEVERR_BLOCK);
+          blk = 0;  // read a valid block; the result is flagged as wrong
+        }
+        const int row0 = blk * p.block_size + t0 % p.block_size;
+        uint8_t *dst = sk + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        if (lp.maps_3d) {
+          tma_load_3d(dst, &lp.tmk, 0, row0, 0, &full[s]);
+        } else {
+          for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d_plain(dst + j * kBoxBytes, &lp.tmk, 64 * j, row0,
+                              &full[s]);
+        }
+        *s_issued = i + 1;
+        cursor_next(wp, p.batch, 1, pc);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0) {
+      constexpr uint32_t idS = umma_idesc_bf16(kM, kRows, false);
+      constexpr uint32_t idO = umma_idesc_bf16(kM, kVQ, true);
+      const uint32_t k_addr = smem_u32(sk);
+      ChunkCursor sc = cursor_at(wp, p.batch, lo);  // next S to issue
+      ChunkCursor oc = sc;                          // next O to issue
+      int s_prev_b = -1, o_prev_b = -1, units = 0;
+      bool ok = true;
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kNS;
+        if (sc.b != s_prev_b) {  // the unit's query tile is in TMEM
+          if (!mbar_wait(qready, units & 1)) return false;
+          ++units;
+          s_prev_b = sc.b;
+        }
+        if (!mbar_wait(&full[s], (j / kNS) & 1)) return false;
+        // the softmax has read S(j-1)
+        if (j >= 1 && !mbar_wait(sfree, (j - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kst = k_addr + s * kStageBytes;
+#pragma unroll 4
+        for (int ks = 0; ks < kDK / 16; ++ks) {
+          const uint64_t b = umma_desc_sw128(
+              kst + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
+          umma_ts(tbase + kColS, tbase + kColQ + ks * 8, b, idS, ks > 0);
+        }
+        umma_commit(sfull);
+        cursor_next(wp, p.batch, 1, sc);
+        return true;
+      };
+      auto issue_o = [&](int i) -> bool {
+        const int s = i % kNS;
+        if (!mbar_wait(pfull, i & 1)) return false;
+        tc_fence_after();
+        const bool first = oc.b != o_prev_b;
+        o_prev_b = oc.b;
+        const uint32_t vst = k_addr + s * kStageBytes + 2 * vq * kBoxBytes;
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          const uint64_t b =
+              umma_desc_sw128(vst + kk * 16 * 128, kBoxBytes, 1024);
+          umma_ts(tbase + kColO, tbase + kColP + kk * 8, b, idO,
+                  (!first || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty[s]);
+        umma_commit(ofull);
+        cursor_next(wp, p.batch, 1, oc);
+        return true;
+      };
+      ok = n > 0 && issue_s(0);
+      for (int i = 0; ok && i < n; ++i) {
+        if (*s_abort) break;
+        // sc is chunk i+1's cursor here
+        const bool next_starts = i + 1 < n && sc.b != s_prev_b;
+        if (i + 1 < n && !next_starts) ok = issue_s(i + 1);
+        ok = ok && issue_o(i);
+        if (ok && next_starts) ok = issue_s(i + 1);
+      }
+      if (!ok) {
+        report(p.err, DEVERR_TIMEOUT);
+        *s_abort = 1;
+      }
+      // every MMA issued has completed before the TMEM is released
+      umma_commit(done);
+      mbar_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax and epilogue ==========================
+    const int qw = warp & 3;  // TMEM lane quarter of this warp
+    const int r = qw * 32 + lane;  // head within the tile
+    const uint32_t tl = tbase + ((uint32_t)(qw * 32) << 16);
+    const float sl2 = p.scale_log2;
+    ChunkCursor cc = cursor_at(wp, p.batch, lo);
+    float m_ref = -INFINITY, l = 0.f;
+    int cur_b = -1;
+    bool ok = true;
+
+    // results of unit b, whose last chunk was chunk `il` of the range
+    auto flush = [&](int b, int il) -> bool {
+      const bool w = mbar_wait(ofull, il & 1);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after();
+      const int ustart = wp.pre[b];
+      const int uend = ustart + wp.nch[b];
+      const bool whole = ustart >= lo && uend <= hi;
+      const long wslot = (long)c * 2 + partial_side(ustart, lo);
+      const long head = (long)ht * kM + r;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int pc = 0; pc < kVQ / 32; ++pc) {
+        uint32_t o[32];
+        tmem_ld32(tl + kColO + pc * 32, o);
+        tmem_wait_ld(o);
+        const int col = vq * kVQ + pc * 32;
+        if (whole) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              p.out + ((long)b * p.n_h + head) * kDV + col);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * q4]) * inv,
+                              __uint_as_float(o[8 * q4 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv,
+                              __uint_as_float(o[8 * q4 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv,
+                              __uint_as_float(o[8 * q4 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv,
+                              __uint_as_float(o[8 * q4 + 7]) * inv);
+            dst[q4] = v;
+          }
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(
+              p.ws_o + (wslot * p.n_h + head) * kDV + col);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv,
+                                  __uint_as_float(o[4 * q4 + 1]) * inv,
+                                  __uint_as_float(o[4 * q4 + 2]) * inv,
+                                  __uint_as_float(o[4 * q4 + 3]) * inv);
+        }
+      }
+      if (vq == 0) {
+        const float lse =
+            l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (whole) {
+          if (p.lse) p.lse[(long)b * p.n_h + head] = lse;
+        } else {
+          p.ws_lse[wslot * p.n_h + head] = lse;
+        }
+      }
+      return true;
+    };
+
+    for (int i = 0; i < n; ++i) {
+      if (__any_sync(0xffffffffu, *s_abort)) {
+        ok = false;
+        break;
+      }
+      const bool first = cc.b != cur_b;
+      if (first) {
+        if (cur_b >= 0 && !flush(cur_b, i - 1)) {
+          ok = false;
+          break;
+        }
+        cur_b = cc.b;
+        m_ref = -INFINITY;
+        l = 0.f;
+        // the unit's query row of this head into TMEM columns [0, 288)
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(
+            p.q + ((long)cc.b * p.n_h + (long)ht * kM + r) * kDK);
+#pragma unroll 1
+        for (int pc = 0; pc < kBoxes; ++pc) {
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 u = __ldg(qrow + pc * 8 + j);
+            v[4 * j] = u.x;
+            v[4 * j + 1] = u.y;
+            v[4 * j + 2] = u.z;
+            v[4 * j + 3] = u.w;
+          }
+          tmem_st32(tl + kColQ + pc * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(qready);
+      }
+      const bool w = mbar_wait(sfull, i & 1);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[kRows];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int h2 = 0; h2 < kRows / 32; ++h2) {
+          tmem_ld32(tl + kColS + h2 * 32, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[h2 * 32 + j] = __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(sfree);
+
+      const int nvalid = min(kRows, wp.len[cc.b] - cc.k * kRows);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        x[j] = j < nvalid ? x[j] * sl2 : -INFINITY;
+        mx = fmaxf(mx, x[j]);
+      }
+      bool need = false;
+      if (first) {
+        m_ref = mx;
+      } else {
+        need = mx > m_ref + kOffsetSlack;
+      }
+      if (i >= 1) {  // O(i-1) has read P and written O
+        const bool w2 = mbar_wait(ofull, (i - 1) & 1);
+        if (!__all_sync(0xffffffffu, w2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {  // rescale this row of O
+        const float cr = need ? ex2(m_ref - mx) : 1.f;
+#pragma unroll 1
+        for (int pc = 0; pc < kVQ / 32; ++pc) {
+          uint32_t o[32];
+          tmem_ld32(tl + kColO + pc * 32, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            o[j] = __float_as_uint(__uint_as_float(o[j]) * cr);
+          tmem_st32(tl + kColO + pc * 32, o);
+        }
+        if (need) {
+          l *= cr;
+          m_ref = mx;
+        }
+      }
+      const float u = m_ref == -INFINITY ? 0.f : m_ref;
+      float sum = 0.f;
+#pragma unroll
+      for (int h2 = 0; h2 < kRows / 32; ++h2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = ex2(x[h2 * 32 + 2 * j] - u);
+          const float p1 = ex2(x[h2 * 32 + 2 * j + 1] - u);
+          sum += p0 + p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tl + kColP + h2 * 16, pk);
+      }
+      l += sum;
+      tmem_wait_st();
+      if (nvalid < kRows) {
+        // rows past the sequence end hold whatever the block held: zero this
+        // quarter's value columns of them, so that P = 0 meets no NaN
+        uint8_t *vb = sk + (i % kNS) * kStageBytes + 2 * vq * kBoxBytes;
+        const int cnt = (kRows - nvalid) * 2 * 8;  // 16-byte pieces
+        for (int e = r; e < cnt; e += kM) {
+          const int row = nvalid + e / 16, box = (e / 8) & 1, piece = e & 7;
+          *reinterpret_cast<uint4 *>(vb + box * kBoxBytes + row * 128 +
+                                     piece * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(pfull);
+      cursor_next(wp, p.batch, 1, cc);
+    }
+    if (ok && cur_b >= 0 && !flush(cur_b, n - 1)) ok = false;
+    if (!ok && lane == 0) {
+      report(p.err, DEVERR_TIMEOUT);
+      *s_abort = 1;
+    }
+  }
+
+  // ======================= teardown ========================================
+  if (tid == 0 && *s_abort) {
+    // no copy may still land in this CTA's shared memory after it exits
+    const int issued = *s_issued;
+    for (int s = 0; s < kNS; ++s) {
+      int last = -1;
+      for (int c2 = s; c2 < issued; c2 += kNS) last = c2;
+      if (last >= 0) mbar_wait(&full[s], (last / kNS) & 1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// The cache as [rows][576] bf16 rows of 1152 bytes: preferably a 3-D view
+// (64 columns, rows, 9 column boxes at 128-byte steps) so that one copy
+// fetches a chunk's nine 128-byte-swizzled boxes; else a 2-D view and nine
+// copies per chunk.
+cudaError_t make_latent_map(CUtensorMap *m, const void *base, long rows,
+                            int *maps_3d) {
+  {
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)kBoxes};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kBoxes};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = tensor_map_encoder()(
+        m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+      *maps_3d = 1;
+      return cudaSuccess;
+    }
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDK * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = tensor_map_encoder()(
+      m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  *maps_3d = 0;
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool latent_tc_supported(int n_h, int block_size, long num_blocks) {
+  return n_h % kM == 0 && block_size % kRows == 0 &&
+         num_blocks * block_size < (1L << 31) && tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s) {
+  if (p.dk != kDK || p.dv != kDV || p.batch > kNB || p.n_kv != 1 ||
+      !latent_tc_supported(p.n_h, p.block_size, p.num_blocks))
+    return cudaErrorNotSupported;
+  LatentTcParams lp;
+  lp.p = p;
+  cudaError_t e = make_latent_map(
+      &lp.tmk, p.k, (long)p.num_blocks * p.block_size, &lp.maps_3d);
+  if (e != cudaSuccess) return e;
+  auto kern = decode_latent_tc_kernel;
+  static bool done[64] = {};
+  e = set_smem_once(kern, SMEM, done);
+  if (e != cudaSuccess) return e;
+  // n_splits counts 64-head tiles per lane (the partial layout and the
+  // merge use it); this launch has n_h / 32 CTAs per lane.
+  const int lanes = p.n_splits / (p.n_h / 64);
+  e = launch_pdl(kern, dim3(lanes * (p.n_h / 32)), dim3(kThreads), SMEM, s, 1,
+                 lp);
+  if (e != cudaSuccess || lanes <= 1) return e;
+  return launch_merge_mla(p, kRows, s);
+}
+
+}  // namespace kvd

@@ -515,7 +515,7 @@ constexpr int kMergeThreads = 256;
 // lanes, all of a lane's loads in flight at once). Part i is the partial of
 // lane c_first + i: side 1 of the first covering lane, side 0 of the
 // others.
-template <int DV, bool GATHER>
+template <int DV, bool GATHER, int ROWS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_wide_kernel(const DecodeParams p) {
   __shared__ WorkPartitionT<kNB> wp;
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   // (this launch's only possible predecessor still running, since it lets
   // its dependants start only after its own predecessor has completed)
   // does not write them. The partials are read after pdl_wait.
-  build_partition(wp, p, &s_len_err, kRows, 1, GATHER ? p.n_idx : 0);
+  build_partition(wp, p, &s_len_err, ROWS, 1, GATHER ? p.n_idx : 0);
   pdl_wait();
   const int total = wp.total;
   if (total == 0 || wp.nch[b] == 0) return;
@@ -560,6 +560,14 @@ __global__ void __launch_bounds__(kMergeThreads)
     p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
+// ROWS: positions per chunk of the decode launch whose partials are merged.
+template <int DV, bool GATHER, int ROWS = kRows>
+cudaError_t launch_merge_wide(const DecodeParams &p, cudaStream_t s) {
+  const dim3 grid(p.batch * (p.n_h / kHeads), kMergeSlices);
+  return launch_pdl(merge_wide_kernel<DV, GATHER, ROWS>, grid,
+                    dim3(kMergeThreads), 0, s, 1, p);
+}
+
 template <int DK, int DV, bool GATHER>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   using C = WCfg<DK, DV, GATHER>;
@@ -570,12 +578,17 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s, 1, p);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  const dim3 grid(p.batch * (p.n_h / kHeads), kMergeSlices);
-  return launch_pdl(merge_wide_kernel<DV, GATHER>, grid, dim3(kMergeThreads),
-                    0, s, 1, p);
+  return launch_merge_wide<DV, GATHER>(p, s);
 }
 
 }  // namespace
+
+cudaError_t launch_merge_mla(const DecodeParams &p, int rows,
+                             cudaStream_t s) {
+  if (rows == 64) return launch_merge_wide<512, false, 64>(p, s);
+  if (rows == kRows) return launch_merge_wide<512, false, kRows>(p, s);
+  return cudaErrorNotSupported;
+}
 
 cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s) {
   if (p.dk != 576 || p.dv != 512 || p.n_h % kHeads != 0 || p.batch > kNB)

@@ -97,8 +97,17 @@ cudaError_t launch_decode_mma(const DecodeParams &p, int dtype,
 // kv heads the tensor-core kernel takes per work unit (its plan and its
 // launch must agree).
 int mma_heads_per_unit(int n_kv, int block_size, int dtype);
-// MLA latent decode (dk 576, dv 512, n_h multiple of 64).
+// MLA latent decode (dk 576, dv 512, n_h multiple of 64), CUDA-core MMAs.
 cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s);
+// The same on tcgen05 tensor cores (n_h multiple of 128, block_size a
+// multiple of 64): 64-position chunks, n_h / 32 CTAs per lane of
+// n_splits / (n_h / 64).
+constexpr int kLatentTcRows = 64;
+bool latent_tc_supported(int n_h, int block_size, long num_blocks);
+cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s);
+// Log-sum-exp merge of the latent decode's split units (chunks of `rows`
+// positions: 32 for the CUDA-core kernel, 64 for the tensor-core one).
+cudaError_t launch_merge_mla(const DecodeParams &p, int rows, cudaStream_t s);
 // Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64).
 cudaError_t launch_decode_sparse(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
