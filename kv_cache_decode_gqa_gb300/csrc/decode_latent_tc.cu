@@ -30,7 +30,8 @@
 // Warp roles (192 threads):
 //   warp 0, one lane: TMA producer (ring stage per chunk; block table
 //     lookup per chunk);
-//   warp 1: TMEM allocation; one lane issues the MMAs: S(j) = 36 k-steps
+//   warp 1: TMEM allocation; the MMA loop (one elected lane issues each
+//     MMA, the warp keeps the operands uniform): S(j) = 36 k-steps
 //     of M=128 N=64 K=16 (A = Q in TMEM, B = K rows, K-major), and
 //     O += P(j) V(j) as 4 k-steps of M=128 N=128 K=16 (A = P in TMEM,
 //     B = the chunk's latent columns of this value quarter, MN-major);
@@ -209,72 +210,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer ====================================
-    if (lane == 0) {
-      constexpr uint32_t idS = umma_idesc_bf16(kM, kRows, false);
-      constexpr uint32_t idO = umma_idesc_bf16(kM, kVQ, true);
-      const uint32_t k_addr = smem_u32(sk);
-      ChunkCursor sc = cursor_at(wp, p.batch, lo);  // next S to issue
-      ChunkCursor oc = sc;                          // next O to issue
-      int s_prev_b = -1, o_prev_b = -1, units = 0;
-      bool ok = true;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kNS;
-        if (sc.b != s_prev_b) {  // the unit's query tile is in TMEM
-          if (!mbar_wait(qready, units & 1)) return false;
-          ++units;
-          s_prev_b = sc.b;
-        }
-        if (!mbar_wait(&full[s], (j / kNS) & 1)) return false;
-        // the softmax has read S(j-1)
-        if (j >= 1 && !mbar_wait(sfree, (j - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kst = k_addr + s * kStageBytes;
-#pragma unroll 4
-        for (int ks = 0; ks < kDK / 16; ++ks) {
-          const uint64_t b = umma_desc_sw128(
-              kst + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-          umma_ts(tbase + kColS, tbase + kColQ + ks * 8, b, idS, ks > 0);
-        }
-        umma_commit(sfull);
-        cursor_next(wp, p.batch, 1, sc);
-        return true;
-      };
-      auto issue_o = [&](int i) -> bool {
-        const int s = i % kNS;
-        if (!mbar_wait(pfull, i & 1)) return false;
-        tc_fence_after();
-        const bool first = oc.b != o_prev_b;
-        o_prev_b = oc.b;
-        const uint32_t vst = k_addr + s * kStageBytes + 2 * vq * kBoxBytes;
+    // The whole warp runs this loop (warp-uniform values); one elected lane
+    // issues each MMA and commit.
+    constexpr uint32_t idS = umma_idesc_bf16(kM, kRows, false);
+    constexpr uint32_t idO = umma_idesc_bf16(kM, kVQ, true);
+    const uint32_t k_addr = smem_u32(sk);
+    ChunkCursor sc = cursor_at(wp, p.batch, lo);  // next S to issue
+    ChunkCursor oc = sc;                          // next O to issue
+    int s_prev_b = -1, o_prev_b = -1, units = 0;
+    bool ok = true;
+    auto wait_all = [&](uint64_t *bar, int parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    };
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % kNS;
+      if (sc.b != s_prev_b) {  // the unit's query tile is in TMEM
+        if (!wait_all(qready, units & 1)) return false;
+        ++units;
+        s_prev_b = sc.b;
+      }
+      if (!wait_all(&full[s], (j / kNS) & 1)) return false;
+      // the softmax has read S(j-1)
+      if (j >= 1 && !wait_all(sfree, (j - 1) & 1)) return false;
+      tc_fence_after();
+      // K-major B: box ks / 4 of the stage, 32-byte step ks % 4 inside the
+      // 128-byte swizzled row (descriptor address field in 16-byte units)
+      const uint64_t b0 = umma_desc_sw128(k_addr + s * kStageBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk) {
-          const uint64_t b =
-              umma_desc_sw128(vst + kk * 16 * 128, kBoxBytes, 1024);
-          umma_ts(tbase + kColO, tbase + kColP + kk * 8, b, idO,
-                  (!first || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&empty[s]);
-        umma_commit(ofull);
-        cursor_next(wp, p.batch, 1, oc);
-        return true;
-      };
-      ok = n > 0 && issue_s(0);
-      for (int i = 0; ok && i < n; ++i) {
-        if (*s_abort) break;
-        // sc is chunk i+1's cursor here
-        const bool next_starts = i + 1 < n && sc.b != s_prev_b;
-        if (i + 1 < n && !next_starts) ok = issue_s(i + 1);
-        ok = ok && issue_o(i);
-        if (ok && next_starts) ok = issue_s(i + 1);
-      }
-      if (!ok) {
-        report(p.err, DEVERR_TIMEOUT);
-        *s_abort = 1;
-      }
-      // every MMA issued has completed before the TMEM is released
-      umma_commit(done);
-      mbar_wait(done, 0);
+      for (int ks = 0; ks < kDK / 16; ++ks)
+        umma_ts_elect(tbase + kColS, tbase + kColQ + ks * 8,
+                      b0 + (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >>
+                                      4),
+                      idS, ks > 0 ? 1u : 0u);
+      umma_commit_elect(sfull);
+      cursor_next(wp, p.batch, 1, sc);
+      return true;
+    };
+    auto issue_o = [&](int i) -> bool {
+      const int s = i % kNS;
+      if (!wait_all(pfull, i & 1)) return false;
+      tc_fence_after();
+      const bool first = oc.b != o_prev_b;
+      o_prev_b = oc.b;
+      // MN-major B: the quarter's two 64-column boxes (LBO apart), 16
+      // positions (2 groups of 8 rows, SBO apart) per k-step
+      const uint64_t b0 = umma_desc_sw128(
+          k_addr + s * kStageBytes + 2 * vq * kBoxBytes, kBoxBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kRows / 16; ++kk)
+        umma_ts_elect(tbase + kColO, tbase + kColP + kk * 8,
+                      b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
+                      (!first || kk > 0) ? 1u : 0u);
+      umma_commit_elect(&empty[s]);
+      umma_commit_elect(ofull);
+      cursor_next(wp, p.batch, 1, oc);
+      return true;
+    };
+    ok = n > 0 && issue_s(0);
+    for (int i = 0; ok && i < n; ++i) {
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      // sc is chunk i+1's cursor here
+      const bool next_starts = i + 1 < n && sc.b != s_prev_b;
+      if (i + 1 < n && !next_starts) ok = issue_s(i + 1);
+      ok = ok && issue_o(i);
+      if (ok && next_starts) ok = issue_s(i + 1);
     }
+    if (!ok && lane == 0) {
+      report(p.err, DEVERR_TIMEOUT);
+      *s_abort = 1;
+    }
+    // every MMA issued has completed before the TMEM is released
+    umma_commit_elect(done);
+    mbar_wait(done, 0);
     __syncwarp();
   } else {
     // ======================= softmax and epilogue ==========================

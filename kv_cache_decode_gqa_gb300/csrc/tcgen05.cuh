@@ -77,6 +77,46 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// The same two MMAs issued by one elected lane of a converged warp: the
+// whole warp runs the issuing loop, so that the operands stay warp-uniform
+// values (a loop inside `if (lane == 0)` rebuilds and moves them for every
+// instruction, and issues at a fraction of the tensor core's rate).
+__device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Commit by one elected lane of a converged warp.
+__device__ __forceinline__ void umma_commit_elect(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // One arrival on `bar` once every MMA this thread issued so far completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
