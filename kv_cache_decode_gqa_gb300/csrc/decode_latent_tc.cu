@@ -21,18 +21,19 @@
 //   [288, 352)  S: 128 x 64 fp32 scores of one chunk
 //   [352, 384)  P: 128 x 64 bf16 probabilities (A operand of O)
 //   [384, 512)  O: 128 x 128 fp32 output accumulator
-// Shared memory holds only the ring of cache chunks (3 x 64 rows x 1152 B,
-// copied by TMA as nine 64-column boxes with 128-byte swizzle), so the
-// tensor core reads just the B operand from shared memory. An MMA of N = 64
+// Shared memory holds only rings of cache chunks (64 rows x 1152 B, copied
+// by TMA as nine 64-column boxes with 128-byte swizzle), so the tensor core
+// reads just the B operand from shared memory. An MMA of N = 64
 // positions streams its 128 x 16 A operand once per 64 positions; at N = 32
 // that stream, not the multiply-adds, set the MMA's duration.
 //
 // Warp roles (192 threads):
-//   warp 0, one lane: TMA producer (ring stage per chunk; block table
-//     lookup per chunk);
+//   warp 0, one lane: TMA producer (per chunk: the block table lookup,
+//     seven score-only boxes into the score ring, this quarter's two value
+//     boxes into the value ring);
 //   warp 1: TMEM allocation; the MMA loop (one elected lane issues each
-//     MMA, the warp keeps the operands uniform): S(j) = 36 k-steps
-//     of M=128 N=64 K=16 (A = Q in TMEM, B = K rows, K-major), and
+//     MMA, the warp keeps the operands uniform): S(j) = 36 k-steps of
+//     M=128 N=64 K=16 (A = Q in TMEM, B = K rows, K-major), and
 //     O += P(j) V(j) as 4 k-steps of M=128 N=128 K=16 (A = P in TMEM,
 //     B = the chunk's latent columns of this value quarter, MN-major);
 //   warps 2..5 (one thread per head): online softmax. Thread r reads row r
@@ -41,12 +42,12 @@
 //     running maximum of the head's scaled scores. When a chunk raises m the
 //     thread rescales its row of O in TMEM and its running sum l. They also
 //     store each unit's query tile into TMEM and write the results.
-// Order of the MMA lane: S(j+1) as soon as the softmax has read S(j) (so it
-// runs while the softmax of chunk j does), then O(j) once P(j) is written;
-// a chunk that starts a unit gets its S only after the previous unit's
-// last O (its softmax threads first write that unit's results, then the
-// new query tile). The softmax of chunk j+1 writes P and rescales O only
-// after O(j) completed.
+// Order of the MMA warp: S(j+1) as soon as the softmax has read S(j) (so it
+// runs while the softmax of chunk j does), then O(j) once P(j) is written
+// (the tensor core runs them in issue order); a chunk that starts a unit
+// gets its S only after the previous unit's last O (its softmax threads
+// first write that unit's results, then the new query tile). The softmax
+// of chunk j+1 writes P and rescales O only after O(j) completed.
 #include <cmath>
 
 #include "kvd_common.cuh"
@@ -64,8 +65,14 @@ constexpr int kVQ = 128;            // output columns per CTA
 constexpr int kRows = kLatentTcRows;  // positions per chunk (MMA N of S)
 constexpr int kBoxes = kDK / 64;    // 128-byte column boxes of a row
 constexpr int kBoxBytes = kRows * 128;
-constexpr int kStageBytes = kBoxes * kBoxBytes;  // 73,728
-constexpr int kNS = 3;              // ring stages
+// A chunk's nine boxes go to two rings: the seven that only the scores read
+// (freed as soon as S has run) and the two of this CTA's value quarter
+// (read by S and by P V, freed after P V). So a chunk's copy starts about
+// two periods before its S needs it, not one.
+constexpr int kKBoxes = kBoxes - 2;
+constexpr int kKSlot = kKBoxes * kBoxBytes;  // 57,344
+constexpr int kVSlot = 2 * kBoxBytes;        // 16,384
+constexpr int kNS = 3;              // slots of each ring
 constexpr int kNB = 256;            // largest batch of these calls
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
@@ -77,11 +84,12 @@ constexpr uint32_t kColQ = 0, kColS = 288, kColP = 352, kColO = 384;
 constexpr float kOffsetSlack = 0.f;
 
 constexpr int K_OFF = 0;
-constexpr int WP_OFF = K_OFF + kNS * kStageBytes;
+constexpr int V_OFF = K_OFF + kNS * kKSlot;
+constexpr int WP_OFF = V_OFF + kNS * kVSlot;
 constexpr int BAR_OFF =
     (WP_OFF + (int)sizeof(WorkPartitionT<kNB>) + 15) / 16 * 16;
-// full[3] empty[3] sfull sfree pfull ofull qready done
-constexpr int kBars = 2 * kNS + 6;
+// kfull[3] kempty[3] vfull[3] vempty[3] sfull sfree pfull ofull qready done
+constexpr int kBars = 4 * kNS + 6;
 constexpr int FLAG_OFF = BAR_OFF + kBars * 8;
 constexpr int SMEM = FLAG_OFF + 16;
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -89,8 +97,7 @@ static_assert(kColO + kVQ == kTmemCols, "tensor memory budget");
 
 struct LatentTcParams {
   DecodeParams p;
-  CUtensorMap tmk;  // cache rows: 3-D (64 cols, rows, 9 boxes) or 2-D
-  int maps_3d;
+  CUtensorMap tmk;  // cache rows [rows][576], 64-column boxes
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -98,11 +105,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const DecodeParams &p = lp.p;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sk = smem + K_OFF;
+  uint8_t *sv = smem + V_OFF;
   WorkPartitionT<kNB> &wp =
       *reinterpret_cast<WorkPartitionT<kNB> *>(smem + WP_OFF);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
-  uint64_t *empty = full + kNS;
-  uint64_t *sfull = empty + kNS;
+  uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+  uint64_t *kempty = kfull + kNS;
+  uint64_t *vfull = kempty + kNS;
+  uint64_t *vempty = vfull + kNS;
+  uint64_t *sfull = vempty + kNS;
   uint64_t *sfree = sfull + 1;
   uint64_t *pfull = sfree + 1;
   uint64_t *ofull = pfull + 1;
@@ -155,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
     }
     mbar_init(sfull, 1);
     mbar_init(sfree, kM);
@@ -182,11 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ChunkCursor pc = cursor_at(wp, p.batch, lo);
       for (int i = 0; i < n; ++i) {
         const int s = i % kNS;
-        if (i >= kNS && !mbar_wait(&empty[s], (i / kNS - 1) & 1)) {
-          report(p.err, DEVERR_TIMEOUT);
-          *s_abort = 1;
-        }
-        if (*s_abort) break;
         const int t0 = pc.k * kRows;  // chunk start (inside one block)
         int blk = p.block_table[(long)pc.b * p.max_blocks + t0 / p.block_size];
         if (blk < 0 || blk >= p.num_blocks) {
@@ -194,16 +201,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           blk = 0;  // read a valid block; the result is flagged as wrong
         }
         const int row0 = blk * p.block_size + t0 % p.block_size;
-        uint8_t *dst = sk + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        if (lp.maps_3d) {
-          tma_load_3d(dst, &lp.tmk, 0, row0, 0, &full[s]);
-        } else {
-          for (int j = 0; j < kBoxes; ++j)
-            tma_load_2d_plain(dst + j * kBoxBytes, &lp.tmk, 64 * j, row0,
-                              &full[s]);
+        // the seven score-only boxes, once S(i - 3) has run
+        if (i >= kNS && !mbar_wait(&kempty[s], (i / kNS - 1) & 1)) {
+          report(p.err, DEVERR_TIMEOUT);
+          *s_abort = 1;
         }
-        *s_issued = i + 1;
+        if (*s_abort) break;
+        mbar_arrive_expect_tx(&kfull[s], kKSlot);
+        for (int z = 0, j = 0; z < kBoxes; ++z) {
+          if (z == 2 * vq || z == 2 * vq + 1) continue;
+          tma_load_2d_plain(sk + s * kKSlot + j * kBoxBytes, &lp.tmk, 64 * z,
+                            row0, &kfull[s]);
+          ++j;
+        }
+        *s_issued = 2 * i + 1;
+        // the value quarter's two boxes, once P V of chunk i - 3 has run
+        if (i >= kNS && !mbar_wait(&vempty[s], (i / kNS - 1) & 1)) {
+          report(p.err, DEVERR_TIMEOUT);
+          *s_abort = 1;
+        }
+        if (*s_abort) break;
+        mbar_arrive_expect_tx(&vfull[s], kVSlot);
+        for (int z = 0; z < 2; ++z)
+          tma_load_2d_plain(sv + s * kVSlot + z * kBoxBytes, &lp.tmk,
+                            64 * (2 * vq + z), row0, &vfull[s]);
+        *s_issued = 2 * i + 2;
         cursor_next(wp, p.batch, 1, pc);
       }
     }
@@ -214,13 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issues each MMA and commit.
     constexpr uint32_t idS = umma_idesc_bf16(kM, kRows, false);
     constexpr uint32_t idO = umma_idesc_bf16(kM, kVQ, true);
-    const uint32_t k_addr = smem_u32(sk);
+    const uint32_t k_addr = smem_u32(sk), v_addr = smem_u32(sv);
     ChunkCursor sc = cursor_at(wp, p.batch, lo);  // next S to issue
     ChunkCursor oc = sc;                          // next O to issue
     int s_prev_b = -1, o_prev_b = -1, units = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t *bar, int parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+      return __all_sync(0xffffffffu, mbar_wait_fast(bar, parity));
     };
     auto issue_s = [&](int j) -> bool {
       const int s = j % kNS;
@@ -229,20 +251,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++units;
         s_prev_b = sc.b;
       }
-      if (!wait_all(&full[s], (j / kNS) & 1)) return false;
+      if (!wait_all(&kfull[s], (j / kNS) & 1)) return false;
+      if (!wait_all(&vfull[s], (j / kNS) & 1)) return false;
       // the softmax has read S(j-1)
       if (j >= 1 && !wait_all(sfree, (j - 1) & 1)) return false;
       tc_fence_after();
-      // K-major B: box ks / 4 of the stage, 32-byte step ks % 4 inside the
-      // 128-byte swizzled row (descriptor address field in 16-byte units)
-      const uint64_t b0 = umma_desc_sw128(k_addr + s * kStageBytes, 16, 1024);
+      // K-major B: box z = ks / 4 (in the value ring if it is one of this
+      // quarter's two, else in the score ring), 32-byte step ks % 4 inside
+      // the 128-byte swizzled row (descriptor address in 16-byte units)
+      const uint64_t bk = umma_desc_sw128(k_addr + s * kKSlot, 16, 1024);
+      const uint64_t bv = umma_desc_sw128(v_addr + s * kVSlot, 16, 1024);
 #pragma unroll
-      for (int ks = 0; ks < kDK / 16; ++ks)
+      for (int ks = 0; ks < kDK / 16; ++ks) {
+        const int z = ks >> 2;
+        const uint64_t b =
+            z == 2 * vq || z == 2 * vq + 1
+                ? bv + (uint64_t)(((z - 2 * vq) * kBoxBytes) >> 4)
+                : bk + (uint64_t)(((z < 2 * vq ? z : z - 2) * kBoxBytes) >> 4);
         umma_ts_elect(tbase + kColS, tbase + kColQ + ks * 8,
-                      b0 + (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >>
-                                      4),
-                      idS, ks > 0 ? 1u : 0u);
+                      b + (uint64_t)(((ks & 3) * 32) >> 4), idS,
+                      ks > 0 ? 1u : 0u);
+      }
       umma_commit_elect(sfull);
+      umma_commit_elect(&kempty[s]);
       cursor_next(wp, p.batch, 1, sc);
       return true;
     };
@@ -254,14 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       o_prev_b = oc.b;
       // MN-major B: the quarter's two 64-column boxes (LBO apart), 16
       // positions (2 groups of 8 rows, SBO apart) per k-step
-      const uint64_t b0 = umma_desc_sw128(
-          k_addr + s * kStageBytes + 2 * vq * kBoxBytes, kBoxBytes, 1024);
+      const uint64_t b0 = umma_desc_sw128(v_addr + s * kVSlot, kBoxBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kRows / 16; ++kk)
         umma_ts_elect(tbase + kColO, tbase + kColP + kk * 8,
                       b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
                       (!first || kk > 0) ? 1u : 0u);
-      umma_commit_elect(&empty[s]);
+      umma_commit_elect(&vempty[s]);
       umma_commit_elect(ofull);
       cursor_next(wp, p.batch, 1, oc);
       return true;
@@ -461,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nvalid < kRows) {
         // rows past the sequence end hold whatever the block held: zero this
         // quarter's value columns of them, so that P = 0 meets no NaN
-        uint8_t *vb = sk + (i % kNS) * kStageBytes + 2 * vq * kBoxBytes;
+        uint8_t *vb = sv + (i % kNS) * kVSlot;
         const int cnt = (kRows - nvalid) * 2 * 8;  // 16-byte pieces
         for (int e = r; e < cnt; e += kM) {
           const int row = nvalid + e / 16, box = (e / 8) & 1, piece = e & 7;
@@ -484,11 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ======================= teardown ========================================
   if (tid == 0 && *s_abort) {
     // no copy may still land in this CTA's shared memory after it exits
+    // loads issued: chunk i's score part when issued > 2i, its value part
+    // when issued > 2i + 1; wait for the last one of each slot
     const int issued = *s_issued;
+    const int nk = (issued + 1) >> 1, nv = issued >> 1;
     for (int s = 0; s < kNS; ++s) {
-      int last = -1;
-      for (int c2 = s; c2 < issued; c2 += kNS) last = c2;
-      if (last >= 0) mbar_wait(&full[s], (last / kNS) & 1);
+      int lk = -1, lv = -1;
+      for (int i = s; i < nk; i += kNS) lk = i;
+      for (int i = s; i < nv; i += kNS) lv = i;
+      if (lk >= 0) mbar_wait(&kfull[s], (lk / kNS) & 1);
+      if (lv >= 0) mbar_wait(&vfull[s], (lv / kNS) & 1);
     }
   }
   tc_fence_before();
@@ -499,27 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// The cache as [rows][576] bf16 rows of 1152 bytes: preferably a 3-D view
-// (64 columns, rows, 9 column boxes at 128-byte steps) so that one copy
-// fetches a chunk's nine 128-byte-swizzled boxes; else a 2-D view and nine
-// copies per chunk.
-cudaError_t make_latent_map(CUtensorMap *m, const void *base, long rows,
-                            int *maps_3d) {
-  {
-    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)kBoxes};
-    const cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kBoxes};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = tensor_map_encoder()(
-        m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
-        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r == CUDA_SUCCESS) {
-      *maps_3d = 1;
-      return cudaSuccess;
-    }
-  }
+// The cache as a 2-D tensor [rows][576] of bf16 rows (1152 bytes), copied
+// in boxes of 64 columns (128 bytes) x one chunk of rows, 128-byte swizzle.
+cudaError_t make_latent_map(CUtensorMap *m, const void *base, long rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kDK * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
@@ -529,7 +546,6 @@ cudaError_t make_latent_map(CUtensorMap *m, const void *base, long rows,
       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  *maps_3d = 0;
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -546,8 +562,8 @@ cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s) {
     return cudaErrorNotSupported;
   LatentTcParams lp;
   lp.p = p;
-  cudaError_t e = make_latent_map(
-      &lp.tmk, p.k, (long)p.num_blocks * p.block_size, &lp.maps_3d);
+  cudaError_t e =
+      make_latent_map(&lp.tmk, p.k, (long)p.num_blocks * p.block_size);
   if (e != cudaSuccess) return e;
   auto kern = decode_latent_tc_kernel;
   static bool done[64] = {};

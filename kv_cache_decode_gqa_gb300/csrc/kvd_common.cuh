@@ -107,6 +107,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar` (true once it completed).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`. Each try_wait may suspend the
 // thread for a short hardware-defined time; 2^22 tries bound the wait to well
 // under a few seconds. Returns false (and the caller reports
@@ -115,6 +128,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   for (uint32_t i = 0; i < (1u << 22); ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+
+// The same, testing first without blocking: a phase that has already
+// completed costs a test instead of a potentially suspending try_wait.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar,
+                                               uint32_t parity) {
+  return mbar_test_wait(bar, parity) || mbar_wait(bar, parity);
 }
 
 // ---------------------------------------------------------------------------
