@@ -45,6 +45,7 @@ from kv_cache_decode_gqa_gb300 import workloads as W  # noqa: E402
 METRIC = ("decode attn: KV-read HBM GB/s (% of GB300 peak) and decode "
           "tokens/s per layer")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------
@@ -82,14 +83,27 @@ def decode_launch_bytes(shape):
     return b
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return ({"hbm_gbs": FALLBACK_HBM_GBS}.get(key, FALLBACK_BF16_TFLOPS),
+                "fallback")
+
+
+def latent_flops(shape):
+    """Multiply-add work of one latent decode call, in FLOPs: useful (each
+    head scores every cached row over 576 dims and sums 512 latent dims) and
+    issued by the tensor-core kernel (each of a lane's four value-quarter
+    CTAs computes the full scores of its 128 heads)."""
+    s = shape
+    rows = sum(s.seq_lens)
+    useful = 2 * rows * s.n_h * (s.head_dim + s.dv)
+    issued = 2 * rows * s.n_h * (4 * s.head_dim + s.dv)
+    return useful, issued
 
 
 def profile_traffic(kernel_tag):
@@ -621,6 +635,17 @@ def run_ours(args, ws, rank, local):
                      "traffic": profile_traffic(kern_tag)},
         "clocks": clock_info,
     }
+    if s.kind == "mla":
+        # the latent decode runs on the tensor cores: its tensor-side rate
+        # against the measured bf16 peak (burst: the kernel is timed alone)
+        useful, issued = latent_flops(s)
+        tpk, tsrc = measured_peaks("bf16_tflops")
+        line["roofline"]["tensor"] = {
+            "useful_tflops": round(useful / (kern_ms / 1e3) / 1e12, 1),
+            "issued_tflops": round(issued / (kern_ms / 1e3) / 1e12, 1),
+            "peak": tpk, "peak_source": tsrc, "unit": "TFLOP/s",
+            "frac_issued": round(issued / (kern_ms / 1e3) / 1e12 / tpk, 4),
+            "flops_per_launch": {"useful": useful, "issued": issued}}
     return line
 
 

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s_prev_b = -1, o_prev_b = -1, units = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t *bar, int parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait_fast(bar, parity));
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
     auto issue_s = [&](int j) -> bool {
       const int s = j % kNS;

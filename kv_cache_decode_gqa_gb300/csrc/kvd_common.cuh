@@ -124,17 +124,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // thread for a short hardware-defined time; 2^22 tries bound the wait to well
 // under a few seconds. Returns false (and the caller reports
 // KVD_DEVERR_TIMEOUT) if the phase never completed.
+// A non-blocking test comes first: a phase that has already completed then
+// costs a test instead of a try_wait, which took a few hundred cycles even
+// then.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < (1u << 22); ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
-}
-
-// The same, testing first without blocking: a phase that has already
-// completed costs a test instead of a potentially suspending try_wait.
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar,
-                                               uint32_t parity) {
-  return mbar_test_wait(bar, parity) || mbar_wait(bar, parity);
 }
 
 // ---------------------------------------------------------------------------
