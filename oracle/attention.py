@@ -27,18 +27,21 @@ import math
 
 import numpy as np
 
-from .numerics import bf16_bits_to_f64, e4m3_codes_to_f64, e4m3_encode_f32
+from .numerics import (bf16_bits_to_f64, e4m3_codes_to_f64, e4m3_encode_f32,
+                       mxfp4_encode_rows, mxfp4_rows_to_f64)
 
 
 # ---------------------------------------------------------------------------
 # storage decoding
 # ---------------------------------------------------------------------------
-def decode_rows(raw, dtype, scale=None):
-    """Raw cache rows [n_kv, T, d] -> float64.
+def decode_rows(raw, dtype, scale=None, d=None):
+    """Raw cache rows [n_kv, T, row] -> float64 [n_kv, T, d].
 
     bf16 rows are exact. fp8 rows are the E4M3 code value times the fp32
     per-(kv head) scale, also exact in fp64 ([KV] "Fewer bits per number":
     the cache holds fewer bits per number; the scale restores the range).
+    mxfp4 rows ([890] section 6) are E2M1 code values times their 16-channel
+    group's E4M3 scale, exact in fp64; ``d`` is the row's channel count.
     """
     if dtype == "bf16":
         return bf16_bits_to_f64(raw)
@@ -46,6 +49,8 @@ def decode_rows(raw, dtype, scale=None):
         vals = e4m3_codes_to_f64(raw)
         s = np.asarray(scale, dtype=np.float32).astype(np.float64)
         return vals * s[:, None, None]
+    if dtype == "mxfp4":
+        return mxfp4_rows_to_f64(raw, d)
     raise ValueError(f"unknown cache dtype {dtype!r}")
 
 
@@ -82,7 +87,8 @@ def kv_append(raw, block_table, pos, new_rows, block_size, dtype="bf16",
 
     fp8: the stored code is E4M3(round-to-nearest-even, saturating) of the
     fp32 product x * inv_scale[kv_head], with x the bf16 input widened to fp32
-    and the product rounded once to fp32.
+    and the product rounded once to fp32. mxfp4: the row's MXFP4 encoding
+    (numerics.mxfp4_encode_rows); ``raw``'s last axis is the row's bytes.
     """
     out = raw.copy()
     new_rows = np.asarray(new_rows, dtype=np.uint16)
@@ -95,6 +101,8 @@ def kv_append(raw, block_table, pos, new_rows, block_size, dtype="bf16",
             inv = np.asarray(inv_scale, dtype=np.float32)[:, None]
             y = (x * inv).astype(np.float32)          # one fp32 rounding
             out[blk[0], :, slot[0], :] = e4m3_encode_f32(y)
+        elif dtype == "mxfp4":
+            out[blk[0], :, slot[0], :] = mxfp4_encode_rows(new_rows[b])
         else:
             raise ValueError(dtype)
     return out
@@ -141,8 +149,9 @@ def gqa_decode(q, k_raw, v_raw, block_table, seq_lens, block_size,
     """One decode step of GQA/MHA attention for every sequence.
 
     q: [B][n_h][d] float64. k_raw / v_raw: cache storage
-    [num_blocks][n_kv][block_size][d]. seq_lens[b] = visible length (after
-    the append). Returns out [B][n_h][d], lse [B][n_h].
+    [num_blocks][n_kv][block_size][row] (row = d elements, or an MXFP4 row's
+    bytes). seq_lens[b] = visible length (after the append). Returns out
+    [B][n_h][d], lse [B][n_h].
     """
     q = np.asarray(q, dtype=np.float64)
     B, n_h, d = q.shape
@@ -150,14 +159,14 @@ def gqa_decode(q, k_raw, v_raw, block_table, seq_lens, block_size,
     g = n_h // n_kv
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    out = np.zeros((B, n_h, v_raw.shape[3]))
+    out = np.zeros((B, n_h, d))
     lse = np.zeros((B, n_h))
     for b in range(B):
         pos = np.arange(int(seq_lens[b]))
         K = decode_rows(gather_rows(k_raw, block_table[b], pos, block_size),
-                        dtype, k_scale)
+                        dtype, k_scale, d)
         V = decode_rows(gather_rows(v_raw, block_table[b], pos, block_size),
-                        dtype, v_scale)
+                        dtype, v_scale, d)
         for kv in range(n_kv):
             heads = slice(kv * g, (kv + 1) * g)
             out[b, heads], lse[b, heads] = attend(q[b, heads], K[kv], V[kv],

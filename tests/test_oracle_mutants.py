@@ -117,3 +117,62 @@ def test_fp8_ties_away_from_zero_are_caught(monkeypatch):
         return orig(np.where(x != 0, bumped, x))
     monkeypatch.setattr(oracle, "e4m3_encode_f32", mutant)
     _fails(P.test_e4m3_encode_midpoints_ties_to_even)
+
+
+def test_fp4_ties_away_from_zero_are_caught(monkeypatch):
+    import oracle.numerics as ON
+    orig = ON.e2m1_encode_f32
+
+    def mutant(x):
+        x = np.asarray(x, dtype=np.float32)
+        bumped = np.nextafter(x, np.float32(np.inf) * np.sign(x),
+                              dtype=np.float32)
+        return orig(np.where(x != 0, bumped, x))
+    monkeypatch.setattr(oracle, "e2m1_encode_f32", mutant)
+    monkeypatch.setattr(ON, "e2m1_encode_f32", mutant)
+    _fails(P.test_e2m1_encode_midpoints_ties_to_even)
+
+
+def test_fp4_sign_dropped_is_caught(monkeypatch):
+    import oracle.numerics as ON
+    orig = ON.e2m1_encode_f32
+    mutant = lambda x: orig(np.abs(np.asarray(x, dtype=np.float32)))
+    monkeypatch.setattr(oracle, "e2m1_encode_f32", mutant)
+    monkeypatch.setattr(ON, "e2m1_encode_f32", mutant)
+    _fails(P.test_e2m1_encode_saturates_and_signs)
+
+
+def test_fp4_nibbles_swapped_is_caught(monkeypatch):
+    # encoder and decoder agree with each other, but not with the layout
+    import oracle.numerics as ON
+    enc, dec = ON.mxfp4_encode_rows, ON.mxfp4_rows_to_f64
+
+    def swap(row, d):
+        row = np.array(row, dtype=np.uint8)
+        c = row[..., :d // 2]
+        row[..., :d // 2] = (c >> 4) | ((c & 0xF) << 4)
+        return row
+    monkeypatch.setattr(oracle, "mxfp4_encode_rows",
+                        lambda bits: swap(enc(bits), np.shape(bits)[-1]))
+    monkeypatch.setattr(oracle, "mxfp4_rows_to_f64",
+                        lambda raw, d: dec(swap(raw, d), d))
+    _fails(P.test_mxfp4_scaled_grid_round_trips)
+
+
+def test_fp4_scale_from_amax_over_4_is_caught(monkeypatch):
+    import oracle.numerics as ON
+
+    def mutant(bits):
+        x = ON.bf16_bits_to_f64(bits).astype(np.float32)
+        d = x.shape[-1]
+        g = x.reshape(x.shape[:-1] + (d // 16, 16))
+        amax = np.fmax.reduce(np.abs(g), axis=-1).astype(np.float32)
+        sc = ON.e4m3_encode_f32((amax / np.float32(4.0)).astype(np.float32))
+        s = ON.e4m3_codes_to_f64(sc).astype(np.float32)[..., None]
+        q = (g / np.where(s > 0, s, np.float32(1))).astype(np.float32)
+        codes = np.where(s > 0, ON.e2m1_encode_f32(q), 0).astype(np.uint8)
+        codes = codes.reshape(x.shape)
+        packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+        return np.concatenate([packed, sc], axis=-1)
+    monkeypatch.setattr(oracle, "mxfp4_encode_rows", mutant)
+    _fails(P.test_mxfp4_scaled_grid_round_trips)

@@ -588,3 +588,151 @@ def test_paged_waste_bound(golden_dir):
         assert waste.sum() <= len(lens) * (bs - 1)
     assert (bs - 1) / Lbar < g["bound_fraction_below"]
     assert O.paged_waste_slots([16, 17, 1], 16).tolist() == [0, 15, 15]
+
+
+# ---------------------------------------------------------------------------
+# fp4 E2M1 and MXFP4 rows ("890 bytes a token ...", section 6)
+# ---------------------------------------------------------------------------
+# The OCP Microscaling Formats specification lists the FP4 (E2M1)
+# magnitudes: 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7), sign in bit 3.
+_OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_values_are_the_ocp_list():
+    t = O.e2m1_value_table()
+    assert list(t[:8]) == _OCP_E2M1
+    assert list(t[8:]) == [-v for v in _OCP_E2M1]
+    assert math.copysign(1.0, t[8]) == -1.0           # code 8 is -0
+
+
+def test_e2m1_encode_round_trip_all_codes():
+    t = O.e2m1_value_table().astype(np.float32)
+    assert np.array_equal(O.e2m1_encode_f32(t), np.arange(16, dtype=np.uint8))
+
+
+def test_e2m1_encode_midpoints_ties_to_even():
+    # each midpoint goes to the neighbour whose mantissa bit is 0
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for x, code in cases.items():
+        assert O.e2m1_encode_f32(np.float32(x)) == code, x
+        assert O.e2m1_encode_f32(np.float32(-x)) == code | 8, -x
+        up = np.nextafter(np.float32(x), np.float32(10))
+        dn = np.nextafter(np.float32(x), np.float32(0))
+        lo = max(c for c in range(8) if _OCP_E2M1[c] < x)
+        hi = min(c for c in range(8) if _OCP_E2M1[c] > x)
+        assert O.e2m1_encode_f32(up) == hi and O.e2m1_encode_f32(dn) == lo
+
+
+def test_e2m1_encode_saturates_and_signs():
+    x = np.array([6.0, 6.5, 1e30, np.inf, -7.0, -np.inf, 0.0, -0.0, -0.1,
+                  0.1], dtype=np.float32)
+    assert list(O.e2m1_encode_f32(x)) == [7, 7, 7, 7, 15, 15, 0, 8, 8, 0]
+
+
+def test_e2m1_encode_is_nearest_brute_force():
+    rng = np.random.default_rng(40)
+    x = (rng.standard_normal(4000) * 3).astype(np.float32)
+    got = O.e2m1_codes_to_f64(O.e2m1_encode_f32(x))
+    for xi, gi in zip(x.astype(np.float64), got):
+        a = min(abs(xi), 6.0)
+        best = min(abs(a - v) for v in _OCP_E2M1)
+        assert abs(abs(gi) - a) == best
+        assert gi == 0 or math.copysign(1, gi) == math.copysign(1, xi)
+
+
+def _mxfp4_groups(codes, scales):
+    """Hand-built rows: 16-channel groups of code values times a scale."""
+    vals = []
+    for g, s in enumerate(scales):
+        vals += [O.e2m1_value_table()[c] * s for c in codes[16 * g:16 * g + 16]]
+    return np.array(vals)
+
+
+def test_mxfp4_scaled_grid_round_trips():
+    # a group whose largest magnitude is 6 s, s an E4M3 value, stores s and
+    # the codes themselves; every such value is exact in bf16
+    rng = np.random.default_rng(41)
+    e4 = O.e4m3_value_table()
+    normal = [c for c in range(0x08, 0x7F) if 6 * e4[c] <= 448 * 6]
+    for _ in range(50):
+        scodes = rng.choice(normal, 8)
+        codes = rng.integers(0, 16, 128)
+        for g in range(8):
+            codes[16 * g + rng.integers(16)] = 7 | (8 * rng.integers(2))
+        x = _mxfp4_groups(codes, e4[scodes])
+        row = O.mxfp4_encode_rows(_bf16_bits(x))
+        assert row.shape == (O.mxfp4_row_bytes(128),) == (72,)
+        assert np.array_equal(row[64:], scodes.astype(np.uint8))
+        # channel 2j in the low nibble, 2j+1 in the high one
+        lo, hi = row[:64] & 0xF, row[:64] >> 4
+        c = codes.astype(np.uint8)
+        zero = O.e2m1_value_table()[c] == 0          # +-0 may swap sign
+        assert np.array_equal(np.where(zero[0::2], 0, lo),
+                              np.where(zero[0::2], 0, c[0::2]))
+        assert np.array_equal(np.where(zero[1::2], 0, hi),
+                              np.where(zero[1::2], 0, c[1::2]))
+        assert np.array_equal(O.mxfp4_rows_to_f64(row, 128), x)
+
+
+def test_mxfp4_bound_is_2688(golden_dir):
+    fig = _load(golden_dir, "page_figures.json")["e4m3_max"]
+    e2, e4 = O.e2m1_value_table(), O.e4m3_value_table()
+    assert np.nanmax(np.abs(np.outer(e2, e4))) == fig["fp4_bound"]
+    x = np.zeros(32)
+    x[3], x[20] = 3000.0, -1e5                 # both groups saturate
+    got = O.mxfp4_rows_to_f64(O.mxfp4_encode_rows(_bf16_bits(x)), 32)
+    assert got[3] == fig["fp4_bound"] and got[20] == -fig["fp4_bound"]
+
+
+def test_mxfp4_error_within_one_scale():
+    # |x - dequant(x)| <= s: the grid's largest gap is 2 (4 to 6), and a
+    # scale rounded down by at most 2^-4 relative overshoots 6 by < 0.4 s
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((300, 64)) * np.exp(rng.uniform(-3, 3, (300, 1)))
+    x[7] = 0.0
+    bits = _bf16_bits(x)
+    xb = O.bf16_bits_to_f64(bits)
+    rows = O.mxfp4_encode_rows(bits)
+    got = O.mxfp4_rows_to_f64(rows, 64)
+    s = np.repeat(O.e4m3_codes_to_f64(rows[:, 32:]), 16, axis=1)
+    assert np.all(np.abs(xb - got) <= s)
+    assert np.all(got[7] == 0)
+    amax = np.abs(xb).reshape(300, 4, 16).max(axis=2)
+    ok = amax[[i for i in range(300) if i != 7]] / 6
+    sc = O.e4m3_codes_to_f64(rows[:, 32:])[[i for i in range(300) if i != 7]]
+    assert np.all(np.abs(sc - ok) <= ok * 2.0 ** -4)   # E4M3 rounding
+
+
+def test_mxfp4_size_against_fp8(golden_dir):
+    fig = _load(golden_dir, "page_figures.json")["fp4_vs_fp8_size"]
+    saving = 1 - O.mxfp4_row_bytes(128) / 128
+    assert abs(saving - fig["value"]) <= fig["abs_tol"]
+
+
+def test_mxfp4_cache_decodes_as_bf16_values():
+    # an MXFP4 cache attends like a bf16 cache holding its decoded values
+    # (each is a code times an E4M3 value: <= 5 significant bits, in range)
+    rng = np.random.default_rng(43)
+    lens = [9, 20]
+    kb, vb, bt = _random_paged(rng, 2, 2, 32, 8, lens)
+    kr, vr = O.mxfp4_encode_rows(kb), O.mxfp4_encode_rows(vb)
+    q = rng.standard_normal((2, 4, 32))
+    o1, l1 = O.gqa_decode(q, kr, vr, bt, lens, 8, dtype="mxfp4")
+    kv = _bf16_bits(O.mxfp4_rows_to_f64(kr, 32))
+    vv = _bf16_bits(O.mxfp4_rows_to_f64(vr, 32))
+    assert np.array_equal(O.bf16_bits_to_f64(kv), O.mxfp4_rows_to_f64(kr, 32))
+    o2, l2 = O.gqa_decode(q, kv, vv, bt, lens, 8)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_append_mxfp4_writes_one_encoded_row():
+    rng = np.random.default_rng(44)
+    kb, _, bt = _random_paged(rng, 2, 2, 32, 8, [5, 9])
+    kr = O.mxfp4_encode_rows(kb)
+    new = _bf16_bits(rng.standard_normal((2, 2, 32)) * 5)
+    out = O.kv_append(kr, bt, [4, 8], new, 8, dtype="mxfp4")
+    for b, p in enumerate([4, 8]):
+        assert np.array_equal(out[bt[b, p // 8], :, p % 8, :],
+                              O.mxfp4_encode_rows(new[b]))
+    assert np.count_nonzero(np.any(out != kr, axis=3)) <= 4
