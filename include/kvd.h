@@ -80,8 +80,9 @@ typedef enum kvd_status {
                                 above the max_seq_len the call was given      */
 
 typedef enum kvd_dtype {
-  KVD_BF16 = 0,    /* 2-byte bfloat16 elements                               */
-  KVD_FP8_E4M3 = 1 /* 1-byte OCP E4M3 codes; value = code * per-head scale   */
+  KVD_BF16 = 0,     /* 2-byte bfloat16 elements                              */
+  KVD_FP8_E4M3 = 1, /* 1-byte OCP E4M3 codes; value = code * per-head scale  */
+  KVD_MXFP4 = 2     /* rows of E2M1 codes + one E4M3 scale per 16 channels   */
 } kvd_dtype;
 
 /*
@@ -95,6 +96,24 @@ typedef enum kvd_dtype {
  * kvd_kv_append stores E4M3(x * inv_scale) rounded to nearest even and
  * saturated to +-448. Scale arrays are device memory, [n_kv] each; unused
  * (may be NULL) for bf16 caches.
+ */
+/*
+ * mxfp4 ("890 bytes a token ...", section 6: E2M1 with one E4M3 scale per
+ * 16 channels, NVFP4's layout without the second-level global scale, so
+ * the largest value is 448 x 6 = 2688). A row of head_dim channels is
+ * head_dim/2 bytes of E2M1 codes (OCP MX FP4: 1 sign, 2 exponent, 1
+ * mantissa bit; channel 2j in the low nibble of byte j, 2j+1 in the high
+ * one) followed by head_dim/16 E4M3 scale codes (scale g covers channels
+ * 16g..16g+15): 72 bytes for head_dim 128, where K and V are laid out
+ * [num_blocks][n_kv][block_size][72] bytes. Value = code value * scale
+ * value. kvd_kv_append (and kvd_gqa_append_decode) encode each group of a
+ * new bf16 row as: amax = max |x| (fp32), scale = E4M3(amax / 6), code =
+ * E2M1(x / scale), both divisions in fp32 and both conversions round to
+ * nearest even and saturate; a group whose scale rounds to 0 stores zero
+ * codes. Quantise after RoPE: the library stores what it is given. The
+ * scale pointers are unused. Supported: head_dim 128, an even block_size,
+ * kv_append and GQA decode with n_h / n_kv <= 4 (dequantised in the
+ * CUDA-core decode kernel; there is no fp4 MMA).
  */
 typedef struct kvd_cache {
   void *k;

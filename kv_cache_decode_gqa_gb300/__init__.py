@@ -7,7 +7,9 @@ does not pass them. Every step of the computation runs in the library's
 CUDA kernels; there is no other path.
 
 Cache layout (per layer): K and V tensors [num_blocks][n_kv][block_size]
-[head_dim] of bf16 (torch.bfloat16) or fp8-e4m3 codes (torch.uint8).
+[head_dim] of bf16 (torch.bfloat16) or fp8-e4m3 codes (torch.uint8), or
+[num_blocks][n_kv][block_size][head_dim/2 + head_dim/16] bytes of MXFP4 rows
+(torch.uint8; include/kvd.h gives the row format).
 """
 import ctypes
 from dataclasses import dataclass
@@ -24,6 +26,8 @@ __all__ = ["PagedCache", "kv_append", "gqa_decode", "mla_decode",
 
 BF16 = 0
 FP8_E4M3 = 1
+MXFP4 = 2
+_DTYPES = {"bf16": BF16, "fp8": FP8_E4M3, "mxfp4": MXFP4}
 OP_GQA_DECODE = 0
 OP_MLA_DECODE = 1
 OP_INDEXER_TOPK = 2
@@ -62,7 +66,7 @@ class PagedCache:
     block_size: int
     n_kv: int
     head_dim: int
-    dtype: str = "bf16"          # "bf16" | "fp8"
+    dtype: str = "bf16"          # "bf16" | "fp8" | "mxfp4"
     k_scale: Optional["torch.Tensor"] = None      # fp32 [n_kv]
     v_scale: Optional["torch.Tensor"] = None
     k_inv_scale: Optional["torch.Tensor"] = None
@@ -78,7 +82,9 @@ class PagedCache:
         _need(self.k, "cache.k", want)
         if self.v is not None:
             _need(self.v, "cache.v", want, self.k.numel())
-        shape = (self.num_blocks, self.n_kv, self.block_size, self.head_dim)
+        row = (self.head_dim // 2 + self.head_dim // 16
+               if self.dtype == "mxfp4" else self.head_dim)
+        shape = (self.num_blocks, self.n_kv, self.block_size, row)
         if tuple(self.k.shape) != shape:
             raise ValueError(f"cache.k shape {tuple(self.k.shape)} != {shape}")
         for n in ("k_scale", "v_scale", "k_inv_scale", "v_inv_scale"):
@@ -87,7 +93,7 @@ class PagedCache:
                 _need(t, n, torch.float32, self.n_kv)
         return _native.KvdCache(
             _ptr(self.k), _ptr(self.v), self.num_blocks, self.block_size,
-            self.n_kv, self.head_dim, BF16 if self.dtype == "bf16" else FP8_E4M3,
+            self.n_kv, self.head_dim, _DTYPES[self.dtype],
             0, _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.k_inv_scale),
             _ptr(self.v_inv_scale))
 

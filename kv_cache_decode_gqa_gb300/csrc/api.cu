@@ -91,11 +91,23 @@ kvd_status check_cache(const kvd_cache *c, bool need_v, const char *what) {
     return fail(KVD_ERR_SHAPE,
                 "%s: num_blocks, block_size, n_kv and head_dim must be >= 1",
                 what);
-  if (c->dtype != KVD_BF16 && c->dtype != KVD_FP8_E4M3)
+  if (c->dtype != KVD_BF16 && c->dtype != KVD_FP8_E4M3 &&
+      c->dtype != KVD_MXFP4)
     return fail(KVD_ERR_UNSUPPORTED, "%s: unknown dtype %d", what, c->dtype);
   if (!aligned(c->k, 16) || (c->v && !aligned(c->v, 16)))
     return fail(KVD_ERR_SHAPE, "%s: cache base pointers must be 16-byte aligned",
                 what);
+  if (c->dtype == KVD_MXFP4) {
+    // 72-byte rows, copied two at a time: whole (block, head) runs stay
+    // 16-byte multiples when the block size is even
+    if (c->head_dim != 128)
+      return fail(KVD_ERR_UNSUPPORTED, "%s: mxfp4 caches need head_dim 128",
+                  what);
+    if (c->block_size % 2 != 0)
+      return fail(KVD_ERR_SHAPE, "%s: mxfp4 caches need an even block_size",
+                  what);
+    return KVD_OK;
+  }
   const long row_bytes =
       (long)c->head_dim * (c->dtype == KVD_BF16 ? 2 : 1);
   if (row_bytes % 16 != 0)
@@ -150,6 +162,9 @@ kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
   if (c->head_dim != 64 && c->head_dim != 128)
     return fail(KVD_ERR_UNSUPPORTED, "gqa_decode: head_dim %d (64 or 128)",
                 c->head_dim);
+  if (c->dtype == KVD_MXFP4 && g != 1 && g != 2 && g != 4)
+    return fail(KVD_ERR_UNSUPPORTED, "gqa_decode: mxfp4 caches are decoded "
+                "on the CUDA-core kernel: group size 1, 2 or 4 (got %d)", g);
   if (g == 1 || g == 2 || g == 4) {
     *kind = DenseKernel::Simt;
   } else if ((g == 8 || g == 16) && c->head_dim == 128) {

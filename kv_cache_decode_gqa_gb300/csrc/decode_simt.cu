@@ -55,8 +55,7 @@ constexpr int kAppendBar = 2;              // finisher -> producer: rows written
 
 template <int D, int G, int DT, int HP>
 struct Cfg {
-  static constexpr int ES = DT == DT_BF16 ? 2 : 1;
-  static constexpr int ROW = D * ES;                 // bytes per cached row
+  static constexpr int ROW = row_bytes(D, DT);       // bytes per cached row
   static constexpr int HSTAGE = kStageRows * ROW;    // one head's K (or V)
   static constexpr int STAGE = HP * HSTAGE;          // K (or V) bytes / chunk
   static constexpr int E = D / 8;                    // elements per lane
@@ -92,11 +91,26 @@ __device__ __forceinline__ int elem_index(int sub, int e) {
   }
 }
 
-// The lane's D/8 elements of a shared-memory row, as floats.
+// The lane's D/8 elements of a shared-memory row, as floats. MXFP4 (D =
+// 128): the lane's 16 channels are one scale group: 8 code bytes at
+// sub * 8 and the group's E4M3 scale at D/2 + sub; each value is exact in
+// fp32 (code value times scale).
 template <int D, int DT>
 __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
                                          float (&x)[D / 8]) {
-  if constexpr (DT == DT_BF16) {
+  if constexpr (DT == DT_MXFP4) {
+    static_assert(D == 128, "one 16-channel scale group per lane");
+    const uint2 u = *reinterpret_cast<const uint2 *>(row + sub * 8);
+    const float s = f16lo(e4m3x2_to_f16x2((uint16_t)row[D / 2 + sub])) *
+                    16384.f;  // the code values below are times 2^-14
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        x[8 * t + k] = e2m1_value_x2m14(w[t] >> (4 * k)) * s;
+    }
+  } else if constexpr (DT == DT_BF16) {
 #pragma unroll
     for (int j = 0; j < D / 64; ++j) {
       const uint4 u =
@@ -313,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the query rows travel only with a unit's first chunk here (the
             // consumers read them when the unit starts)
             const bool qrows = i == 0 || k == 0;
-            mbar_arrive_expect_tx(&full[s], 2u * HP * rows * C::ROW +
+            // MXFP4 rows (72 bytes) are copied in pairs: a copy is a
+            // multiple of 16 bytes. An odd tail takes the next row of its
+            // block too (masked like any row past the end).
+            const int crows =
+                DT == DT_MXFP4 && rows < kStageRows ? (rows + 1) & ~1 : rows;
+            mbar_arrive_expect_tx(&full[s], 2u * HP * crows * C::ROW +
                                                 (qrows ? C::QB : 0u));
             if (qrows)
               bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * D,
@@ -340,17 +359,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < HP; ++j) {
                   const size_t oj = off + (size_t)j * C::HSTAGE;
                   bulk_g2s_hint(sk + s * C::STAGE + j * C::HSTAGE, p.k + oj,
-                                rows * C::ROW, &full[s], policy);
+                                crows * C::ROW, &full[s], policy);
                   bulk_g2s_hint(sv + s * C::STAGE + j * C::HSTAGE, p.v + oj,
-                                rows * C::ROW, &full[s], policy);
+                                crows * C::ROW, &full[s], policy);
                 }
               }
             }
-            int done = HP > 1 ? rows : 0;
-            while (done < rows) {
+            int done = HP > 1 ? crows : 0;
+            while (done < crows) {
               const int t = tok + done;
               const int slot = t % p.block_size;
-              const int piece = min(rows - done, p.block_size - slot);
+              const int piece = min(crows - done, p.block_size - slot);
               const int lb = t / p.block_size - lb0;
               int pb = lb == 0   ? blk[0]
                        : lb == 1 ? blk[1]
@@ -620,7 +639,7 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
 // Head-group sizes built: 1 always; one larger size per row width (a 32 KB
 // copy of 64-token rows), for groups of 1 or 2 query heads.
 template <int D, int DT>
-constexpr int kWideHP = D * (DT == DT_BF16 ? 2 : 1) >= 256 ? 2 : 4;
+constexpr int kWideHP = row_bytes(D, DT) >= 256 ? 2 : 4;
 
 template <int D, int DT>
 cudaError_t launch_g(const DecodeParams &p, cudaStream_t s) {
@@ -646,16 +665,19 @@ cudaError_t launch_g(const DecodeParams &p, cudaStream_t s) {
 int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
                          int block_size) {
   if (block_size != kStageRows || g > 2) return 1;
-  const int w = head_dim == 128 ? (dtype == DT_BF16 ? kWideHP<128, DT_BF16>
-                                                    : kWideHP<128, DT_FP8>)
-                                : (dtype == DT_BF16 ? kWideHP<64, DT_BF16>
-                                                    : kWideHP<64, DT_FP8>);
+  const int w = dtype == DT_MXFP4 ? kWideHP<128, DT_MXFP4>
+                : head_dim == 128 ? (dtype == DT_BF16 ? kWideHP<128, DT_BF16>
+                                                      : kWideHP<128, DT_FP8>)
+                                  : (dtype == DT_BF16 ? kWideHP<64, DT_BF16>
+                                                      : kWideHP<64, DT_FP8>);
   return n_kv % w == 0 ? w : 1;
 }
 
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s) {
   const bool fp8 = p.dtype == DT_FP8;
   if (p.batch > kMaxDecodeBatch) return cudaErrorNotSupported;
+  if (p.dtype == DT_MXFP4)
+    return p.dk == 128 ? launch_g<128, DT_MXFP4>(p, s) : cudaErrorNotSupported;
   if (p.dk == 128) return fp8 ? launch_g<128, DT_FP8>(p, s)
                               : launch_g<128, DT_BF16>(p, s);
   if (p.dk == 64) return fp8 ? launch_g<64, DT_FP8>(p, s)

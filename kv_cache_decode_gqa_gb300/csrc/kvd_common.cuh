@@ -349,6 +349,63 @@ __device__ __forceinline__ void store_new8(uint8_t *dst, const uint16_t *src,
   }
 }
 
+// ---------------------------------------------------------------------------
+// MXFP4 rows: E2M1 codes with one E4M3 scale per 16 channels
+// ---------------------------------------------------------------------------
+// E2M1 code of q: round to nearest with ties to the code whose mantissa bit
+// is 0, saturating at +-6 (comparisons against the midpoints of the grid
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6; NaN saturates), sign in bit 3.
+__device__ __forceinline__ uint32_t e2m1_code(float q) {
+  const float a = fabsf(q);
+  const uint32_t c = a <= 0.25f   ? 0u
+                     : a < 0.75f  ? 1u
+                     : a <= 1.25f ? 2u
+                     : a < 1.75f  ? 3u
+                     : a <= 2.5f  ? 4u
+                     : a < 3.5f   ? 5u
+                     : a <= 5.f   ? 6u
+                                  : 7u;
+  return c | ((__float_as_uint(q) >> 31) << 3);
+}
+
+// Value of an E2M1 code (low 4 bits) times 2^-14, as a half: the code's
+// three magnitude bits placed at the half's bits 9..11 make exponent field
+// 0 the half subnormal m * 2^-15 and the others 2^(e-15) (1 + m/2).
+__device__ __forceinline__ float e2m1_value_x2m14(uint32_t c) {
+  return f16_to_f32((uint16_t)(((c & 7u) << 9) | ((c & 8u) << 12)));
+}
+
+// One 16-channel group of a new bf16 row into an MXFP4 row: 8 bytes of
+// codes (channel 2j low nibble) at `codes`, the E4M3 scale byte at
+// `scale`. amax and both divisions in fp32, conversions round to nearest
+// even and saturate; a scale that rounds to 0 gives zero codes.
+__device__ __forceinline__ void store_mxfp4_group(uint8_t *codes,
+                                                  uint8_t *scale,
+                                                  const uint16_t *src) {
+  const uint4 u0 = *reinterpret_cast<const uint4 *>(src);
+  const uint4 u1 = *reinterpret_cast<const uint4 *>(src + 8);
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float x[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    x[2 * j] = bf16lo(w[j]);
+    x[2 * j + 1] = bf16hi(w[j]);
+    amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+  }
+  const uint32_t sc =
+      e4m3x2_from_f32(__fdiv_rn(amax, 6.0f), 0.f) & 0xffu;  // low byte
+  const float s = f16lo(e4m3x2_to_f16x2((uint16_t)sc));
+  uint32_t packed[2] = {0u, 0u};
+  if (s > 0.f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      packed[j >> 3] |= e2m1_code(__fdiv_rn(x[j], s)) << (4 * (j & 7));
+  }
+  *reinterpret_cast<uint2 *>(codes) = make_uint2(packed[0], packed[1]);
+  *scale = (uint8_t)sc;
+}
+
 // Orders this thread's generic-proxy global-memory writes before later
 // async-proxy (copy engine) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_global() {

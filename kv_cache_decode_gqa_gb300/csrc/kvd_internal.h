@@ -17,7 +17,12 @@ enum : int {
   DEVERR_LEN = 16
 };
 
-enum : int { DT_BF16 = 0, DT_FP8 = 1 };
+enum : int { DT_BF16 = 0, DT_FP8 = 1, DT_MXFP4 = 2 };
+
+// Bytes of one cached row of d channels.
+__host__ __device__ constexpr int row_bytes(int d, int dtype) {
+  return dtype == DT_BF16 ? 2 * d : dtype == DT_FP8 ? d : d / 2 + d / 16;
+}
 // kvd_seqs flags (mirror of KVD_SEQS_STABLE in kvd.h).
 enum : int { FLAG_SEQS_STABLE = 1 };
 
@@ -52,7 +57,7 @@ struct DecodeParams {
   int *counters;           // [batch][n_groups] arrival counters, kept zero
   int32_t n_groups;        // head groups per sequence sharing a counter
   int32_t batch, n_h, n_kv, dk, dv, block_size, num_blocks, max_blocks;
-  int32_t dtype;        // DT_BF16 or DT_FP8
+  int32_t dtype;        // DT_BF16, DT_FP8 or DT_MXFP4
   int32_t max_seq_len;  // clamp for device lengths
   int32_t n_idx;        // entries per row of `indices`
   int32_t split_len;    // tokens (or index entries) per split

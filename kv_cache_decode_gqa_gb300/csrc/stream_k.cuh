@@ -162,12 +162,31 @@ __device__ __forceinline__ int partial_side(int ustart, int lo) {
 // ---------------------------------------------------------------------------
 // The calling warp writes the new key and value rows of kv heads
 // [h0, h0 + nh) of sequence b into slot P of physical block pb (checked by
-// the caller), lane-parallel over 8-element pieces, and each lane orders
-// its writes before later copy-engine reads of the same rows.
+// the caller), lane-parallel over 8-element pieces (16-channel groups for
+// an MXFP4 cache), and each lane orders its writes before later
+// copy-engine reads of the same rows.
 __device__ __forceinline__ void append_rows(const DecodeParams &p, int b,
                                             int h0, int nh, int P, int pb,
                                             int lane) {
-  const int D = p.dk, pieces = D / 8, es = p.dtype == DT_BF16 ? 2 : 1;
+  const int D = p.dk, es = p.dtype == DT_BF16 ? 2 : 1;
+  if (p.dtype == DT_MXFP4) {
+    const int groups = D / 16, rb = row_bytes(D, DT_MXFP4);
+    for (int e = lane; e < 2 * nh * groups; e += 32) {
+      const bool is_v = e >= nh * groups;
+      const int r = is_v ? e - nh * groups : e;
+      const int h = h0 + r / groups, g = r % groups;
+      const uint16_t *src =
+          (is_v ? p.v_new : p.k_new) + ((long)b * p.n_kv + h) * D + g * 16;
+      const long row =
+          ((long)pb * p.n_kv + h) * p.block_size + P % p.block_size;
+      uint8_t *rowp = const_cast<uint8_t *>(is_v ? p.v : p.k) + row * rb;
+      store_mxfp4_group(rowp + g * 8, rowp + D / 2 + g, src);
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    return;
+  }
+  const int pieces = D / 8;
   for (int e = lane; e < 2 * nh * pieces; e += 32) {
     const bool is_v = e >= nh * pieces;
     const int r = is_v ? e - nh * pieces : e;

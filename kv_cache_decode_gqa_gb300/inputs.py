@@ -87,6 +87,25 @@ def fp8_code_table():
     return _TABLES["fp8"]
 
 
+def byte_table():
+    """The 256 byte values: uniform random bytes (the code bytes of an
+    MXFP4 row, two random E2M1 codes each)."""
+    if "byte" not in _TABLES:
+        _TABLES["byte"] = np.arange(256, dtype=np.uint8)
+    return _TABLES["byte"]
+
+
+def mxfp4_scale_table():
+    """256 E4M3 codes of the 16 values 1/8 .. 15/32 (exponent field 4 or
+    5, any mantissa), each 16 times: positive group scales in the range that
+    amax / 6 takes for groups of 16 N(0,1) values."""
+    if "mxscale" not in _TABLES:
+        j = np.arange(256, dtype=np.uint32)
+        codes = ((4 + ((j >> 3) & 1)) << 3) | (j & 7)
+        _TABLES["mxscale"] = codes.astype(np.uint8)
+    return _TABLES["mxscale"]
+
+
 def table_bits(table):
     n = int(table.shape[0])
     bits = n.bit_length() - 1

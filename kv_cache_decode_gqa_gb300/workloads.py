@@ -9,6 +9,8 @@ Shapes (cached lengths are BEFORE this step's append):
   llama31_70b_gqa   B=32, n_h=64, n_kv=8, d=128, L_b = 1024 + draw mod 7169,
                     80 layers, 64-token blocks; "_fp8": E4M3 cache with one
                     scale per (layer, kv head) for K and for V
+  llama2_7b_mha_mxfp4  the Llama-2 shape over an MXFP4 cache (E2M1 codes, an
+                    E4M3 scale per 16 channels: 72 bytes per row)
   mla               B=64, n_h=128, latent 512 + rope 64, L=32768, 1 layer
   sparse            B=8, L=131072, main cache n_kv=1, d=512 (K and V), indexer
                     keys d=64, 4 indexer heads, k=2048, n_h=64, 8 layers:
@@ -17,7 +19,9 @@ Shapes (cached lengths are BEFORE this step's append):
 Every tensor is a stream of the SplitMix64 generator in ``inputs`` keyed by
 (20260 + config id, layer, tensor id). Cache values are N(0,1) bf16 (fp8
 caches: random E4M3 codes, magnitudes 1/8..30, and per-head scales in
-[1/16, 1/8)); indexer weights are U(0,1). Physical blocks are a seeded
+[1/16, 1/8); MXFP4 caches: uniform random code bytes and group scales
+1/8 .. 15/32, so values are about N(0,1)-sized); indexer weights are
+U(0,1). Physical blocks are a seeded
 permutation of the pool, so no sequence is stored contiguously (except in
 tiny_gqa), and two spare blocks per cache stay unused as canaries.
 """
@@ -32,7 +36,9 @@ SEED_BASE = 20260
 
 # tensor ids of the generator streams
 T_K, T_V, T_Q, T_KNEW, T_VNEW, T_QIDX, T_W, T_IDXK, T_LEN, T_PERM, \
-    T_KSCALE, T_VSCALE, T_IDXKNEW = range(13)
+    T_KSCALE, T_VSCALE, T_IDXKNEW, T_KGSCALE, T_VGSCALE = range(15)
+# the group-scale streams of an MXFP4 cache's K and V
+_GROUP_SCALE = {T_K: T_KGSCALE, T_V: T_VGSCALE}
 
 SPARSE_MODES = ["full", "reuse", "reuse", "reuse",
                 "reindex", "reindex", "reindex", "reindex"]
@@ -77,7 +83,8 @@ class Shape:
 
     @property
     def elem_bytes(self):
-        return 1 if self.dtype == "fp8" else 2
+        """Cache bytes per element (MXFP4: 9/16, codes and scales)."""
+        return {"fp8": 1, "mxfp4": 9 / 16}.get(self.dtype, 2)
 
 
 def config(name, **over):
@@ -88,6 +95,8 @@ def config(name, **over):
                   contiguous=True)
     elif name == "llama2_7b_mha":
         s = Shape("llama2_7b_mha", 2, 1, 32, 32, 128, 32, 64, [4096])
+    elif name == "llama2_7b_mha_mxfp4":
+        s = Shape(name, 6, 1, 32, 32, 128, 32, 64, [4096], dtype="mxfp4")
     elif name in ("llama31_70b_gqa", "llama31_70b_gqa_fp8"):
         lens = I.uniform_int(I.stream_key(SEED_BASE + 3, 0, T_LEN), 32, 1024,
                              8192).tolist()
@@ -108,8 +117,8 @@ def config(name, **over):
     return s
 
 
-CONFIGS = ["tiny_gqa", "llama2_7b_mha", "llama31_70b_gqa",
-           "llama31_70b_gqa_fp8", "mla", "sparse"]
+CONFIGS = ["tiny_gqa", "llama2_7b_mha", "llama2_7b_mha_mxfp4",
+           "llama31_70b_gqa", "llama31_70b_gqa_fp8", "mla", "sparse"]
 
 
 # ---------------------------------------------------------------------------
@@ -173,9 +182,21 @@ def cache_dims(shape, paging, width=None, n_kv=None):
             shape.block_size, shape.head_dim if width is None else width)
 
 
+def _mxfp4_parts(shape, tensor):
+    """An MXFP4 cache is drawn as two streams, concatenated per row: the
+    code bytes (d/2 wide) and the group scales (d/16 wide)."""
+    d = shape.head_dim
+    return ((d // 2, I.byte_table(), tensor),
+            (d // 16, I.mxfp4_scale_table(), _GROUP_SCALE[tensor]))
+
+
 def host_cache_full(shape, paging, layer, tensor, width=None, n_kv=None,
                     table=None):
     """The whole physical cache array on the host (small shapes only)."""
+    if shape.dtype == "mxfp4" and width is None and table is None:
+        return np.concatenate(
+            [host_cache_full(shape, paging, layer, t, w, n_kv, tab)
+             for w, tab, t in _mxfp4_parts(shape, tensor)], axis=-1)
     dims = cache_dims(shape, paging, width, n_kv)
     tab = cache_table(shape) if table is None else table
     return I.host_tensor(tab, _key(shape, layer, tensor), dims)
@@ -186,6 +207,11 @@ def host_cache_compact(shape, paging, layer, tensor, seqs, width=None,
     """Host copy of only the blocks the sequences ``seqs`` use, as a compact
     cache plus a remapped block table (for sampled parity at full size).
     Returns (raw [n][n_kv][bs][w], block_table [len(seqs)][max_blocks])."""
+    if shape.dtype == "mxfp4" and width is None and table is None:
+        parts = [host_cache_compact(shape, paging, layer, t, seqs, w, n_kv,
+                                    tab)
+                 for w, tab, t in _mxfp4_parts(shape, tensor)]
+        return np.concatenate([p[0] for p in parts], axis=-1), parts[0][1]
     dims = cache_dims(shape, paging, width, n_kv)
     per_block = int(np.prod(dims[1:]))
     tab = cache_table(shape) if table is None else table
@@ -228,10 +254,18 @@ class DeviceWorkload:
         self.pos = torch.tensor(s.lengths, dtype=torch.int32, device=dev)
         self.seq_lens = torch.tensor(s.seq_lens, dtype=torch.int32, device=dev)
         self.max_seq_len = s.max_seq_len
-        cdt = torch.uint8 if s.dtype == "fp8" else torch.bfloat16
+        cdt = torch.bfloat16 if s.dtype == "bf16" else torch.uint8
         tab = cache_table(s)
 
         def dev_cache(layer, tensor, width, n_kv):
+            if s.dtype == "mxfp4" and width is None:
+                parts = []
+                for w, ptab, t in _mxfp4_parts(s, tensor):
+                    x = torch.empty(cache_dims(s, pg, w, n_kv),
+                                    dtype=torch.uint8, device=dev)
+                    I.device_fill(x, ptab, _key(s, layer, t))
+                    parts.append(x)
+                return torch.cat(parts, dim=-1).contiguous()
             t = torch.empty(cache_dims(s, pg, width, n_kv), dtype=cdt,
                             device=dev)
             I.device_fill(t, tab, _key(s, layer, tensor))

@@ -76,7 +76,12 @@ def oracle_dense_step(shape, paging, layer, seqs=None):
     pos = [s.lengths[b] for b in all_seqs]
     lens = [s.seq_lens[b] for b in all_seqs]
     kn, vn = knew[all_seqs], vnew[all_seqs]
-    if s.dtype == "fp8":
+    if s.dtype == "mxfp4":
+        kr = oracle.kv_append(kr, bt, pos, kn, s.block_size, "mxfp4")
+        vr = oracle.kv_append(vr, bt, pos, vn, s.block_size, "mxfp4")
+        out, lse = oracle.gqa_decode(q[all_seqs], kr, vr, bt, lens,
+                                     s.block_size, dtype="mxfp4")
+    elif s.dtype == "fp8":
         ks, kinv, vs, vinv = host_scales(s, layer)
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size, "fp8", kinv)
         vr = oracle.kv_append(vr, bt, pos, vn, s.block_size, "fp8", vinv)

@@ -147,3 +147,22 @@ def test_no_gpu_means_cuda_error_not_crash(lib):
                                 ctypes.byref(_seqs()), 64, 0,
                                 ctypes.byref(size))
     assert st == 6
+
+
+def test_mxfp4_cache_validation(lib):
+    """MXFP4 caches: head_dim 128 and an even block size; decoded on the
+    CUDA-core kernel, so query groups of 1, 2 or 4 only; the latent,
+    sparse and indexer calls take bf16 caches only."""
+    s = _seqs()
+    c = _cache(dtype=2, head_dim=64)
+    assert _gqa(lib, c, s, n_h=8) == 3                 # head_dim 64
+    c = _cache(dtype=2, block_size=63)
+    assert _gqa(lib, c, s, n_h=8) == 2                 # odd block size
+    c = _cache(dtype=2)                                # n_kv 8, d 128
+    assert _gqa(lib, c, s, n_h=64) == 3                # group 8: no MMA
+    assert _gqa(lib, c, s, n_h=64, q=None) == 3
+    c = _cache(dtype=3)
+    assert _gqa(lib, c, s, n_h=8) == 3                 # unknown dtype
+    lat = _cache(dtype=2, n_kv=1, head_dim=576, v=None)
+    assert lib.kvd_mla_decode(ctypes.byref(lat), 512, ctypes.byref(s), FAKE,
+                              128, 0.0, FAKE, None, None, 0, None) == 3

@@ -36,7 +36,7 @@ def _host_bytes(a):
 # ---------------------------------------------------------------------------
 # append: whole-cache byte equality, canary blocks included
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
 @pytest.mark.parametrize("bs,lengths", [(16, [0, 15, 16, 47]),
                                         (64, [63, 64, 200])])
 def test_append_bitexact(dtype, bs, lengths):
@@ -55,6 +55,9 @@ def test_append_bitexact(dtype, bs, lengths):
         _, kinv, _, vinv = H.host_scales(s, 0)
         kr = oracle.kv_append(kr, bt, s.lengths, kn, bs, "fp8", kinv)
         vr = oracle.kv_append(vr, bt, s.lengths, vn, bs, "fp8", vinv)
+    elif dtype == "mxfp4":
+        kr = oracle.kv_append(kr, bt, s.lengths, kn, bs, "mxfp4")
+        vr = oracle.kv_append(vr, bt, s.lengths, vn, bs, "mxfp4")
     else:
         kr = oracle.kv_append(kr, bt, s.lengths, kn, bs)
         vr = oracle.kv_append(vr, bt, s.lengths, vn, bs)
@@ -97,6 +100,56 @@ def test_append_fp8_rounding_edges():
         assert np.all(cache.cpu().numpy()[0] == 0)        # untouched block
 
 
+def test_append_mxfp4_rounding_edges():
+    """MXFP4 rows through kv_append, against the oracle's encoder: groups
+    whose scale is exactly 1 (amax 6) holding every E2M1 midpoint and its
+    neighbours (ties to even), groups that saturate (amax/6 rounding down,
+    amax past 2688), all-zero and tiny groups (scale 0: zero codes), signed
+    zeros, and N(0,1) groups of every magnitude."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+
+    def bf16_neighbours(m):  # the adjacent bf16 values above and below m
+        e = np.floor(np.log2(m))
+        below = 2.0 ** (e - 8) if m == 2.0 ** e else 2.0 ** (e - 7)
+        return m + 2.0 ** (e - 7), m - below
+    groups = []
+    for m in mids:
+        up, dn = bf16_neighbours(m)
+        g = [6.0, m, -m, up, dn, -0.0, 0.0, -6.0, m / 2, -m / 2, 3 * m, -up,
+             -dn, -4.0, 2.0, 1.0]
+        groups.append(g)
+    groups.append([7.0] + [6.5, -6.9, 1.0, 0.3] + [0.0] * 11)   # scale 1.125
+    groups.append([3000.0, -1e5] + [1.0] * 14)                  # > 2688
+    groups.append([0.0] * 16)
+    groups.append([2.0 ** -13, -2.0 ** -12] + [0.0] * 14)       # scale -> 0
+    groups.append([-0.0] * 8 + [1e-3] * 8)
+    rng = np.random.default_rng(50)
+    for e in range(-12, 12, 3):
+        groups.append(list(rng.standard_normal(16) * 2.0 ** e))
+    vals = np.array(groups, dtype=np.float64).reshape(-1)
+    d = 128
+    rows = (len(vals) + d - 1) // d
+    vals = np.concatenate([vals, np.zeros(rows * d - len(vals))])
+    bits = torch.tensor(vals).to(torch.bfloat16)
+    assert np.array_equal(bits.double().numpy()[:7 * 16],
+                          vals[:7 * 16])              # exact in bf16
+    cache = torch.zeros((rows + 1, 1, 2, 72), dtype=torch.uint8,
+                        device="cuda")
+    c = K.PagedCache(cache, None, 2, 1, d, "mxfp4")
+    bt = torch.arange(rows, dtype=torch.int32, device="cuda").reshape(rows, 1)
+    bt = bt + 1
+    pos = torch.ones(rows, dtype=torch.int32, device="cuda")   # slot 1
+    k_new = bits.reshape(rows, 1, d).cuda()
+    K.kv_append(c, bt, pos, k_new)
+    torch.cuda.synchronize()
+    got = cache.cpu().numpy()
+    want = oracle.mxfp4_encode_rows(
+        bits.view(torch.int16).numpy().view(np.uint16).reshape(rows, d))
+    assert np.array_equal(got[1:, 0, 1, :], want), np.argwhere(
+        got[1:, 0, 1, :] != want)
+    assert np.all(got[0] == 0) and np.all(got[1:, 0, 0, :] == 0)
+
+
 # ---------------------------------------------------------------------------
 # dense decode, every element
 # ---------------------------------------------------------------------------
@@ -131,6 +184,27 @@ def test_gqa_decode_small(case, dtype):
     ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
     H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}")
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/{dtype}")
+
+
+# MXFP4 caches: head_dim 128, query groups of 1, 2 or 4 (CUDA-core kernel)
+MXFP4_CASES = [c for c in DENSE_CASES if c[3] == 128 and c[1] // c[2] <= 4]
+
+
+@pytest.mark.parametrize("case", MXFP4_CASES, ids=[c[0] for c in MXFP4_CASES])
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_gqa_decode_mxfp4(case, fused):
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama2_7b_mha_mxfp4", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, n_h=n_h, n_kv=n_kv)
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0, fused=fused)
+    torch.cuda.synchronize()
+    ref, ref_lse, (kr, vr) = H.oracle_dense_step(s, wl.paging, 0)
+    c = wl.caches[0]
+    assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr)), name
+    assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr)), name
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/mxfp4")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/mxfp4")
 
 
 @pytest.mark.parametrize("case", [c for c in DENSE_CASES if c[0] in
@@ -279,6 +353,19 @@ def test_llama2_7b_full_size_sampled_layers(fused):
         ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, layer, seqs=[0])
         H.assert_close(H.to_np_bf16(out), ref, f"llama2 layer {layer}")
         H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"layer {layer}")
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_llama2_7b_mxfp4_full_size_sampled_layers(fused):
+    s = W.config("llama2_7b_mha_mxfp4")
+    wl = W.DeviceWorkload(s, layers=[0, 31])
+    for layer in (0, 31):
+        out, lse = H.device_step(wl, layer, fused=fused,
+                                 seqs_flags=K.SEQS_STABLE if fused else 0)
+        torch.cuda.synchronize()
+        ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, layer, seqs=[0])
+        H.assert_close(H.to_np_bf16(out), ref, f"mxfp4 layer {layer}")
+        H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"mxfp4 {layer}")
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
