@@ -92,23 +92,22 @@ __device__ __forceinline__ int elem_index(int sub, int e) {
 }
 
 // The lane's D/8 elements of a shared-memory row, as floats. MXFP4 (D =
-// 128): the lane's 16 channels are one scale group: 8 code bytes at
-// sub * 8 and the group's E4M3 scale at D/2 + sub; each value is exact in
-// fp32 (code value times scale).
+// 128): the lane's 16 channels are one scale group (8 code bytes at
+// sub * 8): the code values, without the scale (row_scale gives it; the
+// callers apply it once per row).
 template <int D, int DT>
 __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
                                          float (&x)[D / 8]) {
   if constexpr (DT == DT_MXFP4) {
     static_assert(D == 128, "one 16-channel scale group per lane");
     const uint2 u = *reinterpret_cast<const uint2 *>(row + sub * 8);
-    const float s = f16lo(e4m3x2_to_f16x2((uint16_t)row[D / 2 + sub])) *
-                    16384.f;  // the code values below are times 2^-14
     const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < 4; ++t) {
+      float v[4];
+      e2m1x4_to_f32(w[t >> 1] >> (16 * (t & 1)), v);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        x[8 * t + k] = e2m1_value_x2m14(w[t] >> (4 * k)) * s;
+      for (int k = 0; k < 4; ++k) x[4 * t + k] = v[k];
     }
   } else if constexpr (DT == DT_BF16) {
 #pragma unroll
@@ -141,6 +140,17 @@ __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
       x[4 * t + 2] = f16lo(b);
       x[4 * t + 3] = f16hi(b);
     }
+  }
+}
+
+// The factor the lane's values of a row take: the lane's MXFP4 group scale
+// (its E4M3 code at D/2 + sub), 1 for the other formats.
+template <int D, int DT>
+__device__ __forceinline__ float row_scale(const uint8_t *row, int sub) {
+  if constexpr (DT == DT_MXFP4) {
+    return f16lo(e4m3x2_to_f16x2((uint16_t)row[D / 2 + sub]));
+  } else {
+    return 1.0f;
   }
 }
 
@@ -541,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = lw * 4 * C::ITER + i2 * 4 + grp;
         float kx[E];
         load_row<D, DT>(kst + r * C::ROW, sub, kx);
+        const float ks = row_scale<D, DT>(kst + r * C::ROW, sub);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float a0 = 0.f, a1 = 0.f;
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a0 = fmaf(qf[g][e], kx[e], a0);
             a1 = fmaf(qf[g][e + 1], kx[e + 1], a1);
           }
-          sc[i2][g] = a0 + a1;
+          sc[i2][g] = (a0 + a1) * ks;
         }
       }
 #pragma unroll
@@ -590,11 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r < nvalid) {
           float vx[E];
           load_row<D, DT>(vst + r * C::ROW, sub, vx);
+          const float vsr = row_scale<D, DT>(vst + r * C::ROW, sub);
 #pragma unroll
           for (int g = 0; g < G; ++g) {
+            const float pv = pr[i2][g] * vsr;
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-              o[g][e] = fmaf(pr[i2][g], vx[e], o[g][e]);
+            for (int e = 0; e < E; ++e) o[g][e] = fmaf(pv, vx[e], o[g][e]);
           }
         }
       }

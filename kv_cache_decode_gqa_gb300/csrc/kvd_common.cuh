@@ -368,11 +368,23 @@ __device__ __forceinline__ uint32_t e2m1_code(float q) {
   return c | ((__float_as_uint(q) >> 31) << 3);
 }
 
-// Value of an E2M1 code (low 4 bits) times 2^-14, as a half: the code's
-// three magnitude bits placed at the half's bits 9..11 make exponent field
-// 0 the half subnormal m * 2^-15 and the others 2^(e-15) (1 + m/2).
-__device__ __forceinline__ float e2m1_value_x2m14(uint32_t c) {
-  return f16_to_f32((uint16_t)(((c & 7u) << 9) | ((c & 8u) << 12)));
+// Four E2M1 codes (the low 16 bits of `codes`, code i in bits 4i..4i+3) to
+// their exact fp32 values. The fp32 pattern of every E2M1 value has zero
+// low bytes; its two upper bytes come from eight-entry tables indexed by
+// the code's magnitude bits (byte permutes), then the sign bit is set.
+//   magnitude  0    0.5  1    1.5  2    3    4    6
+//   byte 3     00   3F   3F   3F   40   40   40   40
+//   byte 2     00   00   80   C0   00   40   80   C0
+__device__ __forceinline__ void e2m1x4_to_f32(uint32_t codes, float (&v)[4]) {
+  const uint32_t sel = codes & 0x7777u;
+  const uint32_t b2 = prmt(0xC0800000u, 0xC0804000u, sel);
+  const uint32_t b3 = prmt(0x3F3F3F00u, 0x40404040u, sel);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // bytes 0, 1: the sign-replicated top bit of a byte-3 value (always 0)
+    const uint32_t f = prmt(b2, b3, 0xCCu | (k << 8) | ((4 + k) << 12));
+    v[k] = __uint_as_float(f | ((codes << (28 - 4 * k)) & 0x80000000u));
+  }
 }
 
 // One 16-channel group of a new bf16 row into an MXFP4 row: 8 bytes of
