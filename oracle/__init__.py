@@ -22,7 +22,8 @@ from .attention import (attend, attend_scores, decode_rows, gather_positions, ga
                         gqa_decode, mla_decode, indexer_scores, topk_select,
                         indexer_topk, sparse_decode, lse_merge, split_decode,
                         bytes_per_token, cache_bytes, paged_waste_slots,
-                        sparse_schedule)
+                        sparse_schedule, POOL_BLOCK, POOL_CAP, indexer_pool,
+                        pool_positions, indexer_topk_in_pool)
 
 __all__ = [
     "bf16_bits_to_f64", "e4m3_value_table", "e4m3_codes_to_f64",
@@ -32,5 +33,6 @@ __all__ = [
     "attend", "attend_scores", "decode_rows", "gather_positions", "gather_rows", "kv_append", "gqa_decode",
     "mla_decode", "indexer_scores", "topk_select", "indexer_topk",
     "sparse_decode", "lse_merge", "split_decode", "bytes_per_token",
-    "cache_bytes", "paged_waste_slots", "sparse_schedule",
+    "cache_bytes", "paged_waste_slots", "sparse_schedule", "POOL_BLOCK",
+    "POOL_CAP", "indexer_pool", "pool_positions", "indexer_topk_in_pool",
 ]

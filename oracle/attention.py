@@ -21,7 +21,12 @@ Parity status (each function is pinned in tests/test_oracle_pins.py):
   lse_merge / split_decode ...... pinned (any split = unsplit)
   bytes_per_token / cache_bytes / paged_waste_slots ... pinned (page figures)
   sparse_schedule ............... pinned through its parts (Reuse = earlier
-                                  indices; Reindex = own scores)
+                                  indices; Reindex = own scores; with a pool:
+                                  Reindex picks inside the pool)
+  indexer_pool / pool_positions /
+  indexer_topk_in_pool .......... pinned (set brute force, the cap, the
+                                  page's 16,384 figure, full pool = full
+                                  top-k, plain-loop top-k over candidates)
 """
 import math
 
@@ -279,11 +284,63 @@ def sparse_decode(q, k_raw, v_raw, block_table, seq_lens, block_size,
     return out, lse
 
 
+# ---------------------------------------------------------------------------
+# hierarchical indexer ([890] section 4: the first Full layer publishes the
+# blocks its selection came from as a candidate pool, capped at 2,048 blocks
+# of 8 positions; later Reindex layers pick their own top-k only from the
+# pool. [POD]: "two thousand forty-eight blocks times eight positions,
+# sixteen thousand three hundred eighty-four candidates")
+# ---------------------------------------------------------------------------
+POOL_BLOCK = 8      # positions per pool block
+POOL_CAP = 2048     # blocks a pool holds
+
+
+def indexer_pool(indices, seq_lens, cap=POOL_CAP):
+    """The pool a Full layer publishes, per sequence: the ascending ids of
+    the 8-position blocks (position // 8) that hold its selected positions,
+    entries < 0 or >= seq_len ignored, at most ``cap`` of them (the lowest:
+    a reading, the pages give only the cap). Returns a list of int64
+    arrays."""
+    pools = []
+    for b, row in enumerate(np.asarray(indices, dtype=np.int64)):
+        ok = row[(row >= 0) & (row < int(seq_lens[b]))]
+        pools.append(np.unique(ok // POOL_BLOCK)[:cap])
+    return pools
+
+
+def pool_positions(pool_blocks, seq_len):
+    """The candidates of a pool: every position of its blocks that is
+    visible (< seq_len), ascending."""
+    blocks = np.asarray(pool_blocks, dtype=np.int64)
+    pos = (blocks[:, None] * POOL_BLOCK + np.arange(POOL_BLOCK)).reshape(-1)
+    return pos[pos < int(seq_len)]
+
+
+def indexer_topk_in_pool(q_idx, w, idx_raw, block_table, seq_lens,
+                         block_size, pools, k):
+    """A Reindex layer over a pool: the indexer score of each candidate,
+    then the k largest among the candidates (equal scores to the lower
+    position), as positions in ascending order, -1 padded. Returns
+    (indices [B][k], list of candidate-score arrays)."""
+    full = indexer_scores(q_idx, w, idx_raw, block_table, seq_lens,
+                          block_size)
+    idx, cand = [], []
+    for b, s in enumerate(full):
+        pos = pool_positions(pools[b], seq_lens[b])
+        sel = topk_select(s[pos], k)
+        idx.append(np.where(sel >= 0, pos[np.maximum(sel, 0)], -1))
+        cand.append(s[pos])
+    return np.stack(idx).astype(np.int32), cand
+
+
 def sparse_schedule(modes, q, q_idx, w, k_raw, v_raw, idx_raw, block_table,
-                    seq_lens, block_size, k, scale=None):
+                    seq_lens, block_size, k, scale=None, pool_k=None):
     """A static layer schedule over one shared main cache and one shared
     indexer cache ([890] section 3: Full and Reindex layers score and pick
     their own top-k; a Reuse layer attends to the most recent selection).
+    With ``pool_k`` ([890] section 4), the first Full layer's selection
+    publishes a pool and every Reindex layer picks its top-``pool_k`` from
+    that pool.
 
     modes: sequence of "full" | "reindex" | "reuse" (the first must not be
     "reuse"); q[l], q_idx[l], w[l]: per-layer inputs. Returns
@@ -291,10 +348,17 @@ def sparse_schedule(modes, q, q_idx, w, k_raw, v_raw, idx_raw, block_table,
     """
     outs, lses, sel = [], [], []
     current = None
+    pools = None
     for layer, mode in enumerate(modes):
-        if mode in ("full", "reindex"):
+        if mode == "reindex" and pool_k is not None and pools is not None:
+            current, _ = indexer_topk_in_pool(q_idx[layer], w[layer], idx_raw,
+                                              block_table, seq_lens,
+                                              block_size, pools, pool_k)
+        elif mode in ("full", "reindex"):
             current, _ = indexer_topk(q_idx[layer], w[layer], idx_raw,
                                       block_table, seq_lens, block_size, k)
+            if mode == "full" and pool_k is not None and pools is None:
+                pools = indexer_pool(current, seq_lens)
         elif mode != "reuse" or current is None:
             raise ValueError(f"bad schedule at layer {layer}: {mode}")
         o, l = sparse_decode(q[layer], k_raw, v_raw, block_table, seq_lens,

@@ -176,3 +176,19 @@ def test_fp4_scale_from_amax_over_4_is_caught(monkeypatch):
         return np.concatenate([packed, sc], axis=-1)
     monkeypatch.setattr(oracle, "mxfp4_encode_rows", mutant)
     _fails(P.test_mxfp4_scaled_grid_round_trips)
+
+
+def test_pool_of_16_position_blocks_is_caught(monkeypatch):
+    def mutant(indices, seq_lens, cap=2048):
+        return [np.unique(np.asarray(r)[(np.asarray(r) >= 0)
+                                        & (np.asarray(r) < L)] // 16)[:cap]
+                for r, L in zip(indices, seq_lens)]
+    _patch(monkeypatch, "indexer_pool", mutant)
+    _fails(P.test_pool_is_the_set_of_selected_blocks)
+
+
+def test_reindex_ignoring_the_pool_is_caught(monkeypatch):
+    def mutant(q_idx, w, idx_raw, bt, seq_lens, bs, pools, k):
+        return OA.indexer_topk(q_idx, w, idx_raw, bt, seq_lens, bs, k)
+    _patch(monkeypatch, "indexer_topk_in_pool", mutant)
+    _fails(P.test_topk_in_pool_brute_force)

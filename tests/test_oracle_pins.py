@@ -736,3 +736,94 @@ def test_append_mxfp4_writes_one_encoded_row():
         assert np.array_equal(out[bt[b, p // 8], :, p % 8, :],
                               O.mxfp4_encode_rows(new[b]))
     assert np.count_nonzero(np.any(out != kr, axis=3)) <= 4
+
+
+# ---------------------------------------------------------------------------
+# hierarchical indexer pool ("890 bytes a token ...", section 4)
+# ---------------------------------------------------------------------------
+def test_pool_capacity_is_the_page_figure(golden_dir):
+    fig = _load(golden_dir, "page_figures.json")["indexer_pool"]
+    assert O.POOL_CAP == fig["blocks"]
+    assert O.POOL_BLOCK == fig["positions_per_block"]
+    assert O.POOL_CAP * O.POOL_BLOCK == fig["candidates"] == 16384
+
+
+def test_pool_is_the_set_of_selected_blocks():
+    rng = np.random.default_rng(60)
+    lens = [1000, 37, 0, 5000]
+    idx = np.full((4, 300), -1, dtype=np.int64)
+    for b, L in enumerate(lens):
+        n = min(L, int(rng.integers(0, 300)))
+        if n:
+            idx[b, :n] = np.sort(rng.choice(L + 40, n, replace=False))
+    pools = O.indexer_pool(idx, lens)
+    for b, L in enumerate(lens):
+        want = sorted({int(t) // 8 for t in idx[b] if 0 <= t < L})
+        assert list(pools[b]) == want
+        cand = O.pool_positions(pools[b], L)
+        assert list(cand) == [p for p in range(L) if p // 8 in set(want)]
+        for t in idx[b]:                      # every selection is a candidate
+            if 0 <= t < L:
+                assert t in set(cand)
+
+
+def test_pool_cap_keeps_the_lowest_blocks():
+    idx = np.arange(0, 8 * 3000, 8)[None, :]             # 3000 blocks
+    pools = O.indexer_pool(idx, [8 * 3000])
+    assert list(pools[0]) == list(range(2048))
+
+
+def _pool_case(seed, lens, k_full, bs=8, d=8):
+    rng = np.random.default_rng(seed)
+    ir, _, bt = _random_paged(rng, len(lens), 1, d, bs, lens)
+    qI = rng.standard_normal((len(lens), 2, d))
+    w = rng.uniform(0, 1, (len(lens), 2))
+    full, _ = O.indexer_topk(qI, w, ir, bt, lens, bs, k_full)
+    return ir, bt, qI, w, full
+
+
+def test_topk_in_full_pool_equals_full_topk():
+    lens = [50, 123]
+    ir, bt, qI, w, _ = _pool_case(61, lens, 4)
+    pools = [np.arange((L + 7) // 8) for L in lens]      # every block
+    a, _ = O.indexer_topk_in_pool(qI, w, ir, bt, lens, 8, pools, 9)
+    b, _ = O.indexer_topk(qI, w, ir, bt, lens, 8, 9)
+    assert np.array_equal(a, b)
+
+
+def test_topk_in_pool_brute_force():
+    lens = [90, 200, 13]
+    ir, bt, qI, w, full = _pool_case(62, lens, 6)
+    pools = O.indexer_pool(full, lens)
+    got, cand = O.indexer_topk_in_pool(qI, w, ir, bt, lens, 8, pools, 10)
+    scores = O.indexer_scores(qI, w, ir, bt, lens, 8)
+    for b, L in enumerate(lens):
+        blocks = set(int(t) // 8 for t in full[b] if t >= 0)
+        c = [t for t in range(L) if t // 8 in blocks]      # plain loops
+        best = sorted(c, key=lambda t: (-scores[b][t], t))[:10]
+        want = sorted(best) + [-1] * (10 - len(best))
+        assert list(got[b]) == want
+        assert all(t == -1 or t // 8 in blocks for t in got[b])
+
+
+def test_schedule_with_pool():
+    rng = np.random.default_rng(63)
+    lens = [70, 150]
+    bs, k, kp = 8, 12, 5
+    kr, vr, bt = _random_paged(rng, 2, 1, 16, bs, lens)
+    ir, _, _ = _random_paged(np.random.default_rng(64), 2, 1, 8, bs, lens)
+    ir = ir[:kr.shape[0]]
+    modes = ["full", "reuse", "reindex", "reindex"]
+    q = [rng.standard_normal((2, 4, 16)) for _ in modes]
+    qI = [rng.standard_normal((2, 4, 8)) for _ in modes]
+    w = [rng.uniform(0, 1, (2, 4)) for _ in modes]
+    _, _, sel = O.sparse_schedule(modes, q, qI, w, kr, vr, ir, bt, lens, bs,
+                                  k, pool_k=kp)
+    i0, _ = O.indexer_topk(qI[0], w[0], ir, bt, lens, bs, k)
+    pools = O.indexer_pool(i0, lens)
+    assert np.array_equal(sel[0], i0) and np.array_equal(sel[1], i0)
+    for layer in (2, 3):
+        want, _ = O.indexer_topk_in_pool(qI[layer], w[layer], ir, bt, lens,
+                                         bs, pools, kp)
+        assert np.array_equal(sel[layer], want)
+        assert sel[layer].shape == (2, kp)
