@@ -165,7 +165,8 @@ typedef enum kvd_op {
   KVD_OP_GQA_DECODE = 0,
   KVD_OP_MLA_DECODE = 1,
   KVD_OP_INDEXER_TOPK = 2,
-  KVD_OP_SPARSE_DECODE = 3
+  KVD_OP_SPARSE_DECODE = 3,
+  KVD_OP_INDEXER_TOPK_POOL = 4
 } kvd_op;
 
 /*
@@ -320,6 +321,58 @@ kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
                             const float *w, int32_t k, int32_t *indices,
                             float *scores, void *workspace,
                             size_t workspace_bytes, kvd_stream stream);
+
+/*
+ * The hierarchical indexer ("890 bytes a token", section 4; the My Weird
+ * Prompts 640482 transcript on CSA2): the first Full layer publishes the
+ * blocks its selection came from as a candidate pool of at most 2,048
+ * blocks of 8 positions (16,384 candidates), and later Reindex layers
+ * select only from that pool, so their cost is bounded by the pool, not by
+ * the context length.
+ */
+#define KVD_POOL_BLOCKS 2048 /* blocks a pool holds                         */
+#define KVD_POOL_BLOCK 8     /* positions per pool block                    */
+
+/*
+ * kvd_indexer_pool -- the pool of a selection.
+ *   indices  device int32 [batch][k]: positions in any order; entries < 0
+ *            are skipped, and so are entries >= seq_lens[b] (flagged
+ *            KVD_DEVERR_INDEX)
+ *   pool     device int32 [batch][KVD_POOL_BLOCKS], written: the ascending
+ *            ids (position / 8) of the blocks holding a selected position,
+ *            the lowest KVD_POOL_BLOCKS when there are more; entries past
+ *            pool_n[b] are unspecified
+ *   pool_n   device int32 [batch], written: the blocks in each pool
+ * Reads seqs->seq_lens only (not the block table). Supported: k >= 1,
+ * max_seq_len <= 50,331,648.
+ */
+kvd_status kvd_indexer_pool(const kvd_seqs *seqs, const int32_t *indices,
+                            int32_t k, int32_t *pool, int32_t *pool_n,
+                            kvd_stream stream);
+
+/*
+ * kvd_indexer_topk_pool -- a Reindex layer over a pool: the indexer scores
+ * of the pool's candidates only (positions 8 * pool[b][i] + j, j < 8, that
+ * are below seq_lens[b]), and the top k of them, selected as
+ * kvd_indexer_topk selects (fp32 scores, equal scores to the lower
+ * position, ascending positions, -1 padding).
+ *   pool, pool_n  device, as kvd_indexer_pool writes them
+ *   scores        device fp32 [batch][KVD_POOL_BLOCKS * 8] or NULL: if
+ *                 given, the candidate scores by pool entry (entry e is
+ *                 position 8 * pool[b][e / 8] + e % 8; entries at or past
+ *                 seq_lens[b] are -inf, entries past 8 * pool_n[b]
+ *                 unspecified)
+ *   workspace     when scores is NULL: at least
+ *                 kvd_workspace_size(KVD_OP_INDEXER_TOPK_POOL) bytes
+ * Other arguments as for kvd_indexer_topk, and block_size a multiple of 8.
+ */
+kvd_status kvd_indexer_topk_pool(const kvd_cache *index_cache,
+                                 const kvd_seqs *seqs, const void *q_idx,
+                                 int32_t n_idx_heads, const float *w,
+                                 const int32_t *pool, const int32_t *pool_n,
+                                 int32_t k, int32_t *indices, float *scores,
+                                 void *workspace, size_t workspace_bytes,
+                                 kvd_stream stream);
 
 /*
  * kvd_sparse_decode -- GQA decode restricted to given positions ("890 bytes

@@ -19,7 +19,8 @@ from . import _native
 from ._native import KvdError, check, lib
 
 __all__ = ["PagedCache", "kv_append", "gqa_decode", "mla_decode",
-           "indexer_topk", "sparse_decode", "workspace_size",
+           "indexer_topk", "indexer_pool", "indexer_topk_pool",
+           "sparse_decode", "workspace_size",
            "bytes_per_token", "device_error", "KvdError",
            "OP_GQA_DECODE", "OP_MLA_DECODE", "OP_INDEXER_TOPK",
            "OP_SPARSE_DECODE"]
@@ -32,6 +33,9 @@ OP_GQA_DECODE = 0
 OP_MLA_DECODE = 1
 OP_INDEXER_TOPK = 2
 OP_SPARSE_DECODE = 3
+OP_INDEXER_TOPK_POOL = 4
+POOL_BLOCKS = 2048   # KVD_POOL_BLOCKS
+POOL_BLOCK = 8       # KVD_POOL_BLOCK
 
 
 def _ptr(t):
@@ -243,6 +247,58 @@ def indexer_topk(cache, block_table, seq_lens, max_seq_len, q_idx, w, k,
                                  _ptr(indices), _ptr(scores), _ptr(ws),
                                  0 if ws is None else ws.numel(),
                                  _stream(stream)))
+    return indices, scores
+
+
+def indexer_pool(block_table, seq_lens, max_seq_len, indices, pool=None,
+                 pool_n=None, stream=None):
+    """The hierarchical indexer's pool of a selection indices [batch][k]:
+    returns (pool [batch][POOL_BLOCKS] ascending 8-position block ids,
+    pool_n [batch] their counts)."""
+    import torch
+    _need(indices, "indices", torch.int32)
+    B, k = indices.shape
+    s = _seqs(block_table, seq_lens, max_seq_len)
+    if pool is None:
+        pool = torch.empty((B, POOL_BLOCKS), dtype=torch.int32,
+                           device=indices.device)
+    if pool_n is None:
+        pool_n = torch.empty((B,), dtype=torch.int32, device=indices.device)
+    _need(pool, "pool", torch.int32, B * POOL_BLOCKS)
+    _need(pool_n, "pool_n", torch.int32, B)
+    check(lib().kvd_indexer_pool(ctypes.byref(s), _ptr(indices), k,
+                                 _ptr(pool), _ptr(pool_n), _stream(stream)))
+    return pool, pool_n
+
+
+def indexer_topk_pool(cache, block_table, seq_lens, max_seq_len, q_idx, w,
+                      pool, pool_n, k, indices=None, scores=None,
+                      workspace=None, stream=None):
+    """A Reindex layer over a pool: indexer scores of the pool's candidates
+    and their top k. Returns (indices [batch][k] int32, scores)."""
+    import torch
+    _need(q_idx, "q_idx", torch.bfloat16)
+    _need(w, "w", torch.float32, q_idx.shape[0] * q_idx.shape[1])
+    c = cache.struct()
+    s = _seqs(block_table, seq_lens, max_seq_len)
+    B = q_idx.shape[0]
+    _need(pool, "pool", torch.int32, B * POOL_BLOCKS)
+    _need(pool_n, "pool_n", torch.int32, B)
+    if indices is None:
+        indices = torch.empty((B, k), dtype=torch.int32, device=q_idx.device)
+    _need(indices, "indices", torch.int32, B * k)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, B * POOL_BLOCKS * POOL_BLOCK)
+        ws = None
+    else:
+        ws = _workspace(OP_INDEXER_TOPK_POOL, cache, block_table, seq_lens,
+                        max_seq_len, q_idx.shape[1], k, workspace)
+    check(lib().kvd_indexer_topk_pool(ctypes.byref(c), ctypes.byref(s),
+                                      _ptr(q_idx), q_idx.shape[1], _ptr(w),
+                                      _ptr(pool), _ptr(pool_n), k,
+                                      _ptr(indices), _ptr(scores), _ptr(ws),
+                                      0 if ws is None else ws.numel(),
+                                      _stream(stream)))
     return indices, scores
 
 

@@ -67,6 +67,12 @@ _SIGS = {
     "kvd_indexer_topk": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
                                    c_void_p, c_int32, c_void_p, c_void_p,
                                    c_void_p, c_size_t, c_void_p]),
+    "kvd_indexer_pool": (c_int32, [_PSEQS, c_void_p, c_int32, c_void_p,
+                                   c_void_p, c_void_p]),
+    "kvd_indexer_topk_pool": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
+                                        c_void_p, c_void_p, c_void_p, c_int32,
+                                        c_void_p, c_void_p, c_void_p,
+                                        c_size_t, c_void_p]),
     "kvd_sparse_decode": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
                                     c_void_p, c_int32, c_float, c_void_p,
                                     c_void_p, c_void_p, c_size_t, c_void_p]),

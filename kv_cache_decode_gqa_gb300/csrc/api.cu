@@ -445,6 +445,10 @@ kvd_status kvd_workspace_size(kvd_op op, const kvd_cache *cache,
     case KVD_OP_INDEXER_TOPK:
       *bytes = topk_ws_bytes(seqs);
       return ok();
+    case KVD_OP_INDEXER_TOPK_POOL:
+      *bytes = round_up((size_t)seqs->batch * kvd::kPoolBlocks *
+                            kvd::kPoolBlock * 4, 256);
+      return ok();
   }
   return fail(KVD_ERR_UNSUPPORTED, "workspace_size: unknown op %d", (int)op);
 }
@@ -680,11 +684,18 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   return launched(kvd::launch_decode_sparse(p, s), "sparse_decode");
 }
 
-kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
-                            const void *q_idx, int32_t n_idx_heads,
-                            const float *w, int32_t k, int32_t *indices,
-                            float *scores, void *workspace,
-                            size_t workspace_bytes, kvd_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// kvd_indexer_topk and (pool != NULL) kvd_indexer_topk_pool.
+kvd_status indexer_topk_impl(const kvd_cache *index_cache,
+                             const kvd_seqs *seqs, const void *q_idx,
+                             int32_t n_idx_heads, const float *w,
+                             const int32_t *pool, const int32_t *pool_n,
+                             int32_t k, int32_t *indices, float *scores,
+                             void *workspace, size_t workspace_bytes,
+                             kvd_stream stream) {
   kvd_status st = check_cache(index_cache, false, "indexer_topk");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, index_cache, "indexer_topk");
@@ -697,17 +708,26 @@ kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
     return fail(KVD_ERR_UNSUPPORTED, "indexer_topk: 1..8 indexer heads");
   if (k < 1 || k > 16384)
     return fail(KVD_ERR_UNSUPPORTED, "indexer_topk: k must be in [1, 16384]");
+  if (pool && index_cache->block_size % kvd::kPoolBlock != 0)
+    return fail(KVD_ERR_UNSUPPORTED, "indexer_topk_pool: block_size must be "
+                "a multiple of 8");
   if (seqs->batch == 0) return ok();
   if (!q_idx || !w || !indices)
     return fail(KVD_ERR_NULL, "indexer_topk: q_idx, w and indices required");
+  if (pool && !pool_n)
+    return fail(KVD_ERR_NULL, "indexer_topk_pool: pool and pool_n required");
   if (!aligned(q_idx, 16))
     return fail(KVD_ERR_SHAPE, "indexer_topk: q_idx must be 16-byte aligned");
   const DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != KVD_OK) return st;
+  const int entries = pool ? kvd::kPoolBlocks * kvd::kPoolBlock
+                           : seqs->max_seq_len;
   float *sc = scores;
   if (!sc) {
-    const size_t need = topk_ws_bytes(seqs);
+    const size_t need =
+        pool ? round_up((size_t)seqs->batch * entries * 4, 256)
+             : topk_ws_bytes(seqs);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
       return fail(KVD_ERR_WORKSPACE, "indexer_topk: workspace of %zu bytes "
                   "(256-byte aligned) required when scores is NULL", need);
@@ -727,13 +747,76 @@ kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
   p.num_blocks = index_cache->num_blocks;
   p.max_blocks = seqs->max_blocks_per_seq;
   p.max_seq_len = seqs->max_seq_len;
-  p.score_stride = std::max(seqs->max_seq_len, 1);
+  p.score_stride = std::max(entries, 1);
   p.topk = k;
+  p.pool = pool;
+  p.pool_n = pool_n;
+  p.max_entries = entries;
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = launched(kvd::launch_indexer_scores(p, s), "indexer_topk (scores)");
   if (st != KVD_OK) return st;
   return launched(kvd::launch_topk(p, s), "indexer_topk (select)");
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
+                            const void *q_idx, int32_t n_idx_heads,
+                            const float *w, int32_t k, int32_t *indices,
+                            float *scores, void *workspace,
+                            size_t workspace_bytes, kvd_stream stream) {
+  return indexer_topk_impl(index_cache, seqs, q_idx, n_idx_heads, w, nullptr,
+                           nullptr, k, indices, scores, workspace,
+                           workspace_bytes, stream);
+}
+
+kvd_status kvd_indexer_topk_pool(const kvd_cache *index_cache,
+                                 const kvd_seqs *seqs, const void *q_idx,
+                                 int32_t n_idx_heads, const float *w,
+                                 const int32_t *pool, const int32_t *pool_n,
+                                 int32_t k, int32_t *indices, float *scores,
+                                 void *workspace, size_t workspace_bytes,
+                                 kvd_stream stream) {
+  if (!pool)
+    return fail(KVD_ERR_NULL, "indexer_topk_pool: pool required");
+  return indexer_topk_impl(index_cache, seqs, q_idx, n_idx_heads, w, pool,
+                           pool_n, k, indices, scores, workspace,
+                           workspace_bytes, stream);
+}
+
+kvd_status kvd_indexer_pool(const kvd_seqs *seqs, const int32_t *indices,
+                            int32_t k, int32_t *pool, int32_t *pool_n,
+                            kvd_stream stream) {
+  if (!seqs) return fail(KVD_ERR_NULL, "indexer_pool: seqs is NULL");
+  if (seqs->batch < 0 || seqs->batch > 65535 || seqs->max_seq_len < 0)
+    return fail(KVD_ERR_SHAPE, "indexer_pool: 0 <= batch <= 65535 and "
+                "max_seq_len >= 0 required");
+  if (k < 1) return fail(KVD_ERR_SHAPE, "indexer_pool: k must be >= 1");
+  if ((long)seqs->max_seq_len > 50331648L)
+    return fail(KVD_ERR_UNSUPPORTED, "indexer_pool: max_seq_len above "
+                "50,331,648");
+  if (seqs->batch == 0) return ok();
+  if (!seqs->seq_lens || !indices || !pool || !pool_n)
+    return fail(KVD_ERR_NULL, "indexer_pool: seq_lens, indices, pool and "
+                "pool_n required");
+  const DeviceInfo *d = nullptr;
+  kvd_status st = device_info(&d);
+  if (st != KVD_OK) return st;
+  kvd::PoolParams p{};
+  p.indices = indices;
+  p.seq_lens = seqs->seq_lens;
+  p.pool = pool;
+  p.pool_n = pool_n;
+  p.batch = seqs->batch;
+  p.k = k;
+  p.max_seq_len = seqs->max_seq_len;
+  p.err = d->err;
+  return launched(kvd::launch_indexer_pool(
+                      p, reinterpret_cast<cudaStream_t>(stream)),
+                  "indexer_pool");
 }
 
 }  // extern "C"

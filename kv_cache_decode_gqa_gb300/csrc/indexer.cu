@@ -73,10 +73,13 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const int b = blockIdx.y;
   int T = p.seq_lens[b];
   T = max(0, min(T, p.max_seq_len));
+  // entries: the visible positions, or (pool mode) the pool's positions
+  const int32_t *pool = p.pool ? p.pool + (long)b * kPoolBlocks : nullptr;
+  const int E = pool ? kPoolBlock * max(0, min(p.pool_n[b], kPoolBlocks)) : T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tw = blockIdx.x * kTokPerCta + warp * kSlice;  // warp's first
-  if (tw >= T) return;
-  const int rows = min(kSlice, T - tw);
+  if (tw >= E) return;
+  const int rows = min(kSlice, E - tw);
   uint8_t *mine = srows + warp * kSlice * kIdxDim * 2;
   uint64_t *bar = &bars[warp];
   if (lane == 0) {
@@ -88,8 +91,29 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   // one copy per block piece of the slice; lane j takes pieces j, j + 32..
   const int32_t *bt = p.block_table + (long)b * p.max_blocks;
   const int bs = p.block_size;
+  if (pool) {
+    // one copy per pool block (8 rows, inside one cache block); a block past
+    // the visible length reads block 0 (its scores are set to -inf below)
+    if (lane < rows / kPoolBlock) {
+      const int pos0 = kPoolBlock * pool[tw / kPoolBlock + lane];
+      int blk = 0, slot = 0;
+      if (pos0 >= 0 && pos0 < T) {
+        blk = bt[pos0 / bs];
+        slot = pos0 % bs;
+        if (blk < 0 || blk >= p.num_blocks) {
+          report(p.err, DEVERR_BLOCK);
+          blk = 0;  // read a valid block; the result is flagged as wrong
+        }
+      } else {
+        report(p.err, DEVERR_INDEX);
+      }
+      bulk_g2s(mine + lane * kPoolBlock * kIdxDim * 2,
+               p.cache + ((long)blk * bs + slot) * kIdxDim * 2,
+               kPoolBlock * kIdxDim * 2, bar);
+    }
+  }
   const int lb0 = tw / bs, lb1 = (tw + rows - 1) / bs;
-  for (int lb = lb0 + lane; lb <= lb1; lb += 32) {
+  for (int lb = lb0 + lane; !pool && lb <= lb1; lb += 32) {
     int blk = bt[lb];
     if (blk < 0 || blk >= p.num_blocks) {
       report(p.err, DEVERR_BLOCK);
@@ -149,7 +173,14 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       s = fmaf(w[j], fmaxf(d, 0.f), s);
     }
-    if (sub == 0 && r < rows) out[r] = s;
+    if (sub == 0 && r < rows) {
+      if (pool) {
+        const int pos = kPoolBlock * pool[(tw + r) / kPoolBlock] +
+                        (tw + r) % kPoolBlock;
+        if (pos < 0 || pos >= T) s = -INFINITY;
+      }
+      out[r] = s;
+    }
   }
 }
 
@@ -266,9 +297,21 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int k = p.topk;
   const float *sc = p.scores + (long)b * p.score_stride;
   int32_t *out = p.indices + (long)b * k;
+  // pool mode: entries are the pool's positions (ascending), selected by
+  // entry and written as positions (-1 for one past the visible length,
+  // which are the last entries)
+  const int32_t *pool = p.pool ? p.pool + (long)b * kPoolBlocks : nullptr;
+  const int Tv = T;
+  if (pool) T = kPoolBlock * max(0, min(p.pool_n[b], kPoolBlocks));
+  auto position = [&](int e) -> int32_t {
+    if (!pool) return e;
+    const int pos = kPoolBlock * pool[e / kPoolBlock] + e % kPoolBlock;
+    return pos >= 0 && pos < Tv ? pos : -1;
+  };
   if (T <= k) {  // every position, then -1 padding (uniform per cluster)
     if (rank == 0)
-      for (int i = tid; i < k; i += kTopkThreads) out[i] = i < T ? i : -1;
+      for (int i = tid; i < k; i += kTopkThreads)
+        out[i] = i < T ? position(i) : -1;
     return;
   }
   const int r0 = (int)((long)T * rank / kCluster);
@@ -435,7 +478,8 @@ __global__ void __launch_bounds__(kTopkThreads)
 #pragma unroll
     for (int j = 0; j < kRun / 32; ++j) {
       const int at = pos + __popc(selb[j] & lt);
-      if (((selb[j] >> lane) & 1) && at < k) out[at] = r0 + run + 32 * j + lane;
+      if (((selb[j] >> lane) & 1) && at < k)
+        out[at] = position(r0 + run + 32 * j + lane);
       pos += __popc(selb[j]);
     }
     run_eq += tot_eq;
@@ -446,19 +490,76 @@ __global__ void __launch_bounds__(kTopkThreads)
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// hierarchical indexer pool
+// ---------------------------------------------------------------------------
+// One CTA per sequence: a bitmap of the 8-position blocks holding the
+// selection's visible positions (one bit per block, shared memory), then an
+// ordered compaction: thread t counts the set bits of its run of words, a
+// block scan places the runs, and each thread writes its block ids in
+// ascending order while their rank is below the cap (the lowest blocks
+// kept).
+constexpr int kPoolThreads = 1024;
+constexpr int kPoolSmemMax = 192 * 1024;  // bitmap of up to 50M positions
+
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(const PoolParams p) {
+  extern __shared__ uint32_t bm[];  // (max_seq_len + 255) / 256 words
+  __shared__ int s_wsum[32];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  int T = p.seq_lens[b];
+  T = max(0, min(T, p.max_seq_len));
+  const int words = (T + 255) >> 8;
+  for (int i = tid; i < words; i += kPoolThreads) bm[i] = 0u;
+  __syncthreads();
+  const int32_t *idx = p.indices + (long)b * p.k;
+  for (int i = tid; i < p.k; i += kPoolThreads) {
+    const int t = idx[i];
+    if (t >= T) report(p.err, DEVERR_INDEX);
+    if (t >= 0 && t < T) atomicOr(&bm[t >> 8], 1u << ((t >> 3) & 31));
+  }
+  __syncthreads();
+  const int per = (words + kPoolThreads - 1) / kPoolThreads;
+  const int w0 = min(tid * per, words), w1 = min(w0 + per, words);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+  // exclusive scan of cnt over the CTA: within the warp, then the warps
+  int x = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  int total;
+  const int wexcl =
+      warp_excl_scan(__shfl_sync(0xffffffffu, x, 31), s_wsum, &total);
+  int rank = wexcl + x - cnt;
+  int32_t *pool = p.pool + (long)b * kPoolBlocks;
+  for (int w = w0; w < w1 && rank < kPoolBlocks; ++w) {
+    uint32_t bits = bm[w];
+    while (bits && rank < kPoolBlocks) {
+      pool[rank++] = w * 32 + __ffs(bits) - 1;
+      bits &= bits - 1;
+    }
+  }
+  if (tid == 0) p.pool_n[b] = min(total, kPoolBlocks);
+}
+
 template <int H>
 cudaError_t launch_scores_h(const IndexerParams &p, cudaStream_t s) {
   constexpr int kSmem = kTokPerCta * kIdxDim * 2;
   static bool done[64] = {};
   cudaError_t e = set_smem_once(indexer_score_kernel<H>, kSmem, done);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.max_seq_len + kTokPerCta - 1) / kTokPerCta, p.batch);
+  dim3 grid((p.max_entries + kTokPerCta - 1) / kTokPerCta, p.batch);
   return launch_pdl(indexer_score_kernel<H>, grid, dim3(kScoreThreads), kSmem,
                     s, 1, p);
 }
 
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s) {
-  if (p.batch == 0 || p.max_seq_len == 0) return cudaSuccess;
+  if (p.batch == 0 || p.max_seq_len == 0 || p.max_entries == 0)
+    return cudaSuccess;
   if (p.n_heads <= 1) return launch_scores_h<1>(p, s);
   if (p.n_heads <= 2) return launch_scores_h<2>(p, s);
   if (p.n_heads <= 4) return launch_scores_h<4>(p, s);
@@ -472,10 +573,21 @@ cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s) {
   cudaError_t e = set_smem_once(topk_kernel, kCacheKeys * 4, done);
   if (e != cudaSuccess) return e;
   // the largest range a CTA owns; cached in shared memory when it fits
-  const long range = ((long)p.max_seq_len + kCluster - 1) / kCluster;
+  const long range = ((long)p.max_entries + kCluster - 1) / kCluster;
   return launch_pdl(topk_kernel, dim3(p.batch * kCluster), dim3(kTopkThreads),
                     range <= kCacheKeys ? (size_t)range * 4 : 0, s, kCluster,
                     p);
+}
+
+cudaError_t launch_indexer_pool(const PoolParams &p, cudaStream_t s) {
+  if (p.batch == 0) return cudaSuccess;
+  const int smem = ((p.max_seq_len + 255) / 256) * 4;
+  if (smem > kPoolSmemMax) return cudaErrorNotSupported;
+  static bool done[64] = {};
+  cudaError_t e = set_smem_once(pool_kernel, kPoolSmemMax, done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(pool_kernel, dim3(p.batch), dim3(kPoolThreads),
+                    (size_t)smem, s, 1, p);
 }
 
 }  // namespace kvd

@@ -85,11 +85,33 @@ struct IndexerParams {
   int32_t *indices;   // [batch][k]
   int32_t batch, n_heads, block_size, num_blocks, max_blocks, max_seq_len;
   int32_t score_stride, topk;
+  // pool mode (a Reindex layer of the hierarchical indexer), else null: the
+  // scored entries are the positions of the pool's 8-position blocks,
+  // entry e = position 8 pool[b][e / 8] + e % 8, scores and top-k indexed
+  // by entry, the selection mapped back to positions
+  const int32_t *pool;    // [batch][kPoolBlocks] ascending block ids
+  const int32_t *pool_n;  // [batch] blocks in the pool
+  int32_t max_entries;    // launch sizing: max_seq_len, or 8 * kPoolBlocks
+  int *err;
+};
+
+// The hierarchical indexer's pool: at most 2,048 blocks of 8 positions.
+constexpr int kPoolBlocks = 2048;
+constexpr int kPoolBlock = 8;
+
+struct PoolParams {
+  const int32_t *indices;  // [batch][k] a Full layer's selection
+  const int32_t *seq_lens;
+  int32_t *pool;    // [batch][kPoolBlocks]
+  int32_t *pool_n;  // [batch]
+  int32_t batch, k, max_seq_len;
   int *err;
 };
 
 // Launchers. Each returns the launch error (cudaSuccess if queued).
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+// The pool of a Full layer's selection (one CTA per sequence).
+cudaError_t launch_indexer_pool(const PoolParams &p, cudaStream_t s);
 // Dense GQA/MHA, CUDA cores (group size <= 4).
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s);
 // kv heads the CUDA-core kernel takes per work unit for these shapes (its

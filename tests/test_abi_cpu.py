@@ -38,7 +38,7 @@ def _seqs(**kw):
 
 def test_exports_every_declared_function(lib):
     names = N.header_functions()
-    assert len(names) == 13
+    assert len(names) == 15
     for name in names:
         assert hasattr(lib, name), name
     assert lib.kvd_version() == 1
@@ -166,3 +166,23 @@ def test_mxfp4_cache_validation(lib):
     lat = _cache(dtype=2, n_kv=1, head_dim=576, v=None)
     assert lib.kvd_mla_decode(ctypes.byref(lat), 512, ctypes.byref(s), FAKE,
                               128, 0.0, FAKE, None, None, 0, None) == 3
+
+
+def test_pool_validation(lib):
+    s = _seqs()
+    # k < 1, a NULL output, an overlong max_seq_len: rejected on the host
+    assert lib.kvd_indexer_pool(ctypes.byref(s), FAKE, 0, FAKE, FAKE,
+                                None) == 2
+    assert lib.kvd_indexer_pool(ctypes.byref(s), FAKE, 8, None, FAKE,
+                                None) == 1
+    assert lib.kvd_indexer_pool(ctypes.byref(_seqs(max_seq_len=60000000)),
+                                FAKE, 8, FAKE, FAKE, None) == 3
+    c = _cache(n_kv=1, head_dim=64, v=None, block_size=12)
+    s12 = _seqs(max_blocks_per_seq=100)
+    assert lib.kvd_indexer_topk_pool(ctypes.byref(c), ctypes.byref(s12), FAKE,
+                                     4, FAKE, FAKE, FAKE, 16, FAKE, None,
+                                     None, 0, None) == 3   # block_size % 8
+    c = _cache(n_kv=1, head_dim=64, v=None)
+    assert lib.kvd_indexer_topk_pool(ctypes.byref(c), ctypes.byref(s), FAKE,
+                                     4, FAKE, None, FAKE, 16, FAKE, None,
+                                     None, 0, None) == 1   # no pool

@@ -185,3 +185,166 @@ def test_schedule_matches_oracle():
         assert np.array_equal(used[l].cpu().numpy(), r_idx[l]), f"layer {l}"
         H.assert_close(H.to_np_bf16(outs[l]), r_out[l], f"layer {l}")
         H.assert_lse_close(lses[l].cpu().numpy(), r_lse[l], f"layer {l}")
+
+
+# ---------------------------------------------------------------------------
+# hierarchical indexer pool
+# ---------------------------------------------------------------------------
+def _gpu_pool(wl, idx_t):
+    pool, pool_n = K.indexer_pool(wl.block_table, wl.seq_lens,
+                                  wl.max_seq_len, idx_t)
+    torch.cuda.synchronize()
+    return pool.cpu().numpy(), pool_n.cpu().numpy()
+
+
+def _check_pool(pool, pool_n, want):
+    for b, w in enumerate(want):
+        assert pool_n[b] == len(w), (b, pool_n[b], len(w))
+        assert np.array_equal(pool[b, :len(w)], w), b
+
+
+def test_pool_matches_oracle():
+    s = _shape([5, 700, 3000, 64], 256, 64, 4)
+    wl = W.DeviceWorkload(s)
+    idx, _ = _run_indexer(wl, 0, scores=False)
+    pool, pool_n = _gpu_pool(wl, torch.from_numpy(idx).cuda())
+    _check_pool(pool, pool_n, oracle.indexer_pool(idx, s.seq_lens))
+    # any order, repeats and -1 entries
+    rng = np.random.default_rng(70)
+    sel = np.full((4, 300), -1, dtype=np.int32)
+    for b, T in enumerate(s.seq_lens):
+        n = min(T, 250)
+        sel[b, :n] = rng.integers(0, T, n)        # unsorted, repeats
+    rng.shuffle(sel, axis=1)
+    pool, pool_n = _gpu_pool(wl, torch.from_numpy(sel).cuda())
+    _check_pool(pool, pool_n, oracle.indexer_pool(sel, s.seq_lens))
+
+
+def test_pool_keeps_the_lowest_2048_blocks():
+    s = _shape([30000], 16, 64, 1)
+    wl = W.DeviceWorkload(s)
+    sel = (np.arange(3500, dtype=np.int32) * 8 + 3)[None, :]   # 3500 blocks
+    pool, pool_n = _gpu_pool(wl, torch.from_numpy(sel).cuda())
+    assert pool_n[0] == 2048 and np.array_equal(pool[0], np.arange(2048))
+
+
+def _run_pool_topk(wl, layer, pool_t, pool_n_t, k):
+    s = wl.shape
+    sc = torch.empty((s.batch, K.POOL_BLOCKS * K.POOL_BLOCK),
+                     dtype=torch.float32, device="cuda")
+    idx, sc = K.indexer_topk_pool(wl.idx_cache, wl.block_table, wl.seq_lens,
+                                  wl.max_seq_len, wl.q_idx[layer],
+                                  wl.w[layer], pool_t, pool_n_t, k, scores=sc)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+def _pool_rule_check(idx, sc, pools, lens, k):
+    """(i): the oracle's rule on the GPU's candidate scores, exactly."""
+    for b, T in enumerate(lens):
+        pos = oracle.pool_positions(pools[b], T)
+        cand = sc[b, :len(pos)].astype(np.float64)
+        sel = oracle.topk_select(cand, k)
+        want = np.where(sel >= 0, pos[np.maximum(sel, 0)], -1)
+        assert np.array_equal(idx[b], want), f"row {b}"
+        assert np.all(sc[b, len(pos):8 * len(pools[b])] == -np.inf)
+
+
+@pytest.mark.parametrize("lengths,k_full,k,bs", [
+    ([5, 63, 300, 2000], 64, 32, 64),      # T < k, pools smaller than k
+    ([4000, 1500], 256, 100, 16),
+    ([20000], 2048, 512, 64)])
+def test_pool_selection(lengths, k_full, k, bs):
+    s = _shape(lengths, k_full, bs, 4, modes=("full", "reindex"))
+    wl = W.DeviceWorkload(s)
+    full, _ = _run_indexer(wl, 0, scores=False)
+    pool_t, pool_n_t = K.indexer_pool(wl.block_table, wl.seq_lens,
+                                      wl.max_seq_len,
+                                      torch.from_numpy(full).cuda())
+    idx, sc = _run_pool_topk(wl, 1, pool_t, pool_n_t, k)
+    pools = oracle.indexer_pool(full, s.seq_lens)
+    _pool_rule_check(idx, sc, pools, s.seq_lens, k)
+    # candidate scores against the fp64 oracle
+    ir = _host_idx_cache(s, wl.paging, I.normal_bf16_table())
+    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, 1, W.T_QIDX,
+                                             (s.batch, 4, s.idx_dim)))
+    w = W.host_weights(s, 1).astype(np.float64)
+    _, cand = oracle.indexer_topk_in_pool(qI, w, ir, wl.paging.table,
+                                          s.seq_lens, bs, pools, k)
+    for b in range(s.batch):
+        np.testing.assert_allclose(sc[b, :len(cand[b])], cand[b], rtol=1e-5,
+                                   atol=1e-4)
+
+
+def test_pool_selection_exact_set_matches_fp64_oracle():
+    s = _shape([6000, 900], 512, 64, 4, modes=("full", "reindex"))
+    wl = W.DeviceWorkload(s)
+    tab = _exact_inputs(wl, s, [0, 1])
+    full, _ = _run_indexer(wl, 0, scores=False)
+    pool_t, pool_n_t = K.indexer_pool(wl.block_table, wl.seq_lens,
+                                      wl.max_seq_len,
+                                      torch.from_numpy(full).cuda())
+    idx, _ = _run_pool_topk(wl, 1, pool_t, pool_n_t, 128)
+    ir = _host_idx_cache(s, wl.paging, tab)
+    qs = [oracle.bf16_bits_to_f64(I.host_tensor(tab, W._key(s, l, W.T_QIDX),
+                                                (s.batch, 4, 64)))
+          for l in (0, 1)]
+    ws = [wl.w[l].cpu().numpy().astype(np.float64) for l in (0, 1)]
+    ref_full, _ = oracle.indexer_topk(qs[0], ws[0], ir, wl.paging.table,
+                                      s.seq_lens, 64, 512)
+    assert np.array_equal(full, ref_full)
+    ref, _ = oracle.indexer_topk_in_pool(
+        qs[1], ws[1], ir, wl.paging.table, s.seq_lens, 64,
+        oracle.indexer_pool(ref_full, s.seq_lens), 128)
+    assert np.array_equal(idx, ref)
+
+
+def test_schedule_with_pool_matches_oracle():
+    """Full, Reuse, Reindex x2 with a pool (Reindex layers pick 48 inside
+    the Full layer's pool), exact indexer inputs."""
+    modes = ["full", "reuse", "reindex", "reindex"]
+    kp = 48
+    s = _shape([3000, 900], 128, 64, 4, modes)
+    wl = W.DeviceWorkload(s)
+    tab = _exact_inputs(wl, s, [0, 2, 3])
+    outs = [torch.empty((s.batch, s.n_h, 512), dtype=torch.bfloat16,
+                        device="cuda") for _ in modes]
+    idxs = [torch.empty((s.batch, kp if m == "reindex" else s.topk),
+                        dtype=torch.int32, device="cuda") for m in modes]
+    used = S.sparse_schedule_step(
+        modes, wl.caches[0], wl.idx_cache, wl.block_table, wl.pos,
+        wl.seq_lens, wl.max_seq_len, [wl.q[l] for l in range(len(modes))],
+        wl.q_idx, wl.w, s.topk, outs, idxs, pool_k=kp)
+    torch.cuda.synchronize()
+    pg = wl.paging
+    kr = W.host_cache_full(s, pg, 0, W.T_K, n_kv=1)
+    vr = W.host_cache_full(s, pg, 0, W.T_V, n_kv=1)
+    ir = _host_idx_cache(s, pg, tab)
+    qs = [oracle.bf16_bits_to_f64(W.host_bf16(s, l, W.T_Q,
+                                              (s.batch, s.n_h, 512)))
+          for l in range(len(modes))]
+    qIs = [None if m == "reuse" else oracle.bf16_bits_to_f64(
+        I.host_tensor(tab, W._key(s, l, W.T_QIDX), (s.batch, 4, 64)))
+        for l, m in enumerate(modes)]
+    ws = [None if m == "reuse" else wl.w[l].cpu().numpy().astype(np.float64)
+          for l, m in enumerate(modes)]
+    # no append in this step: the caches as drawn, the same visible lengths
+    r_out, _, r_idx = oracle.sparse_schedule(
+        modes, qs, qIs, ws, kr, vr, ir, pg.table, s.seq_lens, s.block_size,
+        s.topk, pool_k=kp)
+    for l in range(len(modes)):
+        assert np.array_equal(used[l].cpu().numpy(), r_idx[l]), f"layer {l}"
+        H.assert_close(H.to_np_bf16(outs[l]), r_out[l], f"layer {l}")
+
+
+def test_full_size_pool():
+    s = W.config("sparse")
+    wl = W.DeviceWorkload(s, layers=[0, 4])
+    full, _ = _run_indexer(wl, 0, scores=False)
+    pool_t, pool_n_t = K.indexer_pool(wl.block_table, wl.seq_lens,
+                                      wl.max_seq_len,
+                                      torch.from_numpy(full).cuda())
+    idx, sc = _run_pool_topk(wl, 4, pool_t, pool_n_t, 512)
+    pools = oracle.indexer_pool(full, s.seq_lens)
+    _check_pool(pool_t.cpu().numpy(), pool_n_t.cpu().numpy(), pools)
+    _pool_rule_check(idx, sc, pools, s.seq_lens, 512)
