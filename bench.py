@@ -60,10 +60,30 @@ def kv_bytes_layer(shape, layer=0):
         return sum(s.seq_lens) * s.n_kv * 2 * s.head_dim * s.elem_bytes
     if s.kind == "mla":
         return sum(s.seq_lens) * s.head_dim * 2
-    sel = s.batch * min(s.topk, min(s.seq_lens)) * 2 * s.head_dim * 2
-    if s.modes[layer] in ("full", "reindex"):
+    sel = s.batch * min(layer_topk(s, layer), min(s.seq_lens)) * 2 * \
+        s.head_dim * 2
+    if s.modes[layer] == "reindex" and s.pool_k:
+        # a pooled Reindex layer scores only the pool's candidates (8 per
+        # pool block, counted on the device after the warm-up)
+        cands = getattr(s, "pool_cands", None)
+        if cands is None:
+            cands = sum(min(L, 16384) for L in s.seq_lens)
+        sel += cands * s.idx_dim * 2
+    elif s.modes[layer] in ("full", "reindex"):
         sel += sum(s.seq_lens) * s.idx_dim * 2
     return sel
+
+
+def layer_topk(s, layer):
+    """Positions the sparse schedule's layer attends to: its own
+    selection's size, or the one it reuses."""
+    k = s.topk
+    for m in s.modes[:layer + 1]:
+        if m == "full" or (m == "reindex" and not s.pool_k):
+            k = s.topk
+        elif m == "reindex":
+            k = s.pool_k
+    return k
 
 
 def kv_bytes_step(shape):
@@ -75,9 +95,13 @@ def decode_launch_bytes(shape):
     written (GQA: the call also appends, so + the new rows read and
     written)."""
     s = shape
-    b = (kv_bytes_layer(s) if s.kind != "sparse" else
-         s.batch * min(s.topk, min(s.seq_lens)) * 2 * s.head_dim * 2) \
-        + s.batch * s.n_h * s.head_dim * 2 + s.batch * s.n_h * s.dv * 2
+    if s.kind == "sparse":  # the average over the schedule's layers
+        rows = sum(min(layer_topk(s, l), min(s.seq_lens))
+                   for l in range(s.n_layers)) / s.n_layers
+        b = int(s.batch * rows * 2 * s.head_dim * 2)
+    else:
+        b = kv_bytes_layer(s)
+    b += s.batch * s.n_h * s.head_dim * 2 + s.batch * s.n_h * s.dv * 2
     if s.kind == "gqa":
         b += 2 * s.batch * s.n_kv * s.head_dim * (2 + s.elem_bytes)
     return b
@@ -401,12 +425,23 @@ def run_sparse_schedule(K, wl, outs, wss, events=None):
     K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
     K.kv_append(wl.idx_cache, wl.block_table, wl.pos, wl.idx_k_new)
     idx = None
+    pooled = False
     for layer in wl.layers:
-        if s.modes[layer] != "reuse":
+        if s.modes[layer] == "reindex" and pooled:
+            idx = wss["idx"][layer]
+            K.indexer_topk_pool(wl.idx_cache, wl.block_table, wl.seq_lens,
+                                wl.max_seq_len, wl.q_idx[layer], wl.w[layer],
+                                wss["pool"], wss["pool_n"], s.pool_k,
+                                indices=idx, workspace=wss["pooltopk"])
+        elif s.modes[layer] != "reuse":
             idx = wss["idx"][layer]
             K.indexer_topk(wl.idx_cache, wl.block_table, wl.seq_lens,
                            wl.max_seq_len, wl.q_idx[layer], wl.w[layer],
                            s.topk, indices=idx, workspace=wss["topk"])
+            if s.modes[layer] == "full" and s.pool_k and not pooled:
+                K.indexer_pool(wl.block_table, wl.seq_lens, wl.max_seq_len,
+                               idx, pool=wss["pool"], pool_n=wss["pool_n"])
+                pooled = True
         if events is not None:
             events[layer][0].record()
         K.sparse_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len, idx,
@@ -490,11 +525,23 @@ def run_ours(args, ws, rank, local):
                                  wl.seq_lens, wl.max_seq_len, s.n_h)
         wss[l] = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
     if s.kind == "sparse":
-        wss["idx"] = {l: torch.empty((s.batch, s.topk), dtype=torch.int32,
-                                     device=dev) for l in wl.layers}
+        wss["idx"] = {l: torch.empty((s.batch, s.pool_k if s.pool_k and
+                                      s.modes[l] == "reindex" else s.topk),
+                                     dtype=torch.int32, device=dev)
+                      for l in wl.layers}
         n = K.workspace_size(K.OP_INDEXER_TOPK, wl.idx_cache, wl.block_table,
                              wl.seq_lens, wl.max_seq_len, s.idx_heads, s.topk)
         wss["topk"] = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
+        if s.pool_k:
+            wss["pool"] = torch.empty((s.batch, K.POOL_BLOCKS),
+                                      dtype=torch.int32, device=dev)
+            wss["pool_n"] = torch.empty((s.batch,), dtype=torch.int32,
+                                        device=dev)
+            n = K.workspace_size(K.OP_INDEXER_TOPK_POOL, wl.idx_cache,
+                                 wl.block_table, wl.seq_lens, wl.max_seq_len,
+                                 s.idx_heads, s.pool_k)
+            wss["pooltopk"] = torch.zeros(max(n, 256), dtype=torch.uint8,
+                                          device=dev)
     in_buf = pack_inputs(torch, wl)
     out_buf_views = [outs[l] for l in wl.layers]
 
@@ -515,6 +562,10 @@ def run_ours(args, ws, rank, local):
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
+    if s.kind == "sparse" and s.pool_k:
+        # the pooled Reindex layers' candidates (8 per pool block), for the
+        # byte count; the pool is the same every step
+        s.pool_cands = int(wss["pool_n"].sum().item()) * 8
     t_end = time.perf_counter() + 1.0
     while time.perf_counter() < t_end:
         for _ in range(20):
@@ -682,7 +733,7 @@ def launches(s):
     over several CTAs, so every decode has its merge launch.)"""
     if s.kind == "sparse":
         sel = sum(1 for m in s.modes if m != "reuse")
-        return 2 + 2 * sel + 2 * s.n_layers
+        return 2 + 2 * sel + 2 * s.n_layers + (1 if s.pool_k else 0)
     if s.kind == "mla":
         return 3 * s.n_layers
     return 2 * s.n_layers

@@ -15,6 +15,9 @@ Shapes (cached lengths are BEFORE this step's append):
   sparse            B=8, L=131072, main cache n_kv=1, d=512 (K and V), indexer
                     keys d=64, 4 indexer heads, k=2048, n_h=64, 8 layers:
                     Full, Reuse x3, Reindex x4
+  sparse_pool       the same with the hierarchical indexer: the Full layer's
+                    2048 positions publish their 8-position blocks as a pool
+                    (at most 2,048 blocks), Reindex layers pick 512 inside it
 
 Every tensor is a stream of the SplitMix64 generator in ``inputs`` keyed by
 (20260 + config id, layer, tensor id). Cache values are N(0,1) bf16 (fp8
@@ -64,6 +67,7 @@ class Shape:
     idx_heads: int = 4
     topk: int = 2048
     modes: List[str] = field(default_factory=list)
+    pool_k: Optional[int] = None   # hierarchical indexer: Reindex top-k
 
     @property
     def dv(self):
@@ -107,6 +111,9 @@ def config(name, **over):
     elif name == "sparse":
         s = Shape("sparse", 5, 8, 64, 1, 512, 8, 64, [131072] * 8,
                   kind="sparse", modes=list(SPARSE_MODES))
+    elif name == "sparse_pool":
+        s = Shape("sparse_pool", 7, 8, 64, 1, 512, 8, 64, [131072] * 8,
+                  kind="sparse", modes=list(SPARSE_MODES), pool_k=512)
     else:
         raise KeyError(name)
     for k, v in over.items():
@@ -118,7 +125,8 @@ def config(name, **over):
 
 
 CONFIGS = ["tiny_gqa", "llama2_7b_mha", "llama2_7b_mha_mxfp4",
-           "llama31_70b_gqa", "llama31_70b_gqa_fp8", "mla", "sparse"]
+           "llama31_70b_gqa", "llama31_70b_gqa_fp8", "mla", "sparse",
+           "sparse_pool"]
 
 
 # ---------------------------------------------------------------------------
