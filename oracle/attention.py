@@ -12,7 +12,8 @@ Parity status (each function is pinned in tests/test_oracle_pins.py):
                                   identical keys, weights sum to 1)
   gather_* / kv_append .......... pinned (contiguous vs permuted tables,
                                   byte copy, fp8 encoder pins)
-  gqa_decode .................... pinned (MHA special case, repeat-interleave)
+  gqa_decode .................... pinned (MHA special case, repeat-interleave;
+                                  window = the last W rows, W >= T = full)
   mla_decode .................... pinned (absorbed = explicit decompression)
   indexer_scores ................ pinned (brute-force loops, exact-arithmetic set)
   topk_select / indexer_topk .... pinned (sorted() brute force, ties, k >= T)
@@ -150,8 +151,14 @@ def attend(q, K, V, scale):
 # [POD] on MQA / GQA). Query head h reads KV head h // (n_h / n_kv).
 # ---------------------------------------------------------------------------
 def gqa_decode(q, k_raw, v_raw, block_table, seq_lens, block_size,
-               scale=None, dtype="bf16", k_scale=None, v_scale=None):
+               scale=None, dtype="bf16", k_scale=None, v_scale=None,
+               window=0, window_start=None):
     """One decode step of GQA/MHA attention for every sequence.
+
+    window W > 0 ([890] section 7, SWA bounded replay: a query at position
+    i attends to keys in [max(s, i - W + 1), i]; at decode i = seq_len - 1):
+    sequence b attends to positions [max(s_b, seq_len - W), seq_len), s_b =
+    window_start[b] or 0.
 
     q: [B][n_h][d] float64. k_raw / v_raw: cache storage
     [num_blocks][n_kv][block_size][row] (row = d elements, or an MXFP4 row's
@@ -167,7 +174,11 @@ def gqa_decode(q, k_raw, v_raw, block_table, seq_lens, block_size,
     out = np.zeros((B, n_h, d))
     lse = np.zeros((B, n_h))
     for b in range(B):
-        pos = np.arange(int(seq_lens[b]))
+        T = int(seq_lens[b])
+        lo = 0 if window_start is None else int(window_start[b])
+        if window:
+            lo = max(lo, T - int(window))
+        pos = np.arange(min(max(lo, 0), T), T)
         K = decode_rows(gather_rows(k_raw, block_table[b], pos, block_size),
                         dtype, k_scale, d)
         V = decode_rows(gather_rows(v_raw, block_table[b], pos, block_size),

@@ -827,3 +827,32 @@ def test_schedule_with_pool():
                                          bs, pools, kp)
         assert np.array_equal(sel[layer], want)
         assert sel[layer].shape == (2, kp)
+
+
+# ---------------------------------------------------------------------------
+# sliding window ("890 bytes a token ...", section 7)
+# ---------------------------------------------------------------------------
+def test_window_is_attention_over_the_last_w_positions():
+    rng = np.random.default_rng(80)
+    lens = [1, 7, 40, 130]
+    kr, vr, bt = _random_paged(rng, 4, 2, 8, 8, lens)
+    q = rng.standard_normal((4, 4, 8))
+    W, starts = 16, [0, 3, 30, 2]
+    got, lse = O.gqa_decode(q, kr, vr, bt, lens, 8, window=W,
+                            window_start=starts)
+    for b, T in enumerate(lens):
+        lo = max(starts[b], T - W)
+        K = O.bf16_bits_to_f64(kr[bt[b, np.arange(lo, T) // 8], :,
+                                  np.arange(lo, T) % 8, :])
+        V = O.bf16_bits_to_f64(vr[bt[b, np.arange(lo, T) // 8], :,
+                                  np.arange(lo, T) % 8, :])
+        for h in range(4):
+            kv = h // 2                               # group of 2
+            s = (K[:, kv, :] @ q[b, h]) / math.sqrt(8)
+            wgt = np.exp(s - s.max())
+            ref = (wgt / wgt.sum()) @ V[:, kv, :]
+            np.testing.assert_allclose(got[b, h], ref, atol=1e-12)
+    # a window at least the length is plain decode
+    full, _ = O.gqa_decode(q, kr, vr, bt, lens, 8)
+    w_all, _ = O.gqa_decode(q, kr, vr, bt, lens, 8, window=200)
+    np.testing.assert_allclose(w_all, full, atol=0)
