@@ -57,7 +57,8 @@ def kv_bytes_layer(shape, layer=0):
     indexer keys of Full / Reindex layers plus the selected K and V rows)."""
     s = shape
     if s.kind == "gqa":
-        return sum(s.seq_lens) * s.n_kv * 2 * s.head_dim * s.elem_bytes
+        seen = [min(L, s.window) if s.window else L for L in s.seq_lens]
+        return sum(seen) * s.n_kv * 2 * s.head_dim * s.elem_bytes
     if s.kind == "mla":
         return sum(s.seq_lens) * s.head_dim * 2
     sel = s.batch * min(layer_topk(s, layer), min(s.seq_lens)) * 2 * \
@@ -290,6 +291,9 @@ def oracle_unit_inputs(name, layer, seqs):
             vr = oracle.kv_append(vr, bt, pos, vnew, s.block_size)
     d = dict(kind=s.kind, s=s, q=q, kr=kr, vr=vr, bt=bt, lens=lens,
              seqs=seqs, layer=layer)
+    if s.dtype == "mxfp4":
+        d["kr"] = oracle.kv_append(kr, bt, pos, knew, s.block_size, "mxfp4")
+        d["vr"] = oracle.kv_append(vr, bt, pos, vnew, s.block_size, "mxfp4")
     if s.dtype == "fp8":
         ks, kinv = W.host_scales(s, layer, W.T_KSCALE)
         vs, vinv = W.host_scales(s, layer, W.T_VSCALE)
@@ -307,11 +311,12 @@ def oracle_run_unit(d):
         if s.dtype == "fp8":
             oracle.gqa_decode(d["q"], d["kr"], d["vr"], d["bt"], d["lens"],
                               s.block_size, dtype="fp8", k_scale=d["ks"],
-                              v_scale=d["vs"])
+                              v_scale=d["vs"], window=s.window)
         else:
             oracle.gqa_decode(d["q"], d["kr"], d["vr"], d["bt"], d["lens"],
-                              s.block_size)
-        return sum(d["lens"]) * s.n_kv * 2 * s.head_dim * s.elem_bytes
+                              s.block_size, dtype=s.dtype, window=s.window)
+        seen = [min(L, s.window) if s.window else L for L in d["lens"]]
+        return sum(seen) * s.n_kv * 2 * s.head_dim * s.elem_bytes
     if d["kind"] == "mla":
         oracle.mla_decode(d["q"], d["kr"], d["bt"], d["lens"], s.block_size,
                           d_c=s.d_c)
@@ -415,7 +420,8 @@ def build_step(K, wl, outs, wss):
                                     wl.max_seq_len, wl.pos, wl.k_new[layer],
                                     wl.v_new[layer], wl.q[layer],
                                     out=outs[layer], workspace=wss[layer],
-                                    want_lse=False, seqs_flags=K.SEQS_STABLE)
+                                    want_lse=False, seqs_flags=K.SEQS_STABLE,
+                                    window=s.window)
     return step
 
 
@@ -465,7 +471,7 @@ def decode_only(K, wl, outs, wss, layer):
                             wl.pos, wl.k_new[layer], wl.v_new[layer],
                             wl.q[layer], out=outs[layer],
                             workspace=wss[layer], want_lse=False,
-                            seqs_flags=K.SEQS_STABLE)
+                            seqs_flags=K.SEQS_STABLE, window=s.window)
 
 
 def pack_inputs(torch, wl):

@@ -140,6 +140,17 @@ typedef struct kvd_cache {
  *                 block_size (else KVD_ERR_CAPACITY). A device length above
  *                 it is clamped to it and flagged KVD_DEVERR_LEN.
  *   flags         0, or KVD_SEQS_STABLE (other bits: KVD_ERR_SHAPE)
+ *   window        0 (every visible position), or W > 0: sliding-window
+ *                 decode ("890 bytes a token", section 7, SWA bounded
+ *                 replay, n_win = 128; "KV cache" on local-attention
+ *                 layers): the query of sequence b, at position
+ *                 seq_lens[b] - 1, attends to the positions
+ *                 [max(s_b, seq_lens[b] - W), seq_lens[b]) only
+ *   window_start  device int32 [batch] replay starts s_b, or NULL (s_b = 0);
+ *                 read like seq_lens (KVD_SEQS_STABLE covers it too)
+ * window and window_start are honoured by kvd_gqa_decode,
+ * kvd_gqa_append_decode and kvd_gqa_decode_noalloc; the other calls need
+ * window == 0 and window_start == NULL (else KVD_ERR_UNSUPPORTED).
  *
  * Kernels of this library may start while the kernel before them on the
  * stream is still running (programmatic dependent launch); they read their
@@ -159,6 +170,8 @@ typedef struct kvd_seqs {
   int32_t max_blocks_per_seq;
   int32_t max_seq_len;
   int32_t flags;
+  int32_t window;
+  const int32_t *window_start;
 } kvd_seqs;
 
 typedef enum kvd_op {

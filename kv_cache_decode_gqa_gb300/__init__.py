@@ -105,15 +105,19 @@ class PagedCache:
 SEQS_STABLE = 1  # KVD_SEQS_STABLE
 
 
-def _seqs(block_table, seq_lens, max_seq_len, flags=0):
+def _seqs(block_table, seq_lens, max_seq_len, flags=0, window=0,
+          window_start=None):
     import torch
     _need(block_table, "block_table", torch.int32)
     _need(seq_lens, "seq_lens", torch.int32)
     if block_table.dim() != 2 or block_table.shape[0] != seq_lens.numel():
         raise ValueError("block_table must be [batch][max_blocks_per_seq]")
+    if window_start is not None:
+        _need(window_start, "window_start", torch.int32, seq_lens.numel())
     return _native.KvdSeqs(_ptr(block_table), _ptr(seq_lens),
                            block_table.shape[0], block_table.shape[1],
-                           int(max_seq_len), int(flags))
+                           int(max_seq_len), int(flags), int(window),
+                           _ptr(window_start))
 
 
 def workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k=0):
@@ -166,14 +170,17 @@ def _outputs(q, n_h, dv, out, lse, want_lse):
 
 def gqa_decode(cache, block_table, seq_lens, max_seq_len, q, scale=None,
                out=None, lse=None, workspace=None, want_lse=True,
-               stream=None, seqs_flags=0):
+               stream=None, seqs_flags=0, window=0, window_start=None):
     """GQA/MHA decode: q [batch][n_h][head_dim] bf16 -> (out, lse).
-    seqs_flags: 0 or SEQS_STABLE (see KVD_SEQS_STABLE in kvd.h)."""
+    seqs_flags: 0 or SEQS_STABLE (see KVD_SEQS_STABLE in kvd.h). window W >
+    0: sliding-window decode over positions [max(s_b, len_b - W), len_b),
+    s_b = window_start[b] (int32 device tensor) or 0."""
     import torch
     _need(q, "q", torch.bfloat16)
     n_h = q.shape[1]
     c = cache.struct()
-    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags)
+    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags, window,
+              window_start)
     out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
     ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
                     n_h, 0, workspace)
@@ -186,8 +193,9 @@ def gqa_decode(cache, block_table, seq_lens, max_seq_len, q, scale=None,
 def gqa_append_decode(cache, block_table, seq_lens, max_seq_len, pos, k_new,
                       v_new, q, scale=None, out=None, lse=None,
                       workspace=None, want_lse=True, stream=None,
-                      seqs_flags=0):
-    """kv_append then gqa_decode in one pass (kvd_gqa_append_decode)."""
+                      seqs_flags=0, window=0, window_start=None):
+    """kv_append then gqa_decode in one pass (kvd_gqa_append_decode);
+    window / window_start as for gqa_decode."""
     import torch
     _need(q, "q", torch.bfloat16)
     _need(pos, "pos", torch.int32)
@@ -195,7 +203,8 @@ def gqa_append_decode(cache, block_table, seq_lens, max_seq_len, pos, k_new,
     _need(v_new, "v_new", torch.bfloat16)
     n_h = q.shape[1]
     c = cache.struct()
-    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags)
+    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags, window,
+              window_start)
     out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
     ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
                     n_h, 0, workspace)

@@ -33,7 +33,8 @@ class KvdCache(ctypes.Structure):
 class KvdSeqs(ctypes.Structure):
     _fields_ = [("block_table", c_void_p), ("seq_lens", c_void_p),
                 ("batch", c_int32), ("max_blocks_per_seq", c_int32),
-                ("max_seq_len", c_int32), ("flags", c_int32)]
+                ("max_seq_len", c_int32), ("flags", c_int32),
+                ("window", c_int32), ("window_start", c_void_p)]
 
 
 STATUS = {0: "KVD_OK", 1: "KVD_ERR_NULL", 2: "KVD_ERR_SHAPE",

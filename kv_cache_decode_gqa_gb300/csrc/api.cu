@@ -116,6 +116,15 @@ kvd_status check_cache(const kvd_cache *c, bool need_v, const char *what) {
   return KVD_OK;
 }
 
+// Calls other than the dense GQA decode attend to every position they are
+// given: a sliding window there is refused.
+kvd_status no_window(const kvd_seqs *s, const char *what) {
+  if (s && (s->window != 0 || s->window_start))
+    return fail(KVD_ERR_UNSUPPORTED, "%s: no sliding window (window and "
+                "window_start are for the GQA decode calls)", what);
+  return KVD_OK;
+}
+
 kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
   if (!s) return fail(KVD_ERR_NULL, "%s: seqs is NULL", what);
   if (s->batch < 0 || s->max_blocks_per_seq < 1 || s->max_seq_len < 0)
@@ -129,6 +138,8 @@ kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
                 (unsigned)s->flags);
   if (s->batch > 0 && (!s->block_table || !s->seq_lens))
     return fail(KVD_ERR_NULL, "%s: block_table and seq_lens are required", what);
+  if (s->window < 0)
+    return fail(KVD_ERR_SHAPE, "%s: window must be >= 0", what);
   if ((long)s->max_seq_len > (long)s->max_blocks_per_seq * c->block_size)
     return fail(KVD_ERR_CAPACITY,
                 "%s: max_seq_len %d exceeds the block table's capacity %ld",
@@ -526,6 +537,8 @@ kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
   p.n_splits = pl.n_splits;
   p.hp = pl.hp;
   p.flags = seqs->flags;
+  p.window = seqs->window;
+  p.win_start = seqs->window_start;
   p.pos = pos;
   p.k_new = static_cast<const uint16_t *>(k_new);
   p.v_new = static_cast<const uint16_t *>(v_new);
@@ -570,6 +583,8 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
   kvd_status st = check_cache(latent, false, "mla_decode");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, latent, "mla_decode");
+  if (st != KVD_OK) return st;
+  st = no_window(seqs, "mla_decode");
   if (st != KVD_OK) return st;
   if (latent->dtype != KVD_BF16 || latent->n_kv != 1 || d_c != 512 ||
       latent->head_dim != 576)
@@ -630,6 +645,8 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   kvd_status st = check_cache(cache, true, "sparse_decode");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, cache, "sparse_decode");
+  if (st != KVD_OK) return st;
+  st = no_window(seqs, "sparse_decode");
   if (st != KVD_OK) return st;
   if (cache->dtype != KVD_BF16 || cache->n_kv != 1 || cache->head_dim != 512)
     return fail(KVD_ERR_UNSUPPORTED, "sparse_decode: bf16 cache with n_kv = 1 "
@@ -699,6 +716,8 @@ kvd_status indexer_topk_impl(const kvd_cache *index_cache,
   kvd_status st = check_cache(index_cache, false, "indexer_topk");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, index_cache, "indexer_topk");
+  if (st != KVD_OK) return st;
+  st = no_window(seqs, "indexer_topk");
   if (st != KVD_OK) return st;
   if (index_cache->dtype != KVD_BF16 || index_cache->n_kv != 1 ||
       index_cache->head_dim != 64)
@@ -795,6 +814,8 @@ kvd_status kvd_indexer_pool(const kvd_seqs *seqs, const int32_t *indices,
     return fail(KVD_ERR_SHAPE, "indexer_pool: 0 <= batch <= 65535 and "
                 "max_seq_len >= 0 required");
   if (k < 1) return fail(KVD_ERR_SHAPE, "indexer_pool: k must be >= 1");
+  kvd_status wst = no_window(seqs, "indexer_pool");
+  if (wst != KVD_OK) return wst;
   if ((long)seqs->max_seq_len > 50331648L)
     return fail(KVD_ERR_UNSUPPORTED, "indexer_pool: max_seq_len above "
                 "50,331,648");

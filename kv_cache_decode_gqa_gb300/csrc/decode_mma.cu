@@ -191,13 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npiece = 64 / br;            // <= 4 (block_size >= 16)
     for (int base = 0; base < n; base += 32) {
       const int mine = base + lane;
-      int mb = 0, mh = 0, mk = 0, mrows = 0, mblk[4] = {0, 0, 0, 0};
+      int mb = 0, mh = 0, mk = 0, mrows = 0, mtok = 0, mblk[4] = {0, 0, 0, 0};
       int mpos = -1;  // fused append: the sequence's new slot
       if (mine < n) {
         const ChunkCursor cur = cursor_at(wp, p.batch, lo + mine);
         mb = cur.b, mh = cur.h, mk = cur.k;
         if (p.pos) mpos = p.pos[mb];
-        const int tok = mk * kStageRows;
+        const int tok =
+            seq_first(p, mb, wp.len[mb], kStageRows) + mk * kStageRows;
+        mtok = tok;
         mrows = min(kStageRows, wp.len[mb] - tok);
         const int32_t *bt = p.block_table + (long)mb * p.max_blocks;
         for (int j = 0; j < npiece; ++j) {
@@ -216,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = __shfl_sync(0xffffffffu, mh, j);
         const int k = __shfl_sync(0xffffffffu, mk, j);
         const int rows = __shfl_sync(0xffffffffu, mrows, j);
+        // position of the chunk's first row (looked up with its block ids)
+        const int tok = __shfl_sync(0xffffffffu, mtok, j);
         int blk[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) blk[t] = __shfl_sync(0xffffffffu, mblk[t], j);
@@ -223,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // fused append: before the first chunk holding a new row is
           // copied, wait for the finisher to have written this CTA's rows
           const int P = __shfl_sync(0xffffffffu, mpos, j);
-          const int tok = k * kStageRows;
           if (P >= tok && P < tok + rows) {
             named_sync(kAppendBar, 64);
             appended = true;
@@ -239,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (s_abort) go = 0;
           if (go) {
-            const int tok = k * kStageRows;
             const int pieces = (rows + br - 1) / br;  // only visible blocks
             // the query rows travel only with a unit's first chunk here (the
             // consumers read them when the unit starts)
@@ -441,7 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur_h = cc.h;
       start_unit(s, cur_h);
     }
-    const int nvalid = min(kStageRows, wp.len[cc.b] - cc.k * kStageRows);
+    // rows [nlo, nvalid) of the chunk are attended: below nlo lie positions
+    // before the sliding window (first chunk only; cached rows, masked),
+    // from nvalid on positions past the visible length
+    const bool win = has_window(p);
+    const int ctok =
+        (win ? seq_first(p, cc.b, wp.len[cc.b], kStageRows) : 0) +
+        cc.k * kStageRows;
+    const int nvalid = min(kStageRows, wp.len[cc.b] - ctok);
+    const int nlo = win ? seq_lo(p, cc.b, wp.len[cc.b]) - ctok : 0;
     if (ok) {
       const uint32_t kb = sk0 + s * C::STAGE;
       const uint32_t vb = sv0 + s * C::STAGE;
@@ -505,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int col = wt0 + 16 * u + 8 * t2 + 2 * qc + (j & 1);
-            sc[u][t2][j] = col < nvalid ? sc[u][t2][j] * sl2 : -INFINITY;
+            sc[u][t2][j] =
+                col >= nlo && col < nvalid ? sc[u][t2][j] * sl2 : -INFINITY;
           }
           mx0 = fmaxf(mx0, fmaxf(sc[u][t2][0], sc[u][t2][1]));
           mx1 = fmaxf(mx1, fmaxf(sc[u][t2][2], sc[u][t2][3]));

@@ -283,13 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool appended = false;   // fused append: the finisher's rows are written
     for (int base = 0; base < n; base += 32) {
       const int mine = base + lane;
-      int mb = 0, mh = 0, mk = 0, mrows = 0, mblk[kPre] = {0, 0, 0, 0};
+      int mb = 0, mh = 0, mk = 0, mrows = 0, mtok = 0;
+      int mblk[kPre] = {0, 0, 0, 0};
       int mpos = -1;  // fused append: the sequence's new slot
       if (mine < n) {
         const ChunkCursor cur = cursor_at(wp, p.batch, lo + mine);
         mb = cur.b, mh = cur.h, mk = cur.k;
         if (p.pos) mpos = p.pos[mb];
-        const int tok = mk * kStageRows;
+        const int tok =
+            seq_first(p, mb, wp.len[mb], kStageRows) + mk * kStageRows;
+        mtok = tok;
         mrows = min(kStageRows, wp.len[mb] - tok);
         const int lb0 = tok / p.block_size;
         const int lb1 = (tok + mrows - 1) / p.block_size;
@@ -309,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = __shfl_sync(0xffffffffu, mh, j);
         const int k = __shfl_sync(0xffffffffu, mk, j);
         const int rows = __shfl_sync(0xffffffffu, mrows, j);
+        // position of the chunk's first row (looked up with its block ids)
+        const int tok = __shfl_sync(0xffffffffu, mtok, j);
         int blk[kPre];
 #pragma unroll
         for (int t = 0; t < kPre; ++t)
@@ -317,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // fused append: before the first chunk holding a new row is
           // copied, wait for the finisher to have written this CTA's rows
           const int P = __shfl_sync(0xffffffffu, mpos, j);
-          const int tok = k * kStageRows;
           if (P >= tok && P < tok + rows) {
             named_sync(kAppendBar, 64);
             appended = true;
@@ -333,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (s_abort) go = 0;
           if (go) {
-            const int tok = k * kStageRows;
             // the query rows travel only with a unit's first chunk here (the
             // consumers read them when the unit starts)
             const bool qrows = i == 0 || k == 0;
@@ -541,7 +544,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur_h = cc.h;
       start_unit(s, cur_h);
     }
-    const int nvalid = min(kStageRows, wp.len[cc.b] - cc.k * kStageRows);
+    // rows [nlo, nvalid) of the chunk are attended: below nlo lie positions
+    // before the sliding window (first chunk only), from nvalid on
+    // positions past the visible length
+    const bool win = has_window(p);
+    const int ctok =
+        (win ? seq_first(p, cc.b, wp.len[cc.b], kStageRows) : 0) +
+        cc.k * kStageRows;
+    const int nvalid = min(kStageRows, wp.len[cc.b] - ctok);
+    const int nlo = win ? seq_lo(p, cc.b, wp.len[cc.b]) - ctok : 0;
     if (ok) {
       const uint8_t *kst = sk + s * C::STAGE + hj * C::HSTAGE;
       const uint8_t *vst = sv + s * C::STAGE + hj * C::HSTAGE;
@@ -572,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v += __shfl_xor_sync(0xffffffffu, v, 4);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
           v += __shfl_xor_sync(0xffffffffu, v, 1);
-          sc[i2][g] = r < nvalid ? v : -INFINITY;
+          sc[i2][g] = r >= nlo && r < nvalid ? v : -INFINITY;
         }
       }
       float pr[C::ITER][G];
@@ -598,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i2 = 0; i2 < C::ITER; ++i2) {
         const int r = lw * 4 * C::ITER + i2 * 4 + grp;
-        if (r < nvalid) {
+        if (r >= nlo && r < nvalid) {
           float vx[E];
           load_row<D, DT>(vst + r * C::ROW, sub, vx);
           const float vsr = row_scale<D, DT>(vst + r * C::ROW, sub);

@@ -64,6 +64,11 @@ struct DecodeParams {
   int32_t n_splits;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
   int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE)
+  // sliding window (dense GQA only): sequence b attends to positions
+  // [max(win_start[b], len_b - window), len_b); window 0 and no starts:
+  // every visible position
+  int32_t window;
+  const int32_t *win_start;
   // fused append (kvd_gqa_append_decode), else pos == nullptr: the new key
   // and value rows, bf16 [batch][n_kv][dk], written at slot pos[b]
   const int32_t *pos;

@@ -29,11 +29,34 @@ struct WorkPartitionT {
 };
 using WorkPartition = WorkPartitionT<kMaxDecodeBatch>;
 
+// First position sequence b attends to (its visible length is T): the
+// sliding window's and the replay start's lower bound, 0 without them.
+__device__ __forceinline__ int seq_lo(const DecodeParams &p, int b, int T) {
+  int lo = p.win_start ? p.win_start[b] : 0;
+  if (p.window > 0) lo = max(lo, T - p.window);
+  return min(max(lo, 0), T);
+}
+
+// Position of the first row of sequence b's first chunk: its first
+// attended position rounded down to the chunk size (rows below `lo` in
+// that chunk are copied and masked).
+__device__ __forceinline__ int seq_first(const DecodeParams &p, int b, int T,
+                                         int chunk) {
+  const int lo = seq_lo(p, b, T);
+  return lo - lo % chunk;
+}
+
+// Whether any sequence of the call has a lower bound (window or start).
+__device__ __forceinline__ bool has_window(const DecodeParams &p) {
+  return p.window > 0 || p.win_start != nullptr;
+}
+
 // Fill `wp` (shared memory) from the device sequence lengths. Sequence b
 // has `units` units of ceil(rows_b / chunk) chunks, rows_b = its visible
-// length, or `fixed_rows` (a position list's length) when that is > 0 and
-// the sequence is not empty. Every thread of the block calls it (blockDim.x
-// a multiple of 32); it ends with a barrier.
+// length from its first chunk's start (seq_first; 0 when nothing is
+// attended), or `fixed_rows` (a position list's length) when that is > 0
+// and the sequence is not empty. Every thread of the block calls it
+// (blockDim.x a multiple of 32); it ends with a barrier.
 template <int NB>
 __device__ __forceinline__ void build_partition(WorkPartitionT<NB> &wp,
                                                 const DecodeParams &p,
@@ -52,7 +75,10 @@ __device__ __forceinline__ void build_partition(WorkPartitionT<NB> &wp,
     }
     T = max(T, 0);
     wp.len[b] = T;
-    const int rows = (fixed_rows > 0 && T > 0) ? fixed_rows : T;
+    const int lo = seq_lo(p, b, T);
+    const int rows = (fixed_rows > 0 && T > 0)
+                         ? fixed_rows
+                         : (lo < T ? T - (lo - lo % chunk) : 0);
     wp.nch[b] = (rows + chunk - 1) / chunk;
   }
   if (tid == 0) wp.units = units;
@@ -233,8 +259,10 @@ __device__ __forceinline__ void append_range_rows(
     int P = -1, pb = -1;
     if (mb >= 0) {
       P = p.pos[mb];
-      const int xp = mstart + P / kStageRows;  // the chunk holding P
-      if (P >= 0 && P < wp.len[mb] && xp >= lo && xp < hi)
+      const int first = seq_first(p, mb, wp.len[mb], kStageRows);
+      const int xp = mstart + (P - first) / kStageRows;  // chunk holding P
+      if (P >= first && P < wp.len[mb] && wp.nch[mb] > 0 && xp >= lo &&
+          xp < hi)
         pb = p.block_table[(long)mb * p.max_blocks + P / p.block_size];
     }
     if (!waited) {
@@ -265,7 +293,8 @@ __device__ __forceinline__ void append_unread_rows(
     int P = 0, need = 0;
     if (b < p.batch) {
       P = p.pos[b];
-      need = !(P >= 0 && P < wp.len[b]);
+      const int first = seq_first(p, b, wp.len[b], kStageRows);
+      need = !(P >= first && P < wp.len[b] && wp.nch[b] > 0);
     }
     unsigned todo = __ballot_sync(0xffffffffu, need);
     while (todo) {

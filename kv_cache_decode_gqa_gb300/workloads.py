@@ -11,6 +11,8 @@ Shapes (cached lengths are BEFORE this step's append):
                     scale per (layer, kv head) for K and for V
   llama2_7b_mha_mxfp4  the Llama-2 shape over an MXFP4 cache (E2M1 codes, an
                     E4M3 scale per 16 channels: 72 bytes per row)
+  llama31_70b_gqa_fp8_swa  the Llama-3.1 fp8 shape as sliding-window layers:
+                    each query attends to the last 128 positions
   mla               B=64, n_h=128, latent 512 + rope 64, L=32768, 1 layer
   sparse            B=8, L=131072, main cache n_kv=1, d=512 (K and V), indexer
                     keys d=64, 4 indexer heads, k=2048, n_h=64, 8 layers:
@@ -68,6 +70,7 @@ class Shape:
     topk: int = 2048
     modes: List[str] = field(default_factory=list)
     pool_k: Optional[int] = None   # hierarchical indexer: Reindex top-k
+    window: int = 0                # sliding window (0: every position)
 
     @property
     def dv(self):
@@ -101,11 +104,13 @@ def config(name, **over):
         s = Shape("llama2_7b_mha", 2, 1, 32, 32, 128, 32, 64, [4096])
     elif name == "llama2_7b_mha_mxfp4":
         s = Shape(name, 6, 1, 32, 32, 128, 32, 64, [4096], dtype="mxfp4")
-    elif name in ("llama31_70b_gqa", "llama31_70b_gqa_fp8"):
+    elif name in ("llama31_70b_gqa", "llama31_70b_gqa_fp8",
+                  "llama31_70b_gqa_fp8_swa"):
         lens = I.uniform_int(I.stream_key(SEED_BASE + 3, 0, T_LEN), 32, 1024,
                              8192).tolist()
         s = Shape(name, 3, 32, 64, 8, 128, 80, 64, lens,
-                  dtype="fp8" if name.endswith("fp8") else "bf16")
+                  dtype="bf16" if name == "llama31_70b_gqa" else "fp8",
+                  window=128 if name.endswith("swa") else 0)
     elif name == "mla":
         s = Shape("mla", 4, 64, 128, 1, 576, 1, 64, [32768] * 64, kind="mla")
     elif name == "sparse":
@@ -125,8 +130,8 @@ def config(name, **over):
 
 
 CONFIGS = ["tiny_gqa", "llama2_7b_mha", "llama2_7b_mha_mxfp4",
-           "llama31_70b_gqa", "llama31_70b_gqa_fp8", "mla", "sparse",
-           "sparse_pool"]
+           "llama31_70b_gqa", "llama31_70b_gqa_fp8", "llama31_70b_gqa_fp8_swa",
+           "mla", "sparse", "sparse_pool"]
 
 
 # ---------------------------------------------------------------------------

@@ -55,7 +55,8 @@ def host_scales(shape, layer):
     return ks, kinv, vs, vinv
 
 
-def oracle_dense_step(shape, paging, layer, seqs=None):
+def oracle_dense_step(shape, paging, layer, seqs=None, window=0,
+                      window_start=None):
     """Oracle output of one append + decode step of a GQA / MLA workload
     layer, for all sequences (small shapes) or the sampled ``seqs``.
     Returns (out [n][n_h][dv], lse [n][n_h], appended caches)."""
@@ -76,18 +77,22 @@ def oracle_dense_step(shape, paging, layer, seqs=None):
     pos = [s.lengths[b] for b in all_seqs]
     lens = [s.seq_lens[b] for b in all_seqs]
     kn, vn = knew[all_seqs], vnew[all_seqs]
+    ws_sel = (None if window_start is None
+              else [int(window_start[b]) for b in all_seqs])
     if s.dtype == "mxfp4":
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size, "mxfp4")
         vr = oracle.kv_append(vr, bt, pos, vn, s.block_size, "mxfp4")
         out, lse = oracle.gqa_decode(q[all_seqs], kr, vr, bt, lens,
-                                     s.block_size, dtype="mxfp4")
+                                     s.block_size, dtype="mxfp4",
+                                     window=window, window_start=ws_sel)
     elif s.dtype == "fp8":
         ks, kinv, vs, vinv = host_scales(s, layer)
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size, "fp8", kinv)
         vr = oracle.kv_append(vr, bt, pos, vn, s.block_size, "fp8", vinv)
         out, lse = oracle.gqa_decode(q[all_seqs], kr, vr, bt, lens,
                                      s.block_size, dtype="fp8", k_scale=ks,
-                                     v_scale=vs)
+                                     v_scale=vs, window=window,
+                                     window_start=ws_sel)
     elif s.kind == "mla":
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size)
         out, lse = oracle.mla_decode(q[all_seqs], kr, bt, lens, s.block_size,
@@ -96,11 +101,13 @@ def oracle_dense_step(shape, paging, layer, seqs=None):
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size)
         vr = oracle.kv_append(vr, bt, pos, vn, s.block_size)
         out, lse = oracle.gqa_decode(q[all_seqs], kr, vr, bt, lens,
-                                     s.block_size)
+                                     s.block_size, window=window,
+                                     window_start=ws_sel)
     return out, lse, (kr, vr)
 
 
-def device_step(wl, layer, lse=True, seqs_flags=0, fused=False):
+def device_step(wl, layer, lse=True, seqs_flags=0, fused=False, window=0,
+                window_start=None):
     """kv_append then the layer's decode through the C ABI (or, fused, the
     single kvd_gqa_append_decode call)."""
     import kv_cache_decode_gqa_gb300 as K
@@ -110,11 +117,13 @@ def device_step(wl, layer, lse=True, seqs_flags=0, fused=False):
         return K.gqa_append_decode(c, wl.block_table, wl.seq_lens,
                                    wl.max_seq_len, wl.pos, wl.k_new[layer],
                                    wl.v_new[layer], wl.q[layer], want_lse=lse,
-                                   seqs_flags=seqs_flags)
+                                   seqs_flags=seqs_flags, window=window,
+                                   window_start=window_start)
     K.kv_append(c, wl.block_table, wl.pos, wl.k_new[layer],
                 wl.v_new.get(layer))
     if s.kind == "mla":
         return K.mla_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
                             wl.q[layer], d_c=s.d_c, want_lse=lse)
     return K.gqa_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                        wl.q[layer], want_lse=lse, seqs_flags=seqs_flags)
+                        wl.q[layer], want_lse=lse, seqs_flags=seqs_flags,
+                        window=window, window_start=window_start)

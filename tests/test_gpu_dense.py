@@ -385,3 +385,58 @@ def test_llama31_70b_full_size_sampled(name, fused):
     ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0, seqs=seqs)
     H.assert_close(H.to_np_bf16(out)[seqs], ref, name)
     H.assert_lse_close(lse.cpu().numpy()[seqs], ref_lse, name)
+
+
+# ---------------------------------------------------------------------------
+# sliding window ("890 bytes a token ...", section 7: n_win = 128)
+# ---------------------------------------------------------------------------
+WINDOW_CASES = [c for c in DENSE_CASES if c[0] in
+                ("mha_d128", "gqa2_d128", "gqa4_d64", "gqa8_bs64",
+                 "gqa16_bs16", "gqa2_d128_bs64")]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[c[0] for c in
+                                                    WINDOW_CASES])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("window,starts,fused", [
+    (128, False, False), (100, True, True), (1, False, True)],
+    ids=["w128", "w100_starts_fused", "w1_fused"])
+def test_window_decode(case, dtype, window, starts, fused):
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=d)
+    wl = W.DeviceWorkload(s, layers=[0])
+    st = None
+    if starts:   # replay starts: none, inside the window, past it
+        st_host = [(L // 3) if i % 2 else max(0, L - 20)
+                   for i, L in enumerate(s.seq_lens)]
+        st = torch.tensor(st_host, dtype=torch.int32, device="cuda")
+    out, lse = H.device_step(wl, 0, fused=fused, window=window,
+                             window_start=st)
+    torch.cuda.synchronize()
+    ref, ref_lse, (kr, vr) = H.oracle_dense_step(
+        s, wl.paging, 0, window=window,
+        window_start=None if st is None else st.cpu().numpy())
+    if fused:
+        c = wl.caches[0]
+        assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr)), name
+        assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr)), name
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}/w{window}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/w{window}")
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_window_full_size_fp8(fused):
+    """The pages' sliding-window cache: fp8, n_win = 128, on the
+    Llama-3.1-70B shape."""
+    s = W.config("llama31_70b_gqa_fp8")
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0, fused=fused, window=128,
+                             seqs_flags=K.SEQS_STABLE if fused else 0)
+    torch.cuda.synchronize()
+    seqs = [0, int(np.argmax(s.lengths)), 31]
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0, seqs=seqs,
+                                          window=128)
+    H.assert_close(H.to_np_bf16(out)[seqs], ref, "window full size")
+    H.assert_lse_close(lse.cpu().numpy()[seqs], ref_lse, "window full size")
