@@ -25,7 +25,10 @@ from .attention import (attend, attend_scores, decode_rows, gather_positions, ga
                         sparse_schedule, POOL_BLOCK, POOL_CAP, indexer_pool,
                         pool_positions, indexer_topk_in_pool)
 
+from .allocator import CowPool, blocks_for_lengths
+
 __all__ = [
+    "CowPool", "blocks_for_lengths",
     "bf16_bits_to_f64", "e4m3_value_table", "e4m3_codes_to_f64",
     "e4m3_encode_f32", "e2m1_value_table", "e2m1_codes_to_f64",
     "e2m1_encode_f32", "mxfp4_row_bytes", "mxfp4_encode_rows",

@@ -856,3 +856,82 @@ def test_window_is_attention_over_the_last_w_positions():
     full, _ = O.gqa_decode(q, kr, vr, bt, lens, 8)
     w_all, _ = O.gqa_decode(q, kr, vr, bt, lens, 8, window=200)
     np.testing.assert_allclose(w_all, full, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# copy-on-write prefix sharing ("KV cache", "The allocator, not the
+# algorithm")
+# ---------------------------------------------------------------------------
+def test_cow_fork_shares_and_append_copies_once():
+    pool = O.CowPool(10)
+    a = pool.new_sequence("a", 3, payload=["a0", "a1", "a2"])
+    assert a == [0, 1, 2] and pool.free_blocks() == list(range(3, 10))
+    pool.fork("a", "b")                          # a prefix shared, no copy
+    assert [pool.refcount(x) for x in a] == [2, 2, 2]
+    assert pool.blocks_used() == 3
+    # b appends into its last block (slot 2 * 16 + 5): one copy, to block 3
+    cp = pool.prepare_append("b", 2 * 16 + 5, 16)
+    assert cp == (2, 3)
+    assert pool.tables["a"] == [0, 1, 2] and pool.tables["b"] == [0, 1, 3]
+    assert pool.data[3] == "a2" and pool.data[2] == "a2"   # a's view kept
+    assert pool.refcount(2) == 1 and pool.refcount(3) == 1
+    # the same append again: the block is private now
+    assert pool.prepare_append("b", 2 * 16 + 6, 16) is None
+    # a new block past the table: fresh, nothing to copy
+    assert pool.prepare_append("a", 3 * 16, 16) is None
+    assert pool.tables["a"][3] == 4
+    pool.drop("a")
+    assert pool.refcount(2) == 0 and 2 in pool.free_blocks()
+    assert pool.refcount(0) == 1                 # still held by b
+
+
+def test_cow_refcounts_are_table_counts():
+    rng = np.random.default_rng(90)
+    pool = O.CowPool(64)
+    names = []
+    for step in range(200):
+        op = rng.integers(4)
+        if op == 0 or not names:
+            n = f"s{step}"
+            try:
+                pool.new_sequence(n, int(rng.integers(1, 4)))
+                names.append(n)
+            except MemoryError:
+                pass
+        elif op == 1:
+            n = f"f{step}"
+            pool.fork(names[rng.integers(len(names))], n)
+            names.append(n)
+        elif op == 2:
+            n = names[rng.integers(len(names))]
+            try:
+                pool.prepare_append(n, int(rng.integers(0, 6 * 8)), 8)
+            except MemoryError:
+                pass
+        else:
+            pool.drop(names.pop(rng.integers(len(names))))
+        counts = {}
+        for t in pool.tables.values():
+            for b in t:
+                if b >= 0:
+                    counts[b] = counts.get(b, 0) + 1
+        for b in range(64):
+            assert pool.refcount(b) == counts.get(b, 0)
+        assert len(pool.free_blocks()) == 64 - len(counts)
+
+
+def test_cow_unshared_blocks_meet_the_waste_bound(golden_dir):
+    g = _load(golden_dir, "page_figures.json")["paged_waste"]
+    bs, Lbar = g["block_size"], g["mean_len"]
+    rng = np.random.default_rng(91)
+    lens = rng.integers(1, 2 * Lbar, 64)
+    pool = O.CowPool(int(sum(lens)) // bs + 200)
+    for i, L in enumerate(lens):                 # append token by token
+        pool.tables[f"s{i}"] = []
+        for p in range(int(L)):
+            pool.prepare_append(f"s{i}", p, bs)
+    used = pool.blocks_used()
+    assert used == O.blocks_for_lengths(lens, bs)
+    waste = used * bs - int(sum(lens))
+    assert waste == int(O.paged_waste_slots(lens, bs).sum())
+    assert waste <= len(lens) * (bs - 1)
