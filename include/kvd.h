@@ -406,6 +406,55 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                              kvd_stream stream);
 
 /*
+ * Copy-on-write block pool ("KV cache", "The allocator, not the
+ * algorithm": block tables of sequences with a common prefix point at the
+ * same physical blocks, copied when they diverge; each sequence wastes at
+ * most block_size - 1 slots of its last block). A host object: reference
+ * counts of num_blocks physical block ids and their free list (the lowest
+ * free id is handed out first). Thread-safe; block tables and id arrays
+ * passed to it are HOST memory. Errors: KVD_ERR_NULL, KVD_ERR_SHAPE (bad
+ * ids, over-release), KVD_ERR_CAPACITY (pool exhausted); a failing call
+ * changes nothing.
+ */
+typedef struct kvd_block_pool kvd_block_pool;
+
+kvd_status kvd_block_pool_create(int32_t num_blocks, kvd_block_pool **out);
+void kvd_block_pool_destroy(kvd_block_pool *pool);
+/* free blocks, or -1 for a NULL pool */
+int32_t kvd_block_pool_free_count(kvd_block_pool *pool);
+/* references held on a block (0 = free), or -1 for a bad id */
+int32_t kvd_block_pool_refcount(kvd_block_pool *pool, int32_t block);
+/* n fresh blocks (reference count 1) into blocks[0..n) */
+kvd_status kvd_block_pool_alloc(kvd_block_pool *pool, int32_t n,
+                                int32_t *blocks);
+/* one more reference on each held block (a fork sharing a prefix); ids < 0
+ * are skipped */
+kvd_status kvd_block_pool_share(kvd_block_pool *pool, const int32_t *blocks,
+                                int32_t n);
+/* one reference fewer on each block; a block reaching 0 is free again */
+kvd_status kvd_block_pool_release(kvd_block_pool *pool, const int32_t *blocks,
+                                  int32_t n);
+/*
+ * Before appending at slot pos[b] of each sequence: a table entry that is
+ * -1 gets a fresh block; one that names a block with other references gets
+ * a fresh block too, and the pair (old, fresh) goes to src / dst
+ * [*n_copies] so that kvd_copy_blocks can copy the shared rows first (the
+ * table drops its reference on the old block). block_table is HOST int32
+ * [batch][max_blocks], updated in place; src and dst hold up to batch ids.
+ */
+kvd_status kvd_block_pool_prepare_append(kvd_block_pool *pool,
+                                         int32_t *block_table, int32_t batch,
+                                         int32_t max_blocks,
+                                         const int32_t *pos,
+                                         int32_t block_size, int32_t *src,
+                                         int32_t *dst, int32_t *n_copies);
+/* device: whole blocks dst[i] := src[i] of K and V (every kv head's rows),
+ * src / dst DEVICE int32 [n]; an id outside [0, num_blocks) skips that copy
+ * and sets KVD_DEVERR_BLOCK */
+kvd_status kvd_copy_blocks(const kvd_cache *cache, const int32_t *src,
+                           const int32_t *dst, int32_t n, kvd_stream stream);
+
+/*
  * kvd_workspace_size -- bytes of workspace the call `op` needs for these
  * shapes on the current device (the split plan depends on its SM count).
  * `n_h` is the query head count (indexer heads for KVD_OP_INDEXER_TOPK) and

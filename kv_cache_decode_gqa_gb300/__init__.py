@@ -20,6 +20,7 @@ from ._native import KvdError, check, lib
 
 __all__ = ["PagedCache", "kv_append", "gqa_decode", "mla_decode",
            "indexer_topk", "indexer_pool", "indexer_topk_pool",
+           "BlockPool", "copy_blocks",
            "sparse_decode", "workspace_size",
            "bytes_per_token", "device_error", "KvdError",
            "OP_GQA_DECODE", "OP_MLA_DECODE", "OP_INDEXER_TOPK",
@@ -330,6 +331,82 @@ def sparse_decode(cache, block_table, seq_lens, max_seq_len, indices, q,
                                   float(scale or 0.0), _ptr(out), _ptr(lse),
                                   _ptr(ws), ws.numel(), _stream(stream)))
     return out, lse
+
+
+class BlockPool:
+    """The library's copy-on-write block pool (kvd_block_pool_*): host
+    reference counts of num_blocks physical blocks. Block tables and id
+    lists are host numpy int32 arrays."""
+
+    def __init__(self, num_blocks):
+        h = ctypes.c_void_p()
+        check(lib().kvd_block_pool_create(int(num_blocks), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().kvd_block_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _ids(blocks):
+        import numpy as np
+        a = np.ascontiguousarray(blocks, dtype=np.int32)
+        return a, a.ctypes.data
+
+    def free_count(self):
+        return int(lib().kvd_block_pool_free_count(self._h))
+
+    def refcount(self, block):
+        return int(lib().kvd_block_pool_refcount(self._h, int(block)))
+
+    def alloc(self, n):
+        import numpy as np
+        out = np.empty(int(n), dtype=np.int32)
+        check(lib().kvd_block_pool_alloc(self._h, int(n), out.ctypes.data))
+        return out
+
+    def share(self, blocks):
+        a, p = self._ids(blocks)
+        check(lib().kvd_block_pool_share(self._h, p, a.size))
+
+    def release(self, blocks):
+        a, p = self._ids(blocks)
+        check(lib().kvd_block_pool_release(self._h, p, a.size))
+
+    def prepare_append(self, block_table, pos, block_size):
+        """block_table: host int32 [batch][max_blocks], updated in place;
+        pos: host int32 [batch]. Returns (src, dst) block ids of the copies
+        to make before appending."""
+        import numpy as np
+        assert block_table.dtype == np.int32 and block_table.flags.c_contiguous
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        B, M = block_table.shape
+        src = np.empty(max(B, 1), dtype=np.int32)
+        dst = np.empty(max(B, 1), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        check(lib().kvd_block_pool_prepare_append(
+            self._h, block_table.ctypes.data, B, M, pos.ctypes.data,
+            int(block_size), src.ctypes.data, dst.ctypes.data,
+            ctypes.byref(n)))
+        return src[:n.value].copy(), dst[:n.value].copy()
+
+
+def copy_blocks(cache, src, dst, stream=None):
+    """Whole blocks dst[i] := src[i] of the cache's K and V (device int32
+    tensors)."""
+    import torch
+    _need(src, "src", torch.int32)
+    _need(dst, "dst", torch.int32, src.numel())
+    c = cache.struct()
+    check(lib().kvd_copy_blocks(ctypes.byref(c), _ptr(src), _ptr(dst),
+                                src.numel(), _stream(stream)))
 
 
 def bytes_per_token(n_l, n_kv, d_h, elem_bytes):

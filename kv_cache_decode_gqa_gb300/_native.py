@@ -77,6 +77,19 @@ _SIGS = {
     "kvd_sparse_decode": (c_int32, [_PCACHE, _PSEQS, c_void_p, c_int32,
                                     c_void_p, c_int32, c_float, c_void_p,
                                     c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kvd_block_pool_create": (c_int32, [c_int32, ctypes.POINTER(c_void_p)]),
+    "kvd_block_pool_destroy": (None, [c_void_p]),
+    "kvd_block_pool_free_count": (c_int32, [c_void_p]),
+    "kvd_block_pool_refcount": (c_int32, [c_void_p, c_int32]),
+    "kvd_block_pool_alloc": (c_int32, [c_void_p, c_int32, c_void_p]),
+    "kvd_block_pool_share": (c_int32, [c_void_p, c_void_p, c_int32]),
+    "kvd_block_pool_release": (c_int32, [c_void_p, c_void_p, c_int32]),
+    "kvd_block_pool_prepare_append": (c_int32, [c_void_p, c_void_p, c_int32,
+                                                c_int32, c_void_p, c_int32,
+                                                c_void_p, c_void_p,
+                                                ctypes.POINTER(c_int32)]),
+    "kvd_copy_blocks": (c_int32, [_PCACHE, c_void_p, c_void_p, c_int32,
+                                  c_void_p]),
     "kvd_workspace_size": (c_int32, [c_int32, _PCACHE, _PSEQS, c_int32,
                                      c_int32, ctypes.POINTER(c_size_t)]),
 }

@@ -325,6 +325,14 @@ kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
   return KVD_OK;
 }
 
+kvd_status device_error_word(int **err) {
+  const DeviceInfo *d = nullptr;
+  const kvd_status st = device_info(&d);
+  if (st != KVD_OK) return st;
+  *err = d->err;
+  return KVD_OK;
+}
+
 kvd_status set_error(kvd_status st, const char *msg) {
   return fail(st, "%s", msg);
 }

@@ -157,6 +157,9 @@ kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
                                 size_t *counters_bytes);
 // Record `msg` as this host thread's last error and return `st` (api.cu).
 kvd_status set_error(kvd_status st, const char *msg);
+// The current device's error word (KVD_DEVERR_* bits), for kernels that
+// flag bad inputs.
+kvd_status device_error_word(int **err);
 
 // Split plans (shared by workspace sizing and the calls).
 constexpr int kStageRows = 64;  // tokens per pipeline stage (dense paths)
