@@ -506,6 +506,29 @@ def pack_inputs(torch, wl):
     return buf
 
 
+def sparse_buffers(torch, K, wl, dev):
+    """Index tensors of every layer and the selection workspaces of the
+    sparse schedule (and the hierarchical indexer's pool)."""
+    s = wl.shape
+    b = {"idx": {l: torch.empty((s.batch, s.pool_k if s.pool_k and
+                                 s.modes[l] == "reindex" else s.topk),
+                                dtype=torch.int32, device=dev)
+                 for l in wl.layers}}
+    n = K.workspace_size(K.OP_INDEXER_TOPK, wl.idx_cache, wl.block_table,
+                         wl.seq_lens, wl.max_seq_len, s.idx_heads, s.topk)
+    b["topk"] = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
+    if s.pool_k:
+        b["pool"] = torch.empty((s.batch, K.POOL_BLOCKS), dtype=torch.int32,
+                                device=dev)
+        b["pool_n"] = torch.empty((s.batch,), dtype=torch.int32, device=dev)
+        n = K.workspace_size(K.OP_INDEXER_TOPK_POOL, wl.idx_cache,
+                             wl.block_table, wl.seq_lens, wl.max_seq_len,
+                             s.idx_heads, s.pool_k)
+        b["pooltopk"] = torch.zeros(max(n, 256), dtype=torch.uint8,
+                                    device=dev)
+    return b
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import kv_cache_decode_gqa_gb300 as K
@@ -531,23 +554,7 @@ def run_ours(args, ws, rank, local):
                                  wl.seq_lens, wl.max_seq_len, s.n_h)
         wss[l] = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
     if s.kind == "sparse":
-        wss["idx"] = {l: torch.empty((s.batch, s.pool_k if s.pool_k and
-                                      s.modes[l] == "reindex" else s.topk),
-                                     dtype=torch.int32, device=dev)
-                      for l in wl.layers}
-        n = K.workspace_size(K.OP_INDEXER_TOPK, wl.idx_cache, wl.block_table,
-                             wl.seq_lens, wl.max_seq_len, s.idx_heads, s.topk)
-        wss["topk"] = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
-        if s.pool_k:
-            wss["pool"] = torch.empty((s.batch, K.POOL_BLOCKS),
-                                      dtype=torch.int32, device=dev)
-            wss["pool_n"] = torch.empty((s.batch,), dtype=torch.int32,
-                                        device=dev)
-            n = K.workspace_size(K.OP_INDEXER_TOPK_POOL, wl.idx_cache,
-                                 wl.block_table, wl.seq_lens, wl.max_seq_len,
-                                 s.idx_heads, s.pool_k)
-            wss["pooltopk"] = torch.zeros(max(n, 256), dtype=torch.uint8,
-                                          device=dev)
+        wss.update(sparse_buffers(torch, K, wl, dev))
     in_buf = pack_inputs(torch, wl)
     out_buf_views = [outs[l] for l in wl.layers]
 
@@ -720,9 +727,7 @@ def profile_run(args, local):
                            device=dev) for l in wl.layers}
     wss = {l: None for l in wl.layers}
     if s.kind == "sparse":
-        wss["idx"] = {l: torch.empty((s.batch, s.topk), dtype=torch.int32,
-                                     device=dev) for l in wl.layers}
-        wss["topk"] = None
+        wss.update(sparse_buffers(torch, K, wl, dev))
     step = build_step(K, wl, outs, wss)
     for _ in range(args.warmup + args.steps):
         step()
