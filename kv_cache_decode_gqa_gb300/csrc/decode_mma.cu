@@ -39,6 +39,7 @@ namespace kvd {
 namespace {
 
 constexpr int kAppendBar = 1;  // finisher -> producer: fused-append rows written
+constexpr int kFinalBar = 2;   // the consumer warps, at the end
 
 constexpr int kD = 128;
 constexpr int kWarps = 4;                 // consumer warps
@@ -178,6 +179,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  // Write flush slot `sl`, which holds every consumer warp's state of unit
+  // (b, h), as the unit's output (a unit wholly in this CTA's range) or as
+  // this CTA's partial of it, with threads t = 0 .. nt - 1 (whole warps).
+  // Lane jg (a query head of the unit) of every warp combines the states of
+  // its kv head's WPH warps once: M = max m_w, L = sum l_w 2^(m_w - M); the
+  // output row is sum_w c_w o_w with c_w = 2^(m_w - M) vs / L, written by
+  // warps in turn, four columns a lane.
+  auto write_unit = [&](int b, int h, int sl, int t, int nt) {
+    const int ustart = wp.pre[b] + h * wp.nch[b];
+    const int uend = ustart + wp.nch[b];
+    const float *wm = slots + sl * C::SLOT;  // [warp][16]
+    const float *wl = wm + kWarps * 16;      // [warp][16]
+    const float *wo = wl + kWarps * 16;      // [warp][16][D]
+    const bool whole = ustart >= lo && uend <= hi;
+    const int wslot = c * 2 + partial_side(ustart, lo);
+    const long bh0 = (long)b * p.n_h + h * GU;
+    const int ln = t & 31, wq = t >> 5, nw = nt >> 5;
+    float cw[C::WPH];
+    {
+      const int jg = ln < GU ? ln : 0;
+      const int j = jg / G, g = jg % G, w0 = j * C::WPH;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, wm[(w0 + w) * 16 + g]);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) {
+        const float mw = wm[(w0 + w) * 16 + g];
+        cw[w] = mw == -INFINITY ? 0.f : ex2(mw - M);
+        L = fmaf(wl[(w0 + w) * 16 + g], cw[w], L);
+      }
+      const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
+      const float f = L > 0.f ? vs / L : 0.f;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) cw[w] *= f;
+      const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
+      if (wq == 0 && ln < GU) {
+        if (!whole)
+          p.ws_lse[(long)wslot * GU + jg] = lse_nat;
+        else if (p.lse)
+          p.lse[bh0 + jg] = lse_nat;
+      }
+    }
+    for (int jg = wq; jg < GU; jg += nw) {
+      const int w0 = (jg / G) * C::WPH, g = jg % G;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) {
+        const float cf = __shfl_sync(0xffffffffu, cw[w], jg);
+        const float4 v =
+            reinterpret_cast<const float4 *>(wo + ((w0 + w) * 16 + g) * kD)[ln];
+        acc.x = fmaf(cf, v.x, acc.x);
+        acc.y = fmaf(cf, v.y, acc.y);
+        acc.z = fmaf(cf, v.z, acc.z);
+        acc.w = fmaf(cf, v.w, acc.w);
+      }
+      if (whole) {
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(p.out + (bh0 + jg) * kD)[ln] = packed;
+      } else {
+        reinterpret_cast<float4 *>(p.ws_o + ((long)wslot * GU + jg) * kD)[ln] =
+            acc;
+      }
+    }
+  };
+
   // ======================= producer warp ==================================
   if (warp == kProducer) {
     if (lane == 0) {
@@ -297,45 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ustart = wp.pre[b] + h * wp.nch[b];
       const int uend = ustart + wp.nch[b];
       const int xend = min(uend, hi);
+      if (xend >= hi) break;  // the last unit
       const int sl = e % C::NSLOT;
       if (!mbar_wait(&sfull[sl], (e / C::NSLOT) & 1)) {
         if (lane == 0) report(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
         break;
       }
-      const float *wm = slots + sl * C::SLOT;       // [warp][16]
-      const float *wl = wm + kWarps * 16;           // [warp][16]
-      const float *wo = wl + kWarps * 16;           // [warp][16][D]
-      const bool whole = ustart >= lo && uend <= hi;
-      const int wslot = c * 2 + partial_side(ustart, lo);
-      for (int idx = lane; idx < GU * kD; idx += 32) {
-        const int jg = idx / kD, d = idx % kD;  // query head jg of the unit
-        const int j = jg / G, g = jg % G;       // its kv head, row
-        const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
-        const int w0 = j * C::WPH;              // the kv head's warps
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::WPH; ++w)
-          M = fmaxf(M, wm[(w0 + w) * 16 + g]);
-        float L = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::WPH; ++w) {
-          const float mw = wm[(w0 + w) * 16 + g];
-          const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
-          L = fmaf(wl[(w0 + w) * 16 + g], a, L);
-          acc = fmaf(wo[((w0 + w) * 16 + g) * kD + d], a, acc);
-        }
-        const float res = acc / L * vs;
-        const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-        const long bh = (long)b * p.n_h + h * GU + jg;
-        if (whole) {
-          p.out[bh * kD + d] = f2bf(res);
-          if (d == 0 && p.lse) p.lse[bh] = lse_nat;
-        } else {
-          p.ws_o[((long)wslot * GU + jg) * kD + d] = res;
-          if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
-        }
-      }
+      write_unit(b, h, sl, lane, 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sl]);
       x = xend;
@@ -391,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 4; ++j) o[nt][j] = 0.f;
   };
 
-  auto flush = [&]() {
+  auto flush = [&](bool last) {
     // full row sums across the quad
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -424,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sfull[sl]);
+    if (lane == 0 && !last) mbar_arrive(&sfull[sl]);
     ++n_flush;
   };
 
@@ -438,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_abort = 1;
     }
     if (cc.b != cur_b || cc.h != cur_h) {
-      if (cur_b >= 0) flush();
+      if (cur_b >= 0) flush(false);
       cur_b = cc.b;
       cur_h = cc.h;
       start_unit(s, cur_h);
@@ -609,7 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&empty[s]);
     cursor_next(wp, p.batch, n_units, cc);
   }
-  if (cur_b >= 0) flush();
+  if (cur_b >= 0) {
+    flush(true);
+    named_sync(kFinalBar, kConsumers);  // every warp's state is in the slot
+    write_unit(cur_b, cur_h, (n_flush - 1) % C::NSLOT, tid, kConsumers);
+  }
 
   if (s_abort && tid == 0) {
     for (int t = 0; t < (1 << 20) && !s_producer_done; ++t) __nanosleep(1000);

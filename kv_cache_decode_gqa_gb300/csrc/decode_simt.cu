@@ -248,30 +248,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *wo = wl + kWarps * G;  // [warp][G][D]
     const bool whole = ustart >= lo && uend <= hi;
     const int wslot = c * 2 + partial_side(ustart, lo);
-    for (int idx = t; idx < GU * D; idx += nt) {
-      const int jg = idx / D, d = idx % D;  // head (j, g) of the unit
-      const int j = jg / G, g = jg % G;
-      const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
-      const int w0 = j * C::WPH;  // the head's warps
+    const long bh0 = (long)b * p.n_h + h * GU;
+    const int ln = t & 31, wq = t >> 5, nw = nt >> 5;
+    // lane jg (head (j, g) of the unit) of every warp: the weights c_w of
+    // the head's warps, and its log-sum-exp
+    float cw[C::WPH];
+    {
+      const int jg = ln < GU ? ln : 0;
+      const int j = jg / G, g = jg % G, w0 = j * C::WPH;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, wm[(w0 + w) * G + g]);
-      float L = 0.f, acc = 0.f;
+      float L = 0.f;
 #pragma unroll
       for (int w = 0; w < C::WPH; ++w) {
-        const float a = weight(wm[(w0 + w) * G + g], M);
-        L = fmaf(wl[(w0 + w) * G + g], a, L);
-        acc = fmaf(wo[((w0 + w) * G + g) * D + d], a, acc);
+        cw[w] = weight(wm[(w0 + w) * G + g], M);
+        L = fmaf(wl[(w0 + w) * G + g], cw[w], L);
       }
-      const float res = acc / L * vs;
+      const float vs = DT == DT_FP8 ? p.v_scale[h * HP + j] : 1.0f;
+      const float f = L > 0.f ? vs / L : 0.f;
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) cw[w] *= f;
       const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
-      const long bh = (long)b * p.n_h + h * GU + jg;
+      if (wq == 0 && ln < GU) {
+        if (!whole)
+          p.ws_lse[(long)wslot * GU + jg] = lse_nat;
+        else if (p.lse)
+          p.lse[bh0 + jg] = lse_nat;
+      }
+    }
+    // the output rows, four columns a lane (a warp step covers 32 / (D / 4)
+    // rows)
+    constexpr int LPR = D / 4;
+    constexpr int RPI = 32 / LPR;
+    const int col4 = ln % LPR;
+    for (int r0 = wq * RPI; r0 < GU; r0 += nw * RPI) {
+      const int jg = r0 + ln / LPR;
+      const int jr = jg < GU ? jg : 0;
+      const int w0 = (jr / G) * C::WPH, g = jr % G;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) {
+        const float cf = __shfl_sync(0xffffffffu, cw[w], jr);
+        const float4 v =
+            reinterpret_cast<const float4 *>(wo + ((w0 + w) * G + g) * D)[col4];
+        acc.x = fmaf(cf, v.x, acc.x);
+        acc.y = fmaf(cf, v.y, acc.y);
+        acc.z = fmaf(cf, v.z, acc.z);
+        acc.w = fmaf(cf, v.w, acc.w);
+      }
+      if (jg >= GU) continue;
       if (whole) {
-        p.out[bh * D + d] = f2bf(res);
-        if (d == 0 && p.lse) p.lse[bh] = lse_nat;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(p.out + (bh0 + jg) * D)[col4] = packed;
       } else {
-        p.ws_o[((long)wslot * GU + jg) * D + d] = res;
-        if (d == 0) p.ws_lse[(long)wslot * GU + jg] = lse_nat;
+        reinterpret_cast<float4 *>(p.ws_o + ((long)wslot * GU + jg) * D)[col4] =
+            acc;
       }
     }
   };
