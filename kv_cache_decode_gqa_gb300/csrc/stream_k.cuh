@@ -397,11 +397,15 @@ __device__ __forceinline__ void quad_merge(const float *lse, const float *o,
 // Part i is the partial of CTA c_first + i: side 1 of the first covering
 // CTA, side 0 of the others. Units inside one CTA were written whole.
 constexpr int kMergeThreads = 256;
+// Partition capacity of the merge launch for batches up to 64: its CTAs then
+// hold under 1 KB of shared memory, so that one fits beside a decode CTA of
+// the next call (which holds up to ~215 KB) instead of delaying its start.
+constexpr int kMergeSmallBatch = 64;
 
-template <int D, int GU>
+template <int D, int GU, int NB>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_dense_kernel(const DecodeParams p, int n_units) {
-  __shared__ WorkPartition wp;
+  __shared__ WorkPartitionT<NB> wp;
   __shared__ int s_len_err;
   pdl_trigger();
   // The lengths may be read before the decode launch completes: that launch
@@ -468,7 +472,10 @@ inline cudaError_t launch_merge_dense(const DecodeParams &p, int n_units,
   if (p.n_splits <= 1 || p.batch == 0) return cudaSuccess;
   const long nu = (long)p.batch * n_units;
   const int grid = (int)(nu < 1024 ? nu : 1024);
-  return launch_pdl(merge_dense_kernel<D, GU>, dim3(grid),
+  if (p.batch <= kMergeSmallBatch)
+    return launch_pdl(merge_dense_kernel<D, GU, kMergeSmallBatch>, dim3(grid),
+                      dim3(kMergeThreads), 0, s, 1, p, n_units);
+  return launch_pdl(merge_dense_kernel<D, GU, kMaxDecodeBatch>, dim3(grid),
                     dim3(kMergeThreads), 0, s, 1, p, n_units);
 }
 
