@@ -8,7 +8,9 @@
 //
 // Same persistent stream-K structure as the CUDA-core kernel (stream_k.cuh):
 // one CTA per SM with an equal share of all (sequence, head group, 64-token
-// chunk) work, a producer warp, a finisher warp, and four consumer warps.
+// chunk) work, a producer warp, a finisher warp (it writes every unit of the
+// range but the last, which the consumer warps write together), and four
+// consumer warps.
 // A head group is HP consecutive kv heads (HP = 2 for an fp8 cache with
 // 64-token blocks, whose HP heads' rows are adjacent): the producer moves a
 // chunk's K and V with tiled TMA copies of HP x 64 rows (boxes of 128-byte
