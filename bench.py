@@ -26,15 +26,12 @@ data path; the step time is the max over ranks.
 import argparse
 import hashlib
 import json
-import math
 import multiprocessing as mp
 import os
 import statistics
 import subprocess
 import sys
 import time
-
-import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)

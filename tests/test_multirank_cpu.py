@@ -6,8 +6,6 @@ arm runs on rank 0 alone."""
 import os
 import socket
 
-import pytest
-import torch.distributed as dist
 import torch.multiprocessing as mp
 
 import bench

@@ -11,9 +11,7 @@ This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
 import ctypes
-import os
 
-import numpy as np
 import pytest
 
 pytestmark = pytest.mark.gpu
