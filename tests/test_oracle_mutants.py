@@ -192,3 +192,32 @@ def test_reindex_ignoring_the_pool_is_caught(monkeypatch):
         return OA.indexer_topk(q_idx, w, idx_raw, bt, seq_lens, bs, k)
     _patch(monkeypatch, "indexer_topk_in_pool", mutant)
     _fails(P.test_topk_in_pool_brute_force)
+
+
+def test_window_one_position_too_wide_is_caught(monkeypatch):
+    orig = OA.gqa_decode
+
+    def mutant(*a, window=0, **kw):
+        return orig(*a, window=window + 1 if window else 0, **kw)
+    _patch(monkeypatch, "gqa_decode", mutant)
+    _fails(P.test_window_is_attention_over_the_last_w_positions)
+
+
+def test_append_into_a_shared_block_without_copy_is_caught(monkeypatch):
+    def mutant(self, name, pos, block_size):
+        table = self.tables[name]
+        lb = pos // block_size
+        while len(table) <= lb:
+            table.append(-1)
+        if table[lb] < 0:
+            table[lb] = self.free_blocks()[0]
+        return None                              # writes in place
+    monkeypatch.setattr(oracle.CowPool, "prepare_append", mutant)
+    _fails(P.test_cow_fork_shares_and_append_copies_once)
+
+
+def test_fork_that_copies_is_caught(monkeypatch):
+    def mutant(self, src, name):
+        self.new_sequence(name, len(self.tables[src]))
+    monkeypatch.setattr(oracle.CowPool, "fork", mutant)
+    _fails(P.test_cow_fork_shares_and_append_copies_once)
