@@ -449,8 +449,13 @@ kvd_status kvd_block_pool_prepare_append(kvd_block_pool *pool,
                                          int32_t block_size, int32_t *src,
                                          int32_t *dst, int32_t *n_copies);
 /* device: whole blocks dst[i] := src[i] of K and V (every kv head's rows),
- * src / dst DEVICE int32 [n]; an id outside [0, num_blocks) skips that copy
- * and sets KVD_DEVERR_BLOCK */
+ * src / dst DEVICE int32 [n]. The copies run in parallel: the dst ids must be
+ * distinct and none may be a src of the same call (kvd_block_pool_prepare_
+ * append's pairs meet this, every dst being a fresh block). An id outside
+ * [0, num_blocks) skips that copy and sets KVD_DEVERR_BLOCK. Host errors,
+ * before any launch: KVD_ERR_NULL (no cache, or src / dst NULL with n > 0),
+ * KVD_ERR_SHAPE (n < 0, n > 65535, or a block not a multiple of 16 bytes);
+ * KVD_ERR_CUDA if a launch fails. n = 0 does nothing. */
 kvd_status kvd_copy_blocks(const kvd_cache *cache, const int32_t *src,
                            const int32_t *dst, int32_t n, kvd_stream stream);
 
