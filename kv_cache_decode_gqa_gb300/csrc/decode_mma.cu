@@ -68,9 +68,11 @@ struct MCfg {
   static constexpr int TPW = 64 / WPH;       // tokens per warp and chunk
   static constexpr int NSUB = TPW / 16;      // 16-token tiles per warp
   static constexpr int SLOT = kWarps * 16 * (kD + 2);  // floats per slot
-  // One flush slot (units span tens of chunks here, so the finisher is long
-  // done with a unit before the next one ends); the rest of 226 KB is ring,
-  // as deep as fits: the bytes in flight per SM are what keep HBM busy.
+  // One flush slot: the finisher writes a unit in about the time of one or
+  // two chunks, and units span tens of chunks at the long contexts this
+  // kernel is sized for (a short-window unit of 2-3 chunks may wait for the
+  // slot briefly). The rest of 226 KB is ring, as deep as fits: the bytes in
+  // flight per SM are what keep HBM busy.
   static constexpr int NSLOT = 1;
   static constexpr int MERGE = NSLOT * SLOT * 4;
   static constexpr int FIXED =
