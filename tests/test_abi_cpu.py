@@ -73,6 +73,8 @@ def test_gqa_validation(lib):
     assert _gqa(lib, _cache(), _seqs(max_seq_len=64 * 16 + 1)) == 4
     assert b"capacity" in lib.kvd_last_error()
     assert _gqa(lib, _cache(), _seqs(batch=-1)) == 2
+    assert _gqa(lib, _cache(), _seqs(batch=1025)) == 3    # over 1024 a call
+    assert b"1024" in lib.kvd_last_error()
     assert _gqa(lib, _cache(dtype=1), _seqs()) == 1       # fp8 needs scales
     assert _gqa(lib, _cache(), _seqs(batch=0)) == 0       # nothing to do
     assert _gqa(lib, _cache(), _seqs(flags=2)) == 2       # unknown flag bit
@@ -125,6 +127,13 @@ def test_mla_sparse_indexer_validation(lib):
              FAKE, None, None, 0, None) == 2
     assert f(ctypes.byref(_cache(n_kv=2, head_dim=512)), ctypes.byref(s),
              FAKE, 2048, FAKE, 64, 0.0, FAKE, None, None, 0, None) == 3
+    big = _seqs(batch=257)                    # over 256 sequences a call
+    assert m(ctypes.byref(lat), 512, ctypes.byref(big), FAKE, 128, 0.0, FAKE,
+             None, None, 0, None) == 3
+    assert b"256" in lib.kvd_last_error()
+    assert f(ctypes.byref(sp), ctypes.byref(big), FAKE, 2048, FAKE, 64, 0.0,
+             FAKE, None, None, 0, None) == 3
+    assert b"256" in lib.kvd_last_error()
     ix = _cache(v=None, n_kv=1, head_dim=64)
     g = lib.kvd_indexer_topk
     assert g(ctypes.byref(ix), ctypes.byref(s), FAKE, 4, FAKE, 0, FAKE, None,
