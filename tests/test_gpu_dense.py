@@ -204,6 +204,23 @@ def test_gqa_decode_batch_over_64(n_h, n_kv):
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"batch96/{n_h}x{n_kv}")
 
 
+# The largest batch a dense call takes (1024 sequences): the partition scan
+# at its full width, in both kernels and the merge.
+@pytest.mark.parametrize("n_h,n_kv", [(2, 2), (16, 2)], ids=["mha", "gqa8"])
+def test_gqa_decode_max_batch(n_h, n_kv):
+    lengths = [int(x) for x in np.random.default_rng(1024).integers(0, 130,
+                                                                    1024)]
+    s = W.config("llama31_70b_gqa", batch=1024, lengths=lengths, n_layers=1,
+                 block_size=64, dtype="bf16", n_h=n_h, n_kv=n_kv,
+                 head_dim=128)
+    wl = W.DeviceWorkload(s, layers=[0])
+    out, lse = H.device_step(wl, 0)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    H.assert_close(H.to_np_bf16(out), ref, f"batch1024/{n_h}x{n_kv}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"batch1024/{n_h}x{n_kv}")
+
+
 # MXFP4 caches: head_dim 128, query groups of 1, 2 or 4 (CUDA-core kernel)
 MXFP4_CASES = [c for c in DENSE_CASES if c[3] == 128 and c[1] // c[2] <= 4]
 
