@@ -105,6 +105,14 @@ def decode_launch_bytes(shape):
     return b
 
 
+def data_description(shape):
+    """The bench line's `data`: what the seeded synthetic inputs are."""
+    cache = {"fp8": "random E4M3 cache codes with per-head scales",
+             "mxfp4": "random E2M1 cache codes with E4M3 group scales"}.get(
+                 shape.dtype, "N(0,1) bf16 cache")
+    return f"synthetic (seeded {cache}, N(0,1) bf16 queries)"
+
+
 def measured_peaks(key="hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -664,7 +672,7 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": s.dtype,
-        "data": "synthetic (seeded N(0,1) bf16 cache and queries)",
+        "data": data_description(s),
         "config": {"workload": s.name, "batch": s.batch,
                    "cached_len": s.lengths[0] if len(set(s.lengths)) == 1
                    else f"{min(s.lengths)}..{max(s.lengths)}",

@@ -56,3 +56,10 @@ def test_sparse_schedule_bytes():
     for layer, mode in enumerate(s.modes):
         want = gather + (indexer if mode in ("full", "reindex") else 0)
         assert bench.kv_bytes_layer(s, layer) == want, (layer, mode)
+
+
+def test_data_description_names_the_cache_format():
+    assert "bf16 cache" in bench.data_description(W.config("llama2_7b_mha"))
+    assert "E4M3" in bench.data_description(W.config("llama31_70b_gqa_fp8"))
+    assert "E2M1" in bench.data_description(W.config("llama2_7b_mha_mxfp4"))
+    assert "bf16 cache" in bench.data_description(W.config("sparse"))
