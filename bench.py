@@ -42,6 +42,7 @@ from kv_cache_decode_gqa_gb300 import workloads as W  # noqa: E402
 METRIC = ("decode attn: KV-read HBM GB/s (% of GB300 peak) and decode "
           "tokens/s per layer")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e, nominal (context beside the measured peak)
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -686,6 +687,7 @@ def run_ours(args, ws, rank, local):
                           "working set per step larger than L2 (distinct "
                           "per-layer caches); no flush")},
         "pct_of_peak": round(100 * value / ws / peak, 1),
+        "pct_of_nominal_hbm": round(100 * value / ws / NOMINAL_HBM_GBS, 1),
         "tokens_per_s_per_layer": round(s.batch * s.n_layers / (ms / 1e3), 1),
         "kv_bytes_per_step": nbytes,
         "e2e": {"value": round(ws * nbytes / (ms_e2e / 1e3) / 1e9, 1),
