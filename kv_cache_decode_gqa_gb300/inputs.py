@@ -97,8 +97,8 @@ def byte_table():
 
 def mxfp4_scale_table():
     """256 E4M3 codes of the 16 values 1/8 .. 15/32 (exponent field 4 or
-    5, any mantissa), each 16 times: positive group scales in the range that
-    amax / 6 takes for groups of 16 N(0,1) values."""
+    5, any mantissa), each 16 times: positive group scales where amax / 6
+    of 16 N(0,1) values falls for about 92 % of groups (median 0.34)."""
     if "mxscale" not in _TABLES:
         j = np.arange(256, dtype=np.uint32)
         codes = ((4 + ((j >> 3) & 1)) << 3) | (j & 7)

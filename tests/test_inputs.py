@@ -49,3 +49,31 @@ def test_permutation_and_ints():
     assert L.min() >= 1024 and L.max() <= 8192
     u = I.uniform01_f32(I.stream_key(7), 1000)
     assert u.dtype == np.float32 and u.min() >= 0 and u.max() < 1
+
+
+def test_mxfp4_input_tables():
+    """MXFP4 inputs: code bytes are all 256 values (two random E2M1 codes
+    each); group scales decode (with the oracle's E4M3 table) to exactly the
+    16 values 1/8 .. 15/32, each 16 times, where amax / 6 of 16 N(0,1)
+    values falls for about 92 % of groups."""
+    import numpy as np
+    import oracle
+    from kv_cache_decode_gqa_gb300 import inputs as I
+    assert sorted(I.byte_table().tolist()) == list(range(256))
+    vals = oracle.e4m3_codes_to_f64(I.mxfp4_scale_table())
+    want = sorted({e * (1 + m / 8) for e in (1 / 8, 1 / 4) for m in range(8)})
+    assert len(want) == 16 and want[0] == 1 / 8 and want[-1] == 15 / 32
+    u, counts = np.unique(vals, return_counts=True)
+    assert u.tolist() == want and set(counts.tolist()) == {16}
+    amax6 = np.abs(np.random.default_rng(5).standard_normal((100_000, 16))
+                   ).max(axis=1) / 6
+    inside = np.mean((amax6 >= 1 / 8) & (amax6 <= 15 / 32))
+    assert 0.91 < inside < 0.94
+
+
+def test_fp8_cache_codes_cover_eighth_to_thirty():
+    import numpy as np
+    import oracle
+    from kv_cache_decode_gqa_gb300 import inputs as I
+    mag = np.abs(oracle.e4m3_codes_to_f64(I.fp8_code_table()))
+    assert mag.min() == 1 / 8 and mag.max() == 30.0
