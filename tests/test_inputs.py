@@ -77,3 +77,25 @@ def test_fp8_cache_codes_cover_eighth_to_thirty():
     from kv_cache_decode_gqa_gb300 import inputs as I
     mag = np.abs(oracle.e4m3_codes_to_f64(I.fp8_code_table()))
     assert mag.min() == 1 / 8 and mag.max() == 30.0
+
+
+def test_workload_recipe_ranges():
+    """fp8 scales in [1/16, 1/8) with inv_scale their fp32 reciprocal;
+    Llama-3.1-70B cached lengths in [1024, 8192]; indexer weights in
+    [0, 1)."""
+    import numpy as np
+    from kv_cache_decode_gqa_gb300 import workloads as W
+    s = W.config("llama31_70b_gqa_fp8")
+    for layer in (0, 79):
+        for t in (W.T_KSCALE, W.T_VSCALE):
+            sc, inv = W.host_scales(s, layer, t)
+            assert sc.dtype == np.float32 and sc.shape == (8,)
+            assert np.all((sc >= 1 / 16) & (sc < 1 / 8))
+            assert np.array_equal(inv, np.float32(1) / sc)
+    lens = W.config("llama31_70b_gqa").lengths
+    assert len(lens) == 32 and min(lens) >= 1024 and max(lens) <= 8192
+    assert len(set(lens)) > 16                        # a real length mix
+    sp = W.config("sparse")
+    w = W.host_weights(sp, 0)
+    assert w.shape == (sp.batch, sp.idx_heads)
+    assert np.all((w >= 0) & (w < 1))
