@@ -13,8 +13,10 @@
  *
  * Conventions shared by every call:
  *   - Every pointer argument that names tensor data is DEVICE memory owned by
- *     the caller. The library allocates nothing, frees nothing and never
- *     synchronises the device (kvd_device_error is the one exception).
+ *     the caller. The library allocates no device memory, frees none and
+ *     never synchronises the device (kvd_device_error is the one exception).
+ *     The copy-on-write block pool (kvd_block_pool_*) is the one host object:
+ *     it owns host memory for its counts and takes HOST arrays.
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream). Outputs are valid once the stream reaches
  *     that point.
@@ -112,7 +114,7 @@ typedef enum kvd_dtype {
  * nearest even and saturate; a group whose scale rounds to 0 stores zero
  * codes. Quantise after RoPE: the library stores what it is given. The
  * scale pointers are unused. Supported: head_dim 128, an even block_size,
- * kv_append and GQA decode with n_h / n_kv <= 4 (dequantised in the
+ * kv_append and GQA decode with n_h / n_kv of 1, 2 or 4 (dequantised in the
  * CUDA-core decode kernel; there is no fp4 MMA).
  */
 typedef struct kvd_cache {
@@ -195,7 +197,8 @@ typedef enum kvd_op {
  *   k_new, v_new   device bf16 [batch][n_kv][head_dim]; v_new is ignored
  *                  (may be NULL) for a K-only cache and required otherwise
  * bf16 caches receive the bytes unchanged; fp8 caches receive
- * E4M3_rne_satfinite(float(x) * inv_scale[kv_head]).
+ * E4M3_rne_satfinite(float(x) * inv_scale[kv_head]); MXFP4 caches receive
+ * each 16-channel group encoded as described at kvd_cache.
  * Errors: KVD_ERR_NULL, KVD_ERR_SHAPE (batch < 0, head_dim not a multiple of
  * 8, misaligned pointer), KVD_ERR_UNSUPPORTED (dtype). A position or block id
  * out of range on the device skips that row and sets KVD_DEVERR_POS /
@@ -222,8 +225,9 @@ kvd_status kvd_kv_append(const kvd_cache *cache, const int32_t *block_table,
  *             "Workspace" above)
  * Supported: bf16 or fp8 cache, head_dim 64 or 128, n_h / n_kv in
  * {1, 2, 4, 8, 16} (8 and 16 need head_dim 128 and a block_size that is a
- * multiple of 64 or one of 16, 32), at most 1024 sequences per call. An empty sequence
- * gives out = 0 and lse = -inf.
+ * multiple of 64 or one of 16, 32); an MXFP4 cache with head_dim 128 and
+ * n_h / n_kv of 1, 2 or 4; at most 1024 sequences per call. An empty
+ * sequence gives out = 0 and lse = -inf.
  */
 kvd_status kvd_gqa_decode(const kvd_cache *cache, const kvd_seqs *seqs,
                           const void *q, int32_t n_h, float scale, void *out,
