@@ -305,6 +305,8 @@ kvd_status kvd_gqa_decode_noalloc(const kvd_cache *cache,
  *   q         device bf16 [batch][n_h][head_dim] = [q_lat | q_rope]
  *   out       device bf16 [batch][n_h][d_c]
  *   lse       device fp32 [batch][n_h] or NULL
+ *   workspace at least kvd_workspace_size(KVD_OP_MLA_DECODE) bytes (see
+ *             "Workspace" above)
  * Supported: d_c = 512, head_dim = 576, n_h a multiple of 64, at most 256
  * sequences per call.
  */
@@ -331,6 +333,8 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
  *   scores       device fp32 [batch][max_seq_len] or NULL: if given, the
  *                scores the selection used (entries >= seq_lens[b] are
  *                unspecified)
+ *   workspace    when scores is NULL: at least
+ *                kvd_workspace_size(KVD_OP_INDEXER_TOPK) bytes (the scores)
  * Supported: d_idx = 64, n_idx_heads <= 8, 1 <= k <= 16384.
  */
 kvd_status kvd_indexer_topk(const kvd_cache *index_cache, const kvd_seqs *seqs,
@@ -400,6 +404,8 @@ kvd_status kvd_indexer_topk_pool(const kvd_cache *index_cache,
  *   indices  device int32 [batch][k] positions; entries < 0 are skipped, and
  *            so are entries >= seq_lens[b] (flagged KVD_DEVERR_INDEX)
  *   q, out, lse, scale as for kvd_gqa_decode
+ *   workspace at least kvd_workspace_size(KVD_OP_SPARSE_DECODE, ..., k)
+ *            bytes (see "Workspace" above)
  * Supported: bf16 cache with n_kv = 1, head_dim = 512, n_h a multiple of 64,
  * at most 256 sequences per call.
  */
