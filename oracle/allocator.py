@@ -32,9 +32,11 @@ class CowPool:
 
     # -- counting --------------------------------------------------------
     def refcount(self, block):
+        """References on a block: the table entries naming it."""
         return sum(t.count(block) for t in self.tables.values())
 
     def free_blocks(self):
+        """Ascending ids of the blocks no table names."""
         used = {b for t in self.tables.values() for b in t if b >= 0}
         return [b for b in range(self.num_blocks) if b not in used]
 
@@ -81,6 +83,7 @@ class CowPool:
         return (old, fresh)
 
     def blocks_used(self):
+        """Blocks some table names."""
         return self.num_blocks - len(self.free_blocks())
 
 

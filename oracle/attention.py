@@ -1,5 +1,8 @@
 """Decode attention over a paged KV cache, written out plainly in fp64.
 
+TEST INFRASTRUCTURE (see the package docstring): imported only by the tests,
+the smoke check and the benchmark's CPU-baseline / reference leg.
+
 Pages this follows (cited by page title and section):
   [KV]  "KV cache" (this.guide)
   [POD] "My Weird Prompts" episode 640482 (podcast transcript)

@@ -1,5 +1,7 @@
 """Element formats of the cache, decoded and encoded exactly in fp64.
 
+TEST INFRASTRUCTURE (see the package docstring).
+
 Sources:
   * bf16: IEEE-754 binary32 with the low 16 mantissa bits dropped; a bf16 bit
     pattern ``u`` is the binary32 pattern ``u << 16``.
