@@ -260,16 +260,15 @@ def barrier(dist):
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_unit_inputs(name, layer, seqs):
-    """Host inputs of one oracle unit: layer ``layer`` for sequences
-    ``seqs`` (compact caches), with this step's append applied by the
-    oracle's own kv_append."""
+    """Host inputs of one oracle unit: layer ``layer`` (every layer of the
+    schedule for the sparse workloads) for sequences ``seqs`` (compact
+    caches), with this step's append applied by the oracle's own
+    kv_append."""
     import oracle
     s = W.config(name)
     pg = W.Paging(s)
-    q = oracle.bf16_bits_to_f64(W.host_bf16(s, layer, W.T_Q,
-                                            (s.batch, s.n_h, s.head_dim)))[seqs]
-    lens = [s.seq_lens[b] for b in seqs]
     pos = [s.lengths[b] for b in seqs]
+    lens = [s.seq_lens[b] for b in seqs]
     if s.kind == "sparse":
         kr, bt = W.host_cache_compact(s, pg, 0, W.T_K, seqs, n_kv=1)
         vr, _ = W.host_cache_compact(s, pg, 0, W.T_V, seqs, n_kv=1)
@@ -282,8 +281,19 @@ def oracle_unit_inputs(name, layer, seqs):
         kr = oracle.kv_append(kr, bt, pos, kn, s.block_size)
         vr = oracle.kv_append(vr, bt, pos, vn, s.block_size)
         ir = oracle.kv_append(ir, bt, pos, xn, s.block_size)
-        return dict(kind="sparse", s=s, q=q, kr=kr, vr=vr, ir=ir, bt=bt,
-                    lens=lens, seqs=seqs, layer=layer)
+        qs, qis, ws_ = {}, {}, {}
+        for l in range(s.n_layers):
+            qs[l] = oracle.bf16_bits_to_f64(
+                W.host_bf16(s, l, W.T_Q, (s.batch, s.n_h, s.head_dim)))[seqs]
+            if s.modes[l] != "reuse":
+                qis[l] = oracle.bf16_bits_to_f64(
+                    W.host_bf16(s, l, W.T_QIDX,
+                                (s.batch, s.idx_heads, s.idx_dim)))[seqs]
+                ws_[l] = W.host_weights(s, l)[seqs]
+        return dict(kind="sparse", s=s, q=qs, q_idx=qis, w=ws_, kr=kr, vr=vr,
+                    ir=ir, bt=bt, lens=lens, seqs=seqs, layer=layer)
+    q = oracle.bf16_bits_to_f64(W.host_bf16(s, layer, W.T_Q,
+                                            (s.batch, s.n_h, s.head_dim)))[seqs]
     knew = W.host_bf16(s, layer, W.T_KNEW, (s.batch, s.n_kv, s.head_dim))[seqs]
     kr, bt = W.host_cache_compact(s, pg, layer, W.T_K, seqs)
     kr = oracle.kv_append(kr, bt, pos, knew, s.block_size) \
@@ -310,9 +320,12 @@ def oracle_unit_inputs(name, layer, seqs):
 
 
 def oracle_run_unit(d):
-    """One oracle decode of a prepared unit; returns the KV bytes it read."""
+    """One oracle pass over a prepared unit. Returns (KV bytes read,
+    sequence-layer decodes done): the metric's bytes, counted as for the GPU
+    step, and the tokens of `tokens_per_s_per_layer`."""
     import oracle
     s = d["s"]
+    n = len(d["seqs"])
     if d["kind"] == "gqa":
         if s.dtype == "fp8":
             oracle.gqa_decode(d["q"], d["kr"], d["vr"], d["bt"], d["lens"],
@@ -322,70 +335,91 @@ def oracle_run_unit(d):
             oracle.gqa_decode(d["q"], d["kr"], d["vr"], d["bt"], d["lens"],
                               s.block_size, dtype=s.dtype, window=s.window)
         seen = [min(L, s.window) if s.window else L for L in d["lens"]]
-        return sum(seen) * s.n_kv * 2 * s.head_dim * s.elem_bytes
+        return sum(seen) * s.n_kv * 2 * s.head_dim * s.elem_bytes, n
     if d["kind"] == "mla":
         oracle.mla_decode(d["q"], d["kr"], d["bt"], d["lens"], s.block_size,
                           d_c=s.d_c)
-        return sum(d["lens"]) * s.head_dim * 2
-    layer = d["layer"]
-    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, layer, W.T_QIDX,
-                                             (s.batch, s.idx_heads,
-                                              s.idx_dim)))[d["seqs"]]
-    w = W.host_weights(s, layer)[d["seqs"]]
-    idx, _ = oracle.indexer_topk(qI, w, d["ir"], d["bt"], d["lens"],
-                                 s.block_size, s.topk)
-    oracle.sparse_decode(d["q"], d["kr"], d["vr"], d["bt"], d["lens"],
-                         s.block_size, idx)
-    n = len(d["seqs"])
-    return sum(d["lens"]) * s.idx_dim * 2 + n * s.topk * 2 * s.head_dim * 2
+        return sum(d["lens"]) * s.head_dim * 2, n
+    # the sparse workloads: the whole Full / Reuse / Reindex schedule (its
+    # bytes counted as for the GPU step, per sequence)
+    L = range(s.n_layers)
+    oracle.sparse_schedule(s.modes, [d["q"][l] for l in L],
+                           [d["q_idx"].get(l) for l in L],
+                           [d["w"].get(l) for l in L], d["kr"], d["vr"],
+                           d["ir"], d["bt"], d["lens"], s.block_size, s.topk,
+                           pool_k=s.pool_k)
+    return kv_bytes_step(s) * n // s.batch, n * s.n_layers
 
 
 def _oracle_worker_main(args):
-    name, layer, seqs, budget_s = args
-    d = oracle_unit_inputs(name, layer, seqs)
-    oracle_run_unit(d)                               # untimed first run
-    nbytes, reps = 0, 0
+    name, units, budget_s = args
+    ds = [oracle_unit_inputs(name, layer, seqs) for layer, seqs in units]
+    for d in ds:
+        oracle_run_unit(d)                           # untimed first pass
+    nbytes, toks, reps = 0, 0, 0
     t0 = time.perf_counter()
     while True:
-        nbytes += oracle_run_unit(d)
-        reps += 1
+        for d in ds:
+            b, t = oracle_run_unit(d)
+            nbytes += b
+            toks += t
+            reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return nbytes, el, reps
+    return nbytes, toks, el, reps
 
 
-def oracle_units(shape, workers):
-    """Sampled units: (layer, [sequence]) pairs spread over the workload."""
+def oracle_plan(shape, cores):
+    """The oracle baseline's work, one list of (layer, sequences) units per
+    worker (a worker takes its units in turn), and how it covers a step:
+      Llama-2 shapes and tiny: every layer of the step, layers dealt out to
+        the workers;
+      Llama-3.1 shapes: one full layer (all 32 sequences dealt out to the
+        workers), a step being 80 such layers;
+      latent: a subset of the batch rows (one sequence a worker), scaled
+        linearly in B;
+      sparse: the whole 8-layer schedule, one sequence a worker."""
     s = shape
-    seqs = list(range(s.batch))
+    if s.kind == "gqa" and s.n_layers <= 32:
+        units = [(l, list(range(s.batch))) for l in range(s.n_layers)]
+        n = min(cores, len(units))
+        return [units[i::n] for i in range(n)], \
+            f"every layer of the step ({s.n_layers} layers)"
     if s.kind == "gqa":
-        per = max(1, min(s.batch, 4))
-        groups = [seqs[i:i + per] for i in range(0, s.batch, per)]
-    else:
-        groups = [[b] for b in seqs]
-    layers = list(range(s.n_layers)) if s.kind == "gqa" else [0]
-    units = [(l, g) for l in layers for g in groups]
-    stride = max(1, len(units) // workers)
-    return units[::stride][:workers]
+        n = min(cores, s.batch)
+        return [[(0, list(range(s.batch))[i::n])] for i in range(n)], \
+            f"one full layer (all {s.batch} sequences), x{s.n_layers} layers"
+    if s.kind == "mla":
+        n = min(cores, s.batch)
+        return [[(0, [b])] for b in range(n)], \
+            f"{n} of {s.batch} batch rows, scaled x{s.batch / n:g} in B"
+    n = min(cores, s.batch)
+    return [[(0, [b])] for b in range(n)], \
+        f"the whole {s.n_layers}-layer schedule, one sequence a worker"
 
 
-def cpu_baseline(name, budget_s=12.0):
-    """Time the oracle on the host cores: one spawned single-threaded worker
-    per core, each on its own sampled unit for about ``budget_s`` seconds.
-    Returns (GB/s, cores, sample description)."""
+def cpu_baseline(name, budget_s=8.0, budget_1=3.0):
+    """Time the oracle on the host cores, as it stands: one spawned
+    single-threaded worker per core on its sampled unit for ~budget_s
+    seconds (all cores), and one worker alone for ~budget_1 seconds (one
+    thread). GB/s = bytes read / slowest worker's time; tokens/s per layer =
+    sequence-layer decodes / that time."""
     s = W.config(name)
     cores = os.cpu_count() or 1
-    units = oracle_units(s, cores)
+    plan, how = oracle_plan(s, cores)
     env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
     saved = {k: os.environ.get(k) for k in env_keys}
     for k in env_keys:
         os.environ[k] = "1"
     try:
         ctx = mp.get_context("spawn")
-        with ctx.Pool(len(units)) as pool:
+        with ctx.Pool(1) as pool:
+            one = pool.map(_oracle_worker_main,
+                           [(name, plan[0], budget_1)])[0]
+        with ctx.Pool(len(plan)) as pool:
             res = pool.map(_oracle_worker_main,
-                           [(name, l, g, budget_s) for l, g in units])
+                           [(name, u, budget_s) for u in plan])
     finally:
         for k, v in saved.items():
             if v is None:
@@ -393,91 +427,117 @@ def cpu_baseline(name, budget_s=12.0):
             else:
                 os.environ[k] = v
     total = sum(r[0] for r in res)
-    wall = max(r[1] for r in res)
-    reps = sum(r[2] for r in res)
-    sample = (f"{len(units)} units of (layer, sequences) of {name}, each "
-              f"repeated for ~{budget_s:.0f} s in its own single-threaded "
-              f"process ({reps} oracle calls, {total / 1e9:.2f} GB of cache "
-              f"read); GB/s = bytes / slowest worker's time")
-    return total / wall / 1e9, len(units), sample
+    toks = sum(r[1] for r in res)
+    wall = max(r[2] for r in res)
+    reps = sum(r[3] for r in res)
+    gbs = total / wall / 1e9
+    step_bytes = kv_bytes_step(s)
+    return {
+        "value": round(gbs, 4), "unit": "GB/s", "cores": len(plan),
+        "kind": "oracle",
+        "value_1thread": round(one[0] / one[2] / 1e9, 4),
+        "tokens_per_s_per_layer": round(toks / wall, 3),
+        "tokens_per_s_per_layer_1thread": round(one[1] / one[2], 3),
+        "ms_per_step": round(step_bytes / (gbs * 1e9) * 1e3, 2)
+        if gbs > 0 else None,
+        "sample": (f"{how}: {len(plan)} single-threaded processes, each "
+                   f"repeating its units for ~{budget_s:g} s ({reps} oracle "
+                   f"passes, {total / 1e9:.2f} GB of cache read); one thread:"
+                   f" the first process's units alone for ~{budget_1:g} s"),
+    }
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def build_step(K, wl, outs, wss):
+def build_step(K, wl, outs, wss, events=None):
+    """The workload's step as a serving loop issues it. ``events`` (tag ->
+    list of (start, end) event pairs to fill) brackets each call."""
     s = wl.shape
+
+    def mark(tag, i):
+        if events is not None:
+            events.setdefault(tag, [])
+            if len(events[tag]) <= i:
+                import torch
+                events[tag].append((torch.cuda.Event(enable_timing=True,
+                                                     external=True),
+                                    torch.cuda.Event(enable_timing=True,
+                                                     external=True)))
+            return events[tag][i]
+        return None
+
+    def timed(tag, i, fn):
+        ev = mark(tag, i)
+        if ev is not None:
+            ev[0].record()
+        fn()
+        if ev is not None:
+            ev[1].record()
 
     def step():
         if s.kind == "sparse":
-            run_sparse_schedule(K, wl, outs, wss)
+            run_sparse_schedule(K, wl, outs, wss, timed)
             return
-        for layer in wl.layers:
+        for i, layer in enumerate(wl.layers):
             c = wl.caches[layer]
             if s.kind == "mla":
-                K.kv_append(c, wl.block_table, wl.pos, wl.k_new[layer])
-                K.mla_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                             wl.q[layer], d_c=s.d_c, out=outs[layer],
-                             workspace=wss[layer], want_lse=False)
+                timed("append", i, lambda: K.kv_append(
+                    c, wl.block_table, wl.pos, wl.k_new[layer]))
+                timed("decode", i, lambda: K.mla_decode(
+                    c, wl.block_table, wl.seq_lens, wl.max_seq_len,
+                    wl.q[layer], d_c=s.d_c, out=outs[layer],
+                    workspace=wss[layer], want_lse=False))
             else:
                 # the append rides in the decode's pass over the cache; the
                 # lengths and block tables are set before the step
-                K.gqa_append_decode(c, wl.block_table, wl.seq_lens,
-                                    wl.max_seq_len, wl.pos, wl.k_new[layer],
-                                    wl.v_new[layer], wl.q[layer],
-                                    out=outs[layer], workspace=wss[layer],
-                                    want_lse=False, seqs_flags=K.SEQS_STABLE,
-                                    window=s.window)
+                timed("decode", i, lambda: K.gqa_append_decode(
+                    c, wl.block_table, wl.seq_lens, wl.max_seq_len, wl.pos,
+                    wl.k_new[layer], wl.v_new[layer], wl.q[layer],
+                    out=outs[layer], workspace=wss[layer], want_lse=False,
+                    seqs_flags=K.SEQS_STABLE, window=s.window))
     return step
 
 
-def run_sparse_schedule(K, wl, outs, wss, events=None):
+def run_sparse_schedule(K, wl, outs, wss, timed=None):
     s = wl.shape
+    if timed is None:
+        def timed(tag, i, fn):
+            fn()
     c = wl.caches[0]
-    K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
-    K.kv_append(wl.idx_cache, wl.block_table, wl.pos, wl.idx_k_new)
+
+    def appends():
+        K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
+        K.kv_append(wl.idx_cache, wl.block_table, wl.pos, wl.idx_k_new)
+    timed("append", 0, appends)
     idx = None
     pooled = False
+    n_sel = 0
     for layer in wl.layers:
         if s.modes[layer] == "reindex" and pooled:
             idx = wss["idx"][layer]
-            K.indexer_topk_pool(wl.idx_cache, wl.block_table, wl.seq_lens,
-                                wl.max_seq_len, wl.q_idx[layer], wl.w[layer],
-                                wss["pool"], wss["pool_n"], s.pool_k,
-                                indices=idx, workspace=wss["pooltopk"])
+            timed("select", n_sel, lambda: K.indexer_topk_pool(
+                wl.idx_cache, wl.block_table, wl.seq_lens, wl.max_seq_len,
+                wl.q_idx[layer], wl.w[layer], wss["pool"], wss["pool_n"],
+                s.pool_k, indices=wss["idx"][layer],
+                workspace=wss["pooltopk"]))
+            n_sel += 1
         elif s.modes[layer] != "reuse":
             idx = wss["idx"][layer]
-            K.indexer_topk(wl.idx_cache, wl.block_table, wl.seq_lens,
-                           wl.max_seq_len, wl.q_idx[layer], wl.w[layer],
-                           s.topk, indices=idx, workspace=wss["topk"])
+            timed("select", n_sel, lambda: K.indexer_topk(
+                wl.idx_cache, wl.block_table, wl.seq_lens, wl.max_seq_len,
+                wl.q_idx[layer], wl.w[layer], s.topk,
+                indices=wss["idx"][layer], workspace=wss["topk"]))
+            n_sel += 1
             if s.modes[layer] == "full" and s.pool_k and not pooled:
                 K.indexer_pool(wl.block_table, wl.seq_lens, wl.max_seq_len,
                                idx, pool=wss["pool"], pool_n=wss["pool_n"])
                 pooled = True
-        if events is not None:
-            events[layer][0].record()
-        K.sparse_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len, idx,
-                        wl.q[layer], out=outs[layer], workspace=wss[layer],
-                        want_lse=False)
-        if events is not None:
-            events[layer][1].record()
-
-
-def decode_only(K, wl, outs, wss, layer):
-    """The layer's attention call as the step issues it (GQA: the fused
-    append + decode; latent: the decode after its separate append)."""
-    s = wl.shape
-    c = wl.caches[layer]
-    if s.kind == "mla":
-        K.mla_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                     wl.q[layer], d_c=s.d_c, out=outs[layer],
-                     workspace=wss[layer], want_lse=False)
-    elif s.kind == "gqa":
-        K.gqa_append_decode(c, wl.block_table, wl.seq_lens, wl.max_seq_len,
-                            wl.pos, wl.k_new[layer], wl.v_new[layer],
-                            wl.q[layer], out=outs[layer],
-                            workspace=wss[layer], want_lse=False,
-                            seqs_flags=K.SEQS_STABLE, window=s.window)
+        sel = idx
+        timed("decode", layer, lambda: K.sparse_decode(
+            c, wl.block_table, wl.seq_lens, wl.max_seq_len, sel,
+            wl.q[layer], out=outs[layer], workspace=wss[layer],
+            want_lse=False))
 
 
 def pack_inputs(torch, wl):
@@ -496,6 +556,8 @@ def pack_inputs(torch, wl):
         if s.kind == "sparse" and layer in wl.q_idx:
             tensors.append(("q_idx", layer))
     total = sum(getattr(wl, n)[l].numel() for n, l in tensors)
+    if s.kind == "sparse":
+        total += wl.idx_k_new.numel()
     buf = torch.empty(total, dtype=torch.bfloat16, device=wl.block_table.device)
     off = 0
     for n, l in tensors:
@@ -506,9 +568,9 @@ def pack_inputs(torch, wl):
         off += t.numel()
     if s.kind == "sparse":
         t = wl.idx_k_new
-        extra = torch.empty_like(t)
-        extra.copy_(t)
-        wl.idx_k_new = extra
+        view = buf[off:off + t.numel()].view(t.shape)
+        view.copy_(t)
+        wl.idx_k_new = view
     return buf
 
 
@@ -535,15 +597,39 @@ def sparse_buffers(torch, K, wl, dev):
     return b
 
 
-def run_ours(args, ws, rank, local):
-    import torch
-    import kv_cache_decode_gqa_gb300 as K
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = dist_init(ws, "nccl")
-    shape = W.config(args.config)
-    wl = W.DeviceWorkload(shape, device=dev)
-    s = shape
+def config_dict(s, ws):
+    """The bench line's `config`: the workload, by name and sizes (both
+    arms print the same dict)."""
+    return {"workload": s.name, "batch": s.batch,
+            "cached_len": s.lengths[0] if len(set(s.lengths)) == 1
+            else f"{min(s.lengths)}..{max(s.lengths)}",
+            "layers": s.n_layers, "n_h": s.n_h, "n_kv": s.n_kv,
+            "head_dim": s.head_dim, "block_size": s.block_size,
+            "cache_dtype": s.dtype,
+            **({"window": s.window} if s.window else {}),
+            **({"topk": s.topk, "schedule": "/".join(s.modes)}
+               if s.kind == "sparse" else {}),
+            **({"pool_topk": s.pool_k} if s.pool_k else {}),
+            "parallelism": f"replicas x{ws}",
+            "l2": ("indexer keys (134 MB) and the selected rows read per "
+                   "step exceed L2; Reuse layers re-read rows their Full "
+                   "layer read; no flush" if s.kind == "sparse" else
+                   "working set per step larger than L2 (distinct per-layer "
+                   "caches, or one 2.4 GB latent cache); no flush")}
+
+
+def kernel_tag(s):
+    return {"gqa": "decode_simt" if s.n_h // s.n_kv <= 4 else "decode_mma",
+            "mla": "decode_mla", "sparse": "decode_sparse"}[s.kind] + \
+        "_" + s.name
+
+
+def measure(K, torch, name, args, ws, dist, dev, local):
+    """One workload: graph-captured steps, timed; end to end with host
+    copies; each call bracketed by events. Returns its record (rank 0) with
+    the step time as the max over ranks."""
+    s = W.config(name)
+    wl = W.DeviceWorkload(s, device=dev)
     outs = {l: torch.empty((s.batch, s.n_h, s.dv), dtype=torch.bfloat16,
                            device=dev) for l in wl.layers}
     wss = {}
@@ -562,22 +648,23 @@ def run_ours(args, ws, rank, local):
     if s.kind == "sparse":
         wss.update(sparse_buffers(torch, K, wl, dev))
     in_buf = pack_inputs(torch, wl)
-    out_buf_views = [outs[l] for l in wl.layers]
+    out_views = [outs[l] for l in wl.layers]
 
     step = build_step(K, wl, outs, wss)
     step()                                   # eager once: validates, warms
     torch.cuda.synchronize()
     if K.device_error() != 0:
-        raise RuntimeError("device error word set after the first step")
+        raise RuntimeError(f"{name}: device error word set after a step")
 
     stream = torch.cuda.Stream(device=dev)
     graph = torch.cuda.CUDAGraph()
+    n0 = K.launch_count()
     with torch.cuda.graph(graph, stream=stream):
         step()
+    launches_per_step = K.launch_count() - n0
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
-    # warm-up: W steps, then keep replaying ~1 s so clocks are sampled loaded
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -585,9 +672,10 @@ def run_ours(args, ws, rank, local):
         # the pooled Reindex layers' candidates (8 per pool block), for the
         # byte count; the pool is the same every step
         s.pool_cands = int(wss["pool_n"].sum().item()) * 8
-    t_end = time.perf_counter() + 1.0
+    # keep replaying for a moment so the clock samples see the load
+    t_end = time.perf_counter() + args.load_s
     while time.perf_counter() < t_end:
-        for _ in range(20):
+        for _ in range(10):
             graph.replay()
         torch.cuda.synchronize()
 
@@ -602,31 +690,30 @@ def run_ours(args, ws, rank, local):
     e1.record()
     torch.cuda.synchronize()
     barrier(dist)
-    ms = e0.elapsed_time(e1) / args.steps
     clock_info = clocks.stop()
-    ms = max_over_ranks(dist, ms, dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
 
     # ---- end to end: host inputs in, outputs out, every step
     pinned_in = torch.empty(in_buf.numel(), dtype=torch.bfloat16,
                             pin_memory=True)
     pinned_in.copy_(in_buf)
-    out_cat = torch.empty((len(out_buf_views),) + tuple(outs[wl.layers[0]].shape),
+    out_cat = torch.empty((len(out_views),) + tuple(out_views[0].shape),
                           dtype=torch.bfloat16, device=dev)
     pinned_out = torch.empty(out_cat.shape, dtype=torch.bfloat16,
                              pin_memory=True)
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
 
     def e2e_step():
         in_buf.copy_(pinned_in, non_blocking=True)
         graph.replay()
-        torch.stack(out_buf_views, out=out_cat)
+        torch.stack(out_views, out=out_cat)
         pinned_out.copy_(out_cat, non_blocking=True)
 
     for _ in range(max(args.warmup, 3)):
         e2e_step()
     torch.cuda.synchronize()
     barrier(dist)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
     e2.record()
     for _ in range(args.steps):
         e2e_step()
@@ -635,14 +722,44 @@ def run_ours(args, ws, rank, local):
     barrier(dist)
     ms_e2e = max_over_ranks(dist, e2.elapsed_time(e3) / args.steps, dev)
 
-    # ---- the dominant kernel, per launch, CUDA events on its stream
-    kern_ms = time_decode_kernel(torch, K, wl, outs, wss, args)
-    kern_ms = max_over_ranks(dist, kern_ms, dev)
-    if dist is not None:
-        dist.destroy_process_group()
-    if rank != 0:
-        return None
+    # ---- each call, CUDA events on its stream inside a captured step
+    calls = time_calls(torch, K, wl, outs, wss, args)
+    calls = {t: max_over_ranks(dist, v, dev) for t, v in calls.items()}
+    del graph
+    rec = None
+    if dist is None or dist.get_rank() == 0:
+        rec = record(s, ws, args, ms, ms_e2e, calls, clock_info,
+                     launches_per_step, in_buf.numel() * 2,
+                     out_cat.numel() * 2)
+    del wl, outs, wss, in_buf, out_views, pinned_in, pinned_out, out_cat
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
+
+def time_calls(torch, K, wl, outs, wss, args):
+    """Mean device time of each kind of call of a step (tag -> ms): the
+    calls are bracketed by event nodes in a captured step, and the last of
+    several replays is read."""
+    evs = {}
+    step = build_step(K, wl, outs, wss, events=evs)
+    step()                      # creates the events (eager, untimed)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        step()
+    for _ in range(max(args.warmup, 3) + args.steps):
+        g.replay()
+    torch.cuda.synchronize()
+    res = {t: statistics.mean(a.elapsed_time(b) for a, b in pairs)
+           for t, pairs in evs.items()}
+    del g
+    return res
+
+
+def record(s, ws, args, ms, ms_e2e, calls, clock_info, launches_per_step,
+           h2d, d2h):
+    """The JSON record of one workload."""
     nbytes = kv_bytes_step(s)
     value = ws * nbytes / (ms / 1e3) / 1e9
     peak, peak_src = measured_peaks()
@@ -654,14 +771,11 @@ def run_ours(args, ws, rank, local):
         call_ms = ms / s.n_layers
         timing = "timed step / layers (the step is this call per layer)"
     else:
-        call_ms = kern_ms
+        call_ms = calls["decode"]
         timing = "CUDA events around each call in a captured step"
     achieved = launch_bytes / (call_ms / 1e3) / 1e9
-    kern_tag = {"gqa": "decode_simt" if s.n_h // s.n_kv <= 4 else
-                "decode_mma", "mla": "decode_mla",
-                "sparse": "decode_sparse"}[s.kind] + "_" + s.name
-    launches_per_step = launches(s)
-    line = {
+    tag = kernel_tag(s)
+    rec = {
         "metric": METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
@@ -674,50 +788,50 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None,
         "dtype": s.dtype,
         "data": data_description(s),
-        "config": {"workload": s.name, "batch": s.batch,
-                   "cached_len": s.lengths[0] if len(set(s.lengths)) == 1
-                   else f"{min(s.lengths)}..{max(s.lengths)}",
-                   "layers": s.n_layers, "n_h": s.n_h, "n_kv": s.n_kv,
-                   "head_dim": s.head_dim, "block_size": s.block_size,
-                   "parallelism": f"replicas x{ws}",
-                   "l2": ("indexer keys (134 MB) and the selected rows read "
-                          "per step exceed L2; Reuse layers re-read rows "
-                          "their Full layer read; no flush"
-                          if s.kind == "sparse" else
-                          "working set per step larger than L2 (distinct "
-                          "per-layer caches); no flush")},
+        "config": config_dict(s, ws),
         "pct_of_peak": round(100 * value / ws / peak, 1),
         "pct_of_nominal_hbm": round(100 * value / ws / NOMINAL_HBM_GBS, 1),
         "tokens_per_s_per_layer": round(s.batch * s.n_layers / (ms / 1e3), 1),
         "kv_bytes_per_step": nbytes,
         "e2e": {"value": round(ws * nbytes / (ms_e2e / 1e3) / 1e9, 1),
-                "unit": "GB/s",
-                "h2d_bytes_per_step": in_buf.numel() * 2,
-                "d2h_bytes_per_step": out_cat.numel() * 2},
+                "unit": "GB/s", "ms_per_step": round(ms_e2e, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": kern_tag,
+        "gpu_launches_per_step": launches_per_step,
+        "roofline": {"bound": "hbm", "kernel": tag,
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "bytes_per_launch": launch_bytes,
                      "launch_ms": round(call_ms, 5),
                      "launch_timing": timing,
-                     "launch_ms_isolated": round(kern_ms, 5),
-                     "traffic": profile_traffic(kern_tag)},
+                     "launch_ms_isolated": round(calls["decode"], 5),
+                     "traffic": profile_traffic(tag)},
+        "calls_ms": {t: round(v, 5) for t, v in calls.items()},
         "clocks": clock_info,
     }
     if s.kind == "mla":
         # the latent decode runs on the tensor cores: its tensor-side rate
         # against the measured bf16 peak (burst: the kernel is timed alone)
         useful, issued = latent_flops(s)
+        kern_ms = calls["decode"]
         tpk, tsrc = measured_peaks("bf16_tflops")
-        line["roofline"]["tensor"] = {
+        rec["roofline"]["tensor"] = {
             "useful_tflops": round(useful / (kern_ms / 1e3) / 1e12, 1),
             "issued_tflops": round(issued / (kern_ms / 1e3) / 1e12, 1),
             "peak": tpk, "peak_source": tsrc, "unit": "TFLOP/s",
+            "frac_useful": round(useful / (kern_ms / 1e3) / 1e12 / tpk, 4),
             "frac_issued": round(issued / (kern_ms / 1e3) / 1e12 / tpk, 4),
             "flops_per_launch": {"useful": useful, "issued": issued}}
-    return line
+    if s.kind == "sparse" and "select" in calls:
+        # the indexer + top-k call of a Full / Reindex layer, beside it
+        sel_bytes = sum(s.seq_lens) * s.idx_dim * 2
+        rec["select_call"] = {
+            "ms": round(calls["select"], 5),
+            "indexer_bytes_full_layer": sel_bytes,
+            "note": "mean over the schedule's indexer + top-k calls (the "
+                    "Full layer's reads every visible indexer key)"}
+    return rec
 
 
 def profile_run(args, local):
@@ -743,72 +857,6 @@ def profile_run(args, local):
                       "device_error": K.device_error()}))
 
 
-def launches(s):
-    """Kernels the library launches per step. GQA: the fused append + decode
-    and its split merge per layer; latent: append, decode and merge per
-    layer; sparse: two appends, indexer score + select per Full/Reindex
-    layer, gather decode + merge per layer. (Every workload here is split
-    over several CTAs, so every decode has its merge launch.)"""
-    if s.kind == "sparse":
-        sel = sum(1 for m in s.modes if m != "reuse")
-        return 2 + 2 * sel + 2 * s.n_layers + (1 if s.pool_k else 0)
-    if s.kind == "mla":
-        return 3 * s.n_layers
-    return 2 * s.n_layers
-
-
-def time_decode_kernel(torch, K, wl, outs, wss, args):
-    """Average device time of one decode launch. With graph-capturable
-    timing events, the decode launches are bracketed by event nodes in a
-    captured step and the last of K replays is read; otherwise the launches
-    are issued eagerly behind a short GPU sleep that keeps the host ahead."""
-    s = wl.shape
-    layers = wl.layers
-    try:
-        evs = {l: (torch.cuda.Event(enable_timing=True, external=True),
-                   torch.cuda.Event(enable_timing=True, external=True))
-               for l in layers}
-        g = torch.cuda.CUDAGraph()
-        st = torch.cuda.Stream()
-        with torch.cuda.graph(g, stream=st):
-            if s.kind == "sparse":
-                run_sparse_schedule(K, wl, outs, wss, events=evs)
-            else:
-                for l in layers:
-                    c = wl.caches[l]
-                    if s.kind == "mla":
-                        K.kv_append(c, wl.block_table, wl.pos, wl.k_new[l])
-                    evs[l][0].record()
-                    decode_only(K, wl, outs, wss, l)
-                    evs[l][1].record()
-        for _ in range(max(args.warmup, 3)):
-            g.replay()
-        torch.cuda.synchronize()
-        for _ in range(args.steps):
-            g.replay()
-        torch.cuda.synchronize()
-        return statistics.mean(evs[l][0].elapsed_time(evs[l][1])
-                               for l in layers)
-    except TypeError:
-        pass
-    # eager fallback
-    evs = {l: (torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for l in layers}
-    times = []
-    for _ in range(3):
-        torch.cuda._sleep(20_000_000)
-        if s.kind == "sparse":
-            run_sparse_schedule(K, wl, outs, wss, events=evs)
-        else:
-            for l in layers:
-                evs[l][0].record()
-                decode_only(K, wl, outs, wss, l)
-                evs[l][1].record()
-        torch.cuda.synchronize()
-        times += [evs[l][0].elapsed_time(evs[l][1]) for l in layers]
-    return statistics.mean(times)
-
-
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -816,42 +864,56 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return None
     s = W.config(args.config)
-    budget = max(1.0, min(10.0, 120.0 / max(args.steps + args.warmup, 1)))
-    vals = []
-    cores, sample = 1, ""
-    for i in range(args.warmup + args.steps):
-        v, cores, sample = cpu_baseline(args.config, budget_s=budget)
+    n = args.warmup + args.steps
+    budget = max(1.0, min(8.0, 120.0 / max(n, 1)))
+    vals, last = [], None
+    for i in range(n):
+        last = cpu_baseline(args.config, budget_s=budget,
+                            budget_1=max(0.5, budget / 4))
         if i >= args.warmup:
-            vals.append(v)
+            vals.append(last["value"])
     value = statistics.mean(vals) if vals else 0.0
     nbytes = kv_bytes_step(s)
     ms = nbytes / (value * 1e9) * 1e3 if value > 0 else None
+    cpu = dict(last)
+    cpu["value"] = round(value, 4)
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3) if ms else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic (same seeded inputs)",
-        "config": {"workload": s.name, "batch": s.batch,
-                   "layers": s.n_layers},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
-                         "cores": cores, "kind": "oracle", "sample": sample},
+        "dtype": "f64", "data": data_description(s),
+        "config": config_dict(s, ws),
+        "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
+HEADLINE = "llama31_70b_gqa"
+SUB_CONFIGS = ["llama2_7b_mha", "llama31_70b_gqa_fp8", "mla", "sparse",
+               "sparse_pool", "llama2_7b_mha_mxfp4",
+               "llama31_70b_gqa_fp8_swa"]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="llama2_7b_mha", choices=W.CONFIGS)
+    ap.add_argument("--config", default=HEADLINE, choices=W.CONFIGS,
+                    help="the headline workload (top-level fields)")
+    ap.add_argument("--sub-configs", default=",".join(SUB_CONFIGS),
+                    help="comma-separated workloads reported under "
+                         "`configs` in the same line ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for profiler runs)")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=4.0)
+    ap.add_argument("--load-s", type=float, default=0.4,
+                    help="seconds of untimed replays before each timed "
+                         "region, so clock samples see the load")
     ap.add_argument("--profile-run", action="store_true",
                     help="only run warmup + steps eager steps (for ncu)")
     ap.add_argument("--layers", type=int, default=0,
@@ -870,16 +932,41 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    # the oracle's process pool is spawned before this process touches the GPU
-    cpu = None
+    subs = [c for c in args.sub_configs.split(",") if c and c != args.config]
+    for c in subs:
+        if c not in W.CONFIGS:
+            ap.error(f"unknown workload {c}")
+    names = [args.config] + subs
+    # the oracle's process pools are spawned before this process touches
+    # the GPU
+    cpu = {}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline(args.config, args.cpu_budget)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
-               "kind": "oracle", "sample": sample}
-    line = run_ours(args, ws, rank, local)
-    if line is not None:
-        line["cpu_baseline"] = cpu
-        print(json.dumps(line), flush=True)
+        for c in names:
+            cpu[c] = cpu_baseline(c, args.cpu_budget,
+                                  max(1.0, args.cpu_budget / 2.5))
+    import torch
+    import kv_cache_decode_gqa_gb300 as K
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(ws, "nccl")
+    recs = {}
+    for c in names:
+        recs[c] = measure(K, torch, c, args, ws, dist, dev, local)
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = dict(recs[args.config])
+    line["cpu_baseline"] = cpu.get(args.config)
+    line["configs"] = {}
+    for c in subs:
+        r = dict(recs[c])
+        r["cpu_baseline"] = cpu.get(c)
+        line["configs"][c] = r
+    # every launch of the line's timed regions, the sub-records' included
+    line["gpu_launches_all_configs"] = sum(r["gpu_launches"]
+                                           for r in recs.values())
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -499,6 +499,15 @@ kvd_status kvd_device_error(int32_t *code);
 
 int32_t kvd_version(void);
 
+/*
+ * kvd_launch_count -- kernels this library has launched in this process so
+ * far (every device and host thread). A launch recorded into a CUDA graph
+ * under stream capture counts once, when it is recorded, so the count
+ * across a capture is the kernels one replay runs. A diagnostic for
+ * counting a step's kernels; the pages have no counterpart.
+ */
+uint64_t kvd_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = ["PagedCache", "kv_append", "gqa_decode", "mla_decode",
            "indexer_topk", "indexer_pool", "indexer_topk_pool",
            "BlockPool", "copy_blocks",
            "sparse_decode", "workspace_size",
-           "bytes_per_token", "device_error", "KvdError",
+           "bytes_per_token", "device_error", "launch_count", "KvdError",
            "OP_GQA_DECODE", "OP_MLA_DECODE", "OP_INDEXER_TOPK",
            "OP_SPARSE_DECODE"]
 
@@ -416,6 +416,12 @@ def bytes_per_token(n_l, n_kv, d_h, elem_bytes):
 # device error bits (KVD_DEVERR_* in kvd.h)
 DEVERR_BLOCK, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_LEN = (
     1, 2, 4, 8, 16)
+
+
+def launch_count():
+    """Kernels the library has launched in this process (a launch captured
+    into a CUDA graph counts once, when captured)."""
+    return int(lib().kvd_launch_count())
 
 
 def device_error():

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "kvd.h"
@@ -300,6 +301,12 @@ kvd_status launched(cudaError_t e, const char *what) {
 }  // namespace
 
 namespace kvd {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 // Workspace layout of a gqa_decode call with these arguments on the current
 // device: total bytes, and the byte range of the arrival counters (the only
 // part that must be zero when a call starts). Used by the no-allocation
@@ -344,6 +351,10 @@ kvd_status set_error(kvd_status st, const char *msg) {
 extern "C" {
 
 int32_t kvd_version(void) { return KVD_VERSION; }
+
+uint64_t kvd_launch_count(void) {
+  return kvd::g_launches.load(std::memory_order_relaxed);
+}
 
 const char *kvd_last_error(void) { return g_msg; }
 

@@ -63,7 +63,9 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 // ---------------------------------------------------------------------------

@@ -113,6 +113,9 @@ struct PoolParams {
   int *err;
 };
 
+// Count one kernel launch of the library (kvd_launch_count, api.cu).
+void note_launch();
+
 // Launchers. Each returns the launch error (cudaSuccess if queued).
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 // The pool of a Full layer's selection (one CTA per sequence).
