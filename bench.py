@@ -490,12 +490,14 @@ def build_step(K, wl, outs, wss, events=None):
                     workspace=wss[layer], want_lse=False))
             else:
                 # the append rides in the decode's pass over the cache; the
-                # lengths and block tables are set before the step
+                # lengths and block tables are set before the step, and the
+                # rows before the newest were appended by earlier steps
                 timed("decode", i, lambda: K.gqa_append_decode(
                     c, wl.block_table, wl.seq_lens, wl.max_seq_len, wl.pos,
                     wl.k_new[layer], wl.v_new[layer], wl.q[layer],
                     out=outs[layer], workspace=wss[layer], want_lse=False,
-                    seqs_flags=K.SEQS_STABLE, window=s.window))
+                    seqs_flags=K.SEQS_STABLE | K.SEQS_PREFIX_READY,
+                    window=s.window))
     return step
 
 

@@ -35,9 +35,10 @@
  * processed by separate CTAs and merge the partial results (log-sum-exp
  * merge). The caller passes the scratch for the partials: at least
  * kvd_workspace_size() bytes, 256-byte aligned, zero-filled once before its
- * first use. It also holds arrival counters that every call leaves at zero,
- * so a workspace can be reused by later calls on the same stream without
- * clearing; two calls that may run at the same time need two workspaces.
+ * first use. Every partial result a call keeps there is written before
+ * the call reads it, so a workspace can be reused by later calls on the
+ * same stream without clearing; two calls that may run at the same time
+ * need two workspaces.
  *
  * Paged layout ("KV cache", "The allocator, not the algorithm"; the paging
  * of the My Weird Prompts 640482 transcript): a cache is a pool of fixed-size
@@ -141,7 +142,8 @@ typedef struct kvd_cache {
  *                 plan and the workspace. Must be <= max_blocks_per_seq *
  *                 block_size (else KVD_ERR_CAPACITY). A device length above
  *                 it is clamped to it and flagged KVD_DEVERR_LEN.
- *   flags         0, or KVD_SEQS_STABLE (other bits: KVD_ERR_SHAPE)
+ *   flags         0, KVD_SEQS_STABLE, or KVD_SEQS_STABLE |
+ *                 KVD_SEQS_PREFIX_READY (other bits: KVD_ERR_SHAPE)
  *   window        0 (every visible position), or W > 0: sliding-window
  *                 decode ("890 bytes a token", section 7, SWA bounded
  *                 replay, n_win = 128; "KV cache" on local-attention
@@ -163,8 +165,22 @@ typedef struct kvd_cache {
  * are set by host copies at the start of a decode step and read by every
  * layer). kvd_gqa_decode and kvd_gqa_append_decode then read them, and plan
  * their work, while that kernel finishes. Other calls ignore the flag.
+ *
+ * KVD_SEQS_PREFIX_READY (only with KVD_SEQS_STABLE) declares as well that
+ * every cache row the call reads at a position below seq_lens[b] - 1
+ * already holds its final value when the kernel launched just before this
+ * call starts, and that no kernel still running writes it: only the newest
+ * position, seq_lens[b] - 1, may be written by that kernel (a kv_append of
+ * this step), or by kvd_gqa_append_decode itself. That holds in a decode
+ * step, where older rows were appended by earlier steps; it does not hold
+ * right after kvd_copy_blocks, which writes older rows. kvd_gqa_decode and
+ * kvd_gqa_append_decode may then start copying those rows while that
+ * kernel finishes (the query rows, and everything written, still wait for
+ * it); the CUDA-core kernel (query groups of 1, 2 or 4) does. Other calls
+ * ignore the flag.
  */
 #define KVD_SEQS_STABLE 1
+#define KVD_SEQS_PREFIX_READY 2
 typedef struct kvd_seqs {
   const int32_t *block_table;
   const int32_t *seq_lens;
@@ -221,8 +237,7 @@ kvd_status kvd_kv_append(const kvd_cache *cache, const int32_t *block_table,
  *   lse       device fp32 [batch][n_h], natural-log log-sum-exp of the
  *             scaled scores (-inf for an empty sequence); may be NULL
  *   workspace device scratch of at least kvd_workspace_size(KVD_OP_GQA_DECODE)
- *             bytes, 256-byte aligned, zero-filled before its first use (see
- *             "Workspace" above)
+ *             bytes, 256-byte aligned (see "Workspace" above)
  * Supported: bf16 or fp8 cache, head_dim 64 or 128, n_h / n_kv in
  * {1, 2, 4, 8, 16} (8 and 16 need head_dim 128 and a block_size that is a
  * multiple of 64 or one of 16, 32); an MXFP4 cache with head_dim 128 and
@@ -281,7 +296,8 @@ kvd_status kvd_gqa_append_decode(const kvd_cache *cache, const kvd_seqs *seqs,
  *   The first call on each device looks up the array's device address with
  *   that device current; make that first call before any stream capture.
  *   Every call uses the same array, and it keeps the last call's contents
- *   (the call clears the part that must start at zero, in stream order).
+ *   (nothing in it needs to start at zero: each call writes every partial
+ *   result before reading it).
  *   Calls whose work can overlap on the GPU -- on different streams or from
  *   different host threads -- race on the array and give wrong results;
  *   serialise them, or use kvd_gqa_decode with separate workspaces.
@@ -498,6 +514,21 @@ const char *kvd_last_error(void);
 kvd_status kvd_device_error(int32_t *code);
 
 int32_t kvd_version(void);
+
+/*
+ * kvd_set_tuning -- process-wide overrides of the library's launch choices,
+ * for tests and experiments (the pages have no counterpart).
+ *   decode_ctas     > 0: every decode launch uses this many CTAs (the split
+ *                   plan and kvd_workspace_size follow it); 0: the default,
+ *                   one per SM
+ *   mla_cuda_cores  != 0: kvd_mla_decode runs its CUDA-core kernel even
+ *                   where the tcgen05 kernel applies; 0: the default
+ * Their starting values come from the environment variables
+ * KVD_DECODE_CTAS and KVD_MLA_CUDA_CORES, read once when the library is
+ * loaded. A workspace sized before a change may be too small after it.
+ * Errors: KVD_ERR_SHAPE (decode_ctas < 0).
+ */
+kvd_status kvd_set_tuning(int32_t decode_ctas, int32_t mla_cuda_cores);
 
 /*
  * kvd_launch_count -- kernels this library has launched in this process so

@@ -22,7 +22,8 @@ __all__ = ["PagedCache", "kv_append", "gqa_decode", "mla_decode",
            "indexer_topk", "indexer_pool", "indexer_topk_pool",
            "BlockPool", "copy_blocks",
            "sparse_decode", "workspace_size",
-           "bytes_per_token", "device_error", "launch_count", "KvdError",
+           "bytes_per_token", "device_error", "launch_count", "set_tuning",
+           "KvdError",
            "OP_GQA_DECODE", "OP_MLA_DECODE", "OP_INDEXER_TOPK",
            "OP_SPARSE_DECODE"]
 
@@ -104,6 +105,7 @@ class PagedCache:
 
 
 SEQS_STABLE = 1  # KVD_SEQS_STABLE
+SEQS_PREFIX_READY = 2  # KVD_SEQS_PREFIX_READY (with SEQS_STABLE)
 
 
 def _seqs(block_table, seq_lens, max_seq_len, flags=0, window=0,
@@ -137,7 +139,8 @@ def _workspace(op, cache, block_table, seq_lens, max_seq_len, n_h, k,
         _need(workspace, "workspace", torch.uint8)
         return workspace
     n = workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k)
-    # zero-filled once: the library keeps its arrival counters at zero
+    # zero-filled once: every completed call leaves its arrival counters at
+    # zero
     return torch.zeros(max(n, 256), dtype=torch.uint8,
                        device=block_table.device)
 
@@ -416,6 +419,13 @@ def bytes_per_token(n_l, n_kv, d_h, elem_bytes):
 # device error bits (KVD_DEVERR_* in kvd.h)
 DEVERR_BLOCK, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_LEN = (
     1, 2, 4, 8, 16)
+
+
+def set_tuning(decode_ctas=0, mla_cuda_cores=False):
+    """Process-wide launch overrides (kvd_set_tuning): decode_ctas > 0
+    forces the CTAs of every decode launch; mla_cuda_cores runs the latent
+    decode on its CUDA-core kernel."""
+    check(lib().kvd_set_tuning(int(decode_ctas), int(bool(mla_cuda_cores))))
 
 
 def launch_count():

@@ -47,6 +47,7 @@ _PSEQS = ctypes.POINTER(KvdSeqs)
 _SIGS = {
     "kvd_version": (c_int32, []),
     "kvd_launch_count": (ctypes.c_uint64, []),
+    "kvd_set_tuning": (c_int32, [c_int32, c_int32]),
     "kvd_last_error": (ctypes.c_char_p, []),
     "kvd_status_string": (ctypes.c_char_p, [c_int32]),
     "kvd_bytes_per_token": (ctypes.c_uint64, [c_int32] * 4),

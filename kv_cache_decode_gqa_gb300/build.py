@@ -20,6 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 
 LIB_SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "noalloc.cu",
                "decode_mma.cu", "decode_wide.cu", "decode_latent_tc.cu",
+               "decode_gather_tc.cu",
                "indexer.cu", "block_pool.cu"]
 INPUTS_SOURCES = ["inputs_fill.cu"]
 LIB = os.path.join(PKG, "libkvd.so")

@@ -79,6 +79,11 @@ int env_int(const char *name, int dflt) {
   return std::atoi(s);
 }
 
+// Tuning overrides (kvd_set_tuning): read from the environment once, when
+// the library is loaded, and changed only by kvd_set_tuning.
+std::atomic<int> g_decode_ctas{env_int("KVD_DECODE_CTAS", 0)};
+std::atomic<int> g_mla_cuda_cores{env_int("KVD_MLA_CUDA_CORES", 0)};
+
 // ---------------------------------------------------------------------------
 // validation
 // ---------------------------------------------------------------------------
@@ -134,9 +139,12 @@ kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
                 "required", what);
   if (s->batch > 65535)
     return fail(KVD_ERR_SHAPE, "%s: batch %d above 65535", what, s->batch);
-  if (s->flags & ~KVD_SEQS_STABLE)
+  if (s->flags & ~(KVD_SEQS_STABLE | KVD_SEQS_PREFIX_READY))
     return fail(KVD_ERR_SHAPE, "%s: unknown seqs flags 0x%x", what,
                 (unsigned)s->flags);
+  if ((s->flags & KVD_SEQS_PREFIX_READY) && !(s->flags & KVD_SEQS_STABLE))
+    return fail(KVD_ERR_SHAPE, "%s: KVD_SEQS_PREFIX_READY needs "
+                "KVD_SEQS_STABLE", what);
   if (s->batch > 0 && (!s->block_table || !s->seq_lens))
     return fail(KVD_ERR_NULL, "%s: block_table and seq_lens are required", what);
   if (s->window < 0)
@@ -155,10 +163,10 @@ kvd_status check_seqs(const kvd_seqs *s, const kvd_cache *c, const char *what) {
 struct Plan {
   int split_len = kvd::kStageRows;
   int n_splits = 1;
-  int n_groups = 1;        // counters per sequence
+  int n_groups = 1;        // head groups (tiles) per sequence
   size_t ws_o_bytes = 0;   // partial outputs
   size_t ws_lse_bytes = 0; // partial log-sum-exps
-  size_t ws_bytes = 0;     // + arrival counters
+  size_t ws_bytes = 0;     // total
   int hp = 1;              // kv heads per work unit (CUDA-core GQA kernel)
 };
 
@@ -190,22 +198,21 @@ kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
 
 // Persistent stream-K plan of the dense GQA kernels: `ctas_per_sm` CTAs per
 // SM (never more CTAs than 64-token chunks), each leaving at most two
-// partials of G heads x head_dim; one arrival counter per (sequence, kv head).
+// partials of G heads x head_dim, which the merge launch combines.
 Plan plan_stream_k(int sms, int ctas_per_sm, int batch, int n_kv, int g,
                    int d, int max_seq_len) {
   Plan pl;
   const long chunks = (long)batch * n_kv *
                       ((max_seq_len + kvd::kStageRows - 1) / kvd::kStageRows);
   long ctas = (long)sms * ctas_per_sm;
-  const int forced = env_int("KVD_DECODE_CTAS", 0);
+  const int forced = g_decode_ctas.load(std::memory_order_relaxed);
   if (forced > 0) ctas = forced;
   ctas = std::max(1L, std::min(ctas, std::max(chunks, 1L)));
   pl.n_splits = (int)ctas;
   pl.n_groups = n_kv;
   pl.ws_o_bytes = round_up((size_t)ctas * 2 * g * d * 4, 256);
   pl.ws_lse_bytes = round_up((size_t)ctas * 2 * g * 4, 256);
-  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
-                round_up((size_t)batch * n_kv * 4, 256);
+  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
   return pl;
 }
 
@@ -223,10 +230,9 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
   return pl;
 }
 
-// Persistent stream-K plan of the 64-head-tile kernels (latent and sparse
-// decode): 32-position chunks of `rows` positions (or index entries) per
-// sequence and head tile; partials of 64 heads x dv per CTA side; one
-// arrival counter per (sequence, head tile).
+// Persistent stream-K plan of the latent decode kernels: 32-position (or
+// 64-position) chunks of `rows` positions per sequence and head tile;
+// partials of 64 heads x dv per CTA side, merged by a second launch.
 // `per_lane` CTAs of the launch share a lane's chunk range (one per head
 // tile, or per head tile and value quarter for the tensor-core latent
 // kernel); n_splits counts 64-head tiles per lane whatever the kernel.
@@ -237,7 +243,7 @@ Plan plan_wide(int sms, int batch, int n_h, int rows, int dv,
   if (per_lane <= 0) per_lane = tiles;
   const long chunks = (long)batch * ((rows + chunk_rows - 1) / chunk_rows);
   long ctas = sms;
-  const int forced = env_int("KVD_DECODE_CTAS", 0);
+  const int forced = g_decode_ctas.load(std::memory_order_relaxed);
   if (forced > 0) ctas = forced;
   const long lanes =
       std::max(1L, std::min(ctas / per_lane, std::max(chunks, 1L)));
@@ -246,15 +252,14 @@ Plan plan_wide(int sms, int batch, int n_h, int rows, int dv,
   pl.n_groups = tiles;
   pl.ws_o_bytes = round_up((size_t)ctas * 2 * 64 * dv * 4, 256);
   pl.ws_lse_bytes = round_up((size_t)ctas * 2 * 64 * 4, 256);
-  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes +
-                round_up((size_t)batch * tiles * 4, 256);
+  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
   return pl;
 }
 
 // The latent decode runs on the tcgen05 kernel where its shape allows
-// (KVD_MLA_CUDA_CORES=1 selects the CUDA-core kernel everywhere).
+// (kvd_set_tuning can select the CUDA-core kernel everywhere).
 bool mla_on_tensor_memory(const kvd_cache *c, int n_h) {
-  return env_int("KVD_MLA_CUDA_CORES", 0) == 0 &&
+  return g_mla_cuda_cores.load(std::memory_order_relaxed) == 0 &&
          kvd::latent_tc_supported(n_h, c->block_size, c->num_blocks);
 }
 
@@ -264,8 +269,26 @@ Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms, bool tc) {
             : plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
 }
 
+// The tcgen05 gather kernel: clusters of kGatherCluster CTAs, G per
+// (sequence, 64-head tile), as many as one wave of resident clusters holds.
+// With G > 1 each cluster leaves one merged slice per CTA (64 heads x
+// 512 / kGatherCluster values fp32 + 64 lse) for the merge launch.
 Plan sparse_plan(const kvd_seqs *s, int n_h, int k, int dv, int sms) {
-  return plan_wide(sms, s->batch, n_h, k, dv);
+  Plan pl;
+  const int units = std::max(s->batch * (n_h / 64), 1);
+  const int C = kvd::kGatherCluster;
+  int wave = kvd::gather_tc_max_clusters();
+  if (wave <= 0) wave = sms / C;
+  int G = kvd::gather_tc_clusters(units, std::max(k, 1), wave);
+  const int forced = g_decode_ctas.load(std::memory_order_relaxed);
+  if (forced > 0) G = std::min(std::max(1, forced / (units * C)), 4);
+  pl.n_splits = G;
+  pl.n_groups = C;
+  const size_t slots = (size_t)units * G * C;
+  pl.ws_o_bytes = G > 1 ? round_up(slots * 64 * (dv / C) * 4, 256) : 0;
+  pl.ws_lse_bytes = G > 1 ? round_up(slots * 64 * 4, 256) : 0;
+  pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
+  return pl;
 }
 
 size_t topk_ws_bytes(const kvd_seqs *s) {
@@ -307,14 +330,11 @@ std::atomic<unsigned long long> g_launches{0};
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-// Workspace layout of a gqa_decode call with these arguments on the current
-// device: total bytes, and the byte range of the arrival counters (the only
-// part that must be zero when a call starts). Used by the no-allocation
-// entry point.
-kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
-                                int32_t n_h, size_t *total,
-                                size_t *counters_offset,
-                                size_t *counters_bytes) {
+// Workspace bytes of a gqa_decode call with these arguments on the current
+// device (validating them as the call does). Used by the no-allocation entry
+// point.
+kvd_status gqa_workspace_bytes(const kvd_cache *cache, const kvd_seqs *seqs,
+                               int32_t n_h, size_t *total) {
   kvd_status st = check_cache(cache, true, "gqa_decode");
   if (st != KVD_OK) return st;
   st = check_seqs(seqs, cache, "gqa_decode");
@@ -325,10 +345,7 @@ kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
   const DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != KVD_OK) return st;
-  const Plan pl = gqa_plan(cache, seqs, n_h, d->sms, kind);
-  *total = pl.ws_bytes;
-  *counters_offset = pl.ws_o_bytes + pl.ws_lse_bytes;
-  *counters_bytes = pl.ws_bytes - *counters_offset;
+  *total = gqa_plan(cache, seqs, n_h, d->sms, kind).ws_bytes;
   return KVD_OK;
 }
 
@@ -351,6 +368,14 @@ kvd_status set_error(kvd_status st, const char *msg) {
 extern "C" {
 
 int32_t kvd_version(void) { return KVD_VERSION; }
+
+kvd_status kvd_set_tuning(int32_t decode_ctas, int32_t mla_cuda_cores) {
+  if (decode_ctas < 0)
+    return fail(KVD_ERR_SHAPE, "set_tuning: decode_ctas must be >= 0");
+  g_decode_ctas.store(decode_ctas, std::memory_order_relaxed);
+  g_mla_cuda_cores.store(mla_cuda_cores != 0, std::memory_order_relaxed);
+  return ok();
+}
 
 uint64_t kvd_launch_count(void) {
   return kvd::g_launches.load(std::memory_order_relaxed);
@@ -540,8 +565,6 @@ kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
   p.ws_o = static_cast<float *>(workspace);
   p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                        pl.ws_o_bytes);
-  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
-                                       pl.ws_o_bytes + pl.ws_lse_bytes);
   p.n_groups = pl.n_groups;
   p.batch = seqs->batch;
   p.n_h = n_h;
@@ -572,6 +595,7 @@ kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
   return launched(e, "gqa_decode");
 }
 }  // namespace
+
 
 extern "C" {
 
@@ -634,8 +658,6 @@ kvd_status kvd_mla_decode(const kvd_cache *latent, int32_t d_c,
   p.ws_o = static_cast<float *>(workspace);
   p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                        pl.ws_o_bytes);
-  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
-                                       pl.ws_o_bytes + pl.ws_lse_bytes);
   p.n_groups = pl.n_groups;
   p.batch = seqs->batch;
   p.n_h = n_h;
@@ -700,8 +722,6 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.ws_o = static_cast<float *>(workspace);
   p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                        pl.ws_o_bytes);
-  p.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) +
-                                       pl.ws_o_bytes + pl.ws_lse_bytes);
   p.n_groups = pl.n_groups;
   p.batch = seqs->batch;
   p.n_h = n_h;
@@ -717,7 +737,7 @@ kvd_status kvd_sparse_decode(const kvd_cache *cache, const kvd_seqs *seqs,
   p.scale_log2 = log2_scale(scale, cache->head_dim);
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return launched(kvd::launch_decode_sparse(p, s), "sparse_decode");
+  return launched(kvd::launch_decode_sparse_tc(p, s), "sparse_decode");
 }
 
 }  // extern "C"

@@ -1,0 +1,790 @@
+// Top-k sparse decode on the 5th-generation tensor cores ("890 bytes a
+// token ...", section 3: a Reuse layer attends to the selection an earlier
+// layer made; the My Weird Prompts 640482 transcript on DeepSeek Sparse
+// Attention: only the top-k positions of the cache are read). Each
+// sequence's query heads (n_kv = 1) attend to the k cached rows an index
+// list names; K and V rows are 512 wide and stored apart.
+//
+// The scores are computed transposed, S^T = K Q^T: the gathered positions
+// are the MMA's M (128 per chunk, the shape whose tensor-memory layout is
+// one row per lane) and a tile of 64 query heads its N, so no M row is
+// padding. The output is transposed too, O^T = V^T P^T: 4 MMAs of M = 128
+// value columns and N = 64 heads per 16 positions, accumulated in tensor
+// memory (4 x 64 columns). Each gathered byte is copied into shared memory
+// once and read by one MMA; the query tile is a 64 KB B operand loaded once.
+//
+// Rows are gathered with 16-byte cp.async pieces, placed in the MMA's
+// 128-byte-swizzled layout by the address each piece is given (a row that
+// is not attended -- an entry out of the CTA's share, a negative entry, one
+// at or past the length, a bad block id -- is filled with zeros). Measured
+// on this GPU: TMA tile::gather4 (four 128-byte rows per instruction)
+// delivered about 13 GB/s per SM for these random rows, the cp.async
+// pieces about twice that with two slices in flight per CTA and more with
+// four; a bulk copy per row lands unswizzled, which the MMA cannot read.
+//
+// Work: a unit is (sequence, 64-head tile) with k index entries. A cluster
+// of 4 CTAs takes a unit, G clusters per unit when there are few units, as
+// many as one wave of resident clusters holds; CTA q of cluster g takes an
+// equal share of the entries, in chunks of 128. The four CTAs' results are
+// merged in distributed shared memory: each CTA leaves its unnormalised O^T,
+// running maxima and sums in its own shared memory, and CTA q merges value
+// columns [128 q, 128 q + 128) of all four (log-sum-exp merge). With G > 1
+// each cluster's merged slices go to the workspace, and a short second
+// launch merges the G slices of every output.
+//
+// Warp roles (192 threads; at most two warps per SM sub-partition, so a
+// thread may hold up to 255 registers):
+//   warp 0: the query tile, by tiled TMA (eight 64 x 64 boxes).
+//   warp 1: tensor memory; the MMA loop (one elected lane issues): S^T of a
+//     chunk as 32 k-steps (A = K slice, K-major; B = the query tile,
+//     K-major), then O^T += V^T P^T as 4 value blocks x 8 k-steps (A = V
+//     slice, MN-major; B = P, MN-major).
+//   warps 2-5: workers. Per chunk each thread resolves one row (index
+//     entry -> position -> block table -> cache row); worker w copies K
+//     slice w (dims 128 w ..) into ring slot w, and V slice w (values
+//     128 w ..) into the same slot once the scores have read it, so four
+//     32 KB slices are in flight per CTA. Then the softmax, one thread per
+//     position (tensor-memory lane): a thread reads its position's 64
+//     scores; per-head maxima and sums over
+//     the chunk's 128 positions are reduce-scatters across the warp (62
+//     shuffles for 64 heads) and four warps in shared memory. Each thread
+//     writes its position's row of P (bf16) into the swizzled P tile, and
+//     rescales the tensor-memory O^T columns of heads whose maximum grew.
+#include <cmath>
+#include <mutex>
+
+#include "kvd_common.cuh"
+#include "stream_k.cuh"
+#include "tcgen05.cuh"
+#include "tmap.h"
+
+namespace kvd {
+namespace {
+
+constexpr int kH = 64;            // query heads per unit (MMA N)
+constexpr int kD = 512;           // key and value width
+constexpr int kRows = 128;        // positions per chunk (MMA M of S^T)
+constexpr int kSliceCols = 128;   // dims (K) or values (V) per ring slice
+constexpr int kSlicesPerChunk = 2 * kD / kSliceCols;  // 8: 4 of K, 4 of V
+constexpr int kCBBytes = kRows * 128;                 // a 64-column block
+constexpr int kSlotBytes = kRows * kSliceCols * 2;    // 32 KB
+constexpr int kNSlot = 4;
+constexpr int kQCB = kH * 128;                        // Q: one column block
+constexpr int kQBytes = kH * kD * 2;                  // 64 KB
+constexpr int kPBytes = kRows * kH * 2;               // 16 KB
+constexpr int kCluster = kGatherCluster;              // 4
+constexpr int kSliceV = kD / kCluster;                // merged values / CTA
+constexpr int kMaxG = 4;                              // clusters per unit
+constexpr int kMmaWarp = 1;
+constexpr int kSoft0 = 2;                             // first softmax warp
+constexpr int kThreads = 6 * 32;
+constexpr int kSoftBar = 1;                           // softmax warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;     // S^T: 128 lanes (positions) x 64 heads
+constexpr uint32_t kColO = 64;    // O^T: 4 blocks x (128 values x 64 heads)
+
+// shared memory
+constexpr int Q_OFF = 0;
+constexpr int RING_OFF = Q_OFF + kQBytes;
+constexpr int P_OFF = RING_OFF + kNSlot * kSlotBytes;
+constexpr int F_OFF = P_OFF + kPBytes;  // floats: m, l, cr, mu [64] each,
+                                        // red, red2 [4][64], wn [4][64],
+                                        // lse [64]
+constexpr int F_M = 0, F_L = 64, F_CR = 128, F_MU = 192, F_RED = 256,
+              F_RED2 = 512, F_WN = 768, F_LSE = 1024, F_END = 1088;
+constexpr int FLAG_OFF = F_OFF + F_END * 4;         // int [8]
+constexpr int ROW_OFF = FLAG_OFF + 32;              // int [128]: chunk rows
+constexpr int BAR_OFF = ROW_OFF + kRows * 4;
+// full[4] empty[4] qfull sfull sfree pfull ofull done
+constexpr int kBars = 2 * kNSlot + 6;
+constexpr int SMEM = BAR_OFF + kBars * 8;
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+static_assert(kD * kH * 4 <= kNSlot * kSlotBytes,
+              "the merge buffer reuses the ring");
+static_assert(kCluster * kH <= 256, "merge weights [cluster][64]");
+
+struct GatherParams {
+  DecodeParams p;
+  CUtensorMap tq;  // queries [batch * n_h][512] bf16, 64 x 64 boxes
+};
+
+// The epilogue keeps O^T as fp32 [512 values][64 heads] in the ring (128
+// KB), float4 group j of row v at position j ^ (v & 15) (conflict-free
+// stores from one lane per value and loads of consecutive heads).
+__device__ __forceinline__ int obuf_index(int v, int h) {
+  return v * kH + ((((h >> 2) ^ (v & 15)) << 2) | (h & 3));
+}
+
+// Address in a 128-byte-swizzled operand tile of 16-byte piece `c` of row
+// `r`: rows of 128 bytes in 8-row atoms of 1 KB, piece c at c ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Reduce-scatter of 64 values across the 32 lanes of a warp: afterwards
+// lane L holds the reduction over all lanes of values 2L and 2L + 1.
+template <bool MAX>
+__device__ __forceinline__ void reduce_scatter64(const float (&v)[64],
+                                                 float &r0, float &r1) {
+  const int lane = threadIdx.x & 31;
+  float a[32];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float keep = hi ? v[i + 32] : v[i];
+      const float send = hi ? v[i] : v[i + 32];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int w = 16, off = 8; off >= 1; w >>= 1, off >>= 1) {
+    const bool hi = lane & off;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < w) {
+        const float keep = hi ? a[i + w] : a[i];
+        const float send = hi ? a[i] : a[i + w];
+        const float got = __shfl_xor_sync(0xffffffffu, send, off);
+        a[i] = MAX ? fmaxf(keep, got) : keep + got;
+      }
+    }
+  }
+  r0 = a[0];
+  r1 = a[1];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_gather_tc_kernel(const __grid_constant__ GatherParams gp) {
+  const DecodeParams &p = gp.p;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  float *fs = reinterpret_cast<float *>(smem + F_OFF);
+  float *s_m = fs + F_M, *s_l = fs + F_L, *s_cr = fs + F_CR, *s_mu = fs + F_MU;
+  float *s_red = fs + F_RED;    // per-warp maxima
+  float *s_red2 = fs + F_RED2;  // per-warp sums
+  float *s_wn = fs + F_WN, *s_lse = fs + F_LSE;
+  int *flags = reinterpret_cast<int *>(smem + FLAG_OFF);
+  volatile int *s_abort = flags;
+  int *s_merge = flags + 1;
+  volatile int *s_issued = flags + 2;  // the query tile was requested
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(flags + 3);
+  // cache row of each position of the current chunk, -1 for a zero row
+  int *s_row = reinterpret_cast<int *>(smem + ROW_OFF);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+  uint64_t *empty = full + kNSlot;
+  uint64_t *qfull = empty + kNSlot;
+  uint64_t *sfull = qfull + 1;
+  uint64_t *sfree = sfull + 1;
+  uint64_t *pfull = sfree + 1;
+  uint64_t *ofull = pfull + 1;
+  uint64_t *done = ofull + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();  // after the wait: dependants never overlap this grid's
+                  // predecessor
+
+  const int G = p.n_splits;  // clusters per unit
+  const int tiles = p.n_h / kH;
+  const int q = (int)cluster_rank();
+  const int cl = (int)blockIdx.x / kCluster;
+  const int u = cl / G, g = cl % G;
+  const int b = u / tiles, ht = u % tiles;
+  const int k = p.n_idx;
+  const int parts = G * kCluster, part = g * kCluster + q;
+  const int e0 = (int)((long)k * part / parts);
+  const int e1 = (int)((long)k * (part + 1) / parts);
+  const int nch = (e1 - e0 + kRows - 1) / kRows;
+  int T = p.seq_lens[b];
+  if (T > p.max_seq_len) {
+    if (tid == 0 && q == 0 && g == 0 && ht == 0) report(p.err, DEVERR_LEN);
+    T = p.max_seq_len;
+  }
+  T = max(T, 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kNSlot; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(qfull, 1);
+    mbar_init(sfull, 1);
+    mbar_init(sfree, 128);
+    mbar_init(pfull, 128);
+    mbar_init(ofull, 1);
+    mbar_init(done, 1);
+    *s_abort = 0;
+    *s_merge = 0;
+    *s_issued = 0;
+    fence_mbar_init();
+  }
+  if (tid < kH) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.f;
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
+  // the swizzled operand tiles assume 1 KB atoms; every CTA sees the same
+  // layout, so all of them skip the work together
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;
+  if (!aligned && tid == 0) {
+    if (blockIdx.x == 0) report(p.err, DEVERR_TIMEOUT);
+    *s_abort = 1;  // the outputs are then zeros (and flagged)
+  }
+
+  if (!aligned) {
+    // nothing to do: every CTA of every cluster takes this branch
+  } else if (warp == 0) {
+    // ======================= query tile (TMA) =============================
+    if (nch > 0 && lane == 0) {
+      // the unit's query tile: 64 heads x 512, eight 64-column boxes
+      mbar_arrive_expect_tx(qfull, kQBytes);
+      const int y = b * p.n_h + ht * kH;
+      for (int cb = 0; cb < kD / 64; ++cb)
+        tma_load_2d_plain(smem + Q_OFF + cb * kQCB, &gp.tq, 64 * cb, y,
+                          qfull);
+      *s_issued = 1;
+    }
+  } else if (warp == kMmaWarp) {
+    // ======================= MMA issuer ===================================
+    constexpr uint32_t idS = umma_idesc_bf16(kRows, kH, false);  // K, K
+    // A MN-major (bit 15) and B MN-major (bit 16)
+    constexpr uint32_t idO = umma_idesc_bf16(kRows, kH, true) | (1u << 15);
+    const uint32_t q_addr = smem_u32(smem + Q_OFF);
+    const uint32_t ring = smem_u32(smem + RING_OFF);
+    const uint32_t p_addr = smem_u32(smem + P_OFF);
+    bool ok = nch == 0 || __all_sync(0xffffffffu, mbar_wait(qfull, 0));
+    for (int i = 0; ok && i < nch; ++i) {
+      // ---- S^T = K Q^T over four 128-dim slices
+      for (int j = 0; ok && j < kSlicesPerChunk / 2; ++j) {
+        // slot j holds K_j, then V_j: phases 2i and 2i + 1 of each chunk
+        const int slot = j;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], 0));
+        // S^T of the chunk before was read by the softmax
+        if (ok && j == 0 && i > 0)
+          ok = __all_sync(0xffffffffu, mbar_wait(sfree, (i - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = ring + slot * kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < kSliceCols / 16; ++ks) {
+          // 16 dims: column block ks / 4 of the slice, 32-byte step
+          const int cbk = ks >> 2, st = (ks & 3) * 32;
+          const int qcb = j * (kSliceCols / 64) + cbk;  // Q column block
+          const uint64_t a =
+              umma_desc_sw128(a0 + cbk * kCBBytes + st, 16, 1024);
+          const uint64_t bq = umma_desc_sw128(q_addr + qcb * kQCB + st, 16,
+                                              1024);
+          umma_ss_elect(tbase + kColS, a, bq, idS,
+                        (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit_elect(&empty[slot]);
+      }
+      if (!ok) break;
+      umma_commit_elect(sfull);
+      // ---- O^T += V^T P^T over four 128-column value slices
+      for (int j = 0; ok && j < kSlicesPerChunk / 2; ++j) {
+        const int slot = j;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], 1));
+        if (ok && j == 0)  // P of this chunk written, O^T rescaled
+          ok = __all_sync(0xffffffffu, mbar_wait(pfull, i & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = ring + slot * kSlotBytes;
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          // 16 positions = two 8-row groups of the slot and of P
+          const uint64_t a = umma_desc_sw128(a0 + kk * 2048, kCBBytes, 1024);
+          const uint64_t bp = umma_desc_sw128(p_addr + kk * 2048, kPBytes,
+                                              1024);
+          umma_ss_elect(tbase + kColO + j * kH, a, bp, idO,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit_elect(&empty[slot]);
+      }
+      if (!ok) break;
+      umma_commit_elect(ofull);
+    }
+    if (!ok && lane == 0) {
+      report(p.err, DEVERR_TIMEOUT);
+      *s_abort = 1;
+    }
+    // every MMA issued has completed before the epilogue and the dealloc
+    umma_commit_elect(done);
+    mbar_wait(done, 0);
+  } else {
+    // ======================= workers: copies and softmax ==================
+    // Worker warp w owns ring slot w: per chunk it copies K slice w (dims
+    // 128 w ..) into it, hands it over, copies V slice w (values 128 w ..)
+    // into it once the scores have read K slice w, runs the softmax while
+    // that copy lands, then hands the V slice over. Lanes 0-15 copy one
+    // row's 256-byte slice and lanes 16-31 the next, 16 bytes a lane, in
+    // the MMA's 128-byte-swizzled layout; copies complete per thread
+    // (commit groups), then a proxy fence orders them before the tensor
+    // core's reads.
+    const int sw = warp - kSoft0;              // 0..3: the slot it owns
+    const int qw = warp & 3;                   // tensor-memory lane quarter
+    const int r = qw * 32 + lane;              // chunk position (lane)
+    const int st = tid - kSoft0 * 32;          // 0..127
+    const uint32_t tl = tbase + ((uint32_t)(qw * 32) << 16);
+    const float sl2 = p.scale_log2;
+    uint8_t *myslot = smem + RING_OFF + sw * kSlotBytes;
+    const int pc = lane & 15, cb = pc >> 3, c8 = pc & 7;
+    // copy slice `col0` of every row of the chunk from `base` into my slot
+    auto copy_slice = [&](const uint8_t *base, int col0) {
+#pragma unroll 4
+      for (int rr = 0; rr < kRows; rr += 2) {
+        const int rw_i = rr + (lane >> 4);
+        const int rw = s_row[rw_i];
+        const uint8_t *src =
+            base + ((long)max(rw, 0) * kD + col0) * 2 + pc * 16;
+        cp_async16(myslot + cb * kCBBytes + sw128(rw_i, c8), src,
+                   rw >= 0 ? 16 : 0);
+      }
+      cp_async_commit();
+    };
+    auto hand_over = [&]() {
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[sw]);
+    };
+    // After a bounded wait gives up, the loop still runs its course (every
+    // worker warp meets the same named barriers) without copying or
+    // waiting again.
+    bool ok = true;
+    for (int i = 0; i < nch; ++i) {
+      // resolve row st of chunk i (a zero row: an entry out of the CTA's
+      // range, a negative entry, one at or past the length, a bad block);
+      // the barrier also means every worker has issued chunk i-1's copies
+      {
+        const int e = e0 + i * kRows + st;
+        int row = -1;
+        if (e < e1) {
+          const int pos = p.indices[(long)b * p.n_idx + e];
+          if (pos >= T) {
+            report(p.err, DEVERR_INDEX);
+          } else if (pos >= 0) {
+            const int blk =
+                p.block_table[(long)b * p.max_blocks + pos / p.block_size];
+            if (blk < 0 || blk >= p.num_blocks)
+              report(p.err, DEVERR_BLOCK);
+            else
+              row = blk * p.block_size + pos % p.block_size;
+          }
+        }
+        named_sync(kSoftBar, 128);
+        s_row[st] = row;
+        named_sync(kSoftBar, 128);
+      }
+      const bool valid = s_row[r] >= 0;
+      // K slice sw (its slot's V slice of the chunk before was consumed)
+      if (ok && i > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(&empty[sw], 1));
+      if (ok) copy_slice(p.k, sw * kSliceCols);
+      hand_over();
+      // V slice sw once S^T has read K slice sw
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&empty[sw], 0));
+      if (ok) copy_slice(p.v, sw * kSliceCols);
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(sfull, i & 1));
+      tc_fence_after();
+      float x[64];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (ok) {
+            tmem_ld32(tl + kColS + h2 * 32, v);
+            tmem_wait_ld(v);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            x[h2 * 32 + j] =
+                valid && ok ? __uint_as_float(v[j]) * sl2 : -INFINITY;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(sfree);
+      // per-head maximum over the chunk's 128 positions
+      float r0, r1;
+      reduce_scatter64<true>(x, r0, r1);
+      s_red[sw * 64 + 2 * lane] = r0;
+      s_red[sw * 64 + 2 * lane + 1] = r1;
+      named_sync(kSoftBar, 128);
+      if (st < kH) {
+        const float cmax = fmaxf(fmaxf(s_red[st], s_red[64 + st]),
+                                 fmaxf(s_red[128 + st], s_red[192 + st]));
+        const float mo = s_m[st];
+        const float mn = fmaxf(mo, cmax);
+        s_cr[st] = mo == -INFINITY ? 0.f : ex2(mo - mn);
+        s_mu[st] = mn == -INFINITY ? 0.f : mn;
+        s_m[st] = mn;
+      }
+      named_sync(kSoftBar, 128);
+      // the probabilities replace the scores
+#pragma unroll
+      for (int h = 0; h < 64; ++h) x[h] = ex2(x[h] - s_mu[h]);
+      if (i > 0) {
+        // O^T of the chunk before is complete (and P is free again)
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(ofull, (i - 1) & 1));
+        tc_fence_after();
+        // rescale the O^T columns of heads whose maximum grew
+        bool any = false;
+#pragma unroll 8
+        for (int h = 0; h < kH; ++h) any |= s_cr[h] != 1.f;
+        if (any && ok) {
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t o[32];
+              const uint32_t ta = tl + kColO + blk * kH + h2 * 32;
+              tmem_ld32(ta, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                o[j] = __float_as_uint(__uint_as_float(o[j]) *
+                                       s_cr[h2 * 32 + j]);
+              tmem_st32(ta, o);
+            }
+          }
+          tmem_wait_st();
+        }
+      }
+      // this position's row of P, bf16, swizzled (16-byte piece c holds
+      // heads 8c .. 8c + 7)
+      {
+        uint8_t *prow = smem + P_OFF;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 w4;
+          w4.x = pack_bf16x2(x[8 * c], x[8 * c + 1]);
+          w4.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+          w4.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+          w4.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+          *reinterpret_cast<uint4 *>(prow + sw128(r, c)) = w4;
+        }
+      }
+      // per-head sums over the chunk (in their own buffer: the maxima of
+      // the next chunk may be written before these are read)
+      reduce_scatter64<false>(x, r0, r1);
+      s_red2[sw * 64 + 2 * lane] = r0;
+      s_red2[sw * 64 + 2 * lane + 1] = r1;
+      named_sync(kSoftBar, 128);
+      if (st < kH)
+        s_l[st] = s_l[st] * s_cr[st] + (s_red2[st] + s_red2[64 + st]) +
+                  (s_red2[128 + st] + s_red2[192 + st]);
+      fence_proxy_async_smem();  // P is read by the tensor core
+      tc_fence_before();
+      mbar_arrive(pfull);
+      // the V slice, once landed
+      hand_over();
+    }
+    if (ok && nch > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(ofull, (nch - 1) & 1));
+      if (ok) tc_fence_after();
+    }
+    if (!ok && lane == 0) {
+      report(p.err, DEVERR_TIMEOUT);
+      *s_abort = 1;
+    }
+  }
+
+  // ======================= teardown of the copies =========================
+  // Every copy this CTA issued has landed before its ring is reused (the
+  // workers waited for theirs; after an abort, the query tile's too).
+  __syncthreads();
+  if (tid == 0 && *s_abort && *s_issued) mbar_wait(qfull, 0);
+  __syncthreads();
+
+  // ======================= this CTA's O^T into the ring ===================
+  float *obuf = reinterpret_cast<float *>(smem + RING_OFF);
+  if (warp >= kSoft0) {
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    const uint32_t tl = tbase + ((uint32_t)(qw * 32) << 16);
+    const bool have = nch > 0 && !*s_abort;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      const int v = blk * 128 + r;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld32(tl + kColO + blk * kH + h2 * 32, o);
+          tmem_wait_ld(o);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const int h = h2 * 32 + 4 * j4;
+          *reinterpret_cast<float4 *>(obuf + obuf_index(v, h)) =
+              make_float4(__uint_as_float(o[4 * j4]),
+                          __uint_as_float(o[4 * j4 + 1]),
+                          __uint_as_float(o[4 * j4 + 2]),
+                          __uint_as_float(o[4 * j4 + 3]));
+        }
+      }
+    }
+  }
+
+  // ======================= cluster merge ==================================
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every CTA's O^T, maxima and sums are in its memory
+  // per head: the cluster's maximum, each CTA's normalised weight, lse
+  if (tid < kH) {
+    const int h = tid;
+    float mc[kCluster], lc[kCluster];
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) {
+      mc[c] = *cluster_ptr(&s_m[h], (uint32_t)c);
+      lc[c] = *cluster_ptr(&s_l[h], (uint32_t)c);
+      M = fmaxf(M, mc[c]);
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) {
+      mc[c] = mc[c] == -INFINITY ? 0.f : ex2(mc[c] - M);
+      L = fmaf(mc[c], lc[c], L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) s_wn[c * kH + h] = mc[c] * inv;
+    s_lse[h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  // value columns [kSliceV q, kSliceV (q + 1)) of the unit, task (4 heads,
+  // 4 values): all kCluster x 4 float4 loads of distributed shared memory
+  // go out before they are used; a warp's loads cover two whole 256-byte
+  // rows
+  const long bh0 = (long)b * p.n_h + (long)ht * kH;
+  // G > 1: this cluster's slice into the workspace, as
+  // [unit][g][q][64 heads][kSliceV values] fp32 and [unit][g][q][64] lse,
+  // for the merge launch
+  const long wslot = ((long)u * G + g) * kCluster + q;
+  constexpr int kTasks = (kH / 4) * (kSliceV / 4);
+  uint32_t peer[kCluster];
+#pragma unroll
+  for (int c = 0; c < kCluster; ++c) peer[c] = cluster_saddr(obuf, (uint32_t)c);
+  // two tasks per round: 2 x kCluster x 4 loads in flight per thread
+  for (int t0 = tid; t0 < kTasks; t0 += 2 * kThreads) {
+    float4 x[2][kCluster][4];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int task = t0 + w * kThreads;
+      const int tk = task < kTasks ? task : t0;
+      const int h0 = 4 * (tk & 15), v0 = kSliceV * q + 4 * (tk >> 4);
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          x[w][c][j] = ld_dsmem_f4(peer[c] + 4u * obuf_index(v0 + j, h0));
+    }
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int task = t0 + w * kThreads;
+      if (task >= kTasks) break;
+      const int h0 = 4 * (task & 15), vl = 4 * (task >> 4);  // vl: in slice
+      const int v0 = kSliceV * q + vl;
+      float4 acc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c) {
+        const float4 wc =
+            *reinterpret_cast<const float4 *>(s_wn + c * kH + h0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[j].x = fmaf(wc.x, x[w][c][j].x, acc[j].x);
+          acc[j].y = fmaf(wc.y, x[w][c][j].y, acc[j].y);
+          acc[j].z = fmaf(wc.z, x[w][c][j].z, acc[j].z);
+          acc[j].w = fmaf(wc.w, x[w][c][j].w, acc[j].w);
+        }
+      }
+      // acc[j] holds heads h0 .. h0 + 3 of value v0 + j
+      const float o[4][4] = {{acc[0].x, acc[1].x, acc[2].x, acc[3].x},
+                             {acc[0].y, acc[1].y, acc[2].y, acc[3].y},
+                             {acc[0].z, acc[1].z, acc[2].z, acc[3].z},
+                             {acc[0].w, acc[1].w, acc[2].w, acc[3].w}};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // head h0 + i, values v0 .. v0 + 3
+        if (G == 1) {
+          uint2 w2;
+          w2.x = pack_bf16x2(o[i][0], o[i][1]);
+          w2.y = pack_bf16x2(o[i][2], o[i][3]);
+          *reinterpret_cast<uint2 *>(p.out + (bh0 + h0 + i) * kD + v0) = w2;
+        } else {
+          *reinterpret_cast<float4 *>(
+              p.ws_o + (wslot * kH + h0 + i) * kSliceV + vl) =
+              make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+        }
+      }
+    }
+  }
+  if (G == 1) {
+    if (q == 0 && tid < kH && p.lse) p.lse[bh0 + tid] = s_lse[tid];
+  } else {
+    if (tid < kH) p.ws_lse[wslot * kH + tid] = s_lse[tid];
+  }
+  cluster_sync();  // no CTA leaves while another reads its shared memory
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// The G clusters of a unit leave one merged slice per CTA in the
+// workspace (normalised outputs of 64 heads x kSliceV values and their 64
+// log-sum-exps); this second launch merges the G slices of every output
+// (log-sum-exp merge), one thread per float4 with the loads of all G parts
+// in flight together. Grid: (units, 64 x 512 / 4 / 256).
+constexpr int kGMergeThreads = 256;
+__global__ void __launch_bounds__(kGMergeThreads)
+    gather_merge_kernel(const DecodeParams p) {
+  pdl_trigger();
+  pdl_wait();  // the slices of the decode launch
+  const int G = p.n_splits;
+  const int tiles = p.n_h / kH;
+  const int u = blockIdx.x, b = u / tiles, ht = u % tiles;
+  const int e = blockIdx.y * kGMergeThreads + threadIdx.x;  // float4 index
+  if (e >= kH * kD / 4) return;
+  const int h = e / (kD / 4), v = 4 * (e % (kD / 4));
+  const int q = v / kSliceV, vl = v % kSliceV;
+  float lv[kMaxG];
+  float4 ov[kMaxG];
+#pragma unroll
+  for (int gi = 0; gi < kMaxG; ++gi) {
+    lv[gi] = -INFINITY;
+    ov[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gi < G) {
+      const long sl = ((long)u * G + gi) * kCluster + q;
+      lv[gi] = __ldcg(p.ws_lse + sl * kH + h);
+      ov[gi] = __ldcg(reinterpret_cast<const float4 *>(
+          p.ws_o + (sl * kH + h) * kSliceV + vl));
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int gi = 0; gi < kMaxG; ++gi) M = fmaxf(M, lv[gi]);
+  float W = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int gi = 0; gi < kMaxG; ++gi) {
+    if (lv[gi] == -INFINITY) continue;  // an empty part adds nothing
+    const float c1 = expf(lv[gi] - M);
+    W += c1;
+    a.x = fmaf(c1, ov[gi].x, a.x);
+    a.y = fmaf(c1, ov[gi].y, a.y);
+    a.z = fmaf(c1, ov[gi].z, a.z);
+    a.w = fmaf(c1, ov[gi].w, a.w);
+  }
+  const long bh = (long)b * p.n_h + (long)ht * kH + h;
+  const float iw = W > 0.f ? 1.f / W : 0.f;
+  uint2 pk;
+  pk.x = pack_bf16x2(a.x * iw, a.y * iw);
+  pk.y = pack_bf16x2(a.z * iw, a.w * iw);
+  *reinterpret_cast<uint2 *>(p.out + bh * kD + v) = pk;
+  if (v == 0 && p.lse) p.lse[bh] = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+// 2-D tensor map of [rows][512] bf16 with 128-byte swizzle and boxes of 64
+// columns x `box_rows` rows (rows out of range read as zeros).
+cudaError_t make_rows_map(CUtensorMap *m, const void *base, long rows,
+                          int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = tensor_map_encoder()(
+      m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kMaxDevices = 64;
+int g_max_clusters[kMaxDevices] = {};
+std::mutex g_max_clusters_mu;
+
+}  // namespace
+
+// Clusters of this kernel one wave holds on the current device (queried
+// once per device), or 0 if it cannot be launched here.
+int gather_tc_max_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return 0;
+  std::lock_guard<std::mutex> lock(g_max_clusters_mu);
+  if (g_max_clusters[dev] == 0) {
+    auto kern = decode_gather_tc_kernel;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kCluster * 64);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+        n = 0;
+    }
+    g_max_clusters[dev] = n > 0 ? n : -1;
+  }
+  return g_max_clusters[dev] > 0 ? g_max_clusters[dev] : 0;
+}
+
+// Clusters per unit: as many as one wave of resident clusters holds (at
+// least one, at most kMaxG, none whose CTAs would get fewer than 32
+// entries).
+int gather_tc_clusters(int units, int k, int max_clusters) {
+  int G = max_clusters / units;
+  const int cap = (k + kCluster * 32 - 1) / (kCluster * 32);
+  G = G < cap ? G : cap;
+  G = G < kMaxG ? G : kMaxG;
+  return G < 1 ? 1 : G;
+}
+
+cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s) {
+  if (p.dk != kD || p.dv != kD || p.n_h % kH != 0 || p.n_kv != 1 ||
+      p.n_splits < 1 || p.n_splits > kMaxG ||
+      (long)p.num_blocks * p.block_size >= (1L << 31) - 1 ||
+      (long)p.batch * p.n_h >= (1L << 31) || !tensor_map_encoder())
+    return cudaErrorNotSupported;
+  GatherParams gp;
+  gp.p = p;
+  cudaError_t e = make_rows_map(&gp.tq, p.q, (long)p.batch * p.n_h, kH);
+  if (e != cudaSuccess) return e;
+  auto kern = decode_gather_tc_kernel;
+  static bool done[64] = {};
+  e = set_smem_once(kern, SMEM, done);
+  if (e != cudaSuccess) return e;
+  const long ctas = (long)p.batch * (p.n_h / kH) * p.n_splits * kCluster;
+  if (ctas == 0) return cudaSuccess;
+  e = launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), SMEM, s,
+                 kCluster, gp);
+  if (e != cudaSuccess || p.n_splits == 1) return e;
+  const dim3 grid((unsigned)(p.batch * (p.n_h / kH)),
+                  kH * kD / 4 / kGMergeThreads);
+  return launch_pdl(gather_merge_kernel, grid, dim3(kGMergeThreads), 0, s, 1,
+                    p);
+}
+
+}  // namespace kvd

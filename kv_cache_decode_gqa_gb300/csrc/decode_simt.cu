@@ -34,7 +34,15 @@
 // finisher warp combines the warp states of each head of a flushed unit and
 // writes the final output (a unit lying wholly in this CTA's range) or a
 // partial, which the merge launch queued after this one combines with the
-// other covering CTAs' partials (log-sum-exp merge).
+// other covering CTAs' partials (log-sum-exp merge). (A variant in which the
+// last covering CTA to finish merged the unit itself, on arrival counters,
+// was measured slower: its fence, atomic and merge sat at the end of every
+// CTA, where the separate launch overlaps the next call's first copies.)
+//
+// With KVD_SEQS_PREFIX_READY the producer copies the ring's first chunks
+// (not a unit's last chunk, which holds the newest position) before the
+// grid dependency wait, so the cache streams while the previous kernel
+// finishes; their query rows follow after the wait.
 #include <cuda_fp16.h>
 
 #include <cmath>
@@ -182,13 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grp = lane >> 3, sub = lane & 7;
   // With stable lengths and block table, the plan and the producer's first
   // block-id lookups run before the predecessor grid completes; every other
-  // global access (cache, queries, scales, outputs) waits for it. Dependants
-  // are let in only after this grid's own wait (see the merge launch).
+  // global access (cache, queries, scales, outputs) waits for it, except
+  // the cache copies KVD_SEQS_PREFIX_READY allows. Dependants are let in only
+  // after this grid's own wait (see the merge launch).
   const bool early = p.flags & FLAG_SEQS_STABLE;
   if (!early) {
     pdl_wait();
     pdl_trigger();
   }
+  const bool prefetch = early && (p.flags & FLAG_PREFIX_READY);
 
   if (tid == 0) {
     s_len_err = 0;
@@ -315,6 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t policy = policy_evict_first();
     constexpr int kPre = 4;  // block ids prefetched per chunk
     bool appended = false;   // fused append: the finisher's rows are written
+    bool waited = !early;    // past the grid dependency wait
+    int npre = 0;            // chunks copied before the wait (ring's first pass)
+    int fb = 0, fh = 0, fk = 0;  // lane t < 32: chunk t's unit, for the wait
+    // The wait, then the query rows of the chunks copied before it (chunk t
+    // sits in stage t; a unit's first chunk, and chunk 0, carry its rows).
+    auto wait_then_queries = [&]() {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+      for (int t = 0; t < npre; ++t) {
+        const int bt = __shfl_sync(0xffffffffu, fb, t);
+        const int ht = __shfl_sync(0xffffffffu, fh, t);
+        const int kt = __shfl_sync(0xffffffffu, fk, t);
+        if (lane == 0 && (t == 0 || kt == 0))
+          bulk_g2s(sq + t * C::QB, p.q + ((long)bt * p.n_h + ht * GU) * D,
+                   C::QB, &full[t]);
+      }
+    };
     for (int base = 0; base < n; base += 32) {
       const int mine = base + lane;
       int mb = 0, mh = 0, mk = 0, mrows = 0, mtok = 0;
@@ -336,10 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lb0 + j <= lb1) mblk[j] = bt[lb0 + j];
       }
       const int cnt = min(32, n - base);
-      if (early && base == 0) {
-        pdl_wait();
-        pdl_trigger();
-      }
+      if (base == 0) fb = mb, fh = mh, fk = mk;
+      if (early && base == 0 && !prefetch) wait_then_queries();
       bool stop = false;
       for (int j = 0; j < cnt && !stop; ++j) {
         const int b = __shfl_sync(0xffffffffu, mb, j);
@@ -352,6 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kPre; ++t)
           blk[t] = __shfl_sync(0xffffffffu, mblk[t], j);
+        if (!waited) {
+          // before the wait: only the ring's first pass, and no chunk that
+          // holds a unit's newest position or a row this call appends
+          const int pn = p.pos ? __shfl_sync(0xffffffffu, mpos, j) : -1;
+          if (base + j >= C::NS || k == wp.nch[b] - 1 ||
+              (pn >= tok && pn < tok + rows))
+            wait_then_queries();
+        }
         if (p.pos && !appended) {
           // fused append: before the first chunk holding a new row is
           // copied, wait for the finisher to have written this CTA's rows
@@ -381,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 DT == DT_MXFP4 && rows < kStageRows ? (rows + 1) & ~1 : rows;
             mbar_arrive_expect_tx(&full[s], 2u * HP * crows * C::ROW +
                                                 (qrows ? C::QB : 0u));
-            if (qrows)
+            // before the wait the query rows are left to wait_then_queries
+            if (qrows && waited)
               bulk_g2s(sq + s * C::QB, p.q + ((long)b * p.n_h + h * GU) * D,
                        C::QB, &full[s]);
             const int32_t *bt = p.block_table + (long)b * p.max_blocks;
@@ -439,9 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         stop = __shfl_sync(0xffffffffu, go, 0) == 0;
+        if (!waited && !stop) npre = base + j + 1;
       }
       if (stop) break;
     }
+    if (!waited) wait_then_queries();
     if (p.pos && !appended) named_sync(kAppendBar, 64);
     if (lane == 0) s_producer_done = 1;
     return;

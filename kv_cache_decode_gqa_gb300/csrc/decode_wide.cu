@@ -596,11 +596,5 @@ cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s) {
   return launch_t<576, 512, false>(p, s);
 }
 
-cudaError_t launch_decode_sparse(const DecodeParams &p, cudaStream_t s) {
-  if (p.dk != 512 || p.dv != 512 || p.n_h % kHeads != 0 || p.batch > kNB ||
-      p.n_kv != 1)
-    return cudaErrorNotSupported;
-  return launch_t<512, 512, true>(p, s);
-}
 
 }  // namespace kvd

@@ -242,25 +242,6 @@ __device__ __forceinline__ int warp_excl_scan(int v, int *wsum, int *total) {
   return excl;
 }
 
-// ---- thread-block cluster helpers (distributed shared memory) ----
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Generic address of `local`'s counterpart in the shared memory of CTA
-// `rank` of this cluster. Plain loads through it are ordered by the
-// compiler against the cluster barriers and can be issued together.
-__device__ __forceinline__ const int *cluster_ptr(const int *local,
-                                                  uint32_t rank) {
-  const int *r;
-  asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(local), "r"(rank));
-  return r;
-}
 __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
   uint32_t r;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));

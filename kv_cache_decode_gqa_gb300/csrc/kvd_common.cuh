@@ -236,6 +236,71 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
 }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters (distributed shared memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes
+// before the barrier against the other CTAs' reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Generic address of `local`'s counterpart in the shared memory of CTA
+// `rank` of this cluster. Plain loads through it are ordered by the
+// compiler against the cluster barriers and can be issued together.
+template <typename T>
+__device__ __forceinline__ const T *cluster_ptr(const T *local,
+                                                uint32_t rank) {
+  const T *r;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(local), "r"(rank));
+  return r;
+}
+
+// Shared-memory window address (shared::cluster) of `local`'s counterpart in
+// CTA `rank` of this cluster, and a 16-byte load through it.
+__device__ __forceinline__ uint32_t cluster_saddr(const void *local,
+                                                  uint32_t rank) {
+  uint32_t r;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;"
+      : "=r"(r)
+      : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte asynchronous copies global -> shared through the load path
+// (cp.async): `src_bytes` 0 fills the 16 bytes with zeros and reads nothing.
+// Completion is per thread, by commit groups.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *dst, const void *src,
+                                           uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's most recent groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // named barriers (a subset of the CTA's warps)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void named_sync(int id, int count) {

@@ -23,8 +23,9 @@ enum : int { DT_BF16 = 0, DT_FP8 = 1, DT_MXFP4 = 2 };
 __host__ __device__ constexpr int row_bytes(int d, int dtype) {
   return dtype == DT_BF16 ? 2 * d : dtype == DT_FP8 ? d : d / 2 + d / 16;
 }
-// kvd_seqs flags (mirror of KVD_SEQS_STABLE in kvd.h).
-enum : int { FLAG_SEQS_STABLE = 1 };
+// kvd_seqs flags (mirrors of KVD_SEQS_STABLE and KVD_SEQS_PREFIX_READY in
+// kvd.h).
+enum : int { FLAG_SEQS_STABLE = 1, FLAG_PREFIX_READY = 2 };
 
 struct AppendParams {
   uint8_t *k_cache;  // [num_blocks][n_kv][block_size][head_dim]
@@ -54,8 +55,7 @@ struct DecodeParams {
   float *lse;              // [batch][n_h] or null
   float *ws_o;             // partials [batch][n_h][n_splits][dv]
   float *ws_lse;           // partials [batch][n_h][n_splits]
-  int *counters;           // [batch][n_groups] arrival counters, kept zero
-  int32_t n_groups;        // head groups per sequence sharing a counter
+  int32_t n_groups;        // head groups (tiles) per sequence
   int32_t batch, n_h, n_kv, dk, dv, block_size, num_blocks, max_blocks;
   int32_t dtype;        // DT_BF16, DT_FP8 or DT_MXFP4
   int32_t max_seq_len;  // clamp for device lengths
@@ -63,7 +63,7 @@ struct DecodeParams {
   int32_t split_len;    // tokens (or index entries) per split
   int32_t n_splits;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
-  int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE)
+  int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE, FLAG_PREFIX_READY)
   // sliding window (dense GQA only): sequence b attends to positions
   // [max(win_start[b], len_b - window), len_b); window 0 and no starts:
   // every visible position
@@ -143,8 +143,14 @@ cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s);
 // Log-sum-exp merge of the latent decode's split units (chunks of `rows`
 // positions: 32 for the CUDA-core kernel, 64 for the tensor-core one).
 cudaError_t launch_merge_mla(const DecodeParams &p, int rows, cudaStream_t s);
-// Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64).
-cudaError_t launch_decode_sparse(const DecodeParams &p, cudaStream_t s);
+// Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64) on
+// tcgen05: clusters of kGatherCluster CTAs, n_splits = clusters per
+// (sequence, 64-head tile), as gather_tc_clusters plans them for one wave
+// of gather_tc_max_clusters() resident clusters.
+constexpr int kGatherCluster = 4;
+int gather_tc_max_clusters();
+int gather_tc_clusters(int units, int k, int max_clusters);
+cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);
 
@@ -153,11 +159,10 @@ cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);
 #include "kvd.h"
 
 namespace kvd {
-// Workspace layout of a gqa_decode call (api.cu).
-kvd_status gqa_workspace_layout(const kvd_cache *cache, const kvd_seqs *seqs,
-                                int32_t n_h, size_t *total,
-                                size_t *counters_offset,
-                                size_t *counters_bytes);
+// Workspace bytes of a gqa_decode call, its arguments validated (api.cu).
+kvd_status gqa_workspace_bytes(const kvd_cache *cache, const kvd_seqs *seqs,
+                               int32_t n_h, size_t *total);
+
 // Record `msg` as this host thread's last error and return `st` (api.cu).
 kvd_status set_error(kvd_status st, const char *msg);
 // The current device's error word (KVD_DEVERR_* bits), for kernels that

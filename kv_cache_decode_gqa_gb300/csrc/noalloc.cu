@@ -59,9 +59,8 @@ extern "C" kvd_status kvd_gqa_decode_noalloc(const kvd_cache *cache,
                                              const void *q, int32_t n_h,
                                              float scale, void *out,
                                              float *lse, kvd_stream stream) {
-  size_t total = 0, ctr_off = 0, ctr_bytes = 0;
-  kvd_status st =
-      kvd::gqa_workspace_layout(cache, seqs, n_h, &total, &ctr_off, &ctr_bytes);
+  size_t total = 0;
+  kvd_status st = kvd::gqa_workspace_bytes(cache, seqs, n_h, &total);
   if (st != KVD_OK) return st;
   if (total > (size_t)KVD_NOALLOC_SCRATCH_BYTES)
     return kvd::set_error(
@@ -72,15 +71,8 @@ extern "C" kvd_status kvd_gqa_decode_noalloc(const kvd_cache *cache,
   void *scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != KVD_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (ctr_bytes > 0 && seqs->batch > 0) {
-    // the arrival counters must start at zero; clear them in stream order
-    cudaError_t e = cudaMemsetAsync(static_cast<char *>(scratch) + ctr_off, 0,
-                                    ctr_bytes, s);
-    if (e != cudaSuccess)
-      return kvd::set_error(KVD_ERR_CUDA,
-                            "gqa_decode_noalloc: clearing the counters failed");
-  }
+  // the GQA decode's scratch holds only partial results, each written
+  // before it is read within the call: nothing needs clearing
   return kvd_gqa_decode(cache, seqs, q, n_h, scale, out, lse, scratch,
                         (size_t)KVD_NOALLOC_SCRATCH_BYTES, stream);
 }

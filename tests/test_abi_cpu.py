@@ -36,9 +36,15 @@ def _seqs(**kw):
     return s
 
 
+def test_set_tuning_validation(lib):
+    assert lib.kvd_set_tuning(-1, 0) == 2
+    assert b"decode_ctas" in lib.kvd_last_error()
+    assert lib.kvd_set_tuning(0, 0) == 0
+
+
 def test_exports_every_declared_function(lib):
     names = N.header_functions()
-    assert len(names) == 25
+    assert len(names) == 26
     for name in names:
         assert hasattr(lib, name), name
     assert lib.kvd_version() == 1
@@ -77,9 +83,12 @@ def test_gqa_validation(lib):
     assert b"1024" in lib.kvd_last_error()
     assert _gqa(lib, _cache(dtype=1), _seqs()) == 1       # fp8 needs scales
     assert _gqa(lib, _cache(), _seqs(batch=0)) == 0       # nothing to do
-    assert _gqa(lib, _cache(), _seqs(flags=2)) == 2       # unknown flag bit
+    assert _gqa(lib, _cache(), _seqs(flags=4)) == 2       # unknown flag bit
     assert b"flags" in lib.kvd_last_error()
+    assert _gqa(lib, _cache(), _seqs(flags=2)) == 2       # PREFIX_READY alone
+    assert b"KVD_SEQS_STABLE" in lib.kvd_last_error()
     assert _gqa(lib, _cache(), _seqs(batch=0, flags=1)) == 0  # STABLE is known
+    assert _gqa(lib, _cache(), _seqs(batch=0, flags=3)) == 0  # and both
 
 
 def _append_decode(lib, c, s, pos=FAKE, k_new=FAKE, v_new=FAKE):

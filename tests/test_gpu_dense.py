@@ -260,6 +260,119 @@ def test_gqa_decode_stable_seqs_flag(case):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+@pytest.mark.parametrize("case", [c for c in DENSE_CASES if c[0] in
+                                  ("mha_d128", "gqa2_d128", "gqa2_d128_bs64",
+                                   "mha_d64_bs64", "gqa8_bs64", "gqa16_bs16",
+                                   "gqa8_bs32")],
+                         ids=lambda c: c[0])
+def test_gqa_decode_prefix_ready_flag(case, fused, dtype):
+    """KVD_SEQS_PREFIX_READY lets the first chunks of cached rows be copied
+    before the preceding kernel (here the append, or nothing) completes;
+    the chunk holding the newest position waits. Results and cache bytes
+    are those of the default order."""
+    name, n_h, n_kv, d, bs, lengths = case
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=1, block_size=bs, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=d)
+    wl = W.DeviceWorkload(s, layers=[0])
+    flags = K.SEQS_STABLE | K.SEQS_PREFIX_READY
+    out, lse = H.device_step(wl, 0, fused=fused, seqs_flags=flags)
+    torch.cuda.synchronize()
+    ref, ref_lse, (kr, vr) = H.oracle_dense_step(s, wl.paging, 0)
+    c = wl.caches[0]
+    assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr)), name
+    assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr)), name
+    H.assert_close(H.to_np_bf16(out), ref, f"{name}/{dtype}/ready")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"{name}/ready")
+
+
+def test_prefix_ready_needs_stable_flag():
+    s = W.config("llama31_70b_gqa", batch=2, lengths=[10, 20], n_layers=1,
+                 n_h=8, n_kv=8)
+    wl = W.DeviceWorkload(s, layers=[0])
+    with pytest.raises(K.KvdError) as e:
+        K.gqa_decode(wl.caches[0], wl.block_table, wl.seq_lens,
+                     s.max_seq_len, wl.q[0], seqs_flags=K.SEQS_PREFIX_READY)
+    assert e.value.status == 2
+
+
+# Split units with many parts: a forced CTA count far above the units puts
+# up to ~40 CTAs on one unit, so the last to arrive merges them with lane
+# quads (more than 8 parts), in both kernels and in the fused call.
+@pytest.mark.parametrize("n_h,n_kv,dtype", [(2, 2, "bf16"), (4, 1, "fp8"),
+                                            (8, 1, "bf16"), (16, 1, "fp8")],
+                         ids=["mha", "gqa4_fp8", "gqa8", "gqa16_fp8"])
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_many_part_split_merge(n_h, n_kv, dtype, fused):
+    lengths = [2500, 3, 700]
+    s = W.config("llama31_70b_gqa", batch=3, lengths=lengths, n_layers=1,
+                 block_size=64, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=128)
+    wl = W.DeviceWorkload(s, layers=[0])
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    K.set_tuning(decode_ctas=57)
+    try:
+        # twice: the second call finds the counters the first left at zero
+        # (its append rewrites the same rows)
+        for _ in range(2):
+            out, lse = H.device_step(wl, 0, fused=fused,
+                                     seqs_flags=K.SEQS_STABLE)
+            torch.cuda.synchronize()
+            H.assert_close(H.to_np_bf16(out), ref, f"parts {n_h}x{n_kv}")
+            H.assert_lse_close(lse.cpu().numpy(), ref_lse, "parts lse")
+    finally:
+        K.set_tuning()
+
+
+# A step as a serving loop issues it: several layers back to back, each the
+# fused append + decode with both flags, captured in a CUDA graph and
+# replayed, every layer sharing ONE workspace (so a layer's kernel starts
+# while the previous layer's still runs, over the same counters and
+# partials). Each layer's output against the oracle after two replays (the
+# second replay re-appends the same rows, so the results are the same).
+@pytest.mark.parametrize("name,n_h,n_kv,dtype,lengths", [
+    ("mha", 16, 16, "bf16", [3000, 1, 900]),
+    ("gqa8", 32, 4, "bf16", [5000, 64, 2100, 17]),
+    ("gqa8_fp8", 32, 4, "fp8", [4100, 640, 2000]),
+], ids=["mha", "gqa8", "gqa8_fp8"])
+def test_layer_chain_in_graph_shared_workspace(name, n_h, n_kv, dtype,
+                                               lengths):
+    layers = [0, 1, 2, 3]
+    s = W.config("llama31_70b_gqa", batch=len(lengths), lengths=lengths,
+                 n_layers=4, block_size=64, dtype=dtype, n_h=n_h, n_kv=n_kv,
+                 head_dim=128)
+    wl = W.DeviceWorkload(s, layers=layers)
+    need = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                            wl.seq_lens, wl.max_seq_len, n_h)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    outs = {l: torch.empty((s.batch, n_h, 128), dtype=torch.bfloat16,
+                           device="cuda") for l in layers}
+    lses = {l: torch.empty((s.batch, n_h), dtype=torch.float32,
+                           device="cuda") for l in layers}
+    flags = K.SEQS_STABLE | K.SEQS_PREFIX_READY
+
+    def step():
+        for l in layers:
+            K.gqa_append_decode(wl.caches[l], wl.block_table, wl.seq_lens,
+                                wl.max_seq_len, wl.pos, wl.k_new[l],
+                                wl.v_new[l], wl.q[l], out=outs[l],
+                                lse=lses[l], workspace=ws, seqs_flags=flags)
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        step()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for l in layers:
+        ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, l)
+        H.assert_close(H.to_np_bf16(outs[l]), ref, f"{name} layer {l}")
+        H.assert_lse_close(lses[l].cpu().numpy(), ref_lse, f"{name} {l}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("case", DENSE_CASES, ids=[c[0] for c in DENSE_CASES])
 def test_append_decode_fused(case, dtype):
     """kvd_gqa_append_decode: the cache bytes of kv_append (every block,
@@ -377,13 +490,14 @@ def test_workspace_errors():
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences, the bench's launch configuration
 # ---------------------------------------------------------------------------
+BENCH_FLAGS = K.SEQS_STABLE | K.SEQS_PREFIX_READY
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 def test_llama2_7b_full_size_sampled_layers(fused):
     s = W.config("llama2_7b_mha")
     wl = W.DeviceWorkload(s, layers=[0, 31])
     for layer in (0, 31):
         out, lse = H.device_step(wl, layer, fused=fused,
-                                 seqs_flags=K.SEQS_STABLE if fused else 0)
+                                 seqs_flags=BENCH_FLAGS if fused else 0)
         torch.cuda.synchronize()
         ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, layer, seqs=[0])
         H.assert_close(H.to_np_bf16(out), ref, f"llama2 layer {layer}")
@@ -410,7 +524,7 @@ def test_llama31_70b_full_size_sampled(name, fused):
     wl = W.DeviceWorkload(s, layers=[0])
     try:
         out, lse = H.device_step(wl, 0, fused=fused,
-                                 seqs_flags=K.SEQS_STABLE if fused else 0)
+                                 seqs_flags=BENCH_FLAGS if fused else 0)
     except K.KvdError as e:
         if e.status == 3:
             pytest.skip(f"{name}: kernel not built yet")

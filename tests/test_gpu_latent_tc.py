@@ -75,22 +75,27 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=["tails", "h256", "split2",
                                              "split3", "peaked",
                                              "peaked_1lane"])
-def test_latent_tc(case, monkeypatch):
+def test_latent_tc(case):
     n_h, bs, lengths, seed, kw, ctas = case
-    if ctas is not None:
-        monkeypatch.setenv("KVD_DECODE_CTAS", str(ctas))
-    out, lse, ref, ref_lse = run_case(n_h, bs, lengths, seed, **kw)
+    K.set_tuning(decode_ctas=ctas or 0)
+    try:
+        out, lse, ref, ref_lse = run_case(n_h, bs, lengths, seed, **kw)
+    finally:
+        K.set_tuning()
     H.assert_close(out, ref, f"latent tc {case}")
     H.assert_lse_close(lse, ref_lse, f"latent tc {case}")
 
 
-def test_latent_tc_matches_cuda_core_kernel(monkeypatch):
+def test_latent_tc_matches_cuda_core_kernel():
     """Both latent kernels on the same inputs: each within the tolerance of
     the oracle, and of each other."""
     args = (128, 64, [1234, 77, 4096], 7)
     out_tc, lse_tc, ref, ref_lse = run_case(*args)
-    monkeypatch.setenv("KVD_MLA_CUDA_CORES", "1")
-    out_cc, lse_cc, _, _ = run_case(*args)
+    K.set_tuning(mla_cuda_cores=True)
+    try:
+        out_cc, lse_cc, _, _ = run_case(*args)
+    finally:
+        K.set_tuning()
     H.assert_close(out_tc, ref, "tc")
     H.assert_close(out_cc, ref, "cuda cores")
     H.assert_close(out_tc, out_cc, "tc vs cuda cores")

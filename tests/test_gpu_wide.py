@@ -75,13 +75,16 @@ def _index_lists(shape, k, seed):
     return out
 
 
-def _sparse_oracle(shape, paging, layer_q, idx, seqs, host_rows):
-    """Oracle over a compact cache of only the selected rows."""
+def _sparse_oracle(shape, paging, layer_q, idx, seqs, host_rows,
+                   seq_lens=None):
+    """Oracle over a compact cache of only the selected rows (`seq_lens`:
+    the visible lengths, if not the workload's)."""
     q = oracle.bf16_bits_to_f64(layer_q)[seqs]
+    lens = shape.seq_lens if seq_lens is None else seq_lens
     outs, lses = [], []
     for j, b in enumerate(seqs):
         sel = idx[b]
-        valid = sel[(sel >= 0) & (sel < shape.seq_lens[b])]
+        valid = sel[(sel >= 0) & (sel < lens[b])]
         kr, vr = host_rows(b, valid)
         n = len(valid)
         bt = np.arange(n, dtype=np.int64)[None, :] if n else np.zeros((1, 1),
@@ -144,6 +147,73 @@ def test_sparse_small(case):
                                   _row_source(s, wl.paging, knew, vnew))
     H.assert_close(H.to_np_bf16(out), ref, f"sparse {case}")
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"sparse {case}")
+
+
+def _sparse_case(lengths, k, bs, n_h=64, seed=77, idx=None, lens=None):
+    """Sparse decode of a small workload (every output compared with the
+    oracle); `lens` overrides the visible lengths."""
+    s = W.config("sparse", batch=len(lengths), lengths=lengths, topk=k,
+                 block_size=bs, n_layers=1, modes=["full"], n_h=n_h)
+    wl = W.DeviceWorkload(s)
+    c = wl.caches[0]
+    K.kv_append(c, wl.block_table, wl.pos, wl.k_new[0], wl.v_new[0])
+    if idx is None:
+        idx = _index_lists(s, k, seed)
+    seq_lens = wl.seq_lens if lens is None else torch.tensor(
+        lens, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_decode(c, wl.block_table, seq_lens, wl.max_seq_len,
+                               torch.from_numpy(idx).cuda(), wl.q[0])
+    torch.cuda.synchronize()
+    knew = H.host_bits(s, 0, W.T_KNEW, (s.batch, 1, 512))
+    vnew = H.host_bits(s, 0, W.T_VNEW, (s.batch, 1, 512))
+    qbits = H.host_bits(s, 0, W.T_Q, (s.batch, s.n_h, 512))
+    seqs = list(range(s.batch))
+    ref, ref_lse = _sparse_oracle(s, wl.paging, qbits, idx, seqs,
+                                  _row_source(s, wl.paging, knew, vnew),
+                                  seq_lens=lens)
+    return out, lse, ref, ref_lse
+
+
+# The tensor-core gather kernel's work split: 8-CTA clusters per (sequence,
+# 64-head tile), G clusters per unit. Two head tiles; a k that is no
+# multiple of anything; k smaller than the CTAs of a unit (most CTAs get no
+# entry); several 128-entry chunks per CTA (the online rescale across
+# chunks, forced with a small CTA count); many clusters per unit (the
+# workspace merge of G parts, forced with a large CTA count).
+@pytest.mark.parametrize("lengths,k,bs,n_h,ctas", [
+    ([300, 1200, 9], 1000, 64, 128, 0),
+    ([40, 3], 5, 16, 64, 0),
+    ([6000], 5000, 64, 64, 8),
+    ([3000, 2500], 2048, 32, 64, 1024),
+    ([9000, 100, 4000, 2], 3000, 64, 64, 16),
+], ids=["h128_k1000", "k5", "chunks_per_cta", "clusters_max", "b4_g1"])
+def test_sparse_work_splits(lengths, k, bs, n_h, ctas):
+    K.set_tuning(decode_ctas=ctas)
+    try:
+        out, lse, ref, ref_lse = _sparse_case(lengths, k, bs, n_h)
+    finally:
+        K.set_tuning()
+    H.assert_close(H.to_np_bf16(out), ref, f"sparse {lengths} k={k}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"sparse {lengths} lse")
+
+
+def test_sparse_repeats_and_empty_sequence():
+    """A list naming some positions twice (each copy counts, as in the
+    oracle), and a sequence with nothing visible (out = 0, lse = -inf)."""
+    s_len = [500, 300, 50]
+    k = 256
+    idx = np.full((3, k), -1, dtype=np.int32)
+    rng = np.random.default_rng(5)
+    idx[0] = rng.integers(0, 501, k)            # with repeats
+    idx[1, :100] = np.arange(100) * 3
+    idx[2, :40] = np.arange(40)
+    lens = [501, 301, 0]                        # sequence 2: nothing visible
+    out, lse, ref, ref_lse = _sparse_case(s_len, k, 64, idx=idx, lens=lens)
+    H.assert_close(H.to_np_bf16(out), ref, "repeats / empty")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, "repeats / empty lse")
+    assert np.all(H.to_np_bf16(out)[2] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[2]))
+    K.device_error()     # entries of sequence 2 are past its length: flagged
 
 
 def test_sparse_full_size_sampled():

@@ -80,26 +80,33 @@ def test_noalloc_matches_workspace_entry_point(case):
         H.assert_lse_close(lse.cpu().numpy(), ref_l, "noalloc lse")
 
 
-def test_noalloc_refuses_shapes_beyond_its_scratch(monkeypatch):
-    """A launch of 200,000 CTAs (the tuning override KVD_DECODE_CTAS) over 32
-    heads of 128 needs ~200 MB of partials: more than the static array. The
-    call must return KVD_ERR_WORKSPACE without launching anything."""
-    monkeypatch.setenv("KVD_DECODE_CTAS", "200000")
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    """A launch of 200,000 CTAs (forced with kvd_set_tuning) over 32 heads
+    of 128 needs ~200 MB of partials: more than the static array. The call
+    must return KVD_ERR_WORKSPACE and launch nothing: the outputs, filled
+    with NaN before the call, stay NaN, where a decode of this cache (one
+    nonzero row per sequence) would have written numbers."""
     B, n_h, d, bs, T = 8, 32, 128, 64, 65536
     dev = "cuda"
-    cache = K.PagedCache(torch.zeros((2, n_h, bs, d), dtype=torch.bfloat16,
-                                     device=dev),
-                         torch.zeros((2, n_h, bs, d), dtype=torch.bfloat16,
-                                     device=dev), bs, n_h, d)
+    k = torch.zeros((2, n_h, bs, d), dtype=torch.bfloat16, device=dev)
+    v = torch.ones((2, n_h, bs, d), dtype=torch.bfloat16, device=dev)
+    cache = K.PagedCache(k, v, bs, n_h, d)
     bt = torch.zeros((B, T // bs), dtype=torch.int32, device=dev)
     lens = torch.ones(B, dtype=torch.int32, device=dev)
-    need = K.workspace_size(K.OP_GQA_DECODE, cache, bt, lens, T, n_h)
-    assert need > SCRATCH_BYTES
-    q = torch.zeros((B, n_h, d), dtype=torch.bfloat16, device=dev)
-    out = torch.zeros((B, n_h, d), dtype=torch.bfloat16, device=dev)
-    lse = torch.zeros((B, n_h), dtype=torch.float32, device=dev)
-    st = _call_noalloc(cache, bt, lens, T, q, out, lse)
+    q = torch.ones((B, n_h, d), dtype=torch.bfloat16, device=dev)
+    out = torch.full((B, n_h, d), float("nan"), dtype=torch.bfloat16,
+                     device=dev)
+    lse = torch.full((B, n_h), float("nan"), dtype=torch.float32, device=dev)
+    K.set_tuning(decode_ctas=200000)
+    try:
+        need = K.workspace_size(K.OP_GQA_DECODE, cache, bt, lens, T, n_h)
+        assert need > SCRATCH_BYTES
+        st = _call_noalloc(cache, bt, lens, T, q, out, lse)
+        msg = N.lib().kvd_last_error()
+    finally:
+        K.set_tuning()
     assert st == 5                                  # KVD_ERR_WORKSPACE
-    assert b"static array" in N.lib().kvd_last_error()
+    assert b"static array" in msg
     torch.cuda.synchronize()
-    assert torch.count_nonzero(out).item() == 0     # nothing ran
+    assert torch.isnan(out.float()).all().item()    # nothing ran
+    assert torch.isnan(lse).all().item()
