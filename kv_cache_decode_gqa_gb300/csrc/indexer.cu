@@ -5,24 +5,24 @@
 // own indexer query over a shared indexer key cache).
 //
 // Scores: s_t = sum_j w_j * max(0, q_j . k_t) for every visible position t,
-// with the 64-wide indexer keys read from the paged K-only cache and
-// staged in shared memory by bulk copies. Four lanes cover one key row (32
-// bytes each); the lane's slice of every indexer query is held in
-// registers as fp32 pairs, so the products are formed two at a time
-// (packed fp32 fused multiply-adds), each dot product finishes with two
-// xor-shuffles, and every sum is formed in fp32.
+// with the 64-wide indexer keys read from the paged K-only cache into shared
+// memory by 16-byte asynchronous copies. The dot products are bf16 tensor-
+// core products with fp32 accumulation (the bf16 products are exact); the
+// ReLU, the weights and the sum over heads are fp32.
 //
 // Selection: the k largest scores of a sequence, equal scores taken in
 // ascending position order, returned as ascending positions (-1 padding
 // when fewer than k positions are visible). A cluster of eight CTAs per
 // sequence runs an exact radix select on order-preserving 32-bit keys of
-// the fp32 scores (negative zero counted as zero): three histogram passes
-// (12, 12 and 8 bits), summed across the cluster in distributed shared
-// memory, find the k-th largest key K* and how many keys exceed it; a final
-// pass in position order keeps every key above K* and the lowest-indexed
-// keys equal to K*, placing each kept position with block-wide prefix sums
-// after the selections of the lower-ranked CTAs. The result is exactly the
-// selection the scores define.
+// the fp32 scores (negative zero counted as zero): a histogram of the top
+// 12 bits summed across the cluster in distributed shared memory finds the
+// bin of the k-th largest key; the keys in that bin (the candidates) are
+// gathered into every CTA, which finishes the select on them alone (bits
+// 19..8, then 7..0) and finds the k-th largest key K* and how many keys
+// exceed it. A final pass in position order keeps every key above K* and
+// the lowest-indexed keys equal to K*, placing each kept position after the
+// selections of the lower-ranked CTAs. The result is exactly the selection
+// the scores define.
 #include <cmath>
 
 #include "kvd_common.cuh"
@@ -34,154 +34,349 @@ namespace {
 // scores
 // ---------------------------------------------------------------------------
 constexpr int kIdxDim = 64;
-constexpr int kScoreThreads = 256;
-constexpr int kTokPerCta = 512;  // 8 warps x 64 positions
 
-// Packed fp32 pair: two independent fused multiply-adds in one instruction.
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b,
-                                          uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
-  return ((uint64_t)hi << 32) | lo;
-}
-// The two bf16 of a 32-bit word as an fp32 pair (exact).
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  return pack_f32x2(w << 16, w & 0xffff0000u);
-}
-__device__ __forceinline__ float sum_f32x2(uint64_t v) {
-  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+// A persistent launch over the batch's 64-entry slices: slice s of sequence
+// b covers entries 64 s .. 64 s + 63 (the visible positions, or the pool's
+// entries). The J slices, sequence-major, are dealt to the G CTAs in
+// contiguous runs [c J / G, (c + 1) J / G), so every CTA gets the same
+// number whatever the lengths. A CTA walks its run in windows of up to 256
+// slices (32 sequences at most), and warp w takes the slices at offsets w,
+// w + 8, ... of each window, resolved lane-parallel a window ahead: their
+// sequences by a warp scan of the slice counts, their block ids by
+// independent loads. A warp streams its slices' key rows into three 8 KB
+// slots of its own with 16-byte asynchronous copies, two slices in flight
+// while it scores the third (192 KB a CTA); 16-byte chunk c of row r goes
+// to chunk c ^ (r mod 8) of the row, so that the matrix loads below meet no
+// bank conflicts. (Bulk copies would keep fewer bytes in flight: a thread
+// that issues one waits until the copy engine has taken it, about one copy
+// latency for 8 KB.)
+//
+// The dot products q_j . k_t of a slice's 64 rows with the (up to 8)
+// indexer queries form one 64 x 64 by 64 x 8 bf16 product with fp32
+// accumulation: 16 warp-level tensor-core MMAs (m16n8k16). The ReLU, the
+// head weights and the sum over heads run on the accumulators and end in
+// two xor-shuffles across the 4 lanes that hold a row.
+constexpr int kSlice = 64;                         // entries per slice
+constexpr int kSliceBytes = kSlice * kIdxDim * 2;  // 8 KB
+constexpr int kScoreWarps = 8;
+constexpr int kScoreThreads = 32 * kScoreWarps;
+constexpr int kDepth = 3;      // slots a warp
+constexpr int kPieceRegs = 8;  // block pieces a lane resolves ahead
+constexpr int kScoreSmem = kScoreWarps * kDepth * kSliceBytes;  // 192 KB
+
+// A resolved slice: its sequence and geometry, and the cache rows of its
+// first kPieceRegs block pieces (a piece: the rows of the slice in one
+// paged block, or one 8-entry pool block).
+struct SliceJob {
+  int b, tw, rows, T, np;
+  uint32_t row[kPieceRegs];  // cache row of piece q's first row
+  int pos0[kPieceRegs];      // pool mode: the pool block's first position,
+                             // or -1
+};
+
+__device__ __forceinline__ int clamp_len(int v, int hi) {
+  return max(0, min(v, hi));
 }
 
-// Warp w of a CTA owns the 64 positions t0 + 64 w .. + 63. It stages their
-// key rows in shared memory with bulk asynchronous copies (one per paged
-// block the slice touches, completing on the warp's own mbarrier), then
-// scores them eight rows per step: lane group g = lane / 4 takes row
-// 8 i + g, its 4 lanes 16 dims each. Products are summed in fp32 pairs,
-// then across the 4 lanes with two xor-shuffles. Several CTAs per SM keep
-// enough copies in flight to stream the cache at HBM speed.
-constexpr int kSlice = 64;  // positions per warp
-template <int H>
-__global__ void __launch_bounds__(kScoreThreads, 2)
+__global__ void __launch_bounds__(kScoreThreads, 1)
     indexer_score_kernel(const IndexerParams p) {
-  extern __shared__ __align__(128) uint8_t srows[];  // [kTokPerCta][128 B]
-  __shared__ uint64_t bars[kScoreThreads / 32];
+  // [warp][slot][64 rows][128 B], 16-byte chunks swizzled by row
+  extern __shared__ __align__(1024) uint8_t ring[];
+  __shared__ SliceJob s_job[kScoreWarps][32];      // the window's slices
+  __shared__ uint32_t s_row[kScoreWarps][kSlice];  // cache row of each row
+  __shared__ int s_scan[32];
+  __shared__ int s_start[3];  // first sequence, its first slice, slices
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.y;
-  int T = p.seq_lens[b];
-  T = max(0, min(T, p.max_seq_len));
-  // entries: the visible positions, or (pool mode) the pool's positions
-  const int32_t *pool = p.pool ? p.pool + (long)b * kPoolBlocks : nullptr;
-  const int E = pool ? kPoolBlock * max(0, min(p.pool_n[b], kPoolBlocks)) : T;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tw = blockIdx.x * kTokPerCta + warp * kSlice;  // warp's first
-  if (tw >= E) return;
-  const int rows = min(kSlice, E - tw);
-  uint8_t *mine = srows + warp * kSlice * kIdxDim * 2;
-  uint64_t *bar = &bars[warp];
-  if (lane == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, rows * kIdxDim * 2);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.batch, bs = p.block_size;
+  const bool pow2 = (bs & (bs - 1)) == 0;
+  const int bs_shift = __ffs(bs) - 1;
+  auto div_bs = [&](int t) { return pow2 ? t >> bs_shift : t / bs; };
+  auto entries = [&](int b, int T) {
+    return p.pool ? kPoolBlock * clamp_len(p.pool_n[b], kPoolBlocks) : T;
+  };
+  // ---- this CTA's run of slices: thread t counts the slices of its
+  // contiguous chunk of sequences, a block scan places the chunks ----
+  {
+    const int per = (B + kScoreThreads - 1) / kScoreThreads;
+    const int c0 = min(B, tid * per), c1 = min(B, c0 + per);
+    int mine = 0;
+    for (int b = c0; b < c1; ++b) {
+      const int T = clamp_len(p.seq_lens[b], p.max_seq_len);
+      mine += (entries(b, T) + kSlice - 1) / kSlice;
+    }
+    int x = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_scan[warp] = x;
+    __syncthreads();
+    int before = 0, J = 0;
+    for (int w = 0; w < kScoreWarps; ++w) {
+      const int v = s_scan[w];
+      before += w < warp ? v : 0;
+      J += v;
+    }
+    const int excl = before + x - mine;
+    const long j0 = (long)blockIdx.x * J / gridDim.x;
+    const long j1 = (long)(blockIdx.x + 1) * J / gridDim.x;
+    if (tid == 0) s_start[2] = (int)(j1 - j0);
+    if (j0 < j1 && excl <= j0 && j0 < excl + mine) {
+      int acc = excl;
+      for (int b = c0; b < c1; ++b) {
+        const int T = clamp_len(p.seq_lens[b], p.max_seq_len);
+        const int n = (entries(b, T) + kSlice - 1) / kSlice;
+        if (j0 < acc + n) {
+          s_start[0] = b;
+          s_start[1] = (int)(j0 - acc);
+          break;
+        }
+        acc += n;
+      }
+    }
+    __syncthreads();
   }
-  __syncwarp();
-  // one copy per block piece of the slice; lane j takes pieces j, j + 32..
-  const int32_t *bt = p.block_table + (long)b * p.max_blocks;
-  const int bs = p.block_size;
-  if (pool) {
-    // one copy per pool block (8 rows, inside one cache block); a block past
-    // the visible length reads block 0 (its scores are set to -inf below)
-    if (lane < rows / kPoolBlock) {
-      const int pos0 = kPoolBlock * pool[tw / kPoolBlock + lane];
-      int blk = 0, slot = 0;
-      if (pos0 >= 0 && pos0 < T) {
-        blk = bt[pos0 / bs];
-        slot = pos0 % bs;
-        if (blk < 0 || blk >= p.num_blocks) {
-          report(p.err, DEVERR_BLOCK);
-          blk = 0;  // read a valid block; the result is flagged as wrong
+  const int nj = s_start[2];
+  if (nj == 0) return;
+
+  int cb = s_start[0], cs = s_start[1];  // next slice to resolve
+  int k0 = 0;                            // its index in the CTA's run
+  const int g = lane >> 2, t4 = lane & 3;
+  uint32_t qf[4][2];  // B fragments: head g, dims 16 kt + 2 t4 (+8)
+  float w0 = 0.f, w1 = 0.f;  // weights of heads 2 t4, 2 t4 + 1
+  int qb = -1;  // the sequence whose query qf holds
+  uint8_t *wring = ring + warp * kDepth * kSliceBytes;
+  for (;;) {
+    // ---- resolve the next window of up to 256 slices of the run (the same
+    // windows in every warp); lane m takes slice 8 m + warp of it ----
+    if (k0 >= nj || cb >= B) break;
+    const int bl = cb + lane;
+    int Tl = 0, nl = 0;
+    if (bl < B) {
+      Tl = clamp_len(p.seq_lens[bl], p.max_seq_len);
+      nl = (entries(bl, Tl) + kSlice - 1) / kSlice;
+    }
+    int inc = max(0, nl - (lane == 0 ? cs : 0));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, inc, 31);
+    if (total == 0) {  // 32 sequences without slices left
+      cb += 32;
+      cs = 0;
+      continue;
+    }
+    const int win = min(32 * kScoreWarps, min(total, nj - k0));
+    const int idx = kScoreWarps * lane + warp;  // this lane's slice
+    int j = 0;  // the sequence (relative to cb) of this lane's slice
+#pragma unroll 1
+    for (int l = 0; l < 32; ++l) j += __shfl_sync(0xffffffffu, inc, l) <= idx;
+    const int jj = min(j, 31);
+    const int before = __shfl_sync(0xffffffffu, inc, max(jj - 1, 0));
+    const int sl = (jj == 0 ? cs + idx : idx - before);
+    const int bc = min(cb + jj, B - 1);
+    SliceJob job;
+    job.b = bc;
+    job.T = __shfl_sync(0xffffffffu, Tl, jj);
+    const int E = p.pool ? kPoolBlock * clamp_len(p.pool_n[bc], kPoolBlocks)
+                         : job.T;
+    job.tw = sl * kSlice;
+    job.rows = idx < win ? max(0, min(kSlice, E - job.tw)) : 0;
+    // the next window starts after this one's last slice
+    const int jl = __popc(__ballot_sync(0xffffffffu, inc <= win - 1));
+    const int jl_before = __shfl_sync(0xffffffffu, inc, max(jl - 1, 0));
+    cs = (jl == 0 ? cs + win : win - jl_before);
+    cb += jl;
+    k0 += win;
+    // block ids of the first kPieceRegs pieces (independent loads), then
+    // checked and turned into cache rows
+    const int32_t *bt = p.block_table + (long)bc * p.max_blocks;
+    int blk[kPieceRegs];
+    if (p.pool) {
+      job.np = job.rows / kPoolBlock;
+      const int32_t *pool = p.pool + (long)bc * kPoolBlocks;
+#pragma unroll
+      for (int q = 0; q < kPieceRegs; ++q)
+        job.pos0[q] =
+            q < job.np ? kPoolBlock * pool[job.tw / kPoolBlock + q] : -1;
+#pragma unroll
+      for (int q = 0; q < kPieceRegs; ++q) {
+        const int pos = job.pos0[q];
+        blk[q] = (q < job.np && pos >= 0 && pos < job.T) ? bt[div_bs(pos)] : 0;
+      }
+    } else {
+      job.np = job.rows > 0
+                   ? div_bs(job.tw + job.rows - 1) - div_bs(job.tw) + 1 : 0;
+      const int lb0 = div_bs(job.tw);
+#pragma unroll
+      for (int q = 0; q < kPieceRegs; ++q) {
+        blk[q] = q < job.np ? bt[lb0 + q] : 0;
+        job.pos0[q] = -1;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kPieceRegs; ++q) {
+      int bq = blk[q], slot = 0;
+      if (q >= job.np) {
+        job.row[q] = 0;
+        continue;
+      }
+      if (p.pool) {
+        const int pos = job.pos0[q];
+        if (pos >= 0 && pos < job.T) {
+          slot = pos - div_bs(pos) * bs;
+        } else {
+          report(p.err, DEVERR_INDEX);
+          bq = 0;
+          job.pos0[q] = -1;
         }
       } else {
-        report(p.err, DEVERR_INDEX);
+        const int lb = div_bs(job.tw) + q;
+        slot = max(job.tw, lb * bs) - lb * bs;
       }
-      bulk_g2s(mine + lane * kPoolBlock * kIdxDim * 2,
-               p.cache + ((long)blk * bs + slot) * kIdxDim * 2,
-               kPoolBlock * kIdxDim * 2, bar);
-    }
-  }
-  const int lb0 = tw / bs, lb1 = (tw + rows - 1) / bs;
-  for (int lb = lb0 + lane; !pool && lb <= lb1; lb += 32) {
-    int blk = bt[lb];
-    if (blk < 0 || blk >= p.num_blocks) {
-      report(p.err, DEVERR_BLOCK);
-      blk = 0;  // read a valid block; the result is flagged as wrong
-    }
-    const int first = max(tw, lb * bs), last = min(tw + rows, (lb + 1) * bs);
-    bulk_g2s(mine + (first - tw) * kIdxDim * 2,
-             p.cache + ((long)blk * bs + (first - lb * bs)) * kIdxDim * 2,
-             (last - first) * kIdxDim * 2, bar);
-  }
-  // this lane's 16 dims of every indexer query (fp32 pairs), head weights
-  const int grp = lane >> 2, sub = lane & 3;
-  uint64_t q2[H][8];
-  float w[H];
-#pragma unroll
-  for (int j = 0; j < H; ++j) {
-    if (j < p.n_heads) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          p.q + ((long)b * p.n_heads + j) * kIdxDim + sub * 16);
-      const uint4 u0 = src[0], u1 = src[1];
-      const uint32_t v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) q2[j][e] = bf16x2_to_f32x2(v[e]);
-      w[j] = p.w[(long)b * p.n_heads + j];
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) q2[j][e] = 0;
-      w[j] = 0.f;
-    }
-  }
-  if (!mbar_wait(bar, 0)) {
-    // a copy that never lands: flag it, give the copies one more bounded
-    // wait, and leave without scoring
-    if (lane == 0) report(p.err, DEVERR_TIMEOUT);
-    mbar_wait(bar, 0);
-    return;
-  }
-  float *out = p.scores + (long)b * p.score_stride + tw;
-#pragma unroll 2
-  for (int i = 0; i < kSlice / 8; ++i) {
-    const int r = 8 * i + grp;
-    const uint4 *src =
-        reinterpret_cast<const uint4 *>(mine + r * kIdxDim * 2 + sub * 32);
-    const uint4 u0 = src[0], u1 = src[1];
-    const uint32_t v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    uint64_t k2[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) k2[e] = bf16x2_to_f32x2(v[e]);
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < H; ++j) {
-      uint64_t acc = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc = ffma2(q2[j][e], k2[e], acc);
-      float d = sum_f32x2(acc);
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      s = fmaf(w[j], fmaxf(d, 0.f), s);
-    }
-    if (sub == 0 && r < rows) {
-      if (pool) {
-        const int pos = kPoolBlock * pool[(tw + r) / kPoolBlock] +
-                        (tw + r) % kPoolBlock;
-        if (pos < 0 || pos >= T) s = -INFINITY;
+      if (bq < 0 || bq >= p.num_blocks) {
+        report(p.err, DEVERR_BLOCK);
+        bq = 0;  // read a valid block; the result is flagged as wrong
       }
-      out[r] = s;
+      job.row[q] = (uint32_t)bq * (uint32_t)bs + (uint32_t)slot;
+    }
+    __syncwarp();  // the previous window's table has been read
+    s_job[warp][lane] = job;
+    __syncwarp();
+    const int bn = win > warp ? (win - warp + kScoreWarps - 1) / kScoreWarps : 0;
+
+    // ---- this warp's slices of the window: copies two ahead ----
+    const int col = lane & 7;
+    for (int m = -2; m < bn; ++m) {
+      const int mi = m + 2;  // the slice whose copies go out now
+      if (mi < bn) {
+        const SliceJob &J = s_job[warp][mi];
+        const int rows = J.rows, np = J.np;
+        uint8_t *dst = wring + (mi % kDepth) * kSliceBytes;
+        if (p.pool) {
+          // rows 8 q .. 8 q + 7 are pool block q: row r of chunk j is in
+          // block j / 2
+#pragma unroll
+          for (int jc = 0; jc < kSlice / 4; ++jc) {
+            const int r = (lane >> 3) + 4 * jc;
+            if (r < rows)
+              cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
+                         p.cache + ((size_t)J.row[jc >> 1] + (r & 7)) * 128 +
+                             col * 16, 16);
+          }
+        } else if (np == 1) {  // one block piece: consecutive cache rows
+          const size_t r0 = J.row[0];
+#pragma unroll
+          for (int jc = 0; jc < kSlice / 4; ++jc) {
+            const int r = (lane >> 3) + 4 * jc;
+            if (r < rows)
+              cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
+                         p.cache + (r0 + r) * 128 + col * 16, 16);
+          }
+        } else {
+          // several pieces: the cache row of each row first
+          const int tw = J.tw, lb0 = div_bs(tw);
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            const int r = lane + 32 * h;
+            const int t = tw + r;
+            const int q = div_bs(t) - lb0;
+            const int first = max(tw, (lb0 + q) * bs);
+            uint32_t pr = 0;
+            if (r < rows) {
+              if (q < kPieceRegs) {
+                pr = J.row[q];
+              } else {  // pieces past the resolved ones
+                int bq = p.block_table[(long)J.b * p.max_blocks + lb0 + q];
+                if (bq < 0 || bq >= p.num_blocks) {
+                  report(p.err, DEVERR_BLOCK);
+                  bq = 0;
+                }
+                pr = (uint32_t)bq * (uint32_t)bs +
+                     (uint32_t)(first - (lb0 + q) * bs);
+              }
+            }
+            s_row[warp][r] = pr + (uint32_t)(t - first);
+          }
+          __syncwarp();
+#pragma unroll 4
+          for (int jc = 0; jc < kSlice / 4; ++jc) {
+            const int r = (lane >> 3) + 4 * jc;
+            if (r < rows)
+              cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
+                         p.cache + (size_t)s_row[warp][r] * 128 + col * 16,
+                         16);
+          }
+          __syncwarp();  // s_row is rewritten by the next slice
+        }
+      }
+      cp_async_commit();  // one group a step (empty past the last slice)
+      if (m < 0) continue;
+      cp_async_wait<2>();  // slice m has landed (this lane's copies)
+      __syncwarp();        // ... and every lane's
+      const SliceJob &J = s_job[warp][m];
+      const int b = J.b, tw = J.tw, rows = J.rows, T = J.T;
+      if (b != qb) {
+        qb = b;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+            p.q + ((long)b * p.n_heads + min(g, p.n_heads - 1)) * kIdxDim);
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          qf[kt][0] = g < p.n_heads ? q32[8 * kt + t4] : 0u;
+          qf[kt][1] = g < p.n_heads ? q32[8 * kt + 4 + t4] : 0u;
+        }
+        const float *wb = p.w + (long)b * p.n_heads;
+        w0 = 2 * t4 < p.n_heads ? wb[2 * t4] : 0.f;
+        w1 = 2 * t4 + 1 < p.n_heads ? wb[2 * t4 + 1] : 0.f;
+      }
+      const uint32_t sbase = smem_u32(wring + (m % kDepth) * kSliceBytes);
+      float *out = p.scores + (long)b * p.score_stride + tw;
+      float c[4][4];
+#pragma unroll
+      for (int rt = 0; rt < 4; ++rt) {
+        c[rt][0] = c[rt][1] = c[rt][2] = c[rt][3] = 0.f;
+        const int lr = 16 * rt + (lane & 15);  // this lane's ldmatrix row
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          const int chunk = 2 * kt + (lane >> 4);
+          uint32_t a[4];
+          ldsm_x4(a, sbase + lr * 128 + ((chunk ^ (lr & 7)) << 4));
+          mma_bf16(c[rt], a, qf[kt][0], qf[kt][1]);
+        }
+      }
+      __syncwarp();  // every lane has read the slot before it is refilled
+#pragma unroll
+      for (int rt = 0; rt < 4; ++rt) {
+        // rows 16 rt + g and 16 rt + g + 8, heads 2 t4 and 2 t4 + 1
+        float s0 = fmaf(w1, fmaxf(c[rt][1], 0.f), w0 * fmaxf(c[rt][0], 0.f));
+        float s1 = fmaf(w1, fmaxf(c[rt][3], 0.f), w0 * fmaxf(c[rt][2], 0.f));
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        if (t4 == 0) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * rt + g + 8 * hh;
+            float sc = hh ? s1 : s0;
+            if (r < rows) {
+              if (p.pool) {  // a position past the visible length: -inf
+                const int pos0 = J.pos0[r / kPoolBlock];
+                if (pos0 < 0 || pos0 + r % kPoolBlock >= T) sc = -INFINITY;
+              }
+              out[r] = sc;
+            }
+          }
+        }
+      }
     }
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -249,30 +444,88 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 }
 
 constexpr int kCluster = 8;            // CTAs per sequence
-constexpr int kCacheKeys = 40 * 1024;  // keys a CTA keeps in shared memory
+constexpr int kCacheKeys = 20 * 1024;  // keys a CTA keeps in shared memory
+constexpr int kOwnCap = 4096;          // candidates a CTA collects
+constexpr int kGatherCap = 16384;      // candidates of the whole cluster
+
+// The digit (high digits first) whose bin holds the remaining-th largest
+// key, and the count of keys in the bins above it, into *s_digit and
+// *s_above. Thread t holds the bins of range 1023 - t (4 bins of 4096, or 1
+// of 256), read by load(first bin, bins, counts); a block scan over the
+// ranges finds the one that holds it.
+template <class Load>
+__device__ __forceinline__ void find_digit(int nb, int remaining, Load load,
+                                           int *tmp, int *s_digit,
+                                           int *s_above) {
+  const int per = (nb + kTopkThreads - 1) / kTopkThreads;  // 4 or 1
+  const int r = kTopkThreads - 1 - threadIdx.x;  // thread 0 owns the top
+  int cnt[4] = {0, 0, 0, 0};
+  int local = 0;
+  if (r * per < nb) {
+    load(r * per, per, cnt);
+    local = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+  }
+  int all;
+  const int before = block_excl_scan(local, tmp, &all);  // bins above range
+  if (before < remaining && before + local >= remaining) {
+    int acc = before;
+    for (int j = per - 1; j >= 0; --j) {
+      if (acc + cnt[j] >= remaining) {
+        *s_digit = r * per + j;
+        *s_above = acc;
+        break;
+      }
+      acc += cnt[j];
+    }
+  }
+  __syncthreads();
+}
 
 // One cluster per sequence; CTA r of the cluster owns positions
-// [r T / 8, (r + 1) T / 8). When its range fits (T <= 8 * 40960) the CTA
-// reads its scores once, converts them to keys in shared memory and runs
-// every pass from there; otherwise each pass reads the scores again.
-// Histograms are summed across the cluster through distributed shared
-// memory in two steps of 16-byte remote loads: CTA r sums the 8 copies of
-// its eighth of the bins, then every thread reads the totals of its bins
-// from their owners; all CTAs reach the same digits. The compaction places each CTA's selections after those of
-// the lower-ranked CTAs.
+// [r T / 8, (r + 1) T / 8). When its range fits (T <= 8 * 20480) the CTA
+// reads its scores once, converts them to keys in shared memory and works
+// from there; otherwise each sweep reads the scores again.
+//  1. The histogram of the first digit (key bits 31..20) is summed across
+//     the cluster through distributed shared memory in two steps of
+//     16-byte remote loads (CTA r sums the 8 copies of its eighth of the
+//     bins, then every thread reads the totals of its bins from their
+//     owners), giving every CTA the digit d1 of the k-th largest key and
+//     the count of keys above d1's bin.
+//  2. Each CTA counts its keys above d1's bin and collects its candidates
+//     (keys in d1's bin); every CTA then copies the cluster's candidates
+//     (about the k-th key's share of one bin, a few thousand at most for
+//     continuous scores) into its own shared memory and finishes the
+//     select on them alone: two local passes on bits 19..8 and 7..0 give
+//     the k-th largest key K* and how many keys equal to K* to take, and
+//     the candidates of each source CTA above / equal to K* place every
+//     CTA's selections after those of the lower-ranked CTAs.
+//  3. If the candidates do not fit (4,096 a CTA, 16,384 a cluster: many
+//     equal or near-equal scores), the cluster instead runs the second and
+//     third digits as cluster-wide passes over every key, as in step 1.
+//  4. A sweep in position order writes the selections.
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const IndexerParams p) {
-  __shared__ __align__(16) int hist[2][kBins];  // double-buffered per pass
-  __shared__ __align__(16) int tot[kBins];      // cluster totals, own eighth
+  __shared__ __align__(16) int hist[2][kBins];
+  __shared__ __align__(16) int tot[kBins];  // cluster totals, own eighth
   __shared__ int tmp[32];
   __shared__ int s_digit, s_above;
-  __shared__ int s_counts[2];  // this CTA's keys above / equal to K*
-  extern __shared__ uint32_t s_keys[];
+  __shared__ int s_pub[2];           // keys above d1's bin, candidates
+  __shared__ int s_all[2][kCluster];  // every CTA's s_pub
+  __shared__ int s_src[2][kCluster];  // candidates above / equal to K*
+  __shared__ int s_run[2];            // lower-ranked CTAs: selections, K*s
+  __shared__ int s_off[kCluster + 1];  // candidates of the lower ranks
+  __shared__ int s_counts[2];         // this CTA's keys above / equal to K*
+  __shared__ int s_wsum[32];
+  // [kOwnCap] own candidates, [kGatherCap] the cluster's, [n] keys
+  extern __shared__ uint32_t dsm[];
+  uint32_t *s_own = dsm, *s_gath = dsm + kOwnCap;
+  uint32_t *s_keys = dsm + kOwnCap + kGatherCap;
   pdl_trigger();
   pdl_wait();
   const uint32_t rank = cluster_rank();
   const int b = blockIdx.x / kCluster;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned lt = (1u << lane) - 1;
   int T = p.seq_lens[b];
   T = max(0, min(T, p.max_seq_len));
   const int k = p.topk;
@@ -298,47 +551,43 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int r0 = (int)((long)T * rank / kCluster);
   const int r1 = (int)((long)T * (rank + 1) / kCluster);
   const int n = r1 - r0;
-  const bool cached = (uint32_t)n * 4u <= dynamic_smem_bytes();
-  if (cached) {
-    for (int i = tid; i < n; i += kTopkThreads) s_keys[i] = score_key(sc[r0 + i]);
-    __syncthreads();
-  }
+  const bool cached =
+      (uint32_t)(kOwnCap + kGatherCap + n) * 4u <= dynamic_smem_bytes();
   auto key_at = [&](int i) {  // i relative to r0, 0 <= i < n
     return cached ? s_keys[i] : score_key(sc[r0 + i]);
   };
-  // ---- radix select of the k-th largest key ----
-  uint32_t prefix = 0;  // digits chosen so far
-  int remaining = k;    // keys still to take at or below the prefix
-  const int shifts[3] = {20, 8, 0};
-  const int widths[3] = {12, 12, 8};
-  for (int pass = 0; pass < 3; ++pass) {
-    int *h = hist[pass & 1];
-    const int shift = shifts[pass], bits = widths[pass];
-    const int nb = 1 << bits;
-    const int hi_shift = shift + bits;  // bits above this digit
-    for (int i = tid; i < kBins; i += kTopkThreads) h[i] = 0;
-    __syncthreads();
-    constexpr int kU = 16;  // keys per thread per round
+  for (int i = tid; i < kBins; i += kTopkThreads) hist[0][i] = 0;
+  if (tid < 2) s_pub[tid] = 0;
+  if (tid < 2 * kCluster) s_src[tid / kCluster][tid % kCluster] = 0;
+  __syncthreads();
+  // ---- 1. keys, and the cluster's histogram of the first digit ----
+  {
+    constexpr int kU = 8;  // independent loads a thread keeps in flight
     for (int base = 0; base < n; base += kU * kTopkThreads) {
-      uint32_t key[kU];
+      float v[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int i = base + u * kTopkThreads + tid;
-        key[u] = i < n ? key_at(i) : 0u;
+        v[u] = i < n ? sc[r0 + i] : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int i = base + u * kTopkThreads + tid;
-        const bool match =
-            i < n && (hi_shift >= 32 || (key[u] >> hi_shift) == prefix);
-        // plain shared-memory atomics: lanes of a warp that meet on one
-        // bin are serialised by the hardware, which costs less than
-        // grouping the lanes by digit when many distinct digits occur
-        if (match) atomicAdd(&h[(key[u] >> shift) & (nb - 1)], 1);
+        if (i < n) {
+          const uint32_t key = score_key(v[u]);
+          if (cached) s_keys[i] = key;
+          // plain shared-memory atomics: lanes of a warp that meet on one
+          // bin are serialised by the hardware, which costs less than
+          // grouping the lanes by digit when many distinct digits occur
+          atomicAdd(&hist[0][key >> 20], 1);
+        }
       }
     }
+  }
+  // Sum of the cluster's histograms `h` (nb bins) into the totals of this
+  // CTA's eighth, then the digit search over the totals of their owners.
+  auto cluster_digit = [&](const int *h, int nb, int remaining) {
     cluster_sync();  // every CTA's histogram of this pass is complete
-    // totals of this CTA's eighth of the bins, four bins per thread
     const int own = nb / kCluster;  // bins per owner (512 or 32)
     for (int d = rank * own + 4 * tid; d < (int)(rank + 1) * own;
          d += 4 * kTopkThreads) {
@@ -357,78 +606,203 @@ __global__ void __launch_bounds__(kTopkThreads)
       *reinterpret_cast<int4 *>(&tot[d]) = s;
     }
     cluster_sync();  // every owner's totals are complete
-    // suffix sums over thread ranges of bins (high digits first)
-    const int per = (nb + kTopkThreads - 1) / kTopkThreads;  // 4 or 1
-    const int r = kTopkThreads - 1 - tid;  // reversed: thread 0 owns the top
-    int cnt[4] = {0, 0, 0, 0};
-    int local = 0;
-    if (r * per < nb) {
-      const int d0 = r * per;
-      const int *src = cluster_ptr(&tot[d0], (uint32_t)(d0 / own));
-      if (per == 4) {
-        const int4 v = *reinterpret_cast<const int4 *>(src);
-        cnt[0] = v.x, cnt[1] = v.y, cnt[2] = v.z, cnt[3] = v.w;
-      } else {
-        cnt[0] = *src;
-      }
-      local = cnt[0] + cnt[1] + cnt[2] + cnt[3];
-    }
-    int all;
-    const int before = block_excl_scan(local, tmp, &all);  // bins above range
-    if (before < remaining && before + local >= remaining) {
-      int acc = before;
-      for (int j = per - 1; j >= 0; --j) {
-        const int d = r * per + j;
-        if (d >= nb) continue;
-        if (acc + cnt[j] >= remaining) {
-          s_digit = d;
-          s_above = acc;
-          break;
-        }
-        acc += cnt[j];
-      }
-    }
-    __syncthreads();
-    prefix = (prefix << bits) | (uint32_t)s_digit;
-    remaining -= s_above;
-    __syncthreads();
-  }
-  const uint32_t kstar = prefix;
-  const int need_eq = remaining;  // keys equal to K* to take (>= 1)
-  // ---- counts of this CTA's keys above / equal to K* ----
-  int my_gt = 0, my_eq = 0;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const uint32_t key = key_at(i);
-    my_gt += key > kstar;
-    my_eq += key == kstar;
-  }
-  int tot_gt, tot_eq0;
-  block_excl_scan(my_gt, tmp, &tot_gt);
-  block_excl_scan(my_eq, tmp, &tot_eq0);
-  if (tid == 0) {
-    s_counts[0] = tot_gt;
-    s_counts[1] = tot_eq0;
-  }
-  cluster_sync();
-  // selections and equal keys of the lower-ranked CTAs
-  int run_sel = 0, run_eq = 0;
-  for (uint32_t q = 0; q < rank; ++q) {
-    const int g = *cluster_ptr(&s_counts[0], q);
-    const int e = *cluster_ptr(&s_counts[1], q);
-    run_sel += g + max(0, min(e, need_eq - run_eq));
-    run_eq += e;
-  }
-  // ---- compaction of this CTA's range in position order ----
+    find_digit(nb, remaining,
+               [&](int d0, int per, int (&cnt)[4]) {
+                 const int *src = cluster_ptr(&tot[d0], (uint32_t)(d0 / own));
+                 if (per == 4) {
+                   const int4 v = *reinterpret_cast<const int4 *>(src);
+                   cnt[0] = v.x, cnt[1] = v.y, cnt[2] = v.z, cnt[3] = v.w;
+                 } else {
+                   cnt[0] = *src;
+                 }
+               },
+               tmp, &s_digit, &s_above);
+  };
+  cluster_digit(hist[0], kBins, k);
+  const uint32_t d1 = (uint32_t)s_digit;
+  int remaining = k - s_above;  // keys still to take at or below d1's bin
+  // ---- 2. keys above d1's bin, and the candidates ----
   // Warp w owns the runs of kRun positions [base + w kRun, + kRun); lane l
-  // takes positions run + 32 j + l, so position order within a run is
-  // (j, l) and one ballot per j ranks the lanes. A first sweep counts each
-  // warp's keys equal to K*, a second decides every selection, a third
-  // writes the positions; block scans over the 32 warp totals place the
-  // warps after each other.
+  // takes positions run + 32 j + l, so one ballot per j ranks the lanes.
   constexpr int kRun = 512;  // positions per warp and round
-  const int lane = tid & 31, wid = tid >> 5;
-  const unsigned lt = (1u << lane) - 1;
-  __shared__ int s_wsum[32];
+  {
+    int gt = 0;
+    for (int base = 0; base < n; base += kRun * 32) {
+      const int run = base + wid * kRun;
+      uint32_t key[kRun / 32];
+      unsigned eqb[kRun / 32];
+      int weq = 0;
+#pragma unroll
+      for (int j = 0; j < kRun / 32; ++j) {
+        const int i = run + 32 * j + lane;
+        key[j] = i < n ? key_at(i) : 0u;
+        const uint32_t d = key[j] >> 20;
+        gt += i < n && d > d1;
+        eqb[j] = __ballot_sync(0xffffffffu, i < n && d == d1);
+        weq += __popc(eqb[j]);
+      }
+      int at = 0;
+      if (lane == 0 && weq > 0) at = atomicAdd(&s_pub[1], weq);
+      at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+      for (int j = 0; j < kRun / 32; ++j) {
+        const int idx = at + __popc(eqb[j] & lt);
+        if (((eqb[j] >> lane) & 1) && idx < kOwnCap) s_own[idx] = key[j];
+        at += __popc(eqb[j]);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      gt += __shfl_xor_sync(0xffffffffu, gt, off);
+    if (lane == 0 && gt > 0) atomicAdd(&s_pub[0], gt);
+  }
+  cluster_sync();  // every CTA's counts and candidates are complete
+  if (wid == 0) {
+    int g = 0, c = 0;
+    if (lane < kCluster) {
+      g = *cluster_ptr(&s_pub[0], (uint32_t)lane);
+      c = *cluster_ptr(&s_pub[1], (uint32_t)lane);
+      s_all[0][lane] = g;
+      s_all[1][lane] = c;
+    }
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < kCluster; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 0) s_off[0] = 0;
+    if (lane < kCluster) s_off[lane + 1] = inc;
+  }
+  __syncthreads();
+  bool fits = true;
+#pragma unroll
+  for (int q = 0; q < kCluster; ++q) fits = fits && s_all[1][q] <= kOwnCap;
+  const int C = s_off[kCluster];
+  fits = fits && C <= kGatherCap;  // the same decision in every CTA
+  auto source = [&](int i) {  // the CTA candidate i came from
+    int q = 0;
+#pragma unroll
+    for (int j = 1; j < kCluster; ++j) q += i >= s_off[j];
+    return q;
+  };
+  uint32_t kstar;
+  int need_eq, run_sel, run_eq;
+  if (fits) {
+    for (int i = tid; i < C; i += kTopkThreads) {
+      const int q = source(i);
+      s_gath[i] = *cluster_ptr(&s_own[i - s_off[q]], (uint32_t)q);
+    }
+    // done with the other CTAs' shared memory; the matching wait comes
+    // before this CTA leaves
+    cluster_arrive();
+    for (int i = tid; i < kBins; i += kTopkThreads) hist[1][i] = 0;
+    __syncthreads();
+    for (int i = tid; i < C; i += kTopkThreads)
+      atomicAdd(&hist[1][(s_gath[i] >> 8) & 0xfff], 1);
+    __syncthreads();
+    auto local4096 = [&](int d0, int, int (&cnt)[4]) {
+      const int4 v = *reinterpret_cast<const int4 *>(&hist[1][d0]);
+      cnt[0] = v.x, cnt[1] = v.y, cnt[2] = v.z, cnt[3] = v.w;
+    };
+    find_digit(kBins, remaining, local4096, tmp, &s_digit, &s_above);
+    const uint32_t d2 = (uint32_t)s_digit;
+    remaining -= s_above;
+    for (int i = tid; i < 256; i += kTopkThreads) hist[0][i] = 0;
+    __syncthreads();
+    for (int i = tid; i < C; i += kTopkThreads) {
+      const uint32_t key = s_gath[i];
+      if (((key >> 8) & 0xfff) == d2) atomicAdd(&hist[0][key & 0xff], 1);
+    }
+    __syncthreads();
+    find_digit(256, remaining,
+               [&](int d0, int, int (&cnt)[4]) { cnt[0] = hist[0][d0]; },
+               tmp, &s_digit, &s_above);
+    kstar = (d1 << 20) | (d2 << 8) | (uint32_t)s_digit;
+    need_eq = remaining - s_above;
+    for (int i = tid; i < C; i += kTopkThreads) {
+      const uint32_t key = s_gath[i];
+      if (key >= kstar) atomicAdd(&s_src[key == kstar][source(i)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int sel = 0, eq = 0;
+      for (uint32_t q = 0; q < rank; ++q) {
+        const int e = s_src[1][q];
+        sel += s_all[0][q] + s_src[0][q] + max(0, min(e, need_eq - eq));
+        eq += e;
+      }
+      s_run[0] = sel;
+      s_run[1] = eq;
+    }
+    __syncthreads();
+    run_sel = s_run[0];
+    run_eq = s_run[1];
+  } else {
+    // ---- 3. cluster-wide passes on bits 19..8 and 7..0 ----
+    uint32_t prefix = d1;
+    const int shifts[2] = {8, 0};
+    const int widths[2] = {12, 8};
+    for (int pass = 0; pass < 2; ++pass) {
+      int *h = hist[(pass + 1) & 1];
+      const int shift = shifts[pass], bits = widths[pass];
+      const int nb = 1 << bits;
+      const int hi_shift = shift + bits;  // bits above this digit
+      for (int i = tid; i < kBins; i += kTopkThreads) h[i] = 0;
+      __syncthreads();
+      constexpr int kU = 16;  // keys per thread per round
+      for (int base = 0; base < n; base += kU * kTopkThreads) {
+        uint32_t key[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = base + u * kTopkThreads + tid;
+          key[u] = i < n ? key_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = base + u * kTopkThreads + tid;
+          if (i < n && (key[u] >> hi_shift) == prefix)
+            atomicAdd(&h[(key[u] >> shift) & (nb - 1)], 1);
+        }
+      }
+      cluster_digit(h, nb, remaining);
+      prefix = (prefix << bits) | (uint32_t)s_digit;
+      remaining -= s_above;
+      __syncthreads();
+    }
+    kstar = prefix;
+    need_eq = remaining;
+    // counts of this CTA's keys above / equal to K*, placed by rank
+    int my_gt = 0, my_eq = 0;
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = key_at(i);
+      my_gt += key > kstar;
+      my_eq += key == kstar;
+    }
+    int tot_gt, tot_eq0;
+    block_excl_scan(my_gt, tmp, &tot_gt);
+    block_excl_scan(my_eq, tmp, &tot_eq0);
+    if (tid == 0) {
+      s_counts[0] = tot_gt;
+      s_counts[1] = tot_eq0;
+    }
+    cluster_sync();
+    if (tid < kCluster) {
+      s_src[0][tid] = *cluster_ptr(&s_counts[0], (uint32_t)tid);
+      s_src[1][tid] = *cluster_ptr(&s_counts[1], (uint32_t)tid);
+    }
+    __syncthreads();
+    run_sel = run_eq = 0;
+    for (uint32_t q = 0; q < rank; ++q) {
+      const int e = s_src[1][q];
+      run_sel += s_src[0][q] + max(0, min(e, need_eq - run_eq));
+      run_eq += e;
+    }
+  }
+  // ---- 4. compaction of this CTA's range in position order ----
+  // A first sweep counts each warp's keys equal to K*, a second decides
+  // every selection, a third writes the positions; block scans over the 32
+  // warp totals place the warps after each other.
   for (int base = 0; base < n; base += kRun * 32) {
     const int run = base + wid * kRun;
     unsigned gtb[kRun / 32], eqb[kRun / 32];
@@ -466,7 +840,11 @@ __global__ void __launch_bounds__(kTopkThreads)
     run_eq += tot_eq;
     run_sel += tot_sel;
   }
-  cluster_sync();  // no CTA leaves while another may read its shared memory
+  // no CTA leaves while another may read its shared memory
+  if (fits)
+    cluster_wait();
+  else
+    cluster_sync();
 }
 
 }  // namespace
@@ -527,37 +905,40 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const PoolParams p) 
   if (tid == 0) p.pool_n[b] = min(total, kPoolBlocks);
 }
 
-template <int H>
-cudaError_t launch_scores_h(const IndexerParams &p, cudaStream_t s) {
-  constexpr int kSmem = kTokPerCta * kIdxDim * 2;
-  static bool done[64] = {};
-  cudaError_t e = set_smem_once(indexer_score_kernel<H>, kSmem, done);
-  if (e != cudaSuccess) return e;
-  dim3 grid((p.max_entries + kTokPerCta - 1) / kTokPerCta, p.batch);
-  return launch_pdl(indexer_score_kernel<H>, grid, dim3(kScoreThreads), kSmem,
-                    s, 1, p);
-}
-
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s) {
   if (p.batch == 0 || p.max_seq_len == 0 || p.max_entries == 0)
     return cudaSuccess;
-  if (p.n_heads <= 1) return launch_scores_h<1>(p, s);
-  if (p.n_heads <= 2) return launch_scores_h<2>(p, s);
-  if (p.n_heads <= 4) return launch_scores_h<4>(p, s);
-  if (p.n_heads <= 8) return launch_scores_h<8>(p, s);
-  return cudaErrorNotSupported;
+  if (p.n_heads < 1 || p.n_heads > 8) return cudaErrorNotSupported;
+  static bool done[64] = {};
+  cudaError_t e = set_smem_once(indexer_score_kernel, kScoreSmem, done);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // at most one CTA per slice of the longest sequence's entries
+  const long slices =
+      (long)p.batch * ((p.max_entries + kSlice - 1) / kSlice);
+  const int grid = (int)(slices < sms ? slices : sms);
+  return launch_pdl(indexer_score_kernel, dim3(grid), dim3(kScoreThreads),
+                    kScoreSmem, s, 1, p);
 }
 
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
+  constexpr int kCandBytes = (kOwnCap + kGatherCap) * 4;
   static bool done[64] = {};
-  cudaError_t e = set_smem_once(topk_kernel, kCacheKeys * 4, done);
+  cudaError_t e =
+      set_smem_once(topk_kernel, kCandBytes + kCacheKeys * 4, done);
   if (e != cudaSuccess) return e;
-  // the largest range a CTA owns; cached in shared memory when it fits
+  // the largest range a CTA owns; its keys cached in shared memory when
+  // they fit
   const long range = ((long)p.max_entries + kCluster - 1) / kCluster;
+  const size_t smem =
+      kCandBytes + (range <= kCacheKeys ? (size_t)range * 4 : 0);
   return launch_pdl(topk_kernel, dim3(p.batch * kCluster), dim3(kTopkThreads),
-                    range <= kCacheKeys ? (size_t)range * 4 : 0, s, kCluster,
-                    p);
+                    smem, s, kCluster, p);
 }
 
 cudaError_t launch_indexer_pool(const PoolParams &p, cudaStream_t s) {

@@ -139,6 +139,76 @@ def test_full_size_indexer():
     np.testing.assert_allclose(sc[b, :T], ref, rtol=1e-5, atol=1e-4)
 
 
+def test_many_ragged_sequences():
+    """70 sequences of 0 .. 3,000 visible positions (some empty), block
+    size 16, two indexer heads: every sequence's scores against the fp64
+    oracle and its selection against the oracle's rule on those scores.
+    Slices of many sequences share a CTA's run here."""
+    rng = np.random.default_rng(71)
+    lengths = [int(x) for x in rng.integers(0, 3000, 70)]
+    s = _shape(lengths, 128, 16, 2)
+    wl = W.DeviceWorkload(s)
+    vis = list(s.seq_lens)
+    for b in (0, 7, 8, 9, 40, 69):         # empty sequences
+        vis[b] = 0
+    wl.seq_lens.copy_(torch.tensor(vis, dtype=torch.int32))
+    idx, sc = _run_indexer(wl, 0)
+    tab = I.normal_bf16_table()
+    ir = _host_idx_cache(s, wl.paging, tab)
+    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, 0, W.T_QIDX,
+                                             (s.batch, 2, s.idx_dim)))
+    w = W.host_weights(s, 0).astype(np.float64)
+    ref = oracle.indexer_scores(qI, w, ir, wl.paging.table, vis, 16)
+    for b, T in enumerate(vis):
+        np.testing.assert_allclose(sc[b, :T], ref[b], rtol=1e-5, atol=1e-4)
+        want = oracle.topk_select(sc[b, :T].astype(np.float64), 128)
+        assert np.array_equal(idx[b], want), f"row {b}"
+
+
+@pytest.mark.parametrize("kind", ["all_zero", "few_above"])
+def test_selection_with_heavy_ties(kind):
+    """Long sequences whose scores are mostly 0, so that the bin of the
+    k-th largest score holds far more keys than a CTA collects as
+    candidates and the selection takes its cluster-wide passes: "all_zero"
+    (an all-zero indexer cache: every score 0, the first k positions win)
+    and "few_above" (1,000 positions a sequence get key dim 0 in
+    {1/8 .. 1}, scores relu(k_t0) with ties among them; the rest of the k
+    come from the lowest zero-score positions). The short sequence in the
+    same launch takes the candidate path."""
+    lengths = [131071, 60000, 3000]
+    s = _shape(lengths, 2048, 64, 4)
+    wl = W.DeviceWorkload(s)
+    kc = wl.idx_cache.k
+    kc.zero_()
+    if kind == "few_above":
+        rng = np.random.default_rng(72)
+        for b, T in enumerate(s.seq_lens):
+            pos = rng.choice(T, size=1000, replace=False)
+            blk = wl.paging.table[b][pos // 64].astype(np.int64)
+            vals = torch.from_numpy(rng.integers(1, 9, pos.size) / 8.0)
+            kc[torch.from_numpy(blk).cuda(), 0,
+               torch.from_numpy(pos % 64).cuda(), 0] = vals.to(
+                   torch.bfloat16).cuda()
+    q = torch.zeros_like(wl.q_idx[0])
+    q[:, 0, 0] = 1.0
+    w = torch.zeros_like(wl.w[0])
+    w[:, 0] = 1.0
+    wl.q_idx[0] = q
+    wl.w[0] = w
+    idx, sc = _run_indexer(wl, 0)
+    ir = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref_idx, ref_sc = oracle.indexer_topk(
+        q.float().cpu().numpy().astype(np.float64),
+        w.cpu().numpy().astype(np.float64), ir, wl.paging.table, s.seq_lens,
+        64, 2048)
+    for b, T in enumerate(s.seq_lens):
+        assert np.array_equal(sc[b, :T].astype(np.float64), ref_sc[b])
+        assert (ref_sc[b] == 0).sum() > (8 * 4096 if b == 0 else 0)
+    assert np.array_equal(idx, ref_idx)
+    if kind == "all_zero":
+        assert np.array_equal(idx[0], np.arange(2048))
+
+
 def test_schedule_matches_oracle():
     """Full, Reuse x3, Reindex x4 over one main cache and one indexer
     cache (exact indexer inputs, so the selections are identical)."""
