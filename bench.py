@@ -529,7 +529,8 @@ def run_sparse_schedule(K, wl, outs, wss, timed=None):
             timed("select", n_sel, lambda: K.indexer_topk(
                 wl.idx_cache, wl.block_table, wl.seq_lens, wl.max_seq_len,
                 wl.q_idx[layer], wl.w[layer], s.topk,
-                indices=wss["idx"][layer], workspace=wss["topk"]))
+                indices=wss["idx"][layer], workspace=wss["topk"],
+                seqs_flags=K.SEQS_STABLE | K.SEQS_PREFIX_READY))
             n_sel += 1
             if s.modes[layer] == "full" and s.pool_k and not pooled:
                 K.indexer_pool(wl.block_table, wl.seq_lens, wl.max_seq_len,

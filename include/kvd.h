@@ -163,8 +163,9 @@ typedef struct kvd_cache {
  * hold their final values when the kernel launched just before this call
  * starts, and that no kernel still running writes them (for example: they
  * are set by host copies at the start of a decode step and read by every
- * layer). kvd_gqa_decode and kvd_gqa_append_decode then read them, and plan
- * their work, while that kernel finishes. Other calls ignore the flag.
+ * layer). kvd_gqa_decode, kvd_gqa_append_decode and kvd_indexer_topk then
+ * read them, and plan their work, while that kernel finishes. Other calls
+ * ignore the flag.
  *
  * KVD_SEQS_PREFIX_READY (only with KVD_SEQS_STABLE) declares as well that
  * every cache row the call reads at a position below seq_lens[b] - 1
@@ -173,11 +174,11 @@ typedef struct kvd_cache {
  * position, seq_lens[b] - 1, may be written by that kernel (a kv_append of
  * this step), or by kvd_gqa_append_decode itself. That holds in a decode
  * step, where older rows were appended by earlier steps; it does not hold
- * right after kvd_copy_blocks, which writes older rows. kvd_gqa_decode and
- * kvd_gqa_append_decode may then start copying those rows while that
- * kernel finishes (the query rows, and everything written, still wait for
- * it); the CUDA-core kernel (query groups of 1, 2 or 4) does. Other calls
- * ignore the flag.
+ * right after kvd_copy_blocks, which writes older rows. kvd_gqa_decode,
+ * kvd_gqa_append_decode and kvd_indexer_topk may then start copying those
+ * rows while that kernel finishes (the query rows, and everything written,
+ * still wait for it); the CUDA-core decode kernel (query groups of 1, 2 or
+ * 4) and the indexer's scores do. Other calls ignore the flag.
  */
 #define KVD_SEQS_STABLE 1
 #define KVD_SEQS_PREFIX_READY 2

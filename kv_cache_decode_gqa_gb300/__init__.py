@@ -238,13 +238,15 @@ def mla_decode(cache, block_table, seq_lens, max_seq_len, q, d_c=512,
 
 
 def indexer_topk(cache, block_table, seq_lens, max_seq_len, q_idx, w, k,
-                 indices=None, scores=None, workspace=None, stream=None):
-    """Indexer scores + top-k: returns (indices [batch][k] int32, scores)."""
+                 indices=None, scores=None, workspace=None, stream=None,
+                 seqs_flags=0):
+    """Indexer scores + top-k: returns (indices [batch][k] int32, scores).
+    seqs_flags: SEQS_STABLE [| SEQS_PREFIX_READY] (see kvd_seqs)."""
     import torch
     _need(q_idx, "q_idx", torch.bfloat16)
     _need(w, "w", torch.float32, q_idx.shape[0] * q_idx.shape[1])
     c = cache.struct()
-    s = _seqs(block_table, seq_lens, max_seq_len)
+    s = _seqs(block_table, seq_lens, max_seq_len, seqs_flags)
     B = q_idx.shape[0]
     if indices is None:
         indices = torch.empty((B, k), dtype=torch.int32, device=q_idx.device)

@@ -810,6 +810,7 @@ kvd_status indexer_topk_impl(const kvd_cache *index_cache,
   p.pool = pool;
   p.pool_n = pool_n;
   p.max_entries = entries;
+  p.flags = seqs->flags;
   p.err = d->err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = launched(kvd::launch_indexer_scores(p, s), "indexer_topk (scores)");

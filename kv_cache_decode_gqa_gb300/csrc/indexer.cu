@@ -87,7 +87,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __shared__ int s_scan[32];
   __shared__ int s_start[3];  // first sequence, its first slice, slices
   pdl_trigger();
-  pdl_wait();
+  // With stable lengths and block tables (no pool), the plan is made while
+  // the kernel before finishes; with a ready prefix, the copies of slices
+  // without a sequence's newest row go out then too. Queries, weights, the
+  // newest rows and every write wait for it.
+  const bool early = (p.flags & FLAG_SEQS_STABLE) && !p.pool;
+  const bool prefix = early && (p.flags & FLAG_PREFIX_READY);
+  bool waited = !early;
+  if (waited) pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.batch, bs = p.block_size;
   const bool pow2 = (bs & (bs - 1)) == 0;
@@ -145,9 +152,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   int cb = s_start[0], cs = s_start[1];  // next slice to resolve
   int k0 = 0;                            // its index in the CTA's run
   const int g = lane >> 2, t4 = lane & 3;
-  uint32_t qf[4][2];  // B fragments: head g, dims 16 kt + 2 t4 (+8)
-  float w0 = 0.f, w1 = 0.f;  // weights of heads 2 t4, 2 t4 + 1
-  int qb = -1;  // the sequence whose query qf holds
+  // B fragments (head g, dims 16 kt + 2 t4 and + 8) and the weights of
+  // heads 2 t4, 2 t4 + 1 of the sequence qb; the next sequence's are loaded
+  // when its first slice's copies go out
+  uint32_t qf[4][2], qn[4][2];
+  float w0 = 0.f, w1 = 0.f, wn0 = 0.f, wn1 = 0.f;
+  int qb = -1, qbn = -1;
+  auto load_query = [&](int b, uint32_t (&f)[4][2], float &x0, float &x1) {
+    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+        p.q + ((long)b * p.n_heads + min(g, p.n_heads - 1)) * kIdxDim);
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      f[kt][0] = g < p.n_heads ? q32[8 * kt + t4] : 0u;
+      f[kt][1] = g < p.n_heads ? q32[8 * kt + 4 + t4] : 0u;
+    }
+    const float *wb = p.w + (long)b * p.n_heads;
+    x0 = 2 * t4 < p.n_heads ? wb[2 * t4] : 0.f;
+    x1 = 2 * t4 + 1 < p.n_heads ? wb[2 * t4 + 1] : 0.f;
+  };
+  const bool two_lanes = p.n_heads <= 4;  // heads on lanes t4 = 0, 1 only
   uint8_t *wring = ring + warp * kDepth * kSliceBytes;
   for (;;) {
     // ---- resolve the next window of up to 256 slices of the run (the same
@@ -258,6 +281,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const SliceJob &J = s_job[warp][mi];
         const int rows = J.rows, np = J.np;
         uint8_t *dst = wring + (mi % kDepth) * kSliceBytes;
+        if (!waited && !(prefix && J.tw + rows < J.T)) {
+          pdl_wait();
+          waited = true;
+        }
+        if (waited && J.b != qbn && J.b != qb) {  // its query travels with it
+          qbn = J.b;
+          load_query(qbn, qn, wn0, wn1);
+        }
         if (p.pool) {
           // rows 8 q .. 8 q + 7 are pool block q: row r of chunk j is in
           // block j / 2
@@ -317,53 +348,82 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       cp_async_commit();  // one group a step (empty past the last slice)
       if (m < 0) continue;
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
       cp_async_wait<2>();  // slice m has landed (this lane's copies)
       __syncwarp();        // ... and every lane's
       const SliceJob &J = s_job[warp][m];
       const int b = J.b, tw = J.tw, rows = J.rows, T = J.T;
       if (b != qb) {
-        qb = b;
-        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
-            p.q + ((long)b * p.n_heads + min(g, p.n_heads - 1)) * kIdxDim);
+        if (b == qbn) {
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          qf[kt][0] = g < p.n_heads ? q32[8 * kt + t4] : 0u;
-          qf[kt][1] = g < p.n_heads ? q32[8 * kt + 4 + t4] : 0u;
+          for (int kt = 0; kt < 4; ++kt) {
+            qf[kt][0] = qn[kt][0];
+            qf[kt][1] = qn[kt][1];
+          }
+          w0 = wn0;
+          w1 = wn1;
+        } else {  // a sequence of fewer than three slices came between
+          load_query(b, qf, w0, w1);
         }
-        const float *wb = p.w + (long)b * p.n_heads;
-        w0 = 2 * t4 < p.n_heads ? wb[2 * t4] : 0.f;
-        w1 = 2 * t4 + 1 < p.n_heads ? wb[2 * t4 + 1] : 0.f;
+        qb = b;
       }
       const uint32_t sbase = smem_u32(wring + (m % kDepth) * kSliceBytes);
       float *out = p.scores + (long)b * p.score_stride + tw;
+      // the matrix loads of k-step kt + 1 go out before the MMAs of step
+      // kt, which are independent across the four row tiles
       float c[4][4];
+      uint32_t a[2][4][4];
 #pragma unroll
       for (int rt = 0; rt < 4; ++rt) {
         c[rt][0] = c[rt][1] = c[rt][2] = c[rt][3] = 0.f;
-        const int lr = 16 * rt + (lane & 15);  // this lane's ldmatrix row
+      }
+      auto load_a = [&](int kt, uint32_t (&dst)[4][4]) {
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
+        for (int rt = 0; rt < 4; ++rt) {
+          const int lr = 16 * rt + (lane & 15);  // this lane's ldmatrix row
           const int chunk = 2 * kt + (lane >> 4);
-          uint32_t a[4];
-          ldsm_x4(a, sbase + lr * 128 + ((chunk ^ (lr & 7)) << 4));
-          mma_bf16(c[rt], a, qf[kt][0], qf[kt][1]);
+          ldsm_x4(dst[rt], sbase + lr * 128 + ((chunk ^ (lr & 7)) << 4));
         }
+      };
+      load_a(0, a[0]);
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        if (kt < 3) load_a(kt + 1, a[(kt + 1) & 1]);
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt)
+          mma_bf16(c[rt], a[kt & 1][rt], qf[kt][0], qf[kt][1]);
       }
       __syncwarp();  // every lane has read the slot before it is refilled
+      // rows 16 rt + g (s[rt][0]) and 16 rt + g + 8 (s[rt][1]): heads 2 t4
+      // and 2 t4 + 1 here, summed over the lanes t4
+      float sv[4][2];
 #pragma unroll
       for (int rt = 0; rt < 4; ++rt) {
-        // rows 16 rt + g and 16 rt + g + 8, heads 2 t4 and 2 t4 + 1
-        float s0 = fmaf(w1, fmaxf(c[rt][1], 0.f), w0 * fmaxf(c[rt][0], 0.f));
-        float s1 = fmaf(w1, fmaxf(c[rt][3], 0.f), w0 * fmaxf(c[rt][2], 0.f));
-        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-        if (t4 == 0) {
+        sv[rt][0] = fmaf(w1, fmaxf(c[rt][1], 0.f), w0 * fmaxf(c[rt][0], 0.f));
+        sv[rt][1] = fmaf(w1, fmaxf(c[rt][3], 0.f), w0 * fmaxf(c[rt][2], 0.f));
+      }
+#pragma unroll
+      for (int rt = 0; rt < 4; ++rt) {
+        sv[rt][0] += __shfl_xor_sync(0xffffffffu, sv[rt][0], 1);
+        sv[rt][1] += __shfl_xor_sync(0xffffffffu, sv[rt][1], 1);
+      }
+      if (!two_lanes) {
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt) {
+          sv[rt][0] += __shfl_xor_sync(0xffffffffu, sv[rt][0], 2);
+          sv[rt][1] += __shfl_xor_sync(0xffffffffu, sv[rt][1], 2);
+        }
+      }
+      if (t4 == 0) {
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int r = 16 * rt + g + 8 * hh;
-            float sc = hh ? s1 : s0;
+            float sc = sv[rt][hh];
             if (r < rows) {
               if (p.pool) {  // a position past the visible length: -inf
                 const int pos0 = J.pos0[r / kPoolBlock];
@@ -445,8 +505,8 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 
 constexpr int kCluster = 8;            // CTAs per sequence
 constexpr int kCacheKeys = 20 * 1024;  // keys a CTA keeps in shared memory
-constexpr int kOwnCap = 4096;          // candidates a CTA collects
-constexpr int kGatherCap = 16384;      // candidates of the whole cluster
+constexpr int kHiCap = 4096;           // high keys a CTA lists
+constexpr int kGatherCap = 12288;      // high keys of the whole cluster
 
 // The digit (high digits first) whose bin holds the remaining-th largest
 // key, and the count of keys in the bins above it, into *s_digit and
@@ -489,37 +549,40 @@ __device__ __forceinline__ void find_digit(int nb, int remaining, Load load,
 //     the cluster through distributed shared memory in two steps of
 //     16-byte remote loads (CTA r sums the 8 copies of its eighth of the
 //     bins, then every thread reads the totals of its bins from their
-//     owners), giving every CTA the digit d1 of the k-th largest key and
-//     the count of keys above d1's bin.
-//  2. Each CTA counts its keys above d1's bin and collects its candidates
-//     (keys in d1's bin); every CTA then copies the cluster's candidates
-//     (about the k-th key's share of one bin, a few thousand at most for
-//     continuous scores) into its own shared memory and finishes the
-//     select on them alone: two local passes on bits 19..8 and 7..0 give
-//     the k-th largest key K* and how many keys equal to K* to take, and
-//     the candidates of each source CTA above / equal to K* place every
-//     CTA's selections after those of the lower-ranked CTAs.
-//  3. If the candidates do not fit (4,096 a CTA, 16,384 a cluster: many
-//     equal or near-equal scores), the cluster instead runs the second and
-//     third digits as cluster-wide passes over every key, as in step 1.
-//  4. A sweep in position order writes the selections.
+//     owners), giving every CTA the digit d1 of the k-th largest key.
+//  2. Each CTA lists its high keys (first digit >= d1: every selection is
+//     one of them), with their positions, in position order: about k / 8
+//     plus a share of d1's bin. Every CTA copies the cluster's high keys
+//     into its own shared memory and finishes the select on those in d1's
+//     bin alone: two local passes on bits 19..8 and 7..0 give the k-th
+//     largest key K* and how many keys equal to K* to take; the high keys
+//     of each source CTA above / equal to K* place every CTA's selections
+//     after those of the lower-ranked CTAs, and a pass over its own list
+//     writes them.
+//  3. If the high keys do not fit (4,096 a CTA, 12,288 a cluster: a large
+//     k, or many equal or near-equal scores), the cluster instead runs the
+//     second and third digits as cluster-wide passes over every key, as in
+//     step 1, and a sweep over every key in position order writes the
+//     selections.
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const IndexerParams p) {
   __shared__ __align__(16) int hist[2][kBins];
   __shared__ __align__(16) int tot[kBins];  // cluster totals, own eighth
   __shared__ int tmp[32];
   __shared__ int s_digit, s_above;
-  __shared__ int s_pub[2];           // keys above d1's bin, candidates
-  __shared__ int s_all[2][kCluster];  // every CTA's s_pub
-  __shared__ int s_src[2][kCluster];  // candidates above / equal to K*
-  __shared__ int s_run[2];            // lower-ranked CTAs: selections, K*s
-  __shared__ int s_off[kCluster + 1];  // candidates of the lower ranks
-  __shared__ int s_counts[2];         // this CTA's keys above / equal to K*
+  __shared__ int s_nhi;                // this CTA's high keys
+  __shared__ int s_off[kCluster + 1];  // high keys of the lower ranks
+  __shared__ int s_src[2][kCluster];   // high keys above / equal to K*
+  __shared__ int s_run[3];  // lower ranks' selections and K*s, own K*s
+  __shared__ int s_counts[2];  // this CTA's keys above / equal to K*
   __shared__ int s_wsum[32];
-  // [kOwnCap] own candidates, [kGatherCap] the cluster's, [n] keys
+  // [kHiCap] high keys, [kHiCap] their indices, [kGatherCap] the
+  // cluster's high keys, [n] keys
   extern __shared__ uint32_t dsm[];
-  uint32_t *s_own = dsm, *s_gath = dsm + kOwnCap;
-  uint32_t *s_keys = dsm + kOwnCap + kGatherCap;
+  uint32_t *s_hik = dsm;
+  int *s_hii = reinterpret_cast<int *>(dsm + kHiCap);
+  uint32_t *s_gath = dsm + 2 * kHiCap;
+  uint32_t *s_keys = dsm + 2 * kHiCap + kGatherCap;
   pdl_trigger();
   pdl_wait();
   const uint32_t rank = cluster_rank();
@@ -551,13 +614,12 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int r0 = (int)((long)T * rank / kCluster);
   const int r1 = (int)((long)T * (rank + 1) / kCluster);
   const int n = r1 - r0;
-  const bool cached =
-      (uint32_t)(kOwnCap + kGatherCap + n) * 4u <= dynamic_smem_bytes();
+  const bool cached = (uint32_t)(2 * kHiCap + kGatherCap + n) * 4u <=
+                      dynamic_smem_bytes();
   auto key_at = [&](int i) {  // i relative to r0, 0 <= i < n
     return cached ? s_keys[i] : score_key(sc[r0 + i]);
   };
   for (int i = tid; i < kBins; i += kTopkThreads) hist[0][i] = 0;
-  if (tid < 2) s_pub[tid] = 0;
   if (tid < 2 * kCluster) s_src[tid / kCluster][tid % kCluster] = 0;
   __syncthreads();
   // ---- 1. keys, and the cluster's histogram of the first digit ----
@@ -621,50 +683,45 @@ __global__ void __launch_bounds__(kTopkThreads)
   cluster_digit(hist[0], kBins, k);
   const uint32_t d1 = (uint32_t)s_digit;
   int remaining = k - s_above;  // keys still to take at or below d1's bin
-  // ---- 2. keys above d1's bin, and the candidates ----
+  // ---- 2. this CTA's high keys in position order ----
   // Warp w owns the runs of kRun positions [base + w kRun, + kRun); lane l
-  // takes positions run + 32 j + l, so one ballot per j ranks the lanes.
+  // takes positions run + 32 j + l, so position order within a run is
+  // (j, l) and one ballot per j ranks the lanes; a scan over the 32 warp
+  // totals places the warps after each other.
   constexpr int kRun = 512;  // positions per warp and round
   {
-    int gt = 0;
+    int nhi = 0;  // high keys of the earlier rounds
     for (int base = 0; base < n; base += kRun * 32) {
       const int run = base + wid * kRun;
       uint32_t key[kRun / 32];
-      unsigned eqb[kRun / 32];
-      int weq = 0;
+      unsigned hib[kRun / 32];
+      int whi = 0;
 #pragma unroll
       for (int j = 0; j < kRun / 32; ++j) {
         const int i = run + 32 * j + lane;
         key[j] = i < n ? key_at(i) : 0u;
-        const uint32_t d = key[j] >> 20;
-        gt += i < n && d > d1;
-        eqb[j] = __ballot_sync(0xffffffffu, i < n && d == d1);
-        weq += __popc(eqb[j]);
+        hib[j] = __ballot_sync(0xffffffffu, i < n && (key[j] >> 20) >= d1);
+        whi += __popc(hib[j]);
       }
-      int at = 0;
-      if (lane == 0 && weq > 0) at = atomicAdd(&s_pub[1], weq);
-      at = __shfl_sync(0xffffffffu, at, 0);
+      int tot_hi;
+      int at = nhi + warp_excl_scan(whi, s_wsum, &tot_hi);
 #pragma unroll
       for (int j = 0; j < kRun / 32; ++j) {
-        const int idx = at + __popc(eqb[j] & lt);
-        if (((eqb[j] >> lane) & 1) && idx < kOwnCap) s_own[idx] = key[j];
-        at += __popc(eqb[j]);
+        const int idx = at + __popc(hib[j] & lt);
+        if (((hib[j] >> lane) & 1) && idx < kHiCap) {
+          s_hik[idx] = key[j];
+          s_hii[idx] = run + 32 * j + lane;
+        }
+        at += __popc(hib[j]);
       }
+      nhi += tot_hi;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      gt += __shfl_xor_sync(0xffffffffu, gt, off);
-    if (lane == 0 && gt > 0) atomicAdd(&s_pub[0], gt);
+    if (tid == 0) s_nhi = nhi;
   }
-  cluster_sync();  // every CTA's counts and candidates are complete
+  cluster_sync();  // every CTA's high keys are listed
   if (wid == 0) {
-    int g = 0, c = 0;
-    if (lane < kCluster) {
-      g = *cluster_ptr(&s_pub[0], (uint32_t)lane);
-      c = *cluster_ptr(&s_pub[1], (uint32_t)lane);
-      s_all[0][lane] = g;
-      s_all[1][lane] = c;
-    }
+    int c = lane < kCluster ? *cluster_ptr(&s_nhi, (uint32_t)lane) : 0;
+    const bool over = __any_sync(0xffffffffu, c > kHiCap);
     int inc = c;
 #pragma unroll
     for (int o = 1; o < kCluster; o <<= 1) {
@@ -672,15 +729,13 @@ __global__ void __launch_bounds__(kTopkThreads)
       if (lane >= o) inc += y;
     }
     if (lane == 0) s_off[0] = 0;
-    if (lane < kCluster) s_off[lane + 1] = inc;
+    if (lane < kCluster) s_off[lane + 1] = over ? kGatherCap + 1 : inc;
   }
   __syncthreads();
-  bool fits = true;
-#pragma unroll
-  for (int q = 0; q < kCluster; ++q) fits = fits && s_all[1][q] <= kOwnCap;
   const int C = s_off[kCluster];
-  fits = fits && C <= kGatherCap;  // the same decision in every CTA
-  auto source = [&](int i) {  // the CTA candidate i came from
+  const bool fits = C <= kGatherCap;  // the same decision in every CTA
+  const int nhi = s_nhi;
+  auto source = [&](int i) {  // the CTA gathered key i came from
     int q = 0;
 #pragma unroll
     for (int j = 1; j < kCluster; ++j) q += i >= s_off[j];
@@ -691,34 +746,37 @@ __global__ void __launch_bounds__(kTopkThreads)
   if (fits) {
     for (int i = tid; i < C; i += kTopkThreads) {
       const int q = source(i);
-      s_gath[i] = *cluster_ptr(&s_own[i - s_off[q]], (uint32_t)q);
+      s_gath[i] = *cluster_ptr(&s_hik[i - s_off[q]], (uint32_t)q);
     }
     // done with the other CTAs' shared memory; the matching wait comes
     // before this CTA leaves
     cluster_arrive();
     for (int i = tid; i < kBins; i += kTopkThreads) hist[1][i] = 0;
     __syncthreads();
-    for (int i = tid; i < C; i += kTopkThreads)
-      atomicAdd(&hist[1][(s_gath[i] >> 8) & 0xfff], 1);
+    for (int i = tid; i < C; i += kTopkThreads) {
+      const uint32_t key = s_gath[i];
+      if ((key >> 20) == d1) atomicAdd(&hist[1][(key >> 8) & 0xfff], 1);
+    }
     __syncthreads();
-    auto local4096 = [&](int d0, int, int (&cnt)[4]) {
-      const int4 v = *reinterpret_cast<const int4 *>(&hist[1][d0]);
-      cnt[0] = v.x, cnt[1] = v.y, cnt[2] = v.z, cnt[3] = v.w;
-    };
-    find_digit(kBins, remaining, local4096, tmp, &s_digit, &s_above);
-    const uint32_t d2 = (uint32_t)s_digit;
+    find_digit(kBins, remaining,
+               [&](int d0, int, int (&cnt)[4]) {
+                 const int4 v = *reinterpret_cast<const int4 *>(&hist[1][d0]);
+                 cnt[0] = v.x, cnt[1] = v.y, cnt[2] = v.z, cnt[3] = v.w;
+               },
+               tmp, &s_digit, &s_above);
+    const uint32_t p2 = (d1 << 12) | (uint32_t)s_digit;  // bits 31..8
     remaining -= s_above;
     for (int i = tid; i < 256; i += kTopkThreads) hist[0][i] = 0;
     __syncthreads();
     for (int i = tid; i < C; i += kTopkThreads) {
       const uint32_t key = s_gath[i];
-      if (((key >> 8) & 0xfff) == d2) atomicAdd(&hist[0][key & 0xff], 1);
+      if ((key >> 8) == p2) atomicAdd(&hist[0][key & 0xff], 1);
     }
     __syncthreads();
     find_digit(256, remaining,
                [&](int d0, int, int (&cnt)[4]) { cnt[0] = hist[0][d0]; },
                tmp, &s_digit, &s_above);
-    kstar = (d1 << 20) | (d2 << 8) | (uint32_t)s_digit;
+    kstar = (p2 << 8) | (uint32_t)s_digit;
     need_eq = remaining - s_above;
     for (int i = tid; i < C; i += kTopkThreads) {
       const uint32_t key = s_gath[i];
@@ -729,7 +787,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       int sel = 0, eq = 0;
       for (uint32_t q = 0; q < rank; ++q) {
         const int e = s_src[1][q];
-        sel += s_all[0][q] + s_src[0][q] + max(0, min(e, need_eq - eq));
+        sel += s_src[0][q] + max(0, min(e, need_eq - eq));
         eq += e;
       }
       s_run[0] = sel;
@@ -738,8 +796,30 @@ __global__ void __launch_bounds__(kTopkThreads)
     __syncthreads();
     run_sel = s_run[0];
     run_eq = s_run[1];
-  } else {
-    // ---- 3. cluster-wide passes on bits 19..8 and 7..0 ----
+    // ---- the selections: this CTA's high keys in position order ----
+    for (int base = 0; base < nhi; base += kTopkThreads) {
+      const int e = base + tid;
+      const uint32_t key = e < nhi ? s_hik[e] : 0u;
+      const bool eq = e < nhi && key == kstar;
+      const unsigned eqb = __ballot_sync(0xffffffffu, eq);
+      int tot_eq;
+      const int rank_eq = run_eq +
+                          warp_excl_scan(__popc(eqb), s_wsum, &tot_eq) +
+                          __popc(eqb & lt);
+      const bool sel = (e < nhi && key > kstar) || (eq && rank_eq < need_eq);
+      const unsigned selb = __ballot_sync(0xffffffffu, sel);
+      int tot_sel;
+      const int at = run_sel + warp_excl_scan(__popc(selb), s_wsum, &tot_sel) +
+                     __popc(selb & lt);
+      if (sel && at < k) out[at] = position(r0 + s_hii[e]);
+      run_eq += tot_eq;
+      run_sel += tot_sel;
+    }
+    cluster_wait();  // no CTA leaves while another may read its list
+    return;
+  }
+  // ---- 3. cluster-wide passes on bits 19..8 and 7..0 ----
+  {
     uint32_t prefix = d1;
     const int shifts[2] = {8, 0};
     const int widths[2] = {12, 8};
@@ -772,7 +852,9 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     kstar = prefix;
     need_eq = remaining;
-    // counts of this CTA's keys above / equal to K*, placed by rank
+  }
+  // counts of this CTA's keys above / equal to K*, placed by rank
+  {
     int my_gt = 0, my_eq = 0;
     for (int i = tid; i < n; i += kTopkThreads) {
       const uint32_t key = key_at(i);
@@ -799,10 +881,9 @@ __global__ void __launch_bounds__(kTopkThreads)
       run_eq += e;
     }
   }
-  // ---- 4. compaction of this CTA's range in position order ----
-  // A first sweep counts each warp's keys equal to K*, a second decides
-  // every selection, a third writes the positions; block scans over the 32
-  // warp totals place the warps after each other.
+  // the selections: a sweep over every key in position order. A first
+  // sweep counts each warp's keys equal to K*, a second decides every
+  // selection, a third writes the positions.
   for (int base = 0; base < n; base += kRun * 32) {
     const int run = base + wid * kRun;
     unsigned gtb[kRun / 32], eqb[kRun / 32];
@@ -840,11 +921,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     run_eq += tot_eq;
     run_sel += tot_sel;
   }
-  // no CTA leaves while another may read its shared memory
-  if (fits)
-    cluster_wait();
-  else
-    cluster_sync();
+  cluster_sync();  // no CTA leaves while another may read its counts
 }
 
 }  // namespace
@@ -927,7 +1004,7 @@ cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s) {
 
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
-  constexpr int kCandBytes = (kOwnCap + kGatherCap) * 4;
+  constexpr int kCandBytes = (2 * kHiCap + kGatherCap) * 4;
   static bool done[64] = {};
   cudaError_t e =
       set_smem_once(topk_kernel, kCandBytes + kCacheKeys * 4, done);

@@ -97,6 +97,7 @@ struct IndexerParams {
   const int32_t *pool;    // [batch][kPoolBlocks] ascending block ids
   const int32_t *pool_n;  // [batch] blocks in the pool
   int32_t max_entries;    // launch sizing: max_seq_len, or 8 * kPoolBlocks
+  int32_t flags;          // kvd_seqs flags (scores: honoured without a pool)
   int *err;
 };
 

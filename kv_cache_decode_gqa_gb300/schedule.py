@@ -25,7 +25,7 @@ def sparse_schedule_step(modes, cache, idx_cache, block_table, pos, seq_lens,
                          k_new=None, v_new=None, idx_k_new=None,
                          workspaces=None, topk_workspace=None, lses=None,
                          pool_k=None, pool=None, pool_n=None,
-                         pool_workspace=None, stream=None):
+                         pool_workspace=None, stream=None, seqs_flags=0):
     """One decode step through a static schedule.
 
     modes[l] in MODES (the first layer may not be "reuse"); q[l], q_idx[l],
@@ -35,7 +35,9 @@ def sparse_schedule_step(modes, cache, idx_cache, block_table, pos, seq_lens,
     own key and value). With ``pool_k``, Reindex layers select
     ``pool_k`` positions inside the first Full layer's pool (``pool`` /
     ``pool_n``: optional buffers; ``indices[l]`` of those layers then hold
-    ``pool_k`` entries). Returns the index tensor each layer attended to.
+    ``pool_k`` entries). ``seqs_flags`` (SEQS_STABLE, SEQS_PREFIX_READY)
+    passes to the indexer calls. Returns the index tensor each layer
+    attended to.
     """
     if modes and modes[0] == "reuse":
         raise ValueError("the first layer must pick its own top-k")
@@ -59,7 +61,8 @@ def sparse_schedule_step(modes, cache, idx_cache, block_table, pos, seq_lens,
             current = indices[layer]
             indexer_topk(idx_cache, block_table, seq_lens, max_seq_len,
                          q_idx[layer], w[layer], k, indices=current,
-                         workspace=topk_workspace, stream=stream)
+                         workspace=topk_workspace, stream=stream,
+                         seqs_flags=seqs_flags)
             if mode == "full" and pool_k is not None and not pooled:
                 pool, pool_n = indexer_pool(block_table, seq_lens,
                                             max_seq_len, current, pool=pool,

@@ -209,6 +209,37 @@ def test_selection_with_heavy_ties(kind):
         assert np.array_equal(idx[0], np.arange(2048))
 
 
+@pytest.mark.parametrize("flags", [1, 3], ids=["stable", "prefix_ready"])
+def test_seqs_flags_after_an_append(flags):
+    """kvd_indexer_topk with KVD_SEQS_STABLE (plan made while the kernel
+    before finishes) and KVD_SEQS_PREFIX_READY (cached rows copied then
+    too), launched right after the append of this step's indexer keys: the
+    scores, the newest position's included, equal the fp64 oracle's on the
+    appended cache, and the selection is the oracle's rule on them."""
+    s = _shape([20000, 3000, 64, 700], 512, 64, 4)
+    wl = W.DeviceWorkload(s)
+    sc = torch.empty((s.batch, wl.max_seq_len), dtype=torch.float32,
+                     device="cuda")
+    for _ in range(2):                     # the append runs first each time
+        K.kv_append(wl.idx_cache, wl.block_table, wl.pos, wl.idx_k_new)
+        idx, _ = K.indexer_topk(wl.idx_cache, wl.block_table, wl.seq_lens,
+                                wl.max_seq_len, wl.q_idx[0], wl.w[0], s.topk,
+                                scores=sc, seqs_flags=flags)
+    torch.cuda.synchronize()
+    idx, scn = idx.cpu().numpy(), sc.cpu().numpy()
+    ir = _host_idx_cache(s, wl.paging, I.normal_bf16_table())
+    xn = W.host_bf16(s, 0, W.T_IDXKNEW, (s.batch, 1, 64))
+    ir = oracle.kv_append(ir, wl.paging.table, s.lengths, xn, s.block_size)
+    qI = oracle.bf16_bits_to_f64(W.host_bf16(s, 0, W.T_QIDX,
+                                             (s.batch, 4, s.idx_dim)))
+    w = W.host_weights(s, 0).astype(np.float64)
+    ref = oracle.indexer_scores(qI, w, ir, wl.paging.table, s.seq_lens, 64)
+    for b, T in enumerate(s.seq_lens):
+        np.testing.assert_allclose(scn[b, :T], ref[b], rtol=1e-5, atol=1e-4)
+        want = oracle.topk_select(scn[b, :T].astype(np.float64), s.topk)
+        assert np.array_equal(idx[b], want), f"row {b}"
+
+
 def test_schedule_matches_oracle():
     """Full, Reuse x3, Reindex x4 over one main cache and one indexer
     cache (exact indexer inputs, so the selections are identical)."""
