@@ -269,24 +269,19 @@ Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms, bool tc) {
             : plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
 }
 
-// The tcgen05 gather kernel: clusters of kGatherCluster CTAs, G per
-// (sequence, 64-head tile), as many as one wave of resident clusters holds.
-// With G > 1 each cluster leaves one merged slice per CTA (64 heads x
-// 512 / kGatherCluster values fp32 + 64 lse) for the merge launch.
+// The tcgen05 gather kernel: S CTAs per (sequence, 64-head tile), one
+// wave. With S > 1 each CTA leaves its part (64 heads x 512 values fp32 +
+// 64 lse) for the merge launch.
 Plan sparse_plan(const kvd_seqs *s, int n_h, int k, int dv, int sms) {
   Plan pl;
   const int units = std::max(s->batch * (n_h / 64), 1);
-  const int C = kvd::kGatherCluster;
-  int wave = kvd::gather_tc_max_clusters();
-  if (wave <= 0) wave = sms / C;
-  int G = kvd::gather_tc_clusters(units, std::max(k, 1), wave);
-  const int forced = g_decode_ctas.load(std::memory_order_relaxed);
-  if (forced > 0) G = std::min(std::max(1, forced / (units * C)), 4);
-  pl.n_splits = G;
-  pl.n_groups = C;
-  const size_t slots = (size_t)units * G * C;
-  pl.ws_o_bytes = G > 1 ? round_up(slots * 64 * (dv / C) * 4, 256) : 0;
-  pl.ws_lse_bytes = G > 1 ? round_up(slots * 64 * 4, 256) : 0;
+  const int S = kvd::gather_tc_splits(
+      units, std::max(k, 1), sms, g_decode_ctas.load(std::memory_order_relaxed));
+  pl.n_splits = S;
+  pl.n_groups = 1;
+  const size_t slots = (size_t)units * S;
+  pl.ws_o_bytes = S > 1 ? round_up(slots * 64 * dv * 4, 256) : 0;
+  pl.ws_lse_bytes = S > 1 ? round_up(slots * 64 * 4, 256) : 0;
   pl.ws_bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
   return pl;
 }

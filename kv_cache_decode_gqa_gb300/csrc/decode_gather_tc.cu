@@ -22,15 +22,16 @@
 // pieces about twice that with two slices in flight per CTA and more with
 // four; a bulk copy per row lands unswizzled, which the MMA cannot read.
 //
-// Work: a unit is (sequence, 64-head tile) with k index entries. A cluster
-// of 4 CTAs takes a unit, G clusters per unit when there are few units, as
-// many as one wave of resident clusters holds; CTA q of cluster g takes an
-// equal share of the entries, in chunks of 128. The four CTAs' results are
-// merged in distributed shared memory: each CTA leaves its unnormalised O^T,
-// running maxima and sums in its own shared memory, and CTA q merges value
-// columns [128 q, 128 q + 128) of all four (log-sum-exp merge). With G > 1
-// each cluster's merged slices go to the workspace, and a short second
-// launch merges the G slices of every output.
+// Work: a unit is (sequence, 64-head tile) with k index entries, split
+// over S CTAs (one wave: S = SMs / units, at most 32, none with fewer than
+// 32 entries), each taking an equal share of the entries in chunks of 128.
+// With S = 1 a CTA writes the unit's outputs. Otherwise each writes its
+// normalised partial outputs (64 heads x 512 values, fp32: one value per
+// tensor-memory lane, so each store of a warp covers 32 consecutive values)
+// and their log-sum-exps to the workspace, and a short second launch merges
+// the S parts of every output (log-sum-exp merge). (A merge of four CTAs in
+// distributed shared memory, tried first, took longer than the copies: its
+// remote loads were latency-bound with the kernel's 192 threads.)
 //
 // Warp roles (192 threads; at most two warps per SM sub-partition, so a
 // thread may hold up to 255 registers):
@@ -51,7 +52,6 @@
 //     writes its position's row of P (bf16) into the swizzled P tile, and
 //     rescales the tensor-memory O^T columns of heads whose maximum grew.
 #include <cmath>
-#include <mutex>
 
 #include "kvd_common.cuh"
 #include "stream_k.cuh"
@@ -72,9 +72,7 @@ constexpr int kNSlot = 4;
 constexpr int kQCB = kH * 128;                        // Q: one column block
 constexpr int kQBytes = kH * kD * 2;                  // 64 KB
 constexpr int kPBytes = kRows * kH * 2;               // 16 KB
-constexpr int kCluster = kGatherCluster;              // 4
-constexpr int kSliceV = kD / kCluster;                // merged values / CTA
-constexpr int kMaxG = 4;                              // clusters per unit
+constexpr int kMaxS = kGatherMaxSplits;               // CTAs per unit
 constexpr int kMmaWarp = 1;
 constexpr int kSoft0 = 2;                             // first softmax warp
 constexpr int kThreads = 6 * 32;
@@ -88,10 +86,10 @@ constexpr int Q_OFF = 0;
 constexpr int RING_OFF = Q_OFF + kQBytes;
 constexpr int P_OFF = RING_OFF + kNSlot * kSlotBytes;
 constexpr int F_OFF = P_OFF + kPBytes;  // floats: m, l, cr, mu [64] each,
-                                        // red, red2 [4][64], wn [4][64],
-                                        // lse [64]
+                                        // red, red2 [4][64], inverse sums
+                                        // and lse [64] each
 constexpr int F_M = 0, F_L = 64, F_CR = 128, F_MU = 192, F_RED = 256,
-              F_RED2 = 512, F_WN = 768, F_LSE = 1024, F_END = 1088;
+              F_RED2 = 512, F_INV = 768, F_LSE = 832, F_END = 896;
 constexpr int FLAG_OFF = F_OFF + F_END * 4;         // int [8]
 constexpr int ROW_OFF = FLAG_OFF + 32;              // int [128]: chunk rows
 constexpr int BAR_OFF = ROW_OFF + kRows * 4;
@@ -99,21 +97,11 @@ constexpr int BAR_OFF = ROW_OFF + kRows * 4;
 constexpr int kBars = 2 * kNSlot + 6;
 constexpr int SMEM = BAR_OFF + kBars * 8;
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
-static_assert(kD * kH * 4 <= kNSlot * kSlotBytes,
-              "the merge buffer reuses the ring");
-static_assert(kCluster * kH <= 256, "merge weights [cluster][64]");
 
 struct GatherParams {
   DecodeParams p;
   CUtensorMap tq;  // queries [batch * n_h][512] bf16, 64 x 64 boxes
 };
-
-// The epilogue keeps O^T as fp32 [512 values][64 heads] in the ring (128
-// KB), float4 group j of row v at position j ^ (v & 15) (conflict-free
-// stores from one lane per value and loads of consecutive heads).
-__device__ __forceinline__ int obuf_index(int v, int h) {
-  return v * kH + ((((h >> 2) ^ (v & 15)) << 2) | (h & 3));
-}
 
 // Address in a 128-byte-swizzled operand tile of 16-byte piece `c` of row
 // `r`: rows of 128 bytes in 8-row atoms of 1 KB, piece c at c ^ (r % 8).
@@ -163,10 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_m = fs + F_M, *s_l = fs + F_L, *s_cr = fs + F_CR, *s_mu = fs + F_MU;
   float *s_red = fs + F_RED;    // per-warp maxima
   float *s_red2 = fs + F_RED2;  // per-warp sums
-  float *s_wn = fs + F_WN, *s_lse = fs + F_LSE;
+  float *s_inv = fs + F_INV, *s_lse = fs + F_LSE;
   int *flags = reinterpret_cast<int *>(smem + FLAG_OFF);
   volatile int *s_abort = flags;
-  int *s_merge = flags + 1;
   volatile int *s_issued = flags + 2;  // the query tile was requested
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(flags + 3);
   // cache row of each position of the current chunk, -1 for a zero row
@@ -185,20 +172,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();  // after the wait: dependants never overlap this grid's
                   // predecessor
 
-  const int G = p.n_splits;  // clusters per unit
+  const int S = p.n_splits;  // CTAs per unit
   const int tiles = p.n_h / kH;
-  const int q = (int)cluster_rank();
-  const int cl = (int)blockIdx.x / kCluster;
-  const int u = cl / G, g = cl % G;
+  const int u = (int)blockIdx.x / S, part = (int)blockIdx.x % S;
   const int b = u / tiles, ht = u % tiles;
   const int k = p.n_idx;
-  const int parts = G * kCluster, part = g * kCluster + q;
-  const int e0 = (int)((long)k * part / parts);
-  const int e1 = (int)((long)k * (part + 1) / parts);
+  const int e0 = (int)((long)k * part / S);
+  const int e1 = (int)((long)k * (part + 1) / S);
   const int nch = (e1 - e0 + kRows - 1) / kRows;
   int T = p.seq_lens[b];
   if (T > p.max_seq_len) {
-    if (tid == 0 && q == 0 && g == 0 && ht == 0) report(p.err, DEVERR_LEN);
+    if (tid == 0 && part == 0 && ht == 0) report(p.err, DEVERR_LEN);
     T = p.max_seq_len;
   }
   T = max(T, 0);
@@ -215,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ofull, 1);
     mbar_init(done, 1);
     *s_abort = 0;
-    *s_merge = 0;
     *s_issued = 0;
     fence_mbar_init();
   }
@@ -231,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
-  // the swizzled operand tiles assume 1 KB atoms; every CTA sees the same
-  // layout, so all of them skip the work together
+  // the swizzled operand tiles assume 1 KB atoms (every CTA sees the same
+  // layout)
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
   if (!aligned && tid == 0) {
     if (blockIdx.x == 0) report(p.err, DEVERR_TIMEOUT);
@@ -240,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (!aligned) {
-    // nothing to do: every CTA of every cluster takes this branch
+    // nothing to do: every CTA takes this branch
   } else if (warp == 0) {
     // ======================= query tile (TMA) =============================
     if (nch > 0 && lane == 0) {
@@ -504,8 +487,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && *s_abort && *s_issued) mbar_wait(qfull, 0);
   __syncthreads();
 
-  // ======================= this CTA's O^T into the ring ===================
-  float *obuf = reinterpret_cast<float *>(smem + RING_OFF);
+  // ======================= outputs ========================================
+  // per head: 1 / sum and the log-sum-exp of this CTA's part
+  if (tid < kH) {
+    const float L = s_l[tid];
+    const bool any = L > 0.f && !*s_abort && nch > 0;
+    s_inv[tid] = any ? 1.f / L : 0.f;
+    s_lse[tid] =
+        any ? (s_m[tid] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const long bh0 = (long)b * p.n_h + (long)ht * kH;
+  // S = 1: the outputs (bf16); else this CTA's part of the workspace,
+  // [unit][part][64 heads][512 values] fp32 and [unit][part][64] lse
+  const long slot = (long)u * S + part;
   if (warp >= kSoft0) {
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
@@ -513,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool have = nch > 0 && !*s_abort;
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
-      const int v = blk * 128 + r;
+      const int v = blk * 128 + r;  // this lane's value
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t o[32];
@@ -525,169 +522,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) o[j] = 0u;
         }
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const int h = h2 * 32 + 4 * j4;
-          *reinterpret_cast<float4 *>(obuf + obuf_index(v, h)) =
-              make_float4(__uint_as_float(o[4 * j4]),
-                          __uint_as_float(o[4 * j4 + 1]),
-                          __uint_as_float(o[4 * j4 + 2]),
-                          __uint_as_float(o[4 * j4 + 3]));
+        for (int j = 0; j < 32; ++j) {
+          const int h = h2 * 32 + j;
+          const float x = __uint_as_float(o[j]) * s_inv[h];
+          if (S == 1)
+            p.out[(bh0 + h) * kD + v] = f2bf(x);
+          else
+            p.ws_o[(slot * kH + h) * kD + v] = x;
         }
       }
     }
   }
-
-  // ======================= cluster merge ==================================
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // every CTA's O^T, maxima and sums are in its memory
-  // per head: the cluster's maximum, each CTA's normalised weight, lse
   if (tid < kH) {
-    const int h = tid;
-    float mc[kCluster], lc[kCluster];
-    float M = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kCluster; ++c) {
-      mc[c] = *cluster_ptr(&s_m[h], (uint32_t)c);
-      lc[c] = *cluster_ptr(&s_l[h], (uint32_t)c);
-      M = fmaxf(M, mc[c]);
-    }
-    float L = 0.f;
-#pragma unroll
-    for (int c = 0; c < kCluster; ++c) {
-      mc[c] = mc[c] == -INFINITY ? 0.f : ex2(mc[c] - M);
-      L = fmaf(mc[c], lc[c], L);
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int c = 0; c < kCluster; ++c) s_wn[c * kH + h] = mc[c] * inv;
-    s_lse[h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-  }
-  __syncthreads();
-  // value columns [kSliceV q, kSliceV (q + 1)) of the unit, task (4 heads,
-  // 4 values): all kCluster x 4 float4 loads of distributed shared memory
-  // go out before they are used; a warp's loads cover two whole 256-byte
-  // rows
-  const long bh0 = (long)b * p.n_h + (long)ht * kH;
-  // G > 1: this cluster's slice into the workspace, as
-  // [unit][g][q][64 heads][kSliceV values] fp32 and [unit][g][q][64] lse,
-  // for the merge launch
-  const long wslot = ((long)u * G + g) * kCluster + q;
-  constexpr int kTasks = (kH / 4) * (kSliceV / 4);
-  uint32_t peer[kCluster];
-#pragma unroll
-  for (int c = 0; c < kCluster; ++c) peer[c] = cluster_saddr(obuf, (uint32_t)c);
-  // two tasks per round: 2 x kCluster x 4 loads in flight per thread
-  for (int t0 = tid; t0 < kTasks; t0 += 2 * kThreads) {
-    float4 x[2][kCluster][4];
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const int task = t0 + w * kThreads;
-      const int tk = task < kTasks ? task : t0;
-      const int h0 = 4 * (tk & 15), v0 = kSliceV * q + 4 * (tk >> 4);
-#pragma unroll
-      for (int c = 0; c < kCluster; ++c)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          x[w][c][j] = ld_dsmem_f4(peer[c] + 4u * obuf_index(v0 + j, h0));
-    }
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const int task = t0 + w * kThreads;
-      if (task >= kTasks) break;
-      const int h0 = 4 * (task & 15), vl = 4 * (task >> 4);  // vl: in slice
-      const int v0 = kSliceV * q + vl;
-      float4 acc[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < kCluster; ++c) {
-        const float4 wc =
-            *reinterpret_cast<const float4 *>(s_wn + c * kH + h0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[j].x = fmaf(wc.x, x[w][c][j].x, acc[j].x);
-          acc[j].y = fmaf(wc.y, x[w][c][j].y, acc[j].y);
-          acc[j].z = fmaf(wc.z, x[w][c][j].z, acc[j].z);
-          acc[j].w = fmaf(wc.w, x[w][c][j].w, acc[j].w);
-        }
-      }
-      // acc[j] holds heads h0 .. h0 + 3 of value v0 + j
-      const float o[4][4] = {{acc[0].x, acc[1].x, acc[2].x, acc[3].x},
-                             {acc[0].y, acc[1].y, acc[2].y, acc[3].y},
-                             {acc[0].z, acc[1].z, acc[2].z, acc[3].z},
-                             {acc[0].w, acc[1].w, acc[2].w, acc[3].w}};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {  // head h0 + i, values v0 .. v0 + 3
-        if (G == 1) {
-          uint2 w2;
-          w2.x = pack_bf16x2(o[i][0], o[i][1]);
-          w2.y = pack_bf16x2(o[i][2], o[i][3]);
-          *reinterpret_cast<uint2 *>(p.out + (bh0 + h0 + i) * kD + v0) = w2;
-        } else {
-          *reinterpret_cast<float4 *>(
-              p.ws_o + (wslot * kH + h0 + i) * kSliceV + vl) =
-              make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
-        }
-      }
+    if (S == 1) {
+      if (p.lse) p.lse[bh0 + tid] = s_lse[tid];
+    } else {
+      p.ws_lse[slot * kH + tid] = s_lse[tid];
     }
   }
-  if (G == 1) {
-    if (q == 0 && tid < kH && p.lse) p.lse[bh0 + tid] = s_lse[tid];
-  } else {
-    if (tid < kH) p.ws_lse[wslot * kH + tid] = s_lse[tid];
-  }
-  cluster_sync();  // no CTA leaves while another reads its shared memory
+  tc_fence_before();
+  __syncthreads();  // every read of tensor memory is done
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
 }
 
-// The G clusters of a unit leave one merged slice per CTA in the
-// workspace (normalised outputs of 64 heads x kSliceV values and their 64
-// log-sum-exps); this second launch merges the G slices of every output
-// (log-sum-exp merge), one thread per float4 with the loads of all G parts
-// in flight together. Grid: (units, 64 x 512 / 4 / 256).
+// The S CTAs of a unit leave their normalised partial outputs (64 heads x
+// 512 values) and log-sum-exps in the workspace; this second launch merges
+// the S parts of every output (log-sum-exp merge with a running maximum),
+// one thread per float4, the loads of up to 20 parts in flight together
+// (one round for the usual S <= 19; two blocks a SM). Grid: (units, 64 x
+// 512 / 4 / 256).
 constexpr int kGMergeThreads = 256;
+constexpr int kMergeBatch = 20;
 __global__ void __launch_bounds__(kGMergeThreads)
     gather_merge_kernel(const DecodeParams p) {
   pdl_trigger();
-  pdl_wait();  // the slices of the decode launch
-  const int G = p.n_splits;
+  pdl_wait();  // the parts of the decode launch
+  const int S = p.n_splits;
   const int tiles = p.n_h / kH;
   const int u = blockIdx.x, b = u / tiles, ht = u % tiles;
   const int e = blockIdx.y * kGMergeThreads + threadIdx.x;  // float4 index
   if (e >= kH * kD / 4) return;
   const int h = e / (kD / 4), v = 4 * (e % (kD / 4));
-  const int q = v / kSliceV, vl = v % kSliceV;
-  float lv[kMaxG];
-  float4 ov[kMaxG];
-#pragma unroll
-  for (int gi = 0; gi < kMaxG; ++gi) {
-    lv[gi] = -INFINITY;
-    ov[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (gi < G) {
-      const long sl = ((long)u * G + gi) * kCluster + q;
-      lv[gi] = __ldcg(p.ws_lse + sl * kH + h);
-      ov[gi] = __ldcg(reinterpret_cast<const float4 *>(
-          p.ws_o + (sl * kH + h) * kSliceV + vl));
-    }
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int gi = 0; gi < kMaxG; ++gi) M = fmaxf(M, lv[gi]);
-  float W = 0.f;
+  const float *lse = p.ws_lse + (long)u * S * kH + h;
+  const float *o = p.ws_o + ((long)u * S * kH + h) * kD + v;
+  float M = -INFINITY, W = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
+    float l[kMergeBatch];
+    float4 x[kMergeBatch];
 #pragma unroll
-  for (int gi = 0; gi < kMaxG; ++gi) {
-    if (lv[gi] == -INFINITY) continue;  // an empty part adds nothing
-    const float c1 = expf(lv[gi] - M);
-    W += c1;
-    a.x = fmaf(c1, ov[gi].x, a.x);
-    a.y = fmaf(c1, ov[gi].y, a.y);
-    a.z = fmaf(c1, ov[gi].z, a.z);
-    a.w = fmaf(c1, ov[gi].w, a.w);
+    for (int j = 0; j < kMergeBatch; ++j) {
+      l[j] = -INFINITY;
+      if (s0 + j < S) {
+        l[j] = __ldcg(lse + (long)(s0 + j) * kH);
+        x[j] = __ldcg(
+            reinterpret_cast<const float4 *>(o + (long)(s0 + j) * kH * kD));
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) Mn = fmaxf(Mn, l[j]);
+    if (Mn == -INFINITY) continue;  // no part so far has any weight
+    const float r = M == -INFINITY ? 0.f : expf(M - Mn);
+    W *= r;
+    a.x *= r;
+    a.y *= r;
+    a.z *= r;
+    a.w *= r;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (l[j] == -INFINITY) continue;  // an empty part adds nothing
+      const float c = expf(l[j] - Mn);
+      W += c;
+      a.x = fmaf(c, x[j].x, a.x);
+      a.y = fmaf(c, x[j].y, a.y);
+      a.z = fmaf(c, x[j].z, a.z);
+      a.w = fmaf(c, x[j].w, a.w);
+    }
+    M = Mn;
   }
   const long bh = (long)b * p.n_h + (long)ht * kH + h;
   const float iw = W > 0.f ? 1.f / W : 0.f;
@@ -714,57 +629,21 @@ cudaError_t make_rows_map(CUtensorMap *m, const void *base, long rows,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr int kMaxDevices = 64;
-int g_max_clusters[kMaxDevices] = {};
-std::mutex g_max_clusters_mu;
-
 }  // namespace
 
-// Clusters of this kernel one wave holds on the current device (queried
-// once per device), or 0 if it cannot be launched here.
-int gather_tc_max_clusters() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return 0;
-  std::lock_guard<std::mutex> lock(g_max_clusters_mu);
-  if (g_max_clusters[dev] == 0) {
-    auto kern = decode_gather_tc_kernel;
-    int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM) == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(kCluster * 64);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = SMEM;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = kCluster;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
-        n = 0;
-    }
-    g_max_clusters[dev] = n > 0 ? n : -1;
-  }
-  return g_max_clusters[dev] > 0 ? g_max_clusters[dev] : 0;
-}
-
-// Clusters per unit: as many as one wave of resident clusters holds (at
-// least one, at most kMaxG, none whose CTAs would get fewer than 32
-// entries).
-int gather_tc_clusters(int units, int k, int max_clusters) {
-  int G = max_clusters / units;
-  const int cap = (k + kCluster * 32 - 1) / (kCluster * 32);
-  G = G < cap ? G : cap;
-  G = G < kMaxG ? G : kMaxG;
-  return G < 1 ? 1 : G;
+// CTAs per unit: one wave (SMs / units), at most kGatherMaxSplits, none with
+// fewer than 32 entries; `forced` > 0 asks for that many CTAs in all.
+int gather_tc_splits(int units, int k, int sms, int forced) {
+  int S = forced > 0 ? forced / units : sms / units;
+  const int cap = (k + 31) / 32;
+  if (forced <= 0) S = S < cap ? S : cap;
+  S = S < kMaxS ? S : kMaxS;
+  return S < 1 ? 1 : S;
 }
 
 cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s) {
   if (p.dk != kD || p.dv != kD || p.n_h % kH != 0 || p.n_kv != 1 ||
-      p.n_splits < 1 || p.n_splits > kMaxG ||
+      p.n_splits < 1 || p.n_splits > kMaxS ||
       (long)p.num_blocks * p.block_size >= (1L << 31) - 1 ||
       (long)p.batch * p.n_h >= (1L << 31) || !tensor_map_encoder())
     return cudaErrorNotSupported;
@@ -776,10 +655,9 @@ cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s) {
   static bool done[64] = {};
   e = set_smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
-  const long ctas = (long)p.batch * (p.n_h / kH) * p.n_splits * kCluster;
+  const long ctas = (long)p.batch * (p.n_h / kH) * p.n_splits;
   if (ctas == 0) return cudaSuccess;
-  e = launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), SMEM, s,
-                 kCluster, gp);
+  e = launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), SMEM, s, 1, gp);
   if (e != cudaSuccess || p.n_splits == 1) return e;
   const dim3 grid((unsigned)(p.batch * (p.n_h / kH)),
                   kH * kD / 4 / kGMergeThreads);

@@ -145,12 +145,10 @@ cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s);
 // positions: 32 for the CUDA-core kernel, 64 for the tensor-core one).
 cudaError_t launch_merge_mla(const DecodeParams &p, int rows, cudaStream_t s);
 // Gathered-position decode (dk = dv = 512, n_kv 1, n_h multiple of 64) on
-// tcgen05: clusters of kGatherCluster CTAs, n_splits = clusters per
-// (sequence, 64-head tile), as gather_tc_clusters plans them for one wave
-// of gather_tc_max_clusters() resident clusters.
-constexpr int kGatherCluster = 4;
-int gather_tc_max_clusters();
-int gather_tc_clusters(int units, int k, int max_clusters);
+// tcgen05: n_splits = CTAs per (sequence, 64-head tile), as
+// gather_tc_splits plans them (`forced` > 0: that many CTAs in all).
+constexpr int kGatherMaxSplits = 32;
+int gather_tc_splits(int units, int k, int sms, int forced);
 cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_indexer_scores(const IndexerParams &p, cudaStream_t s);
 cudaError_t launch_topk(const IndexerParams &p, cudaStream_t s);

@@ -174,19 +174,22 @@ def _sparse_case(lengths, k, bs, n_h=64, seed=77, idx=None, lens=None):
     return out, lse, ref, ref_lse
 
 
-# The tensor-core gather kernel's work split: 8-CTA clusters per (sequence,
-# 64-head tile), G clusters per unit. Two head tiles; a k that is no
-# multiple of anything; k smaller than the CTAs of a unit (most CTAs get no
-# entry); several 128-entry chunks per CTA (the online rescale across
-# chunks, forced with a small CTA count); many clusters per unit (the
-# workspace merge of G parts, forced with a large CTA count).
+# The tensor-core gather kernel's work split: S CTAs per (sequence, 64-head
+# tile). Two head tiles; a k that is no multiple of anything; k smaller
+# than the CTAs of a unit (most CTAs get no entry); several 128-entry
+# chunks per CTA (the online rescale across chunks, forced with a small CTA
+# count); the most CTAs per unit (32, the workspace merge of 32 parts,
+# forced with a large CTA count); one CTA per unit (outputs written
+# directly).
 @pytest.mark.parametrize("lengths,k,bs,n_h,ctas", [
     ([300, 1200, 9], 1000, 64, 128, 0),
     ([40, 3], 5, 16, 64, 0),
     ([6000], 5000, 64, 64, 8),
     ([3000, 2500], 2048, 32, 64, 1024),
+    ([9000, 100, 4000, 2], 3000, 64, 64, 4),
     ([9000, 100, 4000, 2], 3000, 64, 64, 16),
-], ids=["h128_k1000", "k5", "chunks_per_cta", "clusters_max", "b4_g1"])
+], ids=["h128_k1000", "k5", "chunks_per_cta", "splits_max", "b4_s1",
+        "b4_s4"])
 def test_sparse_work_splits(lengths, k, bs, n_h, ctas):
     K.set_tuning(decode_ctas=ctas)
     try:
