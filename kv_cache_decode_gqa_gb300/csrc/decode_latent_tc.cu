@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_issued = 0;
   }
   __syncthreads();
-  build_partition(wp, p, s_len_err, kRows, 1, 0);
+  build_partition(wp, p, s_len_err, kRows, 1);
   if (tid == 0 && blockIdx.x == 0 && *s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
   const int lanes = (int)gridDim.x / per_lane;

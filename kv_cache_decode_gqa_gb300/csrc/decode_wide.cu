@@ -1,13 +1,10 @@
-// Decode attention for 64-head query tiles against wide cached rows, on the
-// tensor cores (warp-level m16n8k16 MMA, fp32 accumulators):
-//
-//  * latent (MLA) decode ("KV cache", "Caching a compressed latent instead
-//    of the keys"): each cached row is [c (512) | k_rope (64)], scores are
-//    q_lat . c + q_rope . k_rope over the whole 576-wide row, the values are
-//    the row's first 512 elements, every position of the sequence is read;
-//  * top-k sparse decode ("890 bytes a token ...", section 3; the
-//    transcript on DeepSeek Sparse Attention): separate K and V rows of 512,
-//    one kv head, only the positions an index list names are read.
+// Latent (MLA) decode for 64-head query tiles against wide cached rows, on
+// the tensor cores (warp-level m16n8k16 MMA, fp32 accumulators), for the
+// shapes the tcgen05 latent kernel does not take ("KV cache", "Caching a
+// compressed latent instead of the keys"): each cached row is [c (512) |
+// k_rope (64)], scores are q_lat . c + q_rope . k_rope over the whole
+// 576-wide row, the values are the row's first 512 elements, every position
+// of the sequence is read.
 //
 // A unit is (sequence, 64-head tile); its work is cut into 32-position
 // chunks. The stream-K partition of stream_k.cuh spreads the chunks of all
@@ -15,8 +12,8 @@
 // CTAs of a lane take the same chunk range, one head tile each: they stream
 // the same rows at about the same time, so a row read for one tile is
 // still in L2 for the others and HBM delivers it once. A producer warp fetches a chunk with one bulk copy per row
-// and lane (the positions of a chunk need not be contiguous: paged blocks,
-// or index-selected positions) into rows padded by 16 bytes, which keeps
+// and lane (the positions of a chunk need not be contiguous: paged blocks)
+// into rows padded by 16 bytes, which keeps
 // every 8-row ldmatrix read free of bank conflicts. Sixteen consumer warps
 // share the products, with tiles as large as the registers allow (the
 // kernel is bound by its ldmatrix traffic): for S = Q K^T a pair of warps
@@ -51,20 +48,17 @@ constexpr int kThreads = kConsumers + 32 * kPW;
 constexpr int kAllBar = 1;                // all consumer warps
 constexpr int kNB = 256;                  // largest batch of these calls
 
-template <int DK, int DV, bool GATHER>
+// Latent rows: the values are the first DV columns of the K row.
+template <int DK, int DV>
 struct WCfg {
-  static constexpr bool VFROMK = !GATHER;  // latent rows: V = K[:, :DV]
   static constexpr int KROW = DK * 2 + 16;  // padded bytes per K row
-  static constexpr int VROW = DV * 2 + 16;
   static constexpr int KST = kRows * KROW;
-  static constexpr int VST = VFROMK ? 0 : kRows * VROW;
-  static constexpr int NS = VFROMK ? 3 : 2;
+  static constexpr int NS = 3;
   static constexpr int QROW = DK * 2 + 16;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = kHeads * QROW;
-  static constexpr int V_OFF = K_OFF + NS * KST;
   static constexpr int PROW = kRows * 2 + 16;  // padded P row (bf16)
-  static constexpr int P_OFF = V_OFF + NS * VST;   // P, two chunk buffers
+  static constexpr int P_OFF = K_OFF + NS * KST;   // P, two chunk buffers
   static constexpr int PBUF = kHeads * PROW;
   static constexpr int SP_OFF = P_OFF + 2 * PBUF;  // K-split partial S tiles
   static constexpr int RED_OFF = SP_OFF + 8 * 32 * 8 * 4;
@@ -76,14 +70,13 @@ struct WCfg {
   static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8;
 };
 
-template <int DK, int DV, bool GATHER>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_wide_kernel(const DecodeParams p) {
-  using C = WCfg<DK, DV, GATHER>;
+  using C = WCfg<DK, DV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sq = smem + C::Q_OFF;
   uint8_t *sk = smem + C::K_OFF;
-  uint8_t *sv = smem + C::V_OFF;
   uint8_t *spv = smem + C::P_OFF;
   float *spart = reinterpret_cast<float *>(smem + C::SP_OFF);
   float *red = reinterpret_cast<float *>(smem + C::RED_OFF);  // row maxima
@@ -113,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_producer_done = 0;
   }
   __syncthreads();
-  build_partition(wp, p, &s_len_err, kRows, 1, GATHER ? p.n_idx : 0);
+  build_partition(wp, p, &s_len_err, kRows, 1);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
   const int lanes = (int)gridDim.x / tiles;
@@ -160,16 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // position and block of row `row_in_chunk` of the chunk at `cc`
     auto lookup = [&](const ChunkCursor &cc, int &t, int &blk) {
       const int T = wp.len[cc.b];
-      const int e = cc.k * kRows + row_in_chunk;  // entry of the row
-      if constexpr (GATHER) {
-        t = e < p.n_idx ? p.indices[(long)cc.b * p.n_idx + e] : -1;
-        if (t >= T) {
-          if (lane < 8) report(p.err, DEVERR_INDEX);
-          t = -1;
-        }
-      } else {
-        t = e < T ? e : -1;
-      }
+      const int e = cc.k * kRows + row_in_chunk;  // position of the row
+      t = e < T ? e : -1;
       blk = -1;
       if (t >= 0) {
         blk = p.block_table[(long)cc.b * p.max_blocks + t / p.block_size];
@@ -195,17 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < 8 && t < 0) {
         // a row that is not fetched keeps stale data: zero the value part,
         // so that its zero probability cannot meet a NaN in P V
-        uint4 *vz = reinterpret_cast<uint4 *>(
-            C::VFROMK ? sk + s * C::KST + row_in_chunk * C::KROW
-                      : sv + s * C::VST + row_in_chunk * C::VROW);
+        uint4 *vz = reinterpret_cast<uint4 *>(sk + s * C::KST +
+                                              row_in_chunk * C::KROW);
         for (int j = 0; j < DV * 2 / 16; ++j) vz[j] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) {
         s_vpart[s][pw] = (uint8_t)valid;
-        mbar_arrive_expect_tx(&full[s], __popc(valid) *
-                                            (DK * 2 + (C::VFROMK ? 0 : DV * 2)));
+        mbar_arrive_expect_tx(&full[s], __popc(valid) * (DK * 2));
       }
       __syncwarp();
       if (t >= 0) {
@@ -214,17 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 8)
           bulk_g2s(sk + s * C::KST + row_in_chunk * C::KROW,
                    p.k + row * DK * 2, DK * 2, &full[s]);
-      }
-      if constexpr (!C::VFROMK) {
-        // lanes 8..15 copy the values of the rows lanes 0..7 looked up
-        const int tv = __shfl_sync(0xffffffffu, t, r8);
-        const int bv = __shfl_sync(0xffffffffu, blk, r8);
-        if (lane >= 8 && lane < 16 && tv >= 0) {
-          const size_t row =
-              ((size_t)bv * p.n_kv) * p.block_size + tv % p.block_size;
-          bulk_g2s(sv + s * C::VST + row_in_chunk * C::VROW,
-                   p.v + row * DV * 2, DV * 2, &full[s]);
-        }
       }
       if (lane == 0 && pw == 0) s_issued = i + 1;
       // the next chunk's rows are looked up now, while the ring is full
@@ -245,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // m-tiles) x value columns 64 cb .. + 63 (eight n-tiles).
   const int st = warp >> 1, hg = st >> 1, ph = st & 1, kh = warp & 1;
   const int hh = warp >> 3, cb = warp & 7;
-  const uint32_t q0 = smem_u32(sq), k0 = smem_u32(sk), v0 = smem_u32(sv);
+  const uint32_t q0 = smem_u32(sq), k0 = smem_u32(sk);
   float o[2][8][4];            // O: 32 rows x 64 columns
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int cur_b = -1, cur_h = -1, n_units = 0;
@@ -358,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned vmask = *reinterpret_cast<const volatile unsigned *>(
         &s_vpart[s][0]);
     const uint32_t kst = k0 + s * C::KST;
-    const uint32_t vst = (C::VFROMK ? k0 + s * C::KST : v0 + s * C::VST);
+    const uint32_t vst = k0 + s * C::KST;  // values: K's first DV columns
     const int mtx = lane >> 3, ri = lane & 7;
     // ---- S tile: heads 16 hg .., positions 16 ph .., key half kh ----
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -460,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         const uint32_t pbase = smem_u32(spv) + pb * C::PBUF;
-        const int vrs = C::VFROMK ? C::KROW : C::VROW;
+        const int vrs = C::KROW;
 #pragma unroll
         for (int kt = 0; kt < 2; ++kt) {  // 16 positions per k-step
           uint32_t pa[2][4];
@@ -515,7 +487,7 @@ constexpr int kMergeThreads = 256;
 // lanes, all of a lane's loads in flight at once). Part i is the partial of
 // lane c_first + i: side 1 of the first covering lane, side 0 of the
 // others.
-template <int DV, bool GATHER, int ROWS>
+template <int DV, int ROWS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_wide_kernel(const DecodeParams p) {
   __shared__ WorkPartitionT<kNB> wp;
@@ -527,7 +499,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   // (this launch's only possible predecessor still running, since it lets
   // its dependants start only after its own predecessor has completed)
   // does not write them. The partials are read after pdl_wait.
-  build_partition(wp, p, &s_len_err, ROWS, 1, GATHER ? p.n_idx : 0);
+  build_partition(wp, p, &s_len_err, ROWS, 1);
   pdl_wait();
   const int total = wp.total;
   if (total == 0 || wp.nch[b] == 0) return;
@@ -561,39 +533,39 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 // ROWS: positions per chunk of the decode launch whose partials are merged.
-template <int DV, bool GATHER, int ROWS = kRows>
+template <int DV, int ROWS = kRows>
 cudaError_t launch_merge_wide(const DecodeParams &p, cudaStream_t s) {
   const dim3 grid(p.batch * (p.n_h / kHeads), kMergeSlices);
-  return launch_pdl(merge_wide_kernel<DV, GATHER, ROWS>, grid,
+  return launch_pdl(merge_wide_kernel<DV, ROWS>, grid,
                     dim3(kMergeThreads), 0, s, 1, p);
 }
 
-template <int DK, int DV, bool GATHER>
+template <int DK, int DV>
 cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
-  using C = WCfg<DK, DV, GATHER>;
+  using C = WCfg<DK, DV>;
   static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-  auto kern = decode_wide_kernel<DK, DV, GATHER>;
+  auto kern = decode_wide_kernel<DK, DV>;
   static bool done[64] = {};
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s, 1, p);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  return launch_merge_wide<DV, GATHER>(p, s);
+  return launch_merge_wide<DV>(p, s);
 }
 
 }  // namespace
 
 cudaError_t launch_merge_mla(const DecodeParams &p, int rows,
                              cudaStream_t s) {
-  if (rows == 64) return launch_merge_wide<512, false, 64>(p, s);
-  if (rows == kRows) return launch_merge_wide<512, false, kRows>(p, s);
+  if (rows == 64) return launch_merge_wide<512, 64>(p, s);
+  if (rows == kRows) return launch_merge_wide<512, kRows>(p, s);
   return cudaErrorNotSupported;
 }
 
 cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s) {
   if (p.dk != 576 || p.dv != 512 || p.n_h % kHeads != 0 || p.batch > kNB)
     return cudaErrorNotSupported;
-  return launch_t<576, 512, false>(p, s);
+  return launch_t<576, 512>(p, s);
 }
 
 

@@ -54,16 +54,14 @@ __device__ __forceinline__ bool has_window(const DecodeParams &p) {
 // Fill `wp` (shared memory) from the device sequence lengths. Sequence b
 // has `units` units of ceil(rows_b / chunk) chunks, rows_b = its visible
 // length from its first chunk's start (seq_first; 0 when nothing is
-// attended), or `fixed_rows` (a position list's length) when that is > 0
-// and the sequence is not empty. Every thread of the block calls it
-// (blockDim.x a multiple of 32); it ends with a barrier.
+// attended). Every thread of the block calls it (blockDim.x a multiple of
+// 32); it ends with a barrier.
 template <int NB>
 __device__ __forceinline__ void build_partition(WorkPartitionT<NB> &wp,
                                                 const DecodeParams &p,
                                                 int *len_error,
                                                 int chunk = kStageRows,
-                                                int units = -1,
-                                                int fixed_rows = 0) {
+                                                int units = -1) {
   const int nthreads = blockDim.x;
   const int tid = threadIdx.x;
   if (units < 0) units = p.n_kv;
@@ -76,9 +74,7 @@ __device__ __forceinline__ void build_partition(WorkPartitionT<NB> &wp,
     T = max(T, 0);
     wp.len[b] = T;
     const int lo = seq_lo(p, b, T);
-    const int rows = (fixed_rows > 0 && T > 0)
-                         ? fixed_rows
-                         : (lo < T ? T - (lo - lo % chunk) : 0);
+    const int rows = lo < T ? T - (lo - lo % chunk) : 0;
     wp.nch[b] = (rows + chunk - 1) / chunk;
   }
   if (tid == 0) wp.units = units;
