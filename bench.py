@@ -5,14 +5,17 @@
 
 A step is one pass of the hot path over one batch: for every layer of the
 workload, kv_append of the new token and the layer's decode (the sparse
-workload runs its Full / Reuse / Reindex schedule). The default workload is
-the Llama-2-7B-shaped MHA decode (B=1, L=4096, 32 layers of 32x128 heads).
+workload runs its Full / Reuse / Reindex schedule). The headline workload
+is the Llama-3.1-70B-shaped GQA decode (B=32, ragged lengths around 4.5K, 80
+layers of 64 query / 8 kv heads of 128, bf16); every other workload is a
+sub-record of the same line under `configs` (--sub-configs).
 
 Prints ONE JSON line (rank 0). `value` is KV-read GB/s over all ranks:
 algorithmic cache bytes read per step (every visible K and V element once)
 divided by the device time of a step, inputs resident in HBM. Each layer has
-its own cache, so a step's working set (2.1 GB by default) is far larger than
-L2 and no flush is needed between steps. `e2e` is the same metric when every
+its own cache, so a step's working set (45 GB for the headline, 2.1 GB for
+the Llama-2-7B shape) is far larger than L2 and no flush is needed between
+steps. `e2e` is the same metric when every
 step also copies its inputs (q, k_new, v_new of all layers) from pinned host
 memory and reads the outputs back. `roofline` times the dominant kernel
 (the decode kernel) per launch with CUDA events on its stream.

@@ -34,8 +34,8 @@
  * Workspace: the decode calls split each sequence into runs of positions
  * processed by separate CTAs and merge the partial results (log-sum-exp
  * merge). The caller passes the scratch for the partials: at least
- * kvd_workspace_size() bytes, 256-byte aligned, zero-filled once before its
- * first use. Every partial result a call keeps there is written before
+ * kvd_workspace_size() bytes, 256-byte aligned; nothing in it needs to
+ * start at zero. Every partial result a call keeps there is written before
  * the call reads it, so a workspace can be reused by later calls on the
  * same stream without clearing; two calls that may run at the same time
  * need two workspaces.
