@@ -139,9 +139,8 @@ def _workspace(op, cache, block_table, seq_lens, max_seq_len, n_h, k,
         _need(workspace, "workspace", torch.uint8)
         return workspace
     n = workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k)
-    # zero-filled once: every completed call leaves its arrival counters at
-    # zero
-    return torch.zeros(max(n, 256), dtype=torch.uint8,
+    # every partial a call keeps here is written before it is read
+    return torch.empty(max(n, 256), dtype=torch.uint8,
                        device=block_table.device)
 
 
