@@ -196,9 +196,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     const int win = min(32 * kScoreWarps, min(total, nj - k0));
     const int idx = kScoreWarps * lane + warp;  // this lane's slice
-    int j = 0;  // the sequence (relative to cb) of this lane's slice
-#pragma unroll 1
-    for (int l = 0; l < 32; ++l) j += __shfl_sync(0xffffffffu, inc, l) <= idx;
+    // the sequence (relative to cb) of this lane's slice: the first lane l
+    // with inc_l > idx (inc is non-decreasing), by binary search
+    int j = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (__shfl_sync(0xffffffffu, inc, j + step - 1) <= idx) j += step;
+    if (__shfl_sync(0xffffffffu, inc, j) <= idx) ++j;  // idx >= inc_31: 32
     const int jj = min(j, 31);
     const int before = __shfl_sync(0xffffffffu, inc, max(jj - 1, 0));
     const int sl = (jj == 0 ? cs + idx : idx - before);
