@@ -102,7 +102,8 @@ __device__ __forceinline__ int elem_index(int sub, int e) {
 // The lane's D/8 elements of a shared-memory row, as floats. MXFP4 (D =
 // 128): the lane's 16 channels are one scale group (8 code bytes at
 // sub * 8): the code values, without the scale (row_scale gives it; the
-// callers apply it once per row).
+// callers apply it once per row), each byte widened to an exact f16 pair
+// by the hardware conversion.
 template <int D, int DT>
 __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
                                          float (&x)[D / 8]) {
@@ -111,11 +112,10 @@ __device__ __forceinline__ void load_row(const uint8_t *row, int sub,
     const uint2 u = *reinterpret_cast<const uint2 *>(row + sub * 8);
     const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      float v[4];
-      e2m1x4_to_f32(w[t >> 1] >> (16 * (t & 1)), v);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) x[4 * t + k] = v[k];
+    for (int t = 0; t < 8; ++t) {  // byte t: channels 2t (low nibble), 2t+1
+      const uint32_t h = e2m1x2_to_f16x2(w[t >> 2] >> (8 * (t & 3)));
+      x[2 * t] = f16lo(h);
+      x[2 * t + 1] = f16hi(h);
     }
   } else if constexpr (DT == DT_BF16) {
 #pragma unroll

@@ -443,23 +443,16 @@ __device__ __forceinline__ uint32_t e2m1_code(float q) {
   return c | ((__float_as_uint(q) >> 31) << 3);
 }
 
-// Four E2M1 codes (the low 16 bits of `codes`, code i in bits 4i..4i+3) to
-// their exact fp32 values. The fp32 pattern of every E2M1 value has zero
-// low bytes; its two upper bytes come from eight-entry tables indexed by
-// the code's magnitude bits (byte permutes), then the sign bit is set.
-//   magnitude  0    0.5  1    1.5  2    3    4    6
-//   byte 3     00   3F   3F   3F   40   40   40   40
-//   byte 2     00   00   80   C0   00   40   80   C0
-__device__ __forceinline__ void e2m1x4_to_f32(uint32_t codes, float (&v)[4]) {
-  const uint32_t sel = codes & 0x7777u;
-  const uint32_t b2 = prmt(0xC0800000u, 0xC0804000u, sel);
-  const uint32_t b3 = prmt(0x3F3F3F00u, 0x40404040u, sel);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    // bytes 0, 1: the sign-replicated top bit of a byte-3 value (always 0)
-    const uint32_t f = prmt(b2, b3, 0xCCu | (k << 8) | ((4 + k) << 12));
-    v[k] = __uint_as_float(f | ((codes << (28 - 4 * k)) & 0x80000000u));
-  }
+// Two E2M1 codes (the low byte of `b`: the first code in its low nibble) to
+// their f16 values, first in the low half (exact: every E2M1 value is an
+// f16).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t b) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(b & 0xffu));
+  return r;
 }
 
 // One 16-channel group of a new bf16 row into an MXFP4 row: 8 bytes of
