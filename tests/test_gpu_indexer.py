@@ -75,11 +75,17 @@ CASES = [
     ([1000, 4000], 256, 16, 4),
     ([3000], 2048, 64, 8),
     ([700, 1500], 100, 32, 1),
+    # block sizes below 8 (a 64-entry slice spans more block pieces than a
+    # lane resolves ahead) and not powers of two
+    ([2000, 130], 100, 1, 4),
+    ([500, 1900], 64, 3, 2),
+    ([3000, 77], 256, 48, 3),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=["small", "bs16", "k2048",
-                                             "one_head"])
+                                             "one_head", "bs1", "bs3",
+                                             "bs48"])
 def test_scores_and_selection(case):
     lengths, k, bs, heads = case
     s = _shape(lengths, k, bs, heads)
