@@ -168,9 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *done = ofull + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();
-  pdl_trigger();  // after the wait: dependants never overlap this grid's
-                  // predecessor
 
   const int S = p.n_splits;  // CTAs per unit
   const int tiles = p.n_h / kH;
@@ -180,12 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int e0 = (int)((long)k * part / S);
   const int e1 = (int)((long)k * (part + 1) / S);
   const int nch = (e1 - e0 + kRows - 1) / kRows;
-  int T = p.seq_lens[b];
-  if (T > p.max_seq_len) {
-    if (tid == 0 && part == 0 && ht == 0) report(p.err, DEVERR_LEN);
-    T = p.max_seq_len;
-  }
-  T = max(T, 0);
 
   if (tid == 0) {
     for (int s = 0; s < kNSlot; ++s) {
@@ -214,6 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
+  // The setup above (barriers, tensor memory) touches nothing the kernel
+  // before may write, so it overlaps that kernel's end; everything below
+  // reads after its completion.
+  pdl_wait();
+  pdl_trigger();  // after the wait: dependants never overlap this grid's
+                  // predecessor
+  int T = p.seq_lens[b];
+  if (T > p.max_seq_len) {
+    if (tid == 0 && part == 0 && ht == 0) report(p.err, DEVERR_LEN);
+    T = p.max_seq_len;
+  }
+  T = max(T, 0);
   // the swizzled operand tiles assume 1 KB atoms (every CTA sees the same
   // layout)
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
