@@ -277,15 +277,73 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
     const int bn = win > warp ? (win - warp + kScoreWarps - 1) / kScoreWarps : 0;
 
-    // ---- this warp's slices of the window: copies two ahead ----
+    // ---- this warp's slices of the window: three slots, the copies of
+    // slice m + 3 go out into slice m's slot as soon as its MMAs have
+    // read it (three slices in flight during the epilogue) ----
     const int col = lane & 7;
-    for (int m = -2; m < bn; ++m) {
-      const int mi = m + 2;  // the slice whose copies go out now
+    for (int m = -3; m < bn; ++m) {
+      float c[4][4];
+      int rows = 0, T = 0;
+      float *out = nullptr;
+      const SliceJob *Jp = nullptr;
+      if (m >= 0) {
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+        }
+        cp_async_wait<2>();  // slice m has landed (this lane's copies)
+        __syncwarp();        // ... and every lane's
+        Jp = &s_job[warp][m];
+        const int b = Jp->b, tw = Jp->tw;
+        rows = Jp->rows;
+        T = Jp->T;
+        if (b != qb) {
+          if (b == qbn) {
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+              qf[kt][0] = qn[kt][0];
+              qf[kt][1] = qn[kt][1];
+            }
+            w0 = wn0;
+            w1 = wn1;
+          } else {  // a sequence of fewer than three slices came between
+            load_query(b, qf, w0, w1);
+          }
+          qb = b;
+        }
+        const uint32_t sbase = smem_u32(wring + (m % kDepth) * kSliceBytes);
+        out = p.scores + (long)b * p.score_stride + tw;
+        // the matrix loads of k-step kt + 1 go out before the MMAs of step
+        // kt, which are independent across the four row tiles
+        uint32_t a[2][4][4];
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt) {
+          c[rt][0] = c[rt][1] = c[rt][2] = c[rt][3] = 0.f;
+        }
+        auto load_a = [&](int kt, uint32_t (&dst)[4][4]) {
+#pragma unroll
+          for (int rt = 0; rt < 4; ++rt) {
+            const int lr = 16 * rt + (lane & 15);  // this lane's ldmatrix row
+            const int chunk = 2 * kt + (lane >> 4);
+            ldsm_x4(dst[rt], sbase + lr * 128 + ((chunk ^ (lr & 7)) << 4));
+          }
+        };
+        load_a(0, a[0]);
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          if (kt < 3) load_a(kt + 1, a[(kt + 1) & 1]);
+#pragma unroll
+          for (int rt = 0; rt < 4; ++rt)
+            mma_bf16(c[rt], a[kt & 1][rt], qf[kt][0], qf[kt][1]);
+        }
+        __syncwarp();  // every lane has read the slot before it is refilled
+      }
+      const int mi = m + 3;  // the slice whose copies go out now
       if (mi < bn) {
         const SliceJob &J = s_job[warp][mi];
-        const int rows = J.rows, np = J.np;
+        const int irows = J.rows, np = J.np;
         uint8_t *dst = wring + (mi % kDepth) * kSliceBytes;
-        if (!waited && !(prefix && J.tw + rows < J.T)) {
+        if (!waited && !(prefix && J.tw + irows < J.T)) {
           pdl_wait();
           waited = true;
         }
@@ -299,7 +357,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
           for (int jc = 0; jc < kSlice / 4; ++jc) {
             const int r = (lane >> 3) + 4 * jc;
-            if (r < rows)
+            if (r < irows)
               cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
                          p.cache + ((size_t)J.row[jc >> 1] + (r & 7)) * 128 +
                              col * 16, 16);
@@ -309,7 +367,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
           for (int jc = 0; jc < kSlice / 4; ++jc) {
             const int r = (lane >> 3) + 4 * jc;
-            if (r < rows)
+            if (r < irows)
               cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
                          p.cache + (r0 + r) * 128 + col * 16, 16);
           }
@@ -323,7 +381,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const int q = div_bs(t) - lb0;
             const int first = max(tw, (lb0 + q) * bs);
             uint32_t pr = 0;
-            if (r < rows) {
+            if (r < irows) {
               if (q < kPieceRegs) {
                 pr = J.row[q];
               } else {  // pieces past the resolved ones
@@ -342,7 +400,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll 4
           for (int jc = 0; jc < kSlice / 4; ++jc) {
             const int r = (lane >> 3) + 4 * jc;
-            if (r < rows)
+            if (r < irows)
               cp_async16(dst + r * 128 + ((col ^ (r & 7)) << 4),
                          p.cache + (size_t)s_row[warp][r] * 128 + col * 16,
                          16);
@@ -352,55 +410,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       cp_async_commit();  // one group a step (empty past the last slice)
       if (m < 0) continue;
-      if (!waited) {
-        pdl_wait();
-        waited = true;
-      }
-      cp_async_wait<2>();  // slice m has landed (this lane's copies)
-      __syncwarp();        // ... and every lane's
-      const SliceJob &J = s_job[warp][m];
-      const int b = J.b, tw = J.tw, rows = J.rows, T = J.T;
-      if (b != qb) {
-        if (b == qbn) {
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt) {
-            qf[kt][0] = qn[kt][0];
-            qf[kt][1] = qn[kt][1];
-          }
-          w0 = wn0;
-          w1 = wn1;
-        } else {  // a sequence of fewer than three slices came between
-          load_query(b, qf, w0, w1);
-        }
-        qb = b;
-      }
-      const uint32_t sbase = smem_u32(wring + (m % kDepth) * kSliceBytes);
-      float *out = p.scores + (long)b * p.score_stride + tw;
-      // the matrix loads of k-step kt + 1 go out before the MMAs of step
-      // kt, which are independent across the four row tiles
-      float c[4][4];
-      uint32_t a[2][4][4];
-#pragma unroll
-      for (int rt = 0; rt < 4; ++rt) {
-        c[rt][0] = c[rt][1] = c[rt][2] = c[rt][3] = 0.f;
-      }
-      auto load_a = [&](int kt, uint32_t (&dst)[4][4]) {
-#pragma unroll
-        for (int rt = 0; rt < 4; ++rt) {
-          const int lr = 16 * rt + (lane & 15);  // this lane's ldmatrix row
-          const int chunk = 2 * kt + (lane >> 4);
-          ldsm_x4(dst[rt], sbase + lr * 128 + ((chunk ^ (lr & 7)) << 4));
-        }
-      };
-      load_a(0, a[0]);
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        if (kt < 3) load_a(kt + 1, a[(kt + 1) & 1]);
-#pragma unroll
-        for (int rt = 0; rt < 4; ++rt)
-          mma_bf16(c[rt], a[kt & 1][rt], qf[kt][0], qf[kt][1]);
-      }
-      __syncwarp();  // every lane has read the slot before it is refilled
       // rows 16 rt + g (s[rt][0]) and 16 rt + g + 8 (s[rt][1]): heads 2 t4
       // and 2 t4 + 1 here, summed over the lanes t4
       float sv[4][2];
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             float sc = sv[rt][hh];
             if (r < rows) {
               if (p.pool) {  // a position past the visible length: -inf
-                const int pos0 = J.pos0[r / kPoolBlock];
+                const int pos0 = Jp->pos0[r / kPoolBlock];
                 if (pos0 < 0 || pos0 + r % kPoolBlock >= T) sc = -INFINITY;
               }
               out[r] = sc;
