@@ -700,17 +700,19 @@ __global__ void __launch_bounds__(kTopkThreads)
   // Warp w owns the runs of kRun positions [base + w kRun, + kRun); lane l
   // takes positions run + 32 j + l, so position order within a run is
   // (j, l) and one ballot per j ranks the lanes; a scan over the 32 warp
-  // totals places the warps after each other.
-  constexpr int kRun = 512;  // positions per warp and round
+  // totals places the warps after each other. The list's runs are long
+  // enough that a cached range takes one round.
+  constexpr int kRun = 512;  // positions per warp and round (final sweep)
+  constexpr int kHiRun = kCacheKeys / kTopkThreads * 32;  // list: 640
   {
     int nhi = 0;  // high keys of the earlier rounds
-    for (int base = 0; base < n; base += kRun * 32) {
-      const int run = base + wid * kRun;
-      uint32_t key[kRun / 32];
-      unsigned hib[kRun / 32];
+    for (int base = 0; base < n; base += kHiRun * 32) {
+      const int run = base + wid * kHiRun;
+      uint32_t key[kHiRun / 32];
+      unsigned hib[kHiRun / 32];
       int whi = 0;
 #pragma unroll
-      for (int j = 0; j < kRun / 32; ++j) {
+      for (int j = 0; j < kHiRun / 32; ++j) {
         const int i = run + 32 * j + lane;
         key[j] = i < n ? key_at(i) : 0u;
         hib[j] = __ballot_sync(0xffffffffu, i < n && (key[j] >> 20) >= d1);
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       int tot_hi;
       int at = nhi + warp_excl_scan(whi, s_wsum, &tot_hi);
 #pragma unroll
-      for (int j = 0; j < kRun / 32; ++j) {
+      for (int j = 0; j < kHiRun / 32; ++j) {
         const int idx = at + __popc(hib[j] & lt);
         if (((hib[j] >> lane) & 1) && idx < kHiCap) {
           s_hik[idx] = key[j];
