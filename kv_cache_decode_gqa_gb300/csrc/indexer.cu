@@ -583,6 +583,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   __shared__ __align__(16) int tot[kBins];  // cluster totals, own eighth
   __shared__ int tmp[32];
   __shared__ int s_digit, s_above;
+  __shared__ uint32_t s_kstar;         // K* when its last bin holds one key
   __shared__ int s_nhi;                // this CTA's high keys
   __shared__ int s_off[kCluster + 1];  // high keys of the lower ranks
   __shared__ int s_src[2][kCluster];   // high keys above / equal to K*
@@ -781,21 +782,47 @@ __global__ void __launch_bounds__(kTopkThreads)
                tmp, &s_digit, &s_above);
     const uint32_t p2 = (d1 << 12) | (uint32_t)s_digit;  // bits 31..8
     remaining -= s_above;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[0][i] = 0;
-    __syncthreads();
-    for (int i = tid; i < C; i += kTopkThreads) {
-      const uint32_t key = s_gath[i];
-      if ((key >> 8) == p2) atomicAdd(&hist[0][key & 0xff], 1);
+    if (hist[1][s_digit] == 1) {
+      // the usual case for spread scores: the bin holds one key, K*
+      for (int i = tid; i < C; i += kTopkThreads) {
+        const uint32_t key = s_gath[i];
+        if ((key >> 8) == p2) s_kstar = key;
+      }
+      __syncthreads();
+      kstar = s_kstar;
+      need_eq = 1;
+    } else {
+      for (int i = tid; i < 256; i += kTopkThreads) hist[0][i] = 0;
+      __syncthreads();
+      for (int i = tid; i < C; i += kTopkThreads) {
+        const uint32_t key = s_gath[i];
+        if ((key >> 8) == p2) atomicAdd(&hist[0][key & 0xff], 1);
+      }
+      __syncthreads();
+      find_digit(256, remaining,
+                 [&](int d0, int, int (&cnt)[4]) { cnt[0] = hist[0][d0]; },
+                 tmp, &s_digit, &s_above);
+      kstar = (p2 << 8) | (uint32_t)s_digit;
+      need_eq = remaining - s_above;
     }
-    __syncthreads();
-    find_digit(256, remaining,
-               [&](int d0, int, int (&cnt)[4]) { cnt[0] = hist[0][d0]; },
-               tmp, &s_digit, &s_above);
-    kstar = (p2 << 8) | (uint32_t)s_digit;
-    need_eq = remaining - s_above;
-    for (int i = tid; i < C; i += kTopkThreads) {
-      const uint32_t key = s_gath[i];
-      if (key >= kstar) atomicAdd(&s_src[key == kstar][source(i)], 1);
+    // keys above / equal to K* of each source CTA: warp q counts the
+    // gathered list of CTA q (a contiguous segment)
+    if (wid < kCluster) {
+      int gt = 0, eq = 0;
+      for (int i = s_off[wid] + lane; i < s_off[wid + 1]; i += 32) {
+        const uint32_t key = s_gath[i];
+        gt += key > kstar;
+        eq += key == kstar;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        gt += __shfl_xor_sync(0xffffffffu, gt, o);
+        eq += __shfl_xor_sync(0xffffffffu, eq, o);
+      }
+      if (lane == 0) {
+        s_src[0][wid] = gt;
+        s_src[1][wid] = eq;
+      }
     }
     __syncthreads();
     if (tid == 0) {
