@@ -128,15 +128,20 @@ def measured_peaks(key="hbm_gbs"):
                 "fallback")
 
 
+# CTAs of a lane per 128-head tile in the tensor-core latent kernel (each
+# holds 512 / LATENT_TC_PARTS of the output columns)
+LATENT_TC_PARTS = 2
+
+
 def latent_flops(shape):
     """Multiply-add work of one latent decode call, in FLOPs: useful (each
     head scores every cached row over 576 dims and sums 512 latent dims) and
-    issued by the tensor-core kernel (each of a lane's four value-quarter
-    CTAs computes the full scores of its 128 heads)."""
+    issued by the tensor-core kernel (each of a lane's LATENT_TC_PARTS
+    value-part CTAs computes the full scores of its 128 heads)."""
     s = shape
     rows = sum(s.seq_lens)
     useful = 2 * rows * s.n_h * (s.head_dim + s.dv)
-    issued = 2 * rows * s.n_h * (4 * s.head_dim + s.dv)
+    issued = 2 * rows * s.n_h * (LATENT_TC_PARTS * s.head_dim + s.dv)
     return useful, issued
 
 

@@ -234,7 +234,7 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
 // 64-position) chunks of `rows` positions per sequence and head tile;
 // partials of 64 heads x dv per CTA side, merged by a second launch.
 // `per_lane` CTAs of the launch share a lane's chunk range (one per head
-// tile, or per head tile and value quarter for the tensor-core latent
+// tile, or per head tile and value part for the tensor-core latent
 // kernel); n_splits counts 64-head tiles per lane whatever the kernel.
 Plan plan_wide(int sms, int batch, int n_h, int rows, int dv,
                int per_lane = 0, int chunk_rows = 32) {
@@ -264,7 +264,8 @@ bool mla_on_tensor_memory(const kvd_cache *c, int n_h) {
 }
 
 Plan mla_plan(const kvd_seqs *s, int n_h, int dv, int sms, bool tc) {
-  return tc ? plan_wide(sms, s->batch, n_h, s->max_seq_len, dv, n_h / 32,
+  return tc ? plan_wide(sms, s->batch, n_h, s->max_seq_len, dv,
+                       n_h / 128 * kvd::kLatentTcParts,
                        kvd::kLatentTcRows)
             : plan_wide(sms, s->batch, n_h, s->max_seq_len, dv);
 }

@@ -9,39 +9,47 @@
 // bytes. This kernel runs it on tcgen05 MMAs with TMEM accumulators.
 //
 // Work: a persistent stream-K partition like the 64-head-tile latent
-// kernel's, over 64-position chunks, with n_h / 32 CTAs per lane: head tile
-// ht (128 heads = the MMA's M) x value quarter vq (128 of the 512 output
-// columns). Each CTA of a lane computes the full scores S = Q K^T of its
-// head tile (the softmax needs them) and O += P V for its value quarter. The
-// four quarters read the same cache rows at about the same time, so three
-// of the four reads hit L2.
+// kernel's, over 64-position chunks, with n_h / 128 x NP CTAs per lane:
+// head tile ht (128 heads = the MMA's M) x value part vp (512 / NP of the
+// output columns; NP = kLatentTcParts = 2). Each CTA of a lane computes the
+// full scores S = Q K^T of its head tile (the softmax needs them) and
+// O += P V for its value part. The parts read the same cache rows at about
+// the same time, so all but one of the reads of a row hit L2.
 //
-// Tensor memory (512 columns x 128 lanes, lane = query head):
-//   [0, 288)    Q: the tile's 128 x 576 bf16 query (A operand of S)
-//   [288, 352)  S: 128 x 64 fp32 scores of one chunk
-//   [352, 384)  P: 128 x 64 bf16 probabilities (A operand of O)
-//   [384, 512)  O: 128 x 128 fp32 output accumulator
-// Shared memory holds only rings of cache chunks (64 rows x 1152 B, copied
-// by TMA as nine 64-column boxes with 128-byte swizzle), so the tensor core
-// reads just the B operand from shared memory. An MMA of N = 64
-// positions streams its 128 x 16 A operand once per 64 positions; at N = 32
-// that stream, not the multiply-adds, set the MMA's duration.
+// Tensor memory (512 columns x 128 lanes, lane = query head), NP = 2:
+//   [0, 160)    Q: the first 320 of the tile's 576 query columns, bf16
+//               (A operand of S)
+//   [160, 224)  S: 128 x 64 fp32 scores of one chunk
+//   [224, 256)  P: 128 x 64 bf16 probabilities (A operand of O)
+//   [256, 512)  O: 128 x 256 fp32 output accumulator
+// The query's other 256 columns are an A operand in shared memory (four
+// 128-byte-swizzled boxes, 64 KB). With NP = 4 the whole query fits in
+// tensor memory beside a 128-column O, but each tile's scores are then
+// computed four times instead of twice: 1.15 against 0.90 ms for the
+// 128-head, 64 x 32K-position call, whose tensor work the repeated scores
+// dominate. The rest of shared memory holds two slots of each ring of cache
+// chunks (64 rows x 1152 B, copied by TMA as nine 64-column boxes with
+// 128-byte swizzle). An MMA of N = 64 positions streams its 128 x 16 A
+// operand once per 64 positions; at N = 32 that stream, not the
+// multiply-adds, set the MMA's duration.
 //
 // Warp roles (192 threads):
-//   warp 0, one lane: TMA producer (per chunk: the block table lookup,
-//     seven score-only boxes into the score ring, this quarter's two value
-//     boxes into the value ring);
+//   warp 0, one lane: TMA producer (per chunk: the block table lookup, the
+//     score-only boxes into the score ring, this part's value boxes into
+//     the value ring);
 //   warp 1: TMEM allocation; the MMA loop (one elected lane issues each
 //     MMA, the warp keeps the operands uniform): S(j) = 36 k-steps of
-//     M=128 N=64 K=16 (A = Q in TMEM, B = K rows, K-major), and
-//     O += P(j) V(j) as 4 k-steps of M=128 N=128 K=16 (A = P in TMEM,
-//     B = the chunk's latent columns of this value quarter, MN-major);
+//     M=128 N=64 K=16 (A = Q, from TMEM for its first 320 columns and from
+//     shared memory for the rest; B = K rows, K-major), and O += P(j) V(j)
+//     as 4 k-steps of M=128 N=256 K=16 (A = P in TMEM, B = the chunk's
+//     latent columns of this value part, MN-major);
 //   warps 2..5 (one thread per head): online softmax. Thread r reads row r
 //     of S(j) from TMEM, masks positions past the sequence end, and writes
 //     P(j) = exp2(s * scale * log2 e - m) in bf16 back to TMEM, m the
 //     running maximum of the head's scaled scores. When a chunk raises m the
 //     thread rescales its row of O in TMEM and its running sum l. They also
-//     store each unit's query tile into TMEM and write the results.
+//     store each unit's query tile into TMEM and shared memory and write the
+//     results.
 // Order of the MMA warp: S(j+1) as soon as the softmax has read S(j) (so it
 // runs while the softmax of chunk j does), then O(j) once P(j) is written
 // (the tensor core runs them in issue order); a chunk that starts a unit
@@ -61,54 +69,79 @@ namespace {
 constexpr int kM = 128;             // query heads per CTA (MMA M)
 constexpr int kDK = 576;            // row width (latent + rope)
 constexpr int kDV = 512;            // latent width = output width
-constexpr int kVQ = 128;            // output columns per CTA
 constexpr int kRows = kLatentTcRows;  // positions per chunk (MMA N of S)
 constexpr int kBoxes = kDK / 64;    // 128-byte column boxes of a row
 constexpr int kBoxBytes = kRows * 128;
-// A chunk's nine boxes go to two rings: the seven that only the scores read
-// (freed as soon as S has run) and the two of this CTA's value quarter
-// (read by S and by P V, freed after P V). So a chunk's copy starts about
-// two periods before its S needs it, not one.
-constexpr int kKBoxes = kBoxes - 2;
-constexpr int kKSlot = kKBoxes * kBoxBytes;  // 57,344
-constexpr int kVSlot = 2 * kBoxBytes;        // 16,384
-constexpr int kNS = 3;              // slots of each ring
+constexpr int kQBox = kM * 128;     // one 64-column box of the query tile
 constexpr int kNB = 256;            // largest batch of these calls
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0, kColS = 288, kColP = 352, kColO = 384;
 // The softmax offset m moves when a chunk's maximum exceeds it by more than
 // this (log2 units). Any offset gives the same softmax, but the largest P is
 // then up to 2^slack and its bf16 rounding is no longer exact: 0 keeps the
 // running maximum exact, as the CUDA-core kernels do.
 constexpr float kOffsetSlack = 0.f;
 
-constexpr int K_OFF = 0;
-constexpr int V_OFF = K_OFF + kNS * kKSlot;
-constexpr int WP_OFF = V_OFF + kNS * kVSlot;
-constexpr int BAR_OFF =
-    (WP_OFF + (int)sizeof(WorkPartitionT<kNB>) + 15) / 16 * 16;
-// kfull[3] kempty[3] vfull[3] vempty[3] sfull sfree pfull ofull qready done
-constexpr int kBars = 4 * kNS + 6;
-constexpr int FLAG_OFF = BAR_OFF + kBars * 8;
-constexpr int SMEM = FLAG_OFF + 16;
-static_assert(SMEM <= 227 * 1024, "shared memory budget");
-static_assert(kColO + kVQ == kTmemCols, "tensor memory budget");
+// The layout for NP value parts (CTAs of a lane per head tile).
+template <int NP>
+struct LCfg {
+  static_assert(NP == 2 || NP == 4, "two or four value parts");
+  static constexpr int VW = kDV / NP;     // output columns per CTA
+  static constexpr int VB = VW / 64;      // value boxes of a chunk per CTA
+  static constexpr int KB = kBoxes - VB;  // score-only boxes
+  // tensor memory: the query's first QT boxes, S, P, O
+  static constexpr uint32_t ColO = kTmemCols - VW;
+  static constexpr uint32_t ColP = ColO - kRows / 2;
+  static constexpr uint32_t ColS = ColP - kRows;
+  static constexpr uint32_t ColQ = 0;
+  static constexpr int QT = (int)ColS / 32;  // query boxes in tensor memory
+  static constexpr int QS = kBoxes - QT;     // query boxes in shared memory
+  // A chunk's boxes go to two rings: the score-only ones (freed as soon as
+  // S has run) and this CTA's value boxes (read by S and by P V, freed
+  // after P V), so a chunk's copy starts before the chunk ahead is done.
+  static constexpr int KSlot = KB * kBoxBytes;
+  static constexpr int VSlot = VB * kBoxBytes;
+  static constexpr int QBYTES = QS * kQBox;
+  static constexpr int FIXED =
+      QBYTES + (int)sizeof(WorkPartitionT<kNB>) + 16 + (4 * 3 + 6) * 8 + 16;
+  static constexpr int NS_FIT = (227 * 1024 - FIXED) / (KSlot + VSlot);
+  static constexpr int NS = NS_FIT > 3 ? 3 : NS_FIT;  // slots of each ring
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + NS * KSlot;
+  static constexpr int Q_OFF = V_OFF + NS * VSlot;  // 1 KB aligned
+  static constexpr int WP_OFF = Q_OFF + QBYTES;
+  static constexpr int BAR_OFF =
+      (WP_OFF + (int)sizeof(WorkPartitionT<kNB>) + 15) / 16 * 16;
+  // kfull[NS] kempty[NS] vfull[NS] vempty[NS] sfull sfree pfull ofull
+  // qready done
+  static constexpr int kBars = 4 * NS + 6;
+  static constexpr int FLAG_OFF = BAR_OFF + kBars * 8;
+  static constexpr int SMEM = FLAG_OFF + 16;
+  static_assert(NS >= 2, "ring depth");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(ColO + VW == kTmemCols && ColS % 32 == 0,
+                "tensor memory budget");
+  static_assert(Q_OFF % 1024 == 0, "swizzle atoms");
+};
 
 struct LatentTcParams {
   DecodeParams p;
   CUtensorMap tmk;  // cache rows [rows][576], 64-column boxes
 };
 
+template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_latent_tc_kernel(const __grid_constant__ LatentTcParams lp) {
+  using C = LCfg<NP>;
+  constexpr int kNS = C::NS;
   const DecodeParams &p = lp.p;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *sk = smem + K_OFF;
-  uint8_t *sv = smem + V_OFF;
+  uint8_t *sk = smem + C::K_OFF;
+  uint8_t *sv = smem + C::V_OFF;
+  uint8_t *sq = smem + C::Q_OFF;
   WorkPartitionT<kNB> &wp =
-      *reinterpret_cast<WorkPartitionT<kNB> *>(smem + WP_OFF);
-  uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+      *reinterpret_cast<WorkPartitionT<kNB> *>(smem + C::WP_OFF);
+  uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
   uint64_t *kempty = kfull + kNS;
   uint64_t *vfull = kempty + kNS;
   uint64_t *vempty = vfull + kNS;
@@ -118,13 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *ofull = pfull + 1;
   uint64_t *qready = ofull + 1;
   uint64_t *done = qready + 1;
-  int *flags = reinterpret_cast<int *>(smem + FLAG_OFF);
+  int *flags = reinterpret_cast<int *>(smem + C::FLAG_OFF);
   int *s_len_err = flags;
   volatile int *s_abort = flags + 1;
   volatile int *s_issued = flags + 2;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(flags + 3);
 
-  const int per_lane = p.n_h / 32;  // CTAs sharing a chunk range
+  const int per_lane = p.n_h / kM * NP;  // CTAs sharing a chunk range
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
   pdl_trigger();  // after the wait: see the merge launch
@@ -141,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lanes = (int)gridDim.x / per_lane;
   const int P = min(lanes, max(total, 1));
   const int c = (int)blockIdx.x / per_lane;  // lane: a range of chunks
-  const int ht = ((int)blockIdx.x % per_lane) >> 2;  // head tile
-  const int vq = (int)blockIdx.x & 3;                // value quarter
+  const int ht = ((int)blockIdx.x % per_lane) / NP;  // head tile
+  const int vp = (int)blockIdx.x % NP;                // value part
 
   if (blockIdx.x == 0) {  // sequences with nothing visible: out = 0, lse = -inf
     for (int b = 0; b < p.batch; ++b) {
@@ -201,30 +234,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           blk = 0;  // read a valid block; the result is flagged as wrong
         }
         const int row0 = blk * p.block_size + t0 % p.block_size;
-        // the seven score-only boxes, once S(i - 3) has run
+        // the score-only boxes, once S(i - kNS) has run
         if (i >= kNS && !mbar_wait(&kempty[s], (i / kNS - 1) & 1)) {
           report(p.err, DEVERR_TIMEOUT);
           *s_abort = 1;
         }
         if (*s_abort) break;
-        mbar_arrive_expect_tx(&kfull[s], kKSlot);
+        mbar_arrive_expect_tx(&kfull[s], C::KSlot);
         for (int z = 0, j = 0; z < kBoxes; ++z) {
-          if (z == 2 * vq || z == 2 * vq + 1) continue;
-          tma_load_2d_plain(sk + s * kKSlot + j * kBoxBytes, &lp.tmk, 64 * z,
-                            row0, &kfull[s]);
+          if (z >= C::VB * vp && z < C::VB * (vp + 1)) continue;
+          tma_load_2d_plain(sk + s * C::KSlot + j * kBoxBytes, &lp.tmk,
+                            64 * z, row0, &kfull[s]);
           ++j;
         }
         *s_issued = 2 * i + 1;
-        // the value quarter's two boxes, once P V of chunk i - 3 has run
+        // the value part's boxes, once P V of chunk i - kNS has run
         if (i >= kNS && !mbar_wait(&vempty[s], (i / kNS - 1) & 1)) {
           report(p.err, DEVERR_TIMEOUT);
           *s_abort = 1;
         }
         if (*s_abort) break;
-        mbar_arrive_expect_tx(&vfull[s], kVSlot);
-        for (int z = 0; z < 2; ++z)
-          tma_load_2d_plain(sv + s * kVSlot + z * kBoxBytes, &lp.tmk,
-                            64 * (2 * vq + z), row0, &vfull[s]);
+        mbar_arrive_expect_tx(&vfull[s], C::VSlot);
+        for (int z = 0; z < C::VB; ++z)
+          tma_load_2d_plain(sv + s * C::VSlot + z * kBoxBytes, &lp.tmk,
+                            64 * (C::VB * vp + z), row0, &vfull[s]);
         *s_issued = 2 * i + 2;
         cursor_next(wp, p.batch, 1, pc);
       }
@@ -235,8 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs this loop (warp-uniform values); one elected lane
     // issues each MMA and commit.
     constexpr uint32_t idS = umma_idesc_bf16(kM, kRows, false);
-    constexpr uint32_t idO = umma_idesc_bf16(kM, kVQ, true);
+    constexpr uint32_t idO = umma_idesc_bf16(kM, C::VW, true);
     const uint32_t k_addr = smem_u32(sk), v_addr = smem_u32(sv);
+    // the query's boxes held in shared memory (K-major A operand)
+    const uint64_t aq = umma_desc_sw128(smem_u32(sq), 16, 1024);
     ChunkCursor sc = cursor_at(wp, p.batch, lo);  // next S to issue
     ChunkCursor oc = sc;                          // next O to issue
     int s_prev_b = -1, o_prev_b = -1, units = 0;
@@ -257,20 +292,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= 1 && !wait_all(sfree, (j - 1) & 1)) return false;
       tc_fence_after();
       // K-major B: box z = ks / 4 (in the value ring if it is one of this
-      // quarter's two, else in the score ring), 32-byte step ks % 4 inside
-      // the 128-byte swizzled row (descriptor address in 16-byte units)
-      const uint64_t bk = umma_desc_sw128(k_addr + s * kKSlot, 16, 1024);
-      const uint64_t bv = umma_desc_sw128(v_addr + s * kVSlot, 16, 1024);
+      // part's, else in the score ring), 32-byte step ks % 4 inside the
+      // 128-byte swizzled row (descriptor address in 16-byte units). A: the
+      // query's box z, in tensor memory (z < QT) or in shared memory.
+      const uint64_t bk = umma_desc_sw128(k_addr + s * C::KSlot, 16, 1024);
+      const uint64_t bv = umma_desc_sw128(v_addr + s * C::VSlot, 16, 1024);
+      const int v0 = C::VB * vp;
 #pragma unroll
       for (int ks = 0; ks < kDK / 16; ++ks) {
         const int z = ks >> 2;
         const uint64_t b =
-            z == 2 * vq || z == 2 * vq + 1
-                ? bv + (uint64_t)(((z - 2 * vq) * kBoxBytes) >> 4)
-                : bk + (uint64_t)(((z < 2 * vq ? z : z - 2) * kBoxBytes) >> 4);
-        umma_ts_elect(tbase + kColS, tbase + kColQ + ks * 8,
-                      b + (uint64_t)(((ks & 3) * 32) >> 4), idS,
-                      ks > 0 ? 1u : 0u);
+            (z >= v0 && z < v0 + C::VB)
+                ? bv + (uint64_t)(((z - v0) * kBoxBytes) >> 4)
+                : bk + (uint64_t)(((z < v0 ? z : z - C::VB) * kBoxBytes) >> 4);
+        const uint64_t bs = b + (uint64_t)(((ks & 3) * 32) >> 4);
+        if (z < C::QT)
+          umma_ts_elect(tbase + C::ColS, tbase + C::ColQ + ks * 8, bs, idS,
+                        ks > 0 ? 1u : 0u);
+        else
+          umma_ss_elect(tbase + C::ColS,
+                        aq + (uint64_t)(((z - C::QT) * kQBox + (ks & 3) * 32) >>
+                                        4),
+                        bs, idS, ks > 0 ? 1u : 0u);
       }
       umma_commit_elect(sfull);
       umma_commit_elect(&kempty[s]);
@@ -283,12 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool first = oc.b != o_prev_b;
       o_prev_b = oc.b;
-      // MN-major B: the quarter's two 64-column boxes (LBO apart), 16
-      // positions (2 groups of 8 rows, SBO apart) per k-step
-      const uint64_t b0 = umma_desc_sw128(v_addr + s * kVSlot, kBoxBytes, 1024);
+      // MN-major B: the part's 64-column boxes (LBO apart), 16 positions
+      // (2 groups of 8 rows, SBO apart) per k-step
+      const uint64_t b0 =
+          umma_desc_sw128(v_addr + s * C::VSlot, kBoxBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kRows / 16; ++kk)
-        umma_ts_elect(tbase + kColO, tbase + kColP + kk * 8,
+        umma_ts_elect(tbase + C::ColO, tbase + C::ColP + kk * 8,
                       b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
                       (!first || kk > 0) ? 1u : 0u);
       umma_commit_elect(&vempty[s]);
@@ -336,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long head = (long)ht * kM + r;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int pc = 0; pc < kVQ / 32; ++pc) {
+      for (int pc = 0; pc < C::VW / 32; ++pc) {
         uint32_t o[32];
-        tmem_ld32(tl + kColO + pc * 32, o);
+        tmem_ld32(tl + C::ColO + pc * 32, o);
         tmem_wait_ld(o);
-        const int col = vq * kVQ + pc * 32;
+        const int col = vp * C::VW + pc * 32;
         if (whole) {
           uint4 *dst = reinterpret_cast<uint4 *>(
               p.out + ((long)b * p.n_h + head) * kDV + col);
@@ -368,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   __uint_as_float(o[4 * q4 + 3]) * inv);
         }
       }
-      if (vq == 0) {
+      if (vp == 0) {
         const float lse =
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (whole) {
@@ -394,11 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_b = cc.b;
         m_ref = -INFINITY;
         l = 0.f;
-        // the unit's query row of this head into TMEM columns [0, 288)
+        // the unit's query row of this head: its first QT boxes into TMEM
+        // columns [0, 32 QT), the rest into shared memory (row r of each
+        // box, 128-byte swizzled)
         const uint4 *qrow = reinterpret_cast<const uint4 *>(
             p.q + ((long)cc.b * p.n_h + (long)ht * kM + r) * kDK);
 #pragma unroll 1
-        for (int pc = 0; pc < kBoxes; ++pc) {
+        for (int pc = 0; pc < C::QT; ++pc) {
           uint32_t v[32];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -408,7 +454,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * j + 2] = u.z;
             v[4 * j + 3] = u.w;
           }
-          tmem_st32(tl + kColQ + pc * 32, v);
+          tmem_st32(tl + C::ColQ + pc * 32, v);
+        }
+        if constexpr (C::QS > 0) {
+#pragma unroll 1
+          for (int pc = 0; pc < C::QS; ++pc) {
+            uint8_t *row = sq + pc * kQBox + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) =
+                  __ldg(qrow + (C::QT + pc) * 8 + j);
+          }
+          fence_proxy_async_smem();  // read by the tensor core
         }
         tmem_wait_st();
         tc_fence_before();
@@ -425,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
 #pragma unroll
         for (int h2 = 0; h2 < kRows / 32; ++h2) {
-          tmem_ld32(tl + kColS + h2 * 32, v);
+          tmem_ld32(tl + C::ColS + h2 * 32, v);
           tmem_wait_ld(v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[h2 * 32 + j] = __uint_as_float(v[j]);
@@ -458,14 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, need)) {  // rescale this row of O
         const float cr = need ? ex2(m_ref - mx) : 1.f;
 #pragma unroll 1
-        for (int pc = 0; pc < kVQ / 32; ++pc) {
+        for (int pc = 0; pc < C::VW / 32; ++pc) {
           uint32_t o[32];
-          tmem_ld32(tl + kColO + pc * 32, o);
+          tmem_ld32(tl + C::ColO + pc * 32, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             o[j] = __float_as_uint(__uint_as_float(o[j]) * cr);
-          tmem_st32(tl + kColO + pc * 32, o);
+          tmem_st32(tl + C::ColO + pc * 32, o);
         }
         if (need) {
           l *= cr;
@@ -484,17 +541,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum += p0 + p1;
           pk[j] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tl + kColP + h2 * 16, pk);
+        tmem_st16(tl + C::ColP + h2 * 16, pk);
       }
       l += sum;
       tmem_wait_st();
       if (nvalid < kRows) {
         // rows past the sequence end hold whatever the block held: zero this
-        // quarter's value columns of them, so that P = 0 meets no NaN
-        uint8_t *vb = sv + (i % kNS) * kVSlot;
-        const int cnt = (kRows - nvalid) * 2 * 8;  // 16-byte pieces
+        // part's value columns of them, so that P = 0 meets no NaN
+        uint8_t *vb = sv + (i % kNS) * C::VSlot;
+        const int cnt = (kRows - nvalid) * C::VB * 8;  // 16-byte pieces
         for (int e = r; e < cnt; e += kM) {
-          const int row = nvalid + e / 16, box = (e / 8) & 1, piece = e & 7;
+          const int row = nvalid + e / (C::VB * 8), box = (e / 8) % C::VB,
+                    piece = e & 7;
           *reinterpret_cast<uint4 *>(vb + box * kBoxBytes + row * 128 +
                                      piece * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -565,15 +623,16 @@ cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s) {
   cudaError_t e =
       make_latent_map(&lp.tmk, p.k, (long)p.num_blocks * p.block_size);
   if (e != cudaSuccess) return e;
-  auto kern = decode_latent_tc_kernel;
+  constexpr int NP = kLatentTcParts;
+  auto kern = decode_latent_tc_kernel<NP>;
   static bool done[64] = {};
-  e = set_smem_once(kern, SMEM, done);
+  e = set_smem_once(kern, LCfg<NP>::SMEM, done);
   if (e != cudaSuccess) return e;
   // n_splits counts 64-head tiles per lane (the partial layout and the
-  // merge use it); this launch has n_h / 32 CTAs per lane.
+  // merge use it); this launch has n_h / 128 x NP CTAs per lane.
   const int lanes = p.n_splits / (p.n_h / 64);
-  e = launch_pdl(kern, dim3(lanes * (p.n_h / 32)), dim3(kThreads), SMEM, s, 1,
-                 lp);
+  e = launch_pdl(kern, dim3(lanes * (p.n_h / kM) * NP), dim3(kThreads),
+                 LCfg<NP>::SMEM, s, 1, lp);
   if (e != cudaSuccess || lanes <= 1) return e;
   return launch_merge_mla(p, kRows, s);
 }

@@ -139,6 +139,8 @@ cudaError_t launch_decode_mla(const DecodeParams &p, cudaStream_t s);
 // multiple of 64): 64-position chunks, n_h / 32 CTAs per lane of
 // n_splits / (n_h / 64).
 constexpr int kLatentTcRows = 64;
+// value parts of the tcgen05 latent decode: CTAs of a lane per 128-head tile
+constexpr int kLatentTcParts = 2;
 bool latent_tc_supported(int n_h, int block_size, long num_blocks);
 cudaError_t launch_decode_mla_tc(const DecodeParams &p, cudaStream_t s);
 // Log-sum-exp merge of the latent decode's split units (chunks of `rows`

@@ -44,8 +44,9 @@ def test_mla_bytes_and_flops():
     useful, issued = bench.latent_flops(s)
     # per head and cached row: 576 score and 512 value multiply-adds
     assert useful == 2 * rows * 128 * (576 + 512) == 584_133_378_048
-    # the tensor-core kernel's four value quarters each recompute the scores
-    assert issued == 2 * rows * 128 * (4 * 576 + 512)
+    # the tensor-core kernel's two value halves each recompute the scores
+    assert bench.LATENT_TC_PARTS == 2
+    assert issued == 2 * rows * 128 * (2 * 576 + 512)
 
 
 def test_sparse_schedule_bytes():
@@ -63,3 +64,13 @@ def test_data_description_names_the_cache_format():
     assert "E4M3" in bench.data_description(W.config("llama31_70b_gqa_fp8"))
     assert "E2M1" in bench.data_description(W.config("llama2_7b_mha_mxfp4"))
     assert "bf16 cache" in bench.data_description(W.config("sparse"))
+
+
+def test_latent_parts_match_the_library():
+    # the issued-work accounting follows the kernel's value split
+    import os
+    import re
+    h = os.path.join(os.path.dirname(__file__), "..", "kv_cache_decode_gqa_gb300",
+                     "csrc", "kvd_internal.h")
+    m = re.search(r"constexpr int kLatentTcParts = (\d+);", open(h).read())
+    assert m and int(m.group(1)) == bench.LATENT_TC_PARTS
