@@ -129,6 +129,16 @@ struct LatentTcParams {
   CUtensorMap tmk;  // cache rows [rows][576], 64-column boxes
 };
 
+// Bounded wait for the producer: non-blocking tests only. A try_wait may
+// suspend the thread, and the producer's wake-up after a slot is freed
+// delays the copy that the tensor core waits for next (the producer warp
+// has one active lane; the softmax warp on its scheduler has slack).
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 26); ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return false;
+}
+
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_latent_tc_kernel(const __grid_constant__ LatentTcParams lp) {
@@ -235,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int row0 = blk * p.block_size + t0 % p.block_size;
         // the score-only boxes, once S(i - kNS) has run
-        if (i >= kNS && !mbar_wait(&kempty[s], (i / kNS - 1) & 1)) {
+        if (i >= kNS && !spin_wait(&kempty[s], (i / kNS - 1) & 1)) {
           report(p.err, DEVERR_TIMEOUT);
           *s_abort = 1;
         }
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *s_issued = 2 * i + 1;
         // the value part's boxes, once P V of chunk i - kNS has run
-        if (i >= kNS && !mbar_wait(&vempty[s], (i / kNS - 1) & 1)) {
+        if (i >= kNS && !spin_wait(&vempty[s], (i / kNS - 1) & 1)) {
           report(p.err, DEVERR_TIMEOUT);
           *s_abort = 1;
         }
@@ -279,7 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t *bar, int parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
-    auto issue_s = [&](int j) -> bool {
+    // S(j+1)'s commits (sfull, kempty) are issued after O(j)'s MMAs, not
+    // between them: a commit in between delayed O(j) by a few hundred
+    // cycles, and the tensor core idled after S(j+1) until it came; the
+    // softmax and the score ring have that much slack.
+    int pend_k = -1;  // score slot of an S whose commits are deferred
+    auto issue_s = [&](int j, bool defer) -> bool {
       const int s = j % kNS;
       if (sc.b != s_prev_b) {  // the unit's query tile is in TMEM
         if (!wait_all(qready, units & 1)) return false;
@@ -315,8 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         4),
                         bs, idS, ks > 0 ? 1u : 0u);
       }
-      umma_commit_elect(sfull);
-      umma_commit_elect(&kempty[s]);
+      if (defer) {
+        pend_k = s;
+      } else {
+        umma_commit_elect(sfull);
+        umma_commit_elect(&kempty[s]);
+      }
       cursor_next(wp, p.batch, 1, sc);
       return true;
     };
@@ -340,14 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       cursor_next(wp, p.batch, 1, oc);
       return true;
     };
-    ok = n > 0 && issue_s(0);
+    ok = n > 0 && issue_s(0, false);
     for (int i = 0; ok && i < n; ++i) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
       // sc is chunk i+1's cursor here
       const bool next_starts = i + 1 < n && sc.b != s_prev_b;
-      if (i + 1 < n && !next_starts) ok = issue_s(i + 1);
+      if (i + 1 < n && !next_starts) ok = issue_s(i + 1, true);
       ok = ok && issue_o(i);
-      if (ok && next_starts) ok = issue_s(i + 1);
+      if (pend_k >= 0) {
+        umma_commit_elect(sfull);
+        umma_commit_elect(&kempty[pend_k]);
+        pend_k = -1;
+      }
+      if (ok && next_starts) ok = issue_s(i + 1, false);
     }
     if (!ok && lane == 0) {
       report(p.err, DEVERR_TIMEOUT);
