@@ -476,17 +476,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kMergeSlices = 128;   // CTAs per split unit
+constexpr int kMergeSlices = 8;     // CTAs per split unit
 constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 2;      // parts whose loads a thread issues together
 
 // Log-sum-exp merge of the partials of every unit the decode launch cut
 // between CTAs. Grid (units, kMergeSlices): CTA (u, j) rebuilds the launch's
 // partition, returns if unit u lies inside one CTA's range, and otherwise
-// merges the j-th 1/128 of the unit's outputs: 64 float4s (4 values of one
-// head), each by a quad of lanes (quad_merge: the parts split over the 4
-// lanes, all of a lane's loads in flight at once). Part i is the partial of
-// lane c_first + i: side 1 of the first covering lane, side 0 of the
-// others.
+// merges the j-th 1/8 of the unit's outputs, four float4s (4 values of one
+// head) a thread, the loads of all four for kMergeBatch parts in flight
+// together (a unit has 2-3 parts at the usual shapes). The grid stays small
+// enough to be resident beside the decode launch and pass its grid wait at
+// once: one CTA per 1/128 of a unit (16,384 for 64 sequences x 2 tiles), each
+// rebuilding the partition, took 108 us for the 64-sequence latent call.
+// Part i is the partial of lane c_first + i: side 1 of the first covering
+// lane, side 0 of the others.
 template <int DV, int ROWS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_wide_kernel(const DecodeParams p) {
@@ -511,25 +515,67 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (parts == 1) return;  // written whole by the decode launch
   constexpr int N4 = kHeads * DV / 4;
   constexpr int PER = N4 / kMergeSlices;
-  static_assert(4 * PER == kMergeThreads, "one quad of lanes per float4");
+  constexpr int IT = PER / kMergeThreads;  // float4s a thread
+  static_assert(IT * kMergeThreads * kMergeSlices == N4, "merge tiling");
   const long bh0 = (long)b * p.n_h + (long)h * kHeads;
-  const int e = blockIdx.y * PER + (threadIdx.x >> 2);
-  const int g = (4 * e) / DV;  // head within the tile
-  float M, W;
-  float4 acc;
-  quad_merge<4>(p.ws_lse, p.ws_o, kHeads, DV, g, e, parts,
-             [&](int i) {
-               return ((long)(c_first + i) * 2 + (i == 0 ? 1 : 0)) * tiles + h;
-             },
-             M, W, acc);
-  if ((threadIdx.x & 3) != 0) return;
-  const float iw = W > 0.f ? 1.f / W : 0.f;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
-  packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
-  *reinterpret_cast<uint2 *>(p.out + bh0 * DV + 4 * e) = packed;
-  if ((4 * e) % DV == 0 && p.lse)
-    p.lse[bh0 + g] = W > 0.f ? M + logf(W) : -INFINITY;
+  auto slot = [&](int i) {  // partial of part i, in 64-head tiles
+    return ((long)(c_first + i) * 2 + (i == 0 ? 1 : 0)) * tiles + h;
+  };
+  const float4 *o4 = reinterpret_cast<const float4 *>(p.ws_o);
+  float M[IT], W[IT];
+  float4 acc[IT];
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    M[it] = -INFINITY;
+    W[it] = 0.f;
+    acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int e0 = blockIdx.y * PER + threadIdx.x;
+  for (int i0 = 0; i0 < parts; i0 += kMergeBatch) {
+    float l[IT][kMergeBatch];
+    float4 v[IT][kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const bool in = i0 + j < parts;
+      const long sl = in ? slot(i0 + j) : 0;
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int e = e0 + it * kMergeThreads;
+        const int g = (4 * e) / DV;  // head within the tile
+        l[it][j] = in ? __ldcg(p.ws_lse + sl * kHeads + g) : -INFINITY;
+        v[it][j] = in ? __ldcg(o4 + sl * (kHeads * DV / 4) + e)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        if (l[it][j] == -INFINITY) continue;  // an empty part adds nothing
+        const float Mn = fmaxf(M[it], l[it][j]);
+        const float a = M[it] == -INFINITY ? 0.f : expf(M[it] - Mn);
+        const float w = expf(l[it][j] - Mn);
+        W[it] = W[it] * a + w;
+        acc[it].x = acc[it].x * a + w * v[it][j].x;
+        acc[it].y = acc[it].y * a + w * v[it][j].y;
+        acc[it].z = acc[it].z * a + w * v[it][j].z;
+        acc[it].w = acc[it].w * a + w * v[it][j].w;
+        M[it] = Mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int e = e0 + it * kMergeThreads;
+    const int g = (4 * e) / DV;
+    const float iw = W[it] > 0.f ? 1.f / W[it] : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc[it].x * iw, acc[it].y * iw);
+    packed.y = pack_bf16x2(acc[it].z * iw, acc[it].w * iw);
+    *reinterpret_cast<uint2 *>(p.out + bh0 * DV + 4 * e) = packed;
+    if ((4 * e) % DV == 0 && p.lse)
+      p.lse[bh0 + g] = W[it] > 0.f ? M[it] + logf(W[it]) : -INFINITY;
+  }
 }
 
 // ROWS: positions per chunk of the decode launch whose partials are merged.
