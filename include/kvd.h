@@ -38,7 +38,11 @@
  * start at zero. Every partial result a call keeps there is written before
  * the call reads it, so a workspace can be reused by later calls on the
  * same stream without clearing; two calls that may run at the same time
- * need two workspaces.
+ * need two workspaces. A GQA decode whose (sequence, head group) units are
+ * all short -- a window (kvd_seqs.window) of at most 192 positions, or a
+ * longest visible length of at most 256 -- and no more numerous than the
+ * device's SMs runs each unit whole on one CTA and needs no workspace
+ * (kvd_workspace_size returns 0; NULL is then accepted).
  *
  * Paged layout ("KV cache", "The allocator, not the algorithm"; the paging
  * of the My Weird Prompts 640482 transcript): a cache is a pool of fixed-size
@@ -488,7 +492,9 @@ kvd_status kvd_copy_blocks(const kvd_cache *cache, const int32_t *src,
 
 /*
  * kvd_workspace_size -- bytes of workspace the call `op` needs for these
- * shapes on the current device (the split plan depends on its SM count).
+ * shapes on the current device (the split plan depends on its SM count,
+ * and for a GQA decode on `seqs`->window as well, so pass the window the
+ * call will use).
  * `n_h` is the query head count (indexer heads for KVD_OP_INDEXER_TOPK) and
  * `k` the top-k size (0 where unused). Queries the device; KVD_ERR_CUDA if
  * there is none.

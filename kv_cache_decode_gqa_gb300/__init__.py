@@ -123,9 +123,12 @@ def _seqs(block_table, seq_lens, max_seq_len, flags=0, window=0,
                            _ptr(window_start))
 
 
-def workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k=0):
+def workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k=0,
+                   window=0):
+    """Workspace bytes of a call (kvd_workspace_size); a GQA decode's window
+    is part of its plan (short windows need none)."""
     c = cache.struct()
-    s = _seqs(block_table, seq_lens, max_seq_len)
+    s = _seqs(block_table, seq_lens, max_seq_len, window=window)
     out = ctypes.c_size_t(0)
     check(lib().kvd_workspace_size(op, ctypes.byref(c), ctypes.byref(s), n_h,
                                    k, ctypes.byref(out)))
@@ -133,12 +136,13 @@ def workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k=0):
 
 
 def _workspace(op, cache, block_table, seq_lens, max_seq_len, n_h, k,
-               workspace):
+               workspace, window=0):
     import torch
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8)
         return workspace
-    n = workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k)
+    n = workspace_size(op, cache, block_table, seq_lens, max_seq_len, n_h, k,
+                       window)
     # every partial a call keeps here is written before it is read
     return torch.empty(max(n, 256), dtype=torch.uint8,
                        device=block_table.device)
@@ -186,7 +190,7 @@ def gqa_decode(cache, block_table, seq_lens, max_seq_len, q, scale=None,
               window_start)
     out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
     ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
-                    n_h, 0, workspace)
+                    n_h, 0, workspace, window)
     check(lib().kvd_gqa_decode(ctypes.byref(c), ctypes.byref(s), _ptr(q), n_h,
                                float(scale or 0.0), _ptr(out), _ptr(lse),
                                _ptr(ws), ws.numel(), _stream(stream)))
@@ -210,7 +214,7 @@ def gqa_append_decode(cache, block_table, seq_lens, max_seq_len, pos, k_new,
               window_start)
     out, lse = _outputs(q, n_h, cache.head_dim, out, lse, want_lse)
     ws = _workspace(OP_GQA_DECODE, cache, block_table, seq_lens, max_seq_len,
-                    n_h, 0, workspace)
+                    n_h, 0, workspace, window)
     check(lib().kvd_gqa_append_decode(
         ctypes.byref(c), ctypes.byref(s), _ptr(pos), _ptr(k_new), _ptr(v_new),
         _ptr(q), n_h, float(scale or 0.0), _ptr(out), _ptr(lse), _ptr(ws),

@@ -168,6 +168,7 @@ struct Plan {
   size_t ws_lse_bytes = 0; // partial log-sum-exps
   size_t ws_bytes = 0;     // total
   int hp = 1;              // kv heads per work unit (CUDA-core GQA kernel)
+  int whole_units = 0;     // dense GQA: one CTA per unit, no merge
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -196,16 +197,37 @@ kvd_status gqa_shape(const kvd_cache *c, int n_h, DenseKernel *kind) {
   return KVD_OK;
 }
 
+// Units (sequence, head group) of at most this many 64-token chunks run one
+// per CTA when they fit in one wave: the merge launch and its two grid
+// dependencies (about 3 us) then cost more than the imbalance of whole
+// units (at most this many chunks against the average share).
+constexpr int kWholeUnitChunks = 4;
+
 // Persistent stream-K plan of the dense GQA kernels: `ctas_per_sm` CTAs per
 // SM (never more CTAs than 64-token chunks), each leaving at most two
-// partials of G heads x head_dim, which the merge launch combines.
+// partials of G heads x head_dim, which the merge launch combines. Short
+// units instead run whole, one CTA each (no partials, no merge): every unit
+// holds at most kWholeUnitChunks chunks (the window bounds it, or the
+// longest visible length does) and there are no more units than CTAs.
 Plan plan_stream_k(int sms, int ctas_per_sm, int batch, int n_kv, int g,
-                   int d, int max_seq_len) {
+                   int d, int max_seq_len, int window = 0) {
   Plan pl;
-  const long chunks = (long)batch * n_kv *
-                      ((max_seq_len + kvd::kStageRows - 1) / kvd::kStageRows);
+  const int R = kvd::kStageRows;
+  const long unit_chunks =
+      window > 0 ? std::min<long>((window + R - 1) / R + 1,
+                                  (max_seq_len + R - 1) / R)
+                 : (max_seq_len + R - 1) / R;
+  const long chunks = (long)batch * n_kv * ((max_seq_len + R - 1) / R);
   long ctas = (long)sms * ctas_per_sm;
   const int forced = g_decode_ctas.load(std::memory_order_relaxed);
+  const long units = (long)batch * n_kv;
+  if (forced <= 0 && units >= 1 && units <= ctas &&
+      unit_chunks <= kWholeUnitChunks) {
+    pl.whole_units = 1;
+    pl.n_splits = (int)units;
+    pl.n_groups = n_kv;
+    return pl;  // no workspace
+  }
   if (forced > 0) ctas = forced;
   ctas = std::max(1L, std::min(ctas, std::max(chunks, 1L)));
   pl.n_splits = (int)ctas;
@@ -225,7 +247,7 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
                      : kvd::mma_heads_per_unit(c->n_kv, c->block_size,
                                                c->dtype);
   Plan pl = plan_stream_k(sms, 1, s->batch, c->n_kv / hp, g * hp,
-                          c->head_dim, s->max_seq_len);
+                          c->head_dim, s->max_seq_len, s->window);
   pl.hp = hp;
   return pl;
 }
@@ -573,6 +595,7 @@ kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
   p.max_seq_len = seqs->max_seq_len;
   p.split_len = pl.split_len;
   p.n_splits = pl.n_splits;
+  p.whole_units = pl.whole_units;
   p.hp = pl.hp;
   p.flags = seqs->flags;
   p.window = seqs->window;

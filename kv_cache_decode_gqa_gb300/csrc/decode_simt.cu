@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   build_partition(wp, p, &s_len_err, kStageRows, n_units);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
-  const int P = min((int)gridDim.x, max(total, 1));
+  const int P = p.whole_units ? (int)gridDim.x
+                              : min((int)gridDim.x, max(total, 1));
   const int c = blockIdx.x;
 
   // sequences with nothing visible: out = 0, lse = -inf; fused-append rows
@@ -229,9 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (c >= P || total == 0) return;
-  const int lo = range_lo(c, total, P);
-  const int hi = range_lo(c + 1, total, P);
+  const int lo = p.whole_units ? unit_lo(wp, p.batch, n_units, c)
+                               : range_lo(c, total, P);
+  const int hi = p.whole_units ? unit_lo(wp, p.batch, n_units, c + 1)
+                               : range_lo(c + 1, total, P);
   const int n = hi - lo;
+  if (n == 0) return;  // an empty unit of a whole-unit launch
 
   if (tid == 0) {
 #pragma unroll

@@ -62,6 +62,10 @@ struct DecodeParams {
   int32_t n_idx;        // entries per row of `indices`
   int32_t split_len;    // tokens (or index entries) per split
   int32_t n_splits;
+  // dense GQA only: 1 when CTA c takes unit c (sequence c / units per
+  // sequence, head group c % units) whole instead of an equal share of all
+  // chunks: no partials and no merge launch (units all short, see the plan)
+  int32_t whole_units;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
   int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE, FLAG_PREFIX_READY)
   // sliding window (dense GQA only): sequence b attends to positions

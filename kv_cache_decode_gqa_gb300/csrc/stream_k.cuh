@@ -140,6 +140,17 @@ __device__ __forceinline__ int range_lo(int c, int total, int P) {
   return (int)(((long long)c * total) / P);
 }
 
+// First chunk of unit u, units in (sequence, head group) order; u = batch x
+// n_units gives the end of the last (the range of CTA c of a whole-unit
+// launch is [unit_lo(c), unit_lo(c + 1))).
+template <int NB>
+__device__ __forceinline__ int unit_lo(const WorkPartitionT<NB> &wp,
+                                      int batch, int n_units, int u) {
+  const int b = u / n_units;
+  if (b >= batch) return wp.total;
+  return wp.pre[b] + (u % n_units) * wp.nch[b];
+}
+
 // The CTA whose range holds chunk x (P <= total, so no range is empty).
 __device__ __forceinline__ int cta_of(int x, int total, int P) {
   return (int)((((long long)x + 1) * P - 1) / total);
@@ -465,7 +476,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 template <int D, int GU>
 inline cudaError_t launch_merge_dense(const DecodeParams &p, int n_units,
                                       cudaStream_t s) {
-  if (p.n_splits <= 1 || p.batch == 0) return cudaSuccess;
+  if (p.n_splits <= 1 || p.whole_units || p.batch == 0) return cudaSuccess;
   const long nu = (long)p.batch * n_units;
   const int grid = (int)(nu < 1024 ? nu : 1024);
   if (p.batch <= kMergeSmallBatch)

@@ -589,3 +589,51 @@ def test_window_full_size_fp8(fused):
                                           window=128)
     H.assert_close(H.to_np_bf16(out)[seqs], ref, "window full size")
     H.assert_lse_close(lse.cpu().numpy()[seqs], ref_lse, "window full size")
+
+
+# ---------------------------------------------------------------------------
+# whole-unit launches: when every (sequence, head group) unit is short (a
+# window of <= 192 positions, or contexts of <= 256) and they fit in one
+# wave, each runs whole on one CTA -- no partials, so no workspace and no
+# merge launch; otherwise the stream-K split and its merge
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("n_h,n_kv,batch,longest,window,whole", [
+    (8, 2, 6, 1000, 128, True),    # the window bounds every unit
+    (8, 2, 6, 250, 0, True),       # short contexts (and empty sequences)
+    (16, 2, 5, 250, 0, True),      # tensor-core kernel (group 8)
+    (8, 2, 6, 1000, 0, False),     # long units: split and merged
+    (16, 2, 5, 1000, 192, True),   # the longest window it takes
+    (16, 2, 5, 1000, 193, False),
+], ids=["window128", "short", "short_g8", "long", "window192", "window193"])
+def test_whole_unit_plan(dtype, n_h, n_kv, batch, longest, window, whole):
+    lengths = [max(0, longest - 97 * i) for i in range(batch)]
+    s = W.config("llama31_70b_gqa", batch=batch, lengths=lengths, n_layers=1,
+                 block_size=64, dtype=dtype, n_h=n_h, n_kv=n_kv, head_dim=128)
+    wl = W.DeviceWorkload(s, layers=[0])
+    ws = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                          wl.seq_lens, wl.max_seq_len, n_h, window=window)
+    assert (ws == 0) == whole, ws
+    out, lse = H.device_step(wl, 0, window=window)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0, window=window)
+    H.assert_close(H.to_np_bf16(out), ref, f"whole={whole}/{dtype}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"whole={whole}/{dtype}")
+
+
+def test_whole_unit_plan_needs_one_wave():
+    """More units than SMs (bf16 MHA, two kv heads a unit): the split plan,
+    although every unit is short."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    batch = sms // 16 + 2       # 16 units a sequence: more than one wave
+    s = W.config("llama2_7b_mha", batch=batch, lengths=[100] * batch,
+                 n_layers=1)
+    wl = W.DeviceWorkload(s, layers=[0])
+    ws = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                          wl.seq_lens, wl.max_seq_len, s.n_h)
+    assert ws > 0
+    out, lse = H.device_step(wl, 0)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
+    H.assert_close(H.to_np_bf16(out), ref, "one wave")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, "one wave")
