@@ -42,7 +42,10 @@
  * all short -- a window (kvd_seqs.window) of at most 192 positions, or a
  * longest visible length of at most 256 -- and no more numerous than the
  * device's SMs runs each unit whole on one CTA and needs no workspace
- * (kvd_workspace_size returns 0; NULL is then accepted).
+ * (kvd_workspace_size returns 0; NULL is then accepted). Neither does a
+ * single sequence with one query head per kv head (MHA) whose units run as
+ * thread-block clusters merging their parts in distributed shared memory
+ * (units of at most two heads, when the clusters fill most of the SMs).
  *
  * Paged layout ("KV cache", "The allocator, not the algorithm"; the paging
  * of the My Weird Prompts 640482 transcript): a cache is a pool of fixed-size

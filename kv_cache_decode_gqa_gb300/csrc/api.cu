@@ -169,6 +169,7 @@ struct Plan {
   size_t ws_bytes = 0;     // total
   int hp = 1;              // kv heads per work unit (CUDA-core GQA kernel)
   int whole_units = 0;     // dense GQA: one CTA per unit, no merge
+  int cluster = 0;         // dense GQA: CTAs per unit of a cluster merge
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -249,6 +250,24 @@ Plan gqa_plan(const kvd_cache *c, const kvd_seqs *s, int n_h, int sms,
   Plan pl = plan_stream_k(sms, 1, s->batch, c->n_kv / hp, g * hp,
                           c->head_dim, s->max_seq_len, s->window);
   pl.hp = hp;
+  // One sequence (every unit as long as the others) on the CUDA-core
+  // kernel with query groups of 1: its units run as clusters of CTAs that
+  // merge their parts in distributed shared memory, when all the clusters
+  // fit at once -- no workspace and no merge launch.
+  if (kind == DenseKernel::Simt && !pl.whole_units && s->batch == 1 &&
+      g == 1 && g_decode_ctas.load(std::memory_order_relaxed) <= 0) {
+    const int units = c->n_kv / hp;
+    const int cs =
+        kvd::simt_cluster_size(c->head_dim, c->dtype, hp, units, sms);
+    if (cs >= 2) {
+      Plan cl;
+      cl.cluster = cs;
+      cl.n_splits = units * cs;
+      cl.n_groups = units;
+      cl.hp = hp;
+      return cl;
+    }
+  }
   return pl;
 }
 
@@ -596,6 +615,7 @@ kvd_status gqa_decode_impl(const kvd_cache *cache, const kvd_seqs *seqs,
   p.split_len = pl.split_len;
   p.n_splits = pl.n_splits;
   p.whole_units = pl.whole_units;
+  p.cluster = pl.cluster;
   p.hp = pl.hp;
   p.flags = seqs->flags;
   p.window = seqs->window;

@@ -72,21 +72,31 @@ struct Cfg {
   static constexpr int QB = HP * G * D * 2;          // query rows / stage
   static constexpr int SLOT = kWarps * G * (D + 2);   // floats per slot
   static constexpr int MERGE = 2 * SLOT * 4;
+  // cluster merge (query groups of 1, units of at most 2 heads, whose
+  // rings keep their depth with it): the partials of up to 8 CTAs of a unit
+  // (GU heads x D outputs, then GU log-sum-exps, padded to 16 floats) in
+  // the shared memory of the cluster's rank 0
+  static constexpr int GU = HP * G;
+  static constexpr int CL_RANKS = G == 1 && GU <= 2 ? 8 : 0;
+  static constexpr int CPART = GU * D + 16;
+  static constexpr int CBUF = CL_RANKS * CPART * 4;
   // ring depth: up to 160 KB (one head) or 192 KB (head groups) of K and V,
   // within what the flush slots, the partition and the barriers leave of
   // 227 KB (1 KB kept for the kernel's static shared variables)
   static constexpr int RING_BUDGET = HP == 1 ? 160 * 1024 : 192 * 1024;
   static constexpr int FIXED =
-      MERGE + (int)sizeof(WorkPartition) + 16 + 20 * 8 + 1024;
+      MERGE + CBUF + (int)sizeof(WorkPartition) + 16 + 21 * 8 + 1024;
   static constexpr int NS_FIT = (227 * 1024 - FIXED) / (2 * STAGE + QB);
   static constexpr int NS_WANT = RING_BUDGET / (2 * STAGE);
   static constexpr int NS_MIN = NS_FIT < NS_WANT ? NS_FIT : NS_WANT;
   static constexpr int NS = NS_MIN > 8 ? 8 : NS_MIN;  // ring depth
   static constexpr int RING = 2 * NS * STAGE + NS * QB;
-  static constexpr int WP_OFF = RING + MERGE;
+  static constexpr int CB_OFF = RING + MERGE;  // 16-byte aligned
+  static constexpr int WP_OFF = CB_OFF + CBUF;
   static constexpr int BAR_OFF =
       (WP_OFF + (int)sizeof(WorkPartition) + 15) / 16 * 16;
-  static constexpr int SMEM = BAR_OFF + (2 * NS + 4) * 8;
+  static constexpr int SMEM = BAR_OFF + (2 * NS + 5) * 8;
+  static_assert(CB_OFF % 16 == 0 && GU <= 16, "cluster buffer layout");
 };
 
 // Element index (within a row of D) of the e-th value a lane holds.
@@ -183,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *empty = full + C::NS;
   uint64_t *sfull = empty + C::NS;  // flush slot written (8 warp arrivals)
   uint64_t *sempty = sfull + 2;     // flush slot consumed (finisher)
+  uint64_t *cbar = sempty + 2;      // cluster merge: the other ranks' parts
+  float *cbuf = reinterpret_cast<float *>(smem + C::CB_OFF);
   __shared__ int s_len_err;
   __shared__ volatile int s_abort, s_issued, s_producer_done;
 
@@ -211,8 +223,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   build_partition(wp, p, &s_len_err, kStageRows, n_units);
   if (tid == 0 && blockIdx.x == 0 && s_len_err) report(p.err, DEVERR_LEN);
   const int total = wp.total;
-  const int P = p.whole_units ? (int)gridDim.x
-                              : min((int)gridDim.x, max(total, 1));
+  // Cluster merge: the cs CTAs of a cluster share one unit. Rank 0's
+  // barrier counts the other ranks' consumer threads, each arriving after
+  // its stores of the rank's partial into rank 0's buffer; the cluster
+  // barrier here (every thread still present) makes the barrier's
+  // initialisation visible before any arrival.
+  const int cs = C::CL_RANKS >= 2 && p.cluster > 1 ? p.cluster : 1;
+  const int crank = cs > 1 ? (int)cluster_rank() : 0;
+  if (cs > 1) {
+    if (crank == 0 && tid == 0) {
+      mbar_init(cbar, (cs - 1) * kConsumers);
+      fence_mbar_init();
+    }
+    cluster_sync();
+  }
+  const int P = p.whole_units || cs > 1 ? (int)gridDim.x
+                                        : min((int)gridDim.x, max(total, 1));
   const int c = blockIdx.x;
 
   // sequences with nothing visible: out = 0, lse = -inf; fused-append rows
@@ -230,12 +256,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (c >= P || total == 0) return;
-  const int lo = p.whole_units ? unit_lo(wp, p.batch, n_units, c)
-                               : range_lo(c, total, P);
-  const int hi = p.whole_units ? unit_lo(wp, p.batch, n_units, c + 1)
-                               : range_lo(c + 1, total, P);
+  int lo, hi;
+  if (cs > 1) {  // an equal part of unit c / cs
+    const int u = c / cs, ub = u / n_units, uh = u % n_units;
+    const int us = wp.pre[ub] + uh * wp.nch[ub], nc = wp.nch[ub];
+    lo = us + (int)((long)nc * crank / cs);
+    hi = us + (int)((long)nc * (crank + 1) / cs);
+  } else {
+    lo = p.whole_units ? unit_lo(wp, p.batch, n_units, c)
+                       : range_lo(c, total, P);
+    hi = p.whole_units ? unit_lo(wp, p.batch, n_units, c + 1)
+                       : range_lo(c + 1, total, P);
+  }
   const int n = hi - lo;
-  if (n == 0) return;  // an empty unit of a whole-unit launch
+  // an empty unit of a whole-unit launch (a cluster's empty part still
+  // hands rank 0 an empty partial)
+  if (n == 0 && cs == 1) return;
+  // this CTA's partial in rank 0's cluster buffer
+  const uint32_t cpart =
+      cs > 1 ? cluster_saddr(cbuf + crank * C::CPART, 0) : 0u;
 
   if (tid == 0) {
 #pragma unroll
@@ -260,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *wm = slots + sl * C::SLOT;
     const float *wl = wm + kWarps * G;
     const float *wo = wl + kWarps * G;  // [warp][G][D]
-    const bool whole = ustart >= lo && uend <= hi;
+    const bool whole = cs == 1 && ustart >= lo && uend <= hi;
     const int wslot = c * 2 + partial_side(ustart, lo);
     const long bh0 = (long)b * p.n_h + h * GU;
     const int ln = t & 31, wq = t >> 5, nw = nt >> 5;
@@ -285,7 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < C::WPH; ++w) cw[w] *= f;
       const float lse_nat = (M + log2f(L)) * 0.69314718055994531f;
       if (wq == 0 && ln < GU) {
-        if (!whole)
+        if (cs > 1)
+          st_dsmem_f32(cpart + (GU * D + jg) * 4, lse_nat);
+        else if (!whole)
           p.ws_lse[(long)wslot * GU + jg] = lse_nat;
         else if (p.lse)
           p.lse[bh0 + jg] = lse_nat;
@@ -317,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         packed.x = pack_bf16x2(acc.x, acc.y);
         packed.y = pack_bf16x2(acc.z, acc.w);
         reinterpret_cast<uint2 *>(p.out + (bh0 + jg) * D)[col4] = packed;
+      } else if (cs > 1) {
+        st_dsmem_f4(cpart + (jg * D + 4 * col4) * 4, acc);
       } else {
         reinterpret_cast<float4 *>(p.ws_o + ((long)wslot * GU + jg) * D)[col4] =
             acc;
@@ -498,7 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (early) {
       pdl_wait();
     }
-    ChunkCursor fc = cursor_at(wp, p.batch, lo);
+    // (an empty part of a cluster has no chunk to point at)
+    ChunkCursor fc =
+        n > 0 ? cursor_at(wp, p.batch, lo) : ChunkCursor{0, 0, 0};
     int x = lo;
     for (int e = 0; x < hi; ++e) {
       const int b = fc.b, h = fc.h;
@@ -602,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++n_flush;
   };
 
-  ChunkCursor cc = cursor_at(wp, p.batch, lo);
+  // (an empty part of a cluster has no chunk to point at)
+  ChunkCursor cc =
+      n > 0 ? cursor_at(wp, p.batch, lo) : ChunkCursor{0, 0, 0};
   for (int i = 0; i < n; ++i) {
     const int s = i % C::NS;
     // a copy that never completes (bounded wait) sets the abort flag; the
@@ -707,6 +754,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_sync(kFinalBar, kConsumers);  // every warp's state is in the slot
     write_unit(cur_b, cur_h, (n_flush - 1) & 1, tid, kConsumers);
   }
+  if (cs > 1) {
+    // a part with no chunk is empty (its outputs are never read)
+    if (cur_b < 0 && tid < GU)
+      st_dsmem_f32(cpart + (GU * D + tid) * 4, -INFINITY);
+    if (crank != 0) {
+      mbar_arrive_remote(cluster_saddr(cbar, 0));
+    } else {
+      // rank 0: every part is in the buffer; log-sum-exp merge of the cs
+      // parts of each output, one float4 a thread
+      named_sync(kFinalBar, kConsumers);
+      const bool got = mbar_wait_cluster(cbar, 0);
+      if (!got && tid == 0) report(p.err, DEVERR_TIMEOUT);
+      const int u = c / cs, ub = u / n_units, uh = u % n_units;
+      const long bh0 = (long)ub * p.n_h + (long)uh * GU;
+      for (int e = tid; got && e < GU * D / 4; e += kConsumers) {
+        const int jg = (4 * e) / D;
+        float M = -INFINITY;
+        for (int r = 0; r < cs; ++r)
+          M = fmaxf(M, cbuf[r * C::CPART + GU * D + jg]);
+        float W = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < cs && M != -INFINITY; ++r) {
+          const float lr = cbuf[r * C::CPART + GU * D + jg];
+          if (lr == -INFINITY) continue;  // an empty part adds nothing
+          const float w = expf(lr - M);
+          const float4 v =
+              reinterpret_cast<const float4 *>(cbuf + r * C::CPART)[e];
+          W += w;
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+        const float iw = W > 0.f ? 1.f / W : 0.f;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * iw, acc.y * iw);
+        packed.y = pack_bf16x2(acc.z * iw, acc.w * iw);
+        reinterpret_cast<uint2 *>(p.out + bh0 * D)[e] = packed;
+        if ((4 * e) % D == 0 && p.lse)
+          p.lse[bh0 + jg] = W > 0.f ? M + logf(W) : -INFINITY;
+      }
+    }
+  }
 
   if (s_abort && tid == 0) {
     // let every copy the producer issued land before the CTA exits
@@ -726,12 +816,65 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t s) {
   static_assert(C::SMEM <= 226 * 1024, "shared memory budget");
   static_assert(C::NS >= 2, "ring depth");
   auto kern = decode_simt_kernel<D, G, DT, HP>;
+  if (p.cluster > 1 && (C::CL_RANKS < p.cluster || p.n_splits % p.cluster))
+    return cudaErrorNotSupported;
   static bool done[64] = {};  // one table per instantiation
   cudaError_t e = set_smem_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s, 1, p);
+  e = launch_pdl(kern, dim3(p.n_splits), dim3(kThreads), C::SMEM, s,
+                 p.cluster > 1 ? p.cluster : 1, p);
   if (e != cudaSuccess) return e;
   return launch_merge_dense<D, G * HP>(p, p.n_kv / HP, s);
+}
+
+// Largest cluster (2..8 CTAs per unit, at most sms / units) whose `units`
+// clusters are resident together and cover at least 60 % of the SMs (a
+// one-sequence decode took the same time on 96 of 152 SMs as on all of
+// them, and 11 % longer on 76; fewer CTAs would lose more than the merge
+// launch costs), for the instantiation of query groups of 1; 0 when none is.
+// Looked up once per device and unit count.
+template <int D, int DT, int HP>
+int cluster_fit(int units, int sms) {
+  using C = Cfg<D, 1, DT, HP>;
+  if (C::CL_RANKS < 2) return 0;
+  static int memo[64][kMaxDecodeBatch + 1];
+  static bool init = false;
+  if (!init) {
+    for (auto &row : memo)
+      for (int &v : row) v = -1;
+    init = true;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
+      units < 1 || units > kMaxDecodeBatch)
+    return 0;
+  if (memo[dev][units] >= 0) return memo[dev][units];
+  auto kern = decode_simt_kernel<D, 1, DT, HP>;
+  static bool done[64] = {};
+  int best = 0;
+  if (set_smem_once(kern, C::SMEM, done) == cudaSuccess) {
+    for (int cs = sms / units < C::CL_RANKS ? sms / units : C::CL_RANKS;
+         cs >= 2 && !best && 10 * cs * units >= 6 * sms; --cs) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(units * cs);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = cs;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = 1;
+      cfg.attrs = a;
+      cfg.numAttrs = 1;
+      int m = 0;
+      if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) == cudaSuccess &&
+          m >= units)
+        best = cs;
+    }
+  }
+  (void)cudaGetLastError();  // a refused query leaves no sticky error
+  memo[dev][units] = best;
+  return best;
 }
 
 // Head-group sizes built: 1 always; one larger size per row width (a 32 KB
@@ -759,6 +902,30 @@ cudaError_t launch_g(const DecodeParams &p, cudaStream_t s) {
 }
 
 }  // namespace
+
+int simt_cluster_size(int head_dim, int dtype, int hp, int units, int sms) {
+  if (dtype == DT_MXFP4)
+    return head_dim == 128 && hp == kWideHP<128, DT_MXFP4>
+               ? cluster_fit<128, DT_MXFP4, kWideHP<128, DT_MXFP4>>(units, sms)
+               : 0;
+  if (head_dim == 128) {
+    if (dtype == DT_BF16)
+      return hp == 1 ? cluster_fit<128, DT_BF16, 1>(units, sms)
+                     : cluster_fit<128, DT_BF16, kWideHP<128, DT_BF16>>(units,
+                                                                        sms);
+    return hp == 1 ? cluster_fit<128, DT_FP8, 1>(units, sms)
+                   : cluster_fit<128, DT_FP8, kWideHP<128, DT_FP8>>(units, sms);
+  }
+  if (head_dim == 64) {
+    if (dtype == DT_BF16)
+      return hp == 1 ? cluster_fit<64, DT_BF16, 1>(units, sms)
+                     : cluster_fit<64, DT_BF16, kWideHP<64, DT_BF16>>(units,
+                                                                      sms);
+    return hp == 1 ? cluster_fit<64, DT_FP8, 1>(units, sms)
+                   : cluster_fit<64, DT_FP8, kWideHP<64, DT_FP8>>(units, sms);
+  }
+  return 0;
+}
 
 int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
                          int block_size) {

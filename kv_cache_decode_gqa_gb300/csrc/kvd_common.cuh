@@ -278,6 +278,44 @@ __device__ __forceinline__ uint32_t cluster_saddr(const void *local,
       : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
+// Stores into distributed shared memory (an address from cluster_saddr).
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v)
+               : "memory");
+}
+// One arrival on the mbarrier at `addr` in another CTA of the cluster, with
+// release semantics at cluster scope (this thread's earlier writes, remote
+// ones included, are visible to a thread that then observes the phase).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile(
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+          addr)
+      : "memory");
+}
+// Bounded wait for phase `parity` of this CTA's `bar` with acquire
+// semantics at cluster scope (for arrivals of other CTAs of the cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar,
+                                                  uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], "
+        "%2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -66,6 +66,10 @@ struct DecodeParams {
   // sequence, head group c % units) whole instead of an equal share of all
   // chunks: no partials and no merge launch (units all short, see the plan)
   int32_t whole_units;
+  // CUDA-core dense GQA only: > 1 when the units of a single sequence run
+  // as clusters of this many CTAs, each an equal part of its unit, whose
+  // partials merge in distributed shared memory (no merge launch)
+  int32_t cluster;
   int32_t hp;           // kv heads per work unit (CUDA-core GQA kernel)
   int32_t flags;        // kvd_seqs flags (FLAG_SEQS_STABLE, FLAG_PREFIX_READY)
   // sliding window (dense GQA only): sequence b attends to positions
@@ -129,6 +133,10 @@ cudaError_t launch_indexer_pool(const PoolParams &p, cudaStream_t s);
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t s);
 // kv heads the CUDA-core kernel takes per work unit for these shapes (its
 // plan and its launch must agree).
+// CTAs per unit (2..8) of a cluster-merged CUDA-core decode of one sequence
+// (query groups of 1) whose `units` clusters are all resident at once on
+// `sms` SMs; 0 when no size fits.
+int simt_cluster_size(int head_dim, int dtype, int hp, int units, int sms);
 int simt_heads_per_stage(int n_kv, int g, int head_dim, int dtype,
                          int block_size);
 // Dense GQA on the tensor cores (group size 8 or 16, head_dim 128).

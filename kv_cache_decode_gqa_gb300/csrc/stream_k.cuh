@@ -476,7 +476,8 @@ __global__ void __launch_bounds__(kMergeThreads)
 template <int D, int GU>
 inline cudaError_t launch_merge_dense(const DecodeParams &p, int n_units,
                                       cudaStream_t s) {
-  if (p.n_splits <= 1 || p.whole_units || p.batch == 0) return cudaSuccess;
+  if (p.n_splits <= 1 || p.whole_units || p.cluster > 1 || p.batch == 0)
+    return cudaSuccess;
   const long nu = (long)p.batch * n_units;
   const int grid = (int)(nu < 1024 ? nu : 1024);
   if (p.batch <= kMergeSmallBatch)

@@ -474,8 +474,10 @@ def test_bad_block_id_is_flagged_not_faulted():
 
 
 def test_workspace_errors():
-    s = W.config("llama2_7b_mha", batch=1, lengths=[4000], n_layers=1, n_h=2,
-                 n_kv=2)
+    # two sequences: the stream-K split, whose partials need the workspace
+    # (a single one would take the cluster merge, which needs none)
+    s = W.config("llama2_7b_mha", batch=2, lengths=[4000, 3000], n_layers=1,
+                 n_h=2, n_kv=2)
     wl = W.DeviceWorkload(s, layers=[0])
     need = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
                             wl.seq_lens, s.max_seq_len, 2)
@@ -637,3 +639,46 @@ def test_whole_unit_plan_needs_one_wave():
     ref, ref_lse, _ = H.oracle_dense_step(s, wl.paging, 0)
     H.assert_close(H.to_np_bf16(out), ref, "one wave")
     H.assert_lse_close(lse.cpu().numpy(), ref_lse, "one wave")
+
+
+# ---------------------------------------------------------------------------
+# cluster merge: one sequence with query groups of 1 (the CUDA-core kernel)
+# runs each unit as a cluster of CTAs whose parts merge in distributed
+# shared memory -- no workspace, no merge launch; parts with no chunk
+# (fewer chunks than CTAs) hand over empty partials
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "mxfp4"])
+@pytest.mark.parametrize("n_kv,length,fused", [
+    (32, 300, False),    # 5 chunks: some of a unit's CTAs have none
+    (32, 1000, True),
+    (8, 4095, False),    # few units: too few SMs for clusters
+    (32, 4095, True),
+], ids=["n32_l300", "n32_l1000_fused", "n8_l4095", "n32_l4095_fused"])
+def test_cluster_merge_single_sequence(dtype, n_kv, length, fused):
+    s = W.config("llama2_7b_mha", batch=1, lengths=[length], n_layers=1,
+                 n_h=n_kv, n_kv=n_kv, dtype=dtype)
+    wl = W.DeviceWorkload(s, layers=[0])
+    ws = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                          wl.seq_lens, wl.max_seq_len, s.n_h)
+    # clusters for units of 2 heads (bf16) that fill most SMs (16 units);
+    # 4-head units (fp8, MXFP4) and 8 kv heads keep the split and its merge
+    cluster = dtype == "bf16" and n_kv == 32
+    assert (ws == 0) == cluster, ws  # the cluster plan holds no partials
+    out, lse = H.device_step(wl, 0, fused=fused)
+    torch.cuda.synchronize()
+    ref, ref_lse, (kr, vr) = H.oracle_dense_step(s, wl.paging, 0)
+    if fused:
+        c = wl.caches[0]
+        assert np.array_equal(_cache_bytes(c.k), _host_bytes(kr))
+        assert np.array_equal(_cache_bytes(c.v), _host_bytes(vr))
+    H.assert_close(H.to_np_bf16(out), ref, f"cluster/{dtype}/{length}")
+    H.assert_lse_close(lse.cpu().numpy(), ref_lse, f"cluster/{dtype}/{length}")
+
+
+def test_cluster_merge_not_for_two_sequences():
+    """Two sequences (units of different lengths): the stream-K split."""
+    s = W.config("llama2_7b_mha", batch=2, lengths=[1000, 3000], n_layers=1)
+    wl = W.DeviceWorkload(s, layers=[0])
+    ws = K.workspace_size(K.OP_GQA_DECODE, wl.caches[0], wl.block_table,
+                          wl.seq_lens, wl.max_seq_len, s.n_h)
+    assert ws > 0
