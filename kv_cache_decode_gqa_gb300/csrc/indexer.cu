@@ -723,6 +723,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       int at = nhi + warp_excl_scan(whi, s_wsum, &tot_hi);
 #pragma unroll
       for (int j = 0; j < kHiRun / 32; ++j) {
+        if (hib[j] == 0u) continue;  // most groups hold no high key
         const int idx = at + __popc(hib[j] & lt);
         if (((hib[j] >> lane) & 1) && idx < kHiCap) {
           s_hik[idx] = key[j];
