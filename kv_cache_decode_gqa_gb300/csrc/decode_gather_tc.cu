@@ -635,13 +635,23 @@ cudaError_t make_rows_map(CUtensorMap *m, const void *base, long rows,
 }  // namespace
 
 // CTAs per unit: one wave (SMs / units), at most kGatherMaxSplits, none with
-// fewer than 32 entries; `forced` > 0 asks for that many CTAs in all.
+// fewer than 32 entries; when that gives every 128-entry chunk a CTA, the
+// multiple of the chunk count below it if that keeps 3/4 of the CTAs, so
+// that each CTA takes a whole chunk (or an equal fraction of one): for 8
+// sequences and k = 2,048, 16 CTAs each
+// instead of 19 (108 entries each, 20 of a chunk's rows zero-filled, and
+// three more partials to merge) took the 8-layer step from 0.380 to
+// 0.375 ms. `forced` > 0 asks for that many CTAs in all.
 int gather_tc_splits(int units, int k, int sms, int forced) {
   int S = forced > 0 ? forced / units : sms / units;
   const int cap = (k + 31) / 32;
   if (forced <= 0) S = S < cap ? S : cap;
   S = S < kMaxS ? S : kMaxS;
-  return S < 1 ? 1 : S;
+  if (S < 1) return 1;
+  const int chunks = (k + kRows - 1) / kRows;
+  const int aligned = chunks * (S / chunks);
+  if (forced <= 0 && S >= chunks && 4 * aligned >= 3 * S) S = aligned;
+  return S;
 }
 
 cudaError_t launch_decode_sparse_tc(const DecodeParams &p, cudaStream_t s) {
